@@ -1,0 +1,442 @@
+/*
+ * acnn_oracle.c -- plain, slow fp64 CPU oracle for the fused 2-D convolution
+ * layer and its companion ops.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file: only the tests, the package smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library; it is written straight from the definitions on the pages:
+ *
+ *   P1  "inferencelayer -- src/rtdetr_gpu.rs" (docs.rs): IM2COL_SRC (tap order
+ *       and zero padding), RtDetrGpu::conv (output size), MAXPOOL_SRC,
+ *       AVGPOOL_SRC, UPSAMPLE_SRC, CONCAT_SRC, ADDACT_SRC (activations and the
+ *       add-then-activate residual).
+ *   P3  "@framecast/rt 1.0.0 -- package/rt.js": wgslConv (per-channel PReLU
+ *       and the activate-then-add residual), wgslPrepQuarter (RGBA8 unpack,
+ *       BGR order, timestep plane, bilinear 1/4), wgslFlowOut (bilinear x8),
+ *       wgslDeconv (4x4/s2/p1 transposed conv, gather form).
+ *
+ * Every value is a double.  Where the GPU path stores activations in a
+ * narrower type, the caller rounds with oracle_round_storage() between ops
+ * (round-to-nearest-even, the reading taken where the pages are silent).
+ *
+ * Loops are the definitions written out; the only parallelism is a static
+ * split of independent output rows (n, oy) over pthreads.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { O_NHWC = 0, O_NCHW = 1 };
+enum { O_ACT_NONE = 0, O_ACT_RELU = 1, O_ACT_SILU = 2, O_ACT_PRELU = 3 };
+enum { O_RES_NONE = 0, O_RES_ADD_THEN_ACT = 1, O_RES_ACT_THEN_ADD = 2 };
+enum { O_F32 = 0, O_F16 = 1, O_BF16 = 2 };
+
+/* ------------------------------------------------------------------------ */
+/* indexing                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Flat index of activation element (n, c, y, x) in an N x C x H x W tensor
+ * stored NHWC (channels innermost, P1) or NCHW (planes, P3). */
+static size_t act_index(int layout, int C, int H, int W, int n, int c, int y, int x)
+{
+    if (layout == O_NHWC)
+        return (((size_t)n * H + y) * W + x) * C + c;
+    return (((size_t)n * C + c) * H + y) * W + x;
+}
+
+/* Flat index of conv weight (co, ci, ky, kx).  With NHWC activations the
+ * weight is OHWI, so that k = (ky, kx, ci) -- the (dy, dx, c) order of P1's
+ * IM2COL_SRC.  With NCHW activations it is OIHW, P3 wgslConv's [CO,CI,3,3]. */
+static size_t wgt_index(int layout, int C_in, int KH, int KW, int co, int ci, int ky, int kx)
+{
+    if (layout == O_NHWC)
+        return (((size_t)co * KH + ky) * KW + kx) * C_in + ci;
+    return (((size_t)co * C_in + ci) * KH + ky) * KW + kx;
+}
+
+/* ------------------------------------------------------------------------ */
+/* activations: P1 ADDACT_SRC (relu = max(v,0), silu = v/(1+exp(-v))) and    */
+/* P3 wgslConv (prelu = select(alpha*a, a, a >= 0))                          */
+/* ------------------------------------------------------------------------ */
+double oracle_act(int act, double v, double alpha)
+{
+    switch (act) {
+    case O_ACT_RELU: return v > 0.0 ? v : 0.0;
+    case O_ACT_SILU: return v / (1.0 + exp(-v));
+    case O_ACT_PRELU: return v >= 0.0 ? v : alpha * v;
+    default: return v;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* row-parallel driver                                                       */
+/* ------------------------------------------------------------------------ */
+typedef void (*row_fn)(const void* args, int row);
+typedef struct { row_fn fn; const void* args; int rows, tid, nthreads; } row_job;
+
+static void* row_worker(void* p)
+{
+    const row_job* j = (const row_job*)p;
+    for (int r = j->tid; r < j->rows; r += j->nthreads)
+        j->fn(j->args, r);
+    return NULL;
+}
+
+static void for_rows(row_fn fn, const void* args, int rows, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > rows) nthreads = rows > 0 ? rows : 1;
+    if (nthreads == 1) {
+        for (int r = 0; r < rows; ++r) fn(args, r);
+        return;
+    }
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+    row_job* jobs = (row_job*)malloc(sizeof(row_job) * nthreads);
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t].fn = fn; jobs[t].args = args; jobs[t].rows = rows;
+        jobs[t].tid = t; jobs[t].nthreads = nthreads;
+        pthread_create(&th[t], NULL, row_worker, &jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    free(th);
+    free(jobs);
+}
+
+/* ------------------------------------------------------------------------ */
+/* conv2d_fused                                                              */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int layout, N, H, W, C_in, C_out, KH, KW, S, P, OH, OW, act, res_mode;
+    const double *x, *wgt, *bias, *alpha, *res;
+    double* y;
+    const int* pts; /* sampled mode: (n, oy, ox) triples */
+} conv_args;
+
+/* One output element.  P1 RtDetrGpu::conv is im2col then a GEMM with the bias
+ * and activation in its epilogue: the accumulator starts from the bias and
+ * takes every tap k = (ky, kx, ci) in that order; taps that fall outside the
+ * input read zero (IM2COL_SRC writes 0.0 there).  The residual is added before
+ * the activation (P1: addact(relu) after the block's last conv) or after it
+ * (P3 wgslConv: dst = prelu(acc) + res). */
+static double conv_point(const conv_args* a, int n, int co, int oy, int ox)
+{
+    double acc = a->bias ? a->bias[co] : 0.0;
+    for (int ky = 0; ky < a->KH; ++ky) {
+        int iy = oy * a->S + ky - a->P;
+        if (iy < 0 || iy >= a->H) continue;
+        for (int kx = 0; kx < a->KW; ++kx) {
+            int ix = ox * a->S + kx - a->P;
+            if (ix < 0 || ix >= a->W) continue;
+            for (int ci = 0; ci < a->C_in; ++ci)
+                acc += a->x[act_index(a->layout, a->C_in, a->H, a->W, n, ci, iy, ix)] *
+                       a->wgt[wgt_index(a->layout, a->C_in, a->KH, a->KW, co, ci, ky, kx)];
+        }
+    }
+    double al = (a->act == O_ACT_PRELU && a->alpha) ? a->alpha[co] : 0.0;
+    if (a->res_mode == O_RES_NONE || !a->res)
+        return oracle_act(a->act, acc, al);
+    double r = a->res[act_index(a->layout, a->C_out, a->OH, a->OW, n, co, oy, ox)];
+    if (a->res_mode == O_RES_ADD_THEN_ACT)
+        return oracle_act(a->act, acc + r, al);
+    return oracle_act(a->act, acc, al) + r;
+}
+
+static void conv_row(const void* p, int row)
+{
+    const conv_args* a = (const conv_args*)p;
+    int n = row / a->OH, oy = row % a->OH;
+    for (int ox = 0; ox < a->OW; ++ox)
+        for (int co = 0; co < a->C_out; ++co)
+            a->y[act_index(a->layout, a->C_out, a->OH, a->OW, n, co, oy, ox)] =
+                conv_point(a, n, co, oy, ox);
+}
+
+static void conv_pts_row(const void* p, int i)
+{
+    const conv_args* a = (const conv_args*)p;
+    int n = a->pts[3 * i], oy = a->pts[3 * i + 1], ox = a->pts[3 * i + 2];
+    for (int co = 0; co < a->C_out; ++co)
+        a->y[(size_t)i * a->C_out + co] = conv_point(a, n, co, oy, ox);
+}
+
+/* Output size rule of P1 RtDetrGpu::conv: oh = (h + 2p - kh)/s + 1 (floor). */
+int oracle_conv_out(int in, int k, int s, int p) { return (in + 2 * p - k) / s + 1; }
+
+int oracle_conv2d(int layout, int N, int H, int W, int C_in, int C_out, int KH, int KW,
+                  int S, int P, const double* x, const double* wgt, const double* bias,
+                  const double* alpha, const double* res, int res_mode, int act, double* y,
+                  int nthreads)
+{
+    conv_args a = {layout, N, H, W, C_in, C_out, KH, KW, S, P,
+                   oracle_conv_out(H, KH, S, P), oracle_conv_out(W, KW, S, P), act, res_mode,
+                   x, wgt, bias, alpha, res, y, NULL};
+    if (a.OH <= 0 || a.OW <= 0) return -1;
+    for_rows(conv_row, &a, N * a.OH, nthreads);
+    return 0;
+}
+
+/* Same definition at a list of output pixels: y[i*C_out + co] for the pixel
+ * (n, oy, ox) = pts[3i .. 3i+2].  Used to check full-size outputs one by one. */
+int oracle_conv2d_points(int layout, int N, int H, int W, int C_in, int C_out, int KH, int KW,
+                         int S, int P, const double* x, const double* wgt, const double* bias,
+                         const double* alpha, const double* res, int res_mode, int act,
+                         const int* pts, int npts, double* y, int nthreads)
+{
+    conv_args a = {layout, N, H, W, C_in, C_out, KH, KW, S, P,
+                   oracle_conv_out(H, KH, S, P), oracle_conv_out(W, KW, S, P), act, res_mode,
+                   x, wgt, bias, alpha, res, y, pts};
+    for_rows(conv_pts_row, &a, npts, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* pooling: P1 MAXPOOL_SRC (-inf padding: out-of-range taps are skipped) and  */
+/* AVGPOOL_SRC ((a+b+c+d)*0.25 over a 2x2/s2 window, even inputs)            */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int kind, layout, N, C, H, W, K, S, P, OH, OW;
+    const double* x;
+    double* y;
+} pool_args;
+
+static void pool_row(const void* p, int row)
+{
+    const pool_args* a = (const pool_args*)p;
+    int n = row / a->OH, oy = row % a->OH;
+    for (int ox = 0; ox < a->OW; ++ox)
+        for (int c = 0; c < a->C; ++c) {
+            double v;
+            if (a->kind == 0) {
+                v = -INFINITY;
+                for (int dy = 0; dy < a->K; ++dy) {
+                    int iy = oy * a->S + dy - a->P;
+                    if (iy < 0 || iy >= a->H) continue;
+                    for (int dx = 0; dx < a->K; ++dx) {
+                        int ix = ox * a->S + dx - a->P;
+                        if (ix < 0 || ix >= a->W) continue;
+                        double t = a->x[act_index(a->layout, a->C, a->H, a->W, n, c, iy, ix)];
+                        if (t > v) v = t;
+                    }
+                }
+            } else {
+                double s = 0.0;
+                for (int dy = 0; dy < a->K; ++dy)
+                    for (int dx = 0; dx < a->K; ++dx)
+                        s += a->x[act_index(a->layout, a->C, a->H, a->W, n, c,
+                                            oy * a->S + dy, ox * a->S + dx)];
+                v = s * (1.0 / (a->K * a->K));
+            }
+            a->y[act_index(a->layout, a->C, a->OH, a->OW, n, c, oy, ox)] = v;
+        }
+}
+
+/* kind 0 = max (any K, S, P); kind 1 = average over fully in-range windows
+ * (P must be 0, as in AVGPOOL_SRC).  Output size as for conv. */
+int oracle_pool2d(int kind, int layout, int N, int C, int H, int W, int K, int S, int P,
+                  const double* x, double* y, int nthreads)
+{
+    if (kind == 1 && P != 0) return -1;
+    pool_args a = {kind, layout, N, C, H, W, K, S, P,
+                   oracle_conv_out(H, K, S, P), oracle_conv_out(W, K, S, P), x, y};
+    if (a.OH <= 0 || a.OW <= 0) return -1;
+    for_rows(pool_row, &a, N * a.OH, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* resize                                                                    */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int mode, layout, N, C, H, W, OH, OW;
+    const double* x;
+    double* y;
+} resize_args;
+
+static int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+/* Bilinear with align_corners=false, as P3 wgslPrepQuarter / wgslFlowOut
+ * write it: src = (dst + 0.5) * (in/out) - 0.5, x0 = floor(src), f = src - x0,
+ * both taps clamped to the image, mix(mix(v00, v10, fx), mix(v01, v11, fx), fy)
+ * with mix(a, b, t) = a*(1-t) + b*t. */
+static double bilinear_at(const resize_args* a, int n, int c, int oy, int ox)
+{
+    double sy = (oy + 0.5) * ((double)a->H / a->OH) - 0.5;
+    double sx = (ox + 0.5) * ((double)a->W / a->OW) - 0.5;
+    double fy0 = floor(sy), fx0 = floor(sx);
+    double fy = sy - fy0, fx = sx - fx0;
+    int y0 = (int)fy0, x0 = (int)fx0;
+    int ya = clampi(y0, 0, a->H - 1), yb = clampi(y0 + 1, 0, a->H - 1);
+    int xa = clampi(x0, 0, a->W - 1), xb = clampi(x0 + 1, 0, a->W - 1);
+    double v00 = a->x[act_index(a->layout, a->C, a->H, a->W, n, c, ya, xa)];
+    double v10 = a->x[act_index(a->layout, a->C, a->H, a->W, n, c, ya, xb)];
+    double v01 = a->x[act_index(a->layout, a->C, a->H, a->W, n, c, yb, xa)];
+    double v11 = a->x[act_index(a->layout, a->C, a->H, a->W, n, c, yb, xb)];
+    double top = v00 * (1.0 - fx) + v10 * fx;
+    double bot = v01 * (1.0 - fx) + v11 * fx;
+    return top * (1.0 - fy) + bot * fy;
+}
+
+static void resize_row(const void* p, int row)
+{
+    const resize_args* a = (const resize_args*)p;
+    int n = row / a->OH, oy = row % a->OH;
+    for (int ox = 0; ox < a->OW; ++ox)
+        for (int c = 0; c < a->C; ++c) {
+            double v;
+            if (a->mode == 0) {
+                /* nearest, P1 UPSAMPLE_SRC: y[oy, ox] = x[oy/2, ox/2] for 2x;
+                 * for any size the source index is floor(dst * in / out). */
+                int iy = (int)(((long long)oy * a->H) / a->OH);
+                int ix = (int)(((long long)ox * a->W) / a->OW);
+                v = a->x[act_index(a->layout, a->C, a->H, a->W, n, c, iy, ix)];
+            } else {
+                v = bilinear_at(a, n, c, oy, ox);
+            }
+            a->y[act_index(a->layout, a->C, a->OH, a->OW, n, c, oy, ox)] = v;
+        }
+}
+
+/* mode 0 = nearest, mode 1 = bilinear (align_corners=false). */
+int oracle_resize2d(int mode, int layout, int N, int C, int H, int W, int OH, int OW,
+                    const double* x, double* y, int nthreads)
+{
+    if (OH <= 0 || OW <= 0 || H <= 0 || W <= 0) return -1;
+    resize_args a = {mode, layout, N, C, H, W, OH, OW, x, y};
+    for_rows(resize_row, &a, N * OH, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* concat: P1 CONCAT_SRC -- per pixel y = [a | b] along channels.            */
+/* ------------------------------------------------------------------------ */
+int oracle_concat(int layout, int N, int H, int W, int Ca, int Cb, const double* a,
+                  const double* b, double* y)
+{
+    int C = Ca + Cb;
+    for (int n = 0; n < N; ++n)
+        for (int yy = 0; yy < H; ++yy)
+            for (int xx = 0; xx < W; ++xx)
+                for (int c = 0; c < C; ++c)
+                    y[act_index(layout, C, H, W, n, c, yy, xx)] =
+                        c < Ca ? a[act_index(layout, Ca, H, W, n, c, yy, xx)]
+                               : b[act_index(layout, Cb, H, W, n, c - Ca, yy, xx)];
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* deconv: P3 wgslDeconv, gather form.  Weight layout [CI, CO, K, K].        */
+/* y[co, oy, ox] = b[co] + sum over taps (ky, kx) with ty = oy + P - ky >= 0,  */
+/* ty % S == 0, iy = ty / S < IH (same along x) of sum_ci x[ci, iy, ix] *     */
+/* w[ci, co, ky, kx].  Output size (IH - 1)*S - 2P + K (= 2*IH for 4/2/1).    */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int layout, N, C_in, C_out, H, W, K, S, P, OH, OW, act;
+    const double *x, *wgt, *bias, *alpha;
+    double* y;
+} deconv_args;
+
+static void deconv_row(const void* p, int row)
+{
+    const deconv_args* a = (const deconv_args*)p;
+    int n = row / a->OH, oy = row % a->OH;
+    for (int ox = 0; ox < a->OW; ++ox)
+        for (int co = 0; co < a->C_out; ++co) {
+            double acc = a->bias ? a->bias[co] : 0.0;
+            for (int ky = 0; ky < a->K; ++ky) {
+                int ty = oy + a->P - ky;
+                if (ty < 0 || ty % a->S != 0) continue;
+                int iy = ty / a->S;
+                if (iy >= a->H) continue;
+                for (int kx = 0; kx < a->K; ++kx) {
+                    int tx = ox + a->P - kx;
+                    if (tx < 0 || tx % a->S != 0) continue;
+                    int ix = tx / a->S;
+                    if (ix >= a->W) continue;
+                    for (int ci = 0; ci < a->C_in; ++ci)
+                        acc += a->x[act_index(a->layout, a->C_in, a->H, a->W, n, ci, iy, ix)] *
+                               a->wgt[(((size_t)ci * a->C_out + co) * a->K + ky) * a->K + kx];
+                }
+            }
+            double al = (a->act == O_ACT_PRELU && a->alpha) ? a->alpha[co] : 0.0;
+            a->y[act_index(a->layout, a->C_out, a->OH, a->OW, n, co, oy, ox)] =
+                oracle_act(a->act, acc, al);
+        }
+}
+
+int oracle_deconv2d(int layout, int N, int H, int W, int C_in, int C_out, int K, int S, int P,
+                    const double* x, const double* wgt, const double* bias,
+                    const double* alpha, int act, double* y, int nthreads)
+{
+    deconv_args a = {layout, N, C_in, C_out, H, W, K, S, P,
+                     (H - 1) * S - 2 * P + K, (W - 1) * S - 2 * P + K, act,
+                     x, wgt, bias, alpha, y};
+    if (a.OH <= 0 || a.OW <= 0) return -1;
+    for_rows(deconv_row, &a, N * a.OH, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* frame prep: P3 wgslPrepQuarter.  Two RGBA8 frames (byte order R,G,B,A per  */
+/* pixel, unpacked /255) -> 7 planes [B0,G0,R0,B1,G1,R1,t] at (H/4, W/4),     */
+/* each colour plane a bilinear 1/4 downsample (align_corners=false) of the  */
+/* full-resolution plane.                                                    */
+/* ------------------------------------------------------------------------ */
+int oracle_prep_quarter(int H, int W, const uint8_t* rgba0, const uint8_t* rgba1, double t,
+                        double* y)
+{
+    int QH = H / 4, QW = W / 4;
+    if (QH <= 0 || QW <= 0) return -1;
+    double* plane = (double*)malloc(sizeof(double) * (size_t)H * W);
+    for (int f = 0; f < 2; ++f) {
+        const uint8_t* src = f == 0 ? rgba0 : rgba1;
+        for (int k = 0; k < 3; ++k) {
+            int byte = 2 - k; /* plane order B, G, R */
+            for (size_t i = 0; i < (size_t)H * W; ++i) plane[i] = src[4 * i + byte] / 255.0;
+            resize_args a = {1, O_NCHW, 1, 1, H, W, QH, QW, plane, y + (size_t)(3 * f + k) * QH * QW};
+            for (int r = 0; r < QH; ++r) resize_row(&a, r);
+        }
+    }
+    for (size_t i = 0; i < (size_t)QH * QW; ++i) y[(size_t)6 * QH * QW + i] = t;
+    free(plane);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* storage rounding: round-to-nearest-even to binary32, binary16 or bfloat16. */
+/* A format with p significand bits (implicit bit included) and minimum       */
+/* normal exponent emin has, for |v| in [2^e, 2^(e+1)), the quantum            */
+/* 2^(max(e, emin) - p + 1); below 2^emin the quantum stays 2^(emin - p + 1)   */
+/* (subnormals).  Rounding |v| / quantum to the nearest integer, ties to even, */
+/* then scaling back is exact in double.  Results above the largest finite    */
+/* value after rounding become infinity.                                      */
+/* ------------------------------------------------------------------------ */
+static double round_to_format(double v, int p, int emin, double maxfinite)
+{
+    if (v == 0.0 || !isfinite(v)) return v;
+    int e;
+    frexp(v, &e); /* v = m * 2^e, 0.5 <= |m| < 1, so |v| in [2^(e-1), 2^e) */
+    int ex = e - 1;
+    if (ex < emin) ex = emin;
+    double q = ldexp(1.0, ex - p + 1);
+    double r = nearbyint(v / q) * q; /* default rounding mode: to nearest, ties to even */
+    if (fabs(r) > maxfinite) return v > 0 ? INFINITY : -INFINITY;
+    return r;
+}
+
+double oracle_round_value(double v, int dtype)
+{
+    switch (dtype) {
+    case O_F32: return round_to_format(v, 24, -126, 3.4028234663852886e38);
+    case O_F16: return round_to_format(v, 11, -14, 65504.0);
+    case O_BF16: return round_to_format(v, 8, -126, 3.3895313892515355e38);
+    default: return v;
+    }
+}
+
+void oracle_round_storage(double* v, size_t n, int dtype)
+{
+    for (size_t i = 0; i < n; ++i) v[i] = oracle_round_value(v[i], dtype);
+}
