@@ -1,0 +1,334 @@
+"""Thin ctypes binding of libacnn (include/acnn.h).
+
+Two layers, both pure argument marshalling -- every step of the computation
+runs in the library's CUDA kernels:
+
+* ``acnn_*`` functions with the C names and arguments (pointers as ints or
+  tensors, sizes as ints), returning the int status;
+* tensor-level helpers (``conv2d_fused``, ``pool2d``, ...) that allocate the
+  output with PyTorch, pass raw device pointers and the current stream, and
+  raise ``AcnnError`` on a non-zero status.
+
+The library is loaded from ``activation_cnn_gb300/lib/libacnn.so``; if it is
+missing the first call raises -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .inputs import NHWC, NCHW, F32, F16, BF16, TORCH_DTYPE  # noqa: F401  (enum values)
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libacnn.so")
+
+ACT_NONE, ACT_RELU, ACT_SILU, ACT_PRELU = 0, 1, 2, 3
+RES_NONE, RES_ADD_THEN_ACT, RES_ACT_THEN_ADD = 0, 1, 2
+POOL_MAX, POOL_AVG = 0, 1
+RESIZE_NEAREST, RESIZE_BILINEAR = 0, 1
+
+STATUS = {
+    0: "ACNN_OK", 1: "ACNN_ERR_NULL_POINTER", 2: "ACNN_ERR_BAD_GEOMETRY",
+    3: "ACNN_ERR_UNSUPPORTED", 4: "ACNN_ERR_MISALIGNED", 5: "ACNN_ERR_WORKSPACE",
+    6: "ACNN_ERR_ALIAS", 7: "ACNN_ERR_BAD_ENUM", 8: "ACNN_ERR_CUDA",
+    9: "ACNN_ERR_DEVICE_TIMEOUT", 10: "ACNN_ERR_TOO_LARGE",
+}
+EXPORTS = (
+    "acnn_conv2d_fused", "acnn_conv2d_out_hw", "acnn_conv2d_workspace_size", "acnn_conv2d_path",
+    "acnn_pool2d", "acnn_resize2d", "acnn_concat", "acnn_deconv2d", "acnn_frame_prep_quarter",
+    "acnn_status_string", "acnn_last_device_status", "acnn_set_wait_budget",
+    "acnn_section_begin", "acnn_section_end", "acnn_section_launch", "acnn_section_destroy",
+    "acnn_device_sm_count",
+)
+
+
+class AcnnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+class ConvDesc(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_int) for k in
+                ("n", "h", "w", "c_in", "c_out", "kh", "kw", "stride", "pad", "layout", "dtype")]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+def lib() -> ctypes.CDLL:
+    """Load libacnn.so (raises if it was not built: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libacnn.so not found at {LIB_PATH}; build it with "
+                               "`python -m activation_cnn_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        D = ctypes.POINTER(ConvDesc)
+        L.acnn_conv2d_fused.argtypes = [D, _P, _P, _P, _P, _P, _I, _I, _P, _P, ctypes.c_size_t, _P]
+        L.acnn_conv2d_out_hw.argtypes = [D, ctypes.POINTER(_I), ctypes.POINTER(_I)]
+        L.acnn_conv2d_workspace_size.argtypes = [D]
+        L.acnn_conv2d_workspace_size.restype = ctypes.c_size_t
+        L.acnn_conv2d_path.argtypes = [D]
+        L.acnn_pool2d.argtypes = [_I] * 10 + [_P, _P, _P]
+        L.acnn_resize2d.argtypes = [_I] * 10 + [_P, _P, _P]
+        L.acnn_concat.argtypes = [_I] * 7 + [_P, _P, _P, _P]
+        L.acnn_deconv2d.argtypes = [D, _P, _P, _P, _P, _I, _I, _P, _P]
+        L.acnn_frame_prep_quarter.argtypes = [_I, _I, _P, _P, ctypes.c_float, _I, _P, _P]
+        L.acnn_status_string.argtypes = [_I]
+        L.acnn_status_string.restype = ctypes.c_char_p
+        L.acnn_last_device_status.argtypes = [_P]
+        L.acnn_set_wait_budget.argtypes = [ctypes.c_longlong]
+        L.acnn_section_begin.argtypes = [_P]
+        L.acnn_section_end.argtypes = [_P, ctypes.POINTER(_P)]
+        L.acnn_section_launch.argtypes = [_P, _P]
+        L.acnn_section_destroy.argtypes = [_P]
+        L.acnn_device_sm_count.argtypes = []
+        _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------------ raw ABI
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def status_string(status: int) -> str:
+    return lib().acnn_status_string(status).decode()
+
+
+def acnn_conv2d_fused(desc, x, w, bias, alpha, residual, res_mode, act, y, workspace, ws_bytes,
+                      stream=None) -> int:
+    return lib().acnn_conv2d_fused(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(alpha),
+                                   _ptr(residual), res_mode, act, _ptr(y), _ptr(workspace),
+                                   ws_bytes, _stream(stream))
+
+
+def acnn_conv2d_out_hw(desc):
+    oh, ow = _I(), _I()
+    st = lib().acnn_conv2d_out_hw(ctypes.byref(desc), ctypes.byref(oh), ctypes.byref(ow))
+    return st, oh.value, ow.value
+
+
+def acnn_conv2d_workspace_size(desc) -> int:
+    return lib().acnn_conv2d_workspace_size(ctypes.byref(desc))
+
+
+def acnn_conv2d_path(desc) -> int:
+    return lib().acnn_conv2d_path(ctypes.byref(desc))
+
+
+def acnn_pool2d(kind, n, h, w, c, k, stride, pad, layout, dtype, x, y, stream=None) -> int:
+    return lib().acnn_pool2d(kind, n, h, w, c, k, stride, pad, layout, dtype, _ptr(x), _ptr(y),
+                             _stream(stream))
+
+
+def acnn_resize2d(mode, n, c, h, w, oh, ow, layout, in_dtype, out_dtype, x, y,
+                  stream=None) -> int:
+    return lib().acnn_resize2d(mode, n, c, h, w, oh, ow, layout, in_dtype, out_dtype, _ptr(x),
+                               _ptr(y), _stream(stream))
+
+
+def acnn_concat(n, h, w, c_a, c_b, layout, dtype, a, b, y, stream=None) -> int:
+    return lib().acnn_concat(n, h, w, c_a, c_b, layout, dtype, _ptr(a), _ptr(b), _ptr(y),
+                             _stream(stream))
+
+
+def acnn_deconv2d(desc, x, w, bias, alpha, act, out_dtype, y, stream=None) -> int:
+    return lib().acnn_deconv2d(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(alpha),
+                               act, out_dtype, _ptr(y), _stream(stream))
+
+
+def acnn_frame_prep_quarter(h, w, rgba0, rgba1, t, out_dtype, y, stream=None) -> int:
+    return lib().acnn_frame_prep_quarter(h, w, _ptr(rgba0), _ptr(rgba1), float(t), out_dtype,
+                                         _ptr(y), _stream(stream))
+
+
+def acnn_last_device_status(stream=None) -> int:
+    return lib().acnn_last_device_status(_stream(stream))
+
+
+def acnn_set_wait_budget(polls: int) -> int:
+    return lib().acnn_set_wait_budget(int(polls))
+
+
+def acnn_section_begin(stream=None) -> int:
+    return lib().acnn_section_begin(_stream(stream))
+
+
+def acnn_section_end(stream=None):
+    h = _P()
+    st = lib().acnn_section_end(_stream(stream), ctypes.byref(h))
+    return st, h.value
+
+
+def acnn_section_launch(exec_handle, stream=None) -> int:
+    return lib().acnn_section_launch(exec_handle, _stream(stream))
+
+
+def acnn_section_destroy(exec_handle) -> int:
+    return lib().acnn_section_destroy(exec_handle)
+
+
+def acnn_device_sm_count() -> int:
+    return lib().acnn_device_sm_count()
+
+
+# ------------------------------------------------------------------ tensor helpers
+def dtype_code(t: torch.dtype) -> int:
+    return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[t]
+
+
+def check(status: int, where: str) -> None:
+    if status != 0:
+        raise AcnnError(status, where)
+
+
+def conv_desc(x: torch.Tensor, c_out: int, kh: int, kw: int, stride: int, pad: int,
+              layout: int) -> ConvDesc:
+    if layout == NHWC:
+        n, h, w, c = x.shape
+    else:
+        n, c, h, w = x.shape
+    return ConvDesc(n, h, w, c, c_out, kh, kw, stride, pad, layout, dtype_code(x.dtype))
+
+
+def conv_out_shape(desc: ConvDesc):
+    st, oh, ow = acnn_conv2d_out_hw(desc)
+    check(st, "acnn_conv2d_out_hw")
+    if desc.layout == NHWC:
+        return (desc.n, oh, ow, desc.c_out)
+    return (desc.n, desc.c_out, oh, ow)
+
+
+def conv2d_fused(x, w, bias=None, *, stride=1, pad=0, act=ACT_NONE, alpha=None, residual=None,
+                 res_mode=RES_NONE, layout=NHWC, out=None, workspace=None, stream=None):
+    """y = post(conv(x, w) + bias); w is OHWI for NHWC, OIHW for NCHW."""
+    if layout == NHWC:
+        c_out, kh, kw, _ = w.shape
+    else:
+        c_out, _, kh, kw = w.shape
+    d = conv_desc(x, c_out, kh, kw, stride, pad, layout)
+    y = out if out is not None else torch.empty(conv_out_shape(d), dtype=x.dtype, device=x.device)
+    ws_bytes = acnn_conv2d_workspace_size(d)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    st = acnn_conv2d_fused(d, x, w, bias, alpha, residual, res_mode, act, y, workspace,
+                           ws_bytes if workspace is not None else 0, stream)
+    check(st, "acnn_conv2d_fused")
+    return y
+
+
+def pool2d(x, kind, k, stride, pad, *, layout=NHWC, out=None, stream=None):
+    if layout == NHWC:
+        n, h, w, c = x.shape
+    else:
+        n, c, h, w = x.shape
+    oh, ow = (h + 2 * pad - k) // stride + 1, (w + 2 * pad - k) // stride + 1
+    shape = (n, oh, ow, c) if layout == NHWC else (n, c, oh, ow)
+    y = out if out is not None else torch.empty(shape, dtype=x.dtype, device=x.device)
+    check(acnn_pool2d(kind, n, h, w, c, k, stride, pad, layout, dtype_code(x.dtype), x, y, stream),
+          "acnn_pool2d")
+    return y
+
+
+def resize2d(x, mode, oh, ow, *, layout=NHWC, out_dtype=None, out=None, stream=None):
+    if layout == NHWC:
+        n, h, w, c = x.shape
+    else:
+        n, c, h, w = x.shape
+    od = out_dtype or x.dtype
+    shape = (n, oh, ow, c) if layout == NHWC else (n, c, oh, ow)
+    y = out if out is not None else torch.empty(shape, dtype=od, device=x.device)
+    check(acnn_resize2d(mode, n, c, h, w, oh, ow, layout, dtype_code(x.dtype), dtype_code(od), x,
+                        y, stream), "acnn_resize2d")
+    return y
+
+
+def concat(a, b, *, layout=NHWC, out=None, stream=None):
+    if layout == NHWC:
+        n, h, w, ca = a.shape
+        cb = b.shape[3]
+        shape = (n, h, w, ca + cb)
+    else:
+        n, ca, h, w = a.shape
+        cb = b.shape[1]
+        shape = (n, ca + cb, h, w)
+    y = out if out is not None else torch.empty(shape, dtype=a.dtype, device=a.device)
+    check(acnn_concat(n, h, w, ca, cb, layout, dtype_code(a.dtype), a, b, y, stream),
+          "acnn_concat")
+    return y
+
+
+def deconv2d(x, w, bias=None, *, act=ACT_NONE, alpha=None, layout=NCHW, out_dtype=None,
+             out=None, stream=None):
+    """4x4/s2/p1 transposed conv; w is fp32 [CI, CO, 4, 4]."""
+    if layout == NHWC:
+        n, h, wd, c = x.shape
+    else:
+        n, c, h, wd = x.shape
+    ci, co, kh, kw = w.shape
+    d = ConvDesc(n, h, wd, c, co, kh, kw, 2, 1, layout, dtype_code(x.dtype))
+    od = out_dtype or x.dtype
+    shape = (n, 2 * h, 2 * wd, co) if layout == NHWC else (n, co, 2 * h, 2 * wd)
+    y = out if out is not None else torch.empty(shape, dtype=od, device=x.device)
+    check(acnn_deconv2d(d, x, w, bias, alpha, act, dtype_code(od), y, stream), "acnn_deconv2d")
+    return y
+
+
+def frame_prep_quarter(rgba0, rgba1, t, *, out_dtype=torch.float16, out=None, stream=None):
+    h, w, _ = rgba0.shape
+    y = out if out is not None else torch.empty((7, h // 4, w // 4), dtype=out_dtype,
+                                                device=rgba0.device)
+    check(acnn_frame_prep_quarter(h, w, rgba0, rgba1, t, dtype_code(out_dtype), y, stream),
+          "acnn_frame_prep_quarter")
+    return y
+
+
+class Section:
+    """One captured CUDA graph: record ABI calls once, replay with launch()."""
+
+    def __init__(self, stream=None):
+        self.stream = stream
+        self.handle = None
+
+    def __enter__(self):
+        check(acnn_section_begin(self.stream), "acnn_section_begin")
+        return self
+
+    def __exit__(self, exc_type, exc, tb):
+        st, h = acnn_section_end(self.stream)
+        if exc_type is None:
+            check(st, "acnn_section_end")
+        self.handle = h
+        return False
+
+    def launch(self, stream=None):
+        check(acnn_section_launch(self.handle, stream if stream is not None else self.stream),
+              "acnn_section_launch")
+
+    def close(self):
+        if self.handle:
+            acnn_section_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

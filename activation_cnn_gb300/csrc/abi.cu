@@ -1,0 +1,371 @@
+// abi.cu -- the extern "C" entry points of libacnn (include/acnn.h).
+//
+// Each entry point validates its arguments on the host, picks a kernel and
+// enqueues it on the caller's stream.  A rejected call launches nothing.
+// Device pointers are plain addresses owned by the caller; the library
+// allocates no device memory.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace acnn {
+
+// Status word the kernels set when a bounded pipeline wait expires.
+__device__ int g_device_status = 0;
+
+namespace {
+std::atomic<long long> g_wait_budget{0};
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+std::mutex g_mu;
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    return dev;
+}
+}  // namespace
+
+int sm_count() {
+    const int dev = current_device();
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+int* device_status_ptr() {
+    const int dev = current_device();
+    if (!g_status_ptr[dev]) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_status_ptr[dev]) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+            g_status_ptr[dev] = static_cast<int*>(p);
+        }
+    }
+    return g_status_ptr[dev];
+}
+
+long long wait_budget_polls() { return g_wait_budget.load(); }
+
+}  // namespace acnn
+
+using namespace acnn;
+
+namespace {
+
+inline bool valid_dtype(int t) { return t == ACNN_F32 || t == ACNN_F16 || t == ACNN_BF16; }
+inline bool valid_layout(int l) { return l == ACNN_NHWC || l == ACNN_NCHW; }
+inline size_t elem_size(int t) { return t == ACNN_F32 ? 4 : 2; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+inline int status_of(cudaError_t e) { return e == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA; }
+
+constexpr long long kIndexLimit = (1ll << 31) - 1;
+
+// Geometry checks shared by conv and deconv descriptors.
+int check_desc(const acnn_conv_desc* d) {
+    if (!d) return ACNN_ERR_NULL_POINTER;
+    if (!valid_dtype(d->dtype) || !valid_layout(d->layout)) return ACNN_ERR_BAD_ENUM;
+    if (d->n <= 0 || d->h <= 0 || d->w <= 0 || d->c_in <= 0 || d->c_out <= 0 || d->kh <= 0 ||
+        d->kw <= 0 || d->stride <= 0 || d->pad < 0)
+        return ACNN_ERR_BAD_GEOMETRY;
+    return ACNN_OK;
+}
+
+int conv_out(const acnn_conv_desc* d, int* oh, int* ow) {
+    const long long h = ((long long)d->h + 2ll * d->pad - d->kh) / d->stride + 1;
+    const long long w = ((long long)d->w + 2ll * d->pad - d->kw) / d->stride + 1;
+    if ((long long)d->h + 2ll * d->pad < d->kh || (long long)d->w + 2ll * d->pad < d->kw || h <= 0 ||
+        w <= 0)
+        return ACNN_ERR_BAD_GEOMETRY;
+    *oh = (int)h;
+    *ow = (int)w;
+    return ACNN_OK;
+}
+
+// The tensor-core path: fp16/bf16, TMA-addressable channel strides (16-byte
+// multiples), whole 16-channel MMA columns, square kernels whose corner
+// offsets fit the im2col descriptor, and 32-bit pixel indices.
+bool tensor_path_ok(const acnn_conv_desc* d, int oh, int ow) {
+    if (d->dtype == ACNN_F32) return false;
+    if (d->c_in % 8 != 0 || d->c_out % 16 != 0) return false;
+    if (d->kh != d->kw || d->kh > 8 || d->stride > 8 || d->pad > 64) return false;
+    if (d->pad - (d->kh - 1) < -128) return false;
+    const long long m = (long long)d->n * oh * ow;
+    const long long in = (long long)d->n * d->h * d->w;
+    return m <= kIndexLimit && in <= kIndexLimit && (long long)d->c_out * oh * ow <= kIndexLimit;
+}
+
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// Workspace of an NCHW call on the tensor path: the NHWC copy of x and the
+// OHWI copy of w, each 256-byte aligned.
+void nchw_workspace(const acnn_conv_desc* d, size_t* x_bytes, size_t* w_bytes) {
+    *x_bytes = round256((size_t)d->n * d->h * d->w * d->c_in * elem_size(d->dtype));
+    *w_bytes = round256((size_t)d->c_out * d->kh * d->kw * d->c_in * elem_size(d->dtype));
+}
+
+}  // namespace
+
+extern "C" {
+
+int acnn_conv2d_out_hw(const acnn_conv_desc* d, int* oh, int* ow) {
+    if (!oh || !ow) return ACNN_ERR_NULL_POINTER;
+    int st = check_desc(d);
+    if (st != ACNN_OK) return st;
+    return conv_out(d, oh, ow);
+}
+
+int acnn_conv2d_path(const acnn_conv_desc* d) {
+    int oh, ow;
+    if (check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK) return -1;
+    if (!tensor_path_ok(d, oh, ow)) return 0;
+    return (d->kh == 1 && d->kw == 1 && d->stride == 1 && d->pad == 0) ? 1 : 2;
+}
+
+size_t acnn_conv2d_workspace_size(const acnn_conv_desc* d) {
+    int oh, ow;
+    if (check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK) return 0;
+    if (d->layout != ACNN_NCHW || !tensor_path_ok(d, oh, ow)) return 0;
+    size_t xb, wb;
+    nchw_workspace(d, &xb, &wb);
+    return xb + wb;
+}
+
+int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w, const float* bias,
+                      const float* alpha, const void* residual, int res_mode, int act, void* y,
+                      void* workspace, size_t ws_bytes, acnn_stream_t stream) {
+    int st = check_desc(d);
+    if (st != ACNN_OK) return st;
+    if (act < ACNN_ACT_NONE || act > ACNN_ACT_PRELU || res_mode < ACNN_RES_NONE ||
+        res_mode > ACNN_RES_ACT_THEN_ADD)
+        return ACNN_ERR_BAD_ENUM;
+    if (!x || !w || !y) return ACNN_ERR_NULL_POINTER;
+    if (act == ACNN_ACT_PRELU && !alpha) return ACNN_ERR_NULL_POINTER;
+    if (res_mode != ACNN_RES_NONE && !residual) return ACNN_ERR_NULL_POINTER;
+    int oh, ow;
+    st = conv_out(d, &oh, &ow);
+    if (st != ACNN_OK) return st;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
+        (alpha && !aligned16(alpha)) || (residual && !aligned16(residual)) ||
+        (workspace && !aligned16(workspace)))
+        return ACNN_ERR_MISALIGNED;
+    const size_t es = elem_size(d->dtype);
+    const size_t xb = (size_t)d->n * d->h * d->w * d->c_in * es;
+    const size_t wb = (size_t)d->c_out * d->kh * d->kw * d->c_in * es;
+    const size_t yb = (size_t)d->n * oh * ow * d->c_out * es;
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) ||
+        (residual && res_mode != ACNN_RES_NONE && overlaps(y, yb, residual, yb)) ||
+        (bias && overlaps(y, yb, bias, d->c_out * 4)) ||
+        (alpha && act == ACNN_ACT_PRELU && overlaps(y, yb, alpha, d->c_out * 4)))
+        return ACNN_ERR_ALIAS;
+    if ((long long)d->n * oh * ow > kIndexLimit * 64) return ACNN_ERR_TOO_LARGE;
+
+    ConvArgs a{};
+    a.d = *d;
+    a.oh = oh;
+    a.ow = ow;
+    a.x = x;
+    a.w = w;
+    a.bias = bias;
+    a.alpha = act == ACNN_ACT_PRELU ? alpha : nullptr;
+    a.residual = res_mode != ACNN_RES_NONE ? residual : nullptr;
+    a.res_mode = res_mode;
+    a.act = act;
+    a.y = y;
+    a.out_layout = d->layout;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    if (!tensor_path_ok(d, oh, ow)) return status_of(launch_direct_conv(a, s));
+    if (d->layout == ACNN_NHWC) return launch_igemm_conv(a, s);
+
+    // NCHW on the tensor path: NHWC copy of x and OHWI copy of w in the
+    // caller's workspace, then the implicit GEMM writing NCHW directly.
+    size_t xws, wws;
+    nchw_workspace(d, &xws, &wws);
+    if (!workspace || ws_bytes < xws + wws) return ACNN_ERR_WORKSPACE;
+    if (overlaps(workspace, xws + wws, y, yb) || overlaps(workspace, xws + wws, x, xb) ||
+        overlaps(workspace, xws + wws, w, wb) ||
+        (a.residual && overlaps(workspace, xws + wws, residual, yb)))
+        return ACNN_ERR_ALIAS;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaError_t e = launch_nchw_to_nhwc(d->n, d->c_in, d->h * d->w, 2, x, ws, s);
+    if (e != cudaSuccess) return ACNN_ERR_CUDA;
+    e = launch_nchw_to_nhwc(d->c_out, d->c_in, d->kh * d->kw, 2, w, ws + xws, s);
+    if (e != cudaSuccess) return ACNN_ERR_CUDA;
+    a.x = ws;
+    a.w = ws + xws;
+    a.d.layout = ACNN_NHWC;
+    a.out_layout = ACNN_NCHW;
+    return launch_igemm_conv(a, s);
+}
+
+int acnn_pool2d(int kind, int n, int h, int w, int c, int k, int stride, int pad, int layout,
+                int dtype, const void* x, void* y, acnn_stream_t stream) {
+    if (kind != ACNN_POOL_MAX && kind != ACNN_POOL_AVG) return ACNN_ERR_BAD_ENUM;
+    if (!valid_dtype(dtype) || !valid_layout(layout)) return ACNN_ERR_BAD_ENUM;
+    if (!x || !y) return ACNN_ERR_NULL_POINTER;
+    if (n <= 0 || h <= 0 || w <= 0 || c <= 0 || k <= 0 || stride <= 0 || pad < 0)
+        return ACNN_ERR_BAD_GEOMETRY;
+    if (kind == ACNN_POOL_AVG && pad != 0) return ACNN_ERR_UNSUPPORTED;
+    if (pad >= k) return ACNN_ERR_UNSUPPORTED;  // a window could hold no input tap
+    if (h + 2 * pad < k || w + 2 * pad < k) return ACNN_ERR_BAD_GEOMETRY;
+    const int oh = (h + 2 * pad - k) / stride + 1, ow = (w + 2 * pad - k) / stride + 1;
+    if (!aligned16(x) || !aligned16(y)) return ACNN_ERR_MISALIGNED;
+    const size_t es = elem_size(dtype);
+    if (overlaps(x, (size_t)n * h * w * c * es, y, (size_t)n * oh * ow * c * es))
+        return ACNN_ERR_ALIAS;
+    return status_of(launch_pool2d(kind, n, h, w, c, k, stride, pad, layout, dtype, x, y,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int acnn_resize2d(int mode, int n, int c, int h, int w, int oh, int ow, int layout, int in_dtype,
+                  int out_dtype, const void* x, void* y, acnn_stream_t stream) {
+    if (mode != ACNN_RESIZE_NEAREST && mode != ACNN_RESIZE_BILINEAR) return ACNN_ERR_BAD_ENUM;
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || !valid_layout(layout))
+        return ACNN_ERR_BAD_ENUM;
+    if (!x || !y) return ACNN_ERR_NULL_POINTER;
+    if (n <= 0 || c <= 0 || h <= 0 || w <= 0 || oh <= 0 || ow <= 0) return ACNN_ERR_BAD_GEOMETRY;
+    if (mode == ACNN_RESIZE_NEAREST && in_dtype != out_dtype) return ACNN_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(y)) return ACNN_ERR_MISALIGNED;
+    if (overlaps(x, (size_t)n * c * h * w * elem_size(in_dtype), y,
+                 (size_t)n * c * oh * ow * elem_size(out_dtype)))
+        return ACNN_ERR_ALIAS;
+    return status_of(launch_resize2d(mode, n, c, h, w, oh, ow, layout, in_dtype, out_dtype, x, y,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int acnn_concat(int n, int h, int w, int c_a, int c_b, int layout, int dtype, const void* a,
+                const void* b, void* y, acnn_stream_t stream) {
+    if (!valid_dtype(dtype) || !valid_layout(layout)) return ACNN_ERR_BAD_ENUM;
+    if (!a || !b || !y) return ACNN_ERR_NULL_POINTER;
+    if (n <= 0 || h <= 0 || w <= 0 || c_a <= 0 || c_b <= 0) return ACNN_ERR_BAD_GEOMETRY;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(y)) return ACNN_ERR_MISALIGNED;
+    const size_t es = elem_size(dtype), px = (size_t)n * h * w;
+    if ((long long)(c_a + c_b) * h * w > kIndexLimit) return ACNN_ERR_TOO_LARGE;
+    if (overlaps(y, px * (c_a + c_b) * es, a, px * c_a * es) ||
+        overlaps(y, px * (c_a + c_b) * es, b, px * c_b * es))
+        return ACNN_ERR_ALIAS;
+    return status_of(launch_concat(n, h, w, c_a, c_b, layout, dtype, a, b, y,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int acnn_deconv2d(const acnn_conv_desc* d, const void* x, const float* w, const float* bias,
+                  const float* alpha, int act, int out_dtype, void* y, acnn_stream_t stream) {
+    int st = check_desc(d);
+    if (st != ACNN_OK) return st;
+    if (act < ACNN_ACT_NONE || act > ACNN_ACT_PRELU || !valid_dtype(out_dtype))
+        return ACNN_ERR_BAD_ENUM;
+    if (!x || !w || !y) return ACNN_ERR_NULL_POINTER;
+    if (act == ACNN_ACT_PRELU && !alpha) return ACNN_ERR_NULL_POINTER;
+    if (d->kh != 4 || d->kw != 4 || d->stride != 2 || d->pad != 1) return ACNN_ERR_UNSUPPORTED;
+    const int oh = (d->h - 1) * d->stride - 2 * d->pad + d->kh;
+    const int ow = (d->w - 1) * d->stride - 2 * d->pad + d->kw;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
+        (alpha && !aligned16(alpha)))
+        return ACNN_ERR_MISALIGNED;
+    const size_t yb = (size_t)d->n * d->c_out * oh * ow * elem_size(out_dtype);
+    if (overlaps(y, yb, x, (size_t)d->n * d->c_in * d->h * d->w * elem_size(d->dtype)) ||
+        overlaps(y, yb, w, (size_t)d->c_in * d->c_out * 16 * 4))
+        return ACNN_ERR_ALIAS;
+    return status_of(launch_deconv2d(*d, oh, ow, x, w, bias, act == ACNN_ACT_PRELU ? alpha : nullptr,
+                                     act, out_dtype, y, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int acnn_frame_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_t* rgba1, float t,
+                            int out_dtype, void* y, acnn_stream_t stream) {
+    if (!valid_dtype(out_dtype)) return ACNN_ERR_BAD_ENUM;
+    if (!rgba0 || !rgba1 || !y) return ACNN_ERR_NULL_POINTER;
+    if (h <= 0 || w <= 0 || h % 4 != 0 || w % 4 != 0) return ACNN_ERR_BAD_GEOMETRY;
+    if (!aligned16(rgba0) || !aligned16(rgba1) || !aligned16(y)) return ACNN_ERR_MISALIGNED;
+    const size_t yb = (size_t)7 * (h / 4) * (w / 4) * elem_size(out_dtype);
+    if (overlaps(y, yb, rgba0, (size_t)h * w * 4) || overlaps(y, yb, rgba1, (size_t)h * w * 4))
+        return ACNN_ERR_ALIAS;
+    return status_of(launch_prep_quarter(h, w, rgba0, rgba1, t, out_dtype, y,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* acnn_status_string(int status) {
+    switch (status) {
+    case ACNN_OK: return "ok";
+    case ACNN_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case ACNN_ERR_BAD_GEOMETRY: return "invalid geometry (a size is not positive or the output is empty)";
+    case ACNN_ERR_UNSUPPORTED: return "valid but unsupported geometry or mode";
+    case ACNN_ERR_MISALIGNED: return "a device pointer is not 16-byte aligned";
+    case ACNN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ACNN_ERR_ALIAS: return "the output overlaps an input";
+    case ACNN_ERR_BAD_ENUM: return "an enum argument is out of range";
+    case ACNN_ERR_CUDA: return "a CUDA call failed";
+    case ACNN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded pipeline wait expired";
+    case ACNN_ERR_TOO_LARGE: return "an index would overflow 32 bits";
+    default: return "unknown status";
+    }
+}
+
+int acnn_last_device_status(acnn_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ACNN_ERR_CUDA;
+    int* p = device_status_ptr();
+    if (!p) return ACNN_ERR_CUDA;
+    int v = 0;
+    const int zero = 0;
+    if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ACNN_ERR_CUDA;
+    if (v != 0 && cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+        return ACNN_ERR_CUDA;
+    return v;
+}
+
+int acnn_set_wait_budget(long long polls) {
+    if (polls < 0) return ACNN_ERR_BAD_GEOMETRY;
+    g_wait_budget.store(polls);
+    return ACNN_OK;
+}
+
+int acnn_section_begin(acnn_stream_t stream) {
+    return status_of(cudaStreamBeginCapture(reinterpret_cast<cudaStream_t>(stream),
+                                            cudaStreamCaptureModeThreadLocal));
+}
+
+int acnn_section_end(acnn_stream_t stream, void** exec) {
+    if (!exec) return ACNN_ERR_NULL_POINTER;
+    *exec = nullptr;
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(reinterpret_cast<cudaStream_t>(stream), &g);
+    if (e != cudaSuccess) return ACNN_ERR_CUDA;
+    cudaGraphExec_t ge = nullptr;
+    e = cudaGraphInstantiate(&ge, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return ACNN_ERR_CUDA;
+    *exec = ge;
+    return ACNN_OK;
+}
+
+int acnn_section_launch(void* exec, acnn_stream_t stream) {
+    if (!exec) return ACNN_ERR_NULL_POINTER;
+    return status_of(cudaGraphLaunch(static_cast<cudaGraphExec_t>(exec),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int acnn_section_destroy(void* exec) {
+    if (!exec) return ACNN_OK;
+    return status_of(cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(exec)));
+}
+
+int acnn_device_sm_count(void) { return sm_count(); }
+
+}  // extern "C"

@@ -1,0 +1,122 @@
+// common.cuh -- device helpers shared by the kernels of libacnn (sm_103a).
+//
+// Storage types, fp32 conversion, the fused epilogue (bias -> activation /
+// residual -> down-cast) and launch-shape helpers.  Nothing here is shared
+// with the oracle.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/acnn.h"
+
+namespace acnn {
+
+// ---------------------------------------------------------------- storage types
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
+}
+
+// fp32 -> storage type, round to nearest even (the reading used where the
+// pages leave the f32 -> f16 store rounding open).
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// A vector of V storage elements moved as one aligned load/store.
+template <typename T, int V> struct alignas(sizeof(T) * V) Vec {
+    T v[V];
+};
+
+// ---------------------------------------------------------------- activations
+// relu = max(v, 0) and silu = v / (1 + exp(-v)) as in rtdetr_gpu.rs ADDACT_SRC;
+// prelu = v >= 0 ? v : alpha * v as in rt.js wgslConv.
+__device__ __forceinline__ float apply_act(int act, float v, float alpha) {
+    switch (act) {
+    case ACNN_ACT_RELU: return fmaxf(v, 0.0f);
+    case ACNN_ACT_SILU: return v / (1.0f + expf(-v));
+    case ACNN_ACT_PRELU: return v >= 0.0f ? v : alpha * v;
+    default: return v;
+    }
+}
+
+// Epilogue of conv2d_fused on the bias-added accumulator v:
+//   RES_NONE: act(v); ADD_THEN_ACT: act(v + r); ACT_THEN_ADD: act(v) + r.
+__device__ __forceinline__ float epilogue(float v, int act, float alpha, int res_mode, float r) {
+    if (res_mode == ACNN_RES_ADD_THEN_ACT) return apply_act(act, v + r, alpha);
+    float a = apply_act(act, v, alpha);
+    return res_mode == ACNN_RES_ACT_THEN_ADD ? a + r : a;
+}
+
+// Out-of-line copy of epilogue() for kernels whose epilogue is not hot: keeps
+// one copy of the activation code instead of one per unrolled output.
+static __device__ __noinline__ float epilogue_outlined(float v, int act, float alpha, int res_mode, float r) {
+    return epilogue(v, act, alpha, res_mode, r);
+}
+
+__device__ __forceinline__ int64_t act_index(int layout, int C, int H, int W, int n, int c,
+                                             int y, int x) {
+    if (layout == ACNN_NHWC) return (((int64_t)n * H + y) * W + x) * C + c;
+    return (((int64_t)n * C + c) * H + y) * W + x;
+}
+
+}  // namespace acnn
+
+// ---------------------------------------------------------------- host helpers
+// Launch helpers and per-TU launchers, declared here and defined in the .cu
+// file that owns each kernel; the ABI layer (abi.cu) validates arguments
+// before calling any of them.
+namespace acnn {
+
+struct ConvArgs {
+    acnn_conv_desc d;
+    int oh, ow;
+    const void* x;
+    const void* w;
+    const float* bias;
+    const float* alpha;
+    const void* residual;
+    int res_mode, act;
+    void* y;
+    int out_layout;  // layout y and residual are written/read in (may differ from d.layout)
+};
+
+int sm_count();
+int* device_status_ptr();         // device address of the status word
+long long wait_budget_polls();    // 0 = default (time-bounded)
+
+cudaError_t launch_direct_conv(const ConvArgs& a, cudaStream_t s);
+// tensor-core path; returns ACNN_OK or an ACNN_ERR_* status
+int launch_igemm_conv(const ConvArgs& a, cudaStream_t s);
+
+cudaError_t launch_pool2d(int kind, int n, int h, int w, int c, int k, int stride, int pad,
+                          int layout, int dtype, const void* x, void* y, cudaStream_t s);
+cudaError_t launch_resize2d(int mode, int n, int c, int h, int w, int oh, int ow, int layout,
+                            int in_dtype, int out_dtype, const void* x, void* y, cudaStream_t s);
+cudaError_t launch_concat(int n, int h, int w, int ca, int cb, int layout, int dtype,
+                          const void* a, const void* b, void* y, cudaStream_t s);
+cudaError_t launch_deconv2d(const acnn_conv_desc& d, int oh, int ow, const void* x,
+                            const float* w, const float* bias, const float* alpha, int act,
+                            int out_dtype, void* y, cudaStream_t s);
+cudaError_t launch_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_t* rgba1,
+                                float t, int out_dtype, void* y, cudaStream_t s);
+// NCHW -> NHWC activation transpose and OIHW -> OHWI weight transpose (2-byte types)
+cudaError_t launch_nchw_to_nhwc(int n, int c, int hw, int elem_bytes, const void* x, void* y,
+                                cudaStream_t s);
+
+inline int grid_for(long long work_items, int threads, int per_sm = 8) {
+    long long want = (work_items + threads - 1) / threads;
+    long long cap = (long long)sm_count() * per_sm;
+    if (want > cap) want = cap;
+    return want < 1 ? 1 : (int)want;
+}
+
+}  // namespace acnn

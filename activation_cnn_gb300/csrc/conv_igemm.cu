@@ -1,0 +1,604 @@
+// conv_igemm.cu -- NHWC implicit-GEMM conv2d_fused on the 5th-generation
+// tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// GEMM view of the conv (rtdetr_gpu.rs RtDetrGpu::conv: im2col -> GEMM with
+// the bias and activation in the epilogue): M = N*OH*OW output pixels,
+// N_g = C_out, K = kh*kw*C_in in (ky, kx, ci) order.  Nothing is materialised:
+//   * A (128 pixels x 64 channels per k-block) arrives by TMA -- a tiled box of
+//     the [N*H*W, C_in] matrix for 1x1/s1/p0 convs (the NHWC map *is* the GEMM
+//     operand, as the page notes), otherwise an im2col-mode box: 128
+//     consecutive output pixels (wrapping rows and images), each read at the
+//     tap offset (kx, ky), with the conv stride as the traversal stride and the
+//     padding as the bounding box, out-of-image taps filled with zeros.
+//   * B (BN output channels x 64 channels) is a tiled box of the OHWI weight
+//     viewed as [C_out][kh*kw][C_in].
+//   * Both land in shared memory in the 128-byte-swizzled K-major layout that
+//     tcgen05.mma reads directly; a 64-channel k-block is one 128-byte row.
+// Warp roles (192 threads, persistent, one CTA per SM):
+//   warp 0  TMA producer (one lane) over a STAGES-deep ring of smem slots
+//   warp 1  TMEM allocator and MMA issuer (one lane): 4 x (128 x BN x 16) MMAs
+//           per k-block into an fp32 TMEM accumulator
+//   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, + bias, activation,
+//           residual (before or after the activation), down-cast, store.
+// Two TMEM accumulators alternate so the epilogue of one tile overlaps the
+// MMAs of the next.  Every mbarrier wait is bounded: on expiry the kernel
+// records ACNN_ERR_DEVICE_TIMEOUT in a device status word, raises a CTA-wide
+// abort flag, drains its own in-flight copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace acnn {
+
+namespace {
+
+constexpr int BM = 128;             // output pixels per tile (TMEM lanes)
+constexpr int BK = 64;              // channels per k-block: 64 x 2 B = one 128-B swizzle row
+constexpr int kThreads = 192;       // 6 warps
+constexpr uint32_t kABytes = BM * BK * 2;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s per wait
+constexpr unsigned long long kDrainNs = 200000000ull;     // 0.2 s per drain wait
+
+template <int BN> struct Cfg {
+    static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr uint32_t kBBytes = BN * BK * 2;
+    static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+    static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStages * (kABytes + kBBytes) + 256;
+};
+
+struct Params {
+    int M, C_out, taps, KW, kb_per_tap, num_kb;
+    int num_m_tiles, num_n_tiles;
+    int OW, OHW, S, P;
+    int a_mode;       // 0: tiled A (1x1/s1/p0); 1: im2col A
+    int out_layout;   // ACNN_NHWC or ACNN_NCHW for y and the residual
+    int act, res_mode;
+    const float* bias;
+    const float* alpha;
+    const void* res;
+    void* y;
+    int* status;
+    long long budget;  // >0: give up a wait after this many polls; 0: after kTimeoutNs
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Slow path of a bounded wait for the phase of `bar` with parity `parity`.
+// Returns false if the CTA is aborting or this wait expired; on expiry it
+// records the timeout in the device status word and raises the abort flag.
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, long long budget,
+                                             int* status) {
+    const uint64_t t0 = globaltimer();
+    for (long long i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        bool expired = budget > 0 && i >= budget;
+        if ((i & 31) == 0) {
+            if (*abort_flag) return false;
+            if (budget <= 0 && globaltimer() - t0 > kTimeoutNs) expired = true;
+        }
+        if (expired) {
+            atomicCAS(status, 0, ACNN_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
+                                           volatile int* abort_flag, const Params& p) {
+    if (p.budget <= 0 && mbar_try_wait(bar, parity)) return true;
+    return wait_phase_slow(bar, parity, abort_flag, p.budget, p.status);
+}
+
+// Time-bounded wait used only while draining after an abort.
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kDrainNs) return;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// im2col load: coordinates {c, w, h, n} of the first pixel's window corner and
+// the tap offsets {kx, ky} added to every pixel's position.
+__device__ __forceinline__ void tma_load_im2col(uint32_t dst, const CUtensorMap* map,
+                                                uint32_t bar, int c, int w, int h, int n,
+                                                uint16_t off_w, uint16_t off_h) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], {%7, %8};" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c), "r"(w), "r"(h), "r"(n),
+        "h"(off_w), "h"(off_h)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, 128 x N x 16, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 op this thread issued so far completes.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one row per lane).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 B, 8-row core-matrix groups 1024 B apart.  Advancing the start address
+// by 32 B steps K by 16 elements inside the swizzle atom.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4)  // start address >> 4
+           | ((uint64_t)1 << 16)                // leading byte offset (unused here)
+           | ((uint64_t)(1024 >> 4) << 32)      // stride byte offset: 8 rows x 128 B
+           | ((uint64_t)1 << 46)                // descriptor version (tcgen05)
+           | ((uint64_t)2 << 61);               // 128-byte swizzle
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B both bf16 or
+// both fp16, both K-major, N >> 3 and M >> 4 in their fields.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool bf16) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+template <typename T> struct IsBf16 { static constexpr bool v = false; };
+template <> struct IsBf16<__nv_bfloat16> { static constexpr bool v = true; };
+
+// ---------------------------------------------------------------- the kernel
+template <int BN, typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    igemm_conv_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+    using C = Cfg<BN>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + S * kABytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::kBBytes);
+    // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int m0 = (tile / p.num_n_tiles) * BM;
+                const int n0 = (tile % p.num_n_tiles) * BN;
+                // window corner of the tile's first output pixel
+                const int img = m0 / p.OHW, r = m0 % p.OHW;
+                const int wc = (r % p.OW) * p.S - p.P, hc = (r / p.OW) * p.S - p.P;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    const int tap = kb / p.kb_per_tap;
+                    const int c0 = (kb % p.kb_per_tap) * BK;
+                    if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, kABytes + C::kBBytes);
+                    const uint32_t a_dst = smem_u32(sA + stage * kABytes);
+                    if (p.a_mode == 0)
+                        tma_load_2d(a_dst, &tmap_a, fb, c0, m0);
+                    else
+                        tma_load_im2col(a_dst, &tmap_a, fb, c0, wc, hc, img,
+                                        (uint16_t)(tap % p.KW), (uint16_t)(tap / p.KW));
+                    tma_load_3d(smem_u32(sB + stage * C::kBBytes), &tmap_b, fb, c0, tap, n0);
+                    issued_mask |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every copy this thread started land before the CTA exits
+                for (int s = 0; s < S; ++s)
+                    if (issued_mask & (1u << s)) wait_drain(full_bar(s), (issued_parity >> s) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = make_idesc(BM, BN, IsBf16<T>::v);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                if (!wait_phase(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_phase(full_bar(stage), phase, abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = sw128_desc(smem_u32(sA + stage * kABytes));
+                    const uint64_t bdesc = sw128_desc(smem_u32(sB + stage * C::kBBytes));
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) != 0);
+                    mma_commit(empty_bar(stage));  // frees the slot once these MMAs finish
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) {
+                mma_commit(drain_bar);  // wait for every MMA this thread issued
+                wait_drain(drain_bar, 0);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue warps
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        const T* res = static_cast<const T*>(p.res);
+        T* y = static_cast<T*>(p.y);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const int m0 = (tile / p.num_n_tiles) * BM;
+            const int n0 = (tile % p.num_n_tiles) * BN;
+            // every lane waits (acquiring the accumulator); the warp then agrees,
+            // so the warp-collective TMEM loads below run converged or not at all
+            const bool ok = __all_sync(0xffffffffu, wait_phase(tfull_bar(acc), acc_phase, abort_flag, p));
+            if (!ok) break;
+            tc_fence_after();
+            const int m = m0 + row;
+            const bool valid = m < p.M;
+            // NHWC: row m of [M, C_out]; NCHW: pixel m%OHW of image m/OHW, planes OHW apart
+            long long base, cstride;
+            if (p.out_layout == ACNN_NHWC) {
+                base = (long long)m * p.C_out;
+                cstride = 1;
+            } else {
+                const int img = m / p.OHW;
+                base = (long long)img * p.C_out * p.OHW + (m - img * p.OHW);
+                cstride = p.OHW;
+            }
+            for (int c = 0; c < BN; c += 32) {
+                if (n0 + c >= p.C_out) break;  // uniform across the warp
+                float v[32];
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), v);
+                if (!valid) continue;
+                if (p.out_layout == ACNN_NHWC) {
+#pragma unroll
+                    for (int g = 0; g < 32; g += 8) {
+                        const int co = n0 + c + g;
+                        if (co >= p.C_out) break;
+                        Vec<T, 8> rv, ov;
+                        if (p.res_mode != ACNN_RES_NONE)
+                            rv = *reinterpret_cast<const Vec<T, 8>*>(res + base + co);
+                        const float4 b0 = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias + co))
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float4 b1 = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias + co + 4))
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float al = p.act == ACNN_ACT_PRELU ? __ldg(p.alpha + co + j) : 0.f;
+                            const float r = p.res_mode != ACNN_RES_NONE ? to_f32(rv.v[j]) : 0.f;
+                            ov.v[j] = from_f32<T>(epilogue(v[g + j] + bb[j], p.act, al, p.res_mode, r));
+                        }
+                        *reinterpret_cast<Vec<T, 8>*>(y + base + co) = ov;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int co = n0 + c + j;
+                        if (co >= p.C_out) continue;
+                        const long long oi = base + (long long)co * cstride;
+                        const float bv = p.bias ? __ldg(p.bias + co) : 0.f;
+                        const float al = p.act == ACNN_ACT_PRELU ? __ldg(p.alpha + co) : 0.f;
+                        const float r = p.res_mode != ACNN_RES_NONE ? to_f32(res[oi]) : 0.f;
+                        y[oi] = from_f32<T>(epilogue(v[j] + bv, p.act, al, p.res_mode, r));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+PFN_cuTensorMapEncodeIm2col_v12000 g_encode_im2col = nullptr;
+
+bool load_encoders() {
+    static std::once_flag once;
+    static bool ok = false;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q1, q2;
+        cudaError_t e1 = cudaGetDriverEntryPointByVersion(
+            "cuTensorMapEncodeTiled", reinterpret_cast<void**>(&g_encode_tiled), 12000,
+            cudaEnableDefault, &q1);
+        cudaError_t e2 = cudaGetDriverEntryPointByVersion(
+            "cuTensorMapEncodeIm2col", reinterpret_cast<void**>(&g_encode_im2col), 12000,
+            cudaEnableDefault, &q2);
+        ok = e1 == cudaSuccess && e2 == cudaSuccess && q1 == cudaDriverEntryPointSuccess &&
+             q2 == cudaDriverEntryPointSuccess && g_encode_tiled && g_encode_im2col;
+    });
+    return ok;
+}
+
+template <int BN, typename T>
+int launch_bn(const ConvArgs& a, const CUtensorMap& ta, const CUtensorMap& tb, Params prm,
+              cudaStream_t s) {
+    using C = Cfg<BN>;
+    static bool attr_set = false;  // per instantiation; set once per process
+    auto kern = igemm_conv_kernel<BN, T>;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)C::kSmem) != cudaSuccess)
+            return ACNN_ERR_CUDA;
+        attr_set = true;
+    }
+    prm.num_n_tiles = (a.d.c_out + BN - 1) / BN;
+    const int tiles = prm.num_m_tiles * prm.num_n_tiles;
+    const int grid = tiles < sm_count() ? tiles : sm_count();
+    kern<<<grid, kThreads, C::kSmem, s>>>(ta, tb, prm);
+    return cudaGetLastError() == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
+}
+
+template <typename T>
+int launch_typed(const ConvArgs& a, int bn, const CUtensorMap& ta, const CUtensorMap& tb,
+                 const Params& prm, cudaStream_t s) {
+    if (bn == 256) return launch_bn<256, T>(a, ta, tb, prm, s);
+    if (bn == 128) return launch_bn<128, T>(a, ta, tb, prm, s);
+    return launch_bn<64, T>(a, ta, tb, prm, s);
+}
+
+// Output-channel tile: the widest of 256/128/64 that C_out fills, narrowed
+// while the tile count leaves most SMs idle.
+int pick_bn(int c_out, int num_m_tiles) {
+    int bn = c_out >= 256 ? 256 : (c_out > 64 ? 128 : 64);
+    const int sms = sm_count();
+    while (bn > 64 && (long long)num_m_tiles * ((c_out + bn - 1) / bn) < sms) bn >>= 1;
+    return bn;
+}
+
+}  // namespace
+
+int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
+    const acnn_conv_desc& d = a.d;
+    if (!load_encoders()) return ACNN_ERR_CUDA;
+    const int taps = d.kh * d.kw;
+    const long long M = (long long)d.n * a.oh * a.ow;
+    const CUtensorMapDataType dt =
+        d.dtype == ACNN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const bool tiled = d.kh == 1 && d.kw == 1 && d.stride == 1 && d.pad == 0;
+
+    alignas(64) CUtensorMap ta, tb;
+    CUresult r;
+    if (tiled) {
+        cuuint64_t dims[2] = {(cuuint64_t)d.c_in, (cuuint64_t)M};
+        cuuint64_t strides[1] = {(cuuint64_t)d.c_in * 2};
+        cuuint32_t box[2] = {BK, BM};
+        cuuint32_t es[2] = {1, 1};
+        r = g_encode_tiled(&ta, dt, 2, const_cast<void*>(a.x), dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[4] = {(cuuint64_t)d.c_in, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
+        cuuint64_t strides[3] = {(cuuint64_t)d.c_in * 2, (cuuint64_t)d.w * d.c_in * 2,
+                                 (cuuint64_t)d.h * d.w * d.c_in * 2};
+        // window corners range over [-pad, dim - 1 + pad - (k - 1)] (W then H)
+        int lower[2] = {-d.pad, -d.pad};
+        int upper[2] = {d.pad - (d.kw - 1), d.pad - (d.kh - 1)};
+        cuuint32_t es[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
+        r = g_encode_im2col(&ta, dt, 4, const_cast<void*>(a.x), dims, strides, lower, upper, BK,
+                            BM, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
+
+    const int num_m_tiles = (int)((M + BM - 1) / BM);
+    const int bn = pick_bn(d.c_out, num_m_tiles);
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)d.c_in, (cuuint64_t)taps, (cuuint64_t)d.c_out};
+        cuuint64_t strides[2] = {(cuuint64_t)d.c_in * 2, (cuuint64_t)taps * d.c_in * 2};
+        cuuint32_t box[3] = {BK, 1, (cuuint32_t)bn};
+        cuuint32_t es[3] = {1, 1, 1};
+        r = g_encode_tiled(&tb, dt, 3, const_cast<void*>(a.w), dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
+
+    Params prm{};
+    prm.M = (int)M;
+    prm.C_out = d.c_out;
+    prm.taps = taps;
+    prm.KW = d.kw;
+    prm.kb_per_tap = (d.c_in + BK - 1) / BK;
+    prm.num_kb = taps * prm.kb_per_tap;
+    prm.num_m_tiles = num_m_tiles;
+    prm.OW = a.ow;
+    prm.OHW = a.oh * a.ow;
+    prm.S = d.stride;
+    prm.P = d.pad;
+    prm.a_mode = tiled ? 0 : 1;
+    prm.out_layout = a.out_layout;
+    prm.act = a.act;
+    prm.res_mode = a.res_mode;
+    prm.bias = a.bias;
+    prm.alpha = a.alpha;
+    prm.res = a.residual;
+    prm.y = a.y;
+    prm.status = device_status_ptr();
+    prm.budget = wait_budget_polls();
+    if (!prm.status) return ACNN_ERR_CUDA;
+    if (d.dtype == ACNN_BF16) return launch_typed<__nv_bfloat16>(a, bn, ta, tb, prm, s);
+    return launch_typed<__half>(a, bn, ta, tb, prm, s);
+}
+
+}  // namespace acnn

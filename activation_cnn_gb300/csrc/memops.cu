@@ -1,0 +1,513 @@
+// memops.cu -- the memory-bound companion ops of the conv layer:
+// max/avg pool, nearest/bilinear resize, channel concat, the RGBA8 frame
+// prep, the 4x4/s2 transposed conv, and the NCHW -> NHWC transpose that
+// feeds NCHW tensors to the tensor-core conv.
+//
+// NHWC kernels move 16 bytes per thread along the channel axis (8 bf16/fp16
+// or 4 fp32 elements) when the channel count allows it; NCHW kernels walk the
+// innermost (x) axis so that a warp touches consecutive addresses.  All use
+// grid-stride loops over a grid sized in multiples of the SM count.
+#include "common.cuh"
+
+namespace acnn {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// ----------------------------------------------------------------------------
+// pooling: rtdetr_gpu.rs MAXPOOL_SRC (taps outside the input are skipped, so
+// padding acts as -inf; the running max is replaced only by a strictly larger
+// tap, in (dy, dx) order) and AVGPOOL_SRC ((a+b+c+d)*0.25 over a 2x2/s2 window;
+// k x k windows generalise it as sum * (1/k^2)).
+// ----------------------------------------------------------------------------
+template <typename T, int V>
+__global__ void __launch_bounds__(kThreads) pool_nhwc_kernel(
+    const T* __restrict__ x, T* __restrict__ y, int kind, int N, int H, int W, int C, int OH,
+    int OW, int K, int S, int P) {
+    const int CV = C / V;
+    const long long total = (long long)N * OH * OW * CV;
+    const float inv = 1.0f / (float)(K * K);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        int cv = (int)(i % CV);
+        long long p = i / CV;
+        int ox = (int)(p % OW);
+        p /= OW;
+        int oy = (int)(p % OH);
+        int n = (int)(p / OH);
+        float acc[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = kind == ACNN_POOL_MAX ? -INFINITY : 0.0f;
+        for (int dy = 0; dy < K; ++dy) {
+            int iy = oy * S + dy - P;
+            if (iy < 0 || iy >= H) continue;
+            for (int dx = 0; dx < K; ++dx) {
+                int ix = ox * S + dx - P;
+                if (ix < 0 || ix >= W) continue;
+                Vec<T, V> t = *reinterpret_cast<const Vec<T, V>*>(
+                    x + (((long long)n * H + iy) * W + ix) * C + (long long)cv * V);
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    float f = to_f32(t.v[v]);
+                    if (kind == ACNN_POOL_MAX) {
+                        if (f > acc[v]) acc[v] = f;
+                    } else {
+                        acc[v] += f;
+                    }
+                }
+            }
+        }
+        Vec<T, V> o;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            o.v[v] = from_f32<T>(kind == ACNN_POOL_MAX ? acc[v] : acc[v] * inv);
+        *reinterpret_cast<Vec<T, V>*>(y + (((long long)n * OH + oy) * OW + ox) * C +
+                                      (long long)cv * V) = o;
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) pool_nchw_kernel(
+    const T* __restrict__ x, T* __restrict__ y, int kind, int N, int C, int H, int W, int OH,
+    int OW, int K, int S, int P) {
+    const long long total = (long long)N * C * OH * OW;
+    const float inv = 1.0f / (float)(K * K);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        int ox = (int)(i % OW);
+        long long p = i / OW;
+        int oy = (int)(p % OH);
+        long long nc = p / OH;
+        const T* plane = x + nc * H * W;
+        float acc = kind == ACNN_POOL_MAX ? -INFINITY : 0.0f;
+        for (int dy = 0; dy < K; ++dy) {
+            int iy = oy * S + dy - P;
+            if (iy < 0 || iy >= H) continue;
+            for (int dx = 0; dx < K; ++dx) {
+                int ix = ox * S + dx - P;
+                if (ix < 0 || ix >= W) continue;
+                float f = to_f32(plane[(long long)iy * W + ix]);
+                if (kind == ACNN_POOL_MAX) {
+                    if (f > acc) acc = f;
+                } else {
+                    acc += f;
+                }
+            }
+        }
+        y[i] = from_f32<T>(kind == ACNN_POOL_MAX ? acc : acc * inv);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// resize.  Nearest: source index floor(dst * in / out) (rtdetr_gpu.rs
+// UPSAMPLE_SRC for 2x).  Bilinear, align_corners=false (rt.js wgslPrepQuarter,
+// wgslFlowOut): src = (dst + 0.5) * (in/out) - 0.5, x0 = floor(src),
+// f = src - x0, taps x0 and x0 + 1 clamped to the image,
+// mix(mix(v00, v10, fx), mix(v01, v11, fx), fy).
+// ----------------------------------------------------------------------------
+struct BilinearTap {
+    int a, b;
+    float f;
+};
+
+__device__ __forceinline__ BilinearTap bilinear_tap(int dst, float scale, int in) {
+    float src = ((float)dst + 0.5f) * scale - 0.5f;
+    float fl = floorf(src);
+    int i0 = (int)fl;
+    BilinearTap t;
+    t.f = src - fl;
+    t.a = min(max(i0, 0), in - 1);
+    t.b = min(max(i0 + 1, 0), in - 1);
+    return t;
+}
+
+__device__ __forceinline__ float mixf(float a, float b, float t) { return a * (1.0f - t) + b * t; }
+
+template <typename Ti, typename To, int V>
+__global__ void __launch_bounds__(kThreads) resize_nhwc_kernel(
+    const Ti* __restrict__ x, To* __restrict__ y, int mode, int N, int H, int W, int C, int OH,
+    int OW, float sy, float sx) {
+    const int CV = C / V;
+    const long long total = (long long)N * OH * OW * CV;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        int cv = (int)(i % CV);
+        long long p = i / CV;
+        int ox = (int)(p % OW);
+        p /= OW;
+        int oy = (int)(p % OH);
+        int n = (int)(p / OH);
+        const Ti* img = x + (long long)n * H * W * C + (long long)cv * V;
+        Vec<To, V> o;
+        if (mode == ACNN_RESIZE_NEAREST) {
+            int iy = (int)(((long long)oy * H) / OH);
+            int ix = (int)(((long long)ox * W) / OW);
+            Vec<Ti, V> t = *reinterpret_cast<const Vec<Ti, V>*>(img + ((long long)iy * W + ix) * C);
+#pragma unroll
+            for (int v = 0; v < V; ++v) o.v[v] = from_f32<To>(to_f32(t.v[v]));
+        } else {
+            BilinearTap ty = bilinear_tap(oy, sy, H), tx = bilinear_tap(ox, sx, W);
+            Vec<Ti, V> v00 = *reinterpret_cast<const Vec<Ti, V>*>(img + ((long long)ty.a * W + tx.a) * C);
+            Vec<Ti, V> v10 = *reinterpret_cast<const Vec<Ti, V>*>(img + ((long long)ty.a * W + tx.b) * C);
+            Vec<Ti, V> v01 = *reinterpret_cast<const Vec<Ti, V>*>(img + ((long long)ty.b * W + tx.a) * C);
+            Vec<Ti, V> v11 = *reinterpret_cast<const Vec<Ti, V>*>(img + ((long long)ty.b * W + tx.b) * C);
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                float top = mixf(to_f32(v00.v[v]), to_f32(v10.v[v]), tx.f);
+                float bot = mixf(to_f32(v01.v[v]), to_f32(v11.v[v]), tx.f);
+                o.v[v] = from_f32<To>(mixf(top, bot, ty.f));
+            }
+        }
+        *reinterpret_cast<Vec<To, V>*>(y + (((long long)n * OH + oy) * OW + ox) * C +
+                                       (long long)cv * V) = o;
+    }
+}
+
+template <typename Ti, typename To>
+__global__ void __launch_bounds__(kThreads) resize_nchw_kernel(
+    const Ti* __restrict__ x, To* __restrict__ y, int mode, int NC, int H, int W, int OH, int OW,
+    float sy, float sx) {
+    const long long total = (long long)NC * OH * OW;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        int ox = (int)(i % OW);
+        long long p = i / OW;
+        int oy = (int)(p % OH);
+        long long nc = p / OH;
+        const Ti* plane = x + nc * H * W;
+        float v;
+        if (mode == ACNN_RESIZE_NEAREST) {
+            int iy = (int)(((long long)oy * H) / OH);
+            int ix = (int)(((long long)ox * W) / OW);
+            v = to_f32(plane[(long long)iy * W + ix]);
+        } else {
+            BilinearTap ty = bilinear_tap(oy, sy, H), tx = bilinear_tap(ox, sx, W);
+            float top = mixf(to_f32(plane[(long long)ty.a * W + tx.a]),
+                             to_f32(plane[(long long)ty.a * W + tx.b]), tx.f);
+            float bot = mixf(to_f32(plane[(long long)ty.b * W + tx.a]),
+                             to_f32(plane[(long long)ty.b * W + tx.b]), tx.f);
+            v = mixf(top, bot, ty.f);
+        }
+        y[i] = from_f32<To>(v);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// concat: rtdetr_gpu.rs CONCAT_SRC, y = [a | b] along channels.  NHWC: per
+// pixel; NCHW: per image, the c_a planes of a then the c_b planes of b.  Both
+// reduce to copying runs of `ra` elements from a and `rb` from b into
+// consecutive runs of ra + rb elements of y.
+// ----------------------------------------------------------------------------
+template <typename T, int V>
+__global__ void __launch_bounds__(kThreads) concat_kernel(
+    const T* __restrict__ a, const T* __restrict__ b, T* __restrict__ y, long long runs,
+    int ra, int rb) {
+    const int rv = (ra + rb) / V;
+    const long long total = runs * rv;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        long long run = i / rv;
+        int e = (int)(i % rv) * V;
+        const T* src = e < ra ? a + run * ra + e : b + run * rb + (e - ra);
+        *reinterpret_cast<Vec<T, V>*>(y + run * (ra + rb) + e) =
+            *reinterpret_cast<const Vec<T, V>*>(src);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// frame prep: rt.js wgslPrepQuarter.  unpack4x8unorm of each RGBA8 pixel gives
+// r, g, b = bytes 0, 1, 2 over 255; the output planes are b, g, r of frame 0,
+// b, g, r of frame 1 and a plane holding t, each colour plane bilinearly
+// downsampled by 4 (src = (dst + 0.5) * 4 - 0.5, taps clamped).
+// ----------------------------------------------------------------------------
+template <typename To>
+__global__ void __launch_bounds__(kThreads) prep_quarter_kernel(
+    const uint32_t* __restrict__ f0, const uint32_t* __restrict__ f1, To* __restrict__ y, int H,
+    int W, float t) {
+    const int QH = H / 4, QW = W / 4;
+    const long long P = (long long)QH * QW;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < P;
+         i += (long long)gridDim.x * blockDim.x) {
+        int qx = (int)(i % QW), qy = (int)(i / QW);
+        BilinearTap ty = bilinear_tap(qy, 4.0f, H), tx = bilinear_tap(qx, 4.0f, W);
+#pragma unroll
+        for (int f = 0; f < 2; ++f) {
+            const uint32_t* fr = f == 0 ? f0 : f1;
+            uint32_t p00 = fr[(long long)ty.a * W + tx.a], p10 = fr[(long long)ty.a * W + tx.b];
+            uint32_t p01 = fr[(long long)ty.b * W + tx.a], p11 = fr[(long long)ty.b * W + tx.b];
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                int sh = 8 * (2 - k);  // plane k is byte 2 - k: b, g, r
+                float top = mixf(((p00 >> sh) & 255u) / 255.0f, ((p10 >> sh) & 255u) / 255.0f, tx.f);
+                float bot = mixf(((p01 >> sh) & 255u) / 255.0f, ((p11 >> sh) & 255u) / 255.0f, tx.f);
+                y[(3 * f + k) * P + i] = from_f32<To>(mixf(top, bot, ty.f));
+            }
+        }
+        y[6 * P + i] = from_f32<To>(t);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// deconv: rt.js wgslDeconv in gather form.  One thread per output pixel and
+// block of up to 8 output channels.  For output row oy the live taps are the
+// ky with ty = oy + P - ky >= 0, ty % S == 0 and iy = ty / S < H; for 4x4/s2/p1
+// that is two of the four ky (one parity class), so 4 of 16 taps are live.
+// ----------------------------------------------------------------------------
+constexpr int kDeconvCoBlock = 8;
+
+template <typename Ti, typename To>
+__global__ void __launch_bounds__(kThreads) deconv_kernel(
+    const Ti* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
+    const float* __restrict__ alpha, To* __restrict__ y, int layout, int N, int CI, int CO,
+    int H, int W, int OH, int OW, int K, int S, int P, int act) {
+    const long long pix = (long long)N * OH * OW;
+    const int co_blocks = (CO + kDeconvCoBlock - 1) / kDeconvCoBlock;
+    const long long total = pix * co_blocks;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        int cb = (int)(i / pix);
+        long long q = i % pix;
+        int ox = (int)(q % OW);
+        q /= OW;
+        int oy = (int)(q % OH);
+        int n = (int)(q / OH);
+        const int co0 = cb * kDeconvCoBlock;
+        const int nco = min(kDeconvCoBlock, CO - co0);
+        float acc[kDeconvCoBlock];
+#pragma unroll
+        for (int j = 0; j < kDeconvCoBlock; ++j)
+            acc[j] = (bias && j < nco) ? bias[co0 + j] : 0.0f;
+        for (int ky = 0; ky < K; ++ky) {
+            int ty = oy + P - ky;
+            if (ty < 0 || ty % S != 0) continue;
+            int iy = ty / S;
+            if (iy >= H) continue;
+            for (int kx = 0; kx < K; ++kx) {
+                int tx = ox + P - kx;
+                if (tx < 0 || tx % S != 0) continue;
+                int ix = tx / S;
+                if (ix >= W) continue;
+                for (int ci = 0; ci < CI; ++ci) {
+                    float xv = to_f32(x[act_index(layout, CI, H, W, n, ci, iy, ix)]);
+                    const float* wp = w + ((long long)ci * CO + co0) * K * K + ky * K + kx;
+#pragma unroll
+                    for (int j = 0; j < kDeconvCoBlock; ++j)
+                        if (j < nco) acc[j] = fmaf(xv, __ldg(wp + (long long)j * K * K), acc[j]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kDeconvCoBlock; ++j)
+            if (j < nco) {
+                float al = (act == ACNN_ACT_PRELU) ? alpha[co0 + j] : 0.0f;
+                y[act_index(layout, CO, OH, OW, n, co0 + j, oy, ox)] =
+                    from_f32<To>(apply_act(act, acc[j], al));
+            }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// NCHW -> NHWC transpose of 16-bit elements through a 32x32 shared tile:
+// per image, [C][HW] -> [HW][C].  Reads and writes are both coalesced.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) transpose_kernel(const uint16_t* __restrict__ x,
+                                                         uint16_t* __restrict__ y, int C, int HW) {
+    __shared__ uint16_t tile[32][33];
+    const int n = blockIdx.z;
+    const int c0 = blockIdx.y * 32, p0 = blockIdx.x * 32;
+    const uint16_t* xi = x + (long long)n * C * HW;
+    uint16_t* yi = y + (long long)n * C * HW;
+    int c = c0 + threadIdx.y, p = p0 + threadIdx.x;
+    if (c < C && p < HW) tile[threadIdx.y][threadIdx.x] = xi[(long long)c * HW + p];
+    __syncthreads();
+    c = c0 + threadIdx.x;
+    p = p0 + threadIdx.y;
+    if (c < C && p < HW) yi[(long long)p * C + c] = tile[threadIdx.x][threadIdx.y];
+}
+
+template <typename T> int vec_for(int elems) {
+    constexpr int V = 16 / sizeof(T);
+    return elems % V == 0 ? V : 1;
+}
+
+template <typename T>
+cudaError_t pool_typed(int kind, int n, int h, int w, int c, int k, int stride, int pad,
+                       int layout, const void* x, void* y, cudaStream_t s) {
+    int oh = (h + 2 * pad - k) / stride + 1, ow = (w + 2 * pad - k) / stride + 1;
+    const T* xt = static_cast<const T*>(x);
+    T* yt = static_cast<T*>(y);
+    if (layout == ACNN_NHWC) {
+        constexpr int V = 16 / sizeof(T);
+        if (c % V == 0) {
+            long long work = (long long)n * oh * ow * (c / V);
+            pool_nhwc_kernel<T, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+                xt, yt, kind, n, h, w, c, oh, ow, k, stride, pad);
+        } else {
+            long long work = (long long)n * oh * ow * c;
+            pool_nhwc_kernel<T, 1><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+                xt, yt, kind, n, h, w, c, oh, ow, k, stride, pad);
+        }
+    } else {
+        long long work = (long long)n * c * oh * ow;
+        pool_nchw_kernel<T><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+            xt, yt, kind, n, c, h, w, oh, ow, k, stride, pad);
+    }
+    return cudaGetLastError();
+}
+
+template <typename Ti, typename To>
+cudaError_t resize_typed(int mode, int n, int c, int h, int w, int oh, int ow, int layout,
+                         const void* x, void* y, cudaStream_t s) {
+    const Ti* xt = static_cast<const Ti*>(x);
+    To* yt = static_cast<To*>(y);
+    float sy = (float)h / (float)oh, sx = (float)w / (float)ow;
+    if (layout == ACNN_NHWC) {
+        constexpr int V = (16 / sizeof(Ti)) < (16 / sizeof(To)) ? (16 / sizeof(Ti)) : (16 / sizeof(To));
+        if (c % V == 0) {
+            long long work = (long long)n * oh * ow * (c / V);
+            resize_nhwc_kernel<Ti, To, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+                xt, yt, mode, n, h, w, c, oh, ow, sy, sx);
+        } else {
+            long long work = (long long)n * oh * ow * c;
+            resize_nhwc_kernel<Ti, To, 1><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+                xt, yt, mode, n, h, w, c, oh, ow, sy, sx);
+        }
+    } else {
+        long long work = (long long)n * c * oh * ow;
+        resize_nchw_kernel<Ti, To><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+            xt, yt, mode, n * c, h, w, oh, ow, sy, sx);
+    }
+    return cudaGetLastError();
+}
+
+template <typename To>
+cudaError_t resize_from(int in_dtype, int mode, int n, int c, int h, int w, int oh, int ow,
+                        int layout, const void* x, void* y, cudaStream_t s) {
+    switch (in_dtype) {
+    case ACNN_F32: return resize_typed<float, To>(mode, n, c, h, w, oh, ow, layout, x, y, s);
+    case ACNN_F16: return resize_typed<__half, To>(mode, n, c, h, w, oh, ow, layout, x, y, s);
+    default: return resize_typed<__nv_bfloat16, To>(mode, n, c, h, w, oh, ow, layout, x, y, s);
+    }
+}
+
+template <typename T>
+cudaError_t concat_typed(int n, int h, int w, int ca, int cb, int layout, const void* a,
+                         const void* b, void* y, cudaStream_t s) {
+    long long runs;
+    long long ra, rb;
+    if (layout == ACNN_NHWC) {
+        runs = (long long)n * h * w;
+        ra = ca;
+        rb = cb;
+    } else {
+        runs = n;
+        ra = (long long)ca * h * w;
+        rb = (long long)cb * h * w;
+    }
+    constexpr int V = 16 / sizeof(T);
+    const T* at = static_cast<const T*>(a);
+    const T* bt = static_cast<const T*>(b);
+    T* yt = static_cast<T*>(y);
+    if (ra % V == 0 && rb % V == 0) {
+        long long work = runs * ((ra + rb) / V);
+        concat_kernel<T, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(at, bt, yt, runs,
+                                                                          (int)ra, (int)rb);
+    } else {
+        long long work = runs * (ra + rb);
+        concat_kernel<T, 1><<<grid_for(work, kThreads), kThreads, 0, s>>>(at, bt, yt, runs,
+                                                                          (int)ra, (int)rb);
+    }
+    return cudaGetLastError();
+}
+
+template <typename Ti, typename To>
+cudaError_t deconv_typed(const acnn_conv_desc& d, int oh, int ow, const void* x, const float* w,
+                         const float* bias, const float* alpha, int act, void* y,
+                         cudaStream_t s) {
+    long long work = (long long)d.n * oh * ow *
+                     ((d.c_out + kDeconvCoBlock - 1) / kDeconvCoBlock);
+    deconv_kernel<Ti, To><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+        static_cast<const Ti*>(x), w, bias, alpha, static_cast<To*>(y), d.layout, d.n, d.c_in,
+        d.c_out, d.h, d.w, oh, ow, d.kh, d.stride, d.pad, act);
+    return cudaGetLastError();
+}
+
+template <typename Ti>
+cudaError_t deconv_from(int out_dtype, const acnn_conv_desc& d, int oh, int ow, const void* x,
+                        const float* w, const float* bias, const float* alpha, int act, void* y,
+                        cudaStream_t s) {
+    switch (out_dtype) {
+    case ACNN_F32: return deconv_typed<Ti, float>(d, oh, ow, x, w, bias, alpha, act, y, s);
+    case ACNN_F16: return deconv_typed<Ti, __half>(d, oh, ow, x, w, bias, alpha, act, y, s);
+    default: return deconv_typed<Ti, __nv_bfloat16>(d, oh, ow, x, w, bias, alpha, act, y, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pool2d(int kind, int n, int h, int w, int c, int k, int stride, int pad,
+                          int layout, int dtype, const void* x, void* y, cudaStream_t s) {
+    switch (dtype) {
+    case ACNN_F32: return pool_typed<float>(kind, n, h, w, c, k, stride, pad, layout, x, y, s);
+    case ACNN_F16: return pool_typed<__half>(kind, n, h, w, c, k, stride, pad, layout, x, y, s);
+    default: return pool_typed<__nv_bfloat16>(kind, n, h, w, c, k, stride, pad, layout, x, y, s);
+    }
+}
+
+cudaError_t launch_resize2d(int mode, int n, int c, int h, int w, int oh, int ow, int layout,
+                            int in_dtype, int out_dtype, const void* x, void* y, cudaStream_t s) {
+    switch (out_dtype) {
+    case ACNN_F32: return resize_from<float>(in_dtype, mode, n, c, h, w, oh, ow, layout, x, y, s);
+    case ACNN_F16: return resize_from<__half>(in_dtype, mode, n, c, h, w, oh, ow, layout, x, y, s);
+    default: return resize_from<__nv_bfloat16>(in_dtype, mode, n, c, h, w, oh, ow, layout, x, y, s);
+    }
+}
+
+cudaError_t launch_concat(int n, int h, int w, int ca, int cb, int layout, int dtype,
+                          const void* a, const void* b, void* y, cudaStream_t s) {
+    if (dtype == ACNN_F32) return concat_typed<float>(n, h, w, ca, cb, layout, a, b, y, s);
+    return concat_typed<uint16_t>(n, h, w, ca, cb, layout, a, b, y, s);  // 2-byte copy
+}
+
+cudaError_t launch_deconv2d(const acnn_conv_desc& d, int oh, int ow, const void* x,
+                            const float* w, const float* bias, const float* alpha, int act,
+                            int out_dtype, void* y, cudaStream_t s) {
+    switch (d.dtype) {
+    case ACNN_F32: return deconv_from<float>(out_dtype, d, oh, ow, x, w, bias, alpha, act, y, s);
+    case ACNN_F16: return deconv_from<__half>(out_dtype, d, oh, ow, x, w, bias, alpha, act, y, s);
+    default: return deconv_from<__nv_bfloat16>(out_dtype, d, oh, ow, x, w, bias, alpha, act, y, s);
+    }
+}
+
+cudaError_t launch_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_t* rgba1,
+                                float t, int out_dtype, void* y, cudaStream_t s) {
+    long long work = (long long)(h / 4) * (w / 4);
+    const uint32_t* f0 = reinterpret_cast<const uint32_t*>(rgba0);
+    const uint32_t* f1 = reinterpret_cast<const uint32_t*>(rgba1);
+    int g = grid_for(work, kThreads);
+    switch (out_dtype) {
+    case ACNN_F32:
+        prep_quarter_kernel<float><<<g, kThreads, 0, s>>>(f0, f1, static_cast<float*>(y), h, w, t);
+        break;
+    case ACNN_F16:
+        prep_quarter_kernel<__half><<<g, kThreads, 0, s>>>(f0, f1, static_cast<__half*>(y), h, w, t);
+        break;
+    default:
+        prep_quarter_kernel<__nv_bfloat16><<<g, kThreads, 0, s>>>(
+            f0, f1, static_cast<__nv_bfloat16*>(y), h, w, t);
+        break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_nchw_to_nhwc(int n, int c, int hw, int elem_bytes, const void* x, void* y,
+                                cudaStream_t s) {
+    if (elem_bytes != 2) return cudaErrorInvalidValue;
+    dim3 grid((hw + 31) / 32, (c + 31) / 32, n), block(32, 32);
+    transpose_kernel<<<grid, block, 0, s>>>(static_cast<const uint16_t*>(x),
+                                            static_cast<uint16_t*>(y), c, hw);
+    return cudaGetLastError();
+}
+
+}  // namespace acnn

@@ -1,0 +1,421 @@
+"""Layer graphs of the workloads, run through the C ABI and replayed as CUDA graphs.
+
+A ``Net`` is an ordered list of ops grouped into sections.  Each op is one
+ABI call on buffers allocated once (PyTorch supplies the device memory); a
+section is captured once into a CUDA graph with the ABI's section runner and
+replayed per step -- the GPU form of rtdetr_gpu.rs's Recorder (one submit per
+section) and rt.js's single command buffer per frame.
+
+Workloads (seeded, synthetic; the parameters come from
+activation_cnn_gb300.inputs by layer name):
+  conv1   one conv3x3/s1/p1 16->32 + ReLU, NHWC fp32, 1x32x32
+  stem    conv3x3/s2 3->32, conv3x3 32->32, conv3x3 32->64 (+ReLU each),
+          maxpool 3/2/1; NHWC fp32, 1x640x640x3
+  block   ResNet bottleneck at 4x80x80x256 bf16, identity variant and the
+          stride-2 downsample variant with an avgpool + 1x1 shortcut
+  frame   frame-interpolation stack, NCHW fp16, two 1920x1088 RGBA8 frames
+  backbone  ResNet-D-50 (3/4/6/3 bottlenecks) + top-down/bottom-up neck,
+          NHWC bf16, 8x640x640x3
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+from . import acnn as A
+from . import inputs as G
+
+TDT = G.TORCH_DTYPE
+
+
+@dataclass
+class ConvSpec:
+    name: str
+    c_in: int
+    c_out: int
+    k: int
+    stride: int
+    pad: int
+    act: int
+    h: int  # input height
+    w: int  # input width
+    res_mode: int = A.RES_NONE
+
+    @property
+    def oh(self):
+        return (self.h + 2 * self.pad - self.k) // self.stride + 1
+
+    @property
+    def ow(self):
+        return (self.w + 2 * self.pad - self.k) // self.stride + 1
+
+
+@dataclass
+class Op:
+    kind: str                # conv | pool | resize | concat | deconv | prep
+    section: str
+    fn: object = None        # callable(stream) issuing the ABI call(s)
+    flops: float = 0.0       # algorithmic FLOPs of one call
+    bytes: float = 0.0       # algorithmic bytes (inputs read once + output written once)
+    label: str = ""
+    spec: object = None
+
+
+@dataclass
+class Net:
+    name: str
+    batch: int
+    dtype: int
+    layout: int
+    ops: list = field(default_factory=list)
+    tensors: dict = field(default_factory=dict)
+    inputs: dict = field(default_factory=dict)   # name -> device tensor fed per step
+    outputs: list = field(default_factory=list)  # names of the output tensors
+    params: dict = field(default_factory=dict)   # name -> (cpu tensors) for reference checks
+    graphs: list = field(default_factory=list)   # [(section, Section)]
+    order: list = field(default_factory=list)    # section names in execution order
+    conv_inputs: dict = field(default_factory=dict)     # conv name -> input tensor name
+    conv_residuals: dict = field(default_factory=dict)  # conv name -> residual tensor name
+
+    # ------------------------------------------------------------ execution
+    def sections(self):
+        return list(self.order)
+
+    def run_eager(self, stream=None, section=None):
+        s = stream if stream is not None else torch.cuda.current_stream()
+        for op in self.ops:
+            if section is None or op.section == section:
+                op.fn(s)
+
+    def capture(self, stream):
+        """Record one CUDA graph per section on `stream` (ops must have run once)."""
+        self.release()
+        for sec in self.order:
+            g = A.Section(stream)
+            with torch.cuda.stream(stream):
+                with g:
+                    self.run_eager(stream, sec)
+            self.graphs.append((sec, g))
+
+    def replay(self, stream):
+        for _, g in self.graphs:
+            g.launch(stream)
+
+    def release(self):
+        for _, g in self.graphs:
+            g.close()
+        self.graphs = []
+
+    # ------------------------------------------------------------ accounting
+    def conv_flops(self):
+        return sum(op.flops for op in self.ops if op.kind == "conv")
+
+    def total_flops(self):
+        return sum(op.flops for op in self.ops)
+
+    def output_tensors(self):
+        return [self.tensors[n] for n in self.outputs]
+
+
+def _conv_flops(n, s: ConvSpec):
+    return 2.0 * n * s.oh * s.ow * s.c_out * s.c_in * s.k * s.k
+
+
+class Builder:
+    """Allocates buffers, draws parameters and appends ABI ops to a Net."""
+
+    def __init__(self, net: Net, seed: int, device="cuda"):
+        self.net = net
+        self.seed = seed
+        self.device = device
+        self.section = "main"
+        self.es = 4 if net.dtype == G.F32 else 2
+
+    def set_section(self, name):
+        self.section = name
+        if name not in self.net.order:
+            self.net.order.append(name)
+
+    def buffer(self, name, c, h, w, dtype=None, n=None):
+        n = self.net.batch if n is None else n
+        dt = TDT[self.net.dtype if dtype is None else dtype]
+        shape = G.activation_shape(self.net.layout, n, c, h, w)
+        t = torch.empty(shape, dtype=dt, device=self.device)
+        self.net.tensors[name] = t
+        return t
+
+    def conv(self, src, spec: ConvSpec, residual=None, out=None):
+        net = self.net
+        x = net.tensors[src]
+        w = G.conv_weight(self.seed, spec.name, spec.c_out, spec.c_in, spec.k, spec.k,
+                          net.layout, net.dtype)
+        b = G.conv_bias(self.seed, spec.name, spec.c_out)
+        al = G.prelu_alpha(self.seed, spec.name, spec.c_out) if spec.act == A.ACT_PRELU else None
+        net.params[spec.name] = (w, b, al)
+        wd, bd = w.to(self.device), b.to(self.device)
+        ald = al.to(self.device) if al is not None else None
+        y = self.buffer(out or spec.name, spec.c_out, spec.oh, spec.ow)
+        res = net.tensors[residual] if residual else None
+        d = A.conv_desc(x, spec.c_out, spec.k, spec.k, spec.stride, spec.pad, net.layout)
+        ws_bytes = A.acnn_conv2d_workspace_size(d)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device) if ws_bytes else None
+        net.tensors[spec.name + ".ws"] = ws
+        res_mode = spec.res_mode if residual else A.RES_NONE
+        net.conv_inputs[spec.name] = src
+        if residual:
+            net.conv_residuals[spec.name] = residual
+
+        def fn(stream, d=d, x=x, wd=wd, bd=bd, ald=ald, res=res, y=y, ws=ws, res_mode=res_mode):
+            A.check(A.acnn_conv2d_fused(d, x, wd, bd, ald, res, res_mode, spec.act, y, ws,
+                                        ws_bytes, stream), spec.name)
+
+        n = net.batch
+        byts = (x.numel() + w.numel() + y.numel() + (y.numel() if res is not None else 0)) * \
+            self.es + 4 * spec.c_out
+        net.ops.append(Op("conv", self.section, fn, _conv_flops(n, spec), byts, spec.name, spec))
+        return out or spec.name
+
+    def pool(self, src, dst, kind, k, s, p, c, h, w):
+        net = self.net
+        x = net.tensors[src]
+        oh, ow = (h + 2 * p - k) // s + 1, (w + 2 * p - k) // s + 1
+        y = self.buffer(dst, c, oh, ow)
+        n = net.batch
+
+        def fn(stream):
+            A.check(A.acnn_pool2d(kind, n, h, w, c, k, s, p, net.layout, net.dtype, x, y, stream),
+                    dst)
+
+        net.ops.append(Op("pool", self.section, fn, 0.0, (x.numel() + y.numel()) * self.es, dst))
+        return dst
+
+    def resize(self, src, dst, mode, c, h, w, oh, ow, out_dtype=None, touched_in=None):
+        net = self.net
+        x = net.tensors[src]
+        od = net.dtype if out_dtype is None else out_dtype
+        y = self.buffer(dst, c, oh, ow, dtype=od)
+        n = net.batch
+        in_dt = A.dtype_code(x.dtype)
+
+        def fn(stream):
+            A.check(A.acnn_resize2d(mode, n, c, h, w, oh, ow, net.layout, in_dt, od, x, y, stream),
+                    dst)
+
+        rd = touched_in if touched_in is not None else x.numel() * x.element_size()
+        net.ops.append(Op("resize", self.section, fn, 0.0, rd + y.numel() * y.element_size(), dst))
+        return dst
+
+    def concat(self, a, b, dst, ca, cb, h, w):
+        net = self.net
+        ta, tb = net.tensors[a], net.tensors[b]
+        y = self.buffer(dst, ca + cb, h, w)
+        n = net.batch
+
+        def fn(stream):
+            A.check(A.acnn_concat(n, h, w, ca, cb, net.layout, net.dtype, ta, tb, y, stream), dst)
+
+        net.ops.append(Op("concat", self.section, fn, 0.0, 2 * y.numel() * self.es, dst))
+        return dst
+
+
+# ============================================================== workloads
+def conv1_net(device="cuda") -> Net:
+    """Single conv3x3/s1/p1 16->32 + bias + ReLU, NHWC fp32, 1x32x32x16, x ~ U(-1, 1)."""
+    seed = 1234
+    net = Net("conv1", 1, G.F32, G.NHWC)
+    b = Builder(net, seed, device)
+    b.set_section("conv")
+    x = G.tensor(seed, "x", (1, 32, 32, 16), "uniform", -1.0, 1.0, dtype=G.F32)
+    net.tensors["x"] = x.to(device)
+    net.inputs["x"] = net.tensors["x"]
+    b.conv("x", ConvSpec("conv", 16, 32, 3, 1, 1, A.ACT_RELU, 32, 32))
+    net.outputs = ["conv"]
+    return net
+
+
+def stem_specs(h, w, prefix="stem"):
+    s0 = ConvSpec(f"{prefix}.0", 3, 32, 3, 2, 1, A.ACT_RELU, h, w)
+    s1 = ConvSpec(f"{prefix}.1", 32, 32, 3, 1, 1, A.ACT_RELU, s0.oh, s0.ow)
+    s2 = ConvSpec(f"{prefix}.2", 32, 64, 3, 1, 1, A.ACT_RELU, s1.oh, s1.ow)
+    return [s0, s1, s2]
+
+
+def _stem(b: Builder, src, h, w):
+    specs = stem_specs(h, w)
+    cur = src
+    for s in specs:
+        cur = b.conv(cur, s)
+    s2 = specs[-1]
+    return b.pool(cur, "stem.pool", A.POOL_MAX, 3, 2, 1, 64, s2.oh, s2.ow), \
+        (s2.oh + 2 - 3) // 2 + 1, (s2.ow + 2 - 3) // 2 + 1
+
+
+def stem_net(device="cuda", n=1, h=640, w=640) -> Net:
+    """ResNet-D stem, NHWC fp32: 3 convs (+ReLU) then maxpool 3/2/1; x ~ U(0, 1)."""
+    seed = 1235
+    net = Net("stem", n, G.F32, G.NHWC)
+    b = Builder(net, seed, device)
+    b.set_section("stem")
+    x = G.tensor(seed, "x", (n, h, w, 3), "uniform", 0.0, 1.0, dtype=G.F32)
+    net.tensors["x"] = x.to(device)
+    net.inputs["x"] = net.tensors["x"]
+    out, _, _ = _stem(b, "x", h, w)
+    net.outputs = [out]
+    return net
+
+
+def bottleneck(b: Builder, src, name, c_in, width, h, w, stride, shortcut):
+    """ResNet-D bottleneck: 1x1 -> 3x3 (stride here) -> 1x1, shortcut, add, ReLU.
+
+    shortcut: 'identity', 'conv' (1x1, stride 1) or 'pool' (avgpool 2x2/s2 then 1x1).
+    The add and the ReLU run in the last conv's epilogue (residual before act).
+    """
+    mid = width // 4
+    c1 = ConvSpec(f"{name}.conv1", c_in, mid, 1, 1, 0, A.ACT_RELU, h, w)
+    c2 = ConvSpec(f"{name}.conv2", mid, mid, 3, stride, 1, A.ACT_RELU, h, w)
+    c3 = ConvSpec(f"{name}.conv3", mid, width, 1, 1, 0, A.ACT_RELU, c2.oh, c2.ow,
+                  res_mode=A.RES_ADD_THEN_ACT)
+    if shortcut == "identity":
+        res = src
+    elif shortcut == "conv":
+        res = b.conv(src, ConvSpec(f"{name}.short", c_in, width, 1, 1, 0, A.ACT_NONE, h, w))
+    else:
+        pooled = b.pool(src, f"{name}.pool", A.POOL_AVG, 2, 2, 0, c_in, h, w)
+        res = b.conv(pooled, ConvSpec(f"{name}.short", c_in, width, 1, 1, 0, A.ACT_NONE,
+                                      h // 2, w // 2))
+    t = b.conv(src, c1)
+    t = b.conv(t, c2)
+    out = b.conv(t, c3, residual=res)
+    return out, c2.oh, c2.ow
+
+
+def block_net(device="cuda", variant="identity", n=4, h=80, w=80) -> Net:
+    """Bottleneck at 4x80x80x256, NHWC bf16, x ~ N(0, 1): identity or downsample variant."""
+    seed = 1236
+    net = Net(f"block_{variant}", n, G.BF16, G.NHWC)
+    b = Builder(net, seed, device)
+    b.set_section(variant)
+    x = G.tensor(seed, "x", (n, h, w, 256), "normal", dtype=G.BF16)
+    net.tensors["x"] = x.to(device)
+    net.inputs["x"] = net.tensors["x"]
+    if variant == "identity":
+        out, _, _ = bottleneck(b, "x", "id", 256, 256, h, w, 1, "identity")
+    else:
+        out, _, _ = bottleneck(b, "x", "down", 256, 512, h, w, 2, "pool")
+    net.outputs = [out]
+    return net
+
+
+STAGES = [(3, 256, 1, "conv"), (4, 512, 2, "pool"), (6, 1024, 2, "pool"), (3, 2048, 2, "pool")]
+
+
+def backbone_net(device="cuda", n=8, h=640, w=640) -> Net:
+    """ResNet-D-50 backbone + neck, NHWC bf16, N x 640 x 640 x 3, x ~ U(0, 1).
+
+    Neck (top-down then bottom-up, every conv + SiLU): lateral 1x1 convs to 256
+    on C3/C4/C5; F5 = lat5; F4 = conv3x3(cat[up2(F5), lat4]);
+    F3 = conv3x3(cat[up2(F4), lat3]); N4 = conv3x3(cat[conv3x3/s2(F3), F4]);
+    N5 = conv3x3(cat[conv3x3/s2(N4), F5]).  Outputs F3, N4, N5.
+    """
+    seed = 1238
+    net = Net("backbone", n, G.BF16, G.NHWC)
+    b = Builder(net, seed, device)
+    x = G.tensor(seed, "x", (n, h, w, 3), "uniform", 0.0, 1.0, dtype=G.BF16)
+    net.tensors["x"] = x.to(device)
+    net.inputs["x"] = net.tensors["x"]
+    b.set_section("stem")
+    cur, ch, cw = _stem(b, "x", h, w)
+    c_in = 64
+    feats = []
+    for si, (blocks, width, stride, first_short) in enumerate(STAGES):
+        b.set_section(f"stage{si + 1}")
+        for bi in range(blocks):
+            short = first_short if bi == 0 else "identity"
+            cur, ch, cw = bottleneck(b, cur, f"s{si + 1}.b{bi}", c_in, width, ch, cw,
+                                     stride if bi == 0 else 1, short)
+            c_in = width
+        feats.append((cur, ch, cw, width))
+    b.set_section("neck")
+    (c3, h3, w3, ch3), (c4, h4, w4, ch4), (c5, h5, w5, ch5) = feats[1], feats[2], feats[3]
+    S = A.ACT_SILU
+    lat3 = b.conv(c3, ConvSpec("neck.lat3", ch3, 256, 1, 1, 0, S, h3, w3))
+    lat4 = b.conv(c4, ConvSpec("neck.lat4", ch4, 256, 1, 1, 0, S, h4, w4))
+    f5 = b.conv(c5, ConvSpec("neck.lat5", ch5, 256, 1, 1, 0, S, h5, w5))
+    up5 = b.resize(f5, "neck.up5", A.RESIZE_NEAREST, 256, h5, w5, h4, w4)
+    cat4 = b.concat(up5, lat4, "neck.cat4", 256, 256, h4, w4)
+    f4 = b.conv(cat4, ConvSpec("neck.fpn4", 512, 256, 3, 1, 1, S, h4, w4))
+    up4 = b.resize(f4, "neck.up4", A.RESIZE_NEAREST, 256, h4, w4, h3, w3)
+    cat3 = b.concat(up4, lat3, "neck.cat3", 256, 256, h3, w3)
+    f3 = b.conv(cat3, ConvSpec("neck.fpn3", 512, 256, 3, 1, 1, S, h3, w3))
+    d3 = b.conv(f3, ConvSpec("neck.down3", 256, 256, 3, 2, 1, S, h3, w3))
+    catn4 = b.concat(d3, f4, "neck.catn4", 256, 256, h4, w4)
+    n4 = b.conv(catn4, ConvSpec("neck.pan4", 512, 256, 3, 1, 1, S, h4, w4))
+    d4 = b.conv(n4, ConvSpec("neck.down4", 256, 256, 3, 2, 1, S, h4, w4))
+    catn5 = b.concat(d4, f5, "neck.catn5", 256, 256, h5, w5)
+    n5 = b.conv(catn5, ConvSpec("neck.pan5", 512, 256, 3, 1, 1, S, h5, w5))
+    net.outputs = [f3, n4, n5]
+    return net
+
+
+def frame_net(device="cuda", h=1088, w=1920, c1=120, c2=240, t=0.5) -> Net:
+    """Frame-interpolation conv stack, NCHW fp16 (rt.js run(), first 13 dispatches).
+
+    prep (bilinear 1/4 of both RGBA8 frames + t plane) -> conv3x3/s2 7->c1 + PReLU
+    -> conv3x3/s2 c1->c2 + PReLU -> 8 x conv3x3 c2->c2 + PReLU, the 8th adding the
+    map that entered the 8 (after its PReLU) -> deconv 4x4/s2 c2->5 -> bilinear x8.
+    """
+    seed = 1237
+    net = Net("frame", 1, G.F16, G.NCHW)
+    b = Builder(net, seed, device)
+    b.set_section("frame")
+    f0 = G.rgba_frame(seed, "frame0", h, w).to(device)
+    f1 = G.rgba_frame(seed, "frame1", h, w).to(device)
+    net.tensors["frame0"], net.tensors["frame1"] = f0, f1
+    net.inputs["frame0"], net.inputs["frame1"] = f0, f1
+    qh, qw = h // 4, w // 4
+    xq = b.buffer("xq", 7, qh, qw)
+
+    def prep(stream):
+        A.check(A.acnn_frame_prep_quarter(h, w, f0, f1, t, G.F16, xq, stream), "prep")
+
+    touched = 2 * (2 * qh) * w * 4  # two source rows per output row, both frames
+    net.ops.append(Op("prep", "frame", prep, 0.0, touched + xq.numel() * 2, "prep"))
+    P = A.ACT_PRELU
+    a = b.conv("xq", ConvSpec("conv0a", 7, c1, 3, 2, 1, P, qh, qw))
+    s0 = ConvSpec("conv0b", c1, c2, 3, 2, 1, P, qh // 2, qw // 2)
+    cur = b.conv(a, s0)
+    skip = cur
+    hh, ww = s0.oh, s0.ow
+    for i in range(8):
+        last = i == 7
+        spec = ConvSpec(f"convblock.{i}", c2, c2, 3, 1, 1, P, hh, ww,
+                        res_mode=A.RES_ACT_THEN_ADD if last else A.RES_NONE)
+        cur = b.conv(cur, spec, residual=skip if last else None)
+    wdc = G.deconv_weight(seed, "lastconv", c2, 5, 4)
+    bdc = G.conv_bias(seed, "lastconv", 5)
+    net.params["lastconv"] = (wdc, bdc, None)
+    wdd, bdd = wdc.to(device), bdc.to(device)
+    xin = net.tensors[cur]
+    tmp8 = b.buffer("tmp8", 5, 2 * hh, 2 * ww)
+    dd = A.ConvDesc(1, hh, ww, c2, 5, 4, 4, 2, 1, G.NCHW, G.F16)
+
+    def deconv(stream):
+        A.check(A.acnn_deconv2d(dd, xin, wdd, bdd, None, A.ACT_NONE, G.F16, tmp8, stream),
+                "deconv")
+
+    net.ops.append(Op("deconv", "frame", deconv, 2.0 * 5 * c2 * 4 * (2 * hh) * (2 * ww),
+                      (xin.numel() + tmp8.numel()) * 2 + wdc.numel() * 4, "deconv"))
+    b.resize("tmp8", "flow", A.RESIZE_BILINEAR, 5, 2 * hh, 2 * ww, h, w)
+    net.outputs = ["flow"]
+    return net
+
+
+WORKLOADS = {
+    "conv1": conv1_net,
+    "stem": stem_net,
+    "block": lambda device="cuda": block_net(device, "identity"),
+    "block_down": lambda device="cuda": block_net(device, "downsample"),
+    "frame": frame_net,
+    "backbone": backbone_net,
+}

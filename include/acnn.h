@@ -1,0 +1,209 @@
+/*
+ * acnn.h -- C ABI of the GB300 (sm_103a) fused 2-D convolution library.
+ *
+ * Every entry point takes plain pointers and sizes, enqueues its work on the
+ * caller's CUDA stream and returns an int status (ACNN_OK = 0).  Arguments are
+ * validated on the host before anything is launched; a rejected call launches
+ * nothing and returns an ACNN_ERR_* code.  No C++ exception crosses this ABI.
+ *
+ * Memory.  Every buffer is owned by the caller.  Pointers named "device" must
+ * be device (or managed) memory of the current device; pointers named "host"
+ * are host memory.  The library allocates no device memory on any call: the
+ * one call that needs scratch space takes a caller-provided workspace whose
+ * size acnn_conv2d_workspace_size() reports.  Outputs must not alias inputs.
+ *
+ * Asynchrony.  Calls return once the work is enqueued.  They neither
+ * synchronise nor allocate, so they may be recorded into a CUDA graph with
+ * stream capture (see the section runner at the end).
+ *
+ * Layouts.  Activations are NHWC (channels innermost, as in the inferencelayer
+ * rtdetr_gpu.rs page) or NCHW (planes, as in the @framecast/rt rt.js page),
+ * dense, with no padding between rows.  Conv weights are OHWI for NHWC
+ * activations -- so that the GEMM reduction index k runs over (ky, kx, ci), the
+ * order of rtdetr_gpu.rs IM2COL_SRC -- and OIHW for NCHW activations, the
+ * [CO, CI, 3, 3] order of rt.js wgslConv.  Bias and PReLU alpha are always
+ * fp32, as in rt.js wgslConv.
+ *
+ * Alignment.  Device pointers must be 16-byte aligned (the tensor path reads
+ * through TMA, which requires it); misaligned pointers return
+ * ACNN_ERR_MISALIGNED.
+ */
+#ifndef ACNN_H_
+#define ACNN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. NULL = legacy default stream. */
+typedef struct CUstream_st* acnn_stream_t;
+
+#define ACNN_VERSION 1
+
+/* ---- status codes -------------------------------------------------------- */
+enum {
+    ACNN_OK = 0,
+    ACNN_ERR_NULL_POINTER = 1,   /* a required pointer is NULL                   */
+    ACNN_ERR_BAD_GEOMETRY = 2,   /* a size is <= 0, or the output would be empty  */
+    ACNN_ERR_UNSUPPORTED = 3,    /* valid, but outside what this library covers   */
+    ACNN_ERR_MISALIGNED = 4,     /* a device pointer is not 16-byte aligned       */
+    ACNN_ERR_WORKSPACE = 5,      /* workspace NULL or smaller than required       */
+    ACNN_ERR_ALIAS = 6,          /* the output overlaps an input                  */
+    ACNN_ERR_BAD_ENUM = 7,       /* an enum argument is out of range              */
+    ACNN_ERR_CUDA = 8,           /* a CUDA runtime/driver call failed             */
+    ACNN_ERR_DEVICE_TIMEOUT = 9, /* a kernel's bounded pipeline wait expired      */
+    ACNN_ERR_TOO_LARGE = 10      /* an index would overflow 32 bits               */
+};
+
+/* ---- enums --------------------------------------------------------------- */
+typedef enum { ACNN_F32 = 0, ACNN_F16 = 1, ACNN_BF16 = 2 } acnn_dtype;
+typedef enum { ACNN_NHWC = 0, ACNN_NCHW = 1 } acnn_layout;
+/* Activations: relu(v) = max(v, 0) and silu(v) = v / (1 + exp(-v)) as in
+ * rtdetr_gpu.rs ADDACT_SRC; prelu(v) = v >= 0 ? v : alpha[c] * v as in rt.js
+ * wgslConv. */
+typedef enum { ACNN_ACT_NONE = 0, ACNN_ACT_RELU = 1, ACNN_ACT_SILU = 2, ACNN_ACT_PRELU = 3 } acnn_act;
+/* Residual: none; added before the activation, y = act(conv + res) (the
+ * bottleneck's addact(relu) in rtdetr_gpu.rs); or after it, y = act(conv) + res
+ * (rt.js wgslConv, dst = prelu(acc) + res). */
+typedef enum { ACNN_RES_NONE = 0, ACNN_RES_ADD_THEN_ACT = 1, ACNN_RES_ACT_THEN_ADD = 2 } acnn_res;
+typedef enum { ACNN_POOL_MAX = 0, ACNN_POOL_AVG = 1 } acnn_pool_kind;
+typedef enum { ACNN_RESIZE_NEAREST = 0, ACNN_RESIZE_BILINEAR = 1 } acnn_resize_mode;
+
+/* Geometry of one conv (or transposed conv) call.  n, h, w, c_in describe the
+ * input; c_out the output channels; kh x kw the kernel; stride and pad are
+ * the same along both axes.  dtype is the storage type of x, w, residual and
+ * y; accumulation is always fp32. */
+typedef struct {
+    int n, h, w, c_in, c_out;
+    int kh, kw, stride, pad;
+    int layout; /* acnn_layout */
+    int dtype;  /* acnn_dtype  */
+} acnn_conv_desc;
+
+/* ---- conv2d_fused ----------------------------------------------------------
+ * y[n,oy,ox,co] = post(b[co] + sum_{ky,kx,ci} x[n, oy*s+ky-p, ox*s+kx-p, ci]
+ *                                           * w[co,ky,kx,ci])
+ * Taps outside the input read zero (rtdetr_gpu.rs IM2COL_SRC); the output
+ * size is oh = (h + 2p - kh)/s + 1, ow likewise (rtdetr_gpu.rs RtDetrGpu::conv).
+ * post = act for ACNN_RES_NONE; act(v + res) for ADD_THEN_ACT; act(v) + res for
+ * ACT_THEN_ADD.  This is the conv of rtdetr_gpu.rs (im2col -> GEMM with the
+ * bias and activation in the epilogue) and of rt.js wgslConv (PReLU, residual).
+ *
+ *   d          geometry (host pointer, read during the call only)
+ *   x          device, input activations  [n,h,w,c_in] or [n,c_in,h,w]
+ *   w          device, weights OHWI [c_out,kh,kw,c_in] (NHWC) or OIHW (NCHW)
+ *   bias       device fp32 [c_out], or NULL for no bias
+ *   alpha      device fp32 [c_out]; required iff act == ACNN_ACT_PRELU
+ *   residual   device, same shape/layout/dtype as y; required iff res_mode != NONE
+ *   y          device output [n,oh,ow,c_out] or [n,c_out,oh,ow]
+ *   workspace  device scratch of at least acnn_conv2d_workspace_size(d) bytes
+ *              (NULL allowed when that size is 0); contents are clobbered
+ * The tensor-core path runs for fp16/bf16 with c_in % 8 == 0, c_out % 16 == 0
+ * and square kernels; every other valid geometry runs the direct FFMA kernel.
+ */
+int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w,
+                      const float* bias, const float* alpha, const void* residual,
+                      int res_mode, int act, void* y, void* workspace, size_t ws_bytes,
+                      acnn_stream_t stream);
+
+/* Output height and width of a conv with geometry d (host pointers). */
+int acnn_conv2d_out_hw(const acnn_conv_desc* d, int* oh, int* ow);
+
+/* Bytes of workspace acnn_conv2d_fused needs for geometry d (0 for NHWC). */
+size_t acnn_conv2d_workspace_size(const acnn_conv_desc* d);
+
+/* Which kernel acnn_conv2d_fused would run for d: 0 = direct FFMA,
+ * 1 = tcgen05 implicit GEMM with a tiled A load (1x1/s1/p0),
+ * 2 = tcgen05 implicit GEMM with TMA im2col A loads; negative = invalid. */
+int acnn_conv2d_path(const acnn_conv_desc* d);
+
+/* ---- pool2d ----------------------------------------------------------------
+ * MAX: y = max over the in-range taps of each k x k window at stride s, pad p
+ *      (taps outside the input are skipped: -inf padding), rtdetr_gpu.rs
+ *      MAXPOOL_SRC.  Bit-exact.
+ * AVG: y = (sum of the k x k window) * (1/k^2), pad must be 0 (the 2x2/s2
+ *      (a+b+c+d)*0.25 of rtdetr_gpu.rs AVGPOOL_SRC); accumulated in fp32.
+ * x, y: device, layout/dtype as given; y has oh = (h + 2p - k)/s + 1 rows.
+ */
+int acnn_pool2d(int kind, int n, int h, int w, int c, int k, int stride, int pad,
+                int layout, int dtype, const void* x, void* y, acnn_stream_t stream);
+
+/* ---- resize2d --------------------------------------------------------------
+ * NEAREST:  y[oy,ox] = x[floor(oy*h/oh), floor(ox*w/ow)]; the 2x case is
+ *           rtdetr_gpu.rs UPSAMPLE_SRC.  Bit-exact (in_dtype must equal out_dtype).
+ * BILINEAR: align_corners=false, src = (dst + 0.5)*(in/out) - 0.5, taps
+ *           clamped to the image (rt.js wgslPrepQuarter, wgslFlowOut).
+ * x: device [n,c,h,w]/[n,h,w,c] of in_dtype; y: device, oh x ow, out_dtype.
+ */
+int acnn_resize2d(int mode, int n, int c, int h, int w, int oh, int ow, int layout,
+                  int in_dtype, int out_dtype, const void* x, void* y, acnn_stream_t stream);
+
+/* ---- concat ----------------------------------------------------------------
+ * Channel concat y = [a | b] (rtdetr_gpu.rs CONCAT_SRC): per pixel for NHWC,
+ * per image plane block for NCHW.  a: device [.., c_a], b: device [.., c_b],
+ * y: device [.., c_a + c_b], all of dtype.  Bit-exact.
+ */
+int acnn_concat(int n, int h, int w, int c_a, int c_b, int layout, int dtype,
+                const void* a, const void* b, void* y, acnn_stream_t stream);
+
+/* ---- deconv2d --------------------------------------------------------------
+ * Transposed conv, rt.js wgslDeconv (gather form):
+ *   y[co,oy,ox] = b[co] + sum over (ky,kx) with ty = oy + p - ky >= 0, even,
+ *                 iy = ty/s < h (same along x) of sum_ci x[ci,iy,ix]*w[ci,co,ky,kx]
+ * then act.  Only kh = kw = 4, stride 2, pad 1 is supported (oh = 2h).
+ *   d      geometry; d->dtype is the type of x
+ *   x      device input, d->layout
+ *   w      device fp32 [c_in, c_out, 4, 4]   (fp32 as on the page)
+ *   bias   device fp32 [c_out] or NULL; alpha as for conv2d_fused
+ *   y      device output [n, c_out, 2h, 2w] (or NHWC) of out_dtype
+ */
+int acnn_deconv2d(const acnn_conv_desc* d, const void* x, const float* w, const float* bias,
+                  const float* alpha, int act, int out_dtype, void* y, acnn_stream_t stream);
+
+/* ---- frame prep ------------------------------------------------------------
+ * rt.js wgslPrepQuarter: two h x w RGBA8 frames (bytes R,G,B,A per pixel,
+ * device) -> y = [7, h/4, w/4] NCHW of out_dtype (device): the planes B, G, R
+ * of frame 0, then of frame 1, each a bilinear 1/4 downsample of byte/255,
+ * then a plane filled with t.  h and w must be multiples of 4.
+ */
+int acnn_frame_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_t* rgba1, float t,
+                            int out_dtype, void* y, acnn_stream_t stream);
+
+/* ---- status ------------------------------------------------------------------ */
+/* Static string for a status code. */
+const char* acnn_status_string(int status);
+
+/* Synchronises stream, then returns and clears the device status word that
+ * kernels set when a bounded pipeline wait expires (ACNN_OK if none did), or
+ * ACNN_ERR_CUDA if a CUDA error is pending. */
+int acnn_last_device_status(acnn_stream_t stream);
+
+/* Debug knob for fault tests: the spin budget (in polls) of every bounded
+ * device wait in later launches; 0 restores the default.  Host state only. */
+int acnn_set_wait_budget(long long polls);
+
+/* ---- section runner ---------------------------------------------------------
+ * One CUDA graph per network section, the GPU form of rtdetr_gpu.rs's
+ * Recorder (one submit per section) and rt.js's one command buffer per frame.
+ * acnn_section_begin starts stream capture on stream; the ABI calls that
+ * follow are recorded, not run; acnn_section_end ends the capture and returns
+ * an instantiated executable graph in *exec (host handle owned by the caller,
+ * released with acnn_section_destroy); acnn_section_launch replays it on a
+ * stream.  Buffers recorded into a graph must outlive it.
+ */
+int acnn_section_begin(acnn_stream_t stream);
+int acnn_section_end(acnn_stream_t stream, void** exec);
+int acnn_section_launch(void* exec, acnn_stream_t stream);
+int acnn_section_destroy(void* exec);
+
+/* Number of SMs of the current device (host query, cached). */
+int acnn_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ACNN_H_ */

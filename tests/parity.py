@@ -1,0 +1,57 @@
+"""Comparison helpers for the CUDA-vs-oracle parity tests.
+
+Tolerances are the ones the workloads fix:
+  fp32 storage:       relative L2 <= 1e-5 and max-abs <= 1e-4
+  fp16/bf16 storage:  relative L2 <= 2e-2 and cosine >= 0.9999
+plus an element-wise bound derived from the arithmetic, so that a localised
+error (one wrong channel, one wrong tap at an edge) cannot hide inside a
+norm: a stored fp16/bf16 result is the fp32 accumulation rounded once, so it
+lies within one unit in the last place of the fp64 value, i.e.
+|gpu - ref| <= 2^-(p-1) |ref| + 1e-3 * max|ref| (p = 8 for bf16, 11 for fp16;
+the absolute term covers fp32 accumulation error on cancelling sums).
+"""
+import numpy as np
+import torch
+
+REL_L2_F32, MAX_ABS_F32 = 1e-5, 1e-4
+REL_L2_LOW, COS_LOW = 2e-2, 0.9999
+SIG_BITS = {torch.bfloat16: 8, torch.float16: 11}
+
+
+def to64(t) -> np.ndarray:
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float64)
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def metrics(got, ref):
+    g, r = to64(got).ravel(), to64(ref).ravel()
+    d = g - r
+    nr = np.linalg.norm(r)
+    rel = np.linalg.norm(d) / nr if nr > 0 else np.linalg.norm(d)
+    cos = float(g @ r / (np.linalg.norm(g) * nr)) if nr > 0 and np.linalg.norm(g) > 0 else 1.0
+    return {"rel_l2": float(rel), "max_abs": float(np.abs(d).max(initial=0.0)), "cos": cos}
+
+
+def assert_parity(got, ref, dtype, what=""):
+    """`got` (GPU output, any torch dtype) against the fp64 oracle `ref`."""
+    g, r = to64(got), to64(ref)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite GPU output"
+    m = metrics(g, r)
+    if dtype == torch.float32:
+        assert m["rel_l2"] <= REL_L2_F32 and m["max_abs"] <= MAX_ABS_F32, (what, m)
+    else:
+        assert m["rel_l2"] <= REL_L2_LOW and m["cos"] >= COS_LOW, (what, m)
+        p = SIG_BITS[dtype]
+        bound = 2.0 ** (1 - p) * np.abs(r) + 1e-3 * np.abs(r).max(initial=0.0)
+        bad = np.abs(g - r) > bound
+        assert not bad.any(), (what, m, int(bad.sum()), np.argwhere(bad)[:5].tolist())
+    return m
+
+
+def assert_bitexact(got, ref, what=""):
+    g, r = to64(got), to64(ref)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    bad = g != r
+    assert not bad.any(), (what, int(bad.sum()), np.argwhere(bad)[:5].tolist())

@@ -1,0 +1,176 @@
+"""The workloads end to end, CUDA graphs vs the fp64 oracle.
+
+* conv1, stem, block (both variants): full size, end to end against the
+  oracle forward pass with storage emulation (every stored map rounded).
+* frame, backbone: end to end at a reduced spatial size the oracle finishes in
+  seconds, and at full size (the launch configuration bench.py times) layer by
+  layer, teacher-forced: each conv's oracle is fed the GPU's stored input and
+  compared on sampled output pixels (all channels); the memory-bound ops are
+  compared on whole maps.
+"""
+import numpy as np
+import pytest
+import torch
+
+from activation_cnn_gb300 import acnn as A
+from activation_cnn_gb300 import inputs as G
+from activation_cnn_gb300 import network as N
+from oracle import models as M
+from oracle import oracle as O
+from tests.parity import assert_bitexact, assert_parity, metrics, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from activation_cnn_gb300 import build
+    build.build()
+    A.lib()
+    yield
+    torch.cuda.synchronize()
+    assert A.acnn_last_device_status() == 0
+
+
+def run_graph(net):
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        net.run_eager(s)
+    s.synchronize()
+    net.capture(s)
+    for t in net.output_tensors():
+        t.zero_()
+    torch.cuda.synchronize()
+    net.replay(s)
+    s.synchronize()
+    outs = [t.clone() for t in net.output_tensors()]
+    net.release()
+    return outs
+
+
+def assert_maps(outs, refs, dtype):
+    for i, (g, r) in enumerate(zip(outs, refs)):
+        m = metrics(g, r.reshape(g.shape))
+        print(f"map {i}: {m}")
+        if dtype == torch.float32:
+            assert m["rel_l2"] <= 1e-5 and m["max_abs"] <= 1e-4, (i, m)
+        else:
+            assert m["rel_l2"] <= 2e-2 and m["cos"] >= 0.9999, (i, m)
+
+
+def test_conv1_full():
+    net = N.conv1_net()
+    (y,) = run_graph(net)
+    ref = M.conv1(to64(net.inputs["x"]))
+    assert_maps([y], [ref], torch.float32)
+
+
+def test_stem_full():
+    net = N.stem_net()
+    (y,) = run_graph(net)
+    assert tuple(y.shape) == (1, 160, 160, 64)
+    ref = M.stem_f32(to64(net.inputs["x"]))
+    assert_maps([y], [ref], torch.float32)
+
+
+@pytest.mark.parametrize("variant", ["identity", "downsample"])
+def test_block_full(variant):
+    net = N.block_net(variant=variant)
+    (y,) = run_graph(net)
+    ref = M.block(to64(net.inputs["x"]), variant)
+    assert_maps([y], [ref], torch.bfloat16)
+
+
+def test_frame_reduced_end_to_end():
+    net = N.frame_net(h=128, w=192)
+    (y,) = run_graph(net)
+    ref = M.frame(net.inputs["frame0"].cpu().numpy(), net.inputs["frame1"].cpu().numpy())
+    assert_maps([y], [ref], torch.float16)
+
+
+def test_backbone_reduced_end_to_end():
+    net = N.backbone_net(n=1, h=128, w=160)
+    outs = run_graph(net)
+    refs = M.backbone(to64(net.inputs["x"]))
+    assert [tuple(o.shape) for o in outs] == [(1, 16, 20, 256), (1, 8, 10, 256), (1, 4, 5, 256)]
+    assert_maps(outs, refs, torch.bfloat16)
+
+
+# ------------------------------------------------------------------ full size, per layer
+def _sample_pixels(n, oh, ow, k, rng):
+    pts = {(0, 0, 0), (n - 1, oh - 1, ow - 1), (0, oh - 1, 0), (n - 1, 0, ow - 1)}
+    while len(pts) < k:
+        pts.add((int(rng.integers(n)), int(rng.integers(oh)), int(rng.integers(ow))))
+    return sorted(pts)
+
+
+def check_layers(net, samples=48):
+    rng = np.random.default_rng(0)
+    T = net.tensors
+    tdt = {G.F32: torch.float32, G.F16: torch.float16, G.BF16: torch.bfloat16}[net.dtype]
+    checked = 0
+    for op in net.ops:
+        if op.kind != "conv":
+            continue
+        s = op.spec
+        x_name = _input_of(net, op)
+        x = to64(T[x_name])
+        y = T[s.name]
+        w, b, al = net.params[s.name]
+        res = None
+        if s.res_mode != A.RES_NONE:
+            res = to64(T[_residual_of(net, op)])
+        pts = _sample_pixels(net.batch, s.oh, s.ow, samples, rng)
+        ref = O.conv2d_points(x, to64(w), to64(b), pts, stride=s.stride, pad=s.pad, act=s.act,
+                              alpha=None if al is None else to64(al), residual=res,
+                              res_mode=s.res_mode, layout=net.layout)
+        yg = to64(y)
+        if net.layout == G.NHWC:
+            got = np.stack([yg[n, oy, ox, :] for n, oy, ox in pts])
+        else:
+            got = np.stack([yg[n, :, oy, ox] for n, oy, ox in pts])
+        assert_parity(got, ref, tdt, s.name)
+        checked += 1
+    return checked
+
+
+def _input_of(net, op):
+    return net.conv_inputs[op.spec.name]
+
+
+def _residual_of(net, op):
+    return net.conv_residuals[op.spec.name]
+
+
+def test_backbone_full_size_layers():
+    """Every one of the 64 convs of the 8x640x640 workload, teacher-forced, sampled pixels."""
+    net = N.backbone_net()
+    outs = run_graph(net)
+    # the graph replay left every intermediate map in place: check each layer on it
+    assert check_layers(net) == 64
+    # the memory-bound ops on whole maps
+    T = net.tensors
+    assert_bitexact(T["stem.pool"], O.pool2d(to64(T["stem.2"]), O.MAX, 3, 2, 1), "maxpool")
+    assert_bitexact(T["neck.up5"], O.resize2d(to64(T["neck.lat5"]), O.NEAREST, 40, 40), "up5")
+    assert_bitexact(T["neck.cat3"], O.concat(to64(T["neck.up4"]), to64(T["neck.lat3"])), "cat3")
+    ap = T["s2.b0.pool"]
+    assert_parity(ap, O.pool2d(to64(T["s1.b2.conv3"]), O.AVG, 2, 2, 0), torch.bfloat16, "avgpool")
+    assert [tuple(o.shape) for o in outs] == [(8, 80, 80, 256), (8, 40, 40, 256), (8, 20, 20, 256)]
+
+
+def test_frame_full_size_layers():
+    net = N.frame_net()
+    (flow,) = run_graph(net)
+    assert tuple(flow.shape) == (1, 5, 1088, 1920)
+    assert check_layers(net, samples=32) == 10
+    T = net.tensors
+    f0, f1 = net.inputs["frame0"].cpu().numpy(), net.inputs["frame1"].cpu().numpy()
+    assert_parity(T["xq"], O.prep_quarter(f0, f1, 0.5)[None], torch.float16, "prep")
+    w, b, _ = net.params["lastconv"]
+    ref = O.deconv2d(to64(T["convblock.7"]), to64(w), to64(b))
+    assert_parity(T["tmp8"], ref, torch.float16, "deconv")
+    ref = O.resize2d(to64(T["tmp8"]), O.BILINEAR, 1088, 1920, layout=O.NCHW)
+    assert_parity(flow, ref, torch.float16, "bilinear x8")

@@ -1,0 +1,299 @@
+"""Parity of every ABI op (CUDA, through the C ABI) with the fp64 oracle.
+
+Sizes span several tiles with ragged tails; inputs are the seeded generators
+of activation_cnn_gb300.inputs.  Max-pool, nearest resize and concat must be
+bit-exact; integer-valued conv cases must be bit-exact too (every fp32 partial
+sum is exact, so the one rounding at the store is the oracle's rounding).
+"""
+import numpy as np
+import pytest
+import torch
+
+from activation_cnn_gb300 import acnn as A
+from activation_cnn_gb300 import inputs as G
+from oracle import oracle as O
+from tests.parity import assert_bitexact, assert_parity, to64
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": G.F32, "f16": G.F16, "bf16": G.BF16}
+TDT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+ODT = {"f32": O.F32, "f16": O.F16, "bf16": O.BF16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from activation_cnn_gb300 import build
+    build.build()
+    A.lib()
+    yield
+    torch.cuda.synchronize()
+    assert A.acnn_last_device_status() == 0
+
+
+def conv_case(name, n, h, w, cin, cout, k, s, p, dt, layout=G.NHWC, act=A.ACT_RELU,
+              res_mode=A.RES_NONE, bias=True, integer=False, kw=None):
+    kw = kw or k
+    seed = 11
+    xs = G.activation_shape(layout, n, cin, h, w)
+    if integer:
+        x = G.tensor(seed, name + ".x", xs, "int", -3, 3, dtype=DT[dt])
+        wshape = (cout, k, kw, cin) if layout == G.NHWC else (cout, cin, k, kw)
+        wt = G.tensor(seed, name + ".w", wshape, "int", -2, 2, dtype=DT[dt])
+        b = G.tensor(seed, name + ".b", (cout,), "int", -4, 4) if bias else None
+        al = torch.full((cout,), 0.25)
+    else:
+        x = G.tensor(seed, name + ".x", xs, "normal", dtype=DT[dt])
+        wt = G.conv_weight(seed, name, cout, cin, k, kw, layout, DT[dt])
+        b = G.conv_bias(seed, name, cout) if bias else None
+        al = G.prelu_alpha(seed, name, cout)
+    oh, ow = (h + 2 * p - k) // s + 1, (w + 2 * p - kw) // s + 1
+    ys = G.activation_shape(layout, n, cout, oh, ow)
+    r = G.tensor(seed, name + ".r", ys, "normal", dtype=DT[dt]) if res_mode else None
+    dev = lambda t: None if t is None else t.cuda()
+    y = A.conv2d_fused(dev(x), dev(wt), dev(b), stride=s, pad=p, act=act, alpha=dev(al),
+                       residual=dev(r), res_mode=res_mode, layout=layout)
+    torch.cuda.synchronize()
+    ref = O.conv2d(to64(x), to64(wt), None if b is None else to64(b), stride=s, pad=p, act=act,
+                   alpha=to64(al), residual=None if r is None else to64(r), res_mode=res_mode,
+                   layout=layout)
+    return y, ref
+
+
+# ---------------------------------------------------------------- tensor-core path
+TC_CASES = [
+    # name, n, h, w, cin, cout, k, s, p
+    ("1x1_tail", 2, 9, 11, 64, 64, 1, 1, 0),
+    ("1x1_wide", 1, 16, 20, 256, 256, 1, 1, 0),
+    ("1x1_cin128_cout512", 1, 12, 12, 128, 512, 1, 1, 0),
+    ("1x1_cin32", 3, 7, 9, 32, 64, 1, 1, 0),
+    ("1x1_cin8", 1, 10, 13, 8, 16, 1, 1, 0),
+    ("3x3_s1", 2, 13, 17, 64, 64, 3, 1, 1),
+    ("3x3_s2", 3, 15, 14, 64, 128, 3, 2, 1),
+    ("3x3_s2_even", 2, 16, 16, 128, 128, 3, 2, 1),
+    ("3x3_cout240", 1, 11, 19, 128, 240, 3, 1, 1),
+    ("3x3_cin32", 2, 12, 12, 32, 32, 3, 1, 1),
+    ("3x3_cin96", 1, 9, 9, 96, 48, 3, 1, 1),
+    ("3x3_p0", 1, 10, 12, 64, 64, 3, 1, 0),
+    ("5x5_s1", 1, 11, 10, 64, 64, 5, 1, 2),
+    ("7x7_s2", 2, 19, 21, 16, 64, 7, 2, 3),
+    ("1x1_s2", 2, 9, 10, 64, 64, 1, 2, 0),
+    ("3x3_big_m", 2, 40, 41, 64, 64, 3, 1, 1),
+]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("case", TC_CASES, ids=[c[0] for c in TC_CASES])
+def test_conv_tensor_path(case, dt):
+    name, n, h, w, cin, cout, k, s, p = case
+    d = A.ConvDesc(n, h, w, cin, cout, k, k, s, p, G.NHWC, DT[dt])
+    assert A.acnn_conv2d_path(d) in (1, 2)
+    y, ref = conv_case(name, n, h, w, cin, cout, k, s, p, dt)
+    assert_parity(y, ref, TDT[dt], name)
+
+
+@pytest.mark.parametrize("act", [A.ACT_NONE, A.ACT_RELU, A.ACT_SILU, A.ACT_PRELU])
+@pytest.mark.parametrize("res_mode", [A.RES_NONE, A.RES_ADD_THEN_ACT, A.RES_ACT_THEN_ADD])
+def test_conv_tensor_epilogue_modes(act, res_mode):
+    y, ref = conv_case(f"epi{act}{res_mode}", 2, 10, 14, 64, 128, 3, 1, 1, "bf16", act=act,
+                       res_mode=res_mode)
+    assert_parity(y, ref, torch.bfloat16, f"act{act} res{res_mode}")
+
+
+def test_conv_tensor_no_bias():
+    y, ref = conv_case("nobias", 1, 9, 9, 64, 64, 1, 1, 0, "f16", bias=False)
+    assert_parity(y, ref, torch.float16)
+
+
+@pytest.mark.parametrize("k,s,p", [(1, 1, 0), (3, 1, 1), (3, 2, 1)])
+def test_conv_tensor_integer_bitexact(k, s, p):
+    """Integer data: fp32 sums are exact, so the bf16 store equals RNE of the oracle."""
+    y, ref = conv_case(f"int{k}{s}", 2, 11, 13, 64, 64, k, s, p, "bf16", act=A.ACT_PRELU,
+                       integer=True)
+    assert_bitexact(y, O.round_storage(ref, O.BF16), f"int k{k} s{s}")
+
+
+@pytest.mark.parametrize("act,res_mode", [(A.ACT_PRELU, A.RES_ACT_THEN_ADD),
+                                          (A.ACT_RELU, A.RES_ADD_THEN_ACT),
+                                          (A.ACT_NONE, A.RES_NONE)])
+@pytest.mark.parametrize("shape", [(1, 17, 30, 120, 240, 2), (1, 9, 15, 240, 240, 1),
+                                   (2, 8, 8, 64, 32, 1)])
+def test_conv_tensor_nchw(shape, act, res_mode):
+    """NCHW fp16 on the tensor path (workspace transpose + NCHW-writing epilogue)."""
+    n, h, w, cin, cout, s = shape
+    d = A.ConvDesc(n, h, w, cin, cout, 3, 3, s, 1, G.NCHW, G.F16)
+    assert A.acnn_conv2d_path(d) == 2 and A.acnn_conv2d_workspace_size(d) > 0
+    y, ref = conv_case(f"nchw{shape}", n, h, w, cin, cout, 3, s, 1, "f16", layout=G.NCHW,
+                       act=act, res_mode=res_mode)
+    assert_parity(y, ref, torch.float16, f"nchw {shape}")
+
+
+def test_conv_tensor_repeat_is_deterministic():
+    name = "repeat"
+    x = G.tensor(1, name + ".x", (2, 20, 20, 64), "normal", dtype=G.BF16).cuda()
+    wt = G.conv_weight(1, name, 128, 64, 3, 3, G.NHWC, G.BF16).cuda()
+    a = A.conv2d_fused(x, wt, None, pad=1)
+    b = A.conv2d_fused(x, wt, None, pad=1)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------- direct path
+DIRECT_CASES = [
+    # name, n, h, w, cin, cout, k, s, p, dt, layout
+    ("cfg1_like", 1, 32, 32, 16, 32, 3, 1, 1, "f32", G.NHWC),
+    ("stem_s2_f32", 1, 37, 45, 3, 32, 3, 2, 1, "f32", G.NHWC),
+    ("stem_s2_bf16", 2, 33, 30, 3, 32, 3, 2, 1, "bf16", G.NHWC),
+    ("f32_32to64", 1, 21, 19, 32, 64, 3, 1, 1, "f32", G.NHWC),
+    ("prep7_nchw_f16", 1, 34, 60, 7, 120, 3, 2, 1, "f16", G.NCHW),
+    ("f32_nchw", 2, 15, 17, 5, 20, 3, 1, 1, "f32", G.NCHW),
+    ("f32_7x7", 1, 23, 18, 3, 40, 7, 2, 3, "f32", G.NHWC),
+    ("f32_1x1", 1, 10, 10, 12, 36, 1, 1, 0, "f32", G.NHWC),
+    ("f16_cout_odd", 1, 12, 12, 24, 30, 3, 1, 1, "f16", G.NHWC),
+    ("f32_5x5_s3", 1, 20, 26, 6, 33, 5, 3, 2, "f32", G.NHWC),
+]
+
+
+@pytest.mark.parametrize("case", DIRECT_CASES, ids=[c[0] for c in DIRECT_CASES])
+def test_conv_direct_path(case):
+    name, n, h, w, cin, cout, k, s, p, dt, layout = case
+    d = A.ConvDesc(n, h, w, cin, cout, k, k, s, p, layout, DT[dt])
+    assert A.acnn_conv2d_path(d) == 0
+    y, ref = conv_case(name, n, h, w, cin, cout, k, s, p, dt, layout=layout)
+    assert_parity(y, ref, TDT[dt], name)
+
+
+def test_conv_direct_nonsquare():
+    y, ref = conv_case("nonsq", 1, 12, 14, 4, 8, 1, 1, 0, "f32", kw=3)
+    assert_parity(y, ref, torch.float32)
+
+
+@pytest.mark.parametrize("act", [A.ACT_SILU, A.ACT_PRELU])
+@pytest.mark.parametrize("res_mode", [A.RES_ADD_THEN_ACT, A.RES_ACT_THEN_ADD])
+def test_conv_direct_epilogue_modes(act, res_mode):
+    y, ref = conv_case(f"depi{act}{res_mode}", 1, 20, 21, 8, 16, 3, 1, 1, "f32", act=act,
+                       res_mode=res_mode)
+    assert_parity(y, ref, torch.float32)
+
+
+def test_conv_direct_integer_bitexact_f32():
+    y, ref = conv_case("dint", 2, 19, 23, 16, 32, 3, 1, 1, "f32", act=A.ACT_PRELU, integer=True)
+    assert_bitexact(y, ref)
+
+
+# ---------------------------------------------------------------- pools
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("layout", [G.NHWC, G.NCHW])
+@pytest.mark.parametrize("shape", [(2, 17, 23, 64), (1, 8, 8, 3), (3, 1, 1, 16), (1, 2, 5, 24)])
+def test_maxpool_bitexact(dt, layout, shape):
+    n, h, w, c = shape
+    x = G.tensor(3, f"mp{shape}", G.activation_shape(layout, n, c, h, w), "normal", dtype=DT[dt])
+    y = A.pool2d(x.cuda(), A.POOL_MAX, 3, 2, 1, layout=layout)
+    torch.cuda.synchronize()
+    assert_bitexact(y, O.pool2d(to64(x), O.MAX, 3, 2, 1, layout=layout), f"{dt} {shape}")
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("layout", [G.NHWC, G.NCHW])
+@pytest.mark.parametrize("shape", [(2, 16, 22, 64), (1, 8, 6, 5)])
+def test_avgpool(dt, layout, shape):
+    n, h, w, c = shape
+    x = G.tensor(4, f"ap{shape}", G.activation_shape(layout, n, c, h, w), "normal", dtype=DT[dt])
+    y = A.pool2d(x.cuda(), A.POOL_AVG, 2, 2, 0, layout=layout)
+    torch.cuda.synchronize()
+    assert_parity(y, O.pool2d(to64(x), O.AVG, 2, 2, 0, layout=layout), TDT[dt])
+
+
+def test_avgpool_integer_bitexact():
+    x = G.tensor(4, "api", (2, 10, 12, 16), "int", -8, 8, dtype=G.BF16)
+    y = A.pool2d(x.cuda(), A.POOL_AVG, 2, 2, 0)
+    torch.cuda.synchronize()
+    assert_bitexact(y, O.round_storage(O.pool2d(to64(x), O.AVG, 2, 2, 0), O.BF16))
+
+
+# ---------------------------------------------------------------- resize
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("layout", [G.NHWC, G.NCHW])
+@pytest.mark.parametrize("io", [((5, 7), (10, 14)), ((20, 20), (40, 40)), ((3, 5), (7, 11))])
+def test_nearest_bitexact(dt, layout, io):
+    (h, w), (oh, ow) = io
+    x = G.tensor(5, f"nn{io}", G.activation_shape(layout, 2, 24, h, w), "normal", dtype=DT[dt])
+    y = A.resize2d(x.cuda(), A.RESIZE_NEAREST, oh, ow, layout=layout)
+    torch.cuda.synchronize()
+    assert_bitexact(y, O.resize2d(to64(x), O.NEAREST, oh, ow, layout=layout))
+
+
+@pytest.mark.parametrize("dt_in,dt_out", [("f32", "f32"), ("f16", "f16"), ("bf16", "bf16"),
+                                          ("f16", "f32")])
+@pytest.mark.parametrize("layout", [G.NHWC, G.NCHW])
+@pytest.mark.parametrize("io", [((16, 24), (4, 6)), ((9, 15), (72, 120)), ((7, 9), (5, 13))])
+def test_bilinear(dt_in, dt_out, layout, io):
+    (h, w), (oh, ow) = io
+    x = G.tensor(6, f"bl{io}", G.activation_shape(layout, 2, 8, h, w), "normal", dtype=DT[dt_in])
+    y = A.resize2d(x.cuda(), A.RESIZE_BILINEAR, oh, ow, layout=layout, out_dtype=TDT[dt_out])
+    torch.cuda.synchronize()
+    assert_parity(y, O.resize2d(to64(x), O.BILINEAR, oh, ow, layout=layout), TDT[dt_out])
+
+
+# ---------------------------------------------------------------- concat
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("layout", [G.NHWC, G.NCHW])
+@pytest.mark.parametrize("cc", [(256, 256), (3, 5), (64, 8)])
+def test_concat_bitexact(dt, layout, cc):
+    ca, cb = cc
+    a = G.tensor(7, f"ca{cc}", G.activation_shape(layout, 2, ca, 9, 11), "normal", dtype=DT[dt])
+    b = G.tensor(7, f"cb{cc}", G.activation_shape(layout, 2, cb, 9, 11), "normal", dtype=DT[dt])
+    y = A.concat(a.cuda(), b.cuda(), layout=layout)
+    torch.cuda.synchronize()
+    assert_bitexact(y, O.concat(to64(a), to64(b), layout=layout))
+
+
+# ---------------------------------------------------------------- deconv
+@pytest.mark.parametrize("dt_in,dt_out", [("f16", "f16"), ("f32", "f32"), ("bf16", "f32")])
+@pytest.mark.parametrize("layout", [G.NCHW, G.NHWC])
+def test_deconv(dt_in, dt_out, layout):
+    n, ci, co, h, w = 2, 24, 5, 7, 9
+    x = G.tensor(8, "dcx", G.activation_shape(layout, n, ci, h, w), "normal", dtype=DT[dt_in])
+    wt = G.deconv_weight(8, "dc", ci, co, 4)
+    b = G.conv_bias(8, "dc", co)
+    y = A.deconv2d(x.cuda(), wt.cuda(), b.cuda(), layout=layout, out_dtype=TDT[dt_out])
+    torch.cuda.synchronize()
+    ref = O.deconv2d(to64(x), to64(wt), to64(b), layout=layout)
+    assert_parity(y, ref, TDT[dt_out])
+
+
+# ---------------------------------------------------------------- frame prep
+@pytest.mark.parametrize("hw", [(16, 24), (68, 120)])
+@pytest.mark.parametrize("dt", ["f16", "f32"])
+def test_frame_prep_quarter(hw, dt):
+    h, w = hw
+    f0 = G.rgba_frame(9, "f0", h, w)
+    f1 = G.rgba_frame(9, "f1", h, w)
+    y = A.frame_prep_quarter(f0.cuda(), f1.cuda(), 0.5, out_dtype=TDT[dt])
+    torch.cuda.synchronize()
+    assert_parity(y, O.prep_quarter(f0.numpy(), f1.numpy(), 0.5), TDT[dt])
+
+
+# ---------------------------------------------------------------- section runner
+def test_section_graph_replay_matches_eager():
+    x = G.tensor(10, "gx", (2, 12, 12, 64), "normal", dtype=G.BF16).cuda()
+    wt = G.conv_weight(10, "g", 64, 64, 3, 3, G.NHWC, G.BF16).cuda()
+    b = G.conv_bias(10, "g", 64).cuda()
+    eager = A.pool2d(A.conv2d_fused(x, wt, b, pad=1, act=A.ACT_RELU), A.POOL_MAX, 3, 2, 1)
+    s = torch.cuda.Stream()
+    y1 = torch.empty(2, 12, 12, 64, dtype=torch.bfloat16, device="cuda")
+    y2 = torch.empty(2, 6, 6, 64, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        sec = A.Section(s)
+        with sec:
+            A.conv2d_fused(x, wt, b, pad=1, act=A.ACT_RELU, out=y1, stream=s)
+            A.pool2d(y1, A.POOL_MAX, 3, 2, 1, out=y2, stream=s)
+        y2.zero_()
+        sec.launch()
+        sec.launch()
+    s.synchronize()
+    assert torch.equal(y2, eager)
+    sec.close()
