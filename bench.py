@@ -1,0 +1,399 @@
+"""Benchmark: backbone+neck images/s (and fused-conv TFLOP/s) on GB300.
+
+python bench.py [--gpus N --steps K --warmup W] [--workload backbone|block|...]
+               [--impl ours|reference] [--no-cpu-baseline]
+
+A step is one pass of the whole workload (every op of every section) over one
+batch of synthetic input already resident in HBM: the default workload is the
+ResNet-D-50 backbone + neck at 8 x 640 x 640 x 3, NHWC bf16.  Each step replays
+the workload's per-section CUDA graphs; L2 is flushed (a 512 MB write) before
+every step, outside the timed interval.  Under torchrun each rank runs its own
+batch (weak scaling, replicas: no data-path collective); the reported time is
+the max over ranks.
+
+Printed: ONE JSON line on rank 0 with value (img/s), the fused-conv TFLOP/s,
+a roofline object for the dominant kernel (the tcgen05 implicit-GEMM conv,
+per-launch times from CUDA events recorded inside the graphs), an
+end-to-end figure through host buffers, the oracle timed on the host cores,
+the SM clocks sampled during the timed region and the kernel launch count.
+
+--impl reference times the fp64 CPU oracle on the same workload and metric
+(each step a bounded sample), rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("fused-conv TFLOP/s (% of GB300 BF16 dense peak); backbone img/s @640x640")
+L2_FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"bf16_burst": d.get("bf16_tflops"), "bf16_sustained": d.get("bf16_tflops_sustained"),
+                "hbm": d.get("hbm_gbs"), "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for name, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def build_net(name, device, batch=None):
+    from activation_cnn_gb300 import network as N
+    if name == "backbone":
+        return N.backbone_net(device, n=batch or 8)
+    if name == "block":
+        return N.block_net(device, "identity")
+    if name == "block_down":
+        return N.block_net(device, "downsample")
+    return N.WORKLOADS[name](device)
+
+
+def workload_config(name, net, world):
+    from activation_cnn_gb300 import inputs as G
+    base = {"workload": name, "batch_per_gpu": net.batch, "global_batch": net.batch * world,
+            "dtype": {G.F32: "f32", G.F16: "f16", G.BF16: "bf16"}[net.dtype],
+            "layout": "NHWC" if net.layout == G.NHWC else "NCHW",
+            "parallelism": f"replicas x{world}", "l2": "flushed (512 MB write) before every step",
+            "graphs": "one CUDA graph per section: " + ",".join(net.order)}
+    if name == "backbone":
+        base.update({"image": "640x640x3", "model": "ResNet-D-50 (3/4/6/3) + top-down/bottom-up neck"})
+    return base
+
+
+def launches_per_step(net):
+    from activation_cnn_gb300 import acnn as A
+    n = 0
+    for op in net.ops:
+        if op.kind == "conv":
+            s = op.spec
+            d = A.ConvDesc(net.batch, s.h, s.w, s.c_in, s.c_out, s.k, s.k, s.stride, s.pad,
+                           net.layout, net.dtype)
+            n += 3 if (A.acnn_conv2d_workspace_size(d) > 0) else 1
+        else:
+            n += 1
+    return n
+
+
+def time_roofline(net, stream, steps, flush):
+    """Per-launch device time of every conv, from external events inside the graphs."""
+    import torch
+    from activation_cnn_gb300 import acnn as A
+    conv_ops = [op for op in net.ops if op.kind == "conv"]
+    evs = {id(op): (torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True)) for op in conv_ops}
+    graphs = []
+    for sec in net.order:
+        g = A.Section(stream)
+        with torch.cuda.stream(stream):
+            with g:
+                for op in net.ops:
+                    if op.section != sec:
+                        continue
+                    if op.kind == "conv":
+                        evs[id(op)][0].record(stream)
+                    op.fn(stream)
+                    if op.kind == "conv":
+                        evs[id(op)][1].record(stream)
+        graphs.append(g)
+    per_op = {id(op): [] for op in conv_ops}
+    for _ in range(steps):
+        flush()
+        for g in graphs:
+            g.launch(stream)
+        stream.synchronize()
+        for op in conv_ops:
+            a, b = evs[id(op)]
+            per_op[id(op)].append(a.elapsed_time(b) * 1e-3)
+    for g in graphs:
+        g.close()
+    rows = []
+    for op in conv_ops:
+        s = op.spec
+        d = A.ConvDesc(net.batch, s.h, s.w, s.c_in, s.c_out, s.k, s.k, s.stride, s.pad,
+                       net.layout, net.dtype)
+        rows.append({"name": op.label, "path": A.acnn_conv2d_path(d), "flops": op.flops,
+                     "bytes": op.bytes, "s": statistics.mean(per_op[id(op)])})
+    return rows
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from activation_cnn_gb300 import acnn as A
+    from activation_cnn_gb300 import build as B
+    from activation_cnn_gb300 import replicas as R
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    B.build()
+    A.lib()
+    net = build_net(args.workload, dev, args.batch)
+    stream = torch.cuda.Stream(device=dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.add_(1)  # read + write of a buffer 4x the L2, on torch's stream
+        torch.cuda.current_stream().synchronize()
+
+    # one eager pass (checks every call), then one CUDA graph per section
+    with torch.cuda.stream(stream):
+        net.run_eager(stream)
+    stream.synchronize()
+    st = A.acnn_last_device_status(stream.cuda_stream)
+    if st != 0:
+        raise RuntimeError(f"device status after eager pass: {A.status_string(st)}")
+    net.capture(stream)
+    for _ in range(max(args.warmup, 3)):
+        net.replay(stream)
+    stream.synchronize()
+
+    # ------------------------------------------------ timed region (device time)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    R.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush()
+        starts[i].record(stream)
+        net.replay(stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    R.barrier()
+    step_s = [a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends)]
+    total = sum(step_s)
+    total = R.max_over_ranks(total)
+    st = A.acnn_last_device_status(stream.cuda_stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed region: {A.status_string(st)}")
+
+    imgs = net.batch * world * args.steps
+    value = imgs / total
+    ms_per_step = 1e3 * total / args.steps
+    conv_tflops = net.conv_flops() * world * args.steps / total / 1e12
+
+    # ------------------------------------------------ roofline of the dominant kernel
+    rows = time_roofline(net, stream, max(3, min(args.steps, 10)), flush)
+    ig = [r for r in rows if r["path"] in (1, 2)]
+    ig_flops = sum(r["flops"] for r in ig)
+    ig_s = sum(r["s"] for r in ig)
+    pk = peaks()
+    achieved = ig_flops / ig_s / 1e12 if ig_s > 0 else 0.0
+    peak = pk["bf16_sustained"]
+    roofline = {"kernel": "igemm_conv_kernel (tcgen05 implicit-GEMM conv)",
+                "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4) if peak else None,
+                "peak_source": f"{pk['source']} bf16 sustained",
+                "traffic": None,
+                "launches_per_step": len(ig),
+                "flops_per_launch": ig_flops / max(1, len(ig)),
+                "avg_launch_us": 1e6 * ig_s / max(1, len(ig)),
+                "share_of_step": round(ig_s / (total / args.steps / 1), 4) if world == 1 else None}
+
+    # ------------------------------------------------ end to end through host buffers
+    e2e = None
+    if args.e2e:
+        in_names = list(net.inputs)
+        host_in = {k: net.inputs[k].detach().cpu().pin_memory() for k in in_names}
+        outs = net.output_tensors()
+        host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        bi = sum(t.numel() * t.element_size() for t in host_in.values())
+        bo = sum(t.numel() * t.element_size() for t in host_out)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for _ in range(args.steps):
+            flush()
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                for k in in_names:
+                    net.inputs[k].copy_(host_in[k], non_blocking=True)
+                net.replay(stream)
+                for o, h in zip(outs, host_out):
+                    h.copy_(o, non_blocking=True)
+            e1.record(stream)
+            stream.synchronize()
+            tot += e0.elapsed_time(e1) * 1e-3
+        tot = R.max_over_ranks(tot)
+        e2e = {"value": round(net.batch * world * args.steps / tot, 3), "unit": "img/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+    net.release()
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "img/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(net),
+        "data": "synthetic (seeded; He-normal weights, BN folded into bias)",
+        "config": workload_config(args.workload, net, world),
+        "conv_tflops": round(conv_tflops, 2),
+        "conv_frac_bf16_peak": round(conv_tflops / pk["bf16_sustained"], 4),
+        "conv_gflop_per_step": round(net.conv_flops() / 1e9, 2),
+        "roofline": roofline, "e2e": e2e,
+        "gpu_launches": launches_per_step(net) * args.steps,
+        "clocks": clk, "wall_s_timed": round(t_wall, 3),
+    }
+    if args.layers:
+        line["layers"] = [{k: (round(v, 9) if isinstance(v, float) else v) for k, v in r.items()}
+                          for r in rows]
+    return line
+
+
+def dtype_name(net):
+    from activation_cnn_gb300 import inputs as G
+    return {G.F32: "f32", G.F16: "f16", G.BF16: "bf16"}[net.dtype]
+
+
+# ---------------------------------------------------------------- oracle arms
+def oracle_sample(workload, kind):
+    """(callable, fraction of one step's images it covers, description)."""
+    import torch
+    from activation_cnn_gb300 import inputs as G
+    from oracle import models as M
+    from oracle import oracle as O
+    O.build()
+    if workload != "backbone":
+        raise SystemExit("the oracle baseline is implemented for the backbone workload")
+    # cpu_baseline: one full 640x640 image (1/8 of a step); reference steps: a 160x160
+    # image, i.e. 1/16 of one image's conv work (every op scales with the pixel count)
+    side = 640 if kind == "baseline" else 160
+    x = G.tensor(1238, "x", (1, side, side, 3), "uniform", 0.0, 1.0, dtype=G.BF16)
+    x64 = x.to(torch.float64).numpy()
+    frac = (side * side) / (640 * 640)
+    desc = (f"oracle backbone+neck forward (fp64, bf16 storage emulation) on one "
+            f"{side}x{side}x3 image = {frac:g} of one image's work, {O.nthreads()} threads")
+    return (lambda: M.backbone(x64)), frac, desc
+
+
+def cpu_baseline(workload):
+    from oracle import oracle as O
+    fn, frac, desc = oracle_sample(workload, "baseline")
+    t0 = time.perf_counter()
+    fn()
+    dt = time.perf_counter() - t0
+    return {"value": round(frac / dt, 5), "unit": "img/s", "cores": O.nthreads(),
+            "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    from oracle import oracle as O
+    fn, frac, desc = oracle_sample(args.workload, "reference")
+    for _ in range(args.warmup):
+        fn()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fn()
+    dt = time.perf_counter() - t0
+    value = frac * args.steps / dt
+    return {"metric": METRIC, "value": round(value, 5), "unit": "img/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * dt / args.steps, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": args.workload, "image": "640x640x3",
+                       "sample_per_step": desc},
+            "cpu_baseline": {"value": round(value, 5), "unit": "img/s", "cores": O.nthreads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 5), "unit": "img/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="backbone",
+                    choices=["backbone", "block", "block_down", "stem", "conv1", "frame"])
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--layers", action="store_true", help="add per-conv timings")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="backbone batch per GPU (default 8; smaller only for profiler captures)")
+    args = ap.parse_args()
+
+    from activation_cnn_gb300 import replicas as R
+    rank, world, local_rank = R.env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if args.cpu_baseline and args.workload == "backbone":
+            line["cpu_baseline"] = cpu_baseline(args.workload)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad arguments on the host before any CUDA call."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def A():
+    from activation_cnn_gb300 import build
+    build.build()
+    from activation_cnn_gb300 import acnn
+    acnn.lib()
+    return acnn
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "acnn.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(acnn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_names():
+    from activation_cnn_gb300 import acnn
+    assert sorted(acnn.EXPORTS) == declared_symbols()
+
+
+def test_library_exports_every_declared_symbol(A):
+    lib = A.lib()
+    missing = [s for s in declared_symbols() if not hasattr(lib, s)]
+    assert not missing, missing
+
+
+def test_status_strings(A):
+    for code in range(11):
+        assert A.status_string(code) and A.status_string(code) != "unknown status"
+    assert A.status_string(999) == "unknown status"
+
+
+def desc(A, **kw):
+    d = dict(n=1, h=8, w=8, c_in=16, c_out=32, kh=3, kw=3, stride=1, pad=1, layout=0, dtype=2)
+    d.update(kw)
+    return A.ConvDesc(*[d[k] for k in ("n", "h", "w", "c_in", "c_out", "kh", "kw", "stride",
+                                       "pad", "layout", "dtype")])
+
+
+X, W, Y, R, B = 0x1000000, 0x2000000, 0x3000000, 0x4000000, 0x5000000  # never dereferenced
+
+
+def test_conv_rejects_before_launch(A):
+    c = A.acnn_conv2d_fused
+    d = desc(A)
+    assert c(d, None, W, None, None, None, 0, 0, Y, None, 0, 0) == 1          # NULL x
+    assert c(d, X, W, None, None, None, 0, A.ACT_PRELU, Y, None, 0, 0) == 1   # PReLU w/o alpha
+    assert c(d, X, W, None, None, None, 1, 0, Y, None, 0, 0) == 1             # residual missing
+    assert c(d, X, W, None, None, None, 0, 9, Y, None, 0, 0) == 7             # bad act
+    assert c(d, X, W, None, None, None, 5, 0, Y, None, 0, 0) == 7             # bad res mode
+    assert c(desc(A, dtype=5), X, W, None, None, None, 0, 0, Y, None, 0, 0) == 7
+    assert c(desc(A, layout=3), X, W, None, None, None, 0, 0, Y, None, 0, 0) == 7
+    assert c(desc(A, n=0), X, W, None, None, None, 0, 0, Y, None, 0, 0) == 2
+    assert c(desc(A, h=1, pad=0), X, W, None, None, None, 0, 0, Y, None, 0, 0) == 2
+    assert c(desc(A, stride=0), X, W, None, None, None, 0, 0, Y, None, 0, 0) == 2
+    assert c(d, X + 4, W, None, None, None, 0, 0, Y, None, 0, 0) == 4        # misaligned
+    assert c(d, X, W, B + 4, None, None, 0, 0, Y, None, 0, 0) == 4
+    assert c(d, X, W, None, None, None, 0, 0, X + 256, None, 0, 0) == 6      # y overlaps x
+    # NCHW on the tensor path needs its workspace
+    dn = desc(A, layout=1, c_in=64, c_out=64)
+    assert A.acnn_conv2d_workspace_size(dn) > 0
+    assert c(dn, X, W, None, None, None, 0, 0, Y, None, 0, 0) == 5
+
+
+def test_conv_path_selection(A):
+    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=64, kh=1, kw=1, pad=0)) == 1
+    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=64)) == 2
+    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=64, stride=2)) == 2
+    assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=32)) == 0         # tiny C_in
+    assert A.acnn_conv2d_path(desc(A, dtype=0)) == 0                  # fp32
+    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=120)) == 0       # C_out % 16
+    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=64, kw=1, pad=0)) == 0  # non-square
+    assert A.acnn_conv2d_path(desc(A, n=0)) == -1
+    assert A.acnn_conv2d_workspace_size(desc(A, c_in=64, c_out=64)) == 0
+
+
+def test_conv_out_hw(A):
+    st, oh, ow = A.acnn_conv2d_out_hw(desc(A, h=640, w=640, stride=2))
+    assert (st, oh, ow) == (0, 320, 320)
+    st, oh, ow = A.acnn_conv2d_out_hw(desc(A, h=7, w=9, kh=3, kw=3, stride=2, pad=1))
+    assert (st, oh, ow) == (0, 4, 5)
+
+
+def test_companions_reject_before_launch(A):
+    assert A.acnn_pool2d(2, 1, 8, 8, 4, 3, 2, 1, 0, 0, X, Y, 0) == 7           # bad kind
+    assert A.acnn_pool2d(1, 1, 8, 8, 4, 2, 2, 1, 0, 0, X, Y, 0) == 3           # avg with pad
+    assert A.acnn_pool2d(0, 1, 8, 8, 4, 3, 2, 3, 0, 0, X, Y, 0) == 3           # pad >= k
+    assert A.acnn_pool2d(0, 1, 8, 8, 4, 3, 2, 1, 0, 0, None, Y, 0) == 1
+    assert A.acnn_pool2d(0, 1, 8, 8, 4, 3, 2, 1, 0, 0, X, X + 16, 0) == 6
+    assert A.acnn_resize2d(0, 1, 4, 8, 8, 16, 16, 0, 2, 0, X, Y, 0) == 3       # nearest casts
+    assert A.acnn_resize2d(1, 1, 4, 8, 8, 0, 16, 0, 2, 2, X, Y, 0) == 2
+    assert A.acnn_resize2d(3, 1, 4, 8, 8, 4, 16, 0, 2, 2, X, Y, 0) == 7
+    assert A.acnn_concat(1, 4, 4, 8, 8, 0, 2, X, W, X + 32, 0) == 6
+    assert A.acnn_concat(1, 4, 4, 0, 8, 0, 2, X, W, Y, 0) == 2
+    d = desc(A, kh=3, kw=3, stride=2, pad=1)
+    assert A.acnn_deconv2d(d, X, W, None, None, 0, 1, Y, 0) == 3               # only 4/2/1
+    d4 = desc(A, kh=4, kw=4, stride=2, pad=1)
+    assert A.acnn_deconv2d(d4, X, W, None, None, 0, 7, Y, 0) == 7
+    assert A.acnn_frame_prep_quarter(10, 16, X, W, 0.5, 1, Y, 0) == 2          # h % 4
+    assert A.acnn_frame_prep_quarter(16, 16, X, None, 0.5, 1, Y, 0) == 1
+
+
+def test_wait_budget_knob(A):
+    assert A.acnn_set_wait_budget(-1) == 2
+    assert A.acnn_set_wait_budget(0) == 0
+
+
+def test_section_end_null(A):
+    assert A.lib().acnn_section_end(None, None) == 1
+    assert A.acnn_section_launch(None, 0) == 1
+    assert A.acnn_section_destroy(None) == 0
