@@ -62,6 +62,13 @@ static __device__ __noinline__ float epilogue_outlined(float v, int act, float a
     return epilogue(v, act, alpha, res_mode, r);
 }
 
+// epilogue() with the SiLU (the one activation that needs expf) kept out of
+// line: unrolled epilogues then carry one call instead of one expf each.
+__device__ __forceinline__ float epilogue_fast(float v, int act, float alpha, int res_mode, float r) {
+    if (act == ACNN_ACT_SILU) return epilogue_outlined(v, act, alpha, res_mode, r);
+    return epilogue(v, act, alpha, res_mode, r);
+}
+
 __device__ __forceinline__ int64_t act_index(int layout, int C, int H, int W, int n, int c,
                                              int y, int x) {
     if (layout == ACNN_NHWC) return (((int64_t)n * H + y) * W + x) * C + c;

@@ -134,19 +134,46 @@ __global__ void __launch_bounds__(kThreads) direct_conv_kernel(
     }
 
     // fused epilogue: bias -> act / residual -> storage type
+    const int cb = co0 + cg * kCoPerThread;  // first of this thread's 8 output channels
+    float bv[kCoPerThread], av[kCoPerThread];
+#pragma unroll
+    for (int c = 0; c < kCoPerThread; ++c) {
+        const bool in = cb + c < C_out;
+        bv[c] = (bias && in) ? bias[cb + c] : 0.0f;
+        av[c] = (act == ACNN_ACT_PRELU && in) ? alpha[cb + c] : 0.0f;
+    }
+    // NHWC with 8 | C_out: the 8 channels are one aligned vector in memory
+    const bool vec = out_layout == ACNN_NHWC && (C_out % kCoPerThread) == 0 && cb < C_out;
 #pragma unroll
     for (int j = 0; j < kPxPerThread; ++j) {
         const int oy = oy0 + ty0 + 4 * j, ox = ox0 + tx;
         if (oy >= OH || ox >= OW) continue;
+        if (vec) {
+            // 16-byte vectors (the only alignment the ABI guarantees): 1 for 2-byte
+            // types, 2 for fp32
+            constexpr int V = 16 / sizeof(T);
+            const long long oi = (((long long)n * OH + oy) * OW + ox) * C_out + cb;
+#pragma unroll
+            for (int h = 0; h < kCoPerThread; h += V) {
+                Vec<T, V> rv, ov;
+                if (res_mode != ACNN_RES_NONE) rv = *reinterpret_cast<const Vec<T, V>*>(res + oi + h);
+#pragma unroll
+                for (int c = 0; c < V; ++c) {
+                    const float r = res_mode != ACNN_RES_NONE ? to_f32(rv.v[c]) : 0.0f;
+                    ov.v[c] = from_f32<T>(
+                        epilogue_fast(bv[h + c] + acc[j][h + c], act, av[h + c], res_mode, r));
+                }
+                *reinterpret_cast<Vec<T, V>*>(y + oi + h) = ov;
+            }
+            continue;
+        }
 #pragma unroll
         for (int c = 0; c < kCoPerThread; ++c) {
-            const int co = co0 + cg * kCoPerThread + c;
+            const int co = cb + c;
             if (co >= C_out) continue;
             const long long oi = act_index(out_layout, C_out, OH, OW, n, co, oy, ox);
-            float v = (bias ? bias[co] : 0.0f) + acc[j][c];
             const float r = res_mode != ACNN_RES_NONE ? to_f32(res[oi]) : 0.0f;
-            const float al = act == ACNN_ACT_PRELU ? alpha[co] : 0.0f;
-            y[oi] = from_f32<T>(epilogue_outlined(v, act, al, res_mode, r));
+            y[oi] = from_f32<T>(epilogue_fast(bv[c] + acc[j][c], act, av[c], res_mode, r));
         }
     }
 }

@@ -39,14 +39,19 @@ constexpr int BM = 128;             // output pixels per tile (TMEM lanes)
 constexpr int BK = 64;              // channels per k-block: 64 x 2 B = one 128-B swizzle row
 constexpr int kThreads = 192;       // 6 warps
 constexpr uint32_t kABytes = BM * BK * 2;
-constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s per wait
-constexpr unsigned long long kDrainNs = 200000000ull;     // 0.2 s per drain wait
+constexpr long long kTimeoutCycles = 8000000000ll;  // ~4 s per wait at 2 GHz
+constexpr long long kDrainCycles = 400000000ll;     // ~0.2 s per drain wait
+
+constexpr uint32_t kStageBytes = 32 * 64;  // epilogue staging: 32 rows x 32 channels x 2 B
+constexpr uint32_t kEpiBytes = 4 /*warps*/ * 2 /*buffers*/ * kStageBytes;
 
 template <int BN> struct Cfg {
     static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
     static constexpr uint32_t kBBytes = BN * BK * 2;
     static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-    static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStages * (kABytes + kBBytes) + 256;
+    // ring + output staging + residual staging + barriers, plus alignment slack
+    static constexpr size_t kSmem =
+        1024 + kStages * (kABytes + kBBytes) + 2 * kEpiBytes + 256;
 };
 
 struct Params {
@@ -67,12 +72,6 @@ struct Params {
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -103,16 +102,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Slow path of a bounded wait for the phase of `bar` with parity `parity`.
 // Returns false if the CTA is aborting or this wait expired; on expiry it
 // records the timeout in the device status word and raises the abort flag.
+// Time is measured with the SM's cycle counter (cheap to read, unlike the
+// global timer); kTimeoutCycles is ~4 s at the maximum SM clock.
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag, long long budget,
                                              int* status) {
-    const uint64_t t0 = globaltimer();
+    long long t0 = -1;
     for (long long i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         bool expired = budget > 0 && i >= budget;
-        if ((i & 31) == 0) {
+        if ((i & 255) == 0) {
             if (*abort_flag) return false;
-            if (budget <= 0 && globaltimer() - t0 > kTimeoutNs) expired = true;
+            const long long now = clock64();
+            if (t0 < 0) t0 = now;
+            if (budget <= 0 && now - t0 > kTimeoutCycles) expired = true;
         }
         if (expired) {
             atomicCAS(status, 0, ACNN_ERR_DEVICE_TIMEOUT);
@@ -130,9 +133,9 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
 
 // Time-bounded wait used only while draining after an abort.
 __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer();
+    const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))
-        if (globaltimer() - t0 > kDrainNs) return;
+        if (clock64() - t0 > kDrainCycles) return;
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -164,6 +167,31 @@ __device__ __forceinline__ void tma_load_im2col(uint32_t dst, const CUtensorMap*
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c), "r"(w), "r"(h), "r"(n),
         "h"(off_w), "h"(off_h)
         : "memory");
+}
+
+// Tiled TMA store of a shared-memory box to global; tracked by bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0,
+                                             int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N committed store groups still read shared memory.
+template <int N> __device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until every committed store group has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Order this thread's generic-proxy shared-memory writes before async-proxy (TMA) reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
@@ -247,11 +275,34 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool bf16) {
 template <typename T> struct IsBf16 { static constexpr bool v = false; };
 template <> struct IsBf16<__nv_bfloat16> { static constexpr bool v = true; };
 
+// Two fp32 values -> two storage values (round to nearest even), lo at the lower address.
+template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+template <typename T> __device__ __forceinline__ void unpack2(uint32_t u, float& lo, float& hi);
+template <> __device__ __forceinline__ void unpack2<__nv_bfloat16>(uint32_t u, float& lo, float& hi) {
+    lo = __uint_as_float(u << 16);
+    hi = __uint_as_float(u & 0xffff0000u);
+}
+template <> __device__ __forceinline__ void unpack2<__half>(uint32_t u, float& lo, float& hi) {
+    __half2 h = *reinterpret_cast<__half2*>(&u);
+    lo = __low2float(h);
+    hi = __high2float(h);
+}
+
 // ---------------------------------------------------------------- the kernel
 template <int BN, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_conv_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                      const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+                      const __grid_constant__ CUtensorMap tmap_b,
+                      const __grid_constant__ CUtensorMap tmap_y,
+                      const __grid_constant__ CUtensorMap tmap_r, const Params p) {
     using C = Cfg<BN>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -259,9 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + S * kABytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * C::kBBytes);
-    // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    uint8_t* sO = sB + S * C::kBBytes;  // output staging, 1024-aligned (64-B swizzle atoms)
+    uint8_t* sR = sO + kEpiBytes;       // residual staging
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sR + kEpiBytes);
+    // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, residual[4][2]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 13);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -271,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+    auto res_bar = [&](int e, int b) { return bar0 + 8u * (2 * S + 5 + 2 * e + b); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -282,10 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
         }
         mbar_init(drain_bar, 1);
+        for (int i = 0; i < 8; ++i) mbar_init(res_bar(i >> 1, i & 1), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
+        if (p.out_layout == ACNN_NHWC) {
+            prefetch_tmap(&tmap_y);
+            if (p.res_mode != ACNN_RES_NONE) prefetch_tmap(&tmap_r);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
@@ -386,8 +445,124 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (p.out_layout == ACNN_NHWC) {
+        // ---------------------------------------------------- epilogue warps, NHWC
+        // Each warp owns 32 rows (its TMEM lane quarter) of the 128-row tile and
+        // walks the tile's channels 32 at a time: the residual box arrives by TMA
+        // one chunk ahead into a double buffer, the 32 x 32 result is written to a
+        // 64-byte-swizzled staging buffer and leaves by a TMA store (which also
+        // clips rows >= M and channels >= C_out).
+        const int q = warp & 3;
+        const int e = warp - 2;
+        uint8_t* ost = sO + e * 2 * kStageBytes;
+        uint8_t* rst = sR + e * 2 * kStageBytes;
+        const bool has_res = p.res_mode != ACNN_RES_NONE;
+        const bool prelu = p.act == ACNN_ACT_PRELU;
+        const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // 64-B swizzle of this lane's row
+        int acc = 0, ob = 0, rb = 0;
+        uint32_t acc_phase = 0, rpar = 0, r_inflight = 0;
+        bool aborted = false;
+        auto issue_res = [&](int buf, int c0, int r0) {
+            const uint32_t bar = res_bar(e, buf);
+            mbar_arrive_expect_tx(bar, kStageBytes);
+            tma_load_2d(smem_u32(rst + buf * kStageBytes), &tmap_r, bar, c0, r0);
+        };
+        for (int tile = blockIdx.x; !aborted && tile < num_tiles; tile += gridDim.x) {
+            const int m0 = (tile / p.num_n_tiles) * BM;
+            const int n0 = (tile % p.num_n_tiles) * BN;
+            const int row0 = m0 + q * 32;
+            const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
+            if (has_res) {
+                if (lane == 0) issue_res(rb, n0, row0);
+                r_inflight |= 1u << rb;
+            }
+            const bool ok = __all_sync(0xffffffffu, wait_phase(tfull_bar(acc), acc_phase, abort_flag, p));
+            if (!ok) break;
+            tc_fence_after();
+            for (int i = 0; i < nch; ++i) {
+                const int c = i * 32;
+                if (has_res && i + 1 < nch) {
+                    if (lane == 0) issue_res(rb ^ 1, n0 + c + 32, row0);
+                    r_inflight |= 1u << (rb ^ 1);
+                }
+                // bias / alpha of the chunk (same addresses in every lane: broadcast loads)
+                float bv[32], av[32];
+#pragma unroll
+                for (int g = 0; g < 32; g += 4) {
+                    const int co = n0 + c + g;
+                    float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f), a4 = b4;
+                    if (co < p.C_out) {  // C_out % 8 == 0: a float4 is all in or all out
+                        if (p.bias) b4 = __ldg(reinterpret_cast<const float4*>(p.bias + co));
+                        if (prelu) a4 = __ldg(reinterpret_cast<const float4*>(p.alpha + co));
+                    }
+                    bv[g] = b4.x; bv[g + 1] = b4.y; bv[g + 2] = b4.z; bv[g + 3] = b4.w;
+                    av[g] = a4.x; av[g + 1] = a4.y; av[g + 2] = a4.z; av[g + 3] = a4.w;
+                }
+                float v[32];
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), v);
+                float r[32];
+                if (has_res) {
+                    const bool okr = __all_sync(
+                        0xffffffffu, wait_phase(res_bar(e, rb), (rpar >> rb) & 1u, abort_flag, p));
+                    if (!okr) {
+                        aborted = true;
+                        break;
+                    }
+                    rpar ^= 1u << rb;
+                    r_inflight &= ~(1u << rb);
+                    const uint8_t* rrow = rst + rb * kStageBytes + lane * 64;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(rrow + ((j ^ swz) << 4));
+                        unpack2<T>(u.x, r[8 * j + 0], r[8 * j + 1]);
+                        unpack2<T>(u.y, r[8 * j + 2], r[8 * j + 3]);
+                        unpack2<T>(u.z, r[8 * j + 4], r[8 * j + 5]);
+                        unpack2<T>(u.w, r[8 * j + 6], r[8 * j + 7]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = 0.f;
+                }
+                uint32_t packed[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    packed[k] = pack2<T>(
+                        epilogue(v[2 * k] + bv[2 * k], p.act, av[2 * k], p.res_mode, r[2 * k]),
+                        epilogue(v[2 * k + 1] + bv[2 * k + 1], p.act, av[2 * k + 1], p.res_mode,
+                                 r[2 * k + 1]));
+                // the store that last used this staging buffer must have read it
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                uint8_t* orow = ost + ob * kStageBytes + lane * 64;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(orow + ((j ^ swz) << 4)) =
+                        make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                   packed[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmap_y, smem_u32(ost + ob * kStageBytes), n0 + c, row0);
+                    bulk_commit();
+                }
+                ob ^= 1;
+                if (has_res) rb ^= 1;
+            }
+            if (aborted) break;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (lane == 0) {
+            bulk_wait_all();  // every output box written before the CTA exits
+            for (int b = 0; b < 2; ++b)  // residual boxes still in flight after an abort
+                if (r_inflight & (1u << b)) wait_drain(res_bar(e, b), (rpar >> b) & 1u);
+        }
+        __syncwarp();
     } else {
-        // ---------------------------------------------------- epilogue warps
+        // ---------------------------------------------------- epilogue warps, NCHW
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
         const T* res = static_cast<const T*>(p.res);
@@ -490,9 +665,12 @@ bool load_encoders() {
     return ok;
 }
 
+struct Maps {
+    CUtensorMap a, b, y, r;
+};
+
 template <int BN, typename T>
-int launch_bn(const ConvArgs& a, const CUtensorMap& ta, const CUtensorMap& tb, Params prm,
-              cudaStream_t s) {
+int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     using C = Cfg<BN>;
     static bool attr_set = false;  // per instantiation; set once per process
     auto kern = igemm_conv_kernel<BN, T>;
@@ -505,16 +683,27 @@ int launch_bn(const ConvArgs& a, const CUtensorMap& ta, const CUtensorMap& tb, P
     prm.num_n_tiles = (a.d.c_out + BN - 1) / BN;
     const int tiles = prm.num_m_tiles * prm.num_n_tiles;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    kern<<<grid, kThreads, C::kSmem, s>>>(ta, tb, prm);
+    kern<<<grid, kThreads, C::kSmem, s>>>(m.a, m.b, m.y, m.r, prm);
     return cudaGetLastError() == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
 }
 
 template <typename T>
-int launch_typed(const ConvArgs& a, int bn, const CUtensorMap& ta, const CUtensorMap& tb,
-                 const Params& prm, cudaStream_t s) {
-    if (bn == 256) return launch_bn<256, T>(a, ta, tb, prm, s);
-    if (bn == 128) return launch_bn<128, T>(a, ta, tb, prm, s);
-    return launch_bn<64, T>(a, ta, tb, prm, s);
+int launch_typed(const ConvArgs& a, int bn, const Maps& m, const Params& prm, cudaStream_t s) {
+    if (bn == 256) return launch_bn<256, T>(a, m, prm, s);
+    if (bn == 128) return launch_bn<128, T>(a, m, prm, s);
+    return launch_bn<64, T>(a, m, prm, s);
+}
+
+// [M, C_out] NHWC output (or residual) viewed 2-D, 32 x 32 boxes, 64-byte swizzle.
+CUresult encode_out_map(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, int c_out,
+                        long long m) {
+    cuuint64_t dims[2] = {(cuuint64_t)c_out, (cuuint64_t)m};
+    cuuint64_t strides[1] = {(cuuint64_t)c_out * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode_tiled(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 // Output-channel tile: the widest of 256/128/64 that C_out fills, narrowed
@@ -537,7 +726,9 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
         d.dtype == ACNN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const bool tiled = d.kh == 1 && d.kw == 1 && d.stride == 1 && d.pad == 0;
 
-    alignas(64) CUtensorMap ta, tb;
+    alignas(64) Maps maps;
+    CUtensorMap& ta = maps.a;
+    CUtensorMap& tb = maps.b;
     CUresult r;
     if (tiled) {
         cuuint64_t dims[2] = {(cuuint64_t)d.c_in, (cuuint64_t)M};
@@ -573,6 +764,17 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
+    if (a.out_layout == ACNN_NHWC) {
+        if (encode_out_map(&maps.y, dt, a.y, d.c_out, M) != CUDA_SUCCESS) return ACNN_ERR_CUDA;
+        if (a.residual) {
+            if (encode_out_map(&maps.r, dt, a.residual, d.c_out, M) != CUDA_SUCCESS)
+                return ACNN_ERR_CUDA;
+        } else {
+            maps.r = maps.y;  // never read without a residual
+        }
+    } else {
+        maps.y = maps.r = maps.a;  // the NCHW epilogue stores with plain instructions
+    }
 
     Params prm{};
     prm.M = (int)M;
@@ -597,8 +799,8 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     prm.status = device_status_ptr();
     prm.budget = wait_budget_polls();
     if (!prm.status) return ACNN_ERR_CUDA;
-    if (d.dtype == ACNN_BF16) return launch_typed<__nv_bfloat16>(a, bn, ta, tb, prm, s);
-    return launch_typed<__half>(a, bn, ta, tb, prm, s);
+    if (d.dtype == ACNN_BF16) return launch_typed<__nv_bfloat16>(a, bn, maps, prm, s);
+    return launch_typed<__half>(a, bn, maps, prm, s);
 }
 
 }  // namespace acnn

@@ -134,13 +134,16 @@ def launches_per_step(net):
     return n
 
 
-def time_roofline(net, stream, steps, flush):
-    """Per-launch device time of every conv, from external events inside the graphs."""
+def time_ops(net, stream, steps, flush):
+    """Per-launch device time of every op, from external events inside the graphs.
+
+    Each op of each section is bracketed by two CUDA events recorded as event
+    nodes of the section's graph (on the launching stream); the graphs are
+    replayed `steps` times after an L2 flush and the per-op times averaged."""
     import torch
     from activation_cnn_gb300 import acnn as A
-    conv_ops = [op for op in net.ops if op.kind == "conv"]
     evs = {id(op): (torch.cuda.Event(enable_timing=True, external=True),
-                    torch.cuda.Event(enable_timing=True, external=True)) for op in conv_ops}
+                    torch.cuda.Event(enable_timing=True, external=True)) for op in net.ops}
     graphs = []
     for sec in net.order:
         g = A.Section(stream)
@@ -149,29 +152,30 @@ def time_roofline(net, stream, steps, flush):
                 for op in net.ops:
                     if op.section != sec:
                         continue
-                    if op.kind == "conv":
-                        evs[id(op)][0].record(stream)
+                    evs[id(op)][0].record(stream)
                     op.fn(stream)
-                    if op.kind == "conv":
-                        evs[id(op)][1].record(stream)
+                    evs[id(op)][1].record(stream)
         graphs.append(g)
-    per_op = {id(op): [] for op in conv_ops}
+    per_op = {id(op): [] for op in net.ops}
     for _ in range(steps):
         flush()
         for g in graphs:
             g.launch(stream)
         stream.synchronize()
-        for op in conv_ops:
+        for op in net.ops:
             a, b = evs[id(op)]
             per_op[id(op)].append(a.elapsed_time(b) * 1e-3)
     for g in graphs:
         g.close()
     rows = []
-    for op in conv_ops:
-        s = op.spec
-        d = A.ConvDesc(net.batch, s.h, s.w, s.c_in, s.c_out, s.k, s.k, s.stride, s.pad,
-                       net.layout, net.dtype)
-        rows.append({"name": op.label, "path": A.acnn_conv2d_path(d), "flops": op.flops,
+    for op in net.ops:
+        path = None
+        if op.kind == "conv":
+            s = op.spec
+            d = A.ConvDesc(net.batch, s.h, s.w, s.c_in, s.c_out, s.k, s.k, s.stride, s.pad,
+                           net.layout, net.dtype)
+            path = A.acnn_conv2d_path(d)
+        rows.append({"name": op.label, "kind": op.kind, "path": path, "flops": op.flops,
                      "bytes": op.bytes, "s": statistics.mean(per_op[id(op)])})
     return rows
 
@@ -237,8 +241,8 @@ def run_ours(args, rank, world, local_rank):
     conv_tflops = net.conv_flops() * world * args.steps / total / 1e12
 
     # ------------------------------------------------ roofline of the dominant kernel
-    rows = time_roofline(net, stream, max(3, min(args.steps, 10)), flush)
-    ig = [r for r in rows if r["path"] in (1, 2)]
+    rows = time_ops(net, stream, max(3, min(args.steps, 10)), flush)
+    ig = [r for r in rows if r["kind"] == "conv" and r["path"] in (1, 2)]
     ig_flops = sum(r["flops"] for r in ig)
     ig_s = sum(r["s"] for r in ig)
     pk = peaks()
@@ -295,6 +299,25 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches_per_step(net) * args.steps,
         "clocks": clk, "wall_s_timed": round(t_wall, 3),
     }
+    # memory-bound companions: algorithmic bytes / launch time vs HBM
+    mem = {}
+    for r in rows:
+        if r["kind"] in ("pool", "resize", "concat", "prep", "deconv"):
+            k = mem.setdefault(r["label_kind"] if "label_kind" in r else r["kind"],
+                               {"launches": 0, "bytes": 0.0, "s": 0.0})
+            k["launches"] += 1
+            k["bytes"] += r["bytes"]
+            k["s"] += r["s"]
+    line["memops"] = {k: {"launches": v["launches"], "GB_s": round(v["bytes"] / v["s"] / 1e9, 1),
+                          "frac_hbm": round(v["bytes"] / v["s"] / 1e9 / pk["hbm"], 4),
+                          "us_per_step": round(1e6 * v["s"], 1)}
+                      for k, v in mem.items()}
+    line["memops_peak"] = f"{pk['source']} HBM copy {pk['hbm']} GB/s"
+    direct = [r for r in rows if r["kind"] == "conv" and r["path"] == 0]
+    if direct:
+        ds = sum(r["s"] for r in direct)
+        line["direct_conv"] = {"launches": len(direct), "us_per_step": round(1e6 * ds, 1),
+                               "TFLOP_s": round(sum(r["flops"] for r in direct) / ds / 1e12, 2)}
     if args.layers:
         line["layers"] = [{k: (round(v, 9) if isinstance(v, float) else v) for k, v in r.items()}
                           for r in rows]
