@@ -39,8 +39,9 @@ EXPORTS = (
     "acnn_pool2d", "acnn_resize2d", "acnn_concat", "acnn_deconv2d", "acnn_frame_prep_quarter",
     "acnn_status_string", "acnn_last_device_status", "acnn_set_wait_budget",
     "acnn_section_begin", "acnn_section_end", "acnn_section_launch", "acnn_section_destroy",
-    "acnn_device_sm_count",
+    "acnn_device_sm_count", "acnn_conv2d_fused_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 16 << 20  # ACNN_NOALLOC_SCRATCH_BYTES in include/acnn.h
 
 
 class AcnnError(RuntimeError):
@@ -87,6 +88,7 @@ def lib() -> ctypes.CDLL:
         L.acnn_section_launch.argtypes = [_P, _P]
         L.acnn_section_destroy.argtypes = [_P]
         L.acnn_device_sm_count.argtypes = []
+        L.acnn_conv2d_fused_noalloc.argtypes = [D, _P, _P, _P, _P, _P, _I, _I, _P, _P]
         _lib = L
     return _lib
 
@@ -117,6 +119,15 @@ def acnn_conv2d_fused(desc, x, w, bias, alpha, residual, res_mode, act, y, works
     return lib().acnn_conv2d_fused(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(alpha),
                                    _ptr(residual), res_mode, act, _ptr(y), _ptr(workspace),
                                    ws_bytes, _stream(stream))
+
+
+def acnn_conv2d_fused_noalloc(desc, x, w, bias, alpha, residual, res_mode, act, y,
+                              stream=None) -> int:
+    """conv2d_fused for callers that cannot allocate: scratch comes from a static
+    device array inside the library (see include/acnn.h)."""
+    return lib().acnn_conv2d_fused_noalloc(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias),
+                                           _ptr(alpha), _ptr(residual), res_mode, act, _ptr(y),
+                                           _stream(stream))
 
 
 def acnn_conv2d_out_hw(desc):

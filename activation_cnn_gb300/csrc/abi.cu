@@ -369,3 +369,52 @@ int acnn_section_destroy(void* exec) {
 int acnn_device_sm_count(void) { return sm_count(); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// acnn_conv2d_fused_noalloc: conv2d_fused for callers that cannot allocate.
+//
+// Some callers have no way to obtain device memory at the point where they
+// run a conv: a plugin inside a host framework that owns every device
+// allocation and hands the plugin no allocator, or a latency-critical loop
+// where a cudaMalloc/cudaFree may synchronise the whole device.  For them the
+// scratch that the NCHW tensor-core path needs (the NHWC copy of x and the
+// OHWI copy of w) lives in the file-scope array below, sized once at
+// ACNN_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library holds
+// until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+__device__ __align__(256) uint8_t g_noalloc_scratch[ACNN_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_scratch_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current (the host-side symbol is only a
+// stand-in, never a device address).  NULL if the lookup fails.
+void* noalloc_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+        g_noalloc_scratch_ptr[dev] = p;
+    }
+    return g_noalloc_scratch_ptr[dev];
+}
+}  // namespace
+
+extern "C" int acnn_conv2d_fused_noalloc(const acnn_conv_desc* d, const void* x, const void* w,
+                                         const float* bias, const float* alpha,
+                                         const void* residual, int res_mode, int act, void* y,
+                                         acnn_stream_t stream) {
+    int st = check_desc(d);
+    if (st != ACNN_OK) return st;
+    const size_t need = acnn_conv2d_workspace_size(d);
+    if (need > (size_t)ACNN_NOALLOC_SCRATCH_BYTES) return ACNN_ERR_WORKSPACE;
+    void* ws = nullptr;
+    if (need > 0) {
+        ws = noalloc_scratch();
+        if (!ws) return ACNN_ERR_CUDA;
+    }
+    return acnn_conv2d_fused(d, x, w, bias, alpha, residual, res_mode, act, y, ws, need, stream);
+}

@@ -120,6 +120,31 @@ size_t acnn_conv2d_workspace_size(const acnn_conv_desc* d);
  * 2 = tcgen05 implicit GEMM with TMA im2col A loads; negative = invalid. */
 int acnn_conv2d_path(const acnn_conv_desc* d);
 
+/* ---- conv2d_fused without caller workspace ----------------------------------
+ * No counterpart on the pages: an addition for callers that cannot allocate
+ * device memory where they run a conv -- e.g. a plugin inside a framework
+ * that owns all device memory and gives the plugin no allocator, or a
+ * latency-critical loop in which cudaMalloc/cudaFree could synchronise the
+ * device.  Same arguments, semantics and results as acnn_conv2d_fused, minus
+ * the workspace: the scratch the NCHW tensor-core path needs is taken from a
+ * static device array of ACNN_NOALLOC_SCRATCH_BYTES that the library holds on
+ * every GPU that loads it, until the process exits.  Nothing is allocated or
+ * freed (no cudaMalloc, cudaFree or allocating library call).
+ *   - A call whose acnn_conv2d_workspace_size(d) exceeds
+ *     ACNN_NOALLOC_SCRATCH_BYTES returns ACNN_ERR_WORKSPACE and launches nothing.
+ *   - The first call on a device that needs scratch looks the array's device
+ *     address up (cudaGetSymbolAddress) with that device current; make that
+ *     first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     nothing in it has to start at zero (each call overwrites what it reads).
+ *     Calls whose kernels overlap on the GPU (other streams, other threads)
+ *     race on it: serialise them.
+ */
+#define ACNN_NOALLOC_SCRATCH_BYTES (16u << 20)
+int acnn_conv2d_fused_noalloc(const acnn_conv_desc* d, const void* x, const void* w,
+                              const float* bias, const float* alpha, const void* residual,
+                              int res_mode, int act, void* y, acnn_stream_t stream);
+
 /* ---- pool2d ----------------------------------------------------------------
  * MAX: y = max over the in-range taps of each k x k window at stride s, pad p
  *      (taps outside the input are skipped: -inf padding), rtdetr_gpu.rs
