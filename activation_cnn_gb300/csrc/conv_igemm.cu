@@ -37,21 +37,25 @@ namespace {
 
 constexpr int BM = 128;             // output pixels per tile (TMEM lanes)
 constexpr int BK = 64;              // channels per k-block: 64 x 2 B = one 128-B swizzle row
-constexpr int kThreads = 192;       // 6 warps
+constexpr int kEpiWarps = 8;        // two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue warps
 constexpr uint32_t kABytes = BM * BK * 2;
 constexpr long long kTimeoutCycles = 8000000000ll;  // ~4 s per wait at 2 GHz
 constexpr long long kDrainCycles = 400000000ll;     // ~0.2 s per drain wait
 
 constexpr uint32_t kStageBytes = 32 * 64;  // epilogue staging: 32 rows x 32 channels x 2 B
-constexpr uint32_t kEpiBytes = 4 /*warps*/ * 2 /*buffers*/ * kStageBytes;
+constexpr uint32_t kEpiBytes = kEpiWarps * 2 /*buffers*/ * kStageBytes;
 
 template <int BN> struct Cfg {
-    static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int kStages = BN == 256 ? 3 : (BN == 128 ? 5 : 6);
     static constexpr uint32_t kBBytes = BN * BK * 2;
     static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
     // ring + output staging + residual staging + barriers, plus alignment slack
-    static constexpr size_t kSmem =
-        1024 + kStages * (kABytes + kBBytes) + 2 * kEpiBytes + 256;
+    static constexpr int kBarriers = 2 * kStages + 5 + 2 * kEpiWarps;
+    static constexpr size_t kBarBytes = 512;
+    static_assert(kBarriers * 8 + 8 <= kBarBytes, "barrier region too small");
+    static constexpr size_t kSmem = 1024 + kStages * (kABytes + kBBytes) + 2 * kEpiBytes + kBarBytes;
+    static_assert(kSmem <= 232448, "exceeds the 227 KB of shared memory per CTA");
 };
 
 struct Params {
@@ -296,6 +300,57 @@ template <> __device__ __forceinline__ void unpack2<__half>(uint32_t u, float& l
     hi = __high2float(h);
 }
 
+// Activation with the code fixed at compile time (no per-element branching).
+// SiLU uses the fast exp and divide intrinsics: their error (a few fp32 ulp)
+// is far below the fp16/bf16 storage rounding that follows.
+template <int ACT> __device__ __forceinline__ float act_fixed(float v, float alpha) {
+    if constexpr (ACT == ACNN_ACT_RELU) return fmaxf(v, 0.0f);
+    else if constexpr (ACT == ACNN_ACT_SILU) return __fdividef(v, 1.0f + __expf(-v));
+    else if constexpr (ACT == ACNN_ACT_PRELU) return v >= 0.0f ? v : alpha * v;
+    else return v;
+}
+
+// 32 outputs of one row: act(acc + bias + kpre*res) + kpost*res, with
+// (kpre, kpost) = (1, 0) for a residual before the activation, (0, 1) after
+// it, (0, 0) without one.
+template <int ACT>
+__device__ __forceinline__ void epi32(const float (&v)[32], const float (&bv)[32],
+                                      const float (&av)[32], const float (&r)[32], float kpre,
+                                      float kpost, float (&o)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        o[j] = fmaf(kpost, r[j], act_fixed<ACT>(fmaf(kpre, r[j], v[j] + bv[j]), av[j]));
+}
+
+__device__ __forceinline__ void epi32_any(int act, const float (&v)[32], const float (&bv)[32],
+                                          const float (&av)[32], const float (&r)[32], float kpre,
+                                          float kpost, float (&o)[32]) {
+    switch (act) {  // uniform across the CTA
+    case ACNN_ACT_RELU: epi32<ACNN_ACT_RELU>(v, bv, av, r, kpre, kpost, o); break;
+    case ACNN_ACT_SILU: epi32<ACNN_ACT_SILU>(v, bv, av, r, kpre, kpost, o); break;
+    case ACNN_ACT_PRELU: epi32<ACNN_ACT_PRELU>(v, bv, av, r, kpre, kpost, o); break;
+    default: epi32<ACNN_ACT_NONE>(v, bv, av, r, kpre, kpost, o); break;
+    }
+}
+
+// Bias and PReLU alpha of channels [co, co + 32): broadcast loads (every lane
+// reads the same addresses); channels >= C_out read as zero.
+__device__ __forceinline__ void load_chunk_params(const float* __restrict__ bias,
+                                                  const float* __restrict__ alpha, bool prelu,
+                                                  int co, int c_out, float (&bv)[32],
+                                                  float (&av)[32]) {
+#pragma unroll
+    for (int g = 0; g < 32; g += 4) {
+        float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f), a4 = b4;
+        if (co + g < c_out) {  // C_out % 16 == 0: a float4 is all in or all out
+            if (bias) b4 = __ldg(reinterpret_cast<const float4*>(bias + co + g));
+            if (prelu) a4 = __ldg(reinterpret_cast<const float4*>(alpha + co + g));
+        }
+        bv[g] = b4.x; bv[g + 1] = b4.y; bv[g + 2] = b4.z; bv[g + 3] = b4.w;
+        av[g] = a4.x; av[g + 1] = a4.y; av[g + 2] = a4.z; av[g + 3] = a4.w;
+    }
+}
+
 // ---------------------------------------------------------------- the kernel
 template <int BN, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -313,8 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sO = sB + S * C::kBBytes;  // output staging, 1024-aligned (64-B swizzle atoms)
     uint8_t* sR = sO + kEpiBytes;       // residual staging
     uint64_t* bars = reinterpret_cast<uint64_t*>(sR + kEpiBytes);
-    // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, residual[4][2]
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 13);
+    // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, residual[8][2]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5 + 2 * kEpiWarps);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -333,10 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
+            mbar_init(tempty_bar(a), kEpiWarps);  // one arrival per epilogue warp
         }
         mbar_init(drain_bar, 1);
-        for (int i = 0; i < 8; ++i) mbar_init(res_bar(i >> 1, i & 1), 1);
+        for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(res_bar(i >> 1, i & 1), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tmap_a);
@@ -447,17 +502,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (p.out_layout == ACNN_NHWC) {
         // ---------------------------------------------------- epilogue warps, NHWC
-        // Each warp owns 32 rows (its TMEM lane quarter) of the 128-row tile and
-        // walks the tile's channels 32 at a time: the residual box arrives by TMA
-        // one chunk ahead into a double buffer, the 32 x 32 result is written to a
-        // 64-byte-swizzled staging buffer and leaves by a TMA store (which also
-        // clips rows >= M and channels >= C_out).
+        // Warp e (0..7) owns the 32 rows of its TMEM lane quarter (warp % 4) and
+        // every other 32-channel chunk of the tile (e / 4 picks even or odd): the
+        // residual box arrives by TMA one chunk ahead into a double buffer, the
+        // 32 x 32 result goes to a 64-byte-swizzled staging buffer and leaves by
+        // a TMA store (which also clips rows >= M and channels >= C_out).
         const int q = warp & 3;
         const int e = warp - 2;
+        const int half = e >> 2;
         uint8_t* ost = sO + e * 2 * kStageBytes;
         uint8_t* rst = sR + e * 2 * kStageBytes;
         const bool has_res = p.res_mode != ACNN_RES_NONE;
         const bool prelu = p.act == ACNN_ACT_PRELU;
+        const float kpre = p.res_mode == ACNN_RES_ADD_THEN_ACT ? 1.f : 0.f;
+        const float kpost = p.res_mode == ACNN_RES_ACT_THEN_ADD ? 1.f : 0.f;
         const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // 64-B swizzle of this lane's row
         int acc = 0, ob = 0, rb = 0;
         uint32_t acc_phase = 0, rpar = 0, r_inflight = 0;
@@ -472,32 +530,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n0 = (tile % p.num_n_tiles) * BN;
             const int row0 = m0 + q * 32;
             const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
-            if (has_res) {
-                if (lane == 0) issue_res(rb, n0, row0);
+            if (has_res && half < nch) {
+                if (lane == 0) issue_res(rb, n0 + half * 32, row0);
                 r_inflight |= 1u << rb;
             }
             const bool ok = __all_sync(0xffffffffu, wait_phase(tfull_bar(acc), acc_phase, abort_flag, p));
             if (!ok) break;
             tc_fence_after();
-            for (int i = 0; i < nch; ++i) {
+            for (int i = half; i < nch; i += 2) {
                 const int c = i * 32;
-                if (has_res && i + 1 < nch) {
-                    if (lane == 0) issue_res(rb ^ 1, n0 + c + 32, row0);
+                if (has_res && i + 2 < nch) {
+                    if (lane == 0) issue_res(rb ^ 1, n0 + c + 64, row0);
                     r_inflight |= 1u << (rb ^ 1);
                 }
-                // bias / alpha of the chunk (same addresses in every lane: broadcast loads)
                 float bv[32], av[32];
-#pragma unroll
-                for (int g = 0; g < 32; g += 4) {
-                    const int co = n0 + c + g;
-                    float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f), a4 = b4;
-                    if (co < p.C_out) {  // C_out % 8 == 0: a float4 is all in or all out
-                        if (p.bias) b4 = __ldg(reinterpret_cast<const float4*>(p.bias + co));
-                        if (prelu) a4 = __ldg(reinterpret_cast<const float4*>(p.alpha + co));
-                    }
-                    bv[g] = b4.x; bv[g + 1] = b4.y; bv[g + 2] = b4.z; bv[g + 3] = b4.w;
-                    av[g] = a4.x; av[g + 1] = a4.y; av[g + 2] = a4.z; av[g + 3] = a4.w;
-                }
+                load_chunk_params(p.bias, p.alpha, prelu, n0 + c, p.C_out, bv, av);
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), v);
                 float r[32];
@@ -523,22 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = 0.f;
                 }
-                uint32_t packed[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    packed[k] = pack2<T>(
-                        epilogue(v[2 * k] + bv[2 * k], p.act, av[2 * k], p.res_mode, r[2 * k]),
-                        epilogue(v[2 * k + 1] + bv[2 * k + 1], p.act, av[2 * k + 1], p.res_mode,
-                                 r[2 * k + 1]));
+                float o[32];
+                epi32_any(p.act, v, bv, av, r, kpre, kpost, o);
                 // the store that last used this staging buffer must have read it
                 if (lane == 0) bulk_wait_read<1>();
                 __syncwarp();
                 uint8_t* orow = ost + ob * kStageBytes + lane * 64;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(orow + ((j ^ swz) << 4)) =
-                        make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
-                                   packed[4 * j + 3]);
+                    *reinterpret_cast<uint4*>(orow + ((j ^ swz) << 4)) = make_uint4(
+                        pack2<T>(o[8 * j + 0], o[8 * j + 1]), pack2<T>(o[8 * j + 2], o[8 * j + 3]),
+                        pack2<T>(o[8 * j + 4], o[8 * j + 5]), pack2<T>(o[8 * j + 6], o[8 * j + 7]));
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -563,10 +605,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------------- epilogue warps, NCHW
+        // Same row/chunk split as above; lane l holds output pixel m0 + 32q + l,
+        // so each of the 32 channel planes is written by 32 consecutive pixels.
         const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         const T* res = static_cast<const T*>(p.res);
         T* y = static_cast<T*>(p.y);
+        const bool has_res = p.res_mode != ACNN_RES_NONE;
+        const bool prelu = p.act == ACNN_ACT_PRELU;
+        const float kpre = p.res_mode == ACNN_RES_ADD_THEN_ACT ? 1.f : 0.f;
+        const float kpost = p.res_mode == ACNN_RES_ACT_THEN_ADD ? 1.f : 0.f;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -579,53 +628,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int m = m0 + row;
             const bool valid = m < p.M;
-            // NHWC: row m of [M, C_out]; NCHW: pixel m%OHW of image m/OHW, planes OHW apart
-            long long base, cstride;
-            if (p.out_layout == ACNN_NHWC) {
-                base = (long long)m * p.C_out;
-                cstride = 1;
-            } else {
-                const int img = m / p.OHW;
-                base = (long long)img * p.C_out * p.OHW + (m - img * p.OHW);
-                cstride = p.OHW;
-            }
-            for (int c = 0; c < BN; c += 32) {
-                if (n0 + c >= p.C_out) break;  // uniform across the warp
-                float v[32];
+            const int img = m / p.OHW;
+            const long long base = (long long)img * p.C_out * p.OHW + (m - img * p.OHW);
+            const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
+            for (int i = half; i < nch; i += 2) {
+                const int c = i * 32;
+                float bv[32], av[32], r[32], o[32], v[32];
+                load_chunk_params(p.bias, p.alpha, prelu, n0 + c, p.C_out, bv, av);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    r[j] = (has_res && valid && n0 + c + j < p.C_out)
+                               ? to_f32(res[base + (long long)(n0 + c + j) * p.OHW])
+                               : 0.f;
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), v);
-                if (!valid) continue;
-                if (p.out_layout == ACNN_NHWC) {
+                epi32_any(p.act, v, bv, av, r, kpre, kpost, o);
+                if (valid) {
 #pragma unroll
-                    for (int g = 0; g < 32; g += 8) {
-                        const int co = n0 + c + g;
-                        if (co >= p.C_out) break;
-                        Vec<T, 8> rv, ov;
-                        if (p.res_mode != ACNN_RES_NONE)
-                            rv = *reinterpret_cast<const Vec<T, 8>*>(res + base + co);
-                        const float4 b0 = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias + co))
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-                        const float4 b1 = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias + co + 4))
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-                        const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float al = p.act == ACNN_ACT_PRELU ? __ldg(p.alpha + co + j) : 0.f;
-                            const float r = p.res_mode != ACNN_RES_NONE ? to_f32(rv.v[j]) : 0.f;
-                            ov.v[j] = from_f32<T>(epilogue(v[g + j] + bb[j], p.act, al, p.res_mode, r));
-                        }
-                        *reinterpret_cast<Vec<T, 8>*>(y + base + co) = ov;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int co = n0 + c + j;
-                        if (co >= p.C_out) continue;
-                        const long long oi = base + (long long)co * cstride;
-                        const float bv = p.bias ? __ldg(p.bias + co) : 0.f;
-                        const float al = p.act == ACNN_ACT_PRELU ? __ldg(p.alpha + co) : 0.f;
-                        const float r = p.res_mode != ACNN_RES_NONE ? to_f32(res[oi]) : 0.f;
-                        y[oi] = from_f32<T>(epilogue(v[j] + bv, p.act, al, p.res_mode, r));
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        if (n0 + c + j < p.C_out)
+                            y[base + (long long)(n0 + c + j) * p.OHW] = from_f32<T>(o[j]);
                 }
             }
             tc_fence_before();
