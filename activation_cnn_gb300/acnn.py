@@ -39,7 +39,7 @@ EXPORTS = (
     "acnn_pool2d", "acnn_resize2d", "acnn_concat", "acnn_deconv2d", "acnn_frame_prep_quarter",
     "acnn_status_string", "acnn_last_device_status", "acnn_set_wait_budget",
     "acnn_section_begin", "acnn_section_end", "acnn_section_launch", "acnn_section_destroy",
-    "acnn_device_sm_count", "acnn_conv2d_fused_noalloc",
+    "acnn_device_sm_count", "acnn_conv2d_fused_noalloc", "acnn_conv2d_plan",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # ACNN_NOALLOC_SCRATCH_BYTES in include/acnn.h
 
@@ -89,6 +89,7 @@ def lib() -> ctypes.CDLL:
         L.acnn_section_destroy.argtypes = [_P]
         L.acnn_device_sm_count.argtypes = []
         L.acnn_conv2d_fused_noalloc.argtypes = [D, _P, _P, _P, _P, _P, _I, _I, _P, _P]
+        L.acnn_conv2d_plan.argtypes = [D, ctypes.c_size_t] + [ctypes.POINTER(_I)] * 3
         _lib = L
     return _lib
 
@@ -138,6 +139,14 @@ def acnn_conv2d_out_hw(desc):
 
 def acnn_conv2d_workspace_size(desc) -> int:
     return lib().acnn_conv2d_workspace_size(ctypes.byref(desc))
+
+
+def acnn_conv2d_plan(desc, ws_bytes):
+    """(status, rows, bn, splits) of the tensor-core plan with ws_bytes of workspace."""
+    rows, bn, sp = _I(), _I(), _I()
+    st = lib().acnn_conv2d_plan(ctypes.byref(desc), ws_bytes, ctypes.byref(rows),
+                                ctypes.byref(bn), ctypes.byref(sp))
+    return st, rows.value, bn.value, sp.value
 
 
 def acnn_conv2d_path(desc) -> int:

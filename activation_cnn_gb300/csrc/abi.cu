@@ -6,6 +6,8 @@
 // allocates no device memory.
 #include <cuda_runtime.h>
 
+#include <stdint.h>
+
 #include <atomic>
 #include <mutex>
 
@@ -98,12 +100,13 @@ int conv_out(const acnn_conv_desc* d, int* oh, int* ow) {
     return ACNN_OK;
 }
 
-// The tensor-core path: fp16/bf16, TMA-addressable channel strides (16-byte
-// multiples), whole 16-channel MMA columns, square kernels whose corner
-// offsets fit the im2col descriptor, and 32-bit pixel indices.
+// The tensor-core path with TMA loads of x itself: fp16/bf16, TMA-addressable
+// channel strides (16-byte multiples), output rows of whole 16-byte vectors,
+// square kernels whose corner offsets fit the im2col descriptor, and 32-bit
+// pixel indices.
 bool tensor_path_ok(const acnn_conv_desc* d, int oh, int ow) {
     if (d->dtype == ACNN_F32) return false;
-    if (d->c_in % 8 != 0 || d->c_out % 16 != 0) return false;
+    if (d->c_in % 8 != 0 || d->c_out % 8 != 0) return false;
     if (d->kh != d->kw || d->kh > 8 || d->stride > 8 || d->pad > 64) return false;
     if (d->pad - (d->kh - 1) < -128) return false;
     const long long m = (long long)d->n * oh * ow;
@@ -111,13 +114,52 @@ bool tensor_path_ok(const acnn_conv_desc* d, int oh, int ow) {
     return m <= kIndexLimit && in <= kIndexLimit && (long long)d->c_out * oh * ow <= kIndexLimit;
 }
 
+// Padded reduction length of the packed path: K = kh*kw*c_in rounded up to 8.
+int packed_k(const acnn_conv_desc* d) { return (d->kh * d->kw * d->c_in + 7) / 8 * 8; }
+
+// The packed tensor-core path, for the convs TMA cannot address (few or odd
+// input channels, non-square kernels): an explicit im2col matrix with
+// K = kh*kw*c_in padded to a multiple of 8 is built in the workspace and
+// multiplied on the tensor cores as a 1x1 conv.  Used while K stays small
+// (at most 512), where the packed matrix costs little next to the output.
+bool packed_path_ok(const acnn_conv_desc* d, int oh, int ow) {
+    if (d->dtype == ACNN_F32 || d->c_out % 8 != 0 || tensor_path_ok(d, oh, ow)) return false;
+    const long long m = (long long)d->n * oh * ow;
+    return packed_k(d) <= 512 && m * packed_k(d) <= kIndexLimit &&
+           (long long)d->n * d->h * d->w * d->c_in <= kIndexLimit &&
+           (long long)d->c_out * oh * ow <= kIndexLimit;
+}
+
 size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 
-// Workspace of an NCHW call on the tensor path: the NHWC copy of x and the
-// OHWI copy of w, each 256-byte aligned.
-void nchw_workspace(const acnn_conv_desc* d, size_t* x_bytes, size_t* w_bytes) {
-    *x_bytes = round256((size_t)d->n * d->h * d->w * d->c_in * elem_size(d->dtype));
-    *w_bytes = round256((size_t)d->c_out * d->kh * d->kw * d->c_in * elem_size(d->dtype));
+// How a conv reaches the tensor cores: the path, the workspace it requires
+// (staging copies: NHWC x and OHWI w for NCHW convs, or the packed im2col
+// matrix and packed weights) and the geometry the GEMM kernel sees.
+struct Route {
+    int path;           // 0 direct, 1 tiled 1x1, 2 im2col, 3 packed
+    size_t stage_x;     // bytes of the staged activation operand
+    size_t stage_w;     // bytes of the staged weight operand
+    acnn_conv_desc g;   // geometry of the tensor-core launch (NHWC)
+};
+
+Route route(const acnn_conv_desc* d, int oh, int ow) {
+    Route r{0, 0, 0, *d};
+    const size_t es = elem_size(d->dtype);
+    if (tensor_path_ok(d, oh, ow)) {
+        r.path = (d->kh == 1 && d->kw == 1 && d->stride == 1 && d->pad == 0) ? 1 : 2;
+        if (d->layout == ACNN_NCHW) {
+            r.stage_x = round256((size_t)d->n * d->h * d->w * d->c_in * es);
+            r.stage_w = round256((size_t)d->c_out * d->kh * d->kw * d->c_in * es);
+        }
+        r.g.layout = ACNN_NHWC;
+    } else if (packed_path_ok(d, oh, ow)) {
+        const int kp = packed_k(d);
+        r.path = 3;
+        r.stage_x = round256((size_t)d->n * oh * ow * kp * es);
+        r.stage_w = round256((size_t)d->c_out * kp * es);
+        r.g = acnn_conv_desc{d->n, oh, ow, kp, d->c_out, 1, 1, 1, 0, ACNN_NHWC, d->dtype};
+    }
+    return r;
 }
 
 }  // namespace
@@ -134,17 +176,29 @@ int acnn_conv2d_out_hw(const acnn_conv_desc* d, int* oh, int* ow) {
 int acnn_conv2d_path(const acnn_conv_desc* d) {
     int oh, ow;
     if (check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK) return -1;
-    if (!tensor_path_ok(d, oh, ow)) return 0;
-    return (d->kh == 1 && d->kw == 1 && d->stride == 1 && d->pad == 0) ? 1 : 2;
+    return route(d, oh, ow).path;
 }
 
 size_t acnn_conv2d_workspace_size(const acnn_conv_desc* d) {
     int oh, ow;
     if (check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK) return 0;
-    if (d->layout != ACNN_NCHW || !tensor_path_ok(d, oh, ow)) return 0;
-    size_t xb, wb;
-    nchw_workspace(d, &xb, &wb);
-    return xb + wb;
+    const Route r = route(d, oh, ow);
+    if (r.path == 0) return 0;
+    return r.stage_x + r.stage_w + round256(igemm_plan(r.g, oh, ow, SIZE_MAX).part_bytes);
+}
+
+int acnn_conv2d_plan(const acnn_conv_desc* d, size_t ws_bytes, int* rows, int* bn,
+                     int* splits) {
+    int oh, ow;
+    if (!rows || !bn || !splits || check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK)
+        return -1;
+    const Route r = route(d, oh, ow);
+    if (r.path == 0 || ws_bytes < r.stage_x + r.stage_w) return -1;
+    const IgemmPlan pl = igemm_plan(r.g, oh, ow, ws_bytes - r.stage_x - r.stage_w);
+    *rows = 128 * pl.ms;
+    *bn = pl.bn;
+    *splits = pl.splits;
+    return 0;
 }
 
 int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w, const float* bias,
@@ -191,25 +245,43 @@ int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w, con
     a.out_layout = d->layout;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    if (!tensor_path_ok(d, oh, ow)) return status_of(launch_direct_conv(a, s));
-    if (d->layout == ACNN_NHWC) return launch_igemm_conv(a, s);
+    const Route r = route(d, oh, ow);
+    if (r.path == 0) return status_of(launch_direct_conv(a, s));
 
-    // NCHW on the tensor path: NHWC copy of x and OHWI copy of w in the
-    // caller's workspace, then the implicit GEMM writing NCHW directly.
-    size_t xws, wws;
-    nchw_workspace(d, &xws, &wws);
-    if (!workspace || ws_bytes < xws + wws) return ACNN_ERR_WORKSPACE;
-    if (overlaps(workspace, xws + wws, y, yb) || overlaps(workspace, xws + wws, x, xb) ||
-        overlaps(workspace, xws + wws, w, wb) ||
-        (a.residual && overlaps(workspace, xws + wws, residual, yb)))
+    // Workspace: [staged x | staged w] (required for NCHW and packed convs), then
+    // split-K partial sums (optional: a smaller remainder selects fewer splits).
+    const size_t stage = r.stage_x + r.stage_w;
+    if (!workspace) ws_bytes = 0;
+    if (ws_bytes < stage) return ACNN_ERR_WORKSPACE;
+    if (ws_bytes > 0 &&
+        (overlaps(workspace, ws_bytes, y, yb) || overlaps(workspace, ws_bytes, x, xb) ||
+         overlaps(workspace, ws_bytes, w, wb) ||
+         (a.residual && overlaps(workspace, ws_bytes, residual, yb))))
         return ACNN_ERR_ALIAS;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    cudaError_t e = launch_nchw_to_nhwc(d->n, d->c_in, d->h * d->w, 2, x, ws, s);
+    a.ws_part = ws_bytes > stage ? ws + stage : nullptr;
+    a.ws_part_bytes = ws_bytes - stage;
+    cudaError_t e = cudaSuccess;
+    if (r.path == 3) {
+        // explicit im2col: [n*oh*ow, kp] and [c_out, kp], then a 1x1 GEMM whose
+        // epilogue writes y in the caller's layout
+        e = launch_im2col_pack(*d, oh, ow, r.g.c_in, x, ws, w, ws + r.stage_x, s);
+        if (e != cudaSuccess) return ACNN_ERR_CUDA;
+        a.d = r.g;
+        a.x = ws;
+        a.w = ws + r.stage_x;
+        return launch_igemm_conv(a, s);
+    }
+    if (d->layout == ACNN_NHWC) return launch_igemm_conv(a, s);
+
+    // NCHW on the TMA paths: NHWC copy of x and OHWI copy of w, then the
+    // implicit GEMM writing NCHW directly.
+    e = launch_nchw_to_nhwc(d->n, d->c_in, d->h * d->w, 2, x, ws, s);
     if (e != cudaSuccess) return ACNN_ERR_CUDA;
-    e = launch_nchw_to_nhwc(d->c_out, d->c_in, d->kh * d->kw, 2, w, ws + xws, s);
+    e = launch_nchw_to_nhwc(d->c_out, d->c_in, d->kh * d->kw, 2, w, ws + r.stage_x, s);
     if (e != cudaSuccess) return ACNN_ERR_CUDA;
     a.x = ws;
-    a.w = ws + xws;
+    a.w = ws + r.stage_x;
     a.d.layout = ACNN_NHWC;
     a.out_layout = ACNN_NCHW;
     return launch_igemm_conv(a, s);
@@ -226,6 +298,7 @@ int acnn_pool2d(int kind, int n, int h, int w, int c, int k, int stride, int pad
     if (pad >= k) return ACNN_ERR_UNSUPPORTED;  // a window could hold no input tap
     if (h + 2 * pad < k || w + 2 * pad < k) return ACNN_ERR_BAD_GEOMETRY;
     const int oh = (h + 2 * pad - k) / stride + 1, ow = (w + 2 * pad - k) / stride + 1;
+    if ((long long)n * h * w * c > kIndexLimit) return ACNN_ERR_TOO_LARGE;
     if (!aligned16(x) || !aligned16(y)) return ACNN_ERR_MISALIGNED;
     const size_t es = elem_size(dtype);
     if (overlaps(x, (size_t)n * h * w * c * es, y, (size_t)n * oh * ow * c * es))
@@ -242,6 +315,8 @@ int acnn_resize2d(int mode, int n, int c, int h, int w, int oh, int ow, int layo
     if (!x || !y) return ACNN_ERR_NULL_POINTER;
     if (n <= 0 || c <= 0 || h <= 0 || w <= 0 || oh <= 0 || ow <= 0) return ACNN_ERR_BAD_GEOMETRY;
     if (mode == ACNN_RESIZE_NEAREST && in_dtype != out_dtype) return ACNN_ERR_UNSUPPORTED;
+    if ((long long)n * c * oh * ow > kIndexLimit || (long long)n * c * h * w > kIndexLimit)
+        return ACNN_ERR_TOO_LARGE;
     if (!aligned16(x) || !aligned16(y)) return ACNN_ERR_MISALIGNED;
     if (overlaps(x, (size_t)n * c * h * w * elem_size(in_dtype), y,
                  (size_t)n * c * oh * ow * elem_size(out_dtype)))
@@ -257,7 +332,7 @@ int acnn_concat(int n, int h, int w, int c_a, int c_b, int layout, int dtype, co
     if (n <= 0 || h <= 0 || w <= 0 || c_a <= 0 || c_b <= 0) return ACNN_ERR_BAD_GEOMETRY;
     if (!aligned16(a) || !aligned16(b) || !aligned16(y)) return ACNN_ERR_MISALIGNED;
     const size_t es = elem_size(dtype), px = (size_t)n * h * w;
-    if ((long long)(c_a + c_b) * h * w > kIndexLimit) return ACNN_ERR_TOO_LARGE;
+    if ((long long)n * (c_a + c_b) * h * w > kIndexLimit) return ACNN_ERR_TOO_LARGE;
     if (overlaps(y, px * (c_a + c_b) * es, a, px * c_a * es) ||
         overlaps(y, px * (c_a + c_b) * es, b, px * c_b * es))
         return ACNN_ERR_ALIAS;
@@ -276,6 +351,9 @@ int acnn_deconv2d(const acnn_conv_desc* d, const void* x, const float* w, const 
     if (d->kh != 4 || d->kw != 4 || d->stride != 2 || d->pad != 1) return ACNN_ERR_UNSUPPORTED;
     const int oh = (d->h - 1) * d->stride - 2 * d->pad + d->kh;
     const int ow = (d->w - 1) * d->stride - 2 * d->pad + d->kw;
+    if ((long long)d->n * oh * ow * ((d->c_out + 7) / 8) > kIndexLimit ||
+        (long long)d->n * d->c_in * d->h * d->w > kIndexLimit)
+        return ACNN_ERR_TOO_LARGE;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
         (alpha && !aligned16(alpha)))
         return ACNN_ERR_MISALIGNED;
@@ -292,6 +370,7 @@ int acnn_frame_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_t* r
     if (!valid_dtype(out_dtype)) return ACNN_ERR_BAD_ENUM;
     if (!rgba0 || !rgba1 || !y) return ACNN_ERR_NULL_POINTER;
     if (h <= 0 || w <= 0 || h % 4 != 0 || w % 4 != 0) return ACNN_ERR_BAD_GEOMETRY;
+    if ((long long)h * w > kIndexLimit) return ACNN_ERR_TOO_LARGE;
     if (!aligned16(rgba0) || !aligned16(rgba1) || !aligned16(y)) return ACNN_ERR_MISALIGNED;
     const size_t yb = (size_t)7 * (h / 4) * (w / 4) * elem_size(out_dtype);
     if (overlaps(y, yb, rgba0, (size_t)h * w * 4) || overlaps(y, yb, rgba1, (size_t)h * w * 4))
@@ -409,12 +488,20 @@ extern "C" int acnn_conv2d_fused_noalloc(const acnn_conv_desc* d, const void* x,
                                          acnn_stream_t stream) {
     int st = check_desc(d);
     if (st != ACNN_OK) return st;
-    const size_t need = acnn_conv2d_workspace_size(d);
-    if (need > (size_t)ACNN_NOALLOC_SCRATCH_BYTES) return ACNN_ERR_WORKSPACE;
+    // The staging copies must fit; split-K partial sums use what is left
+    // of the array (fewer splits when little is left).
+    int oh, ow;
+    st = conv_out(d, &oh, &ow);
+    if (st != ACNN_OK) return st;
+    const Route r = route(d, oh, ow);
+    if (r.stage_x + r.stage_w > (size_t)ACNN_NOALLOC_SCRATCH_BYTES) return ACNN_ERR_WORKSPACE;
+    const size_t want = acnn_conv2d_workspace_size(d);
+    const size_t give = want < (size_t)ACNN_NOALLOC_SCRATCH_BYTES ? want
+                                                                  : (size_t)ACNN_NOALLOC_SCRATCH_BYTES;
     void* ws = nullptr;
-    if (need > 0) {
+    if (give > 0) {
         ws = noalloc_scratch();
         if (!ws) return ACNN_ERR_CUDA;
     }
-    return acnn_conv2d_fused(d, x, w, bias, alpha, residual, res_mode, act, y, ws, need, stream);
+    return acnn_conv2d_fused(d, x, w, bias, alpha, residual, res_mode, act, y, ws, give, stream);
 }

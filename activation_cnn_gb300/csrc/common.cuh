@@ -94,7 +94,20 @@ struct ConvArgs {
     int res_mode, act;
     void* y;
     int out_layout;  // layout y and residual are written/read in (may differ from d.layout)
+    void* ws_part;         // split-K partial-sum workspace (256-byte aligned) or NULL
+    size_t ws_part_bytes;  // its size: the planner uses at most this much
 };
+
+// Tile width and K split of the tensor-core conv for a geometry, given the
+// bytes available for split-K partial sums (SIZE_MAX: as many as it wants).
+struct IgemmPlan {
+    int bn;             // output channels per tile: 64, 128 or 256
+    int ms;             // 128-pixel row blocks per tile: 1 or 2
+    int splits;         // K splits (1 = none)
+    int kb_per_split;   // 64-channel k-blocks per split
+    size_t part_bytes;  // fp32 partial-sum workspace the plan needs
+};
+IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget);
 
 int sm_count();
 int* device_status_ptr();         // device address of the status word
@@ -115,6 +128,9 @@ cudaError_t launch_deconv2d(const acnn_conv_desc& d, int oh, int ow, const void*
                             int out_dtype, void* y, cudaStream_t s);
 cudaError_t launch_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_t* rgba1,
                                 float t, int out_dtype, void* y, cudaStream_t s);
+// im2col pack of x into a [n*oh*ow, kp] matrix and of w into [c_out, kp] (2-byte types)
+cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, const void* x,
+                               void* a, const void* w, void* wp, cudaStream_t s);
 // NCHW -> NHWC activation transpose and OIHW -> OHWI weight transpose (2-byte types)
 cudaError_t launch_nchw_to_nhwc(int n, int c, int hw, int elem_bytes, const void* x, void* y,
                                 cudaStream_t s);

@@ -76,24 +76,38 @@ __global__ void __launch_bounds__(kThreads) direct_conv_kernel(
         // stage the input halo tile of channels [ci0, ci0 + nci); taps outside
         // the image are zero (rtdetr_gpu.rs IM2COL_SRC)
         const int tile_elems = nci * ITH * ITW;
-        for (int idx = tid; idx < tile_elems; idx += kThreads) {
-            int ci, iy, ix;
-            if (layout == ACNN_NHWC) {
-                ci = idx % nci;
-                int r = idx / nci;
-                ix = r % ITW;
-                iy = r / ITW;
-            } else {
-                ix = idx % ITW;
-                int r = idx / ITW;
-                iy = r % ITH;
-                ci = r / ITH;
+        // eight independent loads per thread in flight before any is stored
+        constexpr int kBatch = 8;
+        for (int base = tid; base < tile_elems; base += kThreads * kBatch) {
+            float v[kBatch];
+            int dst[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int idx = base + u * kThreads;
+                v[u] = 0.0f;
+                dst[u] = -1;
+                if (idx < tile_elems) {
+                    int ci, iy, ix;
+                    if (layout == ACNN_NHWC) {
+                        ci = idx % nci;
+                        const int r = idx / nci;
+                        ix = r % ITW;
+                        iy = r / ITW;
+                    } else {
+                        ix = idx % ITW;
+                        const int r = idx / ITW;
+                        iy = r % ITH;
+                        ci = r / ITH;
+                    }
+                    dst[u] = (ci * ITH + iy) * ITW + ix;
+                    const int gy = gy0 + iy, gx = gx0 + ix;
+                    if (gy >= 0 && gy < H && gx >= 0 && gx < W)
+                        v[u] = to_f32(x[act_index(layout, C_in, H, W, n, ci0 + ci, gy, gx)]);
+                }
             }
-            const int gy = gy0 + iy, gx = gx0 + ix;
-            float v = 0.0f;
-            if (gy >= 0 && gy < H && gx >= 0 && gx < W)
-                v = to_f32(x[act_index(layout, C_in, H, W, n, ci0 + ci, gy, gx)]);
-            s_in[(ci * ITH + iy) * ITW + ix] = v;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (dst[u] >= 0) s_in[dst[u]] = v[u];
         }
         // stage the weights of those channels for kCOB output channels
         const int w_elems = nci * KK * kCOB;

@@ -46,21 +46,29 @@ constexpr long long kDrainCycles = 400000000ll;     // ~0.2 s per drain wait
 constexpr uint32_t kStageBytes = 32 * 64;  // epilogue staging: 32 rows x 32 channels x 2 B
 constexpr uint32_t kEpiBytes = kEpiWarps * 2 /*buffers*/ * kStageBytes;
 
-template <int BN> struct Cfg {
-    static constexpr int kStages = BN == 256 ? 3 : (BN == 128 ? 5 : 6);
+// Tile of (128 * MS) output pixels x BN output channels: MS row blocks of 128
+// share each B tile, so one pipeline step carries MS x 4 MMAs.
+template <int BN, int MS> struct Cfg {
+    static constexpr uint32_t kAB = MS * kABytes;  // A bytes per stage
     static constexpr uint32_t kBBytes = BN * BK * 2;
-    static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-    // ring + output staging + residual staging + barriers, plus alignment slack
-    static constexpr int kBarriers = 2 * kStages + 5 + 2 * kEpiWarps;
+    static constexpr uint32_t kTmemCols = 2 * MS * BN < 32 ? 32 : 2 * MS * BN;
     static constexpr size_t kBarBytes = 512;
+    static constexpr size_t kFixed = 1024 /*alignment slack*/ + 2 * kEpiBytes + kBarBytes;
+    static constexpr int kStagesFit = (int)((232448 - kFixed) / (kAB + kBBytes));
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    static constexpr int kBarriers = 2 * kStages + 5 + 2 * kEpiWarps;
+    static_assert(kStages >= 2, "ring too shallow");
     static_assert(kBarriers * 8 + 8 <= kBarBytes, "barrier region too small");
-    static constexpr size_t kSmem = 1024 + kStages * (kABytes + kBBytes) + 2 * kEpiBytes + kBarBytes;
+    static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
+    static constexpr size_t kSmem = kFixed + kStages * (kAB + kBBytes);
     static_assert(kSmem <= 232448, "exceeds the 227 KB of shared memory per CTA");
 };
 
 struct Params {
     int M, C_out, taps, KW, kb_per_tap, num_kb;
     int num_m_tiles, num_n_tiles;
+    int splits, kb_per_split;  // split-K: unit = tile * splits + split
+    float* part;               // split-K partial sums [splits][M][C_out] (fp32), or NULL
     int OW, OHW, S, P;
     int a_mode;       // 0: tiled A (1x1/s1/p0); 1: im2col A
     int out_layout;   // ACNN_NHWC or ACNN_NCHW for y and the residual
@@ -352,19 +360,20 @@ __device__ __forceinline__ void load_chunk_params(const float* __restrict__ bias
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int BN, typename T>
+template <int BN, int MS, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_conv_kernel(const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_y,
                       const __grid_constant__ CUtensorMap tmap_r, const Params p) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, MS>;
     constexpr int S = C::kStages;
+    constexpr int TM = BM * MS;  // output pixels per tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint8_t* sA = smem;
-    uint8_t* sB = smem + S * kABytes;
+    uint8_t* sB = smem + S * C::kAB;
     uint8_t* sO = sB + S * C::kBBytes;  // output staging, 1024-aligned (64-B swizzle atoms)
     uint8_t* sR = sO + kEpiBytes;       // residual staging
     uint64_t* bars = reinterpret_cast<uint64_t*>(sR + kEpiBytes);
@@ -410,7 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+    // a work unit is one output tile and one K range (the whole K without split-K)
+    const int num_tiles = p.num_m_tiles * p.num_n_tiles * p.splits;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -419,33 +429,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int m0 = (tile / p.num_n_tiles) * BM;
+            for (int unit = blockIdx.x; ok && unit < num_tiles; unit += gridDim.x) {
+                const int tile = unit / p.splits, split = unit - tile * p.splits;
+                const int m0 = (tile / p.num_n_tiles) * TM;
                 const int n0 = (tile % p.num_n_tiles) * BN;
+                const int kb0 = split * p.kb_per_split;
+                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
                 // window corner of the tile's first output pixel
                 const int img = m0 / p.OHW, r = m0 % p.OHW;
                 const int wc = (r % p.OW) * p.S - p.P, hc = (r / p.OW) * p.S - p.P;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    const int tap = kb / p.kb_per_tap;
-                    const int c0 = (kb % p.kb_per_tap) * BK;
+                // (tap, channel block) of k-block kb0, then stepped without divisions
+                int tap = kb0 / p.kb_per_tap;
+                int c0 = (kb0 - tap * p.kb_per_tap) * BK;
+                int ky = tap / p.KW, kx = tap - ky * p.KW;
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, kABytes + C::kBBytes);
-                    const uint32_t a_dst = smem_u32(sA + stage * kABytes);
+                    mbar_arrive_expect_tx(fb, C::kAB + C::kBBytes);
+                    const uint32_t a_dst = smem_u32(sA + stage * C::kAB);
                     if (p.a_mode == 0)
                         tma_load_2d(a_dst, &tmap_a, fb, c0, m0);
                     else
-                        tma_load_im2col(a_dst, &tmap_a, fb, c0, wc, hc, img,
-                                        (uint16_t)(tap % p.KW), (uint16_t)(tap / p.KW));
+                        tma_load_im2col(a_dst, &tmap_a, fb, c0, wc, hc, img, (uint16_t)kx,
+                                        (uint16_t)ky);
                     tma_load_3d(smem_u32(sB + stage * C::kBBytes), &tmap_b, fb, c0, tap, n0);
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
+                    }
+                    c0 += BK;
+                    if (c0 >= p.kb_per_tap * BK) {
+                        c0 = 0;
+                        ++tap;
+                        if (++kx == p.KW) {
+                            kx = 0;
+                            ++ky;
+                        }
                     }
                 }
             }
@@ -465,24 +489,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int unit = blockIdx.x; ok && unit < num_tiles; unit += gridDim.x) {
+                const int split = unit % p.splits;
+                const int kb0 = split * p.kb_per_split;
+                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
                 if (!wait_phase(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MS * BN);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(full_bar(stage), phase, abort_flag, p)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = sw128_desc(smem_u32(sA + stage * kABytes));
                     const uint64_t bdesc = sw128_desc(smem_u32(sB + stage * C::kBBytes));
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        mma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) != 0);
+                    for (int ms = 0; ms < MS; ++ms) {
+                        const uint64_t adesc =
+                            sw128_desc(smem_u32(sA + stage * C::kAB + ms * kABytes));
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            mma_f16(d_tmem + (uint32_t)(ms * BN), adesc + 2u * k, bdesc + 2u * k,
+                                    idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+                    }
                     mma_commit(empty_bar(stage));  // frees the slot once these MMAs finish
                     if (++stage == S) {
                         stage = 0;
@@ -500,6 +532,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (p.part) {
+        // ---------------------------------------------------- epilogue warps, split-K
+        // Raw fp32 accumulators of this unit's K range go to the partial-sum
+        // buffer; the reduce kernel adds the splits and applies bias,
+        // activation, residual and the down-cast.
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int row = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int unit = blockIdx.x; unit < num_tiles; unit += gridDim.x) {
+            const int tile = unit / p.splits, split = unit - tile * p.splits;
+            const int m0 = (tile / p.num_n_tiles) * TM;
+            const int n0 = (tile % p.num_n_tiles) * BN;
+            const bool ok = __all_sync(0xffffffffu, wait_phase(tfull_bar(acc), acc_phase, abort_flag, p));
+            if (!ok) break;
+            tc_fence_after();
+            const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
+            for (int i = half; i < MS * nch; i += 2) {
+                const int ms = i / nch, c = (i - ms * nch) * 32;
+                const int m = m0 + ms * BM + row;
+                float v[32];
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
+                              (uint32_t)(acc * MS * BN + ms * BN + c),
+                          v);
+                if (m < p.M) {
+                    float* dst = p.part + ((long long)split * p.M + m) * p.C_out + n0 + c;
+#pragma unroll
+                    for (int g = 0; g < 32; g += 4)
+                        if (n0 + c + g < p.C_out)
+                            *reinterpret_cast<float4*>(dst + g) =
+                                make_float4(v[g], v[g + 1], v[g + 2], v[g + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
     } else if (p.out_layout == ACNN_NHWC) {
         // ---------------------------------------------------- epilogue warps, NHWC
         // Warp e (0..7) owns the 32 rows of its TMEM lane quarter (warp % 4) and
@@ -525,28 +597,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar, kStageBytes);
             tma_load_2d(smem_u32(rst + buf * kStageBytes), &tmap_r, bar, c0, r0);
         };
-        for (int tile = blockIdx.x; !aborted && tile < num_tiles; tile += gridDim.x) {
-            const int m0 = (tile / p.num_n_tiles) * BM;
+        for (int tile = blockIdx.x; !aborted && tile < num_tiles; tile += gridDim.x) {  // splits == 1
+            const int m0 = (tile / p.num_n_tiles) * TM;
             const int n0 = (tile % p.num_n_tiles) * BN;
-            const int row0 = m0 + q * 32;
             const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
-            if (has_res && half < nch) {
-                if (lane == 0) issue_res(rb, n0 + half * 32, row0);
+            const int nchunks = MS * nch;  // chunk i: row block i / nch, channels (i % nch) * 32
+            auto chunk_row = [&](int i) { return m0 + (i / nch) * BM + q * 32; };
+            auto chunk_col = [&](int i) { return n0 + (i % nch) * 32; };
+            if (has_res && half < nchunks) {
+                if (lane == 0) issue_res(rb, chunk_col(half), chunk_row(half));
                 r_inflight |= 1u << rb;
             }
             const bool ok = __all_sync(0xffffffffu, wait_phase(tfull_bar(acc), acc_phase, abort_flag, p));
             if (!ok) break;
             tc_fence_after();
-            for (int i = half; i < nch; i += 2) {
-                const int c = i * 32;
-                if (has_res && i + 2 < nch) {
-                    if (lane == 0) issue_res(rb ^ 1, n0 + c + 64, row0);
+            for (int i = half; i < nchunks; i += 2) {
+                const int ms = i / nch, c = (i - ms * nch) * 32;
+                const int row0 = m0 + ms * BM + q * 32;
+                if (has_res && i + 2 < nchunks) {
+                    if (lane == 0) issue_res(rb ^ 1, chunk_col(i + 2), chunk_row(i + 2));
                     r_inflight |= 1u << (rb ^ 1);
                 }
                 float bv[32], av[32];
                 load_chunk_params(p.bias, p.alpha, prelu, n0 + c, p.C_out, bv, av);
                 float v[32];
-                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), v);
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
+                              (uint32_t)(acc * MS * BN + ms * BN + c),
+                          v);
                 float r[32];
                 if (has_res) {
                     const bool okr = __all_sync(
@@ -618,21 +695,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float kpost = p.res_mode == ACNN_RES_ACT_THEN_ADD ? 1.f : 0.f;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const int m0 = (tile / p.num_n_tiles) * BM;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {  // splits == 1
+            const int m0 = (tile / p.num_n_tiles) * TM;
             const int n0 = (tile % p.num_n_tiles) * BN;
             // every lane waits (acquiring the accumulator); the warp then agrees,
             // so the warp-collective TMEM loads below run converged or not at all
             const bool ok = __all_sync(0xffffffffu, wait_phase(tfull_bar(acc), acc_phase, abort_flag, p));
             if (!ok) break;
             tc_fence_after();
-            const int m = m0 + row;
-            const bool valid = m < p.M;
-            const int img = m / p.OHW;
-            const long long base = (long long)img * p.C_out * p.OHW + (m - img * p.OHW);
             const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
-            for (int i = half; i < nch; i += 2) {
-                const int c = i * 32;
+            for (int i = half; i < MS * nch; i += 2) {
+                const int ms = i / nch, c = (i - ms * nch) * 32;
+                const int m = m0 + ms * BM + row;
+                const bool valid = m < p.M;
+                const int img = m / p.OHW;
+                const long long base = (long long)img * p.C_out * p.OHW + (m - img * p.OHW);
                 float bv[32], av[32], r[32], o[32], v[32];
                 load_chunk_params(p.bias, p.alpha, prelu, n0 + c, p.C_out, bv, av);
 #pragma unroll
@@ -640,7 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     r[j] = (has_res && valid && n0 + c + j < p.C_out)
                                ? to_f32(res[base + (long long)(n0 + c + j) * p.OHW])
                                : 0.f;
-                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), v);
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
+                              (uint32_t)(acc * MS * BN + ms * BN + c),
+                          v);
                 epi32_any(p.act, v, bv, av, r, kpre, kpost, o);
                 if (valid) {
 #pragma unroll
@@ -663,6 +742,108 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
     }
+}
+
+// ---------------------------------------------------------------- split-K reduce
+// y = act(sum_s part[s] + bias + kpre*res) + kpost*res, cast to the storage
+// type.  One thread per output pixel and 8 channels; NHWC walks channels
+// fastest (16-byte stores), NCHW walks pixels fastest (coalesced planes).
+template <int ACT, typename T>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(
+    const float* __restrict__ part, int splits, int M, int C_out, int OHW, int out_layout,
+    const float* __restrict__ bias, const float* __restrict__ alpha, const T* __restrict__ res,
+    int res_mode, T* __restrict__ y) {
+    const int G = C_out / 8;
+    const long long total = (long long)M * G;
+    const float kpre = res_mode == ACNN_RES_ADD_THEN_ACT ? 1.f : 0.f;
+    const float kpost = res_mode == ACNN_RES_ACT_THEN_ADD ? 1.f : 0.f;
+    const long long plane = (long long)M * C_out;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        int m, g;
+        if (out_layout == ACNN_NHWC) {
+            m = (int)(i / G);
+            g = (int)(i - (long long)m * G);
+        } else {
+            g = (int)(i / M);
+            m = (int)(i - (long long)g * M);
+        }
+        const int n = g * 8;
+        const float* src = part + (long long)m * C_out + n;
+        float acc[8];
+        {
+            const float4 a = *reinterpret_cast<const float4*>(src);
+            const float4 b = *reinterpret_cast<const float4*>(src + 4);
+            acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+            acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+        }
+        for (int s = 1; s < splits; ++s) {
+            const float4 a = *reinterpret_cast<const float4*>(src + s * plane);
+            const float4 b = *reinterpret_cast<const float4*>(src + s * plane + 4);
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
+        float r[8], o[8];
+        long long oi[8];
+        if (out_layout == ACNN_NHWC) {
+            const long long base = (long long)m * C_out + n;
+            if (res_mode != ACNN_RES_NONE) {
+                const Vec<T, 8> rv = *reinterpret_cast<const Vec<T, 8>*>(res + base);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) r[j] = to_f32(rv.v[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) r[j] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) oi[j] = base + j;
+        } else {
+            const int img = m / OHW;
+            const long long base = (long long)img * C_out * OHW + (m - img * OHW);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                oi[j] = base + (long long)(n + j) * OHW;
+                r[j] = res_mode != ACNN_RES_NONE ? to_f32(res[oi[j]]) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float bv = bias ? __ldg(bias + n + j) : 0.f;
+            const float av = ACT == ACNN_ACT_PRELU ? __ldg(alpha + n + j) : 0.f;
+            o[j] = fmaf(kpost, r[j], act_fixed<ACT>(fmaf(kpre, r[j], acc[j] + bv), av));
+        }
+        if (out_layout == ACNN_NHWC) {
+            Vec<T, 8> ov;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ov.v[j] = from_f32<T>(o[j]);
+            *reinterpret_cast<Vec<T, 8>*>(y + oi[0]) = ov;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) y[oi[j]] = from_f32<T>(o[j]);
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_reduce(const ConvArgs& a, const IgemmPlan& pl, long long M, cudaStream_t s) {
+    const long long work = M * (a.d.c_out / 8);
+    const int grid = grid_for(work, 256);
+    const float* part = static_cast<const float*>(a.ws_part);
+    const T* res = static_cast<const T*>(a.residual);
+    T* y = static_cast<T*>(a.y);
+    const int OHW = a.oh * a.ow;
+#define ACNN_REDUCE(ACT)                                                                     \
+    splitk_reduce_kernel<ACT, T><<<grid, 256, 0, s>>>(part, pl.splits, (int)M, a.d.c_out, OHW, \
+                                                      a.out_layout, a.bias, a.alpha, res,    \
+                                                      a.res_mode, y)
+    switch (a.act) {
+    case ACNN_ACT_RELU: ACNN_REDUCE(ACNN_ACT_RELU); break;
+    case ACNN_ACT_SILU: ACNN_REDUCE(ACNN_ACT_SILU); break;
+    case ACNN_ACT_PRELU: ACNN_REDUCE(ACNN_ACT_PRELU); break;
+    default: ACNN_REDUCE(ACNN_ACT_NONE); break;
+    }
+#undef ACNN_REDUCE
+    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- host side
@@ -690,11 +871,11 @@ struct Maps {
     CUtensorMap a, b, y, r;
 };
 
-template <int BN, typename T>
+template <int BN, int MS, typename T>
 int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, MS>;
     static bool attr_set = false;  // per instantiation; set once per process
-    auto kern = igemm_conv_kernel<BN, T>;
+    auto kern = igemm_conv_kernel<BN, MS, T>;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::kSmem) != cudaSuccess)
@@ -702,17 +883,19 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
         attr_set = true;
     }
     prm.num_n_tiles = (a.d.c_out + BN - 1) / BN;
-    const int tiles = prm.num_m_tiles * prm.num_n_tiles;
+    const int tiles = prm.num_m_tiles * prm.num_n_tiles * prm.splits;
     const int grid = tiles < sm_count() ? tiles : sm_count();
     kern<<<grid, kThreads, C::kSmem, s>>>(m.a, m.b, m.y, m.r, prm);
     return cudaGetLastError() == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
 }
 
 template <typename T>
-int launch_typed(const ConvArgs& a, int bn, const Maps& m, const Params& prm, cudaStream_t s) {
-    if (bn == 256) return launch_bn<256, T>(a, m, prm, s);
-    if (bn == 128) return launch_bn<128, T>(a, m, prm, s);
-    return launch_bn<64, T>(a, m, prm, s);
+int launch_typed(const ConvArgs& a, int bn, int ms, const Maps& m, const Params& prm,
+                 cudaStream_t s) {
+    if (bn == 256) return launch_bn<256, 1, T>(a, m, prm, s);
+    if (bn == 128) return ms == 2 ? launch_bn<128, 2, T>(a, m, prm, s)
+                                  : launch_bn<128, 1, T>(a, m, prm, s);
+    return ms == 2 ? launch_bn<64, 2, T>(a, m, prm, s) : launch_bn<64, 1, T>(a, m, prm, s);
 }
 
 // [M, C_out] NHWC output (or residual) viewed 2-D, 32 x 32 boxes, 64-byte swizzle.
@@ -727,16 +910,55 @@ CUresult encode_out_map(CUtensorMap* map, CUtensorMapDataType dt, const void* pt
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-// Output-channel tile: the widest of 256/128/64 that C_out fills, narrowed
-// while the tile count leaves most SMs idle.
-int pick_bn(int c_out, int num_m_tiles) {
-    int bn = c_out >= 256 ? 256 : (c_out > 64 ? 128 : 64);
-    const int sms = sm_count();
-    while (bn > 64 && (long long)num_m_tiles * ((c_out + bn - 1) / bn) < sms) bn >>= 1;
-    return bn;
-}
-
 }  // namespace
+
+// Tile width and K split from a small cost model of one launch, in
+// microseconds: every unit (tile x K range) streams its k-blocks at the
+// slower of the producer's per-k-block issue cost (~0.3 us: the barrier wait,
+// expect-tx and two TMA issues of one thread) and the MMA time of the block;
+// units run in waves of one per SM; the layer cannot beat its HBM traffic;
+// split-K adds a reduce launch that reads the fp32 partials and writes y.
+IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget) {
+    const double kIssueUs = 0.30, kMmaUsPerMflop = 1.0 / 15.0, kHbmBytesPerUs = 6.0e6;
+    const double kLaunchUs = 3.0, kEpiUsPerChunk = 0.15;
+    const long long M = (long long)d.n * oh * ow;
+    const int num_kb = d.kh * d.kw * ((d.c_in + BK - 1) / BK);
+    const int sms = sm_count();
+    const double io_bytes = 2.0 * ((double)d.n * d.h * d.w * d.c_in + (double)M * d.c_out +
+                                   (double)d.c_out * d.kh * d.kw * d.c_in);
+    IgemmPlan best{64, 1, 1, num_kb, 0}, best1{64, 1, 1, num_kb, 0};
+    double best_cost = 1e30, best1_cost = 1e30;
+    const int bn0 = d.c_out >= 256 ? 256 : (d.c_out > 64 ? 128 : 64);
+    for (int bn = bn0; bn >= 64; bn >>= 1) {
+        for (int ms = 1; ms <= (bn == 256 ? 1 : 2); ++ms) {  // TMEM: 2 * ms * bn <= 512
+            const long long mt = (M + BM * ms - 1) / (BM * ms);
+            const long long tiles = mt * ((d.c_out + bn - 1) / bn);
+            const double t_kb = fmax(kIssueUs, 2.0 * BM * ms * bn * BK * 1e-6 * kMmaUsPerMflop);
+            for (int sp = 1; sp <= 16 && sp <= num_kb; ++sp) {
+                const int kbs = (num_kb + sp - 1) / sp;
+                const int eff = (num_kb + kbs - 1) / kbs;  // splits actually used
+                if (eff != sp) continue;
+                const size_t part = eff > 1 ? (size_t)eff * M * d.c_out * sizeof(float) : 0;
+                if (part > part_budget) continue;
+                const long long units = tiles * eff;
+                const long long waves = (units + sms - 1) / sms;
+                double cost = waves * kbs * t_kb + ms * (bn / 64.0) * kEpiUsPerChunk * 2.0;
+                cost = fmax(cost, io_bytes / kHbmBytesPerUs);
+                if (eff > 1) cost += kLaunchUs + (double)part * 2.0 / kHbmBytesPerUs;
+                if (cost < best_cost * 0.97) {  // prefer wide, short tiles and no split on ties
+                    best_cost = cost;
+                    best = IgemmPlan{bn, ms, eff, kbs, part};
+                }
+                if (eff == 1 && cost < best1_cost * 0.97) {
+                    best1_cost = cost;
+                    best1 = IgemmPlan{bn, ms, 1, kbs, 0};
+                }
+            }
+        }
+    }
+    // split only for a clear gain: the reduce adds a launch and its latency
+    return best.splits > 1 && best_cost > 0.8 * best1_cost ? best1 : best;
+}
 
 int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     const acnn_conv_desc& d = a.d;
@@ -746,6 +968,7 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     const CUtensorMapDataType dt =
         d.dtype == ACNN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const bool tiled = d.kh == 1 && d.kw == 1 && d.stride == 1 && d.pad == 0;
+    const IgemmPlan plan = igemm_plan(d, a.oh, a.ow, a.ws_part ? a.ws_part_bytes : 0);
 
     alignas(64) Maps maps;
     CUtensorMap& ta = maps.a;
@@ -754,7 +977,7 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     if (tiled) {
         cuuint64_t dims[2] = {(cuuint64_t)d.c_in, (cuuint64_t)M};
         cuuint64_t strides[1] = {(cuuint64_t)d.c_in * 2};
-        cuuint32_t box[2] = {BK, BM};
+        cuuint32_t box[2] = {BK, (cuuint32_t)(BM * plan.ms)};
         cuuint32_t es[2] = {1, 1};
         r = g_encode_tiled(&ta, dt, 2, const_cast<void*>(a.x), dims, strides, box, es,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -768,13 +991,14 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
         int upper[2] = {d.pad - (d.kw - 1), d.pad - (d.kh - 1)};
         cuuint32_t es[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
         r = g_encode_im2col(&ta, dt, 4, const_cast<void*>(a.x), dims, strides, lower, upper, BK,
-                            BM, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            BM * plan.ms, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
 
-    const int num_m_tiles = (int)((M + BM - 1) / BM);
-    const int bn = pick_bn(d.c_out, num_m_tiles);
+    const int num_m_tiles = (int)((M + BM * plan.ms - 1) / (BM * plan.ms));
+    const int bn = plan.bn;
     {
         cuuint64_t dims[3] = {(cuuint64_t)d.c_in, (cuuint64_t)taps, (cuuint64_t)d.c_out};
         cuuint64_t strides[2] = {(cuuint64_t)d.c_in * 2, (cuuint64_t)taps * d.c_in * 2};
@@ -805,6 +1029,9 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     prm.kb_per_tap = (d.c_in + BK - 1) / BK;
     prm.num_kb = taps * prm.kb_per_tap;
     prm.num_m_tiles = num_m_tiles;
+    prm.splits = plan.splits;
+    prm.kb_per_split = plan.kb_per_split;
+    prm.part = plan.splits > 1 ? static_cast<float*>(a.ws_part) : nullptr;
     prm.OW = a.ow;
     prm.OHW = a.oh * a.ow;
     prm.S = d.stride;
@@ -820,8 +1047,13 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     prm.status = device_status_ptr();
     prm.budget = wait_budget_polls();
     if (!prm.status) return ACNN_ERR_CUDA;
-    if (d.dtype == ACNN_BF16) return launch_typed<__nv_bfloat16>(a, bn, maps, prm, s);
-    return launch_typed<__half>(a, bn, maps, prm, s);
+    const bool bf16 = d.dtype == ACNN_BF16;
+    int st = bf16 ? launch_typed<__nv_bfloat16>(a, bn, plan.ms, maps, prm, s)
+                  : launch_typed<__half>(a, bn, plan.ms, maps, prm, s);
+    if (st != ACNN_OK || plan.splits == 1) return st;
+    const cudaError_t e = bf16 ? launch_reduce<__nv_bfloat16>(a, plan, M, s)
+                               : launch_reduce<__half>(a, plan, M, s);
+    return e == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
 }
 
 }  // namespace acnn

@@ -28,10 +28,10 @@ __global__ void __launch_bounds__(kThreads) pool_nhwc_kernel(
     const int CV = C / V;
     const long long total = (long long)N * OH * OW * CV;
     const float inv = 1.0f / (float)(K * K);
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)total;
+         i += gridDim.x * blockDim.x) {
         int cv = (int)(i % CV);
-        long long p = i / CV;
+        uint32_t p = i / CV;
         int ox = (int)(p % OW);
         p /= OW;
         int oy = (int)(p % OH);
@@ -67,19 +67,95 @@ __global__ void __launch_bounds__(kThreads) pool_nhwc_kernel(
     }
 }
 
+// 3x3/s2/p1 max-pool, NHWC (the stem's pool): all nine taps are loaded before
+// any is compared (addresses clamped into the image, out-of-image taps then
+// masked), so a thread keeps nine 16-byte loads in flight; the comparison
+// order and the strictly-greater rule are those of the generic kernel.
+template <typename T, int V>
+__global__ void __launch_bounds__(kThreads) maxpool3s2_nhwc_kernel(
+    const T* __restrict__ x, T* __restrict__ y, int N, int H, int W, int C, int OH, int OW) {
+    const int CV = C / V;
+    const long long total = (long long)N * OH * OW * CV;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)total;
+         i += gridDim.x * blockDim.x) {
+        const int cv = (int)(i % CV);
+        uint32_t p = i / CV;
+        const int ox = (int)(p % OW);
+        p /= OW;
+        const int oy = (int)(p % OH);
+        const int n = (int)(p / OH);
+        const T* img = x + (long long)n * H * W * C + (long long)cv * V;
+        Vec<T, V> t[9];
+        bool ok[9];
+#pragma unroll
+        for (int dy = 0; dy < 3; ++dy)
+#pragma unroll
+            for (int dx = 0; dx < 3; ++dx) {
+                const int iy = 2 * oy - 1 + dy, ix = 2 * ox - 1 + dx;
+                ok[dy * 3 + dx] = iy >= 0 && iy < H && ix >= 0 && ix < W;
+                const int iyc = min(max(iy, 0), H - 1), ixc = min(max(ix, 0), W - 1);
+                t[dy * 3 + dx] = *reinterpret_cast<const Vec<T, V>*>(
+                    img + ((long long)iyc * W + ixc) * C);
+            }
+        float best[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) best[v] = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 9; ++k)
+            if (ok[k]) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const float f = to_f32(t[k].v[v]);
+                    if (f > best[v]) best[v] = f;
+                }
+            }
+        Vec<T, V> o;
+#pragma unroll
+        for (int v = 0; v < V; ++v) o.v[v] = from_f32<T>(best[v]);
+        *reinterpret_cast<Vec<T, V>*>(y + (((long long)n * OH + oy) * OW + ox) * C +
+                                      (long long)cv * V) = o;
+    }
+}
+
+// Nearest 2x, NHWC: one thread per input pixel and 16-byte channel vector,
+// one load and the four stores of its 2x2 output block.
+template <typename T, int V>
+__global__ void __launch_bounds__(kThreads) up2_nhwc_kernel(const T* __restrict__ x,
+                                                            T* __restrict__ y, int N, int H,
+                                                            int W, int C) {
+    const int CV = C / V;
+    const long long total = (long long)N * H * W * CV;
+    const int OW = 2 * W;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)total;
+         i += gridDim.x * blockDim.x) {
+        const int cv = (int)(i % CV);
+        uint32_t p = i / CV;
+        const int ix = (int)(p % W);
+        p /= W;
+        const int iy = (int)(p % H);
+        const int n = (int)(p / H);
+        const Vec<T, V> t = *reinterpret_cast<const Vec<T, V>*>(x + (long long)i * V);
+        T* o = y + (((long long)n * 2 * H + 2 * iy) * OW + 2 * ix) * C + (long long)cv * V;
+        *reinterpret_cast<Vec<T, V>*>(o) = t;
+        *reinterpret_cast<Vec<T, V>*>(o + C) = t;
+        *reinterpret_cast<Vec<T, V>*>(o + (long long)OW * C) = t;
+        *reinterpret_cast<Vec<T, V>*>(o + (long long)OW * C + C) = t;
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) pool_nchw_kernel(
     const T* __restrict__ x, T* __restrict__ y, int kind, int N, int C, int H, int W, int OH,
     int OW, int K, int S, int P) {
     const long long total = (long long)N * C * OH * OW;
     const float inv = 1.0f / (float)(K * K);
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)total;
+         i += gridDim.x * blockDim.x) {
         int ox = (int)(i % OW);
-        long long p = i / OW;
+        uint32_t p = i / OW;
         int oy = (int)(p % OH);
-        long long nc = p / OH;
-        const T* plane = x + nc * H * W;
+        const uint32_t nc = p / OH;
+        const T* plane = x + (long long)nc * H * W;
         float acc = kind == ACNN_POOL_MAX ? -INFINITY : 0.0f;
         for (int dy = 0; dy < K; ++dy) {
             int iy = oy * S + dy - P;
@@ -130,10 +206,10 @@ __global__ void __launch_bounds__(kThreads) resize_nhwc_kernel(
     int OW, float sy, float sx) {
     const int CV = C / V;
     const long long total = (long long)N * OH * OW * CV;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)total;
+         i += gridDim.x * blockDim.x) {
         int cv = (int)(i % CV);
-        long long p = i / CV;
+        uint32_t p = i / CV;
         int ox = (int)(p % OW);
         p /= OW;
         int oy = (int)(p % OH);
@@ -169,13 +245,13 @@ __global__ void __launch_bounds__(kThreads) resize_nchw_kernel(
     const Ti* __restrict__ x, To* __restrict__ y, int mode, int NC, int H, int W, int OH, int OW,
     float sy, float sx) {
     const long long total = (long long)NC * OH * OW;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)total;
+         i += gridDim.x * blockDim.x) {
         int ox = (int)(i % OW);
-        long long p = i / OW;
+        uint32_t p = i / OW;
         int oy = (int)(p % OH);
-        long long nc = p / OH;
-        const Ti* plane = x + nc * H * W;
+        const uint32_t nc = p / OH;
+        const Ti* plane = x + (long long)nc * H * W;
         float v;
         if (mode == ACNN_RESIZE_NEAREST) {
             int iy = (int)(((long long)oy * H) / OH);
@@ -203,15 +279,32 @@ template <typename T, int V>
 __global__ void __launch_bounds__(kThreads) concat_kernel(
     const T* __restrict__ a, const T* __restrict__ b, T* __restrict__ y, long long runs,
     int ra, int rb) {
-    const int rv = (ra + rb) / V;
-    const long long total = runs * rv;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        long long run = i / rv;
-        int e = (int)(i % rv) * V;
-        const T* src = e < ra ? a + run * ra + e : b + run * rb + (e - ra);
-        *reinterpret_cast<Vec<T, V>*>(y + run * (ra + rb) + e) =
-            *reinterpret_cast<const Vec<T, V>*>(src);
+    // four independent vectors per thread per round keep more bytes in flight
+    constexpr int U = 4;
+    const uint32_t rv = (uint32_t)((ra + rb) / V);
+    const uint32_t total = (uint32_t)(runs * rv);
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += stride * U) {
+        Vec<T, V> t[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t i = i0 + u * stride;
+            if (i < total) {
+                const uint32_t run = i / rv;
+                const int e = (int)(i - run * rv) * V;
+                const T* src = e < ra ? a + (long long)run * ra + e : b + (long long)run * rb + (e - ra);
+                t[u] = *reinterpret_cast<const Vec<T, V>*>(src);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t i = i0 + u * stride;
+            if (i < total) {
+                const uint32_t run = i / rv;
+                const int e = (int)(i - run * rv) * V;
+                *reinterpret_cast<Vec<T, V>*>(y + (long long)run * (ra + rb) + e) = t[u];
+            }
+        }
     }
 }
 
@@ -227,8 +320,8 @@ __global__ void __launch_bounds__(kThreads) prep_quarter_kernel(
     int W, float t) {
     const int QH = H / 4, QW = W / 4;
     const long long P = (long long)QH * QW;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < P;
-         i += (long long)gridDim.x * blockDim.x) {
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)P;
+         i += gridDim.x * blockDim.x) {
         int qx = (int)(i % QW), qy = (int)(i / QW);
         BilinearTap ty = bilinear_tap(qy, 4.0f, H), tx = bilinear_tap(qx, 4.0f, W);
 #pragma unroll
@@ -264,10 +357,10 @@ __global__ void __launch_bounds__(kThreads) deconv_kernel(
     const long long pix = (long long)N * OH * OW;
     const int co_blocks = (CO + kDeconvCoBlock - 1) / kDeconvCoBlock;
     const long long total = pix * co_blocks;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        int cb = (int)(i / pix);
-        long long q = i % pix;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)total;
+         i += gridDim.x * blockDim.x) {
+        int cb = (int)(i / (uint32_t)pix);
+        uint32_t q = i - (uint32_t)cb * (uint32_t)pix;
         int ox = (int)(q % OW);
         q /= OW;
         int oy = (int)(q % OH);
@@ -308,6 +401,64 @@ __global__ void __launch_bounds__(kThreads) deconv_kernel(
 }
 
 // ----------------------------------------------------------------------------
+// im2col pack for convs with few input channels (rtdetr_gpu.rs IM2COL_SRC:
+// row m = output pixel, k = (ky, kx, ci), taps outside the input are zero),
+// padded with zeros from K = kh*kw*C to Kp (a multiple of 8) so that rows are
+// 16-byte aligned for the tensor-core GEMM.  Values are copied as raw 16-bit
+// patterns.  One thread per output pixel and group of 8 k.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) im2col_pack_kernel(
+    const uint16_t* __restrict__ x, uint16_t* __restrict__ a, int layout, int N, int H, int W,
+    int C, int KH, int KW, int S, int P, int OH, int OW, int Kp) {
+    const int KG = Kp / 8, K = KH * KW * C;
+    const uint32_t total = (uint32_t)N * OH * OW * KG;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += gridDim.x * blockDim.x) {
+        const uint32_t m = i / KG;
+        const int g = (int)(i - m * KG);
+        const int ox = (int)(m % OW);
+        const uint32_t t = m / OW;
+        const int oy = (int)(t % OH), n = (int)(t / OH);
+        Vec<uint16_t, 8> v;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int k = g * 8 + j;
+            uint16_t val = 0;
+            if (k < K) {
+                const int tap = k / C, ci = k - tap * C;
+                const int ky = tap / KW, kx = tap - ky * KW;
+                const int iy = oy * S + ky - P, ix = ox * S + kx - P;
+                if (iy >= 0 && iy < H && ix >= 0 && ix < W)
+                    val = x[act_index(layout, C, H, W, n, ci, iy, ix)];
+            }
+            v.v[j] = val;
+        }
+        *reinterpret_cast<Vec<uint16_t, 8>*>(a + (long long)m * Kp + g * 8) = v;
+    }
+}
+
+// Weights to the packed K order: wp[co][k], k = (ky, kx, ci), zero for k >= K;
+// from OHWI (NHWC convs) or OIHW (NCHW convs).
+__global__ void __launch_bounds__(kThreads) weight_pack_kernel(
+    const uint16_t* __restrict__ w, uint16_t* __restrict__ wp, int layout, int C_out, int C,
+    int KH, int KW, int Kp) {
+    const int K = KH * KW * C;
+    const uint32_t total = (uint32_t)C_out * Kp;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += gridDim.x * blockDim.x) {
+        const int co = (int)(i / Kp), k = (int)(i - (uint32_t)co * Kp);
+        uint16_t val = 0;
+        if (k < K) {
+            const int tap = k / C, ci = k - tap * C;
+            const int ky = tap / KW, kx = tap - ky * KW;
+            val = layout == ACNN_NHWC ? w[(((long long)co * KH + ky) * KW + kx) * C + ci]
+                                      : w[(((long long)co * C + ci) * KH + ky) * KW + kx];
+        }
+        wp[i] = val;
+    }
+}
+
+// ----------------------------------------------------------------------------
 // NCHW -> NHWC transpose of 16-bit elements through a 32x32 shared tile:
 // per image, [C][HW] -> [HW][C].  Reads and writes are both coalesced.
 // ----------------------------------------------------------------------------
@@ -339,7 +490,11 @@ cudaError_t pool_typed(int kind, int n, int h, int w, int c, int k, int stride, 
     T* yt = static_cast<T*>(y);
     if (layout == ACNN_NHWC) {
         constexpr int V = 16 / sizeof(T);
-        if (c % V == 0) {
+        if (c % V == 0 && kind == ACNN_POOL_MAX && k == 3 && stride == 2 && pad == 1) {
+            long long work = (long long)n * oh * ow * (c / V);
+            maxpool3s2_nhwc_kernel<T, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+                xt, yt, n, h, w, c, oh, ow);
+        } else if (c % V == 0) {
             long long work = (long long)n * oh * ow * (c / V);
             pool_nhwc_kernel<T, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(
                 xt, yt, kind, n, h, w, c, oh, ow, k, stride, pad);
@@ -364,6 +519,14 @@ cudaError_t resize_typed(int mode, int n, int c, int h, int w, int oh, int ow, i
     float sy = (float)h / (float)oh, sx = (float)w / (float)ow;
     if (layout == ACNN_NHWC) {
         constexpr int V = (16 / sizeof(Ti)) < (16 / sizeof(To)) ? (16 / sizeof(Ti)) : (16 / sizeof(To));
+        if constexpr (sizeof(Ti) == sizeof(To)) {
+            if (mode == ACNN_RESIZE_NEAREST && oh == 2 * h && ow == 2 * w && c % V == 0) {
+                long long work = (long long)n * h * w * (c / V);
+                up2_nhwc_kernel<Ti, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+                    xt, reinterpret_cast<Ti*>(yt), n, h, w, c);
+                return cudaGetLastError();
+            }
+        }
         if (c % V == 0) {
             long long work = (long long)n * oh * ow * (c / V);
             resize_nhwc_kernel<Ti, To, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(
@@ -498,6 +661,20 @@ cudaError_t launch_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_
             f0, f1, static_cast<__nv_bfloat16*>(y), h, w, t);
         break;
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, const void* x,
+                               void* a, const void* w, void* wp, cudaStream_t s) {
+    const long long work = (long long)d.n * oh * ow * (kp / 8);
+    im2col_pack_kernel<<<grid_for(work, kThreads), kThreads, 0, s>>>(
+        static_cast<const uint16_t*>(x), static_cast<uint16_t*>(a), d.layout, d.n, d.h, d.w,
+        d.c_in, d.kh, d.kw, d.stride, d.pad, oh, ow, kp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    weight_pack_kernel<<<grid_for((long long)d.c_out * kp, kThreads), kThreads, 0, s>>>(
+        static_cast<const uint16_t*>(w), static_cast<uint16_t*>(wp), d.layout, d.c_out, d.c_in,
+        d.kh, d.kw, kp);
     return cudaGetLastError();
 }
 

@@ -339,14 +339,15 @@ def oracle_sample(workload, kind):
     O.build()
     if workload != "backbone":
         raise SystemExit("the oracle baseline is implemented for the backbone workload")
-    # cpu_baseline: one full 640x640 image (1/8 of a step); reference steps: a 160x160
-    # image, i.e. 1/16 of one image's conv work (every op scales with the pixel count)
-    side = 640 if kind == "baseline" else 160
-    x = G.tensor(1238, "x", (1, side, side, 3), "uniform", 0.0, 1.0, dtype=G.BF16)
+    # cpu_baseline: three full 640x640 images (3/8 of a step, ~10 s on 16 cores);
+    # reference steps: one 160x160 image, i.e. 1/16 of one image's conv work (every
+    # op scales with the pixel count)
+    side, n = (640, 3) if kind == "baseline" else (160, 1)
+    x = G.tensor(1238, "x", (n, side, side, 3), "uniform", 0.0, 1.0, dtype=G.BF16)
     x64 = x.to(torch.float64).numpy()
-    frac = (side * side) / (640 * 640)
-    desc = (f"oracle backbone+neck forward (fp64, bf16 storage emulation) on one "
-            f"{side}x{side}x3 image = {frac:g} of one image's work, {O.nthreads()} threads")
+    frac = n * (side * side) / (640 * 640)
+    desc = (f"oracle backbone+neck forward (fp64, bf16 storage emulation) on {n} "
+            f"{side}x{side}x3 image(s) = {frac:g} of one image's work, {O.nthreads()} threads")
     return (lambda: M.backbone(x64)), frac, desc
 
 

@@ -22,7 +22,8 @@
  * activations -- so that the GEMM reduction index k runs over (ky, kx, ci), the
  * order of rtdetr_gpu.rs IM2COL_SRC -- and OIHW for NCHW activations, the
  * [CO, CI, 3, 3] order of rt.js wgslConv.  Bias and PReLU alpha are always
- * fp32, as in rt.js wgslConv.
+ * fp32, as in rt.js wgslConv.  The companion ops index elements with 32 bits:
+ * a tensor of 2^31 elements or more returns ACNN_ERR_TOO_LARGE.
  *
  * Alignment.  Device pointers must be 16-byte aligned (the tensor path reads
  * through TMA, which requires it); misaligned pointers return
@@ -99,10 +100,17 @@ typedef struct {
  *   alpha      device fp32 [c_out]; required iff act == ACNN_ACT_PRELU
  *   residual   device, same shape/layout/dtype as y; required iff res_mode != NONE
  *   y          device output [n,oh,ow,c_out] or [n,c_out,oh,ow]
- *   workspace  device scratch of at least acnn_conv2d_workspace_size(d) bytes
- *              (NULL allowed when that size is 0); contents are clobbered
- * The tensor-core path runs for fp16/bf16 with c_in % 8 == 0, c_out % 16 == 0
- * and square kernels; every other valid geometry runs the direct FFMA kernel.
+ *   workspace  device scratch (contents clobbered), ws_bytes long.  Required:
+ *              room for NHWC copies of x and w (NCHW calls on paths 1-2) or
+ *              for the packed im2col matrix and weights (path 3).  Beyond
+ *              that, up to acnn_conv2d_workspace_size(d) bytes let the
+ *              tensor cores split K across more SMs (fewer bytes select fewer
+ *              splits; NULL / 0 bytes is valid when nothing is required).
+ * fp16/bf16 convs with c_out % 8 == 0 run on the tensor cores: x is read by
+ * TMA (tiled for 1x1/s1/p0, im2col otherwise) when c_in % 8 == 0 and the
+ * kernel is square; other such convs whose kh*kw*c_in is at most 512 are first
+ * packed into an explicit im2col matrix in the workspace.  Every other valid
+ * geometry (fp32 storage included) runs the direct FFMA kernel.
  */
 int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w,
                       const float* bias, const float* alpha, const void* residual,
@@ -112,13 +120,22 @@ int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w,
 /* Output height and width of a conv with geometry d (host pointers). */
 int acnn_conv2d_out_hw(const acnn_conv_desc* d, int* oh, int* ow);
 
-/* Bytes of workspace acnn_conv2d_fused needs for geometry d (0 for NHWC). */
+/* Bytes of workspace for the fastest plan of geometry d: the staging copies
+ * (required) plus split-K partial sums (optional). 0 when neither applies. */
 size_t acnn_conv2d_workspace_size(const acnn_conv_desc* d);
 
 /* Which kernel acnn_conv2d_fused would run for d: 0 = direct FFMA,
  * 1 = tcgen05 implicit GEMM with a tiled A load (1x1/s1/p0),
- * 2 = tcgen05 implicit GEMM with TMA im2col A loads; negative = invalid. */
+ * 2 = tcgen05 implicit GEMM with TMA im2col A loads,
+ * 3 = explicit im2col pack, then the tcgen05 GEMM; negative = invalid. */
 int acnn_conv2d_path(const acnn_conv_desc* d);
+
+/* Tensor-core plan for d given ws_bytes of workspace: output pixels per tile
+ * (*rows: 128/256), output channels per tile (*bn: 64/128/256) and K splits
+ * (*splits, 1 = none).  Returns 0, or -1 when d does not take the tensor-core
+ * path or ws_bytes is below the required staging (host pointers; the plan
+ * depends on the current device's SM count). */
+int acnn_conv2d_plan(const acnn_conv_desc* d, size_t ws_bytes, int* rows, int* bn, int* splits);
 
 /* ---- conv2d_fused without caller workspace ----------------------------------
  * No counterpart on the pages: an addition for callers that cannot allocate
@@ -130,8 +147,9 @@ int acnn_conv2d_path(const acnn_conv_desc* d);
  * static device array of ACNN_NOALLOC_SCRATCH_BYTES that the library holds on
  * every GPU that loads it, until the process exits.  Nothing is allocated or
  * freed (no cudaMalloc, cudaFree or allocating library call).
- *   - A call whose acnn_conv2d_workspace_size(d) exceeds
- *     ACNN_NOALLOC_SCRATCH_BYTES returns ACNN_ERR_WORKSPACE and launches nothing.
+ *   - A call whose required scratch (the staging copies) exceeds
+ *     ACNN_NOALLOC_SCRATCH_BYTES returns ACNN_ERR_WORKSPACE and launches nothing;
+ *     optional split-K scratch is limited to what the array holds.
  *   - The first call on a device that needs scratch looks the array's device
  *     address up (cudaGetSymbolAddress) with that device current; make that
  *     first call before any stream capture.

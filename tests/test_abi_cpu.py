@@ -77,10 +77,15 @@ def test_conv_path_selection(A):
     assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=64, kh=1, kw=1, pad=0)) == 1
     assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=64)) == 2
     assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=64, stride=2)) == 2
-    assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=32)) == 0         # tiny C_in
+    assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=32)) == 3         # tiny C_in: packed
+    assert A.acnn_conv2d_path(desc(A, c_in=7, c_out=120, layout=1, dtype=1)) == 3
     assert A.acnn_conv2d_path(desc(A, dtype=0)) == 0                  # fp32
-    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=120)) == 0       # C_out % 16
-    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=64, kw=1, pad=0)) == 0  # non-square
+    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=120)) == 2       # C_out % 8 == 0
+    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=30)) == 0        # C_out % 8 != 0
+    assert A.acnn_conv2d_path(desc(A, c_in=8, c_out=64, kw=1, pad=0)) == 3  # non-square
+    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=64, kw=1, pad=0)) == 3
+    assert A.acnn_conv2d_path(desc(A, c_in=100, c_out=64, kh=3, kw=3)) == 0  # K > 512
+    assert A.acnn_conv2d_workspace_size(desc(A, c_in=3, c_out=32)) >= 64 * 32 * 2
     assert A.acnn_conv2d_path(desc(A, n=0)) == -1
     assert A.acnn_conv2d_workspace_size(desc(A, c_in=64, c_out=64)) == 0
 

@@ -145,9 +145,7 @@ DIRECT_CASES = [
     # name, n, h, w, cin, cout, k, s, p, dt, layout
     ("cfg1_like", 1, 32, 32, 16, 32, 3, 1, 1, "f32", G.NHWC),
     ("stem_s2_f32", 1, 37, 45, 3, 32, 3, 2, 1, "f32", G.NHWC),
-    ("stem_s2_bf16", 2, 33, 30, 3, 32, 3, 2, 1, "bf16", G.NHWC),
     ("f32_32to64", 1, 21, 19, 32, 64, 3, 1, 1, "f32", G.NHWC),
-    ("prep7_nchw_f16", 1, 34, 60, 7, 120, 3, 2, 1, "f16", G.NCHW),
     ("f32_nchw", 2, 15, 17, 5, 20, 3, 1, 1, "f32", G.NCHW),
     ("f32_7x7", 1, 23, 18, 3, 40, 7, 2, 3, "f32", G.NHWC),
     ("f32_1x1", 1, 10, 10, 12, 36, 1, 1, 0, "f32", G.NHWC),
@@ -162,6 +160,27 @@ def test_conv_direct_path(case):
     d = A.ConvDesc(n, h, w, cin, cout, k, k, s, p, layout, DT[dt])
     assert A.acnn_conv2d_path(d) == 0
     y, ref = conv_case(name, n, h, w, cin, cout, k, s, p, dt, layout=layout)
+    assert_parity(y, ref, TDT[dt], name)
+
+
+PACKED_CASES = [
+    # name, n, h, w, cin, cout, k, kw, s, p, dt, layout
+    ("stem_s2_bf16", 2, 33, 30, 3, 32, 3, 3, 2, 1, "bf16", G.NHWC),
+    ("stem_s2_big", 2, 160, 150, 3, 32, 3, 3, 2, 1, "bf16", G.NHWC),
+    ("prep7_nchw_f16", 1, 34, 60, 7, 120, 3, 3, 2, 1, "f16", G.NCHW),
+    ("cin5_7x7_s2", 1, 41, 37, 5, 64, 7, 7, 2, 3, "bf16", G.NHWC),
+    ("nonsq_1x3", 2, 12, 17, 16, 48, 1, 3, 1, 0, "f16", G.NHWC),
+    ("cin12_3x3", 1, 23, 29, 12, 40, 3, 3, 1, 1, "bf16", G.NCHW),
+]
+
+
+@pytest.mark.parametrize("case", PACKED_CASES, ids=[c[0] for c in PACKED_CASES])
+def test_conv_packed_path(case):
+    """Few/odd input channels or non-square kernels: explicit im2col pack + tcgen05 GEMM."""
+    name, n, h, w, cin, cout, k, kw, s, p, dt, layout = case
+    d = A.ConvDesc(n, h, w, cin, cout, k, kw, s, p, layout, DT[dt])
+    assert A.acnn_conv2d_path(d) == 3
+    y, ref = conv_case(name, n, h, w, cin, cout, k, s, p, dt, layout=layout, kw=kw)
     assert_parity(y, ref, TDT[dt], name)
 
 
@@ -297,3 +316,86 @@ def test_section_graph_replay_matches_eager():
     s.synchronize()
     assert torch.equal(y2, eager)
     sec.close()
+
+
+# ---------------------------------------------------------------- split-K
+SPLITK_CASES = [
+    # name, n, h, w, cin, cout, k, s, p, layout, act, res
+    ("s4_3x3", 8, 20, 20, 512, 512, 3, 1, 1, G.NHWC, A.ACT_RELU, A.RES_NONE),
+    ("pan5_silu", 2, 20, 20, 512, 256, 3, 1, 1, G.NHWC, A.ACT_SILU, A.RES_NONE),
+    ("res_prelu_nchw", 1, 17, 30, 240, 240, 3, 1, 1, G.NCHW, A.ACT_PRELU, A.RES_ACT_THEN_ADD),
+    ("1x1_addres", 2, 10, 10, 2048, 256, 1, 1, 0, G.NHWC, A.ACT_RELU, A.RES_ADD_THEN_ACT),
+]
+
+
+def min_workspace(d, full):
+    """Smallest workspace the call accepts (the NCHW staging copies; 0 for NHWC)."""
+    if A.acnn_conv2d_plan(d, 0)[0] == 0:
+        return 0
+    lo, hi = 0, full
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if A.acnn_conv2d_plan(d, mid)[0] == 0:
+            hi = mid
+        else:
+            lo = mid
+    return hi
+
+
+@pytest.mark.parametrize("case", SPLITK_CASES, ids=[c[0] for c in SPLITK_CASES])
+def test_conv_split_k(case):
+    """Shapes whose plan splits K (fp32 partial sums + reduce kernel) match the oracle,
+    and a workspace too small for the split gives the same answer unsplit."""
+    name, n, h, w, cin, cout, k, s, p, layout, act, res_mode = case
+    dt = "bf16" if layout == G.NHWC else "f16"
+    d = A.ConvDesc(n, h, w, cin, cout, k, k, s, p, layout, DT[dt])
+    full = A.acnn_conv2d_workspace_size(d)
+    st, rows, bn, splits = A.acnn_conv2d_plan(d, full)
+    assert st == 0 and splits > 1, (rows, bn, splits)
+    y, ref = conv_case("sk" + name, n, h, w, cin, cout, k, s, p, dt, layout=layout, act=act,
+                       res_mode=res_mode)
+    assert_parity(y, ref, TDT[dt], name)
+    # only the NCHW staging part of the workspace: the plan falls back to one split
+    seed = 11
+    x = G.tensor(seed, "sk" + name + ".x", G.activation_shape(layout, n, cin, h, w), "normal",
+                 dtype=DT[dt]).cuda()
+    wt = G.conv_weight(seed, "sk" + name, cout, cin, k, k, layout, DT[dt]).cuda()
+    b = G.conv_bias(seed, "sk" + name, cout).cuda()
+    al = G.prelu_alpha(seed, "sk" + name, cout).cuda()
+    r = None
+    if res_mode:
+        oh, ow = (h + 2 * p - k) // s + 1, (w + 2 * p - k) // s + 1
+        r = G.tensor(seed, "sk" + name + ".r", G.activation_shape(layout, n, cout, oh, ow),
+                     "normal", dtype=DT[dt]).cuda()
+    staging = min_workspace(d, full)
+    st, _, _, sp1 = A.acnn_conv2d_plan(d, staging)
+    assert st == 0 and sp1 == 1
+    ws = torch.empty(max(staging, 16), dtype=torch.uint8, device="cuda")
+    y1 = torch.empty_like(y)
+    st = A.acnn_conv2d_fused(d, x, wt, b, al, r, res_mode, act, y1, ws if staging else None,
+                             staging)
+    assert st == 0, A.status_string(st)
+    torch.cuda.synchronize()
+    assert_parity(y1, ref, TDT[dt], name + " unsplit")
+
+
+# ---------------------------------------------------------------- 256-row tiles
+ROWS256_CASES = [
+    # name, n, h, w, cin, cout, k, s, p, layout, act, res
+    ("3x3_64", 4, 100, 100, 64, 64, 3, 1, 1, G.NHWC, A.ACT_RELU, A.RES_NONE),
+    ("3x3_32_res", 4, 96, 100, 32, 32, 3, 1, 1, G.NHWC, A.ACT_SILU, A.RES_ACT_THEN_ADD),
+    ("3x3_128_nchw", 2, 90, 120, 128, 128, 3, 1, 1, G.NCHW, A.ACT_PRELU, A.RES_ADD_THEN_ACT),
+]
+
+
+@pytest.mark.parametrize("case", ROWS256_CASES, ids=[c[0] for c in ROWS256_CASES])
+def test_conv_256_row_tiles(case):
+    """Narrow-output convs whose plan uses 256-pixel tiles (two 128-row MMAs per k-block)."""
+    name, n, h, w, cin, cout, k, s, p, layout, act, res_mode = case
+    dt = "bf16" if layout == G.NHWC else "f16"
+    d = A.ConvDesc(n, h, w, cin, cout, k, k, s, p, layout, DT[dt])
+    st, rows, bn, splits = A.acnn_conv2d_plan(d, A.acnn_conv2d_workspace_size(d))
+    assert st == 0 and rows == 256, (rows, bn, splits)
+    y, ref = conv_case("r256" + name, n, h, w, cin, cout, k, s, p, dt, layout=layout, act=act,
+                       res_mode=res_mode)
+    assert_parity(y, ref, TDT[dt], name)
