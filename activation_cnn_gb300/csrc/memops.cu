@@ -419,19 +419,27 @@ __global__ void __launch_bounds__(kThreads) im2col_pack_kernel(
         const int ox = (int)(m % OW);
         const uint32_t t = m / OW;
         const int oy = (int)(t % OH), n = (int)(t / OH);
+        // (tap, channel) of the chunk's first k, then stepped along k
+        const int k0 = g * 8;
+        const int tap0 = k0 / C;
+        int ci = k0 - tap0 * C, ky = tap0 / KW, kx = tap0 - (tap0 / KW) * KW;
         Vec<uint16_t, 8> v;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int k = g * 8 + j;
             uint16_t val = 0;
-            if (k < K) {
-                const int tap = k / C, ci = k - tap * C;
-                const int ky = tap / KW, kx = tap - ky * KW;
+            if (k0 + j < K) {
                 const int iy = oy * S + ky - P, ix = ox * S + kx - P;
                 if (iy >= 0 && iy < H && ix >= 0 && ix < W)
                     val = x[act_index(layout, C, H, W, n, ci, iy, ix)];
             }
             v.v[j] = val;
+            if (++ci == C) {
+                ci = 0;
+                if (++kx == KW) {
+                    kx = 0;
+                    ++ky;
+                }
+            }
         }
         *reinterpret_cast<Vec<uint16_t, 8>*>(a + (long long)m * Kp + g * 8) = v;
     }

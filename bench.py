@@ -38,6 +38,34 @@ METRIC = ("fused-conv TFLOP/s (% of GB300 BF16 dense peak); backbone img/s @640x
 L2_FLUSH_BYTES = 512 << 20
 
 
+def kernel_source_hash():
+    """sha256 of the tensor-core conv source, to tie ncu counters to the kernel they measured."""
+    import hashlib
+    src = os.path.join(ROOT, "activation_cnn_gb300", "csrc", "conv_igemm.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(workload):
+    """Per-launch DRAM bytes of the conv kernel from the committed ncu summary, or None
+    when the summary was taken on another workload or another version of the kernel."""
+    path = os.path.join(ROOT, "profiles", f"igemm_conv_{workload}_traffic.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -252,7 +280,10 @@ def run_ours(args, rank, world, local_rank):
                 "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4) if peak else None,
                 "peak_source": f"{pk['source']} bf16 sustained",
-                "traffic": None,
+                "traffic": measured_traffic(args.workload) if args.batch in (None, 8) else None,
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the "
+                                  "conv launches of one step, averaged per launch "
+                                  f"(profiles/igemm_conv_{args.workload}_traffic.md)",
                 "launches_per_step": len(ig),
                 "flops_per_launch": ig_flops / max(1, len(ig)),
                 "avg_launch_us": 1e6 * ig_s / max(1, len(ig)),
