@@ -14,12 +14,15 @@
 //     viewed as [C_out][kh*kw][C_in].
 //   * Both land in shared memory in the 128-byte-swizzled K-major layout that
 //     tcgen05.mma reads directly; a 64-channel k-block is one 128-byte row.
-// Warp roles (192 threads, persistent, one CTA per SM):
-//   warp 0  TMA producer (one lane) over a STAGES-deep ring of smem slots
-//   warp 1  TMEM allocator and MMA issuer (one lane): 4 x (128 x BN x 16) MMAs
-//           per k-block into an fp32 TMEM accumulator
-//   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, + bias, activation,
-//           residual (before or after the activation), down-cast, store.
+// Warp roles (320 threads, persistent, one CTA per SM):
+//   warp 0  TMA producer (one lane) over a ring of operand stages in shared
+//           memory (as deep as the shared memory left by the epilogue allows)
+//   warp 1  TMEM allocator and MMA issuer (one lane): MS x 4 x (128 x BN x 16)
+//           MMAs per k-block into an fp32 TMEM accumulator
+//   warps 2-9  epilogue, two per TMEM lane quarter: tcgen05.ld 32 columns at
+//           a time, + bias, activation, residual (before or after the
+//           activation), down-cast, TMA store; residual boxes stream in by TMA
+//           several chunks ahead.
 // Two TMEM accumulators alternate so the epilogue of one tile overlaps the
 // MMAs of the next.  Every mbarrier wait is bounded: on expiry the kernel
 // records ACNN_ERR_DEVICE_TIMEOUT in a device status word, raises a CTA-wide
@@ -45,23 +48,29 @@ constexpr long long kDrainCycles = 400000000ll;     // ~0.2 s per drain wait
 
 constexpr uint32_t kStageBytes = 32 * 64;  // epilogue staging: 32 rows x 32 channels x 2 B
 constexpr uint32_t kEpiBytes = kEpiWarps * 2 /*buffers*/ * kStageBytes;
+constexpr uint32_t kParamBytes = kEpiWarps * 64 * 4;  // per warp: 32 biases + 32 alphas
+constexpr int kMaxStages = 8;
+constexpr int kMaxResDepth = 4;  // residual boxes in flight per epilogue warp
+constexpr size_t kBarBytes = 512;
+constexpr size_t kSmemMax = 232448;  // 227 KB of dynamic shared memory per CTA
+// Shared memory besides the operand ring and the residual ring.  The window
+// must start 1024-byte aligned (the kernel checks): the swizzled operand
+// tiles and staging boxes rely on it.
+constexpr size_t kSmemFixed = kEpiBytes + kParamBytes + kBarBytes;
+static_assert((2 * kMaxStages + 5 + kEpiWarps * kMaxResDepth) * 8 + 8 <= kBarBytes,
+              "barrier region too small");
 
 // Tile of (128 * MS) output pixels x BN output channels: MS row blocks of 128
-// share each B tile, so one pipeline step carries MS x 4 MMAs.
+// share each B tile, so one pipeline step carries MS x 4 MMAs.  The ring depth
+// is chosen per launch from the shared memory left by the residual ring.
 template <int BN, int MS> struct Cfg {
     static constexpr uint32_t kAB = MS * kABytes;  // A bytes per stage
     static constexpr uint32_t kBBytes = BN * BK * 2;
     static constexpr uint32_t kTmemCols = 2 * MS * BN < 32 ? 32 : 2 * MS * BN;
-    static constexpr size_t kBarBytes = 512;
-    static constexpr size_t kFixed = 1024 /*alignment slack*/ + 2 * kEpiBytes + kBarBytes;
-    static constexpr int kStagesFit = (int)((232448 - kFixed) / (kAB + kBBytes));
-    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-    static constexpr int kBarriers = 2 * kStages + 5 + 2 * kEpiWarps;
-    static_assert(kStages >= 2, "ring too shallow");
-    static_assert(kBarriers * 8 + 8 <= kBarBytes, "barrier region too small");
     static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
-    static constexpr size_t kSmem = kFixed + kStages * (kAB + kBBytes);
-    static_assert(kSmem <= 232448, "exceeds the 227 KB of shared memory per CTA");
+    static_assert(kSmemFixed + (size_t)kEpiWarps * kMaxResDepth * kStageBytes + 2 * (kAB + kBBytes) <=
+                      kSmemMax,
+                  "two stages and the deepest residual ring must fit");
 };
 
 struct Params {
@@ -79,6 +88,8 @@ struct Params {
     void* y;
     int* status;
     long long budget;  // >0: give up a wait after this many polls; 0: after kTimeoutNs
+    int stages;        // depth of the operand ring (2..kMaxStages)
+    int res_depth;     // residual boxes in flight per epilogue warp (0: no residual)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -341,6 +352,48 @@ __device__ __forceinline__ void epi32_any(int act, const float (&v)[32], const f
     }
 }
 
+// The NHWC epilogue's form: the residual mode fixed at compile time (no
+// residual term at all without one), the bias and PReLU alpha read from a
+// shared-memory slot ([0, 32) bias, [32, 64) alpha) four at a time, and the
+// result written over the accumulator values.
+template <int ACT, int RES>
+__device__ __forceinline__ void epi32_slot(float (&v)[32], const float* slot,
+                                           const float (&r)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        const float4 b4 = *reinterpret_cast<const float4*>(slot + j);
+        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (ACT == ACNN_ACT_PRELU) a4 = *reinterpret_cast<const float4*>(slot + 32 + j);
+        const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+        const float aa[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float x = v[j + k] + bb[k];
+            if constexpr (RES == ACNN_RES_NONE) v[j + k] = act_fixed<ACT>(x, aa[k]);
+            else if constexpr (RES == ACNN_RES_ADD_THEN_ACT) v[j + k] = act_fixed<ACT>(x + r[j + k], aa[k]);
+            else v[j + k] = act_fixed<ACT>(x, aa[k]) + r[j + k];
+        }
+    }
+}
+
+template <int ACT>
+__device__ __forceinline__ void epi32_slot_act(int res_mode, float (&v)[32], const float* slot,
+                                               const float (&r)[32]) {
+    if (res_mode == ACNN_RES_ADD_THEN_ACT) epi32_slot<ACT, ACNN_RES_ADD_THEN_ACT>(v, slot, r);
+    else if (res_mode == ACNN_RES_ACT_THEN_ADD) epi32_slot<ACT, ACNN_RES_ACT_THEN_ADD>(v, slot, r);
+    else epi32_slot<ACT, ACNN_RES_NONE>(v, slot, r);
+}
+
+__device__ __forceinline__ void epi32_slot_mode(int act, int res_mode, float (&v)[32],
+                                                const float* slot, const float (&r)[32]) {
+    switch (act) {  // both uniform across the CTA
+    case ACNN_ACT_RELU: epi32_slot_act<ACNN_ACT_RELU>(res_mode, v, slot, r); break;
+    case ACNN_ACT_SILU: epi32_slot_act<ACNN_ACT_SILU>(res_mode, v, slot, r); break;
+    case ACNN_ACT_PRELU: epi32_slot_act<ACNN_ACT_PRELU>(res_mode, v, slot, r); break;
+    default: epi32_slot_act<ACNN_ACT_NONE>(res_mode, v, slot, r); break;
+    }
+}
+
 // Bias and PReLU alpha of channels [co, co + 32): broadcast loads (every lane
 // reads the same addresses); channels >= C_out read as zero.
 __device__ __forceinline__ void load_chunk_params(const float* __restrict__ bias,
@@ -367,18 +420,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmap_y,
                       const __grid_constant__ CUtensorMap tmap_r, const Params p) {
     using C = Cfg<BN, MS>;
-    constexpr int S = C::kStages;
     constexpr int TM = BM * MS;  // output pixels per tile
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + S * C::kAB;
+    // The swizzled tiles need a 1024-aligned window; the host sized the
+    // allocation on that assumption.  A misaligned window is reported, not used.
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, ACNN_ERR_UNSUPPORTED);
+        return;
+    }
+    const int S = p.stages;
+    uint8_t* sA = smem_raw;
+    uint8_t* sB = sA + S * C::kAB;
     uint8_t* sO = sB + S * C::kBBytes;  // output staging, 1024-aligned (64-B swizzle atoms)
-    uint8_t* sR = sO + kEpiBytes;       // residual staging
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sR + kEpiBytes);
-    // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, residual[8][2]
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5 + 2 * kEpiWarps);
+    uint8_t* sR = sO + kEpiBytes;       // residual ring: kEpiWarps x res_depth boxes
+    float* sP = reinterpret_cast<float*>(sR + (size_t)kEpiWarps * p.res_depth * kStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sP) + kParamBytes);
+    // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, residual[8][res_depth]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5 +
+                                                        kEpiWarps * kMaxResDepth);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -388,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
-    auto res_bar = [&](int e, int b) { return bar0 + 8u * (2 * S + 5 + 2 * e + b); };
+    auto res_bar = [&](int e, int b) { return bar0 + 8u * (2 * S + 5 + kMaxResDepth * e + b); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -400,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tempty_bar(a), kEpiWarps);  // one arrival per epilogue warp
         }
         mbar_init(drain_bar, 1);
-        for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(res_bar(i >> 1, i & 1), 1);
+        for (int e = 0; e < kEpiWarps; ++e)
+            for (int b = 0; b < p.res_depth; ++b) mbar_init(res_bar(e, b), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tmap_a);
@@ -575,57 +635,117 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (p.out_layout == ACNN_NHWC) {
         // ---------------------------------------------------- epilogue warps, NHWC
         // Warp e (0..7) owns the 32 rows of its TMEM lane quarter (warp % 4) and
-        // every other 32-channel chunk of the tile (e / 4 picks even or odd): the
-        // residual box arrives by TMA one chunk ahead into a double buffer, the
-        // 32 x 32 result goes to a 64-byte-swizzled staging buffer and leaves by
-        // a TMA store (which also clips rows >= M and channels >= C_out).
+        // every other 32-channel chunk of each tile (e / 4 picks even or odd).
+        // Its chunks form one stream across tiles, walked by three cursors:
+        //   * residual boxes arrive by TMA through a ring of res_depth buffers,
+        //     up to res_depth chunks ahead (across tile boundaries);
+        //   * the bias and PReLU alpha of the next chunk are loaded a chunk
+        //     ahead, one channel per lane, then shared through a per-warp slot;
+        //   * the 32 x 32 result goes to a 64-byte-swizzled staging buffer and
+        //     leaves by a TMA store (which clips rows >= M and channels >= C_out).
         const int q = warp & 3;
         const int e = warp - 2;
         const int half = e >> 2;
+        const int RD = p.res_depth;  // 0 without a residual
+        const int nnt = p.num_n_tiles;
         uint8_t* ost = sO + e * 2 * kStageBytes;
-        uint8_t* rst = sR + e * 2 * kStageBytes;
-        const bool has_res = p.res_mode != ACNN_RES_NONE;
+        uint8_t* rst = sR + (size_t)e * RD * kStageBytes;
+        float* slot = sP + e * 64;  // [0, 32) bias, [32, 64) alpha of the current chunk
         const bool prelu = p.act == ACNN_ACT_PRELU;
-        const float kpre = p.res_mode == ACNN_RES_ADD_THEN_ACT ? 1.f : 0.f;
-        const float kpost = p.res_mode == ACNN_RES_ACT_THEN_ADD ? 1.f : 0.f;
         const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // 64-B swizzle of this lane's row
-        int acc = 0, ob = 0, rb = 0;
-        uint32_t acc_phase = 0, rpar = 0, r_inflight = 0;
-        bool aborted = false;
-        auto issue_res = [&](int buf, int c0, int r0) {
-            const uint32_t bar = res_bar(e, buf);
-            mbar_arrive_expect_tx(bar, kStageBytes);
-            tma_load_2d(smem_u32(rst + buf * kStageBytes), &tmap_r, bar, c0, r0);
+        // A cursor walks this warp's chunks: tile t (column tile nt = t % nnt),
+        // row block ms, 32-channel chunk ci within the row block.
+        const int nch_full = BN / 32;
+        const int nch_last = ((p.C_out - (nnt - 1) * BN) + 31) >> 5;  // ragged last column tile
+        struct Cursor {
+            int t, nt, ms, ci;
         };
+        auto settle = [&](Cursor& c) {  // carry ci into ms, then into the next tile
+            while (c.t < num_tiles) {
+                const int nch = c.nt == nnt - 1 ? nch_last : nch_full;
+                while (c.ci >= nch) {
+                    c.ci -= nch;
+                    ++c.ms;
+                }
+                if (c.ms < MS) break;
+                c.t += gridDim.x;
+                c.nt = nnt == 1 ? 0 : c.t % nnt;
+                c.ms = 0;
+                c.ci = half;
+            }
+        };
+        auto start_cursor = [&](Cursor& c) {
+            c = Cursor{(int)blockIdx.x, nnt == 1 ? 0 : (int)blockIdx.x % nnt, 0, half};
+            settle(c);
+        };
+        auto cursor_col = [&](const Cursor& c) { return c.nt * BN + c.ci * 32; };
+        auto cursor_row = [&](const Cursor& c) {
+            return (nnt == 1 ? c.t : c.t / nnt) * TM + c.ms * BM + q * 32;
+        };
+        // residual cursor
+        Cursor rc;
+        start_cursor(rc);
+        int pend = 0, wb = 0, rb = 0;
+        uint32_t rpar = 0;
+        auto refill = [&]() {
+            while (pend < RD && rc.t < num_tiles) {
+                if (lane == 0) {
+                    const uint32_t bar = res_bar(e, wb);
+                    mbar_arrive_expect_tx(bar, kStageBytes);
+                    tma_load_2d(smem_u32(rst + wb * kStageBytes), &tmap_r, bar, cursor_col(rc),
+                                cursor_row(rc));
+                }
+                wb = wb + 1 == RD ? 0 : wb + 1;
+                ++pend;
+                rc.ci += 2;
+                settle(rc);
+            }
+        };
+        // parameter cursor: this lane's bias / alpha of the chunk after the current one
+        Cursor pc;
+        start_cursor(pc);
+        float bnext = 0.f, anext = 0.f;
+        auto fetch_params = [&]() {
+            if (pc.t < num_tiles) {
+                const int ch = cursor_col(pc) + lane;
+                bnext = (p.bias && ch < p.C_out) ? __ldg(p.bias + ch) : 0.f;
+                anext = (prelu && ch < p.C_out) ? __ldg(p.alpha + ch) : 0.f;
+                pc.ci += 2;
+                settle(pc);
+            }
+        };
+        fetch_params();
+        refill();
+        int acc = 0, ob = 0;
+        uint32_t acc_phase = 0;
+        bool aborted = false;
         for (int tile = blockIdx.x; !aborted && tile < num_tiles; tile += gridDim.x) {  // splits == 1
-            const int m0 = (tile / p.num_n_tiles) * TM;
-            const int n0 = (tile % p.num_n_tiles) * BN;
+            const int mt = nnt == 1 ? tile : tile / nnt;
+            const int m0 = mt * TM;
+            const int n0 = (tile - mt * nnt) * BN;
             const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
             const int nchunks = MS * nch;  // chunk i: row block i / nch, channels (i % nch) * 32
-            auto chunk_row = [&](int i) { return m0 + (i / nch) * BM + q * 32; };
-            auto chunk_col = [&](int i) { return n0 + (i % nch) * 32; };
-            if (has_res && half < nchunks) {
-                if (lane == 0) issue_res(rb, chunk_col(half), chunk_row(half));
-                r_inflight |= 1u << rb;
-            }
             const bool ok = __all_sync(0xffffffffu, wait_phase(tfull_bar(acc), acc_phase, abort_flag, p));
             if (!ok) break;
             tc_fence_after();
+            int ms = 0, ci = half;
             for (int i = half; i < nchunks; i += 2) {
-                const int ms = i / nch, c = (i - ms * nch) * 32;
-                const int row0 = m0 + ms * BM + q * 32;
-                if (has_res && i + 2 < nchunks) {
-                    if (lane == 0) issue_res(rb ^ 1, chunk_col(i + 2), chunk_row(i + 2));
-                    r_inflight |= 1u << (rb ^ 1);
+                while (ci >= nch) {
+                    ci -= nch;
+                    ++ms;
                 }
-                float bv[32], av[32];
-                load_chunk_params(p.bias, p.alpha, prelu, n0 + c, p.C_out, bv, av);
+                const int c = ci * 32;
+                ci += 2;
+                const int row0 = m0 + ms * BM + q * 32;
+                slot[lane] = bnext;
+                slot[32 + lane] = anext;
+                fetch_params();
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
                               (uint32_t)(acc * MS * BN + ms * BN + c),
                           v);
                 float r[32];
-                if (has_res) {
+                if (RD > 0) {
                     const bool okr = __all_sync(
                         0xffffffffu, wait_phase(res_bar(e, rb), (rpar >> rb) & 1u, abort_flag, p));
                     if (!okr) {
@@ -633,7 +753,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     rpar ^= 1u << rb;
-                    r_inflight &= ~(1u << rb);
                     const uint8_t* rrow = rst + rb * kStageBytes + lane * 64;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -643,12 +762,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         unpack2<T>(u.z, r[8 * j + 4], r[8 * j + 5]);
                         unpack2<T>(u.w, r[8 * j + 6], r[8 * j + 7]);
                     }
+                    rb = rb + 1 == RD ? 0 : rb + 1;
+                    --pend;
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = 0.f;
                 }
-                float o[32];
-                epi32_any(p.act, v, bv, av, r, kpre, kpost, o);
+                __syncwarp();  // the slot written above is visible to every lane
+                epi32_slot_mode(p.act, RD > 0 ? p.res_mode : ACNN_RES_NONE, v, slot, r);
                 // the store that last used this staging buffer must have read it
                 if (lane == 0) bulk_wait_read<1>();
                 __syncwarp();
@@ -656,8 +777,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     *reinterpret_cast<uint4*>(orow + ((j ^ swz) << 4)) = make_uint4(
-                        pack2<T>(o[8 * j + 0], o[8 * j + 1]), pack2<T>(o[8 * j + 2], o[8 * j + 3]),
-                        pack2<T>(o[8 * j + 4], o[8 * j + 5]), pack2<T>(o[8 * j + 6], o[8 * j + 7]));
+                        pack2<T>(v[8 * j + 0], v[8 * j + 1]), pack2<T>(v[8 * j + 2], v[8 * j + 3]),
+                        pack2<T>(v[8 * j + 4], v[8 * j + 5]), pack2<T>(v[8 * j + 6], v[8 * j + 7]));
+                // orders this lane's staging writes and its reads of the residual
+                // box before the async-proxy store and the box's refill below
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -665,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_commit();
                 }
                 ob ^= 1;
-                if (has_res) rb ^= 1;
+                refill();
             }
             if (aborted) break;
             tc_fence_before();
@@ -676,8 +799,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) {
             bulk_wait_all();  // every output box written before the CTA exits
-            for (int b = 0; b < 2; ++b)  // residual boxes still in flight after an abort
-                if (r_inflight & (1u << b)) wait_drain(res_bar(e, b), (rpar >> b) & 1u);
+            for (int k = 0; k < pend; ++k) {  // residual boxes still in flight after an abort
+                const int b = (rb + k) % RD;
+                wait_drain(res_bar(e, b), (rpar >> b) & 1u);
+                rpar ^= 1u << b;
+            }
         }
         __syncwarp();
     } else {
@@ -878,14 +1004,28 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     auto kern = igemm_conv_kernel<BN, MS, T>;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)C::kSmem) != cudaSuccess)
+                                 (int)kSmemMax) != cudaSuccess)
             return ACNN_ERR_CUDA;
         attr_set = true;
     }
+    // Residual ring: deep (4 boxes per warp) when a tile has few k-blocks and
+    // the epilogue's memory traffic dominates, else 3, leaving the operand ring
+    // the rest of shared memory (at most kMaxStages deep).
+    const bool nhwc_res = prm.res_mode != ACNN_RES_NONE && prm.out_layout == ACNN_NHWC && !prm.part;
+    int rd = nhwc_res ? (prm.kb_per_split <= 2 ? kMaxResDepth : 3) : 0;
+    auto stages_for = [](int depth) {
+        const size_t left = kSmemMax - kSmemFixed - (size_t)kEpiWarps * depth * kStageBytes;
+        const int n = (int)(left / (C::kAB + C::kBBytes));
+        return n > kMaxStages ? kMaxStages : n;
+    };
+    prm.stages = stages_for(rd);
+    prm.res_depth = rd;
+    const size_t smem = kSmemFixed + (size_t)kEpiWarps * rd * kStageBytes +
+                        (size_t)prm.stages * (C::kAB + C::kBBytes);
     prm.num_n_tiles = (a.d.c_out + BN - 1) / BN;
     const int tiles = prm.num_m_tiles * prm.num_n_tiles * prm.splits;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    kern<<<grid, kThreads, C::kSmem, s>>>(m.a, m.b, m.y, m.r, prm);
+    kern<<<grid, kThreads, smem, s>>>(m.a, m.b, m.y, m.r, prm);
     return cudaGetLastError() == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
 }
 
