@@ -101,11 +101,12 @@ struct ConvArgs {
 // Tile width and K split of the tensor-core conv for a geometry, given the
 // bytes available for split-K partial sums (SIZE_MAX: as many as it wants).
 struct IgemmPlan {
-    int bn;             // output channels per tile: 64, 128 or 256
+    int bn;             // output channels per tile: 32, 64, 128 or 256
     int ms;             // 128-pixel row blocks per tile: 1 or 2
     int splits;         // K splits (1 = none)
-    int kb_per_split;   // 64-channel k-blocks per split
+    int kb_per_split;   // k-blocks per split
     size_t part_bytes;  // fp32 partial-sum workspace the plan needs
+    int bk;             // channels per k-block: 64, or 32 when C_in <= 32
 };
 IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget);
 

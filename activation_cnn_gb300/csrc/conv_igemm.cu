@@ -39,10 +39,8 @@ namespace acnn {
 namespace {
 
 constexpr int BM = 128;             // output pixels per tile (TMEM lanes)
-constexpr int BK = 64;              // channels per k-block: 64 x 2 B = one 128-B swizzle row
 constexpr int kEpiWarps = 8;        // two per TMEM lane quarter
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue warps
-constexpr uint32_t kABytes = BM * BK * 2;
 constexpr long long kTimeoutCycles = 8000000000ll;  // ~4 s per wait at 2 GHz
 constexpr long long kDrainCycles = 400000000ll;     // ~0.2 s per drain wait
 
@@ -57,14 +55,18 @@ constexpr size_t kSmemMax = 232448;  // 227 KB of dynamic shared memory per CTA
 // must start 1024-byte aligned (the kernel checks): the swizzled operand
 // tiles and staging boxes rely on it.
 constexpr size_t kSmemFixed = kEpiBytes + kParamBytes + kBarBytes;
-static_assert((2 * kMaxStages + 5 + kEpiWarps * kMaxResDepth) * 8 + 8 <= kBarBytes,
+static_assert((2 * kMaxStages + 6 + kEpiWarps * kMaxResDepth) * 8 + 8 <= kBarBytes,
               "barrier region too small");
 
-// Tile of (128 * MS) output pixels x BN output channels: MS row blocks of 128
-// share each B tile, so one pipeline step carries MS x 4 MMAs.  The ring depth
-// is chosen per launch from the shared memory left by the residual ring.
-template <int BN, int MS> struct Cfg {
-    static constexpr uint32_t kAB = MS * kABytes;  // A bytes per stage
+// Tile of (128 * MS) output pixels x BN output channels, K in blocks of BK
+// channels: MS row blocks of 128 share each B tile, so one pipeline step
+// carries MS x BK/16 MMAs.  A k-block row is BK x 2 bytes: 128 B (BK = 64,
+// 128-byte swizzle) or 64 B (BK = 32, 64-byte swizzle, for C_in <= 32).  The
+// ring depth is chosen per launch from the shared memory left by the
+// residual ring and, when the weights stay resident, by the weights.
+template <int BN, int MS, int BK> struct Cfg {
+    static constexpr uint32_t kABytes = BM * BK * 2;  // one 128-row block
+    static constexpr uint32_t kAB = MS * kABytes;     // A bytes per stage
     static constexpr uint32_t kBBytes = BN * BK * 2;
     static constexpr uint32_t kTmemCols = 2 * MS * BN < 32 ? 32 : 2 * MS * BN;
     static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
@@ -90,6 +92,7 @@ struct Params {
     long long budget;  // >0: give up a wait after this many polls; 0: after kTimeoutNs
     int stages;        // depth of the operand ring (2..kMaxStages)
     int res_depth;     // residual boxes in flight per epilogue warp (0: no residual)
+    int b_resident;    // 1: all num_kb weight blocks loaded once, the ring carries A only
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -277,15 +280,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 B, 8-row core-matrix groups 1024 B apart.  Advancing the start address
-// by 32 B steps K by 16 elements inside the swizzle atom.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+// Shared-memory matrix descriptor of a K-major operand whose rows are BK x 2
+// bytes: BK = 64 -> 128-byte rows, 128-byte swizzle, 8-row core-matrix groups
+// 1024 B apart; BK = 32 -> 64-byte rows, 64-byte swizzle, groups 512 B apart.
+// Advancing the start address by 32 B steps K by 16 elements inside a row.
+template <int BK> __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+    static_assert(BK == 64 || BK == 32, "k-block of 64 or 32 channels");
+    constexpr uint64_t sbo = (uint64_t)BK * 2 * 8;
+    constexpr uint64_t layout = BK == 64 ? 2 : 4;  // SWIZZLE_128B : SWIZZLE_64B
     return (uint64_t)((saddr & 0x3FFFFu) >> 4)  // start address >> 4
            | ((uint64_t)1 << 16)                // leading byte offset (unused here)
-           | ((uint64_t)(1024 >> 4) << 32)      // stride byte offset: 8 rows x 128 B
+           | ((sbo >> 4) << 32)                 // stride byte offset: 8 rows
            | ((uint64_t)1 << 46)                // descriptor version (tcgen05)
-           | ((uint64_t)2 << 61);               // 128-byte swizzle
+           | (layout << 61);
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B both bf16 or
@@ -413,13 +420,13 @@ __device__ __forceinline__ void load_chunk_params(const float* __restrict__ bias
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int BN, int MS, typename T>
+template <int BN, int MS, int BK, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_conv_kernel(const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_y,
                       const __grid_constant__ CUtensorMap tmap_r, const Params p) {
-    using C = Cfg<BN, MS>;
+    using C = Cfg<BN, MS, BK>;
     constexpr int TM = BM * MS;  // output pixels per tile
     extern __shared__ uint8_t smem_raw[];
     // The swizzled tiles need a 1024-aligned window; the host sized the
@@ -429,14 +436,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
     const int S = p.stages;
+    const bool bres = p.b_resident != 0;
     uint8_t* sA = smem_raw;
-    uint8_t* sB = sA + S * C::kAB;
-    uint8_t* sO = sB + S * C::kBBytes;  // output staging, 1024-aligned (64-B swizzle atoms)
+    uint8_t* sB = sA + S * C::kAB;  // B ring (S slots) or all num_kb resident B blocks
+    uint8_t* sO = sB + (size_t)(bres ? p.num_kb : S) * C::kBBytes;  // output staging
     uint8_t* sR = sO + kEpiBytes;       // residual ring: kEpiWarps x res_depth boxes
     float* sP = reinterpret_cast<float*>(sR + (size_t)kEpiWarps * p.res_depth * kStageBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sP) + kParamBytes);
-    // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, residual[8][res_depth]
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5 +
+    // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, weights,
+    // residual[8][res_depth]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 6 +
                                                         kEpiWarps * kMaxResDepth);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -447,7 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
-    auto res_bar = [&](int e, int b) { return bar0 + 8u * (2 * S + 5 + kMaxResDepth * e + b); };
+    const uint32_t wres_bar = bar0 + 8u * (2 * S + 5);  // resident weights landed
+    auto res_bar = [&](int e, int b) { return bar0 + 8u * (2 * S + 6 + kMaxResDepth * e + b); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -459,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tempty_bar(a), kEpiWarps);  // one arrival per epilogue warp
         }
         mbar_init(drain_bar, 1);
+        mbar_init(wres_bar, 1);
         for (int e = 0; e < kEpiWarps; ++e)
             for (int b = 0; b < p.res_depth; ++b) mbar_init(res_bar(e, b), 1);
         *abort_flag = 0;
@@ -489,6 +500,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
+            if (bres) {
+                // every weight block of the (single) column tile, once
+                mbar_arrive_expect_tx(wres_bar, (uint32_t)p.num_kb * C::kBBytes);
+                int tap = 0, c0 = 0;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    tma_load_3d(smem_u32(sB + kb * C::kBBytes), &tmap_b, wres_bar, c0, tap, 0);
+                    c0 += BK;
+                    if (c0 >= p.kb_per_tap * BK) {
+                        c0 = 0;
+                        ++tap;
+                    }
+                }
+            }
+            const uint32_t stage_tx = C::kAB + (bres ? 0u : C::kBBytes);
             for (int unit = blockIdx.x; ok && unit < num_tiles; unit += gridDim.x) {
                 const int tile = unit / p.splits, split = unit - tile * p.splits;
                 const int m0 = (tile / p.num_n_tiles) * TM;
@@ -508,14 +533,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, C::kAB + C::kBBytes);
+                    mbar_arrive_expect_tx(fb, stage_tx);
                     const uint32_t a_dst = smem_u32(sA + stage * C::kAB);
                     if (p.a_mode == 0)
                         tma_load_2d(a_dst, &tmap_a, fb, c0, m0);
                     else
                         tma_load_im2col(a_dst, &tmap_a, fb, c0, wc, hc, img, (uint16_t)kx,
                                         (uint16_t)ky);
-                    tma_load_3d(smem_u32(sB + stage * C::kBBytes), &tmap_b, fb, c0, tap, n0);
+                    if (!bres)
+                        tma_load_3d(smem_u32(sB + stage * C::kBBytes), &tmap_b, fb, c0, tap, n0);
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == S) {
@@ -537,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // let every copy this thread started land before the CTA exits
                 for (int s = 0; s < S; ++s)
                     if (issued_mask & (1u << s)) wait_drain(full_bar(s), (issued_parity >> s) & 1u);
+                if (bres) wait_drain(wres_bar, 0);
             }
         }
         __syncwarp();
@@ -548,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            bool ok = true;
+            bool ok = !bres || wait_phase(wres_bar, 0, abort_flag, p);
             for (int unit = blockIdx.x; ok && unit < num_tiles; unit += gridDim.x) {
                 const int split = unit % p.splits;
                 const int kb0 = split * p.kb_per_split;
@@ -565,11 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t bdesc = sw128_desc(smem_u32(sB + stage * C::kBBytes));
+                    const uint64_t bdesc =
+                        smem_desc<BK>(smem_u32(sB + (bres ? kb : stage) * C::kBBytes));
 #pragma unroll
                     for (int ms = 0; ms < MS; ++ms) {
                         const uint64_t adesc =
-                            sw128_desc(smem_u32(sA + stage * C::kAB + ms * kABytes));
+                            smem_desc<BK>(smem_u32(sA + stage * C::kAB + ms * C::kABytes));
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
                             mma_f16(d_tmem + (uint32_t)(ms * BN), adesc + 2u * k, bdesc + 2u * k,
@@ -997,45 +1025,67 @@ struct Maps {
     CUtensorMap a, b, y, r;
 };
 
-template <int BN, int MS, typename T>
+template <int BN, int MS, int BK, typename T>
 int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
-    using C = Cfg<BN, MS>;
+    using C = Cfg<BN, MS, BK>;
     static bool attr_set = false;  // per instantiation; set once per process
-    auto kern = igemm_conv_kernel<BN, MS, T>;
+    auto kern = igemm_conv_kernel<BN, MS, BK, T>;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kSmemMax) != cudaSuccess)
             return ACNN_ERR_CUDA;
         attr_set = true;
     }
-    // Residual ring: deep (4 boxes per warp) when a tile has few k-blocks and
-    // the epilogue's memory traffic dominates, else 3, leaving the operand ring
-    // the rest of shared memory (at most kMaxStages deep).
-    const bool nhwc_res = prm.res_mode != ACNN_RES_NONE && prm.out_layout == ACNN_NHWC && !prm.part;
-    int rd = nhwc_res ? (prm.kb_per_split <= 2 ? kMaxResDepth : 3) : 0;
-    auto stages_for = [](int depth) {
-        const size_t left = kSmemMax - kSmemFixed - (size_t)kEpiWarps * depth * kStageBytes;
-        const int n = (int)(left / (C::kAB + C::kBBytes));
-        return n > kMaxStages ? kMaxStages : n;
-    };
-    prm.stages = stages_for(rd);
-    prm.res_depth = rd;
-    const size_t smem = kSmemFixed + (size_t)kEpiWarps * rd * kStageBytes +
-                        (size_t)prm.stages * (C::kAB + C::kBBytes);
     prm.num_n_tiles = (a.d.c_out + BN - 1) / BN;
+    // Residual ring: deep (4 boxes per warp) when a tile has few k-blocks and
+    // the epilogue's memory traffic dominates, else 3.
+    const bool nhwc_res = prm.res_mode != ACNN_RES_NONE && prm.out_layout == ACNN_NHWC && !prm.part;
+    const int rd = nhwc_res ? (prm.kb_per_split <= 2 ? kMaxResDepth : 3) : 0;
+    // The operand ring takes the rest of shared memory (at most kMaxStages
+    // deep).  With a single column tile the weights can instead stay resident
+    // (loaded once per CTA), the ring then carrying A alone: chosen when that
+    // still leaves a ring of 3 (or one as deep as without).
+    const size_t b_all = (size_t)prm.num_kb * C::kBBytes;
+    auto stages_for = [&](bool resident) -> int {
+        size_t left = kSmemMax - kSmemFixed - (size_t)kEpiWarps * rd * kStageBytes;
+        if (resident) {
+            if (left < b_all) return 0;
+            left -= b_all;
+        }
+        const size_t n = left / (C::kAB + (resident ? 0 : C::kBBytes));
+        return n > (size_t)kMaxStages ? kMaxStages : (int)n;
+    };
+    const int s_ring = stages_for(false);
+    const int s_res = prm.num_n_tiles == 1 ? stages_for(true) : 0;
+    const bool resident = s_res >= 2 && s_res >= (s_ring < 3 ? s_ring : 3);
+    prm.b_resident = resident ? 1 : 0;
+    prm.stages = resident ? s_res : s_ring;
+    prm.res_depth = rd;
+    if (prm.stages < 2) return ACNN_ERR_UNSUPPORTED;  // excluded by Cfg's static_assert
+    const size_t smem = kSmemFixed + (size_t)kEpiWarps * rd * kStageBytes +
+                        (size_t)prm.stages * (C::kAB + (resident ? 0 : C::kBBytes)) +
+                        (resident ? b_all : 0);
     const int tiles = prm.num_m_tiles * prm.num_n_tiles * prm.splits;
     const int grid = tiles < sm_count() ? tiles : sm_count();
     kern<<<grid, kThreads, smem, s>>>(m.a, m.b, m.y, m.r, prm);
     return cudaGetLastError() == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
 }
 
+// The instantiated tile shapes: BK = 64 with (BN, MS) in {(256, 1), (128, 1),
+// (128, 2), (64, 1), (64, 2)}; BK = 32 (C_in <= 32) with MS = 2 and BN in
+// {128, 64, 32}.  igemm_plan picks only among these.
 template <typename T>
-int launch_typed(const ConvArgs& a, int bn, int ms, const Maps& m, const Params& prm,
+int launch_typed(const ConvArgs& a, const IgemmPlan& pl, const Maps& m, const Params& prm,
                  cudaStream_t s) {
-    if (bn == 256) return launch_bn<256, 1, T>(a, m, prm, s);
-    if (bn == 128) return ms == 2 ? launch_bn<128, 2, T>(a, m, prm, s)
-                                  : launch_bn<128, 1, T>(a, m, prm, s);
-    return ms == 2 ? launch_bn<64, 2, T>(a, m, prm, s) : launch_bn<64, 1, T>(a, m, prm, s);
+    if (pl.bk == 32) {
+        if (pl.bn == 128) return launch_bn<128, 2, 32, T>(a, m, prm, s);
+        if (pl.bn == 64) return launch_bn<64, 2, 32, T>(a, m, prm, s);
+        return launch_bn<32, 2, 32, T>(a, m, prm, s);
+    }
+    if (pl.bn == 256) return launch_bn<256, 1, 64, T>(a, m, prm, s);
+    if (pl.bn == 128) return pl.ms == 2 ? launch_bn<128, 2, 64, T>(a, m, prm, s)
+                                        : launch_bn<128, 1, 64, T>(a, m, prm, s);
+    return pl.ms == 2 ? launch_bn<64, 2, 64, T>(a, m, prm, s) : launch_bn<64, 1, 64, T>(a, m, prm, s);
 }
 
 // [M, C_out] NHWC output (or residual) viewed 2-D, 32 x 32 boxes, 64-byte swizzle.
@@ -1062,18 +1112,29 @@ IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget
     const double kIssueUs = 0.30, kMmaUsPerMflop = 1.0 / 15.0, kHbmBytesPerUs = 6.0e6;
     const double kLaunchUs = 3.0, kEpiUsPerChunk = 0.15;
     const long long M = (long long)d.n * oh * ow;
-    const int num_kb = d.kh * d.kw * ((d.c_in + BK - 1) / BK);
+    // 32-channel k-blocks when C_in <= 32: a 64-channel block would be half zeros
+    const int bk = d.c_in <= 32 ? 32 : 64;
+    const int num_kb = d.kh * d.kw * ((d.c_in + bk - 1) / bk);
     const int sms = sm_count();
     const double io_bytes = 2.0 * ((double)d.n * d.h * d.w * d.c_in + (double)M * d.c_out +
                                    (double)d.c_out * d.kh * d.kw * d.c_in);
-    IgemmPlan best{64, 1, 1, num_kb, 0}, best1{64, 1, 1, num_kb, 0};
+    IgemmPlan best{64, 1, 1, num_kb, 0, bk}, best1{64, 1, 1, num_kb, 0, bk};
     double best_cost = 1e30, best1_cost = 1e30;
-    const int bn0 = d.c_out >= 256 ? 256 : (d.c_out > 64 ? 128 : 64);
-    for (int bn = bn0; bn >= 64; bn >>= 1) {
-        for (int ms = 1; ms <= (bn == 256 ? 1 : 2); ++ms) {  // TMEM: 2 * ms * bn <= 512
+    int bn0, bn_min;
+    if (bk == 64) {
+        bn0 = d.c_out >= 256 ? 256 : (d.c_out > 64 ? 128 : 64);
+        bn_min = 64;
+    } else {
+        bn0 = d.c_out >= 128 ? 128 : (d.c_out > 32 ? 64 : 32);
+        bn_min = 32;
+    }
+    for (int bn = bn0; bn >= bn_min; bn >>= 1) {
+        for (int ms = 1; ms <= 2; ++ms) {
+            if (bk == 32 && ms != 2) continue;   // instantiated: MS = 2 only
+            if (bk == 64 && bn == 256 && ms != 1) continue;  // TMEM: 2 * ms * bn <= 512
             const long long mt = (M + BM * ms - 1) / (BM * ms);
             const long long tiles = mt * ((d.c_out + bn - 1) / bn);
-            const double t_kb = fmax(kIssueUs, 2.0 * BM * ms * bn * BK * 1e-6 * kMmaUsPerMflop);
+            const double t_kb = fmax(kIssueUs, 2.0 * BM * ms * bn * bk * 1e-6 * kMmaUsPerMflop);
             for (int sp = 1; sp <= 16 && sp <= num_kb; ++sp) {
                 const int kbs = (num_kb + sp - 1) / sp;
                 const int eff = (num_kb + kbs - 1) / kbs;  // splits actually used
@@ -1087,11 +1148,11 @@ IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget
                 if (eff > 1) cost += kLaunchUs + (double)part * 2.0 / kHbmBytesPerUs;
                 if (cost < best_cost * 0.97) {  // prefer wide, short tiles and no split on ties
                     best_cost = cost;
-                    best = IgemmPlan{bn, ms, eff, kbs, part};
+                    best = IgemmPlan{bn, ms, eff, kbs, part, bk};
                 }
                 if (eff == 1 && cost < best1_cost * 0.97) {
                     best1_cost = cost;
-                    best1 = IgemmPlan{bn, ms, 1, kbs, 0};
+                    best1 = IgemmPlan{bn, ms, 1, kbs, 0, bk};
                 }
             }
         }
@@ -1109,6 +1170,8 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
         d.dtype == ACNN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const bool tiled = d.kh == 1 && d.kw == 1 && d.stride == 1 && d.pad == 0;
     const IgemmPlan plan = igemm_plan(d, a.oh, a.ow, a.ws_part ? a.ws_part_bytes : 0);
+    const int bk = plan.bk;
+    const CUtensorMapSwizzle swz = bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
 
     alignas(64) Maps maps;
     CUtensorMap& ta = maps.a;
@@ -1117,10 +1180,10 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     if (tiled) {
         cuuint64_t dims[2] = {(cuuint64_t)d.c_in, (cuuint64_t)M};
         cuuint64_t strides[1] = {(cuuint64_t)d.c_in * 2};
-        cuuint32_t box[2] = {BK, (cuuint32_t)(BM * plan.ms)};
+        cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)(BM * plan.ms)};
         cuuint32_t es[2] = {1, 1};
         r = g_encode_tiled(&ta, dt, 2, const_cast<void*>(a.x), dims, strides, box, es,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
         cuuint64_t dims[4] = {(cuuint64_t)d.c_in, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
@@ -1130,9 +1193,8 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
         int lower[2] = {-d.pad, -d.pad};
         int upper[2] = {d.pad - (d.kw - 1), d.pad - (d.kh - 1)};
         cuuint32_t es[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
-        r = g_encode_im2col(&ta, dt, 4, const_cast<void*>(a.x), dims, strides, lower, upper, BK,
-                            BM * plan.ms, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B,
+        r = g_encode_im2col(&ta, dt, 4, const_cast<void*>(a.x), dims, strides, lower, upper, bk,
+                            BM * plan.ms, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
@@ -1142,10 +1204,10 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     {
         cuuint64_t dims[3] = {(cuuint64_t)d.c_in, (cuuint64_t)taps, (cuuint64_t)d.c_out};
         cuuint64_t strides[2] = {(cuuint64_t)d.c_in * 2, (cuuint64_t)taps * d.c_in * 2};
-        cuuint32_t box[3] = {BK, 1, (cuuint32_t)bn};
+        cuuint32_t box[3] = {(cuuint32_t)bk, 1, (cuuint32_t)bn};
         cuuint32_t es[3] = {1, 1, 1};
         r = g_encode_tiled(&tb, dt, 3, const_cast<void*>(a.w), dims, strides, box, es,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
@@ -1166,7 +1228,7 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     prm.C_out = d.c_out;
     prm.taps = taps;
     prm.KW = d.kw;
-    prm.kb_per_tap = (d.c_in + BK - 1) / BK;
+    prm.kb_per_tap = (d.c_in + bk - 1) / bk;
     prm.num_kb = taps * prm.kb_per_tap;
     prm.num_m_tiles = num_m_tiles;
     prm.splits = plan.splits;
@@ -1188,8 +1250,8 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     prm.budget = wait_budget_polls();
     if (!prm.status) return ACNN_ERR_CUDA;
     const bool bf16 = d.dtype == ACNN_BF16;
-    int st = bf16 ? launch_typed<__nv_bfloat16>(a, bn, plan.ms, maps, prm, s)
-                  : launch_typed<__half>(a, bn, plan.ms, maps, prm, s);
+    int st = bf16 ? launch_typed<__nv_bfloat16>(a, plan, maps, prm, s)
+                  : launch_typed<__half>(a, plan, maps, prm, s);
     if (st != ACNN_OK || plan.splits == 1) return st;
     const cudaError_t e = bf16 ? launch_reduce<__nv_bfloat16>(a, plan, M, s)
                                : launch_reduce<__half>(a, plan, M, s);

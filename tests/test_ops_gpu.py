@@ -81,6 +81,12 @@ TC_CASES = [
     ("7x7_s2", 2, 19, 21, 16, 64, 7, 2, 3),
     ("1x1_s2", 2, 9, 10, 64, 64, 1, 2, 0),
     ("3x3_big_m", 2, 40, 41, 64, 64, 3, 1, 1),
+    # C_in <= 32: 32-channel k-blocks (64-byte swizzle), BN = 32/64/128
+    ("3x3_cin32_cout64_big", 2, 40, 37, 32, 64, 3, 1, 1),
+    ("3x3_cin24_cout32", 1, 21, 23, 24, 32, 3, 1, 1),
+    ("1x1_cin16_cout128", 1, 30, 30, 16, 128, 1, 1, 0),
+    ("3x3_cin32_cout96", 1, 19, 22, 32, 96, 3, 1, 1),
+    ("3x3_s2_cin8", 2, 33, 29, 8, 48, 3, 2, 1),
 ]
 
 
@@ -100,6 +106,20 @@ def test_conv_tensor_epilogue_modes(act, res_mode):
     y, ref = conv_case(f"epi{act}{res_mode}", 2, 10, 14, 64, 128, 3, 1, 1, "bf16", act=act,
                        res_mode=res_mode)
     assert_parity(y, ref, torch.bfloat16, f"act{act} res{res_mode}")
+
+
+# Several tiles per CTA (more tiles than SMs), so the epilogue's residual ring
+# and its bias prefetch cross tile boundaries; a ragged second column tile
+# (C_out = 96 with 64-wide tiles) in the second case.
+@pytest.mark.parametrize("shape", [(4, 96, 96, 64, 256), (4, 64, 64, 64, 96), (2, 80, 80, 32, 64)])
+@pytest.mark.parametrize("act,res_mode", [(A.ACT_RELU, A.RES_ADD_THEN_ACT),
+                                          (A.ACT_PRELU, A.RES_ACT_THEN_ADD),
+                                          (A.ACT_SILU, A.RES_NONE)])
+def test_conv_tensor_multi_tile_epilogue(shape, act, res_mode):
+    n, h, w, cin, cout = shape
+    y, ref = conv_case(f"mt{shape}", n, h, w, cin, cout, 1, 1, 0, "bf16", act=act,
+                       res_mode=res_mode)
+    assert_parity(y, ref, torch.bfloat16, f"multi-tile {shape}")
 
 
 def test_conv_tensor_no_bias():
