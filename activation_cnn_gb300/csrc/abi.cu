@@ -104,9 +104,14 @@ int conv_out(const acnn_conv_desc* d, int* oh, int* ow) {
 // channel strides (16-byte multiples), output rows of whole 16-byte vectors,
 // square kernels whose corner offsets fit the im2col descriptor, and 32-bit
 // pixel indices.
+// Largest C_out of the tensor-core paths: the NHWC epilogue keeps a copy of
+// the bias and PReLU alpha of every column in shared memory.
+constexpr int kTensorMaxCout = 4096;
+
 bool tensor_path_ok(const acnn_conv_desc* d, int oh, int ow) {
     if (d->dtype == ACNN_F32) return false;
     if (d->c_in % 8 != 0 || d->c_out % 8 != 0) return false;
+    if (d->c_out > kTensorMaxCout) return false;  // the epilogue's shared bias copy
     if (d->kh != d->kw || d->kh > 8 || d->stride > 8 || d->pad > 64) return false;
     if (d->pad - (d->kh - 1) < -128) return false;
     const long long m = (long long)d->n * oh * ow;
@@ -124,6 +129,7 @@ int packed_k(const acnn_conv_desc* d) { return (d->kh * d->kw * d->c_in + 7) / 8
 // (at most 512), where the packed matrix costs little next to the output.
 bool packed_path_ok(const acnn_conv_desc* d, int oh, int ow) {
     if (d->dtype == ACNN_F32 || d->c_out % 8 != 0 || tensor_path_ok(d, oh, ow)) return false;
+    if (d->c_out > kTensorMaxCout) return false;
     const long long m = (long long)d->n * oh * ow;
     return packed_k(d) <= 512 && m * packed_k(d) <= kIndexLimit &&
            (long long)d->n * d->h * d->w * d->c_in <= kIndexLimit &&

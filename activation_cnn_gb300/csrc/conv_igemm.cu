@@ -46,15 +46,15 @@ constexpr long long kDrainCycles = 400000000ll;     // ~0.2 s per drain wait
 
 constexpr uint32_t kStageBytes = 32 * 64;  // epilogue staging: 32 rows x 32 channels x 2 B
 constexpr uint32_t kEpiBytes = kEpiWarps * 2 /*buffers*/ * kStageBytes;
-constexpr uint32_t kParamBytes = kEpiWarps * 64 * 4;  // per warp: 32 biases + 32 alphas
 constexpr int kMaxStages = 8;
 constexpr int kMaxResDepth = 4;  // residual boxes in flight per epilogue warp
 constexpr size_t kBarBytes = 512;
 constexpr size_t kSmemMax = 232448;  // 227 KB of dynamic shared memory per CTA
-// Shared memory besides the operand ring and the residual ring.  The window
+// Shared memory besides the operand ring, the residual ring and the bias /
+// PReLU-alpha copy (par_floats fp32 values).  The window
 // must start 1024-byte aligned (the kernel checks): the swizzled operand
 // tiles and staging boxes rely on it.
-constexpr size_t kSmemFixed = kEpiBytes + kParamBytes + kBarBytes;
+constexpr size_t kSmemFixed = kEpiBytes + kBarBytes;
 static_assert((2 * kMaxStages + 6 + kEpiWarps * kMaxResDepth) * 8 + 8 <= kBarBytes,
               "barrier region too small");
 
@@ -93,6 +93,7 @@ struct Params {
     int stages;        // depth of the operand ring (2..kMaxStages)
     int res_depth;     // residual boxes in flight per epilogue warp (0: no residual)
     int b_resident;    // 1: all num_kb weight blocks loaded once, the ring carries A only
+    int par_floats;    // NHWC epilogue: shared copy of bias [cpad] then alpha [cpad] (0: none)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -360,17 +361,17 @@ __device__ __forceinline__ void epi32_any(int act, const float (&v)[32], const f
 }
 
 // The NHWC epilogue's form: the residual mode fixed at compile time (no
-// residual term at all without one), the bias and PReLU alpha read from a
-// shared-memory slot ([0, 32) bias, [32, 64) alpha) four at a time, and the
+// residual term at all without one), the 32 biases and PReLU alphas of the
+// chunk read from shared memory four at a time (bias[j], alpha[j]), and the
 // result written over the accumulator values.
 template <int ACT, int RES>
-__device__ __forceinline__ void epi32_slot(float (&v)[32], const float* slot,
+__device__ __forceinline__ void epi32_slot(float (&v)[32], const float* bias, const float* alpha,
                                            const float (&r)[32]) {
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
-        const float4 b4 = *reinterpret_cast<const float4*>(slot + j);
+        const float4 b4 = *reinterpret_cast<const float4*>(bias + j);
         float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if constexpr (ACT == ACNN_ACT_PRELU) a4 = *reinterpret_cast<const float4*>(slot + 32 + j);
+        if constexpr (ACT == ACNN_ACT_PRELU) a4 = *reinterpret_cast<const float4*>(alpha + j);
         const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
         const float aa[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
@@ -384,20 +385,22 @@ __device__ __forceinline__ void epi32_slot(float (&v)[32], const float* slot,
 }
 
 template <int ACT>
-__device__ __forceinline__ void epi32_slot_act(int res_mode, float (&v)[32], const float* slot,
-                                               const float (&r)[32]) {
-    if (res_mode == ACNN_RES_ADD_THEN_ACT) epi32_slot<ACT, ACNN_RES_ADD_THEN_ACT>(v, slot, r);
-    else if (res_mode == ACNN_RES_ACT_THEN_ADD) epi32_slot<ACT, ACNN_RES_ACT_THEN_ADD>(v, slot, r);
-    else epi32_slot<ACT, ACNN_RES_NONE>(v, slot, r);
+__device__ __forceinline__ void epi32_slot_act(int res_mode, float (&v)[32], const float* bias,
+                                               const float* alpha, const float (&r)[32]) {
+    if (res_mode == ACNN_RES_ADD_THEN_ACT) epi32_slot<ACT, ACNN_RES_ADD_THEN_ACT>(v, bias, alpha, r);
+    else if (res_mode == ACNN_RES_ACT_THEN_ADD)
+        epi32_slot<ACT, ACNN_RES_ACT_THEN_ADD>(v, bias, alpha, r);
+    else epi32_slot<ACT, ACNN_RES_NONE>(v, bias, alpha, r);
 }
 
 __device__ __forceinline__ void epi32_slot_mode(int act, int res_mode, float (&v)[32],
-                                                const float* slot, const float (&r)[32]) {
+                                                const float* bias, const float* alpha,
+                                                const float (&r)[32]) {
     switch (act) {  // both uniform across the CTA
-    case ACNN_ACT_RELU: epi32_slot_act<ACNN_ACT_RELU>(res_mode, v, slot, r); break;
-    case ACNN_ACT_SILU: epi32_slot_act<ACNN_ACT_SILU>(res_mode, v, slot, r); break;
-    case ACNN_ACT_PRELU: epi32_slot_act<ACNN_ACT_PRELU>(res_mode, v, slot, r); break;
-    default: epi32_slot_act<ACNN_ACT_NONE>(res_mode, v, slot, r); break;
+    case ACNN_ACT_RELU: epi32_slot_act<ACNN_ACT_RELU>(res_mode, v, bias, alpha, r); break;
+    case ACNN_ACT_SILU: epi32_slot_act<ACNN_ACT_SILU>(res_mode, v, bias, alpha, r); break;
+    case ACNN_ACT_PRELU: epi32_slot_act<ACNN_ACT_PRELU>(res_mode, v, bias, alpha, r); break;
+    default: epi32_slot_act<ACNN_ACT_NONE>(res_mode, v, bias, alpha, r); break;
     }
 }
 
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sO = sB + (size_t)(bres ? p.num_kb : S) * C::kBBytes;  // output staging
     uint8_t* sR = sO + kEpiBytes;       // residual ring: kEpiWarps x res_depth boxes
     float* sP = reinterpret_cast<float*>(sR + (size_t)kEpiWarps * p.res_depth * kStageBytes);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sP) + kParamBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + p.par_floats);
     // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, weights,
     // residual[8][res_depth]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 6 +
@@ -667,8 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Its chunks form one stream across tiles, walked by three cursors:
         //   * residual boxes arrive by TMA through a ring of res_depth buffers,
         //     up to res_depth chunks ahead (across tile boundaries);
-        //   * the bias and PReLU alpha of the next chunk are loaded a chunk
-        //     ahead, one channel per lane, then shared through a per-warp slot;
+        //   * the bias and PReLU alpha come from a shared-memory copy;
         //   * the 32 x 32 result goes to a 64-byte-swizzled staging buffer and
         //     leaves by a TMA store (which clips rows >= M and channels >= C_out).
         const int q = warp & 3;
@@ -678,7 +680,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nnt = p.num_n_tiles;
         uint8_t* ost = sO + e * 2 * kStageBytes;
         uint8_t* rst = sR + (size_t)e * RD * kStageBytes;
-        float* slot = sP + e * 64;  // [0, 32) bias, [32, 64) alpha of the current chunk
         const bool prelu = p.act == ACNN_ACT_PRELU;
         const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // 64-B swizzle of this lane's row
         // A cursor walks this warp's chunks: tile t (column tile nt = t % nnt),
@@ -729,20 +730,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 settle(rc);
             }
         };
-        // parameter cursor: this lane's bias / alpha of the chunk after the current one
-        Cursor pc;
-        start_cursor(pc);
-        float bnext = 0.f, anext = 0.f;
-        auto fetch_params = [&]() {
-            if (pc.t < num_tiles) {
-                const int ch = cursor_col(pc) + lane;
-                bnext = (p.bias && ch < p.C_out) ? __ldg(p.bias + ch) : 0.f;
-                anext = (prelu && ch < p.C_out) ? __ldg(p.alpha + ch) : 0.f;
-                pc.ci += 2;
-                settle(pc);
-            }
-        };
-        fetch_params();
+        // bias (and PReLU alpha) of every column, zero past C_out, copied once
+        // into shared memory by the epilogue warps, which then sync among
+        // themselves (named barrier 1)
+        const int cpad = prelu ? p.par_floats / 2 : p.par_floats;
+        for (int i = threadIdx.x - 64; i < cpad; i += 32 * kEpiWarps) {
+            sP[i] = (p.bias && i < p.C_out) ? __ldg(p.bias + i) : 0.f;
+            if (prelu) sP[cpad + i] = i < p.C_out ? __ldg(p.alpha + i) : 0.f;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
         refill();
         int acc = 0, ob = 0;
         uint32_t acc_phase = 0;
@@ -765,9 +761,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int c = ci * 32;
                 ci += 2;
                 const int row0 = m0 + ms * BM + q * 32;
-                slot[lane] = bnext;
-                slot[32 + lane] = anext;
-                fetch_params();
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
                               (uint32_t)(acc * MS * BN + ms * BN + c),
@@ -796,8 +789,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = 0.f;
                 }
-                __syncwarp();  // the slot written above is visible to every lane
-                epi32_slot_mode(p.act, RD > 0 ? p.res_mode : ACNN_RES_NONE, v, slot, r);
+                epi32_slot_mode(p.act, RD > 0 ? p.res_mode : ACNN_RES_NONE, v, sP + n0 + c,
+                                sP + cpad + n0 + c, r);
                 // the store that last used this staging buffer must have read it
                 if (lane == 0) bulk_wait_read<1>();
                 __syncwarp();
@@ -1046,8 +1039,14 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     // (loaded once per CTA), the ring then carrying A alone: chosen when that
     // still leaves a ring of 3 (or one as deep as without).
     const size_t b_all = (size_t)prm.num_kb * C::kBBytes;
+    // shared bias / alpha copy for the NHWC epilogue: every column tile's
+    // columns, so reads past C_out in a ragged last tile stay inside
+    const bool nhwc_epi = prm.out_layout == ACNN_NHWC && !prm.part;
+    prm.par_floats = nhwc_epi ? prm.num_n_tiles * BN * (prm.act == ACNN_ACT_PRELU ? 2 : 1) : 0;
+    const size_t par_bytes = (size_t)prm.par_floats * 4;
     auto stages_for = [&](bool resident) -> int {
-        size_t left = kSmemMax - kSmemFixed - (size_t)kEpiWarps * rd * kStageBytes;
+        if (kSmemFixed + (size_t)kEpiWarps * rd * kStageBytes + par_bytes > kSmemMax) return 0;
+        size_t left = kSmemMax - kSmemFixed - (size_t)kEpiWarps * rd * kStageBytes - par_bytes;
         if (resident) {
             if (left < b_all) return 0;
             left -= b_all;
@@ -1061,8 +1060,8 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     prm.b_resident = resident ? 1 : 0;
     prm.stages = resident ? s_res : s_ring;
     prm.res_depth = rd;
-    if (prm.stages < 2) return ACNN_ERR_UNSUPPORTED;  // excluded by Cfg's static_assert
-    const size_t smem = kSmemFixed + (size_t)kEpiWarps * rd * kStageBytes +
+    if (prm.stages < 2) return ACNN_ERR_UNSUPPORTED;  // C_out too large for the bias copy
+    const size_t smem = kSmemFixed + (size_t)kEpiWarps * rd * kStageBytes + par_bytes +
                         (size_t)prm.stages * (C::kAB + (resident ? 0 : C::kBBytes)) +
                         (resident ? b_all : 0);
     const int tiles = prm.num_m_tiles * prm.num_n_tiles * prm.splits;

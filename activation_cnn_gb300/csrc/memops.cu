@@ -405,43 +405,70 @@ __global__ void __launch_bounds__(kThreads) deconv_kernel(
 // row m = output pixel, k = (ky, kx, ci), taps outside the input are zero),
 // padded with zeros from K = kh*kw*C to Kp (a multiple of 8) so that rows are
 // 16-byte aligned for the tensor-core GEMM.  Values are copied as raw 16-bit
-// patterns.  One thread per output pixel and group of 8 k.
+// patterns.
+// One block per (image, output row, segment of TP output pixels): the KH input
+// rows the segment reads -- columns [ox0*S - P, ox0*S - P + RW) with
+// RW = (TP - 1)*S + KW, every channel -- are staged in shared memory as
+// [ky][px][c], zero outside the image, so that packed element k of output
+// pixel px sits at staged offset px*S*C + (k / (KW*C))*RL + k % (KW*C)
+// (RL = RW*C).  That offset minus px*S*C depends on k alone and is tabulated
+// once per block; consecutive threads then write consecutive 16-byte chunks
+// (8 k) of the segment's packed rows.
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) im2col_pack_kernel(
-    const uint16_t* __restrict__ x, uint16_t* __restrict__ a, int layout, int N, int H, int W,
-    int C, int KH, int KW, int S, int P, int OH, int OW, int Kp) {
-    const int KG = Kp / 8, K = KH * KW * C;
-    const uint32_t total = (uint32_t)N * OH * OW * KG;
-    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += gridDim.x * blockDim.x) {
-        const uint32_t m = i / KG;
-        const int g = (int)(i - m * KG);
-        const int ox = (int)(m % OW);
-        const uint32_t t = m / OW;
-        const int oy = (int)(t % OH), n = (int)(t / OH);
-        // (tap, channel) of the chunk's first k, then stepped along k
-        const int k0 = g * 8;
-        const int tap0 = k0 / C;
-        int ci = k0 - tap0 * C, ky = tap0 / KW, kx = tap0 - (tap0 / KW) * KW;
-        Vec<uint16_t, 8> v;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            uint16_t val = 0;
-            if (k0 + j < K) {
-                const int iy = oy * S + ky - P, ix = ox * S + kx - P;
-                if (iy >= 0 && iy < H && ix >= 0 && ix < W)
-                    val = x[act_index(layout, C, H, W, n, ci, iy, ix)];
-            }
-            v.v[j] = val;
-            if (++ci == C) {
-                ci = 0;
-                if (++kx == KW) {
-                    kx = 0;
-                    ++ky;
-                }
+    const uint16_t* __restrict__ x, uint16_t* __restrict__ a, int layout, int H, int W, int C,
+    int KH, int KW, int S, int P, int OH, int OW, int Kp, int TP, int segs) {
+    extern __shared__ __align__(16) uint16_t st[];
+    const int RW = (TP - 1) * S + KW;  // staged pixels per input row
+    const int RL = RW * C;             // staged values per input row
+    int* tab = reinterpret_cast<int*>(st + ((KH * RL + 1) & ~1));  // [Kp] staged offsets
+    int b = blockIdx.x;
+    const int seg = b % segs;
+    b /= segs;
+    const int oy = b % OH, n = b / OH;
+    const int ox0 = seg * TP;
+    const int np = min(TP, OW - ox0);
+    const int ix0 = ox0 * S - P, iy0 = oy * S - P;
+    const int K = KH * KW * C, KWC = KW * C;
+    for (int k = threadIdx.x; k < Kp; k += blockDim.x)
+        tab[k] = k < K ? (k / KWC) * RL + k % KWC : -1;
+    // staged values [lo, hi) of a row lie inside the image (pixels 0..W-1)
+    const int lo = max(0, -ix0) * C, hi = max(0, min(RW, W - ix0)) * C;
+    for (int ky = 0; ky < KH; ++ky) {
+        const int iy = iy0 + ky;
+        uint16_t* row = st + ky * RL;
+        if (iy < 0 || iy >= H) {
+            for (int e = threadIdx.x; e < RL; e += blockDim.x) row[e] = 0;
+        } else if (layout == ACNN_NHWC) {
+            // the row's staged pixels are contiguous in an NHWC image
+            const long long base = ((long long)n * H + iy) * W * C + (long long)ix0 * C;
+            for (int e = threadIdx.x; e < RL; e += blockDim.x)
+                row[e] = (e >= lo && e < hi) ? x[base + e] : (uint16_t)0;
+        } else {
+            // NCHW: pixel fastest for coalesced plane reads
+            for (int e = threadIdx.x; e < RL; e += blockDim.x) {
+                const int c = e / RW, px = e - c * RW;
+                const int ix = ix0 + px;
+                row[px * C + c] = (ix >= 0 && ix < W)
+                                      ? x[(((long long)n * C + c) * H + iy) * W + ix]
+                                      : (uint16_t)0;
             }
         }
-        *reinterpret_cast<Vec<uint16_t, 8>*>(a + (long long)m * Kp + g * 8) = v;
+    }
+    __syncthreads();
+    const int KG = Kp / 8;
+    uint16_t* out = a + ((long long)(n * OH + oy) * OW + ox0) * Kp;
+    for (int j = threadIdx.x; j < np * KG; j += blockDim.x) {
+        const int px = j / KG, g = j - px * KG;
+        const uint16_t* src = st + px * S * C;
+        const int* t8 = tab + g * 8;
+        Vec<uint16_t, 8> v;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const int o = t8[jj];
+            v.v[jj] = o >= 0 ? src[o] : (uint16_t)0;
+        }
+        *reinterpret_cast<Vec<uint16_t, 8>*>(out + (long long)px * Kp + g * 8) = v;
     }
 }
 
@@ -674,10 +701,21 @@ cudaError_t launch_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_
 
 cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, const void* x,
                                void* a, const void* w, void* wp, cudaStream_t s) {
-    const long long work = (long long)d.n * oh * ow * (kp / 8);
-    im2col_pack_kernel<<<grid_for(work, kThreads), kThreads, 0, s>>>(
-        static_cast<const uint16_t*>(x), static_cast<uint16_t*>(a), d.layout, d.n, d.h, d.w,
-        d.c_in, d.kh, d.kw, d.stride, d.pad, oh, ow, kp);
+    // segment width: a whole output row, halved until the staged rows and the
+    // offset table take at most 32 KB of shared memory (tp = 1 needs at most
+    // 3 KB: K <= 512)
+    auto staged = [&](int tp) {
+        return (size_t)((d.kh * ((tp - 1) * d.stride + d.kw) * d.c_in + 1) & ~1) * 2 +
+               (size_t)kp * 4;
+    };
+    int tp = ow;
+    while (tp > 1 && staged(tp) > 32768) tp = (tp + 1) / 2;
+    const int segs = (ow + tp - 1) / tp;
+    const long long blocks = (long long)d.n * oh * segs;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    im2col_pack_kernel<<<(unsigned)blocks, kThreads, staged(tp), s>>>(
+        static_cast<const uint16_t*>(x), static_cast<uint16_t*>(a), d.layout, d.h, d.w, d.c_in,
+        d.kh, d.kw, d.stride, d.pad, oh, ow, kp, tp, segs);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     weight_pack_kernel<<<grid_for((long long)d.c_out * kp, kThreads), kThreads, 0, s>>>(

@@ -106,11 +106,12 @@ typedef struct {
  *              that, up to acnn_conv2d_workspace_size(d) bytes let the
  *              tensor cores split K across more SMs (fewer bytes select fewer
  *              splits; NULL / 0 bytes is valid when nothing is required).
- * fp16/bf16 convs with c_out % 8 == 0 run on the tensor cores: x is read by
- * TMA (tiled for 1x1/s1/p0, im2col otherwise) when c_in % 8 == 0 and the
- * kernel is square; other such convs whose kh*kw*c_in is at most 512 are first
- * packed into an explicit im2col matrix in the workspace.  Every other valid
- * geometry (fp32 storage included) runs the direct FFMA kernel.
+ * fp16/bf16 convs with c_out % 8 == 0 and c_out <= 4096 run on the tensor
+ * cores: x is read by TMA (tiled for 1x1/s1/p0, im2col otherwise) when
+ * c_in % 8 == 0 and the kernel is square; other such convs whose kh*kw*c_in is
+ * at most 512 are first packed into an explicit im2col matrix in the
+ * workspace.  Every other valid geometry (fp32 storage included) runs the
+ * direct FFMA kernel.
  */
 int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w,
                       const float* bias, const float* alpha, const void* residual,
@@ -131,7 +132,7 @@ size_t acnn_conv2d_workspace_size(const acnn_conv_desc* d);
 int acnn_conv2d_path(const acnn_conv_desc* d);
 
 /* Tensor-core plan for d given ws_bytes of workspace: output pixels per tile
- * (*rows: 128/256), output channels per tile (*bn: 64/128/256) and K splits
+ * (*rows: 128/256), output channels per tile (*bn: 32/64/128/256) and K splits
  * (*splits, 1 = none).  Returns 0, or -1 when d does not take the tensor-core
  * path or ws_bytes is below the required staging (host pointers; the plan
  * depends on the current device's SM count). */

@@ -85,6 +85,9 @@ def test_conv_path_selection(A):
     assert A.acnn_conv2d_path(desc(A, c_in=8, c_out=64, kw=1, pad=0)) == 3  # non-square
     assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=64, kw=1, pad=0)) == 3
     assert A.acnn_conv2d_path(desc(A, c_in=100, c_out=64, kh=3, kw=3)) == 0  # K > 512
+    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=4096)) == 2
+    assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=4104)) == 0      # C_out > 4096
+    assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=4104)) == 0
     assert A.acnn_conv2d_workspace_size(desc(A, c_in=3, c_out=32)) >= 64 * 32 * 2
     assert A.acnn_conv2d_path(desc(A, n=0)) == -1
     assert A.acnn_conv2d_workspace_size(desc(A, c_in=64, c_out=64)) == 0
