@@ -10,6 +10,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -41,6 +42,28 @@ int sm_count() {
         g_sm_count[dev] = n;
     }
     return g_sm_count[dev];
+}
+
+int occupancy_blocks(const void* kernel, int threads, size_t smem) {
+    struct Entry {
+        const void* k;
+        int threads;
+        size_t smem;
+        int dev;
+        int blocks;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : cache)
+        if (e.k == kernel && e.threads == threads && e.smem == smem && e.dev == dev) return e.blocks;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess ||
+        n <= 0)
+        n = 1;
+    cache.push_back(Entry{kernel, threads, smem, dev, n});
+    return n;
 }
 
 int* device_status_ptr() {

@@ -136,6 +136,21 @@ cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, 
 cudaError_t launch_nchw_to_nhwc(int n, int c, int hw, int elem_bytes, const void* x, void* y,
                                 cudaStream_t s);
 
+// Resident blocks of `kernel` per SM at this block size (cached per kernel).
+int occupancy_blocks(const void* kernel, int threads, size_t smem);
+
+// Grid for a grid-stride kernel: enough blocks for the work, at most one wave
+// of the blocks that can be resident at once (occupancy from the kernel's
+// registers and shared memory), so no block waits for a second wave.
+template <typename Kern>
+inline int grid_occ(Kern kernel, long long work_items, int threads, size_t smem = 0) {
+    long long want = (work_items + threads - 1) / threads;
+    long long cap = (long long)sm_count() *
+                    occupancy_blocks(reinterpret_cast<const void*>(kernel), threads, smem);
+    if (want > cap) want = cap;
+    return want < 1 ? 1 : (int)want;
+}
+
 inline int grid_for(long long work_items, int threads, int per_sm = 8) {
     long long want = (work_items + threads - 1) / threads;
     long long cap = (long long)sm_count() * per_sm;

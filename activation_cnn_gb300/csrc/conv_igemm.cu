@@ -21,8 +21,8 @@
 //           MMAs per k-block into an fp32 TMEM accumulator
 //   warps 2-9  epilogue, two per TMEM lane quarter: tcgen05.ld 32 columns at
 //           a time, + bias, activation, residual (before or after the
-//           activation), down-cast, TMA store; residual boxes stream in by TMA
-//           several chunks ahead.
+//           activation), down-cast, 16-byte stores through a shared-memory
+//           slot; residual boxes stream in by cp.async several chunks ahead.
 // Two TMEM accumulators alternate so the epilogue of one tile overlaps the
 // MMAs of the next.  Every mbarrier wait is bounded: on expiry the kernel
 // records ACNN_ERR_DEVICE_TIMEOUT in a device status word, raises a CTA-wide
@@ -44,19 +44,16 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue warps
 constexpr long long kTimeoutCycles = 8000000000ll;  // ~4 s per wait at 2 GHz
 constexpr long long kDrainCycles = 400000000ll;     // ~0.2 s per drain wait
 
-constexpr uint32_t kStageBytes = 32 * 64;  // epilogue staging: 32 rows x 32 channels x 2 B
-constexpr uint32_t kEpiBytes = kEpiWarps * 2 /*buffers*/ * kStageBytes;
+constexpr uint32_t kStageBytes = 32 * 64;  // epilogue slot: 32 rows x 32 channels x 2 B
 constexpr int kMaxStages = 8;
 constexpr int kMaxResDepth = 4;  // residual boxes in flight per epilogue warp
 constexpr size_t kBarBytes = 512;
 constexpr size_t kSmemMax = 232448;  // 227 KB of dynamic shared memory per CTA
-// Shared memory besides the operand ring, the residual ring and the bias /
-// PReLU-alpha copy (par_floats fp32 values).  The window
-// must start 1024-byte aligned (the kernel checks): the swizzled operand
-// tiles and staging boxes rely on it.
-constexpr size_t kSmemFixed = kEpiBytes + kBarBytes;
-static_assert((2 * kMaxStages + 6 + kEpiWarps * kMaxResDepth) * 8 + 8 <= kBarBytes,
-              "barrier region too small");
+// Shared memory besides the operand ring, the epilogue slots and the bias /
+// PReLU-alpha copy (par_floats fp32 values).  The window must start 1024-byte
+// aligned (the kernel checks): the swizzled operand tiles rely on it.
+constexpr size_t kSmemFixed = kBarBytes;
+static_assert((2 * kMaxStages + 6) * 8 + 8 <= kBarBytes, "barrier region too small");
 
 // Tile of (128 * MS) output pixels x BN output channels, K in blocks of BK
 // channels: MS row blocks of 128 share each B tile, so one pipeline step
@@ -70,9 +67,9 @@ template <int BN, int MS, int BK> struct Cfg {
     static constexpr uint32_t kBBytes = BN * BK * 2;
     static constexpr uint32_t kTmemCols = 2 * MS * BN < 32 ? 32 : 2 * MS * BN;
     static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
-    static_assert(kSmemFixed + (size_t)kEpiWarps * kMaxResDepth * kStageBytes + 2 * (kAB + kBBytes) <=
-                      kSmemMax,
-                  "two stages and the deepest residual ring must fit");
+    static_assert(kSmemFixed + (size_t)kEpiWarps * kMaxResDepth * kStageBytes + 2 * (kAB + kBBytes) +
+                          4096 * 4 * 2 <= kSmemMax,
+                  "two stages, the deepest residual ring and the largest bias copy must fit");
 };
 
 struct Params {
@@ -94,6 +91,7 @@ struct Params {
     int res_depth;     // residual boxes in flight per epilogue warp (0: no residual)
     int b_resident;    // 1: all num_kb weight blocks loaded once, the ring carries A only
     int par_floats;    // NHWC epilogue: shared copy of bias [cpad] then alpha [cpad] (0: none)
+    int ring_slots;    // NHWC epilogue: 2 KB slots per epilogue warp (0: other epilogues)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -196,29 +194,24 @@ __device__ __forceinline__ void tma_load_im2col(uint32_t dst, const CUtensorMap*
         : "memory");
 }
 
-// Tiled TMA store of a shared-memory box to global; tracked by bulk groups.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0,
-                                             int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(src), "r"(c0), "r"(c1)
-        : "memory");
+// 16-byte asynchronous global -> shared copy (L2 only); src_bytes = 0 writes
+// zeros without reading.  Groups of copies are committed and waited on per
+// thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
 }
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
 }
-// Wait until at most N committed store groups still read shared memory.
-template <int N> __device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Wait until every committed store group has completed.
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-// Order this thread's generic-proxy shared-memory writes before async-proxy (TMA) reads.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// Wait until at most n (0..3, larger values act as 3) of this thread's
+// committed groups are still pending.
+__device__ __forceinline__ void cp_async_wait_newer(int n) {
+    if (n <= 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
+    else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else if (n == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+    else asm volatile("cp.async.wait_group 3;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
@@ -426,9 +419,7 @@ __device__ __forceinline__ void load_chunk_params(const float* __restrict__ bias
 template <int BN, int MS, int BK, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_conv_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                      const __grid_constant__ CUtensorMap tmap_b,
-                      const __grid_constant__ CUtensorMap tmap_y,
-                      const __grid_constant__ CUtensorMap tmap_r, const Params p) {
+                      const __grid_constant__ CUtensorMap tmap_b, const Params p) {
     using C = Cfg<BN, MS, BK>;
     constexpr int TM = BM * MS;  // output pixels per tile
     extern __shared__ uint8_t smem_raw[];
@@ -442,14 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool bres = p.b_resident != 0;
     uint8_t* sA = smem_raw;
     uint8_t* sB = sA + S * C::kAB;  // B ring (S slots) or all num_kb resident B blocks
-    uint8_t* sO = sB + (size_t)(bres ? p.num_kb : S) * C::kBBytes;  // output staging
-    uint8_t* sR = sO + kEpiBytes;       // residual ring: kEpiWarps x res_depth boxes
-    float* sP = reinterpret_cast<float*>(sR + (size_t)kEpiWarps * p.res_depth * kStageBytes);
+    // epilogue slots: kEpiWarps x ring_slots x 2 KB, 1024-aligned
+    uint8_t* sR = sB + (size_t)(bres ? p.num_kb : S) * C::kBBytes;
+    float* sP = reinterpret_cast<float*>(sR + (size_t)kEpiWarps * p.ring_slots * kStageBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sP + p.par_floats);
-    // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, weights,
-    // residual[8][res_depth]
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 6 +
-                                                        kEpiWarps * kMaxResDepth);
+    // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, weights
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 6);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -460,7 +449,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
     const uint32_t wres_bar = bar0 + 8u * (2 * S + 5);  // resident weights landed
-    auto res_bar = [&](int e, int b) { return bar0 + 8u * (2 * S + 6 + kMaxResDepth * e + b); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -473,16 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(drain_bar, 1);
         mbar_init(wres_bar, 1);
-        for (int e = 0; e < kEpiWarps; ++e)
-            for (int b = 0; b < p.res_depth; ++b) mbar_init(res_bar(e, b), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
-        if (p.out_layout == ACNN_NHWC) {
-            prefetch_tmap(&tmap_y);
-            if (p.res_mode != ACNN_RES_NONE) prefetch_tmap(&tmap_r);
-        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
@@ -667,21 +649,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------- epilogue warps, NHWC
         // Warp e (0..7) owns the 32 rows of its TMEM lane quarter (warp % 4) and
         // every other 32-channel chunk of each tile (e / 4 picks even or odd).
-        // Its chunks form one stream across tiles, walked by three cursors:
-        //   * residual boxes arrive by TMA through a ring of res_depth buffers,
-        //     up to res_depth chunks ahead (across tile boundaries);
-        //   * the bias and PReLU alpha come from a shared-memory copy;
-        //   * the 32 x 32 result goes to a 64-byte-swizzled staging buffer and
-        //     leaves by a TMA store (which clips rows >= M and channels >= C_out).
+        // Its chunks form one stream across tiles.  Each chunk uses one 2 KB
+        // slot of the warp's ring in shared memory (32 rows x 64 B, 16-byte
+        // pieces swizzled by row so that both row-wise and column-wise accesses
+        // are free of bank conflicts):
+        //   * with a residual, the ring has res_depth slots and the residual
+        //     box of a chunk is copied in by cp.async up to res_depth chunks
+        //     ahead (across tile boundaries), eight 64-byte rows per warp
+        //     instruction;
+        //   * the result of the chunk is written over its row of the slot, then
+        //     read back eight rows per instruction and stored with 16-byte
+        //     stores (rows >= M and channels >= C_out are skipped);
+        //   * the bias and PReLU alpha come from a shared-memory copy.
         const int q = warp & 3;
         const int e = warp - 2;
         const int half = e >> 2;
         const int RD = p.res_depth;  // 0 without a residual
         const int nnt = p.num_n_tiles;
-        uint8_t* ost = sO + e * 2 * kStageBytes;
-        uint8_t* rst = sR + (size_t)e * RD * kStageBytes;
+        uint8_t* ring = sR + (size_t)e * (RD > 0 ? RD : 1) * kStageBytes;
+        const T* res = static_cast<const T*>(p.res);
+        T* y = static_cast<T*>(p.y);
         const bool prelu = p.act == ACNN_ACT_PRELU;
-        const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // 64-B swizzle of this lane's row
+        const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // swizzle of this lane's row
+        const int crow = lane >> 2, cpiece = lane & 3;     // row-major copy pattern
+        // byte offset of 16-byte piece j of row r inside a slot
+        auto piece = [](int r, int j) { return r * 64 + ((j ^ ((r >> 1) & 3)) << 4); };
         // A cursor walks this warp's chunks: tile t (column tile nt = t % nnt),
         // row block ms, 32-channel chunk ci within the row block.
         const int nch_full = BN / 32;
@@ -703,27 +695,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 c.ci = half;
             }
         };
-        auto start_cursor = [&](Cursor& c) {
-            c = Cursor{(int)blockIdx.x, nnt == 1 ? 0 : (int)blockIdx.x % nnt, 0, half};
-            settle(c);
-        };
-        auto cursor_col = [&](const Cursor& c) { return c.nt * BN + c.ci * 32; };
-        auto cursor_row = [&](const Cursor& c) {
-            return (nnt == 1 ? c.t : c.t / nnt) * TM + c.ms * BM + q * 32;
-        };
         // residual cursor
-        Cursor rc;
-        start_cursor(rc);
+        Cursor rc{(int)blockIdx.x, nnt == 1 ? 0 : (int)blockIdx.x % nnt, 0, half};
+        settle(rc);
         int pend = 0, wb = 0, rb = 0;
-        uint32_t rpar = 0;
         auto refill = [&]() {
             while (pend < RD && rc.t < num_tiles) {
-                if (lane == 0) {
-                    const uint32_t bar = res_bar(e, wb);
-                    mbar_arrive_expect_tx(bar, kStageBytes);
-                    tma_load_2d(smem_u32(rst + wb * kStageBytes), &tmap_r, bar, cursor_col(rc),
-                                cursor_row(rc));
+                const int row0 = (nnt == 1 ? rc.t : rc.t / nnt) * TM + rc.ms * BM + q * 32;
+                const int col = rc.nt * BN + rc.ci * 32 + cpiece * 8;
+                const uint32_t sl = smem_u32(ring + wb * kStageBytes);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 8 * k + crow;
+                    const bool in = row0 + r < p.M && col < p.C_out;
+                    const T* src = res + (in ? (long long)(row0 + r) * p.C_out + col : 0);
+                    cp_async16(sl + piece(r, cpiece), src, in ? 16u : 0u);
                 }
+                cp_async_commit();
                 wb = wb + 1 == RD ? 0 : wb + 1;
                 ++pend;
                 rc.ci += 2;
@@ -740,10 +728,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
         refill();
-        int acc = 0, ob = 0;
+        int acc = 0;
         uint32_t acc_phase = 0;
-        bool aborted = false;
-        for (int tile = blockIdx.x; !aborted && tile < num_tiles; tile += gridDim.x) {  // splits == 1
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {  // splits == 1
             const int mt = nnt == 1 ? tile : tile / nnt;
             const int m0 = mt * TM;
             const int n0 = (tile - mt * nnt) * BN;
@@ -759,22 +746,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++ms;
                 }
                 const int c = ci * 32;
+                const int msc = ms;
                 ci += 2;
                 const int row0 = m0 + ms * BM + q * 32;
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
-                              (uint32_t)(acc * MS * BN + ms * BN + c),
+                              (uint32_t)(acc * MS * BN + msc * BN + c),
                           v);
+                uint8_t* slot = ring + (RD > 0 ? rb : 0) * kStageBytes;
                 float r[32];
                 if (RD > 0) {
-                    const bool okr = __all_sync(
-                        0xffffffffu, wait_phase(res_bar(e, rb), (rpar >> rb) & 1u, abort_flag, p));
-                    if (!okr) {
-                        aborted = true;
-                        break;
-                    }
-                    rpar ^= 1u << rb;
-                    const uint8_t* rrow = rst + rb * kStageBytes + lane * 64;
+                    // this chunk's box is the oldest in flight: let the newer
+                    // pend - 1 stay pending, then see every lane's part of it
+                    cp_async_wait_newer(pend - 1);
+                    __syncwarp();
+                    const uint8_t* rrow = slot + lane * 64;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const uint4 u = *reinterpret_cast<const uint4*>(rrow + ((j ^ swz) << 4));
@@ -791,42 +777,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 epi32_slot_mode(p.act, RD > 0 ? p.res_mode : ACNN_RES_NONE, v, sP + n0 + c,
                                 sP + cpad + n0 + c, r);
-                // the store that last used this staging buffer must have read it
-                if (lane == 0) bulk_wait_read<1>();
-                __syncwarp();
-                uint8_t* orow = ost + ob * kStageBytes + lane * 64;
+                // this lane's row of results over its row of the slot
+                uint8_t* orow = slot + lane * 64;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     *reinterpret_cast<uint4*>(orow + ((j ^ swz) << 4)) = make_uint4(
                         pack2<T>(v[8 * j + 0], v[8 * j + 1]), pack2<T>(v[8 * j + 2], v[8 * j + 3]),
                         pack2<T>(v[8 * j + 4], v[8 * j + 5]), pack2<T>(v[8 * j + 6], v[8 * j + 7]));
-                // orders this lane's staging writes and its reads of the residual
-                // box before the async-proxy store and the box's refill below
-                fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tmap_y, smem_u32(ost + ob * kStageBytes), n0 + c, row0);
-                    bulk_commit();
+                // eight rows per instruction out to y
+                const int col = n0 + c + cpiece * 8;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int rr = 8 * k + crow;
+                    const uint4 u = *reinterpret_cast<const uint4*>(slot + piece(rr, cpiece));
+                    if (row0 + rr < p.M && col < p.C_out)
+                        *reinterpret_cast<uint4*>(y + (long long)(row0 + rr) * p.C_out + col) = u;
                 }
-                ob ^= 1;
+                __syncwarp();  // the slot is read out before a refill overwrites it
                 refill();
             }
-            if (aborted) break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
-        if (lane == 0) {
-            bulk_wait_all();  // every output box written before the CTA exits
-            for (int k = 0; k < pend; ++k) {  // residual boxes still in flight after an abort
-                const int b = (rb + k) % RD;
-                wait_drain(res_bar(e, b), (rpar >> b) & 1u);
-                rpar ^= 1u << b;
-            }
-        }
-        __syncwarp();
+        cp_async_wait_newer(0);  // no copy into shared memory outlives the CTA
     } else {
         // ---------------------------------------------------- epilogue warps, NCHW
         // Same row/chunk split as above; lane l holds output pixel m0 + 32q + l,
@@ -1015,7 +992,7 @@ bool load_encoders() {
 }
 
 struct Maps {
-    CUtensorMap a, b, y, r;
+    CUtensorMap a, b;
 };
 
 template <int BN, int MS, int BK, typename T>
@@ -1044,9 +1021,11 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     const bool nhwc_epi = prm.out_layout == ACNN_NHWC && !prm.part;
     prm.par_floats = nhwc_epi ? prm.num_n_tiles * BN * (prm.act == ACNN_ACT_PRELU ? 2 : 1) : 0;
     const size_t par_bytes = (size_t)prm.par_floats * 4;
+    prm.ring_slots = nhwc_epi ? (rd > 0 ? rd : 1) : 0;
+    const size_t ring_bytes = (size_t)kEpiWarps * prm.ring_slots * kStageBytes;
     auto stages_for = [&](bool resident) -> int {
-        if (kSmemFixed + (size_t)kEpiWarps * rd * kStageBytes + par_bytes > kSmemMax) return 0;
-        size_t left = kSmemMax - kSmemFixed - (size_t)kEpiWarps * rd * kStageBytes - par_bytes;
+        if (kSmemFixed + ring_bytes + par_bytes > kSmemMax) return 0;
+        size_t left = kSmemMax - kSmemFixed - ring_bytes - par_bytes;
         if (resident) {
             if (left < b_all) return 0;
             left -= b_all;
@@ -1061,12 +1040,12 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     prm.stages = resident ? s_res : s_ring;
     prm.res_depth = rd;
     if (prm.stages < 2) return ACNN_ERR_UNSUPPORTED;  // C_out too large for the bias copy
-    const size_t smem = kSmemFixed + (size_t)kEpiWarps * rd * kStageBytes + par_bytes +
+    const size_t smem = kSmemFixed + ring_bytes + par_bytes +
                         (size_t)prm.stages * (C::kAB + (resident ? 0 : C::kBBytes)) +
                         (resident ? b_all : 0);
     const int tiles = prm.num_m_tiles * prm.num_n_tiles * prm.splits;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    kern<<<grid, kThreads, smem, s>>>(m.a, m.b, m.y, m.r, prm);
+    kern<<<grid, kThreads, smem, s>>>(m.a, m.b, prm);
     return cudaGetLastError() == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
 }
 
@@ -1085,18 +1064,6 @@ int launch_typed(const ConvArgs& a, const IgemmPlan& pl, const Maps& m, const Pa
     if (pl.bn == 128) return pl.ms == 2 ? launch_bn<128, 2, 64, T>(a, m, prm, s)
                                         : launch_bn<128, 1, 64, T>(a, m, prm, s);
     return pl.ms == 2 ? launch_bn<64, 2, 64, T>(a, m, prm, s) : launch_bn<64, 1, 64, T>(a, m, prm, s);
-}
-
-// [M, C_out] NHWC output (or residual) viewed 2-D, 32 x 32 boxes, 64-byte swizzle.
-CUresult encode_out_map(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, int c_out,
-                        long long m) {
-    cuuint64_t dims[2] = {(cuuint64_t)c_out, (cuuint64_t)m};
-    cuuint64_t strides[1] = {(cuuint64_t)c_out * 2};
-    cuuint32_t box[2] = {32, 32};
-    cuuint32_t es[2] = {1, 1};
-    return g_encode_tiled(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 }  // namespace
@@ -1210,18 +1177,6 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
-    if (a.out_layout == ACNN_NHWC) {
-        if (encode_out_map(&maps.y, dt, a.y, d.c_out, M) != CUDA_SUCCESS) return ACNN_ERR_CUDA;
-        if (a.residual) {
-            if (encode_out_map(&maps.r, dt, a.residual, d.c_out, M) != CUDA_SUCCESS)
-                return ACNN_ERR_CUDA;
-        } else {
-            maps.r = maps.y;  // never read without a residual
-        }
-    } else {
-        maps.y = maps.r = maps.a;  // the NCHW epilogue stores with plain instructions
-    }
-
     Params prm{};
     prm.M = (int)M;
     prm.C_out = d.c_out;

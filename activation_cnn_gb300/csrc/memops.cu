@@ -440,10 +440,21 @@ __global__ void __launch_bounds__(kThreads) im2col_pack_kernel(
         if (iy < 0 || iy >= H) {
             for (int e = threadIdx.x; e < RL; e += blockDim.x) row[e] = 0;
         } else if (layout == ACNN_NHWC) {
-            // the row's staged pixels are contiguous in an NHWC image
+            // the row's staged pixels are contiguous in an NHWC image; eight
+            // loads per thread are issued before their stores
             const long long base = ((long long)n * H + iy) * W * C + (long long)ix0 * C;
-            for (int e = threadIdx.x; e < RL; e += blockDim.x)
-                row[e] = (e >= lo && e < hi) ? x[base + e] : (uint16_t)0;
+            constexpr int U = 8;
+            for (int e0 = threadIdx.x; e0 < RL; e0 += U * kThreads) {
+                uint16_t v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int e = e0 + u * kThreads;
+                    v[u] = (e >= lo && e < hi) ? x[base + e] : (uint16_t)0;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (e0 + u * kThreads < RL) row[e0 + u * kThreads] = v[u];
+            }
         } else {
             // NCHW: pixel fastest for coalesced plane reads
             for (int e = threadIdx.x; e < RL; e += blockDim.x) {
@@ -527,20 +538,20 @@ cudaError_t pool_typed(int kind, int n, int h, int w, int c, int k, int stride, 
         constexpr int V = 16 / sizeof(T);
         if (c % V == 0 && kind == ACNN_POOL_MAX && k == 3 && stride == 2 && pad == 1) {
             long long work = (long long)n * oh * ow * (c / V);
-            maxpool3s2_nhwc_kernel<T, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+            maxpool3s2_nhwc_kernel<T, V><<<grid_occ(maxpool3s2_nhwc_kernel<T, V>, work, kThreads), kThreads, 0, s>>>(
                 xt, yt, n, h, w, c, oh, ow);
         } else if (c % V == 0) {
             long long work = (long long)n * oh * ow * (c / V);
-            pool_nhwc_kernel<T, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+            pool_nhwc_kernel<T, V><<<grid_occ(pool_nhwc_kernel<T, V>, work, kThreads), kThreads, 0, s>>>(
                 xt, yt, kind, n, h, w, c, oh, ow, k, stride, pad);
         } else {
             long long work = (long long)n * oh * ow * c;
-            pool_nhwc_kernel<T, 1><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+            pool_nhwc_kernel<T, 1><<<grid_occ(pool_nhwc_kernel<T, 1>, work, kThreads), kThreads, 0, s>>>(
                 xt, yt, kind, n, h, w, c, oh, ow, k, stride, pad);
         }
     } else {
         long long work = (long long)n * c * oh * ow;
-        pool_nchw_kernel<T><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+        pool_nchw_kernel<T><<<grid_occ(pool_nchw_kernel<T>, work, kThreads), kThreads, 0, s>>>(
             xt, yt, kind, n, c, h, w, oh, ow, k, stride, pad);
     }
     return cudaGetLastError();
@@ -557,23 +568,23 @@ cudaError_t resize_typed(int mode, int n, int c, int h, int w, int oh, int ow, i
         if constexpr (sizeof(Ti) == sizeof(To)) {
             if (mode == ACNN_RESIZE_NEAREST && oh == 2 * h && ow == 2 * w && c % V == 0) {
                 long long work = (long long)n * h * w * (c / V);
-                up2_nhwc_kernel<Ti, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+                up2_nhwc_kernel<Ti, V><<<grid_occ(up2_nhwc_kernel<Ti, V>, work, kThreads), kThreads, 0, s>>>(
                     xt, reinterpret_cast<Ti*>(yt), n, h, w, c);
                 return cudaGetLastError();
             }
         }
         if (c % V == 0) {
             long long work = (long long)n * oh * ow * (c / V);
-            resize_nhwc_kernel<Ti, To, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+            resize_nhwc_kernel<Ti, To, V><<<grid_occ(resize_nhwc_kernel<Ti, To, V>, work, kThreads), kThreads, 0, s>>>(
                 xt, yt, mode, n, h, w, c, oh, ow, sy, sx);
         } else {
             long long work = (long long)n * oh * ow * c;
-            resize_nhwc_kernel<Ti, To, 1><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+            resize_nhwc_kernel<Ti, To, 1><<<grid_occ(resize_nhwc_kernel<Ti, To, 1>, work, kThreads), kThreads, 0, s>>>(
                 xt, yt, mode, n, h, w, c, oh, ow, sy, sx);
         }
     } else {
         long long work = (long long)n * c * oh * ow;
-        resize_nchw_kernel<Ti, To><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+        resize_nchw_kernel<Ti, To><<<grid_occ(resize_nchw_kernel<Ti, To>, work, kThreads), kThreads, 0, s>>>(
             xt, yt, mode, n * c, h, w, oh, ow, sy, sx);
     }
     return cudaGetLastError();
@@ -609,11 +620,11 @@ cudaError_t concat_typed(int n, int h, int w, int ca, int cb, int layout, const 
     T* yt = static_cast<T*>(y);
     if (ra % V == 0 && rb % V == 0) {
         long long work = runs * ((ra + rb) / V);
-        concat_kernel<T, V><<<grid_for(work, kThreads), kThreads, 0, s>>>(at, bt, yt, runs,
+        concat_kernel<T, V><<<grid_occ(concat_kernel<T, V>, work, kThreads), kThreads, 0, s>>>(at, bt, yt, runs,
                                                                           (int)ra, (int)rb);
     } else {
         long long work = runs * (ra + rb);
-        concat_kernel<T, 1><<<grid_for(work, kThreads), kThreads, 0, s>>>(at, bt, yt, runs,
+        concat_kernel<T, 1><<<grid_occ(concat_kernel<T, 1>, work, kThreads), kThreads, 0, s>>>(at, bt, yt, runs,
                                                                           (int)ra, (int)rb);
     }
     return cudaGetLastError();
@@ -625,7 +636,7 @@ cudaError_t deconv_typed(const acnn_conv_desc& d, int oh, int ow, const void* x,
                          cudaStream_t s) {
     long long work = (long long)d.n * oh * ow *
                      ((d.c_out + kDeconvCoBlock - 1) / kDeconvCoBlock);
-    deconv_kernel<Ti, To><<<grid_for(work, kThreads), kThreads, 0, s>>>(
+    deconv_kernel<Ti, To><<<grid_occ(deconv_kernel<Ti, To>, work, kThreads), kThreads, 0, s>>>(
         static_cast<const Ti*>(x), w, bias, alpha, static_cast<To*>(y), d.layout, d.n, d.c_in,
         d.c_out, d.h, d.w, oh, ow, d.kh, d.stride, d.pad, act);
     return cudaGetLastError();
@@ -718,7 +729,7 @@ cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, 
         d.kh, d.kw, d.stride, d.pad, oh, ow, kp, tp, segs);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    weight_pack_kernel<<<grid_for((long long)d.c_out * kp, kThreads), kThreads, 0, s>>>(
+    weight_pack_kernel<<<grid_occ(weight_pack_kernel, (long long)d.c_out * kp, kThreads), kThreads, 0, s>>>(
         static_cast<const uint16_t*>(w), static_cast<uint16_t*>(wp), d.layout, d.c_out, d.c_in,
         d.kh, d.kw, kp);
     return cudaGetLastError();
