@@ -14,12 +14,12 @@
 //     viewed as [C_out][kh*kw][C_in].
 //   * Both land in shared memory in the 128-byte-swizzled K-major layout that
 //     tcgen05.mma reads directly; a 64-channel k-block is one 128-byte row.
-// Warp roles (320 threads, persistent, one CTA per SM):
+// Warp roles (448 threads, persistent, one CTA per SM):
 //   warp 0  TMA producer (one lane) over a ring of operand stages in shared
 //           memory (as deep as the shared memory left by the epilogue allows)
 //   warp 1  TMEM allocator and MMA issuer (one lane): MS x 4 x (128 x BN x 16)
 //           MMAs per k-block into an fp32 TMEM accumulator
-//   warps 2-9  epilogue, two per TMEM lane quarter: tcgen05.ld 32 columns at
+//   warps 2-13 epilogue, three per TMEM lane quarter: tcgen05.ld 32 columns at
 //           a time, + bias, activation, residual (before or after the
 //           activation), down-cast, 16-byte stores through a shared-memory
 //           slot; residual boxes stream in by cp.async several chunks ahead.
@@ -39,7 +39,8 @@ namespace acnn {
 namespace {
 
 constexpr int BM = 128;             // output pixels per tile (TMEM lanes)
-constexpr int kEpiWarps = 8;        // two per TMEM lane quarter
+constexpr int kEpiGroups = 3;       // epilogue warps per TMEM lane quarter
+constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue warps
 constexpr long long kTimeoutCycles = 8000000000ll;  // ~4 s per wait at 2 GHz
 constexpr long long kDrainCycles = 400000000ll;     // ~0.2 s per drain wait
@@ -330,88 +331,65 @@ template <int ACT> __device__ __forceinline__ float act_fixed(float v, float alp
     else return v;
 }
 
-// 32 outputs of one row: act(acc + bias + kpre*res) + kpost*res, with
-// (kpre, kpost) = (1, 0) for a residual before the activation, (0, 1) after
-// it, (0, 0) without one.
-template <int ACT>
-__device__ __forceinline__ void epi32(const float (&v)[32], const float (&bv)[32],
-                                      const float (&av)[32], const float (&r)[32], float kpre,
-                                      float kpost, float (&o)[32]) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-        o[j] = fmaf(kpost, r[j], act_fixed<ACT>(fmaf(kpre, r[j], v[j] + bv[j]), av[j]));
-}
-
-__device__ __forceinline__ void epi32_any(int act, const float (&v)[32], const float (&bv)[32],
-                                          const float (&av)[32], const float (&r)[32], float kpre,
-                                          float kpost, float (&o)[32]) {
-    switch (act) {  // uniform across the CTA
-    case ACNN_ACT_RELU: epi32<ACNN_ACT_RELU>(v, bv, av, r, kpre, kpost, o); break;
-    case ACNN_ACT_SILU: epi32<ACNN_ACT_SILU>(v, bv, av, r, kpre, kpost, o); break;
-    case ACNN_ACT_PRELU: epi32<ACNN_ACT_PRELU>(v, bv, av, r, kpre, kpost, o); break;
-    default: epi32<ACNN_ACT_NONE>(v, bv, av, r, kpre, kpost, o); break;
-    }
-}
-
 // The NHWC epilogue's form: the residual mode fixed at compile time (no
 // residual term at all without one), the 32 biases and PReLU alphas of the
-// chunk read from shared memory four at a time (bias[j], alpha[j]), and the
-// result written over the accumulator values.
-template <int ACT, int RES>
+// chunk read from shared memory four at a time (bias[j], alpha[j]), the
+// residual row read eight values at a time from its swizzled shared-memory
+// row (16-byte piece j at rrow + ((j ^ swz) << 4)), and the result written
+// over the accumulator values.
+template <int ACT, int RES, typename T>
 __device__ __forceinline__ void epi32_slot(float (&v)[32], const float* bias, const float* alpha,
-                                           const float (&r)[32]) {
+                                           const uint8_t* rrow, uint32_t swz) {
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-        const float4 b4 = *reinterpret_cast<const float4*>(bias + j);
-        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if constexpr (ACT == ACNN_ACT_PRELU) a4 = *reinterpret_cast<const float4*>(alpha + j);
-        const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
-        const float aa[4] = {a4.x, a4.y, a4.z, a4.w};
+    for (int j8 = 0; j8 < 4; ++j8) {
+        float r[8];
+        if constexpr (RES != ACNN_RES_NONE) {
+            const uint4 u = *reinterpret_cast<const uint4*>(rrow + ((j8 ^ swz) << 4));
+            unpack2<T>(u.x, r[0], r[1]);
+            unpack2<T>(u.y, r[2], r[3]);
+            unpack2<T>(u.z, r[4], r[5]);
+            unpack2<T>(u.w, r[6], r[7]);
+        }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float x = v[j + k] + bb[k];
-            if constexpr (RES == ACNN_RES_NONE) v[j + k] = act_fixed<ACT>(x, aa[k]);
-            else if constexpr (RES == ACNN_RES_ADD_THEN_ACT) v[j + k] = act_fixed<ACT>(x + r[j + k], aa[k]);
-            else v[j + k] = act_fixed<ACT>(x, aa[k]) + r[j + k];
+        for (int j4 = 0; j4 < 8; j4 += 4) {
+            const int j = j8 * 8 + j4;
+            const float4 b4 = *reinterpret_cast<const float4*>(bias + j);
+            float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (ACT == ACNN_ACT_PRELU) a4 = *reinterpret_cast<const float4*>(alpha + j);
+            const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+            const float aa[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float x = v[j + k] + bb[k];
+                if constexpr (RES == ACNN_RES_NONE) v[j + k] = act_fixed<ACT>(x, aa[k]);
+                else if constexpr (RES == ACNN_RES_ADD_THEN_ACT)
+                    v[j + k] = act_fixed<ACT>(x + r[j4 + k], aa[k]);
+                else v[j + k] = act_fixed<ACT>(x, aa[k]) + r[j4 + k];
+            }
         }
     }
 }
 
-template <int ACT>
+template <int ACT, typename T>
 __device__ __forceinline__ void epi32_slot_act(int res_mode, float (&v)[32], const float* bias,
-                                               const float* alpha, const float (&r)[32]) {
-    if (res_mode == ACNN_RES_ADD_THEN_ACT) epi32_slot<ACT, ACNN_RES_ADD_THEN_ACT>(v, bias, alpha, r);
+                                               const float* alpha, const uint8_t* rrow,
+                                               uint32_t swz) {
+    if (res_mode == ACNN_RES_ADD_THEN_ACT)
+        epi32_slot<ACT, ACNN_RES_ADD_THEN_ACT, T>(v, bias, alpha, rrow, swz);
     else if (res_mode == ACNN_RES_ACT_THEN_ADD)
-        epi32_slot<ACT, ACNN_RES_ACT_THEN_ADD>(v, bias, alpha, r);
-    else epi32_slot<ACT, ACNN_RES_NONE>(v, bias, alpha, r);
+        epi32_slot<ACT, ACNN_RES_ACT_THEN_ADD, T>(v, bias, alpha, rrow, swz);
+    else epi32_slot<ACT, ACNN_RES_NONE, T>(v, bias, alpha, rrow, swz);
 }
 
+template <typename T>
 __device__ __forceinline__ void epi32_slot_mode(int act, int res_mode, float (&v)[32],
                                                 const float* bias, const float* alpha,
-                                                const float (&r)[32]) {
+                                                const uint8_t* rrow, uint32_t swz) {
     switch (act) {  // both uniform across the CTA
-    case ACNN_ACT_RELU: epi32_slot_act<ACNN_ACT_RELU>(res_mode, v, bias, alpha, r); break;
-    case ACNN_ACT_SILU: epi32_slot_act<ACNN_ACT_SILU>(res_mode, v, bias, alpha, r); break;
-    case ACNN_ACT_PRELU: epi32_slot_act<ACNN_ACT_PRELU>(res_mode, v, bias, alpha, r); break;
-    default: epi32_slot_act<ACNN_ACT_NONE>(res_mode, v, bias, alpha, r); break;
-    }
-}
-
-// Bias and PReLU alpha of channels [co, co + 32): broadcast loads (every lane
-// reads the same addresses); channels >= C_out read as zero.
-__device__ __forceinline__ void load_chunk_params(const float* __restrict__ bias,
-                                                  const float* __restrict__ alpha, bool prelu,
-                                                  int co, int c_out, float (&bv)[32],
-                                                  float (&av)[32]) {
-#pragma unroll
-    for (int g = 0; g < 32; g += 4) {
-        float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f), a4 = b4;
-        if (co + g < c_out) {  // C_out % 16 == 0: a float4 is all in or all out
-            if (bias) b4 = __ldg(reinterpret_cast<const float4*>(bias + co + g));
-            if (prelu) a4 = __ldg(reinterpret_cast<const float4*>(alpha + co + g));
-        }
-        bv[g] = b4.x; bv[g + 1] = b4.y; bv[g + 2] = b4.z; bv[g + 3] = b4.w;
-        av[g] = a4.x; av[g + 1] = a4.y; av[g + 2] = a4.z; av[g + 3] = a4.w;
+    case ACNN_ACT_RELU: epi32_slot_act<ACNN_ACT_RELU, T>(res_mode, v, bias, alpha, rrow, swz); break;
+    case ACNN_ACT_SILU: epi32_slot_act<ACNN_ACT_SILU, T>(res_mode, v, bias, alpha, rrow, swz); break;
+    case ACNN_ACT_PRELU: epi32_slot_act<ACNN_ACT_PRELU, T>(res_mode, v, bias, alpha, rrow, swz); break;
+    default: epi32_slot_act<ACNN_ACT_NONE, T>(res_mode, v, bias, alpha, rrow, swz); break;
     }
 }
 
@@ -611,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // buffer; the reduce kernel adds the splits and applies bias,
         // activation, residual and the down-cast.
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int grp = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -623,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
-            for (int i = half; i < MS * nch; i += 2) {
+            for (int i = grp; i < MS * nch; i += kEpiGroups) {
                 const int ms = i / nch, c = (i - ms * nch) * 32;
                 const int m = m0 + ms * BM + row;
                 float v[32];
@@ -647,8 +625,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (p.out_layout == ACNN_NHWC) {
         // ---------------------------------------------------- epilogue warps, NHWC
-        // Warp e (0..7) owns the 32 rows of its TMEM lane quarter (warp % 4) and
-        // every other 32-channel chunk of each tile (e / 4 picks even or odd).
+        // Warp e (0..11) owns the 32 rows of its TMEM lane quarter (warp % 4)
+        // and every third 32-channel chunk of each tile (group e / 4 picks
+        // which), in (row block, channel) order.
         // Its chunks form one stream across tiles.  Each chunk uses one 2 KB
         // slot of the warp's ring in shared memory (32 rows x 64 B, 16-byte
         // pieces swizzled by row so that both row-wise and column-wise accesses
@@ -663,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         //   * the bias and PReLU alpha come from a shared-memory copy.
         const int q = warp & 3;
         const int e = warp - 2;
-        const int half = e >> 2;
+        const int grp = e >> 2;
         const int RD = p.res_depth;  // 0 without a residual
         const int nnt = p.num_n_tiles;
         uint8_t* ring = sR + (size_t)e * (RD > 0 ? RD : 1) * kStageBytes;
@@ -692,11 +671,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 c.t += gridDim.x;
                 c.nt = nnt == 1 ? 0 : c.t % nnt;
                 c.ms = 0;
-                c.ci = half;
+                c.ci = grp;
             }
         };
         // residual cursor
-        Cursor rc{(int)blockIdx.x, nnt == 1 ? 0 : (int)blockIdx.x % nnt, 0, half};
+        Cursor rc{(int)blockIdx.x, nnt == 1 ? 0 : (int)blockIdx.x % nnt, 0, grp};
         settle(rc);
         int pend = 0, wb = 0, rb = 0;
         auto refill = [&]() {
@@ -714,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cp_async_commit();
                 wb = wb + 1 == RD ? 0 : wb + 1;
                 ++pend;
-                rc.ci += 2;
+                rc.ci += kEpiGroups;
                 settle(rc);
             }
         };
@@ -739,44 +718,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool ok = __all_sync(0xffffffffu, wait_phase(tfull_bar(acc), acc_phase, abort_flag, p));
             if (!ok) break;
             tc_fence_after();
-            int ms = 0, ci = half;
-            for (int i = half; i < nchunks; i += 2) {
+            int ms = 0, ci = grp;
+            for (int i = grp; i < nchunks; i += kEpiGroups) {
                 while (ci >= nch) {
                     ci -= nch;
                     ++ms;
                 }
                 const int c = ci * 32;
                 const int msc = ms;
-                ci += 2;
+                ci += kEpiGroups;
                 const int row0 = m0 + ms * BM + q * 32;
                 float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
                               (uint32_t)(acc * MS * BN + msc * BN + c),
                           v);
                 uint8_t* slot = ring + (RD > 0 ? rb : 0) * kStageBytes;
-                float r[32];
                 if (RD > 0) {
                     // this chunk's box is the oldest in flight: let the newer
                     // pend - 1 stay pending, then see every lane's part of it
                     cp_async_wait_newer(pend - 1);
                     __syncwarp();
-                    const uint8_t* rrow = slot + lane * 64;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(rrow + ((j ^ swz) << 4));
-                        unpack2<T>(u.x, r[8 * j + 0], r[8 * j + 1]);
-                        unpack2<T>(u.y, r[8 * j + 2], r[8 * j + 3]);
-                        unpack2<T>(u.z, r[8 * j + 4], r[8 * j + 5]);
-                        unpack2<T>(u.w, r[8 * j + 6], r[8 * j + 7]);
-                    }
                     rb = rb + 1 == RD ? 0 : rb + 1;
                     --pend;
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = 0.f;
                 }
-                epi32_slot_mode(p.act, RD > 0 ? p.res_mode : ACNN_RES_NONE, v, sP + n0 + c,
-                                sP + cpad + n0 + c, r);
+                epi32_slot_mode<T>(p.act, RD > 0 ? p.res_mode : ACNN_RES_NONE, v, sP + n0 + c,
+                                   sP + cpad + n0 + c, slot + lane * 64, swz);
                 // this lane's row of results over its row of the slot
                 uint8_t* orow = slot + lane * 64;
 #pragma unroll
@@ -807,16 +773,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------------------------------------------- epilogue warps, NCHW
         // Same row/chunk split as above; lane l holds output pixel m0 + 32q + l,
-        // so each of the 32 channel planes is written by 32 consecutive pixels.
+        // so each of the 32 channel planes is written by 32 consecutive pixels
+        // (and the residual read the same way).  Bias and alpha come from the
+        // shared copy.
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int half = (warp - 2) >> 2;
+        const int grp = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         const T* res = static_cast<const T*>(p.res);
         T* y = static_cast<T*>(p.y);
         const bool has_res = p.res_mode != ACNN_RES_NONE;
+        const bool pre = p.res_mode == ACNN_RES_ADD_THEN_ACT;
         const bool prelu = p.act == ACNN_ACT_PRELU;
-        const float kpre = p.res_mode == ACNN_RES_ADD_THEN_ACT ? 1.f : 0.f;
-        const float kpost = p.res_mode == ACNN_RES_ACT_THEN_ADD ? 1.f : 0.f;
+        const int cpad = prelu ? p.par_floats / 2 : p.par_floats;
+        for (int i = threadIdx.x - 64; i < cpad; i += 32 * kEpiWarps) {
+            sP[i] = (p.bias && i < p.C_out) ? __ldg(p.bias + i) : 0.f;
+            if (prelu) sP[cpad + i] = i < p.C_out ? __ldg(p.alpha + i) : 0.f;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {  // splits == 1
@@ -828,28 +801,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
-            for (int i = half; i < MS * nch; i += 2) {
+            for (int i = grp; i < MS * nch; i += kEpiGroups) {
                 const int ms = i / nch, c = (i - ms * nch) * 32;
                 const int m = m0 + ms * BM + row;
                 const bool valid = m < p.M;
                 const int img = m / p.OHW;
                 const long long base = (long long)img * p.C_out * p.OHW + (m - img * p.OHW);
-                float bv[32], av[32], r[32], o[32], v[32];
-                load_chunk_params(p.bias, p.alpha, prelu, n0 + c, p.C_out, bv, av);
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    r[j] = (has_res && valid && n0 + c + j < p.C_out)
-                               ? to_f32(res[base + (long long)(n0 + c + j) * p.OHW])
-                               : 0.f;
+                float v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
                               (uint32_t)(acc * MS * BN + ms * BN + c),
                           v);
-                epi32_any(p.act, v, bv, av, r, kpre, kpost, o);
-                if (valid) {
+                const int nj = p.C_out - (n0 + c) < 32 ? p.C_out - (n0 + c) : 32;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (n0 + c + j < p.C_out)
-                            y[base + (long long)(n0 + c + j) * p.OHW] = from_f32<T>(o[j]);
+                for (int j = 0; j < 32; ++j) {
+                    if (j >= nj) break;
+                    const int ch = n0 + c + j;
+                    const long long idx = base + (long long)ch * p.OHW;
+                    const float rv = (has_res && valid) ? to_f32(res[idx]) : 0.f;
+                    const float x = v[j] + sP[ch];
+                    const float al = prelu ? sP[cpad + ch] : 0.f;
+                    const float o = pre ? apply_act(p.act, x + rv, al) : apply_act(p.act, x, al) + rv;
+                    if (valid) y[idx] = from_f32<T>(o);
                 }
             }
             tc_fence_before();
@@ -1019,7 +991,7 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     // shared bias / alpha copy for the NHWC epilogue: every column tile's
     // columns, so reads past C_out in a ragged last tile stay inside
     const bool nhwc_epi = prm.out_layout == ACNN_NHWC && !prm.part;
-    prm.par_floats = nhwc_epi ? prm.num_n_tiles * BN * (prm.act == ACNN_ACT_PRELU ? 2 : 1) : 0;
+    prm.par_floats = prm.part ? 0 : prm.num_n_tiles * BN * (prm.act == ACNN_ACT_PRELU ? 2 : 1);
     const size_t par_bytes = (size_t)prm.par_floats * 4;
     prm.ring_slots = nhwc_epi ? (rd > 0 ? rd : 1) : 0;
     const size_t ring_bytes = (size_t)kEpiWarps * prm.ring_slots * kStageBytes;
