@@ -130,9 +130,9 @@ def build_net(name, device, batch=None):
     if name == "backbone":
         return N.backbone_net(device, n=batch or 8)
     if name == "block":
-        return N.block_net(device, "identity")
+        return N.block_net(device, "identity", n=batch or 4)
     if name == "block_down":
-        return N.block_net(device, "downsample")
+        return N.block_net(device, "downsample", n=batch or 4)
     return N.WORKLOADS[name](device)
 
 
@@ -441,7 +441,8 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--layers", action="store_true", help="add per-conv timings")
     ap.add_argument("--batch", type=int, default=None,
-                    help="backbone batch per GPU (default 8; smaller only for profiler captures)")
+                    help="batch per GPU of the backbone (default 8) or a bottleneck block (default 4); "
+                         "other sizes for profiler captures")
     args = ap.parse_args()
 
     from activation_cnn_gb300 import replicas as R
