@@ -117,6 +117,125 @@ __global__ void __launch_bounds__(kThreads) maxpool3s2_nhwc_kernel(
     }
 }
 
+// Row-blocked NHWC kernels for the backbone's hot shapes.  Block (r, g) of the
+// 2-D grid covers output row r = n*OH + oy and the g-th run of U*256 16-byte
+// channel vectors of that row (vector j of the row: pixel j / CV, vector
+// j % CV), so each thread computes its coordinates with one division and
+// issues the loads of all its vectors before it stores any.
+
+// 2x2/s2/p0 average pool: (a + b + c + d) * 0.25 in (dy, dx) order, as the
+// generic kernel computes it.
+template <typename T, int V, int U>
+__global__ void __launch_bounds__(kThreads) avgpool2_rows_kernel(
+    const T* __restrict__ x, T* __restrict__ y, int H, int W, int C, int OH, int OW) {
+    const int CV = C / V;
+    const int r = blockIdx.x, oy = r % OH, n = r / OH;
+    const int row_vecs = OW * CV;
+    const T* x0 = x + ((long long)n * H + 2 * oy) * W * C;
+    const T* x1 = x0 + (long long)W * C;
+    T* yr = y + (long long)r * OW * C;
+    Vec<T, V> t[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int j = (blockIdx.y * U + u) * kThreads + threadIdx.x;
+        if (j < row_vecs) {
+            const int ox = j / CV, cv = j - ox * CV;
+            const long long o = (long long)(2 * ox) * C + (long long)cv * V;
+            t[u][0] = *reinterpret_cast<const Vec<T, V>*>(x0 + o);
+            t[u][1] = *reinterpret_cast<const Vec<T, V>*>(x0 + o + C);
+            t[u][2] = *reinterpret_cast<const Vec<T, V>*>(x1 + o);
+            t[u][3] = *reinterpret_cast<const Vec<T, V>*>(x1 + o + C);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int j = (blockIdx.y * U + u) * kThreads + threadIdx.x;
+        if (j < row_vecs) {
+            const int ox = j / CV, cv = j - ox * CV;
+            Vec<T, V> o;
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc += to_f32(t[u][k].v[v]);
+                o.v[v] = from_f32<T>(acc * 0.25f);
+            }
+            *reinterpret_cast<Vec<T, V>*>(yr + (long long)ox * C + (long long)cv * V) = o;
+        }
+    }
+}
+
+// 3x3/s2/p1 max pool, row-blocked: nine clamped loads per vector, then the
+// out-of-image taps masked, strictly-greater replacement in (dy, dx) order.
+template <typename T, int V>
+__global__ void __launch_bounds__(kThreads) maxpool3s2_rows_kernel(
+    const T* __restrict__ x, T* __restrict__ y, int H, int W, int C, int OH, int OW) {
+    const int CV = C / V;
+    const int r = blockIdx.x, oy = r % OH, n = r / OH;
+    const int j = blockIdx.y * kThreads + threadIdx.x;
+    if (j >= OW * CV) return;
+    const int ox = j / CV, cv = j - ox * CV;
+    const T* img = x + (long long)n * H * W * C + (long long)cv * V;
+    Vec<T, V> t[9];
+    bool ok[9];
+#pragma unroll
+    for (int dy = 0; dy < 3; ++dy)
+#pragma unroll
+        for (int dx = 0; dx < 3; ++dx) {
+            const int iy = 2 * oy - 1 + dy, ix = 2 * ox - 1 + dx;
+            ok[dy * 3 + dx] = iy >= 0 && iy < H && ix >= 0 && ix < W;
+            const int iyc = min(max(iy, 0), H - 1), ixc = min(max(ix, 0), W - 1);
+            t[dy * 3 + dx] = *reinterpret_cast<const Vec<T, V>*>(img + ((long long)iyc * W + ixc) * C);
+        }
+    float best[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) best[v] = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 9; ++k)
+        if (ok[k]) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const float f = to_f32(t[k].v[v]);
+                if (f > best[v]) best[v] = f;
+            }
+        }
+    Vec<T, V> o;
+#pragma unroll
+    for (int v = 0; v < V; ++v) o.v[v] = from_f32<T>(best[v]);
+    *reinterpret_cast<Vec<T, V>*>(y + ((long long)r * OW + ox) * C + (long long)cv * V) = o;
+}
+
+// Nearest 2x, row-blocked over input rows: one load, four stores per vector.
+template <typename T, int V, int U>
+__global__ void __launch_bounds__(kThreads) up2_rows_kernel(const T* __restrict__ x,
+                                                            T* __restrict__ y, int H, int W,
+                                                            int C) {
+    const int CV = C / V;
+    const int r = blockIdx.x, iy = r % H, n = r / H;
+    const int OW = 2 * W;
+    const T* xr = x + (long long)r * W * C;
+    T* y0 = y + ((long long)n * 2 * H + 2 * iy) * OW * C;
+    T* y1 = y0 + (long long)OW * C;
+    Vec<T, V> t[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int j = (blockIdx.y * U + u) * kThreads + threadIdx.x;
+        if (j < W * CV) t[u] = *reinterpret_cast<const Vec<T, V>*>(xr + (long long)j * V);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int j = (blockIdx.y * U + u) * kThreads + threadIdx.x;
+        if (j < W * CV) {
+            const int ix = j / CV, cv = j - ix * CV;
+            const long long o = (long long)(2 * ix) * C + (long long)cv * V;
+            *reinterpret_cast<Vec<T, V>*>(y0 + o) = t[u];
+            *reinterpret_cast<Vec<T, V>*>(y0 + o + C) = t[u];
+            *reinterpret_cast<Vec<T, V>*>(y1 + o) = t[u];
+            *reinterpret_cast<Vec<T, V>*>(y1 + o + C) = t[u];
+        }
+    }
+}
+
 // Nearest 2x, NHWC: one thread per input pixel and 16-byte channel vector,
 // one load and the four stores of its 2x2 output block.
 template <typename T, int V>
@@ -279,32 +398,30 @@ template <typename T, int V>
 __global__ void __launch_bounds__(kThreads) concat_kernel(
     const T* __restrict__ a, const T* __restrict__ b, T* __restrict__ y, long long runs,
     int ra, int rb) {
-    // four independent vectors per thread per round keep more bytes in flight
+    // four vectors per thread (one block-width apart), all loaded before any
+    // is stored; one division per vector
     constexpr int U = 4;
     const uint32_t rv = (uint32_t)((ra + rb) / V);
     const uint32_t total = (uint32_t)(runs * rv);
-    const uint32_t stride = gridDim.x * blockDim.x;
-    for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += stride * U) {
-        Vec<T, V> t[U];
+    Vec<T, V> t[U];
+    uint32_t run[U];
+    int e[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t i = i0 + u * stride;
-            if (i < total) {
-                const uint32_t run = i / rv;
-                const int e = (int)(i - run * rv) * V;
-                const T* src = e < ra ? a + (long long)run * ra + e : b + (long long)run * rb + (e - ra);
-                t[u] = *reinterpret_cast<const Vec<T, V>*>(src);
-            }
+    for (int u = 0; u < U; ++u) {
+        const uint32_t i = (blockIdx.x * U + u) * blockDim.x + threadIdx.x;
+        run[u] = i / rv;
+        e[u] = (int)(i - run[u] * rv) * V;
+        if (i < total) {
+            const T* src = e[u] < ra ? a + (long long)run[u] * ra + e[u]
+                                     : b + (long long)run[u] * rb + (e[u] - ra);
+            t[u] = *reinterpret_cast<const Vec<T, V>*>(src);
         }
+    }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t i = i0 + u * stride;
-            if (i < total) {
-                const uint32_t run = i / rv;
-                const int e = (int)(i - run * rv) * V;
-                *reinterpret_cast<Vec<T, V>*>(y + (long long)run * (ra + rb) + e) = t[u];
-            }
-        }
+    for (int u = 0; u < U; ++u) {
+        const uint32_t i = (blockIdx.x * U + u) * blockDim.x + threadIdx.x;
+        if (i < total)
+            *reinterpret_cast<Vec<T, V>*>(y + (long long)run[u] * (ra + rb) + e[u]) = t[u];
     }
 }
 
@@ -536,7 +653,17 @@ cudaError_t pool_typed(int kind, int n, int h, int w, int c, int k, int stride, 
     T* yt = static_cast<T*>(y);
     if (layout == ACNN_NHWC) {
         constexpr int V = 16 / sizeof(T);
-        if (c % V == 0 && kind == ACNN_POOL_MAX && k == 3 && stride == 2 && pad == 1) {
+        const long long rows = (long long)n * oh;
+        const int row_vecs = c % V == 0 ? ow * (c / V) : 0;
+        if (c % V == 0 && kind == ACNN_POOL_MAX && k == 3 && stride == 2 && pad == 1 &&
+            rows <= 0x7fffffffLL && (row_vecs + kThreads - 1) / kThreads <= 65535) {
+            dim3 g((unsigned)rows, (row_vecs + kThreads - 1) / kThreads);
+            maxpool3s2_rows_kernel<T, V><<<g, kThreads, 0, s>>>(xt, yt, h, w, c, oh, ow);
+        } else if (c % V == 0 && kind == ACNN_POOL_AVG && k == 2 && stride == 2 && pad == 0 &&
+                   rows <= 0x7fffffffLL && (row_vecs + 2 * kThreads - 1) / (2 * kThreads) <= 65535) {
+            dim3 g((unsigned)rows, (row_vecs + 2 * kThreads - 1) / (2 * kThreads));
+            avgpool2_rows_kernel<T, V, 2><<<g, kThreads, 0, s>>>(xt, yt, h, w, c, oh, ow);
+        } else if (c % V == 0 && kind == ACNN_POOL_MAX && k == 3 && stride == 2 && pad == 1) {
             long long work = (long long)n * oh * ow * (c / V);
             maxpool3s2_nhwc_kernel<T, V><<<grid_occ(maxpool3s2_nhwc_kernel<T, V>, work, kThreads), kThreads, 0, s>>>(
                 xt, yt, n, h, w, c, oh, ow);
@@ -566,6 +693,14 @@ cudaError_t resize_typed(int mode, int n, int c, int h, int w, int oh, int ow, i
     if (layout == ACNN_NHWC) {
         constexpr int V = (16 / sizeof(Ti)) < (16 / sizeof(To)) ? (16 / sizeof(Ti)) : (16 / sizeof(To));
         if constexpr (sizeof(Ti) == sizeof(To)) {
+            const long long in_rows = (long long)n * h;
+            const int in_row_vecs = c % V == 0 ? w * (c / V) : 0;
+            if (mode == ACNN_RESIZE_NEAREST && oh == 2 * h && ow == 2 * w && c % V == 0 &&
+                in_rows <= 0x7fffffffLL && (in_row_vecs + 2 * kThreads - 1) / (2 * kThreads) <= 65535) {
+                dim3 g((unsigned)in_rows, (in_row_vecs + 2 * kThreads - 1) / (2 * kThreads));
+                up2_rows_kernel<Ti, V, 2><<<g, kThreads, 0, s>>>(xt, reinterpret_cast<Ti*>(yt), h, w, c);
+                return cudaGetLastError();
+            }
             if (mode == ACNN_RESIZE_NEAREST && oh == 2 * h && ow == 2 * w && c % V == 0) {
                 long long work = (long long)n * h * w * (c / V);
                 up2_nhwc_kernel<Ti, V><<<grid_occ(up2_nhwc_kernel<Ti, V>, work, kThreads), kThreads, 0, s>>>(
@@ -618,14 +753,14 @@ cudaError_t concat_typed(int n, int h, int w, int ca, int cb, int layout, const 
     const T* at = static_cast<const T*>(a);
     const T* bt = static_cast<const T*>(b);
     T* yt = static_cast<T*>(y);
+    // one block per 4 x 256 vectors (the index stays below 2^32: the host checks it)
+    auto blocks = [](long long work) { return (unsigned)((work + 4LL * kThreads - 1) / (4LL * kThreads)); };
     if (ra % V == 0 && rb % V == 0) {
-        long long work = runs * ((ra + rb) / V);
-        concat_kernel<T, V><<<grid_occ(concat_kernel<T, V>, work, kThreads), kThreads, 0, s>>>(at, bt, yt, runs,
-                                                                          (int)ra, (int)rb);
+        const long long work = runs * ((ra + rb) / V);
+        concat_kernel<T, V><<<blocks(work), kThreads, 0, s>>>(at, bt, yt, runs, (int)ra, (int)rb);
     } else {
-        long long work = runs * (ra + rb);
-        concat_kernel<T, 1><<<grid_occ(concat_kernel<T, 1>, work, kThreads), kThreads, 0, s>>>(at, bt, yt, runs,
-                                                                          (int)ra, (int)rb);
+        const long long work = runs * (ra + rb);
+        concat_kernel<T, 1><<<blocks(work), kThreads, 0, s>>>(at, bt, yt, runs, (int)ra, (int)rb);
     }
     return cudaGetLastError();
 }

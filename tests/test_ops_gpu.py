@@ -225,7 +225,8 @@ def test_conv_direct_integer_bitexact_f32():
 # ---------------------------------------------------------------- pools
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("layout", [G.NHWC, G.NCHW])
-@pytest.mark.parametrize("shape", [(2, 17, 23, 64), (1, 8, 8, 3), (3, 1, 1, 16), (1, 2, 5, 24)])
+@pytest.mark.parametrize("shape", [(2, 17, 23, 64), (1, 8, 8, 3), (3, 1, 1, 16), (1, 2, 5, 24),
+                                   (1, 65, 129, 64)])
 def test_maxpool_bitexact(dt, layout, shape):
     n, h, w, c = shape
     x = G.tensor(3, f"mp{shape}", G.activation_shape(layout, n, c, h, w), "normal", dtype=DT[dt])
@@ -236,7 +237,7 @@ def test_maxpool_bitexact(dt, layout, shape):
 
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("layout", [G.NHWC, G.NCHW])
-@pytest.mark.parametrize("shape", [(2, 16, 22, 64), (1, 8, 6, 5)])
+@pytest.mark.parametrize("shape", [(2, 16, 22, 64), (1, 8, 6, 5), (2, 33, 47, 256)])
 def test_avgpool(dt, layout, shape):
     n, h, w, c = shape
     x = G.tensor(4, f"ap{shape}", G.activation_shape(layout, n, c, h, w), "normal", dtype=DT[dt])
