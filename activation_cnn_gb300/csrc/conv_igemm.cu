@@ -54,7 +54,7 @@ constexpr size_t kSmemMax = 232448;  // 227 KB of dynamic shared memory per CTA
 // PReLU-alpha copy (par_floats fp32 values).  The window must start 1024-byte
 // aligned (the kernel checks): the swizzled operand tiles rely on it.
 constexpr size_t kSmemFixed = kBarBytes;
-static_assert((2 * kMaxStages + 6) * 8 + 8 <= kBarBytes, "barrier region too small");
+static_assert((2 * kMaxStages + 6) * 8 + 12 <= kBarBytes, "barrier region too small");
 
 // Tile of (128 * MS) output pixels x BN output channels, K in blocks of BK
 // channels: MS row blocks of 128 share each B tile, so one pipeline step
@@ -77,7 +77,11 @@ struct Params {
     int M, C_out, taps, KW, kb_per_tap, num_kb;
     int num_m_tiles, num_n_tiles;
     int splits, kb_per_split;  // split-K: unit = tile * splits + split
-    float* part;               // split-K partial sums [splits][M][C_out] (fp32), or NULL
+    // split-K: fp32 partial tiles [tile][split][TM x BN] (chunk-blocked, see the
+    // split-K epilogue) and one arrival counter per output tile (zeroed by the
+    // host before the launch); NULL without a split
+    float* part;
+    unsigned* cnt;
     int OW, OHW, S, P;
     int a_mode;       // 0: tiled A (1x1/s1/p0); 1: im2col A
     int out_layout;   // ACNN_NHWC or ACNN_NCHW for y and the residual
@@ -155,6 +159,32 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
                                            volatile int* abort_flag, const Params& p) {
     if (p.budget <= 0 && mbar_try_wait(bar, parity)) return true;
     return wait_phase_slow(bar, parity, abort_flag, p.budget, p.status);
+}
+
+// Bounded wait until the global counter *cnt reaches n (the splits of one
+// output tile, run by CTAs that are all resident).  Returns false if the CTA
+// is aborting or the wait expired (recorded like an mbarrier timeout).
+__device__ __noinline__ bool wait_count(const unsigned* cnt, unsigned n, volatile int* abort_flag,
+                                        const Params& p) {
+    long long t0 = -1;
+    for (long long i = 1;; ++i) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+        if (v >= n) return true;
+        bool expired = p.budget > 0 && i >= p.budget;
+        if ((i & 255) == 0) {
+            if (*abort_flag) return false;
+            const long long now = clock64();
+            if (t0 < 0) t0 = now;
+            if (p.budget <= 0 && now - t0 > kTimeoutCycles) expired = true;
+        }
+        if (expired) {
+            atomicCAS(p.status, 0, ACNN_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+        __nanosleep(64);
+    }
 }
 
 // Time-bounded wait used only while draining after an abort.
@@ -585,37 +615,160 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (p.part) {
         // ---------------------------------------------------- epilogue warps, split-K
-        // Raw fp32 accumulators of this unit's K range go to the partial-sum
-        // buffer; the reduce kernel adds the splits and applies bias,
-        // activation, residual and the down-cast.
+        // Every split of an output tile writes its raw fp32 accumulators to its
+        // partial tile in the workspace and counts itself in on the tile's
+        // counter; once all S have arrived, each finishes 1/S of the tile's
+        // 32 x 32 blocks: the sum of all partial tiles in split order (so the
+        // result does not depend on arrival order), then the bias / residual /
+        // activation / store epilogue.  Partial tiles are chunk-blocked: the 32 x 32 block of
+        // (row block ms, chunk ci, lane quarter q) holds lane l's columns
+        // 4j..4j+3 at float offset (j * 32 + l) * 4, so each warp store or load
+        // instruction moves 512 contiguous bytes.
         const int q = warp & 3;
-        const int grp = (warp - 2) >> 2;
-        const int row = q * 32 + lane;
+        const int e = warp - 2;
+        const int grp = e >> 2;
+        const int S = p.splits;
+        const T* res = static_cast<const T*>(p.res);
+        T* y = static_cast<T*>(p.y);
+        const bool prelu = p.act == ACNN_ACT_PRELU;
+        const uint32_t swz = (uint32_t)((lane >> 1) & 3);
+        const int crow = lane >> 2, cpiece = lane & 3;
+        auto piece = [](int r, int j) { return r * 64 + ((j ^ ((r >> 1) & 3)) << 4); };
+        uint8_t* slot = sR + (size_t)e * kStageBytes;  // one slot per warp (NHWC output)
+        volatile int* met_flag = abort_flag + 1;  // all splits of the tile arrived
+        const int cpad = prelu ? p.par_floats / 2 : p.par_floats;
+        for (int i = threadIdx.x - 64; i < cpad; i += 32 * kEpiWarps) {
+            sP[i] = (p.bias && i < p.C_out) ? __ldg(p.bias + i) : 0.f;
+            if (prelu) sP[cpad + i] = i < p.C_out ? __ldg(p.alpha + i) : 0.f;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+        constexpr int kChunksPerTile = MS * (BN / 32);
+        auto block_of = [&](int tile, int split, int ms, int ci) {
+            return p.part +
+                   ((((size_t)tile * S + split) * kChunksPerTile + ms * (BN / 32) + ci) * 4 + q) *
+                       1024;
+        };
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int unit = blockIdx.x; unit < num_tiles; unit += gridDim.x) {
-            const int tile = unit / p.splits, split = unit - tile * p.splits;
+            const int tile = unit / S, split = unit - tile * S;
             const int m0 = (tile / p.num_n_tiles) * TM;
             const int n0 = (tile % p.num_n_tiles) * BN;
             const bool ok = __all_sync(0xffffffffu, wait_phase(tfull_bar(acc), acc_phase, abort_flag, p));
             if (!ok) break;
             tc_fence_after();
             const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
+            auto tmem_col = [&](int ms, int c) {
+                return tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * MS * BN + ms * BN + c);
+            };
             for (int i = grp; i < MS * nch; i += kEpiGroups) {
-                const int ms = i / nch, c = (i - ms * nch) * 32;
-                const int m = m0 + ms * BM + row;
+                const int ms = i / nch, ci = i - ms * nch;
                 float v[32];
-                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
-                              (uint32_t)(acc * MS * BN + ms * BN + c),
-                          v);
-                if (m < p.M) {
-                    float* dst = p.part + ((long long)split * p.M + m) * p.C_out + n0 + c;
+                tmem_ld32(tmem_col(ms, ci * 32), v);
+                float* blk = block_of(tile, split, ms, ci);
 #pragma unroll
-                    for (int g = 0; g < 32; g += 4)
-                        if (n0 + c + g < p.C_out)
-                            *reinterpret_cast<float4*>(dst + g) =
-                                make_float4(v[g], v[g + 1], v[g + 2], v[g + 3]);
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4*>(blk + (j * 32 + lane) * 4) =
+                        make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+            // every epilogue warp has written this split's partial tile
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+            // finish one 32 x 32 block (row block ms, chunk ci, lane quarter qb)
+            // of the tile from its split-order sum t
+            auto finish = [&](int ms, int ci, int qb, float (&t)[32]) {
+                const int c = ci * 32;
+                const int row0 = m0 + ms * BM + qb * 32;
+                if (p.out_layout == ACNN_NHWC) {
+                    // residual row of this lane into its slot row, then the
+                    // NHWC epilogue arithmetic and coalesced stores
+                    const int m = row0 + lane;
+                    if (p.res_mode != ACNN_RES_NONE) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const bool in = m < p.M && n0 + c + j * 8 < p.C_out;
+                            const T* src = res + (in ? (long long)m * p.C_out + n0 + c + j * 8 : 0);
+                            cp_async16(smem_u32(slot + lane * 64 + ((j ^ swz) << 4)), src, in ? 16u : 0u);
+                        }
+                        cp_async_commit();
+                        cp_async_wait_newer(0);
+                    }
+                    epi32_slot_mode<T>(p.act, p.res_mode, t, sP + n0 + c, sP + cpad + n0 + c,
+                                       slot + lane * 64, swz);
+                    uint8_t* orow = slot + lane * 64;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(orow + ((j ^ swz) << 4)) = make_uint4(
+                            pack2<T>(t[8 * j + 0], t[8 * j + 1]), pack2<T>(t[8 * j + 2], t[8 * j + 3]),
+                            pack2<T>(t[8 * j + 4], t[8 * j + 5]), pack2<T>(t[8 * j + 6], t[8 * j + 7]));
+                    __syncwarp();
+                    const int col = n0 + c + cpiece * 8;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int rr = 8 * k + crow;
+                        const uint4 u = *reinterpret_cast<const uint4*>(slot + piece(rr, cpiece));
+                        if (row0 + rr < p.M && col < p.C_out)
+                            *reinterpret_cast<uint4*>(y + (long long)(row0 + rr) * p.C_out + col) = u;
+                    }
+                    __syncwarp();  // the slot is read out before the next block reuses it
+                } else {
+                    const int m = row0 + lane;
+                    const bool valid = m < p.M;
+                    const int img = m / p.OHW;
+                    const long long base = (long long)img * p.C_out * p.OHW + (m - img * p.OHW);
+                    const bool pre = p.res_mode == ACNN_RES_ADD_THEN_ACT;
+                    const int nj = p.C_out - (n0 + c) < 32 ? p.C_out - (n0 + c) : 32;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (j >= nj) break;
+                        const int ch = n0 + c + j;
+                        const long long idx = base + (long long)ch * p.OHW;
+                        const float rv =
+                            (p.res_mode != ACNN_RES_NONE && valid) ? to_f32(res[idx]) : 0.f;
+                        const float x = t[j] + sP[ch];
+                        const float al = prelu ? sP[cpad + ch] : 0.f;
+                        const float o = pre ? apply_act(p.act, x + rv, al) : apply_act(p.act, x, al) + rv;
+                        if (valid) y[idx] = from_f32<T>(o);
+                    }
                 }
+            };
+            // add partial tile sp's values of this lane in block (ms, ci, qb)
+            auto add_part = [&](float (&t)[32], int sp, int ms, int ci, int qb) {
+                const float* blk = p.part +
+                    ((((size_t)tile * S + sp) * kChunksPerTile + ms * (BN / 32) + ci) * 4 + qb) * 1024;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 u = __ldcg(reinterpret_cast<const float4*>(blk + (j * 32 + lane) * 4));
+                    if (sp == 0) {
+                        t[4 * j] = u.x; t[4 * j + 1] = u.y; t[4 * j + 2] = u.z; t[4 * j + 3] = u.w;
+                    } else {
+                        t[4 * j] += u.x; t[4 * j + 1] += u.y; t[4 * j + 2] += u.z; t[4 * j + 3] += u.w;
+                    }
+                }
+            };
+            // Every unit has its own CTA and all CTAs are resident (the host
+            // splits only into one wave), so the splits of a tile meet on its
+            // counter and split sp finishes the tile's 32 x 32 blocks
+            // b = sp, sp + S, ..., summing every split's partial tile (read
+            // from L2) in split order.
+            int first = 0, step = 0;  // step 0: this CTA finishes nothing
+            if (e == 0 && lane == 0) {
+                __threadfence();
+                atomicAdd(p.cnt + tile, 1u);
+                *met_flag = wait_count(p.cnt + tile, (unsigned)S, abort_flag, p) ? 1 : 0;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+            if (*met_flag) {
+                __threadfence();  // the other splits' partial tiles are visible
+                first = split + S * e;
+                step = S * kEpiWarps;
+            }
+            const int nblk = MS * nch * 4;
+            for (int b = first; step > 0 && b < nblk; b += step) {
+                const int qb = b & 3, i = b >> 2;
+                const int ms = i / nch, ci = i - ms * nch;
+                float t[32];
+                for (int sp = 0; sp < S; ++sp) add_part(t, sp, ms, ci, qb);
+                finish(ms, ci, qb, t);
             }
             tc_fence_before();
             __syncwarp();
@@ -623,6 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+        cp_async_wait_newer(0);
     } else if (p.out_layout == ACNN_NHWC) {
         // ---------------------------------------------------- epilogue warps, NHWC
         // Warp e (0..11) owns the 32 rows of its TMEM lane quarter (warp % 4)
@@ -840,108 +994,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// ---------------------------------------------------------------- split-K reduce
-// y = act(sum_s part[s] + bias + kpre*res) + kpost*res, cast to the storage
-// type.  One thread per output pixel and 8 channels; NHWC walks channels
-// fastest (16-byte stores), NCHW walks pixels fastest (coalesced planes).
-template <int ACT, typename T>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(
-    const float* __restrict__ part, int splits, int M, int C_out, int OHW, int out_layout,
-    const float* __restrict__ bias, const float* __restrict__ alpha, const T* __restrict__ res,
-    int res_mode, T* __restrict__ y) {
-    const int G = C_out / 8;
-    const long long total = (long long)M * G;
-    const float kpre = res_mode == ACNN_RES_ADD_THEN_ACT ? 1.f : 0.f;
-    const float kpost = res_mode == ACNN_RES_ACT_THEN_ADD ? 1.f : 0.f;
-    const long long plane = (long long)M * C_out;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        int m, g;
-        if (out_layout == ACNN_NHWC) {
-            m = (int)(i / G);
-            g = (int)(i - (long long)m * G);
-        } else {
-            g = (int)(i / M);
-            m = (int)(i - (long long)g * M);
-        }
-        const int n = g * 8;
-        const float* src = part + (long long)m * C_out + n;
-        float acc[8];
-        {
-            const float4 a = *reinterpret_cast<const float4*>(src);
-            const float4 b = *reinterpret_cast<const float4*>(src + 4);
-            acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
-            acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
-        }
-        for (int s = 1; s < splits; ++s) {
-            const float4 a = *reinterpret_cast<const float4*>(src + s * plane);
-            const float4 b = *reinterpret_cast<const float4*>(src + s * plane + 4);
-            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-        }
-        float r[8], o[8];
-        long long oi[8];
-        if (out_layout == ACNN_NHWC) {
-            const long long base = (long long)m * C_out + n;
-            if (res_mode != ACNN_RES_NONE) {
-                const Vec<T, 8> rv = *reinterpret_cast<const Vec<T, 8>*>(res + base);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) r[j] = to_f32(rv.v[j]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) r[j] = 0.f;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) oi[j] = base + j;
-        } else {
-            const int img = m / OHW;
-            const long long base = (long long)img * C_out * OHW + (m - img * OHW);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                oi[j] = base + (long long)(n + j) * OHW;
-                r[j] = res_mode != ACNN_RES_NONE ? to_f32(res[oi[j]]) : 0.f;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float bv = bias ? __ldg(bias + n + j) : 0.f;
-            const float av = ACT == ACNN_ACT_PRELU ? __ldg(alpha + n + j) : 0.f;
-            o[j] = fmaf(kpost, r[j], act_fixed<ACT>(fmaf(kpre, r[j], acc[j] + bv), av));
-        }
-        if (out_layout == ACNN_NHWC) {
-            Vec<T, 8> ov;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) ov.v[j] = from_f32<T>(o[j]);
-            *reinterpret_cast<Vec<T, 8>*>(y + oi[0]) = ov;
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) y[oi[j]] = from_f32<T>(o[j]);
-        }
-    }
-}
-
-template <typename T>
-cudaError_t launch_reduce(const ConvArgs& a, const IgemmPlan& pl, long long M, cudaStream_t s) {
-    const long long work = M * (a.d.c_out / 8);
-    const int grid = grid_for(work, 256);
-    const float* part = static_cast<const float*>(a.ws_part);
-    const T* res = static_cast<const T*>(a.residual);
-    T* y = static_cast<T*>(a.y);
-    const int OHW = a.oh * a.ow;
-#define ACNN_REDUCE(ACT)                                                                     \
-    splitk_reduce_kernel<ACT, T><<<grid, 256, 0, s>>>(part, pl.splits, (int)M, a.d.c_out, OHW, \
-                                                      a.out_layout, a.bias, a.alpha, res,    \
-                                                      a.res_mode, y)
-    switch (a.act) {
-    case ACNN_ACT_RELU: ACNN_REDUCE(ACNN_ACT_RELU); break;
-    case ACNN_ACT_SILU: ACNN_REDUCE(ACNN_ACT_SILU); break;
-    case ACNN_ACT_PRELU: ACNN_REDUCE(ACNN_ACT_PRELU); break;
-    default: ACNN_REDUCE(ACNN_ACT_NONE); break;
-    }
-#undef ACNN_REDUCE
-    return cudaGetLastError();
-}
-
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 PFN_cuTensorMapEncodeIm2col_v12000 g_encode_im2col = nullptr;
@@ -990,10 +1042,10 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     const size_t b_all = (size_t)prm.num_kb * C::kBBytes;
     // shared bias / alpha copy for the NHWC epilogue: every column tile's
     // columns, so reads past C_out in a ragged last tile stay inside
-    const bool nhwc_epi = prm.out_layout == ACNN_NHWC && !prm.part;
-    prm.par_floats = prm.part ? 0 : prm.num_n_tiles * BN * (prm.act == ACNN_ACT_PRELU ? 2 : 1);
+    const bool nhwc_epi = prm.out_layout == ACNN_NHWC;
+    prm.par_floats = prm.num_n_tiles * BN * (prm.act == ACNN_ACT_PRELU ? 2 : 1);
     const size_t par_bytes = (size_t)prm.par_floats * 4;
-    prm.ring_slots = nhwc_epi ? (rd > 0 ? rd : 1) : 0;
+    prm.ring_slots = nhwc_epi ? (rd > 0 ? rd : 1) : 0;  // split-K: rd = 0, one slot
     const size_t ring_bytes = (size_t)kEpiWarps * prm.ring_slots * kStageBytes;
     auto stages_for = [&](bool resident) -> int {
         if (kSmemFixed + ring_bytes + par_bytes > kSmemMax) return 0;
@@ -1017,6 +1069,10 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
                         (resident ? b_all : 0);
     const int tiles = prm.num_m_tiles * prm.num_n_tiles * prm.splits;
     const int grid = tiles < sm_count() ? tiles : sm_count();
+    // split-K: one unit per CTA, one CTA per SM (the shared memory allows no
+    // second), so the splits of a tile can wait for each other; the planner
+    // splits only when that holds
+    if (prm.splits > 1 && tiles > sm_count()) return ACNN_ERR_UNSUPPORTED;
     kern<<<grid, kThreads, smem, s>>>(m.a, m.b, prm);
     return cudaGetLastError() == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
 }
@@ -1048,7 +1104,8 @@ int launch_typed(const ConvArgs& a, const IgemmPlan& pl, const Maps& m, const Pa
 // split-K adds a reduce launch that reads the fp32 partials and writes y.
 IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget) {
     const double kIssueUs = 0.30, kMmaUsPerMflop = 1.0 / 15.0, kHbmBytesPerUs = 6.0e6;
-    const double kLaunchUs = 3.0, kEpiUsPerChunk = 0.15;
+    const double kSplitUs = 1.5, kEpiUsPerChunk = 0.15;
+    const double kL2GBsPerSm = 100.0, kL2Bytes = 96.0e6;
     const long long M = (long long)d.n * oh * ow;
     // 32-channel k-blocks when C_in <= 32: a 64-channel block would be half zeros
     const int bk = d.c_in <= 32 ? 32 : 64;
@@ -1077,13 +1134,26 @@ IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget
                 const int kbs = (num_kb + sp - 1) / sp;
                 const int eff = (num_kb + kbs - 1) / kbs;  // splits actually used
                 if (eff != sp) continue;
-                const size_t part = eff > 1 ? (size_t)eff * M * d.c_out * sizeof(float) : 0;
+                // split-K: tile counters + one fp32 partial tile per (tile, split)
+                const size_t tile_bytes = (size_t)BM * ms * bn * sizeof(float);
+                const size_t part = eff > 1 ? (((size_t)tiles * 4 + 255) & ~(size_t)255) +
+                                                  (size_t)tiles * eff * tile_bytes
+                                            : 0;
                 if (part > part_budget) continue;
                 const long long units = tiles * eff;
+                // split only into one wave of co-resident CTAs: the splits of a
+                // tile then share its reduction (a second wave measured slower
+                // than no split)
+                if (eff > 1 && units > sms) continue;
                 const long long waves = (units + sms - 1) / sms;
                 double cost = waves * kbs * t_kb + ms * (bn / 64.0) * kEpiUsPerChunk * 2.0;
                 cost = fmax(cost, io_bytes / kHbmBytesPerUs);
-                if (eff > 1) cost += kLaunchUs + (double)part * 2.0 / kHbmBytesPerUs;
+                // each split writes its partial tile and reads back one tile's
+                // worth (its 1/S share of every split's partial, from L2 when the
+                // partials fit there); a memset clears the counters
+                if (eff > 1)
+                    cost += kSplitUs + 2.0 * tile_bytes * 1e-6 / kL2GBsPerSm +
+                            (part > kL2Bytes ? (double)part * 2.0 / kHbmBytesPerUs : 0.0);
                 if (cost < best_cost * 0.97) {  // prefer wide, short tiles and no split on ties
                     best_cost = cost;
                     best = IgemmPlan{bn, ms, eff, kbs, part, bk};
@@ -1095,8 +1165,8 @@ IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget
             }
         }
     }
-    // split only for a clear gain: the reduce adds a launch and its latency
-    return best.splits > 1 && best_cost > 0.8 * best1_cost ? best1 : best;
+    // split only for a clear gain: the reduction adds latency the model only estimates
+    return best.splits > 1 && best_cost > 0.85 * best1_cost ? best1 : best;
 }
 
 int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
@@ -1159,7 +1229,14 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     prm.num_m_tiles = num_m_tiles;
     prm.splits = plan.splits;
     prm.kb_per_split = plan.kb_per_split;
-    prm.part = plan.splits > 1 ? static_cast<float*>(a.ws_part) : nullptr;
+    // split-K workspace: tile counters, then the partial tiles
+    const int out_tiles = num_m_tiles * ((d.c_out + plan.bn - 1) / plan.bn);
+    const size_t cnt_bytes = ((size_t)out_tiles * 4 + 255) & ~(size_t)255;
+    prm.cnt = plan.splits > 1 ? static_cast<unsigned*>(a.ws_part) : nullptr;
+    prm.part = plan.splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws_part) + cnt_bytes)
+                               : nullptr;
+    if (plan.splits > 1 && cudaMemsetAsync(a.ws_part, 0, cnt_bytes, s) != cudaSuccess)
+        return ACNN_ERR_CUDA;
     prm.OW = a.ow;
     prm.OHW = a.oh * a.ow;
     prm.S = d.stride;
@@ -1176,12 +1253,8 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     prm.budget = wait_budget_polls();
     if (!prm.status) return ACNN_ERR_CUDA;
     const bool bf16 = d.dtype == ACNN_BF16;
-    int st = bf16 ? launch_typed<__nv_bfloat16>(a, plan, maps, prm, s)
-                  : launch_typed<__half>(a, plan, maps, prm, s);
-    if (st != ACNN_OK || plan.splits == 1) return st;
-    const cudaError_t e = bf16 ? launch_reduce<__nv_bfloat16>(a, plan, M, s)
-                               : launch_reduce<__half>(a, plan, M, s);
-    return e == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
+    return bf16 ? launch_typed<__nv_bfloat16>(a, plan, maps, prm, s)
+                : launch_typed<__half>(a, plan, maps, prm, s);
 }
 
 }  // namespace acnn

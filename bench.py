@@ -151,9 +151,10 @@ def workload_config(name, net, world):
 def launches_per_step(net):
     """Kernels of this library launched by one pass of the network.
 
-    A tensor-core conv is one implicit-GEMM launch, plus one split-K reduction when
-    the plan splits K, plus the two packing kernels of the explicit-im2col path or
-    the two NCHW->NHWC staging transposes of an NCHW conv; every other op is one."""
+    A tensor-core conv is one implicit-GEMM launch (a K split reduces inside it;
+    the split's counter reset is a memset, not a kernel), plus the two packing
+    kernels of the explicit-im2col path or the two NCHW->NHWC staging transposes
+    of an NCHW conv; every other op is one."""
     from activation_cnn_gb300 import acnn as A
     n = 0
     for op in net.ops:
@@ -167,10 +168,7 @@ def launches_per_step(net):
         if path == 0:
             n += 1
             continue
-        st, _, _, splits = A.acnn_conv2d_plan(d, A.acnn_conv2d_workspace_size(d))
-        if st != 0:
-            raise RuntimeError(f"conv plan failed: {A.status_string(st)}")
-        n += 1 + (splits > 1)
+        n += 1
         if path == 3 or net.layout == A.NCHW:
             n += 2
     return n

@@ -365,8 +365,9 @@ def min_workspace(d, full):
 
 @pytest.mark.parametrize("case", SPLITK_CASES, ids=[c[0] for c in SPLITK_CASES])
 def test_conv_split_k(case):
-    """Shapes whose plan splits K (fp32 partial sums + reduce kernel) match the oracle,
-    and a workspace too small for the split gives the same answer unsplit."""
+    """Shapes whose plan splits K (fp32 partial tiles, reduced by the last split of each
+    tile inside the kernel) match the oracle, and a workspace too small for the split
+    gives the same answer unsplit."""
     name, n, h, w, cin, cout, k, s, p, layout, act, res_mode = case
     dt = "bf16" if layout == G.NHWC else "f16"
     d = A.ConvDesc(n, h, w, cin, cout, k, k, s, p, layout, DT[dt])
@@ -398,6 +399,18 @@ def test_conv_split_k(case):
     assert st == 0, A.status_string(st)
     torch.cuda.synchronize()
     assert_parity(y1, ref, TDT[dt], name + " unsplit")
+    # split twice through one workspace: the tile counters start from zero each
+    # time and the split-order sum makes the result bitwise repeatable
+    wsf = torch.empty(full, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        yk = torch.empty_like(y)
+        st = A.acnn_conv2d_fused(d, x, wt, b, al, r, res_mode, act, yk, wsf, full)
+        assert st == 0, A.status_string(st)
+        outs.append(yk)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]), name + " split result not repeatable"
+    assert_parity(outs[0], ref, TDT[dt], name + " reused workspace")
 
 
 # ---------------------------------------------------------------- 256-row tiles
