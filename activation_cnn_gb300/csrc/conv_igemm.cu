@@ -617,10 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------- epilogue warps, split-K
         // Every split of an output tile writes its raw fp32 accumulators to its
         // partial tile in the workspace and counts itself in on the tile's
-        // counter; once all S have arrived, each finishes 1/S of the tile's
-        // 32 x 32 blocks: the sum of all partial tiles in split order (so the
-        // result does not depend on arrival order), then the bias / residual /
-        // activation / store epilogue.  Partial tiles are chunk-blocked: the 32 x 32 block of
+        // counter; after all its units, a CTA waits for the tiles it touched
+        // and finishes 1/S of each one's 32 x 32 blocks: the sum of all partial
+        // tiles in split order (so the result does not depend on arrival
+        // order), then the bias / residual / activation / store epilogue.
+        // Partial tiles are chunk-blocked: the 32 x 32 block of
         // (row block ms, chunk ci, lane quarter q) holds lane l's columns
         // 4j..4j+3 at float offset (j * 32 + l) * 4, so each warp store or load
         // instruction moves 512 contiguous bytes.
@@ -648,31 +649,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                    ((((size_t)tile * S + split) * kChunksPerTile + ms * (BN / 32) + ci) * 4 + q) *
                        1024;
         };
+        // Phase 1: every unit of this CTA -- MMAs, partial tile, count in.
         int acc = 0;
         uint32_t acc_phase = 0;
+        bool ok = true;
         for (int unit = blockIdx.x; unit < num_tiles; unit += gridDim.x) {
             const int tile = unit / S, split = unit - tile * S;
-            const int m0 = (tile / p.num_n_tiles) * TM;
             const int n0 = (tile % p.num_n_tiles) * BN;
-            const bool ok = __all_sync(0xffffffffu, wait_phase(tfull_bar(acc), acc_phase, abort_flag, p));
+            ok = __all_sync(0xffffffffu, wait_phase(tfull_bar(acc), acc_phase, abort_flag, p));
             if (!ok) break;
             tc_fence_after();
             const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
-            auto tmem_col = [&](int ms, int c) {
-                return tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * MS * BN + ms * BN + c);
-            };
             for (int i = grp; i < MS * nch; i += kEpiGroups) {
                 const int ms = i / nch, ci = i - ms * nch;
                 float v[32];
-                tmem_ld32(tmem_col(ms, ci * 32), v);
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
+                              (uint32_t)(acc * MS * BN + ms * BN + ci * 32),
+                          v);
                 float* blk = block_of(tile, split, ms, ci);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     *reinterpret_cast<float4*>(blk + (j * 32 + lane) * 4) =
                         make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
             // every epilogue warp has written this split's partial tile
             asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+            if (e == 0 && lane == 0) {
+                __threadfence();
+                atomicAdd(p.cnt + tile, 1u);
+            }
+        }
+        // Phase 2: for each of this CTA's units (t, sp), once all S splits of
+        // tile t have counted in, finish the tile's 32 x 32 blocks
+        // b = sp, sp + S, ...: the sum of every split's partial tile (read from
+        // L2) in split order, then the epilogue.  No CTA waits before it has
+        // written all its partial tiles and every CTA is resident (grid <= #SMs,
+        // one CTA per SM), so the waits always end.
+        for (int unit = blockIdx.x; ok && unit < num_tiles; unit += gridDim.x) {
+            const int tile = unit / S, split = unit - tile * S;
+            const int m0 = (tile / p.num_n_tiles) * TM;
+            const int n0 = (tile % p.num_n_tiles) * BN;
+            const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
+            if (e == 0 && lane == 0)
+                *met_flag = wait_count(p.cnt + tile, (unsigned)S, abort_flag, p) ? 1 : 0;
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+            if (!*met_flag) break;
+            __threadfence();  // the other splits' partial tiles are visible
             // finish one 32 x 32 block (row block ms, chunk ci, lane quarter qb)
             // of the tile from its split-order sum t
             auto finish = [&](int ms, int ci, int qb, float (&t)[32]) {
@@ -745,36 +772,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             };
-            // Every unit has its own CTA and all CTAs are resident (the host
-            // splits only into one wave), so the splits of a tile meet on its
-            // counter and split sp finishes the tile's 32 x 32 blocks
-            // b = sp, sp + S, ..., summing every split's partial tile (read
-            // from L2) in split order.
-            int first = 0, step = 0;  // step 0: this CTA finishes nothing
-            if (e == 0 && lane == 0) {
-                __threadfence();
-                atomicAdd(p.cnt + tile, 1u);
-                *met_flag = wait_count(p.cnt + tile, (unsigned)S, abort_flag, p) ? 1 : 0;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-            if (*met_flag) {
-                __threadfence();  // the other splits' partial tiles are visible
-                first = split + S * e;
-                step = S * kEpiWarps;
-            }
             const int nblk = MS * nch * 4;
-            for (int b = first; step > 0 && b < nblk; b += step) {
+            for (int b = split + S * e; b < nblk; b += S * kEpiWarps) {
                 const int qb = b & 3, i = b >> 2;
                 const int ms = i / nch, ci = i - ms * nch;
                 float t[32];
                 for (int sp = 0; sp < S; ++sp) add_part(t, sp, ms, ci, qb);
                 finish(ms, ci, qb, t);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
+            // every warp is done with this unit before the flag is reused
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
         }
         cp_async_wait_newer(0);
     } else if (p.out_layout == ACNN_NHWC) {
@@ -1069,10 +1076,8 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
                         (resident ? b_all : 0);
     const int tiles = prm.num_m_tiles * prm.num_n_tiles * prm.splits;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    // split-K: one unit per CTA, one CTA per SM (the shared memory allows no
-    // second), so the splits of a tile can wait for each other; the planner
-    // splits only when that holds
-    if (prm.splits > 1 && tiles > sm_count()) return ACNN_ERR_UNSUPPORTED;
+    // split-K relies on every CTA being resident: grid <= #SMs and one CTA per
+    // SM (the shared memory allows no second)
     kern<<<grid, kThreads, smem, s>>>(m.a, m.b, prm);
     return cudaGetLastError() == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
 }
@@ -1141,9 +1146,8 @@ IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget
                                             : 0;
                 if (part > part_budget) continue;
                 const long long units = tiles * eff;
-                // split only into one wave of co-resident CTAs: the splits of a
-                // tile then share its reduction (a second wave measured slower
-                // than no split)
+                // split only into one wave: with several units per CTA the extra
+                // partial-tile traffic measured slower than no split
                 if (eff > 1 && units > sms) continue;
                 const long long waves = (units + sms - 1) / sms;
                 double cost = waves * kbs * t_kb + ms * (bn / 64.0) * kEpiUsPerChunk * 2.0;
