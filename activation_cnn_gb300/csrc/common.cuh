@@ -136,6 +136,37 @@ cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, 
 cudaError_t launch_nchw_to_nhwc(int n, int c, int hw, int elem_bytes, const void* x, void* y,
                                 cudaStream_t s);
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization, so its CTAs may start (and run
+// their setup) while the previous kernel on the stream is still finishing;
+// each kernel executes griddep_wait() before its first access to global
+// memory, which returns once the previous kernel has completed and its writes
+// are visible (immediately when there is no such kernel).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel on the stream launch once every CTA of this grid has
+// executed it (or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Resident blocks of `kernel` per SM at this block size (cached per kernel).
 int occupancy_blocks(const void* kernel, int threads, size_t smem);
 

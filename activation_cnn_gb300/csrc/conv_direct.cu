@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(kThreads) direct_conv_kernel(
     const float* __restrict__ alpha, const T* __restrict__ res, T* __restrict__ y, int layout,
     int out_layout, int N, int H, int W, int C_in, int C_out, int kh_rt, int kw_rt, int S, int P,
     int OH, int OW, int act, int res_mode, int cic) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const int KH = KH_ > 0 ? KH_ : kh_rt;
     const int KW = KW_ > 0 ? KW_ : kw_rt;
     const int KK = KH * KW;
@@ -212,7 +213,7 @@ cudaError_t launch_typed(const ConvArgs& a, cudaStream_t s) {
     }
     const int tiles = ((a.oh + kTH - 1) / kTH) * ((a.ow + kTW - 1) / kTW);
     dim3 grid(tiles, (d.c_out + kCOB - 1) / kCOB, d.n);
-    kern<<<grid, kThreads, smem, s>>>(
+    launch_pdl(kern, grid, kThreads, smem, s, 
         static_cast<const T*>(a.x), static_cast<const T*>(a.w), a.bias, a.alpha,
         static_cast<const T*>(a.residual), static_cast<T*>(a.y), d.layout, a.out_layout, d.n,
         d.h, d.w, d.c_in, d.c_out, d.kh, d.kw, d.stride, d.pad, a.oh, a.ow, a.act, a.res_mode,

@@ -482,6 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // everything above (barriers, TMEM, tensor-map prefetch) may overlap the
+    // previous kernel on the stream; every global access below comes after it
+    griddep_wait();
 
     // a work unit is one output tile and one K range (the whole K without split-K)
     const int num_tiles = p.num_m_tiles * p.num_n_tiles * p.splits;
@@ -560,6 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+        // this CTA's loads are all issued: the next kernel on the stream may
+        // launch (its CTAs start as SMs free up and wait for this grid to end)
+        griddep_launch_dependents();
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
@@ -1078,7 +1084,7 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     const int grid = tiles < sm_count() ? tiles : sm_count();
     // split-K relies on every CTA being resident: grid <= #SMs and one CTA per
     // SM (the shared memory allows no second)
-    kern<<<grid, kThreads, smem, s>>>(m.a, m.b, prm);
+    launch_pdl(kern, grid, kThreads, smem, s, m.a, m.b, prm);
     return cudaGetLastError() == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
 }
 

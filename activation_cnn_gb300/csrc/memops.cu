@@ -25,6 +25,7 @@ template <typename T, int V>
 __global__ void __launch_bounds__(kThreads) pool_nhwc_kernel(
     const T* __restrict__ x, T* __restrict__ y, int kind, int N, int H, int W, int C, int OH,
     int OW, int K, int S, int P) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const int CV = C / V;
     const long long total = (long long)N * OH * OW * CV;
     const float inv = 1.0f / (float)(K * K);
@@ -74,6 +75,7 @@ __global__ void __launch_bounds__(kThreads) pool_nhwc_kernel(
 template <typename T, int V>
 __global__ void __launch_bounds__(kThreads) maxpool3s2_nhwc_kernel(
     const T* __restrict__ x, T* __restrict__ y, int N, int H, int W, int C, int OH, int OW) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const int CV = C / V;
     const long long total = (long long)N * OH * OW * CV;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)total;
@@ -128,6 +130,7 @@ __global__ void __launch_bounds__(kThreads) maxpool3s2_nhwc_kernel(
 template <typename T, int V, int U>
 __global__ void __launch_bounds__(kThreads) avgpool2_rows_kernel(
     const T* __restrict__ x, T* __restrict__ y, int H, int W, int C, int OH, int OW) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const int CV = C / V;
     const int r = blockIdx.x, oy = r % OH, n = r / OH;
     const int row_vecs = OW * CV;
@@ -170,6 +173,7 @@ __global__ void __launch_bounds__(kThreads) avgpool2_rows_kernel(
 template <typename T, int V>
 __global__ void __launch_bounds__(kThreads) maxpool3s2_rows_kernel(
     const T* __restrict__ x, T* __restrict__ y, int H, int W, int C, int OH, int OW) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const int CV = C / V;
     const int r = blockIdx.x, oy = r % OH, n = r / OH;
     const int j = blockIdx.y * kThreads + threadIdx.x;
@@ -210,6 +214,7 @@ template <typename T, int V, int U>
 __global__ void __launch_bounds__(kThreads) up2_rows_kernel(const T* __restrict__ x,
                                                             T* __restrict__ y, int H, int W,
                                                             int C) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const int CV = C / V;
     const int r = blockIdx.x, iy = r % H, n = r / H;
     const int OW = 2 * W;
@@ -242,6 +247,7 @@ template <typename T, int V>
 __global__ void __launch_bounds__(kThreads) up2_nhwc_kernel(const T* __restrict__ x,
                                                             T* __restrict__ y, int N, int H,
                                                             int W, int C) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const int CV = C / V;
     const long long total = (long long)N * H * W * CV;
     const int OW = 2 * W;
@@ -266,6 +272,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) pool_nchw_kernel(
     const T* __restrict__ x, T* __restrict__ y, int kind, int N, int C, int H, int W, int OH,
     int OW, int K, int S, int P) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const long long total = (long long)N * C * OH * OW;
     const float inv = 1.0f / (float)(K * K);
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)total;
@@ -323,6 +330,7 @@ template <typename Ti, typename To, int V>
 __global__ void __launch_bounds__(kThreads) resize_nhwc_kernel(
     const Ti* __restrict__ x, To* __restrict__ y, int mode, int N, int H, int W, int C, int OH,
     int OW, float sy, float sx) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const int CV = C / V;
     const long long total = (long long)N * OH * OW * CV;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)total;
@@ -363,6 +371,7 @@ template <typename Ti, typename To>
 __global__ void __launch_bounds__(kThreads) resize_nchw_kernel(
     const Ti* __restrict__ x, To* __restrict__ y, int mode, int NC, int H, int W, int OH, int OW,
     float sy, float sx) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const long long total = (long long)NC * OH * OW;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)total;
          i += gridDim.x * blockDim.x) {
@@ -398,6 +407,7 @@ template <typename T, int V>
 __global__ void __launch_bounds__(kThreads) concat_kernel(
     const T* __restrict__ a, const T* __restrict__ b, T* __restrict__ y, long long runs,
     int ra, int rb) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     // four vectors per thread (one block-width apart), all loaded before any
     // is stored; one division per vector
     constexpr int U = 4;
@@ -435,6 +445,7 @@ template <typename To>
 __global__ void __launch_bounds__(kThreads) prep_quarter_kernel(
     const uint32_t* __restrict__ f0, const uint32_t* __restrict__ f1, To* __restrict__ y, int H,
     int W, float t) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const int QH = H / 4, QW = W / 4;
     const long long P = (long long)QH * QW;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)P;
@@ -471,6 +482,7 @@ __global__ void __launch_bounds__(kThreads) deconv_kernel(
     const Ti* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
     const float* __restrict__ alpha, To* __restrict__ y, int layout, int N, int CI, int CO,
     int H, int W, int OH, int OW, int K, int S, int P, int act) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const long long pix = (long long)N * OH * OW;
     const int co_blocks = (CO + kDeconvCoBlock - 1) / kDeconvCoBlock;
     const long long total = pix * co_blocks;
@@ -535,6 +547,7 @@ __global__ void __launch_bounds__(kThreads) deconv_kernel(
 __global__ void __launch_bounds__(kThreads) im2col_pack_kernel(
     const uint16_t* __restrict__ x, uint16_t* __restrict__ a, int layout, int H, int W, int C,
     int KH, int KW, int S, int P, int OH, int OW, int Kp, int TP, int segs) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     extern __shared__ __align__(16) uint16_t st[];
     const int RW = (TP - 1) * S + KW;  // staged pixels per input row
     const int RL = RW * C;             // staged values per input row
@@ -605,6 +618,7 @@ __global__ void __launch_bounds__(kThreads) im2col_pack_kernel(
 __global__ void __launch_bounds__(kThreads) weight_pack_kernel(
     const uint16_t* __restrict__ w, uint16_t* __restrict__ wp, int layout, int C_out, int C,
     int KH, int KW, int Kp) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     const int K = KH * KW * C;
     const uint32_t total = (uint32_t)C_out * Kp;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -627,6 +641,7 @@ __global__ void __launch_bounds__(kThreads) weight_pack_kernel(
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) transpose_kernel(const uint16_t* __restrict__ x,
                                                          uint16_t* __restrict__ y, int C, int HW) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
     __shared__ uint16_t tile[32][33];
     const int n = blockIdx.z;
     const int c0 = blockIdx.y * 32, p0 = blockIdx.x * 32;
@@ -658,27 +673,27 @@ cudaError_t pool_typed(int kind, int n, int h, int w, int c, int k, int stride, 
         if (c % V == 0 && kind == ACNN_POOL_MAX && k == 3 && stride == 2 && pad == 1 &&
             rows <= 0x7fffffffLL && (row_vecs + kThreads - 1) / kThreads <= 65535) {
             dim3 g((unsigned)rows, (row_vecs + kThreads - 1) / kThreads);
-            maxpool3s2_rows_kernel<T, V><<<g, kThreads, 0, s>>>(xt, yt, h, w, c, oh, ow);
+            launch_pdl(maxpool3s2_rows_kernel<T, V>, g, kThreads, 0, s, xt, yt, h, w, c, oh, ow);
         } else if (c % V == 0 && kind == ACNN_POOL_AVG && k == 2 && stride == 2 && pad == 0 &&
                    rows <= 0x7fffffffLL && (row_vecs + 2 * kThreads - 1) / (2 * kThreads) <= 65535) {
             dim3 g((unsigned)rows, (row_vecs + 2 * kThreads - 1) / (2 * kThreads));
-            avgpool2_rows_kernel<T, V, 2><<<g, kThreads, 0, s>>>(xt, yt, h, w, c, oh, ow);
+            launch_pdl(avgpool2_rows_kernel<T, V, 2>, g, kThreads, 0, s, xt, yt, h, w, c, oh, ow);
         } else if (c % V == 0 && kind == ACNN_POOL_MAX && k == 3 && stride == 2 && pad == 1) {
             long long work = (long long)n * oh * ow * (c / V);
-            maxpool3s2_nhwc_kernel<T, V><<<grid_occ(maxpool3s2_nhwc_kernel<T, V>, work, kThreads), kThreads, 0, s>>>(
+            launch_pdl(maxpool3s2_nhwc_kernel<T, V>, grid_occ(maxpool3s2_nhwc_kernel<T, V>, work, kThreads), kThreads, 0, s, 
                 xt, yt, n, h, w, c, oh, ow);
         } else if (c % V == 0) {
             long long work = (long long)n * oh * ow * (c / V);
-            pool_nhwc_kernel<T, V><<<grid_occ(pool_nhwc_kernel<T, V>, work, kThreads), kThreads, 0, s>>>(
+            launch_pdl(pool_nhwc_kernel<T, V>, grid_occ(pool_nhwc_kernel<T, V>, work, kThreads), kThreads, 0, s, 
                 xt, yt, kind, n, h, w, c, oh, ow, k, stride, pad);
         } else {
             long long work = (long long)n * oh * ow * c;
-            pool_nhwc_kernel<T, 1><<<grid_occ(pool_nhwc_kernel<T, 1>, work, kThreads), kThreads, 0, s>>>(
+            launch_pdl(pool_nhwc_kernel<T, 1>, grid_occ(pool_nhwc_kernel<T, 1>, work, kThreads), kThreads, 0, s, 
                 xt, yt, kind, n, h, w, c, oh, ow, k, stride, pad);
         }
     } else {
         long long work = (long long)n * c * oh * ow;
-        pool_nchw_kernel<T><<<grid_occ(pool_nchw_kernel<T>, work, kThreads), kThreads, 0, s>>>(
+        launch_pdl(pool_nchw_kernel<T>, grid_occ(pool_nchw_kernel<T>, work, kThreads), kThreads, 0, s, 
             xt, yt, kind, n, c, h, w, oh, ow, k, stride, pad);
     }
     return cudaGetLastError();
@@ -698,28 +713,28 @@ cudaError_t resize_typed(int mode, int n, int c, int h, int w, int oh, int ow, i
             if (mode == ACNN_RESIZE_NEAREST && oh == 2 * h && ow == 2 * w && c % V == 0 &&
                 in_rows <= 0x7fffffffLL && (in_row_vecs + 2 * kThreads - 1) / (2 * kThreads) <= 65535) {
                 dim3 g((unsigned)in_rows, (in_row_vecs + 2 * kThreads - 1) / (2 * kThreads));
-                up2_rows_kernel<Ti, V, 2><<<g, kThreads, 0, s>>>(xt, reinterpret_cast<Ti*>(yt), h, w, c);
+                launch_pdl(up2_rows_kernel<Ti, V, 2>, g, kThreads, 0, s, xt, reinterpret_cast<Ti*>(yt), h, w, c);
                 return cudaGetLastError();
             }
             if (mode == ACNN_RESIZE_NEAREST && oh == 2 * h && ow == 2 * w && c % V == 0) {
                 long long work = (long long)n * h * w * (c / V);
-                up2_nhwc_kernel<Ti, V><<<grid_occ(up2_nhwc_kernel<Ti, V>, work, kThreads), kThreads, 0, s>>>(
+                launch_pdl(up2_nhwc_kernel<Ti, V>, grid_occ(up2_nhwc_kernel<Ti, V>, work, kThreads), kThreads, 0, s, 
                     xt, reinterpret_cast<Ti*>(yt), n, h, w, c);
                 return cudaGetLastError();
             }
         }
         if (c % V == 0) {
             long long work = (long long)n * oh * ow * (c / V);
-            resize_nhwc_kernel<Ti, To, V><<<grid_occ(resize_nhwc_kernel<Ti, To, V>, work, kThreads), kThreads, 0, s>>>(
+            launch_pdl(resize_nhwc_kernel<Ti, To, V>, grid_occ(resize_nhwc_kernel<Ti, To, V>, work, kThreads), kThreads, 0, s, 
                 xt, yt, mode, n, h, w, c, oh, ow, sy, sx);
         } else {
             long long work = (long long)n * oh * ow * c;
-            resize_nhwc_kernel<Ti, To, 1><<<grid_occ(resize_nhwc_kernel<Ti, To, 1>, work, kThreads), kThreads, 0, s>>>(
+            launch_pdl(resize_nhwc_kernel<Ti, To, 1>, grid_occ(resize_nhwc_kernel<Ti, To, 1>, work, kThreads), kThreads, 0, s, 
                 xt, yt, mode, n, h, w, c, oh, ow, sy, sx);
         }
     } else {
         long long work = (long long)n * c * oh * ow;
-        resize_nchw_kernel<Ti, To><<<grid_occ(resize_nchw_kernel<Ti, To>, work, kThreads), kThreads, 0, s>>>(
+        launch_pdl(resize_nchw_kernel<Ti, To>, grid_occ(resize_nchw_kernel<Ti, To>, work, kThreads), kThreads, 0, s, 
             xt, yt, mode, n * c, h, w, oh, ow, sy, sx);
     }
     return cudaGetLastError();
@@ -757,10 +772,10 @@ cudaError_t concat_typed(int n, int h, int w, int ca, int cb, int layout, const 
     auto blocks = [](long long work) { return (unsigned)((work + 4LL * kThreads - 1) / (4LL * kThreads)); };
     if (ra % V == 0 && rb % V == 0) {
         const long long work = runs * ((ra + rb) / V);
-        concat_kernel<T, V><<<blocks(work), kThreads, 0, s>>>(at, bt, yt, runs, (int)ra, (int)rb);
+        launch_pdl(concat_kernel<T, V>, blocks(work), kThreads, 0, s, at, bt, yt, runs, (int)ra, (int)rb);
     } else {
         const long long work = runs * (ra + rb);
-        concat_kernel<T, 1><<<blocks(work), kThreads, 0, s>>>(at, bt, yt, runs, (int)ra, (int)rb);
+        launch_pdl(concat_kernel<T, 1>, blocks(work), kThreads, 0, s, at, bt, yt, runs, (int)ra, (int)rb);
     }
     return cudaGetLastError();
 }
@@ -771,7 +786,7 @@ cudaError_t deconv_typed(const acnn_conv_desc& d, int oh, int ow, const void* x,
                          cudaStream_t s) {
     long long work = (long long)d.n * oh * ow *
                      ((d.c_out + kDeconvCoBlock - 1) / kDeconvCoBlock);
-    deconv_kernel<Ti, To><<<grid_occ(deconv_kernel<Ti, To>, work, kThreads), kThreads, 0, s>>>(
+    launch_pdl(deconv_kernel<Ti, To>, grid_occ(deconv_kernel<Ti, To>, work, kThreads), kThreads, 0, s, 
         static_cast<const Ti*>(x), w, bias, alpha, static_cast<To*>(y), d.layout, d.n, d.c_in,
         d.c_out, d.h, d.w, oh, ow, d.kh, d.stride, d.pad, act);
     return cudaGetLastError();
@@ -832,13 +847,13 @@ cudaError_t launch_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_
     int g = grid_for(work, kThreads);
     switch (out_dtype) {
     case ACNN_F32:
-        prep_quarter_kernel<float><<<g, kThreads, 0, s>>>(f0, f1, static_cast<float*>(y), h, w, t);
+        launch_pdl(prep_quarter_kernel<float>, g, kThreads, 0, s, f0, f1, static_cast<float*>(y), h, w, t);
         break;
     case ACNN_F16:
-        prep_quarter_kernel<__half><<<g, kThreads, 0, s>>>(f0, f1, static_cast<__half*>(y), h, w, t);
+        launch_pdl(prep_quarter_kernel<__half>, g, kThreads, 0, s, f0, f1, static_cast<__half*>(y), h, w, t);
         break;
     default:
-        prep_quarter_kernel<__nv_bfloat16><<<g, kThreads, 0, s>>>(
+        launch_pdl(prep_quarter_kernel<__nv_bfloat16>, g, kThreads, 0, s, 
             f0, f1, static_cast<__nv_bfloat16*>(y), h, w, t);
         break;
     }
@@ -859,12 +874,12 @@ cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, 
     const int segs = (ow + tp - 1) / tp;
     const long long blocks = (long long)d.n * oh * segs;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    im2col_pack_kernel<<<(unsigned)blocks, kThreads, staged(tp), s>>>(
+    launch_pdl(im2col_pack_kernel, (unsigned)blocks, kThreads, staged(tp), s, 
         static_cast<const uint16_t*>(x), static_cast<uint16_t*>(a), d.layout, d.h, d.w, d.c_in,
         d.kh, d.kw, d.stride, d.pad, oh, ow, kp, tp, segs);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    weight_pack_kernel<<<grid_occ(weight_pack_kernel, (long long)d.c_out * kp, kThreads), kThreads, 0, s>>>(
+    launch_pdl(weight_pack_kernel, grid_occ(weight_pack_kernel, (long long)d.c_out * kp, kThreads), kThreads, 0, s, 
         static_cast<const uint16_t*>(w), static_cast<uint16_t*>(wp), d.layout, d.c_out, d.c_in,
         d.kh, d.kw, kp);
     return cudaGetLastError();
@@ -874,7 +889,7 @@ cudaError_t launch_nchw_to_nhwc(int n, int c, int hw, int elem_bytes, const void
                                 cudaStream_t s) {
     if (elem_bytes != 2) return cudaErrorInvalidValue;
     dim3 grid((hw + 31) / 32, (c + 31) / 32, n), block(32, 32);
-    transpose_kernel<<<grid, block, 0, s>>>(static_cast<const uint16_t*>(x),
+    launch_pdl(transpose_kernel, grid, block, 0, s, static_cast<const uint16_t*>(x),
                                             static_cast<uint16_t*>(y), c, hw);
     return cudaGetLastError();
 }
