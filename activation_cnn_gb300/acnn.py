@@ -37,6 +37,7 @@ STATUS = {
 EXPORTS = (
     "acnn_conv2d_fused", "acnn_conv2d_out_hw", "acnn_conv2d_workspace_size", "acnn_conv2d_path",
     "acnn_pool2d", "acnn_resize2d", "acnn_concat", "acnn_deconv2d", "acnn_frame_prep_quarter",
+    "acnn_frame_flow_out",
     "acnn_status_string", "acnn_last_device_status", "acnn_set_wait_budget",
     "acnn_section_begin", "acnn_section_end", "acnn_section_launch", "acnn_section_destroy",
     "acnn_device_sm_count", "acnn_conv2d_fused_noalloc", "acnn_conv2d_plan",
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
         L.acnn_concat.argtypes = [_I] * 7 + [_P, _P, _P, _P]
         L.acnn_deconv2d.argtypes = [D, _P, _P, _P, _P, _I, _I, _P, _P]
         L.acnn_frame_prep_quarter.argtypes = [_I, _I, _P, _P, ctypes.c_float, _I, _P, _P]
+        L.acnn_frame_flow_out.argtypes = [_I, _I, _P, _I, _P, _P, _P, _P]
         L.acnn_status_string.argtypes = [_I]
         L.acnn_status_string.restype = ctypes.c_char_p
         L.acnn_last_device_status.argtypes = [_P]
@@ -177,6 +179,11 @@ def acnn_deconv2d(desc, x, w, bias, alpha, act, out_dtype, y, stream=None) -> in
 def acnn_frame_prep_quarter(h, w, rgba0, rgba1, t, out_dtype, y, stream=None) -> int:
     return lib().acnn_frame_prep_quarter(h, w, _ptr(rgba0), _ptr(rgba1), float(t), out_dtype,
                                          _ptr(y), _stream(stream))
+
+
+def acnn_frame_flow_out(h, w, tmp8, tmp8_dtype, rgba0, rgba1, out, stream=None) -> int:
+    return lib().acnn_frame_flow_out(h, w, _ptr(tmp8), tmp8_dtype, _ptr(rgba0), _ptr(rgba1),
+                                     _ptr(out), _stream(stream))
 
 
 def acnn_last_device_status(stream=None) -> int:
@@ -317,6 +324,15 @@ def frame_prep_quarter(rgba0, rgba1, t, *, out_dtype=torch.float16, out=None, st
                                                 device=rgba0.device)
     check(acnn_frame_prep_quarter(h, w, rgba0, rgba1, t, dtype_code(out_dtype), y, stream),
           "acnn_frame_prep_quarter")
+    return y
+
+
+def frame_flow_out(tmp8, rgba0, rgba1, *, out=None, stream=None):
+    """[5, h/8, w/8] flow/mask map + two h x w RGBA8 frames -> h x w RGBA8 frame."""
+    h, w, _ = rgba0.shape
+    y = out if out is not None else torch.empty((h, w, 4), dtype=torch.uint8, device=rgba0.device)
+    check(acnn_frame_flow_out(h, w, tmp8, dtype_code(tmp8.dtype), rgba0, rgba1, y, stream),
+          "acnn_frame_flow_out")
     return y
 
 

@@ -408,6 +408,23 @@ int acnn_frame_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_t* r
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int acnn_frame_flow_out(int h, int w, const void* tmp8, int tmp8_dtype, const uint8_t* rgba0,
+                        const uint8_t* rgba1, uint8_t* out_rgba, acnn_stream_t stream) {
+    if (!valid_dtype(tmp8_dtype)) return ACNN_ERR_BAD_ENUM;
+    if (!tmp8 || !rgba0 || !rgba1 || !out_rgba) return ACNN_ERR_NULL_POINTER;
+    if (h <= 0 || w <= 0 || h % 8 != 0 || w % 8 != 0) return ACNN_ERR_BAD_GEOMETRY;
+    if ((long long)h * w > kIndexLimit) return ACNN_ERR_TOO_LARGE;
+    if (!aligned16(tmp8) || !aligned16(rgba0) || !aligned16(rgba1) || !aligned16(out_rgba))
+        return ACNN_ERR_MISALIGNED;
+    const size_t fb = (size_t)h * w * 4;
+    const size_t tb = (size_t)5 * (h / 8) * (w / 8) * elem_size(tmp8_dtype);
+    if (overlaps(out_rgba, fb, rgba0, fb) || overlaps(out_rgba, fb, rgba1, fb) ||
+        overlaps(out_rgba, fb, tmp8, tb))
+        return ACNN_ERR_ALIAS;
+    return status_of(launch_flow_out(h, w, tmp8, tmp8_dtype, rgba0, rgba1, out_rgba,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* acnn_status_string(int status) {
     switch (status) {
     case ACNN_OK: return "ok";

@@ -477,6 +477,92 @@ __global__ void __launch_bounds__(kThreads) prep_quarter_kernel(
 // ----------------------------------------------------------------------------
 constexpr int kDeconvCoBlock = 8;
 
+// 4x4/s2/p1 transposed conv (the only geometry of the ABI), gather form
+// restated per input pixel: output (2a + py, 2b + px) takes its taps from the
+// 3x3 input neighbourhood of (a, b) -- rows a (ky = 1) and a - 1 (ky = 3) for
+// py = 0, rows a + 1 (ky = 0) and a (ky = 2) for py = 1, the same along x --
+// so one thread per input pixel accumulates the 2 x 2 outputs it owns.  A
+// block covers 32 input pixels of one row and 8 output channels; its 8 warps
+// split C_in (warp g takes ci = g, g + 8, ...) and add their partial sums
+// through shared memory in warp order.
+template <typename Ti, typename To>
+__global__ void __launch_bounds__(kThreads) deconv4s2_kernel(
+    const Ti* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
+    const float* __restrict__ alpha, To* __restrict__ y, int layout, int N, int CI, int CO, int H,
+    int W, int act) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+    constexpr int CB = kDeconvCoBlock;
+    __shared__ float red[kThreads / 32][32][4 * CB + 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_x = (W + 31) / 32;
+    const int a = (blockIdx.x / tiles_x) % H, n = (blockIdx.x / tiles_x) / H;
+    const int b = (blockIdx.x % tiles_x) * 32 + lane;
+    const int co0 = blockIdx.y * CB;
+    const int nco = min(CB, CO - co0);
+    float acc[2][2][CB];
+#pragma unroll
+    for (int py = 0; py < 2; ++py)
+#pragma unroll
+        for (int px = 0; px < 2; ++px)
+#pragma unroll
+            for (int j = 0; j < CB; ++j) acc[py][px][j] = 0.0f;
+    if (b < W) {
+        for (int ci = warp; ci < CI; ci += kThreads / 32) {
+            float nb[3][3];  // x at rows a-1..a+1, cols b-1..b+1 (zero outside)
+#pragma unroll
+            for (int dy = 0; dy < 3; ++dy)
+#pragma unroll
+                for (int dx = 0; dx < 3; ++dx) {
+                    const int iy = a - 1 + dy, ix = b - 1 + dx;
+                    nb[dy][dx] = (iy >= 0 && iy < H && ix >= 0 && ix < W)
+                                     ? to_f32(x[act_index(layout, CI, H, W, n, ci, iy, ix)])
+                                     : 0.0f;
+                }
+#pragma unroll
+            for (int j = 0; j < CB; ++j) {
+                if (j >= nco) break;
+                const float* wk = w + ((long long)ci * CO + co0 + j) * 16;  // [ky][kx]
+#pragma unroll
+                for (int py = 0; py < 2; ++py)
+#pragma unroll
+                    for (int px = 0; px < 2; ++px)
+#pragma unroll
+                        for (int ty = 0; ty < 2; ++ty)
+#pragma unroll
+                            for (int tx = 0; tx < 2; ++tx) {
+                                // py = 0: (ky, row) = (1, a), (3, a-1); py = 1: (0, a+1), (2, a)
+                                const int ky = py == 0 ? 1 + 2 * ty : 2 * ty;
+                                const int dy = py == 0 ? 1 - ty : 2 - ty;
+                                const int kx = px == 0 ? 1 + 2 * tx : 2 * tx;
+                                const int dx = px == 0 ? 1 - tx : 2 - tx;
+                                acc[py][px][j] =
+                                    fmaf(nb[dy][dx], __ldg(wk + ky * 4 + kx), acc[py][px][j]);
+                            }
+            }
+        }
+    }
+#pragma unroll
+    for (int py = 0; py < 2; ++py)
+#pragma unroll
+        for (int px = 0; px < 2; ++px)
+#pragma unroll
+            for (int j = 0; j < CB; ++j) red[warp][lane][(py * 2 + px) * CB + j] = acc[py][px][j];
+    __syncthreads();
+    // 32 pixels x 4 outputs x CB channels, summed over the warps in order
+    const int OH = 2 * H, OW = 2 * W;
+    for (int i = threadIdx.x; i < 32 * 4 * CB; i += kThreads) {
+        const int l = i / (4 * CB), r = i - l * 4 * CB;
+        const int pp = r / CB, j = r - pp * CB;
+        const int bb = (blockIdx.x % tiles_x) * 32 + l;
+        if (bb >= W || j >= nco) continue;
+        float v = bias ? bias[co0 + j] : 0.0f;
+        for (int g = 0; g < kThreads / 32; ++g) v += red[g][l][r];
+        const int oy = 2 * a + (pp >> 1), ox = 2 * bb + (pp & 1);
+        const float al = (act == ACNN_ACT_PRELU) ? alpha[co0 + j] : 0.0f;
+        y[act_index(layout, CO, OH, OW, n, co0 + j, oy, ox)] = from_f32<To>(apply_act(act, v, al));
+    }
+}
+
 template <typename Ti, typename To>
 __global__ void __launch_bounds__(kThreads) deconv_kernel(
     const Ti* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
@@ -784,6 +870,16 @@ template <typename Ti, typename To>
 cudaError_t deconv_typed(const acnn_conv_desc& d, int oh, int ow, const void* x, const float* w,
                          const float* bias, const float* alpha, int act, void* y,
                          cudaStream_t s) {
+    if (d.kh == 4 && d.kw == 4 && d.stride == 2 && d.pad == 1) {
+        const long long rows = (long long)d.n * d.h * ((d.w + 31) / 32);
+        const int cob = (d.c_out + kDeconvCoBlock - 1) / kDeconvCoBlock;
+        if (rows <= 0x7fffffffLL && cob <= 65535) {
+            launch_pdl(deconv4s2_kernel<Ti, To>, dim3((unsigned)rows, cob), kThreads, 0, s,
+                       static_cast<const Ti*>(x), w, bias, alpha, static_cast<To*>(y), d.layout,
+                       d.n, d.c_in, d.c_out, d.h, d.w, act);
+            return cudaGetLastError();
+        }
+    }
     long long work = (long long)d.n * oh * ow *
                      ((d.c_out + kDeconvCoBlock - 1) / kDeconvCoBlock);
     launch_pdl(deconv_kernel<Ti, To>, grid_occ(deconv_kernel<Ti, To>, work, kThreads), kThreads, 0, s, 

@@ -14,6 +14,7 @@ activation_cnn_gb300.inputs by layer name):
   block   ResNet bottleneck at 4x80x80x256 bf16, identity variant and the
           stride-2 downsample variant with an avgpool + 1x1 shortcut
   frame   frame-interpolation stack, NCHW fp16, two 1920x1088 RGBA8 frames
+  frame_out  the same stack ending in the flow-out stage (interpolated RGBA8 frame)
   backbone  ResNet-D-50 (3/4/6/3 bottlenecks) + top-down/bottom-up neck,
           NHWC bf16, 8x640x640x3
 """
@@ -358,15 +359,17 @@ def backbone_net(device="cuda", n=8, h=640, w=640) -> Net:
     return net
 
 
-def frame_net(device="cuda", h=1088, w=1920, c1=120, c2=240, t=0.5) -> Net:
+def frame_net(device="cuda", h=1088, w=1920, c1=120, c2=240, t=0.5, flow_out=False) -> Net:
     """Frame-interpolation conv stack, NCHW fp16 (rt.js run(), first 13 dispatches).
 
     prep (bilinear 1/4 of both RGBA8 frames + t plane) -> conv3x3/s2 7->c1 + PReLU
     -> conv3x3/s2 c1->c2 + PReLU -> 8 x conv3x3 c2->c2 + PReLU, the 8th adding the
-    map that entered the 8 (after its PReLU) -> deconv 4x4/s2 c2->5 -> bilinear x8.
+    map that entered the 8 (after its PReLU) -> deconv 4x4/s2 c2->5 -> bilinear x8;
+    with flow_out, the last step is instead the flow-out stage (x8 upsample, warp
+    of both frames, blend, RGBA8 output frame).
     """
     seed = 1237
-    net = Net("frame", 1, G.F16, G.NCHW)
+    net = Net("frame_out" if flow_out else "frame", 1, G.F16, G.NCHW)
     b = Builder(net, seed, device)
     b.set_section("frame")
     f0 = G.rgba_frame(seed, "frame0", h, w).to(device)
@@ -406,8 +409,22 @@ def frame_net(device="cuda", h=1088, w=1920, c1=120, c2=240, t=0.5) -> Net:
 
     net.ops.append(Op("deconv", "frame", deconv, 2.0 * 5 * c2 * 4 * (2 * hh) * (2 * ww),
                       (xin.numel() + tmp8.numel()) * 2 + wdc.numel() * 4, "deconv"))
-    b.resize("tmp8", "flow", A.RESIZE_BILINEAR, 5, 2 * hh, 2 * ww, h, w)
-    net.outputs = ["flow"]
+    if not flow_out:
+        b.resize("tmp8", "flow", A.RESIZE_BILINEAR, 5, 2 * hh, 2 * ww, h, w)
+        net.outputs = ["flow"]
+        return net
+    # flow-out stage (rt.js wgslFlowOut): x8 upsample of tmp8, warp both
+    # frames by their flows, sigmoid-mask blend, RGBA8 pack
+    out = torch.empty((h, w, 4), dtype=torch.uint8, device=device)
+    net.tensors["out"] = out
+
+    def flow_stage(stream):
+        A.check(A.acnn_frame_flow_out(h, w, tmp8, G.F16, f0, f1, out, stream), "flow_out")
+
+    # algorithmic bytes: the 1/8 map, both frames once, the output frame
+    net.ops.append(Op("flow_out", "frame", flow_stage, 0.0,
+                      tmp8.numel() * 2 + 3 * h * w * 4, "flow_out"))
+    net.outputs = ["out"]
     return net
 
 
@@ -417,5 +434,6 @@ WORKLOADS = {
     "block": lambda device="cuda": block_net(device, "identity"),
     "block_down": lambda device="cuda": block_net(device, "downsample"),
     "frame": frame_net,
+    "frame_out": lambda device="cuda": frame_net(device, flow_out=True),
     "backbone": backbone_net,
 }

@@ -434,7 +434,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="backbone",
-                    choices=["backbone", "block", "block_down", "stem", "conv1", "frame"])
+                    choices=["backbone", "block", "block_down", "stem", "conv1", "frame", "frame_out"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--layers", action="store_true", help="add per-conv timings")

@@ -216,6 +216,25 @@ int acnn_deconv2d(const acnn_conv_desc* d, const void* x, const float* w, const 
 int acnn_frame_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_t* rgba1, float t,
                             int out_dtype, void* y, acnn_stream_t stream);
 
+/* ---- frame flow-out ----------------------------------------------------------
+ * rt.js wgslFlowOut (the stage after the deconv of the frame stack), with
+ * wgslPrepFull's full-resolution planes read straight from the frames.
+ *   tmp8     device [5, h/8, w/8] NCHW of tmp8_dtype: flow of frame 0 (x, y),
+ *            flow of frame 1 (x, y), mask logit
+ *   rgba0/1  device h x w RGBA8 frames (bytes R, G, B, A per pixel)
+ *   out_rgba device h x w RGBA8 output
+ * Per output pixel: the five planes upsampled x8 (bilinear, align_corners=
+ * false, clamped taps), flows times 8, m = 1/(1+exp(-mask)); each frame's
+ * B, G, R (byte/255) sampled bilinearly at (x, y) + its flow with clamped taps
+ * (grid_sample border, align_corners=true); v = w0*m + w1*(1-m); output bytes
+ * R, G, B = (uint)(clamp(v, 0, 1) * 255) (truncation), A = 255.  Computed in
+ * binary32 in one fixed order without fused multiply-adds; exp by Cody-Waite
+ * reduction and a degree-7 Taylor polynomial.  h and w multiples of 8; all
+ * pointers 16-byte aligned; out_rgba must not overlap an input.
+ */
+int acnn_frame_flow_out(int h, int w, const void* tmp8, int tmp8_dtype, const uint8_t* rgba0,
+                        const uint8_t* rgba1, uint8_t* out_rgba, acnn_stream_t stream);
+
 /* ---- status ------------------------------------------------------------------ */
 /* Static string for a status code. */
 const char* acnn_status_string(int status);

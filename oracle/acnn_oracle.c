@@ -14,7 +14,9 @@
  *   P3  "@framecast/rt 1.0.0 -- package/rt.js": wgslConv (per-channel PReLU
  *       and the activate-then-add residual), wgslPrepQuarter (RGBA8 unpack,
  *       BGR order, timestep plane, bilinear 1/4), wgslFlowOut (bilinear x8),
- *       wgslDeconv (4x4/s2/p1 transposed conv, gather form).
+ *       wgslDeconv (4x4/s2/p1 transposed conv, gather form), wgslPrepFull and
+ *       wgslFlowOut's warp, blend and RGBA8 pack (the one op computed in
+ *       binary32, because a float there decides an output byte).
  *
  * Every value is a double.  Where the GPU path stores activations in a
  * narrower type, the caller rounds with oracle_round_storage() between ops
@@ -401,6 +403,146 @@ int oracle_prep_quarter(int H, int W, const uint8_t* rgba0, const uint8_t* rgba1
     }
     for (size_t i = 0; i < (size_t)QH * QW; ++i) y[(size_t)6 * QH * QW + i] = t;
     free(plane);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* flow out: P3 wgslFlowOut (the stage after the deconv of the frame stack),  */
+/* with wgslPrepFull's full-resolution planes read straight from the RGBA8    */
+/* frames.  The page computes it in binary32 and truncates to bytes, so a     */
+/* float decides an integer here: this function computes in float, one       */
+/* operation at a time in the order below (gcc -ffp-contract=off: no fused    */
+/* multiply-adds), and the CUDA kernel follows the same order, so the bytes   */
+/* agree exactly.                                                            */
+/*                                                                          */
+/*   t = tmp8, 5 planes (flow0 x,y, flow1 x,y, mask) at (H/8, W/8)           */
+/*   for output pixel (x, y):                                                */
+/*     sx = (x + 0.5) * 0.125 - 0.5, sy likewise  (align_corners=false x8)   */
+/*     up(c) = bilinear of plane c at (sx, sy): x0 = floor(sx), fx = sx - x0, */
+/*             taps clamped into the plane, mix(a, b, f) = a*(1-f) + b*f,    */
+/*             first along x on rows y0 and y0+1, then along y              */
+/*     flow0 = 8 * (up(0), up(1)), flow1 = 8 * (up(2), up(3))                */
+/*     m = 1 / (1 + exp(-up(4)))                                             */
+/*     w_f = bilinear of frame f's B, G, R (byte / 255) at                   */
+/*           (x + flow_f.x, y + flow_f.y), taps clamped into the frame       */
+/*           (grid_sample, border, align_corners=true)                      */
+/*     bgr = w0 * m + w1 * (1 - m)                                           */
+/*     out = bytes R, G, B, 255 with each = (uint)(clamp(v, 0, 1) * 255)     */
+/*                                                                          */
+/* exp is computed by a method named here rather than taken from a math      */
+/* library, so that the CUDA side can implement the same steps: Cody and     */
+/* Waite's argument reduction x = n ln2 + r, |r| <= ln2 / 2, with ln2 split   */
+/* into a head exact in a few bits and a tail, then the degree-7 Taylor       */
+/* polynomial of e^r (error below 1e-8 relative for |r| <= 0.35) in Horner    */
+/* form, each step a correctly rounded fmaf, then scaling by 2^n.             */
+/* ------------------------------------------------------------------------ */
+static float flow_exp(float x)
+{
+    const float log2e = 1.44269504088896341f;
+    const float ln2_hi = 0.693145751953125f;      /* 0x3f317200: 15 significant bits */
+    const float ln2_lo = 1.42860682030941723e-6f; /* ln 2 - ln2_hi */
+    if (x > 88.0f) x = 88.0f;
+    if (x < -87.0f) x = -87.0f;
+    const float n = rintf(x * log2e);
+    float r = x - n * ln2_hi;
+    r = r - n * ln2_lo;
+    float q = 1.0f / 5040.0f;
+    q = fmaf(q, r, 1.0f / 720.0f);
+    q = fmaf(q, r, 1.0f / 120.0f);
+    q = fmaf(q, r, 1.0f / 24.0f);
+    q = fmaf(q, r, 1.0f / 6.0f);
+    q = fmaf(q, r, 0.5f);
+    q = fmaf(q, r, 1.0f);
+    q = fmaf(q, r, 1.0f);
+    return ldexpf(q, (int)n);
+}
+
+static float flow_mix(float a, float b, float f)
+{
+    const float u = a * (1.0f - f);
+    const float v = b * f;
+    return u + v;
+}
+
+typedef struct {
+    int H, W;
+    const float* t;
+    const uint8_t* f0;
+    const uint8_t* f1;
+    float* pre;   /* [3][H][W] clamped R, G, B in [0, 1] before the byte scale */
+    uint8_t* out; /* [H][W][4] */
+} flow_args;
+
+static float flow_up(const flow_args* a, int c, float sx, float sy)
+{
+    const int TH = a->H / 8, TW = a->W / 8;
+    const float* pl = a->t + (size_t)c * TH * TW;
+    const float fx0 = floorf(sx), fy0 = floorf(sy);
+    const int x0 = (int)fx0, y0 = (int)fy0;
+    const float fx = sx - fx0, fy = sy - fy0;
+    const int xa = clampi(x0, 0, TW - 1), xb = clampi(x0 + 1, 0, TW - 1);
+    const int ya = clampi(y0, 0, TH - 1), yb = clampi(y0 + 1, 0, TH - 1);
+    const float top = flow_mix(pl[(size_t)ya * TW + xa], pl[(size_t)ya * TW + xb], fx);
+    const float bot = flow_mix(pl[(size_t)yb * TW + xa], pl[(size_t)yb * TW + xb], fx);
+    return flow_mix(top, bot, fy);
+}
+
+/* Bilinear B, G, R of an RGBA8 frame at pixel-space (px, py), clamped taps. */
+static void flow_warp(const flow_args* a, const uint8_t* f, float px, float py, float bgr[3])
+{
+    const float fx0 = floorf(px), fy0 = floorf(py);
+    const float fx = px - fx0, fy = py - fy0;
+    /* clamp in float first: a flow can put the tap far outside the int range */
+    const float cx0 = fx0 < -1.0f ? -1.0f : (fx0 > (float)a->W ? (float)a->W : fx0);
+    const float cy0 = fy0 < -1.0f ? -1.0f : (fy0 > (float)a->H ? (float)a->H : fy0);
+    const int x0 = (int)cx0, y0 = (int)cy0;
+    const int xa = clampi(x0, 0, a->W - 1), xb = clampi(x0 + 1, 0, a->W - 1);
+    const int ya = clampi(y0, 0, a->H - 1), yb = clampi(y0 + 1, 0, a->H - 1);
+    for (int k = 0; k < 3; ++k) {
+        const int byte = 2 - k; /* B, G, R */
+        const float p00 = (float)f[((size_t)ya * a->W + xa) * 4 + byte] / 255.0f;
+        const float p01 = (float)f[((size_t)ya * a->W + xb) * 4 + byte] / 255.0f;
+        const float p10 = (float)f[((size_t)yb * a->W + xa) * 4 + byte] / 255.0f;
+        const float p11 = (float)f[((size_t)yb * a->W + xb) * 4 + byte] / 255.0f;
+        bgr[k] = flow_mix(flow_mix(p00, p01, fx), flow_mix(p10, p11, fx), fy);
+    }
+}
+
+static void flow_row(const void* p, int y)
+{
+    const flow_args* a = (const flow_args*)p;
+    for (int x = 0; x < a->W; ++x) {
+        const float sx = ((float)x + 0.5f) * 0.125f - 0.5f;
+        const float sy = ((float)y + 0.5f) * 0.125f - 0.5f;
+        const float u0 = flow_up(a, 0, sx, sy) * 8.0f, v0 = flow_up(a, 1, sx, sy) * 8.0f;
+        const float u1 = flow_up(a, 2, sx, sy) * 8.0f, v1 = flow_up(a, 3, sx, sy) * 8.0f;
+        const float m = 1.0f / (1.0f + flow_exp(-flow_up(a, 4, sx, sy)));
+        float w0[3], w1[3];
+        flow_warp(a, a->f0, (float)x + u0, (float)y + v0, w0);
+        flow_warp(a, a->f1, (float)x + u1, (float)y + v1, w1);
+        const float om = 1.0f - m;
+        uint8_t* o = a->out + ((size_t)y * a->W + x) * 4;
+        for (int k = 0; k < 3; ++k) { /* k: B, G, R -> byte 2 - k */
+            const float u = w0[k] * m;
+            const float v = w1[k] * om;
+            float c = u + v;
+            c = c < 0.0f ? 0.0f : (c > 1.0f ? 1.0f : c);
+            if (a->pre) a->pre[(size_t)(2 - k) * a->H * a->W + (size_t)y * a->W + x] = c;
+            o[2 - k] = (uint8_t)(unsigned)(c * 255.0f);
+        }
+        o[3] = 255;
+    }
+}
+
+/* H, W multiples of 8; tmp8 [5][H/8][W/8] float; frames [H][W][4] bytes;
+ * out [H][W][4] bytes (R, G, B, 255); pre (optional) [3][H][W] the clamped
+ * R, G, B values before the byte scale. */
+int oracle_flow_out(int H, int W, const float* tmp8, const uint8_t* rgba0, const uint8_t* rgba1,
+                    uint8_t* out, float* pre, int nthreads)
+{
+    if (H <= 0 || W <= 0 || H % 8 || W % 8) return -1;
+    flow_args a = {H, W, tmp8, rgba0, rgba1, pre, out};
+    for_rows(flow_row, &a, H, nthreads);
     return 0;
 }
 

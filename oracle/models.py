@@ -143,10 +143,11 @@ def backbone(x):
 
 
 # ------------------------------------------------------------------ frame stack
-def frame(rgba0, rgba1, t=0.5, c1=120, c2=240):
+def frame(rgba0, rgba1, t=0.5, c1=120, c2=240, flow_out=False):
     """rt.js run() up to the x8 upsample: prep -> prelu(conv s2) x2 -> 8 x conv +
     PReLU with the map entering the 8 added after the 8th PReLU -> deconv 4x4/s2
-    -> bilinear x8.  NCHW fp16 storage."""
+    -> bilinear x8.  NCHW fp16 storage.  With flow_out the last step is the
+    flow-out stage instead, returning the interpolated [H, W, 4] RGBA8 frame."""
     r = Runner(Params(1237, O.NCHW, G.F16), O.F16)
     xq = r.store(O.prep_quarter(rgba0, rgba1, t))[None]
     P = O.ACT_PRELU
@@ -163,4 +164,7 @@ def frame(rgba0, rgba1, t=0.5, c1=120, c2=240):
     b = _f64(G.conv_bias(1237, "lastconv", 5))
     tmp8 = r.store(O.deconv2d(f, w, b))
     h, wd = rgba0.shape[0], rgba0.shape[1]
+    if flow_out:
+        # rt.js wgslFlowOut on the fp16-stored map, in binary32 as on the page
+        return O.flow_out(tmp8[0].astype(np.float32), rgba0, rgba1)
     return r.store(O.resize2d(tmp8, O.BILINEAR, h, wd, layout=O.NCHW))

@@ -68,6 +68,8 @@ def _load():
     lib.oracle_deconv2d.argtypes = [i] * 9 + [d] * 4 + [i, d, i]
     lib.oracle_prep_quarter.argtypes = [i, i, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_double, d]
+    lib.oracle_flow_out.argtypes = [i, i, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_void_p, i]
     lib.oracle_round_storage.argtypes = [d, ctypes.c_size_t, i]
     lib.oracle_round_value.argtypes = [ctypes.c_double, i]
     lib.oracle_round_value.restype = ctypes.c_double
@@ -217,6 +219,25 @@ def prep_quarter(rgba0, rgba1, t):
     rc = lib.oracle_prep_quarter(h, w, a.ctypes.data, b.ctypes.data, float(t), _ptr(y))
     assert rc == 0
     return y
+
+
+def flow_out(tmp8, rgba0, rgba1, *, with_pre=False, threads=None):
+    """P3 wgslFlowOut: [5, H/8, W/8] flow/mask (float32) + two [H, W, 4] uint8
+    frames -> [H, W, 4] uint8 (and, with_pre, the clamped R, G, B [3, H, W]
+    float32 before the byte scale).  Computed in binary32, as on the page."""
+    lib = _load()
+    a = np.ascontiguousarray(rgba0, dtype=np.uint8)
+    b = np.ascontiguousarray(rgba1, dtype=np.uint8)
+    h, w, four = a.shape
+    assert four == 4 and b.shape == a.shape and h % 8 == 0 and w % 8 == 0
+    t = np.ascontiguousarray(tmp8, dtype=np.float32)
+    assert t.shape == (5, h // 8, w // 8)
+    out = np.empty((h, w, 4), np.uint8)
+    pre = np.empty((3, h, w), np.float32) if with_pre else None
+    rc = lib.oracle_flow_out(h, w, t.ctypes.data, a.ctypes.data, b.ctypes.data, out.ctypes.data,
+                             pre.ctypes.data if with_pre else None, threads or nthreads())
+    assert rc == 0
+    return (out, pre) if with_pre else out
 
 
 def round_storage(v, dtype):

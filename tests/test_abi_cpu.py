@@ -117,6 +117,12 @@ def test_companions_reject_before_launch(A):
     assert A.acnn_deconv2d(d4, X, W, None, None, 0, 7, Y, 0) == 7
     assert A.acnn_frame_prep_quarter(10, 16, X, W, 0.5, 1, Y, 0) == 2          # h % 4
     assert A.acnn_frame_prep_quarter(16, 16, X, None, 0.5, 1, Y, 0) == 1
+    # flow out: h, w multiples of 8, dtype enum, pointers, alignment, aliasing
+    assert A.acnn_frame_flow_out(12, 16, X, 1, W, Y, Y + (1 << 20), 0) == 2
+    assert A.acnn_frame_flow_out(16, 16, X, 9, W, Y, Y + (1 << 20), 0) == 7
+    assert A.acnn_frame_flow_out(16, 16, None, 1, W, Y, Y + (1 << 20), 0) == 1
+    assert A.acnn_frame_flow_out(16, 16, X, 1, W + 4, Y, Y + (1 << 20), 0) == 4
+    assert A.acnn_frame_flow_out(16, 16, X, 1, W, Y, W + 512, 0) == 6
 
 
 def test_wait_budget_knob(A):

@@ -91,6 +91,31 @@ def test_frame_reduced_end_to_end():
     assert_maps([y], [ref], torch.float16)
 
 
+def test_frame_out_reduced_end_to_end():
+    """The frame stack ending in the flow-out stage, against the oracle's stack
+    (fp64 convs with fp16 storage, binary32 flow-out).  The two 1/8-resolution
+    maps differ by fp16 storage-rounding noise, and warping random-noise frames
+    turns a flow difference of d pixels into byte differences of up to ~255*d,
+    so the bytes are compared statistically; the flow-out kernel itself is
+    checked byte for byte in test_ops_gpu.py."""
+    net = N.frame_net(h=128, w=192, flow_out=True)
+    (y,) = run_graph(net)
+    f0, f1 = net.inputs["frame0"].cpu().numpy(), net.inputs["frame1"].cpu().numpy()
+    ref = M.frame(f0, f1, flow_out=True)
+    got = y.cpu().numpy()
+    assert got.shape == ref.shape == (128, 192, 4)
+    assert (got[..., 3] == 255).all()
+    d = np.abs(got[..., :3].astype(np.int32) - ref[..., :3].astype(np.int32))
+    print(f"frame_out: exact {np.mean(d == 0):.4f}, within 1 {np.mean(d <= 1):.4f}, "
+          f"mean {d.mean():.4f}, max {d.max()}")
+    # bound: the maps agree to fp16 storage rounding (about 1e-3 relative), the
+    # flows are scaled by 8, and a flow difference of d pixels moves a byte of a
+    # random-noise frame by up to 255 * d -- so a few bytes per thousand may move
+    # by 2 and none by more than 4; most agree exactly
+    assert d.max() <= 4 and np.mean(d <= 1) >= 0.995 and d.mean() <= 0.3 and \
+        np.mean(d == 0) >= 0.75, (np.mean(d == 0), np.mean(d <= 1), d.mean(), d.max())
+
+
 def test_backbone_reduced_end_to_end():
     net = N.backbone_net(n=1, h=128, w=160)
     outs = run_graph(net)

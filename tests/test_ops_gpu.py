@@ -293,8 +293,9 @@ def test_concat_bitexact(dt, layout, cc):
 # ---------------------------------------------------------------- deconv
 @pytest.mark.parametrize("dt_in,dt_out", [("f16", "f16"), ("f32", "f32"), ("bf16", "f32")])
 @pytest.mark.parametrize("layout", [G.NCHW, G.NHWC])
-def test_deconv(dt_in, dt_out, layout):
-    n, ci, co, h, w = 2, 24, 5, 7, 9
+@pytest.mark.parametrize("shape", [(2, 24, 5, 7, 9), (1, 240, 5, 68, 120), (1, 40, 20, 11, 70)])
+def test_deconv(dt_in, dt_out, layout, shape):
+    n, ci, co, h, w = shape
     x = G.tensor(8, "dcx", G.activation_shape(layout, n, ci, h, w), "normal", dtype=DT[dt_in])
     wt = G.deconv_weight(8, "dc", ci, co, 4)
     b = G.conv_bias(8, "dc", co)
@@ -433,3 +434,40 @@ def test_conv_256_row_tiles(case):
     y, ref = conv_case("r256" + name, n, h, w, cin, cout, k, s, p, dt, layout=layout, act=act,
                        res_mode=res_mode)
     assert_parity(y, ref, TDT[dt], name)
+
+
+# ---------------------------------------------------------------- flow out (NEXT-1)
+def _flow_inputs(h, w, dt, seed=21, flow=3.0, mask_std=3.0):
+    """Flows uniform in [-flow, flow] at 1/8 resolution (x8 on the page: up to
+    8*flow pixels), mask logits N(0, mask_std), two random RGBA8 frames."""
+    t = torch.cat([G.tensor(seed, "flow.uv", (4, h // 8, w // 8), "uniform", -flow, flow),
+                   G.tensor(seed, "flow.mask", (1, h // 8, w // 8), "normal", std=mask_std)])
+    t = t.to(TDT[dt])
+    f0 = G.rgba_frame(seed, "flow.f0", h, w)
+    f1 = G.rgba_frame(seed, "flow.f1", h, w)
+    return t, f0, f1
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("hw", [(8, 8), (64, 96), (136, 200), (1088, 1920)])
+def test_flow_out_bitexact(dt, hw):
+    """Every output byte equals the binary32 oracle's (same operation order,
+    no fused multiply-adds, the same named exp method on both sides)."""
+    h, w = hw
+    t, f0, f1 = _flow_inputs(h, w, dt)
+    y = A.frame_flow_out(t.cuda(), f0.cuda(), f1.cuda())
+    torch.cuda.synchronize()
+    ref = O.flow_out(t.float().numpy(), f0.numpy(), f1.numpy())
+    assert_bitexact(y.cpu(), torch.from_numpy(ref), f"flow_out {dt} {hw}")
+
+
+@pytest.mark.parametrize("flow,mask_std", [(200.0, 40.0), (0.0, 0.0), (0.125, 100.0)])
+def test_flow_out_extremes_bitexact(flow, mask_std):
+    """Flows far outside the frame (clamped taps), zero flow and mask 0 (m = 1/2),
+    whole-pixel flows with saturated masks."""
+    h, w = 72, 136
+    t, f0, f1 = _flow_inputs(h, w, "f32", seed=22, flow=flow, mask_std=mask_std)
+    y = A.frame_flow_out(t.cuda(), f0.cuda(), f1.cuda())
+    torch.cuda.synchronize()
+    ref = O.flow_out(t.numpy(), f0.numpy(), f1.numpy())
+    assert_bitexact(y.cpu(), torch.from_numpy(ref), f"flow_out extremes {flow} {mask_std}")

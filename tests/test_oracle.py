@@ -443,3 +443,119 @@ def test_round_storage_matches_torch_cast(dt, tdt):
     ]).astype(np.float32).astype(np.float64)
     ref = torch.from_numpy(v.astype(np.float32)).to(tdt).to(torch.float64).numpy()
     np.testing.assert_array_equal(O.round_storage(v, dt), ref)
+
+
+# --------------------------------------------------------------------------- flow out (NEXT-1)
+# P3 "@framecast/rt 1.0.0 -- package/rt.js", wgslFlowOut: x8 bilinear upsample of
+# the flow/mask map, backward warp of both frames, sigmoid-mask blend, truncating
+# RGBA8 pack, all in binary32.  The pins below restate the page's arithmetic in
+# numpy float32 (one operation at a time, so nothing is fused) for inputs where
+# the warp or the blend reduce to a closed form.
+f32 = np.float32
+
+
+def _unit(bytes_):
+    return bytes_.astype(f32) / f32(255)
+
+
+def _byte(v):
+    return np.floor(np.clip(v, f32(0), f32(1)) * f32(255)).astype(np.uint8)
+
+
+def _flow_map(h, w, u0=0.0, v0=0.0, u1=0.0, v1=0.0, mask=0.0):
+    """Constant planes: flow values are in 1/8-resolution units (x8 on the page)."""
+    t = np.empty((5, h // 8, w // 8), f32)
+    for c, val in enumerate((u0, v0, u1, v1, mask)):
+        t[c] = val
+    return t
+
+
+def _frames(h, w, seed=5):
+    g = np.random.default_rng(seed)
+    return (g.integers(0, 256, (h, w, 4)).astype(np.uint8),
+            g.integers(0, 256, (h, w, 4)).astype(np.uint8))
+
+
+@pytest.mark.parametrize("mask,which", [(30.0, 0), (-30.0, 1)])
+def test_flow_out_identity_picks_one_frame(mask, which):
+    """Zero flow and a saturated mask: the output is one frame's bytes after the
+    page's byte -> /255 -> *255 -> truncation round trip; alpha 255."""
+    h, w = 24, 40
+    f0, f1 = _frames(h, w)
+    out = O.flow_out(_flow_map(h, w, mask=mask), f0, f1)
+    src = (f0, f1)[which]
+    np.testing.assert_array_equal(out[..., :3], _byte(_unit(src[..., :3])))
+    assert (out[..., 3] == 255).all()
+
+
+@pytest.mark.parametrize("shift", [1, 2, -3, 17])
+def test_flow_out_integer_shift_is_clamped_translation(shift):
+    """flow0.x = shift pixels (shift/8 at 1/8 resolution): out(x) = frame0(clamp(x + shift))."""
+    h, w = 16, 48
+    f0, f1 = _frames(h, w, seed=7)
+    out = O.flow_out(_flow_map(h, w, u0=shift / 8.0, mask=30.0), f0, f1)
+    xs = np.clip(np.arange(w) + shift, 0, w - 1)
+    np.testing.assert_array_equal(out[..., :3], _byte(_unit(f0[:, xs, :3])))
+
+
+def test_flow_out_half_pixel_shift_is_bilinear_mean():
+    """flow1.y = +0.5 px: out(y) = mix(frame1(y), frame1(y+1), 0.5) with mix(a,b,f) = a(1-f)+bf."""
+    h, w = 24, 16
+    f0, f1 = _frames(h, w, seed=9)
+    out = O.flow_out(_flow_map(h, w, v1=0.5 / 8.0, mask=-30.0), f0, f1)
+    a = _unit(f1[:, :, :3])
+    b = _unit(f1[np.clip(np.arange(h) + 1, 0, h - 1), :, :3])
+    ref = a * f32(0.5) + b * f32(0.5)
+    np.testing.assert_array_equal(out[..., :3], _byte(ref))
+
+
+@pytest.mark.parametrize("ca,cb", [(0, 255), (100, 37), (255, 254), (1, 2)])
+def test_flow_out_mask_zero_blends_halves(ca, cb):
+    """Mask logit 0: m = 1/(1+e^0) = 0.5 exactly; constant frames give a constant
+    v = (ca/255)*0.5 + (cb/255)*0.5 in every channel."""
+    h, w = 16, 16
+    f0 = np.full((h, w, 4), ca, np.uint8)
+    f1 = np.full((h, w, 4), cb, np.uint8)
+    out = O.flow_out(_flow_map(h, w, u0=0.3, v1=-0.7, mask=0.0), f0, f1)
+    v = f32(ca) / f32(255) * f32(0.5) + f32(cb) / f32(255) * f32(0.5)
+    assert (out[..., :3] == _byte(np.array([v], f32))[0]).all()
+
+
+def test_flow_out_sigmoid_and_upsample_positions():
+    """Frame 0 all 255, frame 1 all 0: the clamped pre-byte value is the mask
+    m = 1/(1+exp(-l)) of the x8-upsampled logit l.  With a logit plane that is
+    linear in x at 1/8 resolution, l at output x is the line at the align_corners=
+    false source position (x + 0.5)/8 - 0.5, clamped to the plane; m matches
+    float64 arithmetic to a few float32 ulps (the page's exp is binary32)."""
+    h, w = 8, 64
+    f0 = np.full((h, w, 4), 255, np.uint8)
+    f1 = np.zeros((h, w, 4), np.uint8)
+    t = _flow_map(h, w)
+    t[4] = (np.arange(w // 8, dtype=f32) * f32(2.0) - f32(7.0))[None, :]  # -7, -5, ..., 7
+    out, pre = O.flow_out(t, f0, f1, with_pre=True)
+    sx = (np.arange(w) + 0.5) / 8.0 - 0.5
+    l = np.clip(sx, 0, w // 8 - 1) * 2.0 - 7.0
+    m = 1.0 / (1.0 + np.exp(-l))
+    for c in range(3):
+        np.testing.assert_allclose(pre[c], np.broadcast_to(m, (h, w)), rtol=4e-7, atol=0)
+
+
+def test_flow_out_exp_wide_range():
+    """The binary32 exp inside the mask stays within 2 ulp of float64 over
+    [-80, 80] (pinned through the sigmoid of constant-frame blends)."""
+    h, w = 8, 8
+    f0 = np.full((h, w, 4), 255, np.uint8)
+    f1 = np.zeros((h, w, 4), np.uint8)
+    for l in np.linspace(-80.0, 80.0, 161).astype(f32):
+        _, pre = O.flow_out(_flow_map(h, w, mask=float(l)), f0, f1, with_pre=True)
+        ref = 1.0 / (1.0 + math.exp(-float(l)))
+        assert abs(float(pre[0, 0, 0]) - ref) <= 3 * np.spacing(f32(ref)) + 1e-45, (l, pre[0, 0, 0], ref)
+
+
+def test_flow_out_far_flow_clamps_to_border():
+    """A flow far outside the frame samples the clamped border pixel."""
+    h, w = 16, 16
+    f0, f1 = _frames(h, w, seed=11)
+    out = O.flow_out(_flow_map(h, w, u0=1e6, v0=-1e6, mask=30.0), f0, f1)
+    corner = _byte(_unit(f0[0, w - 1, :3]))
+    assert (out[..., :3] == corner).all()
