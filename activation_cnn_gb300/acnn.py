@@ -41,6 +41,7 @@ EXPORTS = (
     "acnn_status_string", "acnn_last_device_status", "acnn_set_wait_budget",
     "acnn_section_begin", "acnn_section_end", "acnn_section_launch", "acnn_section_destroy",
     "acnn_device_sm_count", "acnn_conv2d_fused_noalloc", "acnn_conv2d_plan",
+    "acnn_conv2d_fused_cat2",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # ACNN_NOALLOC_SCRATCH_BYTES in include/acnn.h
 
@@ -72,6 +73,8 @@ def lib() -> ctypes.CDLL:
         D = ctypes.POINTER(ConvDesc)
         L.acnn_conv2d_fused.argtypes = [D, _P, _P, _P, _P, _P, _I, _I, _P, _P, ctypes.c_size_t, _P]
         L.acnn_conv2d_out_hw.argtypes = [D, ctypes.POINTER(_I), ctypes.POINTER(_I)]
+        L.acnn_conv2d_fused_cat2.argtypes = [D, _P, _I, _P, _P, _P, _P, _P, _I, _I, _P, _P,
+                                             ctypes.c_size_t, _P]
         L.acnn_conv2d_workspace_size.argtypes = [D]
         L.acnn_conv2d_workspace_size.restype = ctypes.c_size_t
         L.acnn_conv2d_path.argtypes = [D]
@@ -235,6 +238,13 @@ def conv_desc(x: torch.Tensor, c_out: int, kh: int, kw: int, stride: int, pad: i
     return ConvDesc(n, h, w, c, c_out, kh, kw, stride, pad, layout, dtype_code(x.dtype))
 
 
+def acnn_conv2d_fused_cat2(desc, x_a, c_a, x_b, w, bias, alpha, residual, res_mode, act, y,
+                           workspace, ws_bytes, stream=None) -> int:
+    return lib().acnn_conv2d_fused_cat2(ctypes.byref(desc), _ptr(x_a), c_a, _ptr(x_b), _ptr(w),
+                                        _ptr(bias), _ptr(alpha), _ptr(residual), res_mode, act,
+                                        _ptr(y), _ptr(workspace), ws_bytes, _stream(stream))
+
+
 def conv_out_shape(desc: ConvDesc):
     st, oh, ow = acnn_conv2d_out_hw(desc)
     check(st, "acnn_conv2d_out_hw")
@@ -258,6 +268,24 @@ def conv2d_fused(x, w, bias=None, *, stride=1, pad=0, act=ACT_NONE, alpha=None, 
     st = acnn_conv2d_fused(d, x, w, bias, alpha, residual, res_mode, act, y, workspace,
                            ws_bytes if workspace is not None else 0, stream)
     check(st, "acnn_conv2d_fused")
+    return y
+
+
+def conv2d_fused_cat2(x_a, x_b, w, bias=None, *, stride=1, pad=0, act=ACT_NONE, alpha=None,
+                      residual=None, res_mode=RES_NONE, out=None, workspace=None, stream=None):
+    """conv2d_fused over torch.cat([x_a, x_b], -1) (NHWC) without building it."""
+    n, h, wd, c_a = x_a.shape
+    c_b = x_b.shape[3]
+    c_out, kh, kw, _ = w.shape
+    d = ConvDesc(n, h, wd, c_a + c_b, c_out, kh, kw, stride, pad, NHWC, dtype_code(x_a.dtype))
+    y = out if out is not None else torch.empty(conv_out_shape(d), dtype=x_a.dtype,
+                                                device=x_a.device)
+    ws_bytes = acnn_conv2d_workspace_size(d)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x_a.device)
+    st = acnn_conv2d_fused_cat2(d, x_a, c_a, x_b, w, bias, alpha, residual, res_mode, act, y,
+                                workspace, ws_bytes if workspace is not None else 0, stream)
+    check(st, "acnn_conv2d_fused_cat2")
     return y
 
 

@@ -316,6 +316,67 @@ int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w, con
     return launch_igemm_conv(a, s);
 }
 
+int acnn_conv2d_fused_cat2(const acnn_conv_desc* d, const void* x_a, int c_a, const void* x_b,
+                           const void* w, const float* bias, const float* alpha,
+                           const void* residual, int res_mode, int act, void* y, void* workspace,
+                           size_t ws_bytes, acnn_stream_t stream) {
+    int st = check_desc(d);
+    if (st != ACNN_OK) return st;
+    if (act < ACNN_ACT_NONE || act > ACNN_ACT_PRELU || res_mode < ACNN_RES_NONE ||
+        res_mode > ACNN_RES_ACT_THEN_ADD)
+        return ACNN_ERR_BAD_ENUM;
+    if (!x_a || !x_b || !w || !y) return ACNN_ERR_NULL_POINTER;
+    if (act == ACNN_ACT_PRELU && !alpha) return ACNN_ERR_NULL_POINTER;
+    if (res_mode != ACNN_RES_NONE && !residual) return ACNN_ERR_NULL_POINTER;
+    const int c_b = d->c_in - c_a;
+    if (d->layout != ACNN_NHWC || d->dtype == ACNN_F32 || c_a <= 0 || c_b <= 0 || c_a % 64 != 0 ||
+        c_b % 8 != 0)
+        return ACNN_ERR_UNSUPPORTED;
+    int oh, ow;
+    st = conv_out(d, &oh, &ow);
+    if (st != ACNN_OK) return st;
+    const Route r = route(d, oh, ow);
+    if (r.path != 1 && r.path != 2) return ACNN_ERR_UNSUPPORTED;
+    if (!aligned16(x_a) || !aligned16(x_b) || !aligned16(w) || !aligned16(y) ||
+        (bias && !aligned16(bias)) || (alpha && !aligned16(alpha)) ||
+        (residual && !aligned16(residual)) || (workspace && !aligned16(workspace)))
+        return ACNN_ERR_MISALIGNED;
+    const size_t es = elem_size(d->dtype);
+    const size_t px = (size_t)d->n * d->h * d->w;
+    const size_t xab = px * c_a * es, xbb = px * c_b * es;
+    const size_t wb = (size_t)d->c_out * d->kh * d->kw * d->c_in * es;
+    const size_t yb = (size_t)d->n * oh * ow * d->c_out * es;
+    if (overlaps(y, yb, x_a, xab) || overlaps(y, yb, x_b, xbb) || overlaps(y, yb, w, wb) ||
+        (residual && res_mode != ACNN_RES_NONE && overlaps(y, yb, residual, yb)) ||
+        (bias && overlaps(y, yb, bias, d->c_out * 4)) ||
+        (alpha && act == ACNN_ACT_PRELU && overlaps(y, yb, alpha, d->c_out * 4)))
+        return ACNN_ERR_ALIAS;
+    if (!workspace) ws_bytes = 0;
+    if (ws_bytes > 0 &&
+        (overlaps(workspace, ws_bytes, y, yb) || overlaps(workspace, ws_bytes, x_a, xab) ||
+         overlaps(workspace, ws_bytes, x_b, xbb) || overlaps(workspace, ws_bytes, w, wb) ||
+         (residual && res_mode != ACNN_RES_NONE && overlaps(workspace, ws_bytes, residual, yb))))
+        return ACNN_ERR_ALIAS;
+    ConvArgs a{};
+    a.d = *d;
+    a.oh = oh;
+    a.ow = ow;
+    a.x = x_a;
+    a.x2 = x_b;
+    a.c_split = c_a;
+    a.w = w;
+    a.bias = bias;
+    a.alpha = act == ACNN_ACT_PRELU ? alpha : nullptr;
+    a.residual = res_mode != ACNN_RES_NONE ? residual : nullptr;
+    a.res_mode = res_mode;
+    a.act = act;
+    a.y = y;
+    a.out_layout = ACNN_NHWC;
+    a.ws_part = ws_bytes > 0 ? workspace : nullptr;  // NHWC: no staging, all for split-K
+    a.ws_part_bytes = ws_bytes;
+    return launch_igemm_conv(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int acnn_pool2d(int kind, int n, int h, int w, int c, int k, int stride, int pad, int layout,
                 int dtype, const void* x, void* y, acnn_stream_t stream) {
     if (kind != ACNN_POOL_MAX && kind != ACNN_POOL_AVG) return ACNN_ERR_BAD_ENUM;

@@ -96,6 +96,10 @@ struct ConvArgs {
     int out_layout;  // layout y and residual are written/read in (may differ from d.layout)
     void* ws_part;         // split-K partial-sum workspace (256-byte aligned) or NULL
     size_t ws_part_bytes;  // its size: the planner uses at most this much
+    // channel concat folded into the conv: x holds input channels [0, c_split)
+    // and x2 channels [c_split, c_in), both NHWC (c_split = 0: x holds all)
+    const void* x2 = nullptr;
+    int c_split = 0;
 };
 
 // Tile width and K split of the tensor-core conv for a geometry, given the

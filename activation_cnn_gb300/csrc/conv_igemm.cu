@@ -84,6 +84,7 @@ struct Params {
     unsigned* cnt;
     int OW, OHW, S, P;
     int a_mode;       // 0: tiled A (1x1/s1/p0); 1: im2col A
+    int c_split;      // channels [c_split, C_in) come from the second A map (0: none)
     int out_layout;   // ACNN_NHWC or ACNN_NCHW for y and the residual
     int act, res_mode;
     const float* bias;
@@ -427,6 +428,7 @@ __device__ __forceinline__ void epi32_slot_mode(int act, int res_mode, float (&v
 template <int BN, int MS, int BK, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_conv_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_a2,
                       const __grid_constant__ CUtensorMap tmap_b, const Params p) {
     using C = Cfg<BN, MS, BK>;
     constexpr int TM = BM * MS;  // output pixels per tile
@@ -472,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tmap_a);
+        if (p.c_split) prefetch_tmap(&tmap_a2);
         prefetch_tmap(&tmap_b);
     }
     if (warp == 1) {
@@ -531,10 +534,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = full_bar(stage);
                     mbar_arrive_expect_tx(fb, stage_tx);
                     const uint32_t a_dst = smem_u32(sA + stage * C::kAB);
+                    // a folded concat: channel blocks from c_split on come from
+                    // the second source (c_split is a multiple of BK)
+                    const bool second = p.c_split && c0 >= p.c_split;
+                    const CUtensorMap* am = second ? &tmap_a2 : &tmap_a;
+                    const int ca = second ? c0 - p.c_split : c0;
                     if (p.a_mode == 0)
-                        tma_load_2d(a_dst, &tmap_a, fb, c0, m0);
+                        tma_load_2d(a_dst, am, fb, ca, m0);
                     else
-                        tma_load_im2col(a_dst, &tmap_a, fb, c0, wc, hc, img, (uint16_t)kx,
+                        tma_load_im2col(a_dst, am, fb, ca, wc, hc, img, (uint16_t)kx,
                                         (uint16_t)ky);
                     if (!bres)
                         tma_load_3d(smem_u32(sB + stage * C::kBBytes), &tmap_b, fb, c0, tap, n0);
@@ -1029,7 +1037,7 @@ bool load_encoders() {
 }
 
 struct Maps {
-    CUtensorMap a, b;
+    CUtensorMap a, a2, b;
 };
 
 template <int BN, int MS, int BK, typename T>
@@ -1084,7 +1092,7 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     const int grid = tiles < sm_count() ? tiles : sm_count();
     // split-K relies on every CTA being resident: grid <= #SMs and one CTA per
     // SM (the shared memory allows no second)
-    launch_pdl(kern, grid, kThreads, smem, s, m.a, m.b, prm);
+    launch_pdl(kern, grid, kThreads, smem, s, m.a, m.a2, m.b, prm);
     return cudaGetLastError() == cudaSuccess ? ACNN_OK : ACNN_ERR_CUDA;
 }
 
@@ -1192,28 +1200,38 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     const CUtensorMapSwizzle swz = bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
 
     alignas(64) Maps maps;
-    CUtensorMap& ta = maps.a;
     CUtensorMap& tb = maps.b;
-    CUresult r;
-    if (tiled) {
-        cuuint64_t dims[2] = {(cuuint64_t)d.c_in, (cuuint64_t)M};
-        cuuint64_t strides[1] = {(cuuint64_t)d.c_in * 2};
-        cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)(BM * plan.ms)};
-        cuuint32_t es[2] = {1, 1};
-        r = g_encode_tiled(&ta, dt, 2, const_cast<void*>(a.x), dims, strides, box, es,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
-        cuuint64_t dims[4] = {(cuuint64_t)d.c_in, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
-        cuuint64_t strides[3] = {(cuuint64_t)d.c_in * 2, (cuuint64_t)d.w * d.c_in * 2,
-                                 (cuuint64_t)d.h * d.w * d.c_in * 2};
+    // the A operand's map over an NHWC tensor of `ch` channels (a folded
+    // concat has two: channels [0, c_split) and [c_split, c_in))
+    auto encode_a = [&](CUtensorMap* ta, const void* ptr, int ch) {
+        if (tiled) {
+            cuuint64_t dims[2] = {(cuuint64_t)ch, (cuuint64_t)M};
+            cuuint64_t strides[1] = {(cuuint64_t)ch * 2};
+            cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)(BM * plan.ms)};
+            cuuint32_t es[2] = {1, 1};
+            return g_encode_tiled(ta, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        }
+        cuuint64_t dims[4] = {(cuuint64_t)ch, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
+        cuuint64_t strides[3] = {(cuuint64_t)ch * 2, (cuuint64_t)d.w * ch * 2,
+                                 (cuuint64_t)d.h * d.w * ch * 2};
         // window corners range over [-pad, dim - 1 + pad - (k - 1)] (W then H)
         int lower[2] = {-d.pad, -d.pad};
         int upper[2] = {d.pad - (d.kw - 1), d.pad - (d.kh - 1)};
         cuuint32_t es[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
-        r = g_encode_im2col(&ta, dt, 4, const_cast<void*>(a.x), dims, strides, lower, upper, bk,
-                            BM * plan.ms, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        return g_encode_im2col(ta, dt, 4, const_cast<void*>(ptr), dims, strides, lower, upper, bk,
+                               BM * plan.ms, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    };
+    const bool cat = a.x2 && a.c_split > 0;
+    if (cat && a.c_split % bk != 0) return ACNN_ERR_UNSUPPORTED;  // a k-block must not straddle
+    CUresult r = encode_a(&maps.a, a.x, cat ? a.c_split : d.c_in);
+    if (r == CUDA_SUCCESS) {
+        if (cat) r = encode_a(&maps.a2, a.x2, d.c_in - a.c_split);
+        else maps.a2 = maps.a;
     }
     if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
 
@@ -1252,6 +1270,7 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     prm.S = d.stride;
     prm.P = d.pad;
     prm.a_mode = tiled ? 0 : 1;
+    prm.c_split = cat ? a.c_split : 0;
     prm.out_layout = a.out_layout;
     prm.act = a.act;
     prm.res_mode = a.res_mode;

@@ -76,7 +76,7 @@ class Net:
     params: dict = field(default_factory=dict)   # name -> (cpu tensors) for reference checks
     graphs: list = field(default_factory=list)   # [(section, Section)]
     order: list = field(default_factory=list)    # section names in execution order
-    conv_inputs: dict = field(default_factory=dict)     # conv name -> input tensor name
+    conv_inputs: dict = field(default_factory=dict)     # conv name -> input tensor name(s)
     conv_residuals: dict = field(default_factory=dict)  # conv name -> residual tensor name
 
     # ------------------------------------------------------------ execution
@@ -176,6 +176,36 @@ class Builder:
             self.es + 4 * spec.c_out
         net.ops.append(Op("conv", self.section, fn, _conv_flops(n, spec), byts, spec.name, spec))
         return out or spec.name
+
+    def conv_cat(self, src_a, src_b, spec: ConvSpec):
+        """spec over the channel concat [src_a | src_b] (NHWC), the concat folded
+        into the conv's operand loads (acnn_conv2d_fused_cat2)."""
+        net = self.net
+        xa, xb = net.tensors[src_a], net.tensors[src_b]
+        ca = xa.shape[3]
+        w = G.conv_weight(self.seed, spec.name, spec.c_out, spec.c_in, spec.k, spec.k,
+                          net.layout, net.dtype)
+        b = G.conv_bias(self.seed, spec.name, spec.c_out)
+        al = G.prelu_alpha(self.seed, spec.name, spec.c_out) if spec.act == A.ACT_PRELU else None
+        net.params[spec.name] = (w, b, al)
+        wd, bd = w.to(self.device), b.to(self.device)
+        ald = al.to(self.device) if al is not None else None
+        y = self.buffer(spec.name, spec.c_out, spec.oh, spec.ow)
+        d = A.ConvDesc(net.batch, spec.h, spec.w, spec.c_in, spec.c_out, spec.k, spec.k,
+                       spec.stride, spec.pad, net.layout, net.dtype)
+        ws_bytes = A.acnn_conv2d_workspace_size(d)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device) if ws_bytes else None
+        net.tensors[spec.name + ".ws"] = ws
+        net.conv_inputs[spec.name] = (src_a, src_b)
+
+        def fn(stream):
+            A.check(A.acnn_conv2d_fused_cat2(d, xa, ca, xb, wd, bd, ald, None, A.RES_NONE,
+                                             spec.act, y, ws, ws_bytes, stream), spec.name)
+
+        byts = (xa.numel() + xb.numel() + w.numel() + y.numel()) * self.es + 4 * spec.c_out
+        net.ops.append(Op("conv", self.section, fn, _conv_flops(net.batch, spec), byts, spec.name,
+                          spec))
+        return spec.name
 
     def pool(self, src, dst, kind, k, s, p, c, h, w):
         net = self.net
@@ -317,7 +347,9 @@ def backbone_net(device="cuda", n=8, h=640, w=640) -> Net:
     Neck (top-down then bottom-up, every conv + SiLU): lateral 1x1 convs to 256
     on C3/C4/C5; F5 = lat5; F4 = conv3x3(cat[up2(F5), lat4]);
     F3 = conv3x3(cat[up2(F4), lat3]); N4 = conv3x3(cat[conv3x3/s2(F3), F4]);
-    N5 = conv3x3(cat[conv3x3/s2(N4), F5]).  Outputs F3, N4, N5.
+    N5 = conv3x3(cat[conv3x3/s2(N4), F5]).  Outputs F3, N4, N5.  Each concat is
+    folded into the conv that reads it (acnn_conv2d_fused_cat2: the conv's
+    operand loads take channels 0-255 from one map and 256-511 from the other).
     """
     seed = 1238
     net = Net("backbone", n, G.BF16, G.NHWC)
@@ -344,17 +376,13 @@ def backbone_net(device="cuda", n=8, h=640, w=640) -> Net:
     lat4 = b.conv(c4, ConvSpec("neck.lat4", ch4, 256, 1, 1, 0, S, h4, w4))
     f5 = b.conv(c5, ConvSpec("neck.lat5", ch5, 256, 1, 1, 0, S, h5, w5))
     up5 = b.resize(f5, "neck.up5", A.RESIZE_NEAREST, 256, h5, w5, h4, w4)
-    cat4 = b.concat(up5, lat4, "neck.cat4", 256, 256, h4, w4)
-    f4 = b.conv(cat4, ConvSpec("neck.fpn4", 512, 256, 3, 1, 1, S, h4, w4))
+    f4 = b.conv_cat(up5, lat4, ConvSpec("neck.fpn4", 512, 256, 3, 1, 1, S, h4, w4))
     up4 = b.resize(f4, "neck.up4", A.RESIZE_NEAREST, 256, h4, w4, h3, w3)
-    cat3 = b.concat(up4, lat3, "neck.cat3", 256, 256, h3, w3)
-    f3 = b.conv(cat3, ConvSpec("neck.fpn3", 512, 256, 3, 1, 1, S, h3, w3))
+    f3 = b.conv_cat(up4, lat3, ConvSpec("neck.fpn3", 512, 256, 3, 1, 1, S, h3, w3))
     d3 = b.conv(f3, ConvSpec("neck.down3", 256, 256, 3, 2, 1, S, h3, w3))
-    catn4 = b.concat(d3, f4, "neck.catn4", 256, 256, h4, w4)
-    n4 = b.conv(catn4, ConvSpec("neck.pan4", 512, 256, 3, 1, 1, S, h4, w4))
+    n4 = b.conv_cat(d3, f4, ConvSpec("neck.pan4", 512, 256, 3, 1, 1, S, h4, w4))
     d4 = b.conv(n4, ConvSpec("neck.down4", 256, 256, 3, 2, 1, S, h4, w4))
-    catn5 = b.concat(d4, f5, "neck.catn5", 256, 256, h5, w5)
-    n5 = b.conv(catn5, ConvSpec("neck.pan5", 512, 256, 3, 1, 1, S, h5, w5))
+    n5 = b.conv_cat(d4, f5, ConvSpec("neck.pan5", 512, 256, 3, 1, 1, S, h5, w5))
     net.outputs = [f3, n4, n5]
     return net
 

@@ -118,6 +118,22 @@ int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w,
                       int res_mode, int act, void* y, void* workspace, size_t ws_bytes,
                       acnn_stream_t stream);
 
+/* conv2d_fused over the channel concatenation [x_a | x_b] without
+ * materialising it (the concat of P1 CONCAT_SRC folded into the conv's
+ * operand loads): d describes the conv on the concatenated input (c_in =
+ * c_a + c_b channels); x_a is NHWC [n, h, w, c_a], x_b NHWC [n, h, w, c_b].
+ * The result equals acnn_concat followed by acnn_conv2d_fused bit for bit
+ * (the same operand values in the same k-block order).  Requires NHWC, fp16
+ * or bf16, c_a a positive multiple of 64, c_b a positive multiple of 8 and a
+ * geometry the tensor-core paths 1-2 take; else ACNN_ERR_UNSUPPORTED.  The
+ * workspace is optional (split-K partial sums only); other arguments and
+ * errors as acnn_conv2d_fused.
+ */
+int acnn_conv2d_fused_cat2(const acnn_conv_desc* d, const void* x_a, int c_a, const void* x_b,
+                           const void* w, const float* bias, const float* alpha,
+                           const void* residual, int res_mode, int act, void* y, void* workspace,
+                           size_t ws_bytes, acnn_stream_t stream);
+
 /* Output height and width of a conv with geometry d (host pointers). */
 int acnn_conv2d_out_hw(const acnn_conv_desc* d, int* oh, int* ow);
 

@@ -123,6 +123,16 @@ def test_companions_reject_before_launch(A):
     assert A.acnn_frame_flow_out(16, 16, None, 1, W, Y, Y + (1 << 20), 0) == 1
     assert A.acnn_frame_flow_out(16, 16, X, 1, W + 4, Y, Y + (1 << 20), 0) == 4
     assert A.acnn_frame_flow_out(16, 16, X, 1, W, Y, W + 512, 0) == 6
+    # folded concat conv: NHWC fp16/bf16 only, c_a a multiple of 64, c_b > 0
+    d = desc(A, c_in=128, c_out=64)
+    assert A.acnn_conv2d_fused_cat2(d, X, 64, R, W, None, None, None, 0, 1, Y, None, 0, 0) != 1
+    assert A.acnn_conv2d_fused_cat2(d, X, 32, R, W, None, None, None, 0, 1, Y, None, 0, 0) == 3
+    assert A.acnn_conv2d_fused_cat2(d, X, 128, R, W, None, None, None, 0, 1, Y, None, 0, 0) == 3
+    assert A.acnn_conv2d_fused_cat2(d, X, 64, None, W, None, None, None, 0, 1, Y, None, 0, 0) == 1
+    dn = desc(A, c_in=128, c_out=64, layout=1)
+    assert A.acnn_conv2d_fused_cat2(dn, X, 64, R, W, None, None, None, 0, 1, Y, None, 0, 0) == 3
+    assert A.acnn_conv2d_fused_cat2(d, X, 64, R, W, None, None, None, 0, 1, X + 64, None, 0,
+                                    0) == 6
 
 
 def test_wait_budget_knob(A):

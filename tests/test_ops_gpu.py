@@ -471,3 +471,39 @@ def test_flow_out_extremes_bitexact(flow, mask_std):
     torch.cuda.synchronize()
     ref = O.flow_out(t.numpy(), f0.numpy(), f1.numpy())
     assert_bitexact(y.cpu(), torch.from_numpy(ref), f"flow_out extremes {flow} {mask_std}")
+
+
+# ---------------------------------------------------------------- concat folded into the conv (NEXT-2)
+CAT_CASES = [
+    # name, n, h, w, c_a, c_b, cout, k, s, p, act, res
+    ("neck_3x3", 2, 20, 20, 256, 256, 256, 3, 1, 1, A.ACT_SILU, A.RES_NONE),
+    ("1x1_res", 2, 12, 17, 64, 128, 128, 1, 1, 0, A.ACT_RELU, A.RES_ADD_THEN_ACT),
+    ("3x3_s2_prelu", 1, 23, 19, 128, 64, 96, 3, 2, 1, A.ACT_PRELU, A.RES_NONE),
+    ("big_m", 4, 40, 40, 256, 256, 256, 3, 1, 1, A.ACT_SILU, A.RES_NONE),
+]
+
+
+@pytest.mark.parametrize("case", CAT_CASES, ids=[c[0] for c in CAT_CASES])
+def test_conv_cat2(case):
+    """conv over [x_a | x_b] matches the oracle's concat + conv, and equals the
+    library's own concat + conv2d_fused bit for bit."""
+    name, n, h, w, ca, cb, cout, k, s, p, act, res_mode = case
+    seed = 31
+    xa = G.tensor(seed, name + ".xa", (n, h, w, ca), "normal", dtype=G.BF16)
+    xb = G.tensor(seed, name + ".xb", (n, h, w, cb), "normal", dtype=G.BF16)
+    wt = G.conv_weight(seed, name, cout, ca + cb, k, k, G.NHWC, G.BF16)
+    b = G.conv_bias(seed, name, cout)
+    al = G.prelu_alpha(seed, name, cout)
+    oh, ow = (h + 2 * p - k) // s + 1, (w + 2 * p - k) // s + 1
+    r = G.tensor(seed, name + ".r", (n, oh, ow, cout), "normal", dtype=G.BF16) if res_mode else None
+    dev = lambda t: None if t is None else t.cuda()
+    y = A.conv2d_fused_cat2(dev(xa), dev(xb), dev(wt), dev(b), stride=s, pad=p, act=act,
+                            alpha=dev(al), residual=dev(r), res_mode=res_mode)
+    cat = A.concat(dev(xa), dev(xb))
+    y2 = A.conv2d_fused(cat, dev(wt), dev(b), stride=s, pad=p, act=act, alpha=dev(al),
+                        residual=dev(r), res_mode=res_mode)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2), name + ": folded concat differs from concat + conv"
+    ref = O.conv2d(O.concat(to64(xa), to64(xb)), to64(wt), to64(b), stride=s, pad=p, act=act,
+                   alpha=to64(al), residual=None if r is None else to64(r), res_mode=res_mode)
+    assert_parity(y, ref, torch.bfloat16, name)
