@@ -177,7 +177,7 @@ class Builder:
         net.ops.append(Op("conv", self.section, fn, _conv_flops(n, spec), byts, spec.name, spec))
         return out or spec.name
 
-    def conv_cat(self, src_a, src_b, spec: ConvSpec):
+    def conv_cat(self, src_a, src_b, spec: ConvSpec, residual=None):
         """spec over the channel concat [src_a | src_b] (NHWC), the concat folded
         into the conv's operand loads (acnn_conv2d_fused_cat2)."""
         net = self.net
@@ -197,12 +197,17 @@ class Builder:
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device) if ws_bytes else None
         net.tensors[spec.name + ".ws"] = ws
         net.conv_inputs[spec.name] = (src_a, src_b)
+        res = net.tensors[residual] if residual else None
+        res_mode = spec.res_mode if residual else A.RES_NONE
+        if residual:
+            net.conv_residuals[spec.name] = residual
 
         def fn(stream):
-            A.check(A.acnn_conv2d_fused_cat2(d, xa, ca, xb, wd, bd, ald, None, A.RES_NONE,
+            A.check(A.acnn_conv2d_fused_cat2(d, xa, ca, xb, wd, bd, ald, res, res_mode,
                                              spec.act, y, ws, ws_bytes, stream), spec.name)
 
-        byts = (xa.numel() + xb.numel() + w.numel() + y.numel()) * self.es + 4 * spec.c_out
+        byts = (xa.numel() + xb.numel() + w.numel() + y.numel() +
+                (y.numel() if res is not None else 0)) * self.es + 4 * spec.c_out
         net.ops.append(Op("conv", self.section, fn, _conv_flops(net.batch, spec), byts, spec.name,
                           spec))
         return spec.name
@@ -341,7 +346,24 @@ def block_net(device="cuda", variant="identity", n=4, h=80, w=80) -> Net:
 STAGES = [(3, 256, 1, "conv"), (4, 512, 2, "pool"), (6, 1024, 2, "pool"), (3, 2048, 2, "pool")]
 
 
-def backbone_net(device="cuda", n=8, h=640, w=640) -> Net:
+def csp_block(b: Builder, src_a, src_b, name, h, w, blocks=3, hidden=256):
+    """CSP block over [src_a | src_b] (512 channels) -> 256, as P1
+    RtDetrGpu::csp composes it: a = conv1(x); per RepVGG bottleneck
+    a = SiLU(conv3x3(a) + conv1x1(a)); out = a + conv2(x).  conv1 and conv2 are
+    1x1 + SiLU reading the concat folded into their operand loads; the RepVGG
+    sum is the 3x3 conv's add-then-activate residual (the 1x1's output, no
+    activation); the final add is conv2's activate-then-add residual."""
+    S = A.ACT_SILU
+    a = b.conv_cat(src_a, src_b, ConvSpec(f"{name}.conv1", 512, hidden, 1, 1, 0, S, h, w))
+    for i in range(blocks):
+        q = b.conv(a, ConvSpec(f"{name}.rep{i}.conv1x1", hidden, hidden, 1, 1, 0, A.ACT_NONE, h, w))
+        a = b.conv(a, ConvSpec(f"{name}.rep{i}.conv3x3", hidden, hidden, 3, 1, 1, S, h, w,
+                               res_mode=A.RES_ADD_THEN_ACT), residual=q)
+    return b.conv_cat(src_a, src_b, ConvSpec(name, 512, 256, 1, 1, 0, S, h, w,
+                                             res_mode=A.RES_ACT_THEN_ADD), residual=a)
+
+
+def backbone_net(device="cuda", n=8, h=640, w=640, neck="fusion") -> Net:
     """ResNet-D-50 backbone + neck, NHWC bf16, N x 640 x 640 x 3, x ~ U(0, 1).
 
     Neck (top-down then bottom-up, every conv + SiLU): lateral 1x1 convs to 256
@@ -350,9 +372,11 @@ def backbone_net(device="cuda", n=8, h=640, w=640) -> Net:
     N5 = conv3x3(cat[conv3x3/s2(N4), F5]).  Outputs F3, N4, N5.  Each concat is
     folded into the conv that reads it (acnn_conv2d_fused_cat2: the conv's
     operand loads take channels 0-255 from one map and 256-511 from the other).
+    neck="csp": each of the four 3x3 fusion convs becomes a CSP block with three
+    RepVGG bottlenecks (csp_block), as P1's neck has them.
     """
     seed = 1238
-    net = Net("backbone", n, G.BF16, G.NHWC)
+    net = Net("backbone" if neck == "fusion" else "backbone_csp", n, G.BF16, G.NHWC)
     b = Builder(net, seed, device)
     x = G.tensor(seed, "x", (n, h, w, 3), "uniform", 0.0, 1.0, dtype=G.BF16)
     net.tensors["x"] = x.to(device)
@@ -375,14 +399,19 @@ def backbone_net(device="cuda", n=8, h=640, w=640) -> Net:
     lat3 = b.conv(c3, ConvSpec("neck.lat3", ch3, 256, 1, 1, 0, S, h3, w3))
     lat4 = b.conv(c4, ConvSpec("neck.lat4", ch4, 256, 1, 1, 0, S, h4, w4))
     f5 = b.conv(c5, ConvSpec("neck.lat5", ch5, 256, 1, 1, 0, S, h5, w5))
+    def fuse(src_a, src_b, name, hh, ww):
+        if neck == "csp":
+            return csp_block(b, src_a, src_b, name, hh, ww)
+        return b.conv_cat(src_a, src_b, ConvSpec(name, 512, 256, 3, 1, 1, S, hh, ww))
+
     up5 = b.resize(f5, "neck.up5", A.RESIZE_NEAREST, 256, h5, w5, h4, w4)
-    f4 = b.conv_cat(up5, lat4, ConvSpec("neck.fpn4", 512, 256, 3, 1, 1, S, h4, w4))
+    f4 = fuse(up5, lat4, "neck.fpn4", h4, w4)
     up4 = b.resize(f4, "neck.up4", A.RESIZE_NEAREST, 256, h4, w4, h3, w3)
-    f3 = b.conv_cat(up4, lat3, ConvSpec("neck.fpn3", 512, 256, 3, 1, 1, S, h3, w3))
+    f3 = fuse(up4, lat3, "neck.fpn3", h3, w3)
     d3 = b.conv(f3, ConvSpec("neck.down3", 256, 256, 3, 2, 1, S, h3, w3))
-    n4 = b.conv_cat(d3, f4, ConvSpec("neck.pan4", 512, 256, 3, 1, 1, S, h4, w4))
+    n4 = fuse(d3, f4, "neck.pan4", h4, w4)
     d4 = b.conv(n4, ConvSpec("neck.down4", 256, 256, 3, 2, 1, S, h4, w4))
-    n5 = b.conv_cat(d4, f5, ConvSpec("neck.pan5", 512, 256, 3, 1, 1, S, h5, w5))
+    n5 = fuse(d4, f5, "neck.pan5", h5, w5)
     net.outputs = [f3, n4, n5]
     return net
 
@@ -464,4 +493,5 @@ WORKLOADS = {
     "frame": frame_net,
     "frame_out": lambda device="cuda": frame_net(device, flow_out=True),
     "backbone": backbone_net,
+    "backbone_csp": lambda device="cuda": backbone_net(device, neck="csp"),
 }

@@ -129,6 +129,8 @@ def build_net(name, device, batch=None):
     from activation_cnn_gb300 import network as N
     if name == "backbone":
         return N.backbone_net(device, n=batch or 8)
+    if name == "backbone_csp":
+        return N.backbone_net(device, n=batch or 8, neck="csp")
     if name == "block":
         return N.block_net(device, "identity", n=batch or 4)
     if name == "block_down":
@@ -145,6 +147,9 @@ def workload_config(name, net, world):
             "graphs": "one CUDA graph per section: " + ",".join(net.order)}
     if name == "backbone":
         base.update({"image": "640x640x3", "model": "ResNet-D-50 (3/4/6/3) + top-down/bottom-up neck"})
+    if name == "backbone_csp":
+        base.update({"image": "640x640x3",
+                     "model": "ResNet-D-50 (3/4/6/3) + neck with CSP/RepVGG fusion blocks"})
     return base
 
 
@@ -434,7 +439,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="backbone",
-                    choices=["backbone", "block", "block_down", "stem", "conv1", "frame", "frame_out"])
+                    choices=["backbone", "backbone_csp", "block", "block_down", "stem", "conv1", "frame",
+                             "frame_out"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--layers", action="store_true", help="add per-conv timings")

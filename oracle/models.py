@@ -113,7 +113,21 @@ def block(x, variant):
 
 
 # ------------------------------------------------------------------ backbone + neck
-def backbone(x):
+def csp(r: Runner, x, name, blocks=3, hidden=256):
+    """P1 RtDetrGpu::csp: a = conv1(x) (1x1 + SiLU); per RepVGG bottleneck
+    a = SiLU(conv3x3(a) + conv1x1(a)) (branches without activation); out =
+    a + conv2(x) (conv2 1x1 + SiLU, plain add).  Each conv's output is stored
+    (bf16) before the next op reads it."""
+    S = O.ACT_SILU
+    a = r.conv(x, f"{name}.conv1", hidden, 1, 1, 0, S)
+    for i in range(blocks):
+        q = r.conv(a, f"{name}.rep{i}.conv1x1", hidden, 1, 1, 0, O.ACT_NONE)
+        a = r.conv(a, f"{name}.rep{i}.conv3x3", hidden, 3, 1, 1, S, residual=q,
+                   res_mode=O.RES_ADD_THEN_ACT)
+    return r.conv(x, name, 256, 1, 1, 0, S, residual=a, res_mode=O.RES_ACT_THEN_ADD)
+
+
+def backbone(x, neck="fusion"):
     """ResNet-D-50 (3/4/6/3 blocks, widths 256/512/1024/2048; stage 1 shortcut a
     1x1 conv, later stages avgpool + 1x1; stride on the first 3x3 of stages 2-4)
     and the neck: SiLU lateral 1x1s to 256; top-down nearest-2x + concat
@@ -133,12 +147,18 @@ def backbone(x):
     lat3 = r.conv(c3, "neck.lat3", 256, 1, 1, 0, S)
     lat4 = r.conv(c4, "neck.lat4", 256, 1, 1, 0, S)
     f5 = r.conv(c5, "neck.lat5", 256, 1, 1, 0, S)
-    f4 = r.conv(r.cat(r.up2(f5), lat4), "neck.fpn4", 256, 3, 1, 1, S)
-    f3 = r.conv(r.cat(r.up2(f4), lat3), "neck.fpn3", 256, 3, 1, 1, S)
+
+    def fuse(x, name):
+        if neck == "csp":
+            return csp(r, x, name)
+        return r.conv(x, name, 256, 3, 1, 1, S)
+
+    f4 = fuse(r.cat(r.up2(f5), lat4), "neck.fpn4")
+    f3 = fuse(r.cat(r.up2(f4), lat3), "neck.fpn3")
     d3 = r.conv(f3, "neck.down3", 256, 3, 2, 1, S)
-    n4 = r.conv(r.cat(d3, f4), "neck.pan4", 256, 3, 1, 1, S)
+    n4 = fuse(r.cat(d3, f4), "neck.pan4")
     d4 = r.conv(n4, "neck.down4", 256, 3, 2, 1, S)
-    n5 = r.conv(r.cat(d4, f5), "neck.pan5", 256, 3, 1, 1, S)
+    n5 = fuse(r.cat(d4, f5), "neck.pan5")
     return f3, n4, n5
 
 

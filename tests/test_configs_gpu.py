@@ -124,6 +124,15 @@ def test_backbone_reduced_end_to_end():
     assert_maps(outs, refs, torch.bfloat16)
 
 
+def test_backbone_csp_reduced_end_to_end():
+    """The neck with P1's CSP/RepVGG blocks in place of the single fusion convs."""
+    net = N.backbone_net(n=1, h=128, w=160, neck="csp")
+    outs = run_graph(net)
+    refs = M.backbone(to64(net.inputs["x"]), neck="csp")
+    assert [tuple(o.shape) for o in outs] == [(1, 16, 20, 256), (1, 8, 10, 256), (1, 4, 5, 256)]
+    assert_maps(outs, refs, torch.bfloat16)
+
+
 # ------------------------------------------------------------------ full size, per layer
 def _sample_pixels(n, oh, ow, k, rng):
     pts = {(0, 0, 0), (n - 1, oh - 1, ow - 1), (0, oh - 1, 0), (n - 1, 0, ow - 1)}
@@ -186,6 +195,13 @@ def test_backbone_full_size_layers():
     ap = T["s2.b0.pool"]
     assert_parity(ap, O.pool2d(to64(T["s1.b2.conv3"]), O.AVG, 2, 2, 0), torch.bfloat16, "avgpool")
     assert [tuple(o.shape) for o in outs] == [(8, 80, 80, 256), (8, 40, 40, 256), (8, 20, 20, 256)]
+
+
+def test_backbone_csp_full_size_layers():
+    """The 92 convs of the CSP-neck variant at 8x640x640, teacher-forced, sampled pixels."""
+    net = N.backbone_net(neck="csp")
+    run_graph(net)
+    assert check_layers(net, samples=24) == 92
 
 
 def test_frame_full_size_layers():
