@@ -469,8 +469,9 @@ typedef struct {
     const float* t;
     const uint8_t* f0;
     const uint8_t* f1;
-    float* pre;   /* [3][H][W] clamped R, G, B in [0, 1] before the byte scale */
-    uint8_t* out; /* [H][W][4] */
+    const float* res; /* optional refine residual [3][H/4][W/4] (B, G, R) */
+    float* pre;       /* [3][H][W] clamped R, G, B in [0, 1] before the byte scale */
+    uint8_t* out;     /* [H][W][4] */
 } flow_args;
 
 static float flow_up(const flow_args* a, int c, float sx, float sy)
@@ -521,11 +522,30 @@ static void flow_row(const void* p, int y)
         flow_warp(a, a->f0, (float)x + u0, (float)y + v0, w0);
         flow_warp(a, a->f1, (float)x + u1, (float)y + v1, w1);
         const float om = 1.0f - m;
+        /* refine residual: its x4 bilinear upsample (align_corners=false,
+         * clamped taps), added before the clamp */
+        float rv[3] = {0.0f, 0.0f, 0.0f};
+        if (a->res) {
+            const int RH = a->H / 4, RW = a->W / 4;
+            const float rx = ((float)x + 0.5f) * 0.25f - 0.5f;
+            const float ry = ((float)y + 0.5f) * 0.25f - 0.5f;
+            const float fx0 = floorf(rx), fy0 = floorf(ry);
+            const float fx = rx - fx0, fy = ry - fy0;
+            const int xa = clampi((int)fx0, 0, RW - 1), xb = clampi((int)fx0 + 1, 0, RW - 1);
+            const int ya = clampi((int)fy0, 0, RH - 1), yb = clampi((int)fy0 + 1, 0, RH - 1);
+            for (int k = 0; k < 3; ++k) {
+                const float* pl = a->res + (size_t)k * RH * RW;
+                const float top = flow_mix(pl[(size_t)ya * RW + xa], pl[(size_t)ya * RW + xb], fx);
+                const float bot = flow_mix(pl[(size_t)yb * RW + xa], pl[(size_t)yb * RW + xb], fx);
+                rv[k] = flow_mix(top, bot, fy);
+            }
+        }
         uint8_t* o = a->out + ((size_t)y * a->W + x) * 4;
         for (int k = 0; k < 3; ++k) { /* k: B, G, R -> byte 2 - k */
             const float u = w0[k] * m;
             const float v = w1[k] * om;
             float c = u + v;
+            if (a->res) c = c + rv[k];
             c = c < 0.0f ? 0.0f : (c > 1.0f ? 1.0f : c);
             if (a->pre) a->pre[(size_t)(2 - k) * a->H * a->W + (size_t)y * a->W + x] = c;
             o[2 - k] = (uint8_t)(unsigned)(c * 255.0f);
@@ -535,14 +555,142 @@ static void flow_row(const void* p, int y)
 }
 
 /* H, W multiples of 8; tmp8 [5][H/8][W/8] float; frames [H][W][4] bytes;
- * out [H][W][4] bytes (R, G, B, 255); pre (optional) [3][H][W] the clamped
- * R, G, B values before the byte scale. */
+ * res (optional) the refine residual [3][H/4][W/4] float (B, G, R); out
+ * [H][W][4] bytes (R, G, B, 255); pre (optional) [3][H][W] the clamped R, G, B
+ * values before the byte scale. */
 int oracle_flow_out(int H, int W, const float* tmp8, const uint8_t* rgba0, const uint8_t* rgba1,
-                    uint8_t* out, float* pre, int nthreads)
+                    const float* res, uint8_t* out, float* pre, int nthreads)
 {
     if (H <= 0 || W <= 0 || H % 8 || W % 8) return -1;
-    flow_args a = {H, W, tmp8, rgba0, rgba1, pre, out};
+    flow_args a = {H, W, tmp8, rgba0, rgba1, res, pre, out};
     for_rows(flow_row, &a, H, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* t-factored frame stack (NEXT-3), P3 createRT's tfact path:                */
+/*   FiLM (wgslFilm + filmParams): per timestep t a tiny MLP gives 2C values  */
+/*   s = b2 + W2 relu(w0 t + b0); x' = x * (1 + s[c]) + s[C + c].            */
+/*   Refine prep (wgslRefinePrep): 11 planes at (H/4, W/4), each the mean     */
+/*   over the centre 2x2 of the 4x4 block (X = 4 hx + {1, 2}, Y likewise) of  */
+/*   warped frame 0 (B, G, R), warped frame 1 (B, G, R), the sigmoid mask,    */
+/*   and the four x8 flows scaled by 0.25 / 20.                               */
+/*   Refine out (wgslRefineOut): conv3x3 C -> 3 with replicate (clamped)      */
+/*   padding, bias, then 2 sigmoid(acc) - 1.                                  */
+/* These values are not truncated to bytes, so they are computed in double.   */
+/* ------------------------------------------------------------------------ */
+int oracle_film(int C, int N, const double* x, double t, const double* w0, const double* b0,
+                int HN, const double* w2, const double* b2, double* y)
+{
+    double* h = (double*)malloc(sizeof(double) * (size_t)HN);
+    double* s = (double*)malloc(sizeof(double) * (size_t)2 * C);
+    for (int j = 0; j < HN; ++j) {
+        const double v = w0[j] * t + b0[j];
+        h[j] = v > 0.0 ? v : 0.0;
+    }
+    for (int k = 0; k < 2 * C; ++k) {
+        double acc = b2[k];
+        for (int j = 0; j < HN; ++j) acc += w2[(size_t)k * HN + j] * h[j];
+        s[k] = acc;
+    }
+    for (int c = 0; c < C; ++c)
+        for (int i = 0; i < N; ++i)
+            y[(size_t)c * N + i] = x[(size_t)c * N + i] * (1.0 + s[c]) + s[C + c];
+    free(h);
+    free(s);
+    return 0;
+}
+
+static double rp_up(const double* t, int TH, int TW, int c, double sx, double sy)
+{
+    const double x0 = floor(sx), y0 = floor(sy), fx = sx - x0, fy = sy - y0;
+    const double* pl = t + (size_t)c * TH * TW;
+    const int xa = clampi((int)x0, 0, TW - 1), xb = clampi((int)x0 + 1, 0, TW - 1);
+    const int ya = clampi((int)y0, 0, TH - 1), yb = clampi((int)y0 + 1, 0, TH - 1);
+    const double top = pl[(size_t)ya * TW + xa] * (1 - fx) + pl[(size_t)ya * TW + xb] * fx;
+    const double bot = pl[(size_t)yb * TW + xa] * (1 - fx) + pl[(size_t)yb * TW + xb] * fx;
+    return top * (1 - fy) + bot * fy;
+}
+
+static void rp_warp(const uint8_t* f, int H, int W, double px, double py, double bgr[3])
+{
+    double x0 = floor(px), y0 = floor(py);
+    const double fx = px - x0, fy = py - y0;
+    if (x0 < -1) x0 = -1;
+    if (x0 > W) x0 = W;
+    if (y0 < -1) y0 = -1;
+    if (y0 > H) y0 = H;
+    const int xa = clampi((int)x0, 0, W - 1), xb = clampi((int)x0 + 1, 0, W - 1);
+    const int ya = clampi((int)y0, 0, H - 1), yb = clampi((int)y0 + 1, 0, H - 1);
+    for (int k = 0; k < 3; ++k) {
+        const int byte = 2 - k;
+        const double p00 = f[((size_t)ya * W + xa) * 4 + byte] / 255.0;
+        const double p01 = f[((size_t)ya * W + xb) * 4 + byte] / 255.0;
+        const double p10 = f[((size_t)yb * W + xa) * 4 + byte] / 255.0;
+        const double p11 = f[((size_t)yb * W + xb) * 4 + byte] / 255.0;
+        const double top = p00 * (1 - fx) + p01 * fx, bot = p10 * (1 - fx) + p11 * fx;
+        bgr[k] = top * (1 - fy) + bot * fy;
+    }
+}
+
+/* tmp8 [5][H/8][W/8]; frames [H][W][4]; y [11][H/4][W/4]. */
+int oracle_refine_prep(int H, int W, const double* tmp8, const uint8_t* rgba0,
+                       const uint8_t* rgba1, double* y)
+{
+    if (H <= 0 || W <= 0 || H % 8 || W % 8) return -1;
+    const int TH = H / 8, TW = W / 8, QH = H / 4, QW = W / 4;
+    const size_t P = (size_t)QH * QW;
+    for (int hy = 0; hy < QH; ++hy)
+        for (int hx = 0; hx < QW; ++hx) {
+            double acc[11] = {0};
+            for (int sy = 1; sy <= 2; ++sy)
+                for (int sxp = 1; sxp <= 2; ++sxp) {
+                    const int X = 4 * hx + sxp, Y = 4 * hy + sy;
+                    const double gx = (X + 0.5) / 8.0 - 0.5, gy = (Y + 0.5) / 8.0 - 0.5;
+                    const double u0 = rp_up(tmp8, TH, TW, 0, gx, gy) * 8.0;
+                    const double v0 = rp_up(tmp8, TH, TW, 1, gx, gy) * 8.0;
+                    const double u1 = rp_up(tmp8, TH, TW, 2, gx, gy) * 8.0;
+                    const double v1 = rp_up(tmp8, TH, TW, 3, gx, gy) * 8.0;
+                    const double m = 1.0 / (1.0 + exp(-rp_up(tmp8, TH, TW, 4, gx, gy)));
+                    double w0[3], w1[3];
+                    rp_warp(rgba0, H, W, X + u0, Y + v0, w0);
+                    rp_warp(rgba1, H, W, X + u1, Y + v1, w1);
+                    for (int k = 0; k < 3; ++k) {
+                        acc[k] += w0[k];
+                        acc[3 + k] += w1[k];
+                    }
+                    acc[6] += m;
+                    acc[7] += u0;
+                    acc[8] += v0;
+                    acc[9] += u1;
+                    acc[10] += v1;
+                }
+            const size_t o = (size_t)hy * QW + hx;
+            for (int k = 0; k < 7; ++k) y[k * P + o] = acc[k] * 0.25;
+            for (int k = 7; k < 11; ++k) y[k * P + o] = acc[k] * (0.25 * (0.25 / 20.0));
+        }
+    return 0;
+}
+
+/* x [C][HH][HW]; w [3][C][3][3]; b [3]; y [3][HH][HW]. */
+int oracle_refine_out(int C, int HH, int HW, const double* x, const double* w, const double* b,
+                      double* y)
+{
+    for (int co = 0; co < 3; ++co)
+        for (int oy = 0; oy < HH; ++oy)
+            for (int ox = 0; ox < HW; ++ox) {
+                double acc = b[co];
+                for (int ci = 0; ci < C; ++ci)
+                    for (int ky = 0; ky < 3; ++ky) {
+                        const int iy = clampi(oy + ky - 1, 0, HH - 1);
+                        for (int kx = 0; kx < 3; ++kx) {
+                            const int ix = clampi(ox + kx - 1, 0, HW - 1);
+                            acc += x[((size_t)ci * HH + iy) * HW + ix] *
+                                   w[(((size_t)co * C + ci) * 3 + ky) * 3 + kx];
+                        }
+                    }
+                y[((size_t)co * HH + oy) * HW + ox] = 2.0 / (1.0 + exp(-acc)) - 1.0;
+            }
     return 0;
 }
 

@@ -69,7 +69,10 @@ def _load():
     lib.oracle_prep_quarter.argtypes = [i, i, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_double, d]
     lib.oracle_flow_out.argtypes = [i, i, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                                    ctypes.c_void_p, ctypes.c_void_p, i]
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, i]
+    lib.oracle_film.argtypes = [i, i, d, ctypes.c_double, d, d, i, d, d, d]
+    lib.oracle_refine_prep.argtypes = [i, i, d, ctypes.c_void_p, ctypes.c_void_p, d]
+    lib.oracle_refine_out.argtypes = [i, i, i, d, d, d, d]
     lib.oracle_round_storage.argtypes = [d, ctypes.c_size_t, i]
     lib.oracle_round_value.argtypes = [ctypes.c_double, i]
     lib.oracle_round_value.restype = ctypes.c_double
@@ -221,10 +224,12 @@ def prep_quarter(rgba0, rgba1, t):
     return y
 
 
-def flow_out(tmp8, rgba0, rgba1, *, with_pre=False, threads=None):
+def flow_out(tmp8, rgba0, rgba1, *, res=None, with_pre=False, threads=None):
     """P3 wgslFlowOut: [5, H/8, W/8] flow/mask (float32) + two [H, W, 4] uint8
     frames -> [H, W, 4] uint8 (and, with_pre, the clamped R, G, B [3, H, W]
-    float32 before the byte scale).  Computed in binary32, as on the page."""
+    float32 before the byte scale).  res: the t-factored stack's refine
+    residual [3, H/4, W/4] (B, G, R, float32), upsampled x4 and added before
+    the clamp.  Computed in binary32, as on the page."""
     lib = _load()
     a = np.ascontiguousarray(rgba0, dtype=np.uint8)
     b = np.ascontiguousarray(rgba1, dtype=np.uint8)
@@ -234,10 +239,56 @@ def flow_out(tmp8, rgba0, rgba1, *, with_pre=False, threads=None):
     assert t.shape == (5, h // 8, w // 8)
     out = np.empty((h, w, 4), np.uint8)
     pre = np.empty((3, h, w), np.float32) if with_pre else None
-    rc = lib.oracle_flow_out(h, w, t.ctypes.data, a.ctypes.data, b.ctypes.data, out.ctypes.data,
+    r = None
+    if res is not None:
+        r = np.ascontiguousarray(res, dtype=np.float32)
+        assert r.shape == (3, h // 4, w // 4)
+    rc = lib.oracle_flow_out(h, w, t.ctypes.data, a.ctypes.data, b.ctypes.data,
+                             r.ctypes.data if r is not None else None, out.ctypes.data,
                              pre.ctypes.data if with_pre else None, threads or nthreads())
     assert rc == 0
     return (out, pre) if with_pre else out
+
+
+def film(x, t, w0, b0, w2, b2):
+    """P3 wgslFilm with filmParams: x [C, N] (any trailing shape) -> x * (1 + s[c])
+    + s[C + c], s = b2 + W2 relu(w0 t + b0) (W2 [2C, HN])."""
+    lib = _load()
+    x = _f64(x)
+    c = x.shape[0]
+    n = x.size // c
+    w0, b0, w2, b2 = _f64(w0).ravel(), _f64(b0).ravel(), _f64(w2), _f64(b2).ravel()
+    hn = w0.size
+    assert w2.shape == (2 * c, hn) and b2.size == 2 * c
+    y = np.empty_like(x)
+    assert lib.oracle_film(c, n, _ptr(x), float(t), _ptr(w0), _ptr(b0), hn, _ptr(w2), _ptr(b2),
+                           _ptr(y)) == 0
+    return y
+
+
+def refine_prep(tmp8, rgba0, rgba1):
+    """P3 wgslRefinePrep: [5, H/8, W/8] + two [H, W, 4] frames -> [11, H/4, W/4]."""
+    lib = _load()
+    a = np.ascontiguousarray(rgba0, dtype=np.uint8)
+    b = np.ascontiguousarray(rgba1, dtype=np.uint8)
+    h, w, _ = a.shape
+    t = _f64(tmp8)
+    assert t.shape == (5, h // 8, w // 8)
+    y = np.empty((11, h // 4, w // 4), np.float64)
+    assert lib.oracle_refine_prep(h, w, _ptr(t), a.ctypes.data, b.ctypes.data, _ptr(y)) == 0
+    return y
+
+
+def refine_out(x, w, b):
+    """P3 wgslRefineOut: x [C, HH, HW], w [3, C, 3, 3], b [3] -> 2 sigmoid(conv) - 1
+    with replicate padding, [3, HH, HW]."""
+    lib = _load()
+    x, w, b = _f64(x), _f64(w), _f64(b).ravel()
+    c, hh, hw = x.shape
+    assert w.shape == (3, c, 3, 3)
+    y = np.empty((3, hh, hw), np.float64)
+    assert lib.oracle_refine_out(c, hh, hw, _ptr(x), _ptr(w), _ptr(b), _ptr(y)) == 0
+    return y
 
 
 def round_storage(v, dtype):

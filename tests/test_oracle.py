@@ -559,3 +559,86 @@ def test_flow_out_far_flow_clamps_to_border():
     out = O.flow_out(_flow_map(h, w, u0=1e6, v0=-1e6, mask=30.0), f0, f1)
     corner = _byte(_unit(f0[0, w - 1, :3]))
     assert (out[..., :3] == corner).all()
+
+
+# --------------------------------------------------------------------------- t-factored stack (NEXT-3)
+# P3 "@framecast/rt 1.0.0 -- package/rt.js": wgslFilm + filmParams (FiLM of the
+# trunk features by a per-timestep MLP), wgslRefinePrep, wgslRefineOut, and the
+# refine residual folded into the flow-out stage.
+def test_film_matches_torch_mlp():
+    """s = Linear2(relu(Linear1(t))) is torch's linear + relu; FiLM is x*(1+s_c)+s_{C+c}."""
+    c, hn = 6, 5
+    x = rng.standard_normal((c, 4, 7))
+    w0, b0 = rng.standard_normal(hn), rng.standard_normal(hn)
+    w2, b2 = rng.standard_normal((2 * c, hn)), rng.standard_normal(2 * c)
+    t = 0.37
+    h = F.relu(F.linear(torch.tensor([[t]], dtype=torch.float64), torch.from_numpy(w0[:, None]),
+                        torch.from_numpy(b0)))
+    s = F.linear(h, torch.from_numpy(w2), torch.from_numpy(b2))[0].numpy()
+    ref = x * (1.0 + s[:c, None, None]) + s[c:, None, None]
+    np.testing.assert_allclose(O.film(x, t, w0, b0, w2, b2), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_film_dead_hidden_units_and_identity():
+    """All hidden units negative (relu = 0): s = b2; b2 = 0 then gives the identity."""
+    c = 3
+    x = rng.standard_normal((c, 10))
+    w0, b0 = np.ones(4), -np.ones(4) * 5.0  # w0 t + b0 < 0 for t < 5
+    w2 = rng.standard_normal((2 * c, 4))
+    np.testing.assert_array_equal(O.film(x, 1.0, w0, b0, w2, np.zeros(2 * c)), x)
+    b2 = np.array([0.5, -1.0, 0.0, 2.0, 0.25, -3.0])
+    np.testing.assert_allclose(O.film(x, 1.0, w0, b0, w2, b2),
+                               x * (1 + b2[:c, None]) + b2[c:, None], rtol=1e-15, atol=0)
+
+
+def test_refine_prep_zero_flow_is_quarter_bilinear():
+    """With zero flow the warped planes are the frames, and the mean over the centre
+    2x2 of each 4x4 block is torch's bilinear 1/4 resize (align_corners=False)."""
+    h, w = 16, 24
+    f0, f1 = _frames(h, w, seed=13)
+    t = np.zeros((5, h // 8, w // 8))
+    t[4] = 0.7
+    y = O.refine_prep(t, f0, f1)
+    for f, off in ((f0, 0), (f1, 3)):
+        planes = np.stack([f[..., 2], f[..., 1], f[..., 0]]).astype(np.float64) / 255.0
+        ref = F.interpolate(torch.from_numpy(planes[None]), size=(h // 4, w // 4),
+                            mode="bilinear", align_corners=False).numpy()[0]
+        np.testing.assert_allclose(y[off:off + 3], ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y[6], 1.0 / (1.0 + math.exp(-0.7)), rtol=1e-14)
+    np.testing.assert_array_equal(y[7:], 0.0)
+
+
+def test_refine_prep_constant_flow_channels():
+    """A constant flow value u at 1/8 resolution is 8u pixels; the flow planes hold
+    the mean flow times 0.25/20 = u/10."""
+    h, w = 16, 16
+    f0, f1 = _frames(h, w, seed=15)
+    t = np.zeros((5, h // 8, w // 8))
+    t[0], t[1], t[2], t[3] = 0.5, -0.25, 1.5, 0.125
+    y = O.refine_prep(t, f0, f1)
+    for k, u in enumerate((0.5, -0.25, 1.5, 0.125)):
+        np.testing.assert_allclose(y[7 + k], u / 10.0, rtol=1e-14)
+
+
+def test_refine_out_is_replicate_padded_conv_then_2sigmoid_minus_1():
+    c, hh, hw = 5, 7, 9
+    x = rng.standard_normal((c, hh, hw))
+    w = rng.standard_normal((3, c, 3, 3))
+    b = rng.standard_normal(3)
+    xp = F.pad(torch.from_numpy(x[None]), (1, 1, 1, 1), mode="replicate")
+    acc = F.conv2d(xp, torch.from_numpy(w), torch.from_numpy(b)).numpy()[0]
+    np.testing.assert_allclose(O.refine_out(x, w, b), 2.0 / (1.0 + np.exp(-acc)) - 1.0,
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_flow_out_constant_refine_residual_is_added_before_clamp():
+    """Identity warp (mask saturated to frame 0) plus a constant residual r per channel
+    (exact in binary32, so its x4 upsample is r): byte = trunc(clamp(p + r) * 255)."""
+    h, w = 16, 24
+    f0, f1 = _frames(h, w, seed=17)
+    res = np.empty((3, h // 4, w // 4), f32)
+    res[0], res[1], res[2] = 0.125, -0.25, 0.5  # B, G, R
+    out = O.flow_out(_flow_map(h, w, mask=30.0), f0, f1, res=res)
+    for k, (byte, r) in enumerate(((2, 0.125), (1, -0.25), (0, 0.5))):
+        ref = _byte(_unit(f0[..., byte]) + f32(r))
+        np.testing.assert_array_equal(out[..., byte], ref, err_msg=f"channel {k}")
