@@ -37,7 +37,7 @@ STATUS = {
 EXPORTS = (
     "acnn_conv2d_fused", "acnn_conv2d_out_hw", "acnn_conv2d_workspace_size", "acnn_conv2d_path",
     "acnn_pool2d", "acnn_resize2d", "acnn_concat", "acnn_deconv2d", "acnn_frame_prep_quarter",
-    "acnn_frame_flow_out",
+    "acnn_frame_flow_out", "acnn_frame_refine_prep", "acnn_frame_refine_out", "acnn_film",
     "acnn_status_string", "acnn_last_device_status", "acnn_set_wait_budget",
     "acnn_section_begin", "acnn_section_end", "acnn_section_launch", "acnn_section_destroy",
     "acnn_device_sm_count", "acnn_conv2d_fused_noalloc", "acnn_conv2d_plan",
@@ -83,7 +83,11 @@ def lib() -> ctypes.CDLL:
         L.acnn_concat.argtypes = [_I] * 7 + [_P, _P, _P, _P]
         L.acnn_deconv2d.argtypes = [D, _P, _P, _P, _P, _I, _I, _P, _P]
         L.acnn_frame_prep_quarter.argtypes = [_I, _I, _P, _P, ctypes.c_float, _I, _P, _P]
-        L.acnn_frame_flow_out.argtypes = [_I, _I, _P, _I, _P, _P, _P, _P]
+        L.acnn_frame_flow_out.argtypes = [_I, _I, _P, _I, _P, _P, _P, _P, _P]
+        L.acnn_frame_refine_prep.argtypes = [_I, _I, _P, _I, _P, _P, _I, _P, _P]
+        L.acnn_frame_refine_out.argtypes = [_I, _I, _I, _P, _I, _P, _P, _P, _P]
+        L.acnn_film.argtypes = [_I, ctypes.c_longlong, _I, _P, ctypes.c_float, _P, _P, _I, _P, _P,
+                                _P, _P]
         L.acnn_status_string.argtypes = [_I]
         L.acnn_status_string.restype = ctypes.c_char_p
         L.acnn_last_device_status.argtypes = [_P]
@@ -184,9 +188,26 @@ def acnn_frame_prep_quarter(h, w, rgba0, rgba1, t, out_dtype, y, stream=None) ->
                                          _ptr(y), _stream(stream))
 
 
-def acnn_frame_flow_out(h, w, tmp8, tmp8_dtype, rgba0, rgba1, out, stream=None) -> int:
+def acnn_frame_flow_out(h, w, tmp8, tmp8_dtype, rgba0, rgba1, refine_res, out,
+                        stream=None) -> int:
     return lib().acnn_frame_flow_out(h, w, _ptr(tmp8), tmp8_dtype, _ptr(rgba0), _ptr(rgba1),
-                                     _ptr(out), _stream(stream))
+                                     _ptr(refine_res), _ptr(out), _stream(stream))
+
+
+def acnn_frame_refine_prep(h, w, tmp8, tmp8_dtype, rgba0, rgba1, out_dtype, y,
+                           stream=None) -> int:
+    return lib().acnn_frame_refine_prep(h, w, _ptr(tmp8), tmp8_dtype, _ptr(rgba0), _ptr(rgba1),
+                                        out_dtype, _ptr(y), _stream(stream))
+
+
+def acnn_frame_refine_out(c, hh, hw, x, dtype, w, bias, y, stream=None) -> int:
+    return lib().acnn_frame_refine_out(c, hh, hw, _ptr(x), dtype, _ptr(w), _ptr(bias), _ptr(y),
+                                       _stream(stream))
+
+
+def acnn_film(c, n, dtype, x, t, w0, b0, hn, w2, b2, y, stream=None) -> int:
+    return lib().acnn_film(c, n, dtype, _ptr(x), float(t), _ptr(w0), _ptr(b0), hn, _ptr(w2),
+                           _ptr(b2), _ptr(y), _stream(stream))
 
 
 def acnn_last_device_status(stream=None) -> int:
@@ -355,12 +376,42 @@ def frame_prep_quarter(rgba0, rgba1, t, *, out_dtype=torch.float16, out=None, st
     return y
 
 
-def frame_flow_out(tmp8, rgba0, rgba1, *, out=None, stream=None):
-    """[5, h/8, w/8] flow/mask map + two h x w RGBA8 frames -> h x w RGBA8 frame."""
+def frame_flow_out(tmp8, rgba0, rgba1, *, refine_res=None, out=None, stream=None):
+    """[5, h/8, w/8] flow/mask map + two h x w RGBA8 frames (+ optional [3, h/4, w/4]
+    fp32 refine residual) -> h x w RGBA8 frame."""
     h, w, _ = rgba0.shape
     y = out if out is not None else torch.empty((h, w, 4), dtype=torch.uint8, device=rgba0.device)
-    check(acnn_frame_flow_out(h, w, tmp8, dtype_code(tmp8.dtype), rgba0, rgba1, y, stream),
-          "acnn_frame_flow_out")
+    check(acnn_frame_flow_out(h, w, tmp8, dtype_code(tmp8.dtype), rgba0, rgba1, refine_res, y,
+                              stream), "acnn_frame_flow_out")
+    return y
+
+
+def frame_refine_prep(tmp8, rgba0, rgba1, *, out_dtype=torch.float16, out=None, stream=None):
+    """[5, h/8, w/8] flow/mask map + two frames -> [11, h/4, w/4] refine-head input."""
+    h, w, _ = rgba0.shape
+    y = out if out is not None else torch.empty((11, h // 4, w // 4), dtype=out_dtype,
+                                                device=rgba0.device)
+    check(acnn_frame_refine_prep(h, w, tmp8, dtype_code(tmp8.dtype), rgba0, rgba1,
+                                 dtype_code(y.dtype), y, stream), "acnn_frame_refine_prep")
+    return y
+
+
+def frame_refine_out(x, w, bias, *, out=None, stream=None):
+    """[C, hh, hw] map -> [3, hh, hw] fp32 residual (replicate-padded conv3x3, 2 sigmoid - 1)."""
+    c, hh, hw = x.shape
+    y = out if out is not None else torch.empty((3, hh, hw), dtype=torch.float32, device=x.device)
+    check(acnn_frame_refine_out(c, hh, hw, x, dtype_code(x.dtype), w, bias, y, stream),
+          "acnn_frame_refine_out")
+    return y
+
+
+def film(x, t, w0, b0, w2, b2, *, out=None, stream=None):
+    """x [C, ...] -> x * (1 + s[c]) + s[C + c], s = the timestep MLP at t."""
+    c = x.shape[0]
+    n = x.numel() // c
+    y = out if out is not None else torch.empty_like(x)
+    check(acnn_film(c, n, dtype_code(x.dtype), x, t, w0, b0, b0.numel(), w2, b2, y, stream),
+          "acnn_film")
     return y
 
 

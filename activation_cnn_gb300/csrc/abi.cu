@@ -470,20 +470,69 @@ int acnn_frame_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_t* r
 }
 
 int acnn_frame_flow_out(int h, int w, const void* tmp8, int tmp8_dtype, const uint8_t* rgba0,
-                        const uint8_t* rgba1, uint8_t* out_rgba, acnn_stream_t stream) {
+                        const uint8_t* rgba1, const float* refine_res, uint8_t* out_rgba,
+                        acnn_stream_t stream) {
     if (!valid_dtype(tmp8_dtype)) return ACNN_ERR_BAD_ENUM;
     if (!tmp8 || !rgba0 || !rgba1 || !out_rgba) return ACNN_ERR_NULL_POINTER;
     if (h <= 0 || w <= 0 || h % 8 != 0 || w % 8 != 0) return ACNN_ERR_BAD_GEOMETRY;
     if ((long long)h * w > kIndexLimit) return ACNN_ERR_TOO_LARGE;
-    if (!aligned16(tmp8) || !aligned16(rgba0) || !aligned16(rgba1) || !aligned16(out_rgba))
+    if (!aligned16(tmp8) || !aligned16(rgba0) || !aligned16(rgba1) || !aligned16(out_rgba) ||
+        (refine_res && !aligned16(refine_res)))
         return ACNN_ERR_MISALIGNED;
     const size_t fb = (size_t)h * w * 4;
     const size_t tb = (size_t)5 * (h / 8) * (w / 8) * elem_size(tmp8_dtype);
+    const size_t rb = (size_t)3 * (h / 4) * (w / 4) * sizeof(float);
     if (overlaps(out_rgba, fb, rgba0, fb) || overlaps(out_rgba, fb, rgba1, fb) ||
-        overlaps(out_rgba, fb, tmp8, tb))
+        overlaps(out_rgba, fb, tmp8, tb) || (refine_res && overlaps(out_rgba, fb, refine_res, rb)))
         return ACNN_ERR_ALIAS;
-    return status_of(launch_flow_out(h, w, tmp8, tmp8_dtype, rgba0, rgba1, out_rgba,
+    return status_of(launch_flow_out(h, w, tmp8, tmp8_dtype, rgba0, rgba1, refine_res, out_rgba,
                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int acnn_frame_refine_prep(int h, int w, const void* tmp8, int tmp8_dtype, const uint8_t* rgba0,
+                           const uint8_t* rgba1, int out_dtype, void* y, acnn_stream_t stream) {
+    if (!valid_dtype(tmp8_dtype) || !valid_dtype(out_dtype)) return ACNN_ERR_BAD_ENUM;
+    if (!tmp8 || !rgba0 || !rgba1 || !y) return ACNN_ERR_NULL_POINTER;
+    if (h <= 0 || w <= 0 || h % 8 != 0 || w % 8 != 0) return ACNN_ERR_BAD_GEOMETRY;
+    if ((long long)h * w > kIndexLimit) return ACNN_ERR_TOO_LARGE;
+    if (!aligned16(tmp8) || !aligned16(rgba0) || !aligned16(rgba1) || !aligned16(y))
+        return ACNN_ERR_MISALIGNED;
+    const size_t fb = (size_t)h * w * 4;
+    const size_t tb = (size_t)5 * (h / 8) * (w / 8) * elem_size(tmp8_dtype);
+    const size_t yb = (size_t)11 * (h / 4) * (w / 4) * elem_size(out_dtype);
+    if (overlaps(y, yb, rgba0, fb) || overlaps(y, yb, rgba1, fb) || overlaps(y, yb, tmp8, tb))
+        return ACNN_ERR_ALIAS;
+    return status_of(launch_refine_prep(h, w, tmp8, tmp8_dtype, rgba0, rgba1, out_dtype, y,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int acnn_frame_refine_out(int c, int hh, int hw, const void* x, int dtype, const float* w,
+                          const float* bias, float* y, acnn_stream_t stream) {
+    if (!valid_dtype(dtype)) return ACNN_ERR_BAD_ENUM;
+    if (!x || !w || !bias || !y) return ACNN_ERR_NULL_POINTER;
+    if (c <= 0 || hh <= 0 || hw <= 0) return ACNN_ERR_BAD_GEOMETRY;
+    if ((long long)c * hh * hw > kIndexLimit) return ACNN_ERR_TOO_LARGE;
+    if (!aligned16(x) || !aligned16(y)) return ACNN_ERR_MISALIGNED;
+    const size_t yb = (size_t)3 * hh * hw * sizeof(float);
+    if (overlaps(y, yb, x, (size_t)c * hh * hw * elem_size(dtype)) ||
+        overlaps(y, yb, w, (size_t)27 * c * sizeof(float)) || overlaps(y, yb, bias, 3 * sizeof(float)))
+        return ACNN_ERR_ALIAS;
+    return status_of(launch_refine_out(c, hh, hw, x, dtype, w, bias, y,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int acnn_film(int c, long long n, int dtype, const void* x, float t, const float* w0,
+              const float* b0, int hn, const float* w2, const float* b2, void* y,
+              acnn_stream_t stream) {
+    if (!valid_dtype(dtype)) return ACNN_ERR_BAD_ENUM;
+    if (!x || !w0 || !b0 || !w2 || !b2 || !y) return ACNN_ERR_NULL_POINTER;
+    if (c <= 0 || n <= 0 || hn <= 0) return ACNN_ERR_BAD_GEOMETRY;
+    if (n > kIndexLimit || c > 65535 || (long long)c * n > kIndexLimit * 64) return ACNN_ERR_TOO_LARGE;
+    const size_t xb = (size_t)c * n * elem_size(dtype);
+    // y may be x itself (each element is read, then written, by one thread)
+    if (y != x && overlaps(y, xb, x, xb)) return ACNN_ERR_ALIAS;
+    return status_of(launch_film(c, (int)n, dtype, x, t, w0, b0, hn, w2, b2, y,
+                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
 const char* acnn_status_string(int status) {

@@ -135,7 +135,16 @@ cudaError_t launch_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_
                                 float t, int out_dtype, void* y, cudaStream_t s);
 // flow-out stage of the frame stack (flow_out.cu)
 cudaError_t launch_flow_out(int h, int w, const void* tmp8, int tmp8_dtype, const uint8_t* rgba0,
-                            const uint8_t* rgba1, uint8_t* out, cudaStream_t s);
+                            const uint8_t* rgba1, const float* res, uint8_t* out, cudaStream_t s);
+// t-factored frame stack (flow_out.cu)
+cudaError_t launch_refine_prep(int h, int w, const void* tmp8, int tmp8_dtype,
+                               const uint8_t* rgba0, const uint8_t* rgba1, int out_dtype,
+                               void* out, cudaStream_t s);
+cudaError_t launch_refine_out(int c, int hh, int hw, const void* x, int dtype, const float* w,
+                              const float* bias, float* y, cudaStream_t s);
+cudaError_t launch_film(int c, int n, int dtype, const void* x, float t, const float* w0,
+                        const float* b0, int hn, const float* w2, const float* b2, void* y,
+                        cudaStream_t s);
 // im2col pack of x into a [n*oh*ow, kp] matrix and of w into [c_out, kp] (2-byte types)
 cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, const void* x,
                                void* a, const void* w, void* wp, cudaStream_t s);

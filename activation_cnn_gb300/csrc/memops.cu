@@ -482,23 +482,28 @@ constexpr int kDeconvCoBlock = 8;
 // 3x3 input neighbourhood of (a, b) -- rows a (ky = 1) and a - 1 (ky = 3) for
 // py = 0, rows a + 1 (ky = 0) and a (ky = 2) for py = 1, the same along x --
 // so one thread per input pixel accumulates the 2 x 2 outputs it owns.  A
-// block covers 32 input pixels of one row and 8 output channels; its 8 warps
-// split C_in (warp g takes ci = g, g + 8, ...) and add their partial sums
-// through shared memory in warp order.
+// block covers 32 input pixels of one row and up to 8 output channels; its 16
+// warps split C_in (warp g takes ci = g, g + 16, ...) and add their partial
+// sums through shared memory in warp order.  A (ci, co) pair's 16 taps are
+// one 64-byte row of the weight, read as four 16-byte vectors (the same
+// address across the warp: a broadcast).
+constexpr int kDeconvWarps = 16;
+
 template <typename Ti, typename To>
-__global__ void __launch_bounds__(kThreads) deconv4s2_kernel(
+__global__ void __launch_bounds__(32 * kDeconvWarps, 2) deconv4s2_kernel(
     const Ti* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
     const float* __restrict__ alpha, To* __restrict__ y, int layout, int N, int CI, int CO, int H,
     int W, int act) {
     griddep_wait();  // inputs may come from the previous kernel on the stream
     constexpr int CB = kDeconvCoBlock;
-    __shared__ float red[kThreads / 32][32][4 * CB + 1];
+    extern __shared__ float red[];  // [warp][lane][4 * nco + 1]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles_x = (W + 31) / 32;
     const int a = (blockIdx.x / tiles_x) % H, n = (blockIdx.x / tiles_x) / H;
     const int b = (blockIdx.x % tiles_x) * 32 + lane;
     const int co0 = blockIdx.y * CB;
     const int nco = min(CB, CO - co0);
+    const int rs = 4 * nco + 1;
     float acc[2][2][CB];
 #pragma unroll
     for (int py = 0; py < 2; ++py)
@@ -507,7 +512,7 @@ __global__ void __launch_bounds__(kThreads) deconv4s2_kernel(
 #pragma unroll
             for (int j = 0; j < CB; ++j) acc[py][px][j] = 0.0f;
     if (b < W) {
-        for (int ci = warp; ci < CI; ci += kThreads / 32) {
+        for (int ci = warp; ci < CI; ci += kDeconvWarps) {
             float nb[3][3];  // x at rows a-1..a+1, cols b-1..b+1 (zero outside)
 #pragma unroll
             for (int dy = 0; dy < 3; ++dy)
@@ -521,7 +526,14 @@ __global__ void __launch_bounds__(kThreads) deconv4s2_kernel(
 #pragma unroll
             for (int j = 0; j < CB; ++j) {
                 if (j >= nco) break;
-                const float* wk = w + ((long long)ci * CO + co0 + j) * 16;  // [ky][kx]
+                const float4* wk =
+                    reinterpret_cast<const float4*>(w + ((long long)ci * CO + co0 + j) * 16);
+                float wt[4][4];  // [ky][kx]
+#pragma unroll
+                for (int ky = 0; ky < 4; ++ky) {
+                    const float4 v = __ldg(wk + ky);
+                    wt[ky][0] = v.x, wt[ky][1] = v.y, wt[ky][2] = v.z, wt[ky][3] = v.w;
+                }
 #pragma unroll
                 for (int py = 0; py < 2; ++py)
 #pragma unroll
@@ -535,28 +547,29 @@ __global__ void __launch_bounds__(kThreads) deconv4s2_kernel(
                                 const int dy = py == 0 ? 1 - ty : 2 - ty;
                                 const int kx = px == 0 ? 1 + 2 * tx : 2 * tx;
                                 const int dx = px == 0 ? 1 - tx : 2 - tx;
-                                acc[py][px][j] =
-                                    fmaf(nb[dy][dx], __ldg(wk + ky * 4 + kx), acc[py][px][j]);
+                                acc[py][px][j] = fmaf(nb[dy][dx], wt[ky][kx], acc[py][px][j]);
                             }
             }
         }
     }
+    float* mine = red + ((size_t)warp * 32 + lane) * rs;
 #pragma unroll
     for (int py = 0; py < 2; ++py)
 #pragma unroll
         for (int px = 0; px < 2; ++px)
 #pragma unroll
-            for (int j = 0; j < CB; ++j) red[warp][lane][(py * 2 + px) * CB + j] = acc[py][px][j];
+            for (int j = 0; j < CB; ++j)
+                if (j < nco) mine[(py * 2 + px) * nco + j] = acc[py][px][j];
     __syncthreads();
-    // 32 pixels x 4 outputs x CB channels, summed over the warps in order
+    // 32 pixels x 4 outputs x nco channels, summed over the warps in order
     const int OH = 2 * H, OW = 2 * W;
-    for (int i = threadIdx.x; i < 32 * 4 * CB; i += kThreads) {
-        const int l = i / (4 * CB), r = i - l * 4 * CB;
-        const int pp = r / CB, j = r - pp * CB;
+    for (int i = threadIdx.x; i < 32 * 4 * nco; i += 32 * kDeconvWarps) {
+        const int l = i / (4 * nco), r = i - l * 4 * nco;
+        const int pp = r / nco, j = r - pp * nco;
         const int bb = (blockIdx.x % tiles_x) * 32 + l;
-        if (bb >= W || j >= nco) continue;
+        if (bb >= W) continue;
         float v = bias ? bias[co0 + j] : 0.0f;
-        for (int g = 0; g < kThreads / 32; ++g) v += red[g][l][r];
+        for (int g = 0; g < kDeconvWarps; ++g) v += red[((size_t)g * 32 + l) * rs + r];
         const int oy = 2 * a + (pp >> 1), ox = 2 * bb + (pp & 1);
         const float al = (act == ACNN_ACT_PRELU) ? alpha[co0 + j] : 0.0f;
         y[act_index(layout, CO, OH, OW, n, co0 + j, oy, ox)] = from_f32<To>(apply_act(act, v, al));
@@ -874,9 +887,18 @@ cudaError_t deconv_typed(const acnn_conv_desc& d, int oh, int ow, const void* x,
         const long long rows = (long long)d.n * d.h * ((d.w + 31) / 32);
         const int cob = (d.c_out + kDeconvCoBlock - 1) / kDeconvCoBlock;
         if (rows <= 0x7fffffffLL && cob <= 65535) {
-            launch_pdl(deconv4s2_kernel<Ti, To>, dim3((unsigned)rows, cob), kThreads, 0, s,
-                       static_cast<const Ti*>(x), w, bias, alpha, static_cast<To*>(y), d.layout,
-                       d.n, d.c_in, d.c_out, d.h, d.w, act);
+            const int nco = d.c_out < kDeconvCoBlock ? d.c_out : kDeconvCoBlock;
+            const size_t smem = (size_t)kDeconvWarps * 32 * (4 * nco + 1) * sizeof(float);
+            static bool attr = false;  // per instantiation: the largest partial-sum buffer
+            if (!attr) {
+                const size_t mx = (size_t)kDeconvWarps * 32 * (4 * kDeconvCoBlock + 1) * 4;
+                cudaFuncSetAttribute(deconv4s2_kernel<Ti, To>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx);
+                attr = true;
+            }
+            launch_pdl(deconv4s2_kernel<Ti, To>, dim3((unsigned)rows, cob), 32 * kDeconvWarps,
+                       smem, s, static_cast<const Ti*>(x), w, bias, alpha, static_cast<To*>(y),
+                       d.layout, d.n, d.c_in, d.c_out, d.h, d.w, act);
             return cudaGetLastError();
         }
     }

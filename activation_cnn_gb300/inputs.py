@@ -67,6 +67,23 @@ def deconv_weight(seed: int, name: str, c_in: int, c_out: int, k: int) -> torch.
     return tensor(seed, name + ".w", (c_in, c_out, k, k), "normal", std=std)
 
 
+def film_mlp(seed: int, name: str, c: int, hn: int):
+    """Timestep MLP Linear(1, hn) -> ReLU -> Linear(hn, 2c), fp32: (w0 [hn], b0 [hn],
+    w2 [2c, hn], b2 [2c]); t in [0, 1], w0 U(-2, 2), b0 U(-0.5, 0.5), w2 N(0, 0.2 / sqrt(hn))
+    and b2 U(-0.05, 0.05), so the modulation 1 + s stays near 1."""
+    w0 = tensor(seed, name + ".0.w", (hn,), "uniform", -2.0, 2.0)
+    b0 = tensor(seed, name + ".0.b", (hn,), "uniform", -0.5, 0.5)
+    w2 = tensor(seed, name + ".2.w", (2 * c, hn), "normal", std=0.2 / hn ** 0.5)
+    b2 = tensor(seed, name + ".2.b", (2 * c,), "uniform", -0.05, 0.05)
+    return w0, b0, w2, b2
+
+
+def refine_out_weight(seed: int, name: str, c_in: int) -> torch.Tensor:
+    """The refine head's last conv, [3, c_in, 3, 3] fp32, N(0, 0.25 / sqrt(9 c_in)):
+    a small correction, so 2 sigmoid - 1 stays well inside (-1, 1)."""
+    return tensor(seed, name + ".w", (3, c_in, 3, 3), "normal", std=0.25 / (9 * c_in) ** 0.5)
+
+
 def rgba_frame(seed: int, name: str, h: int, w: int) -> torch.Tensor:
     """An [H, W, 4] uint8 frame of uniform random bytes."""
     g = _gen(seed, name)

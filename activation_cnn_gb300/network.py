@@ -42,6 +42,7 @@ class ConvSpec:
     h: int  # input height
     w: int  # input width
     res_mode: int = A.RES_NONE
+    param: str = ""  # name the weights are drawn under (default: name)
 
     @property
     def oh(self):
@@ -61,6 +62,7 @@ class Op:
     bytes: float = 0.0       # algorithmic bytes (inputs read once + output written once)
     label: str = ""
     spec: object = None
+    launches: int = 1        # kernels one call launches (non-conv ops)
 
 
 @dataclass
@@ -149,10 +151,11 @@ class Builder:
     def conv(self, src, spec: ConvSpec, residual=None, out=None):
         net = self.net
         x = net.tensors[src]
-        w = G.conv_weight(self.seed, spec.name, spec.c_out, spec.c_in, spec.k, spec.k,
-                          net.layout, net.dtype)
-        b = G.conv_bias(self.seed, spec.name, spec.c_out)
-        al = G.prelu_alpha(self.seed, spec.name, spec.c_out) if spec.act == A.ACT_PRELU else None
+        pn = spec.param or spec.name
+        w = G.conv_weight(self.seed, pn, spec.c_out, spec.c_in, spec.k, spec.k, net.layout,
+                          net.dtype)
+        b = G.conv_bias(self.seed, pn, spec.c_out)
+        al = G.prelu_alpha(self.seed, pn, spec.c_out) if spec.act == A.ACT_PRELU else None
         net.params[spec.name] = (w, b, al)
         wd, bd = w.to(self.device), b.to(self.device)
         ald = al.to(self.device) if al is not None else None
@@ -476,12 +479,129 @@ def frame_net(device="cuda", h=1088, w=1920, c1=120, c2=240, t=0.5, flow_out=Fal
     net.tensors["out"] = out
 
     def flow_stage(stream):
-        A.check(A.acnn_frame_flow_out(h, w, tmp8, G.F16, f0, f1, out, stream), "flow_out")
+        A.check(A.acnn_frame_flow_out(h, w, tmp8, G.F16, f0, f1, None, out, stream), "flow_out")
 
     # algorithmic bytes: the 1/8 map, both frames once, the output frame
     net.ops.append(Op("flow_out", "frame", flow_stage, 0.0,
                       tmp8.numel() * 2 + 3 * h * w * 4, "flow_out"))
     net.outputs = ["out"]
+    return net
+
+
+def frame_tfact_net(device="cuda", h=1088, w=1920, c1=120, c2=240, ts=(0.25, 0.5, 0.75),
+                    hn=64, rc=32) -> Net:
+    """t-factored frame stack with the refine head (rt.js tfact2: prepPair once
+    per frame pair, runT per timestep), NCHW fp16.
+
+    trunk, once: prep (the six frame planes of the bilinear 1/4 prep) -> conv3x3/s2
+    6->c1 + PReLU -> conv3x3/s2 c1->c2 + PReLU (feat0) -> convblocks 0..5.
+    per t: FiLM(t) of the trunk map -> convblocks 6, 7 (7 adds feat0 after its
+    PReLU) -> deconv 4x4/s2 c2->5 -> refine prep (11 planes at 1/4) -> three
+    conv3x3 + PReLU (11->rc->rc->rc, zero padding) -> refine out (replicate-padded
+    conv3x3 rc->3, 2 sigmoid - 1, fp32) -> flow-out with that residual.
+    Outputs: one h x w RGBA8 frame per t.
+    """
+    assert rc % 4 == 0, "refine channels must be a multiple of 4"
+    seed = 1238
+    net = Net("frame_tfact", 1, G.F16, G.NCHW)
+    b = Builder(net, seed, device)
+    b.set_section("frame")
+    f0 = G.rgba_frame(seed, "frame0", h, w).to(device)
+    f1 = G.rgba_frame(seed, "frame1", h, w).to(device)
+    net.tensors["frame0"], net.tensors["frame1"] = f0, f1
+    net.inputs["frame0"], net.inputs["frame1"] = f0, f1
+    qh, qw = h // 4, w // 4
+    # the 6-channel prep is the first six planes of the 7-plane prep (its t
+    # plane is written and not read): the same kernel, no second variant
+    xq = b.buffer("xq", 7, qh, qw)
+    net.tensors["xq6"] = xq[:, :6]
+
+    def prep(stream):
+        A.check(A.acnn_frame_prep_quarter(h, w, f0, f1, 0.0, G.F16, xq, stream), "prep")
+
+    touched = 2 * (2 * qh) * w * 4
+    net.ops.append(Op("prep", "frame", prep, 0.0, touched + xq.numel() * 2, "prep"))
+    P = A.ACT_PRELU
+    a = b.conv("xq6", ConvSpec("conv0a", 6, c1, 3, 2, 1, P, qh, qw))
+    s0 = ConvSpec("conv0b", c1, c2, 3, 2, 1, P, qh // 2, qw // 2)
+    feat0 = b.conv(a, s0)
+    hh, ww = s0.oh, s0.ow
+    cur = feat0
+    for i in range(6):
+        cur = b.conv(cur, ConvSpec(f"convblock.{i}", c2, c2, 3, 1, 1, P, hh, ww))
+    trunk = net.tensors[cur]
+    fw = [t.to(device) for t in G.film_mlp(seed, "film", c2, hn)]
+    net.params["film"] = G.film_mlp(seed, "film", c2, hn)
+    wdc = G.deconv_weight(seed, "lastconv", c2, 5, 4)
+    bdc = G.conv_bias(seed, "lastconv", 5)
+    net.params["lastconv"] = (wdc, bdc, None)
+    wdd, bdd = wdc.to(device), bdc.to(device)
+    wro = G.refine_out_weight(seed, "refine.c3", rc)
+    bro = G.conv_bias(seed, "refine.c3", 3)
+    net.params["refine.c3"] = (wro, bro, None)
+    wrod, brod = wro.to(device), bro.to(device)
+    dd = A.ConvDesc(1, hh, ww, c2, 5, 4, 4, 2, 1, G.NCHW, G.F16)
+    outs = []
+    for i, t in enumerate(ts):
+        sfx = f"@t{i}"
+        fm = b.buffer("film" + sfx, c2, hh, ww)
+
+        def film(stream, t=t, fm=fm):
+            A.check(A.acnn_film(c2, hh * ww, G.F16, trunk, t, *fw[:2], hn, *fw[2:], fm, stream),
+                    "film")
+
+        net.ops.append(Op("film", "frame", film, 2.0 * c2 * hh * ww + 4.0 * c2 * hn,
+                          2 * trunk.numel() * 2, "film" + sfx))
+        cur = b.conv("film" + sfx, ConvSpec("convblock.6" + sfx, c2, c2, 3, 1, 1, P, hh, ww,
+                                            param="convblock.6"))
+        cur = b.conv(cur, ConvSpec("convblock.7" + sfx, c2, c2, 3, 1, 1, P, hh, ww,
+                                   res_mode=A.RES_ACT_THEN_ADD, param="convblock.7"),
+                     residual=feat0)
+        xin = net.tensors[cur]
+        tmp8 = b.buffer("tmp8" + sfx, 5, 2 * hh, 2 * ww)
+
+        def deconv(stream, xin=xin, tmp8=tmp8):
+            A.check(A.acnn_deconv2d(dd, xin, wdd, bdd, None, A.ACT_NONE, G.F16, tmp8, stream),
+                    "deconv")
+
+        net.ops.append(Op("deconv", "frame", deconv, 2.0 * 5 * c2 * 4 * (2 * hh) * (2 * ww),
+                          (xin.numel() + tmp8.numel()) * 2 + wdc.numel() * 4, "deconv" + sfx))
+        rin = b.buffer("rin" + sfx, 11, qh, qw)
+
+        def rprep(stream, tmp8=tmp8, rin=rin):
+            A.check(A.acnn_frame_refine_prep(h, w, tmp8, G.F16, f0, f1, G.F16, rin, stream),
+                    "refine_prep")
+
+        # algorithmic bytes: the 1/8 map, the frames' pixels the four centre taps
+        # of each 4x4 block reach (about half of each frame), the 11 planes
+        net.ops.append(Op("refine_prep", "frame", rprep, 0.0,
+                          tmp8.numel() * 2 + 2 * (h * w * 4) // 2 + rin.numel() * 2,
+                          "refine_prep" + sfx))
+        r = b.conv("rin" + sfx, ConvSpec("refine.c0" + sfx, 11, rc, 3, 1, 1, P, qh, qw,
+                                         param="refine.c0"))
+        r = b.conv(r, ConvSpec("refine.c1" + sfx, rc, rc, 3, 1, 1, P, qh, qw, param="refine.c1"))
+        r = b.conv(r, ConvSpec("refine.c2" + sfx, rc, rc, 3, 1, 1, P, qh, qw, param="refine.c2"))
+        rx = net.tensors[r]
+        rres = b.buffer("rres" + sfx, 3, qh, qw, dtype=G.F32)
+
+        def rout(stream, rx=rx, rres=rres):
+            A.check(A.acnn_frame_refine_out(rc, qh, qw, rx, G.F16, wrod, brod, rres, stream),
+                    "refine_out")
+
+        net.ops.append(Op("refine_out", "frame", rout, 2.0 * 3 * rc * 9 * qh * qw,
+                          rx.numel() * 2 + rres.numel() * 4, "refine_out" + sfx))
+        out = torch.empty((h, w, 4), dtype=torch.uint8, device=device)
+        net.tensors["out" + sfx] = out
+
+        def flow_stage(stream, tmp8=tmp8, rres=rres, out=out):
+            A.check(A.acnn_frame_flow_out(h, w, tmp8, G.F16, f0, f1, rres, out, stream),
+                    "flow_out")
+
+        net.ops.append(Op("flow_out", "frame", flow_stage, 0.0,
+                          tmp8.numel() * 2 + rres.numel() * 4 + 3 * h * w * 4,
+                          "flow_out" + sfx))
+        outs.append("out" + sfx)
+    net.outputs = outs
     return net
 
 
@@ -494,4 +614,5 @@ WORKLOADS = {
     "frame_out": lambda device="cuda": frame_net(device, flow_out=True),
     "backbone": backbone_net,
     "backbone_csp": lambda device="cuda": backbone_net(device, neck="csp"),
+    "frame_tfact": frame_tfact_net,
 }

@@ -164,7 +164,7 @@ def launches_per_step(net):
     n = 0
     for op in net.ops:
         if op.kind != "conv":
-            n += 1
+            n += op.launches
             continue
         s = op.spec
         d = A.ConvDesc(net.batch, s.h, s.w, s.c_in, s.c_out, s.k, s.k, s.stride, s.pad,
@@ -440,7 +440,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="backbone",
                     choices=["backbone", "backbone_csp", "block", "block_down", "stem", "conv1", "frame",
-                             "frame_out"])
+                             "frame_out", "frame_tfact"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--layers", action="store_true", help="add per-conv timings")

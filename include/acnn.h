@@ -235,21 +235,64 @@ int acnn_frame_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_t* r
 /* ---- frame flow-out ----------------------------------------------------------
  * rt.js wgslFlowOut (the stage after the deconv of the frame stack), with
  * wgslPrepFull's full-resolution planes read straight from the frames.
- *   tmp8     device [5, h/8, w/8] NCHW of tmp8_dtype: flow of frame 0 (x, y),
- *            flow of frame 1 (x, y), mask logit
- *   rgba0/1  device h x w RGBA8 frames (bytes R, G, B, A per pixel)
- *   out_rgba device h x w RGBA8 output
+ *   tmp8       device [5, h/8, w/8] NCHW of tmp8_dtype: flow of frame 0 (x, y),
+ *              flow of frame 1 (x, y), mask logit
+ *   rgba0/1    device h x w RGBA8 frames (bytes R, G, B, A per pixel)
+ *   refine_res device [3, h/4, w/4] fp32 (planes B, G, R), the refine head's
+ *              residual (rt.js tfact2, withRes), or NULL for none
+ *   out_rgba   device h x w RGBA8 output
  * Per output pixel: the five planes upsampled x8 (bilinear, align_corners=
  * false, clamped taps), flows times 8, m = 1/(1+exp(-mask)); each frame's
  * B, G, R (byte/255) sampled bilinearly at (x, y) + its flow with clamped taps
- * (grid_sample border, align_corners=true); v = w0*m + w1*(1-m); output bytes
- * R, G, B = (uint)(clamp(v, 0, 1) * 255) (truncation), A = 255.  Computed in
- * binary32 in one fixed order without fused multiply-adds; exp by Cody-Waite
- * reduction and a degree-7 Taylor polynomial.  h and w multiples of 8; all
- * pointers 16-byte aligned; out_rgba must not overlap an input.
+ * (grid_sample border, align_corners=true); v = w0*m + w1*(1-m), plus, with a
+ * residual, its x4 bilinear upsample (align_corners=false, clamped taps);
+ * output bytes R, G, B = (uint)(clamp(v, 0, 1) * 255) (truncation), A = 255.
+ * Computed in binary32 in one fixed order without fused multiply-adds; exp by
+ * Cody-Waite reduction and a degree-7 Taylor polynomial.  h and w multiples of
+ * 8; all pointers 16-byte aligned; out_rgba must not overlap an input.
  */
 int acnn_frame_flow_out(int h, int w, const void* tmp8, int tmp8_dtype, const uint8_t* rgba0,
-                        const uint8_t* rgba1, uint8_t* out_rgba, acnn_stream_t stream);
+                        const uint8_t* rgba1, const float* refine_res, uint8_t* out_rgba,
+                        acnn_stream_t stream);
+
+/* ---- t-factored frame stack (rt.js tfact / tfact2) --------------------------
+ * Refine prep, rt.js wgslRefinePrep: the refine head's input y = [11, h/4, w/4]
+ * NCHW of out_dtype (device) from the same tmp8 and frames as the flow-out
+ * stage.  For each quarter-resolution pixel (hx, hy), over the four pixels
+ * (4 hx + i, 4 hy + j), i, j in {1, 2} (the centre 2x2 of its 4x4 block, the
+ * taps of a 1/4 bilinear downsample with align_corners=false): the mean of
+ * warped frame 0 (B, G, R), warped frame 1 (B, G, R) and the sigmoid mask,
+ * then the mean of the four x8 flows (u0, v0, u1, v1) times 0.25 / 20.
+ * Upsample and warp as in acnn_frame_flow_out; fp32 arithmetic, one rounding
+ * to out_dtype on store.  h and w multiples of 8; pointers 16-byte aligned;
+ * y must not overlap an input.
+ */
+int acnn_frame_refine_prep(int h, int w, const void* tmp8, int tmp8_dtype, const uint8_t* rgba0,
+                           const uint8_t* rgba1, int out_dtype, void* y, acnn_stream_t stream);
+
+/* Refine out, rt.js wgslRefineOut: y[co] = 2 sigmoid(b[co] + sum over ci, ky,
+ * kx of x[ci][clamp(oy+ky-1)][clamp(ox+kx-1)] * w[co][ci][ky][kx]) - 1 for
+ * co = 0..2 -- a 3x3 conv C -> 3 with replicate (clamped-index) padding.
+ *   x  device [c, hh, hw] NCHW of dtype (16-byte aligned)
+ *   w  device fp32 [3, c, 3, 3];  bias device fp32 [3]
+ *   y  device fp32 [3, hh, hw] (16-byte aligned, no overlap with the inputs)
+ * fp32 accumulation, in input-channel order.
+ */
+int acnn_frame_refine_out(int c, int hh, int hw, const void* x, int dtype, const float* w,
+                          const float* bias, float* y, acnn_stream_t stream);
+
+/* FiLM, rt.js wgslFilm with filmParams: the timestep MLP
+ *   s[k] = b2[k] + sum_j w2[k][j] * max(0, w0[j] * t + b0[j]),  k < 2c,
+ * evaluated on the device (the page runs it on the host), then
+ *   y[ci][i] = x[ci][i] * (1 + s[ci]) + s[c + ci]   (i < n, one plane per channel)
+ * with x, y device [c, n] of dtype (y may be x itself, else no overlap);
+ * w0, b0 device fp32 [hn]; w2 device fp32 [2c, hn]; b2 device fp32 [2c];
+ * c <= 65535.  One kernel on stream; fp32 arithmetic, one rounding to dtype
+ * on store.
+ */
+int acnn_film(int c, long long n, int dtype, const void* x, float t, const float* w0,
+              const float* b0, int hn, const float* w2, const float* b2, void* y,
+              acnn_stream_t stream);
 
 /* ---- status ------------------------------------------------------------------ */
 /* Static string for a status code. */

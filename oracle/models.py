@@ -9,7 +9,8 @@ to the storage type (round to nearest even) between ops, as the GPU stores it
 
 Layer naming (shared with the generator only): stem.{0,1,2};
 s{stage}.b{block}.conv{1,2,3} and .short; neck.lat{3,4,5}, neck.fpn{4,3},
-neck.down{3,4}, neck.pan{4,5}; conv0a, conv0b, convblock.{i}, lastconv.
+neck.down{3,4}, neck.pan{4,5}; conv0a, conv0b, convblock.{i}, lastconv;
+film, refine.c{0,1,2,3}.
 """
 from __future__ import annotations
 
@@ -188,3 +189,40 @@ def frame(rgba0, rgba1, t=0.5, c1=120, c2=240, flow_out=False):
         # rt.js wgslFlowOut on the fp16-stored map, in binary32 as on the page
         return O.flow_out(tmp8[0].astype(np.float32), rgba0, rgba1)
     return r.store(O.resize2d(tmp8, O.BILINEAR, h, wd, layout=O.NCHW))
+
+
+def frame_tfact(rgba0, rgba1, ts=(0.25, 0.5, 0.75), c1=120, c2=240, hn=64, rc=32):
+    """rt.js tfact2, prepPair then runT per t: the t-free trunk (six prep planes
+    -> prelu(conv s2) x2 -> convblocks 0..5) once, then per t: FiLM(t) ->
+    convblocks 6, 7 (7 adding the map that entered convblock 0 after its
+    PReLU) -> deconv 4x4/s2 -> refine prep -> three conv3x3 + PReLU (zero pad)
+    -> refine out (replicate pad, 2 sigmoid - 1) -> flow-out with that residual.
+    NCHW fp16 storage; the refine residual is fp32 (its buffer type on the
+    page); the flow-out stage runs in binary32.  One RGBA8 frame per t."""
+    seed = 1238
+    r = Runner(Params(seed, O.NCHW, G.F16), O.F16)
+    xq = r.store(O.prep_quarter(rgba0, rgba1, 0.0)[:6])[None]
+    P = O.ACT_PRELU
+    a = r.conv(xq, "conv0a", c1, 3, 2, 1, P)
+    feat0 = r.conv(a, "conv0b", c2, 3, 2, 1, P)
+    trunk = feat0
+    for i in range(6):
+        trunk = r.conv(trunk, f"convblock.{i}", c2, 3, 1, 1, P)
+    w0, b0, w2, b2 = (_f64(t) for t in G.film_mlp(seed, "film", c2, hn))
+    wdc = _f64(G.deconv_weight(seed, "lastconv", c2, 5, 4))
+    bdc = _f64(G.conv_bias(seed, "lastconv", 5))
+    wro = _f64(G.refine_out_weight(seed, "refine.c3", rc))
+    bro = _f64(G.conv_bias(seed, "refine.c3", 3))
+    outs = []
+    for t in ts:
+        f = r.store(O.film(trunk[0], t, w0, b0, w2, b2))[None]
+        f = r.conv(f, "convblock.6", c2, 3, 1, 1, P)
+        f = r.conv(f, "convblock.7", c2, 3, 1, 1, P, residual=feat0, res_mode=O.RES_ACT_THEN_ADD)
+        tmp8 = r.store(O.deconv2d(f, wdc, bdc))
+        rin = r.store(O.refine_prep(tmp8[0], rgba0, rgba1))[None]
+        x = r.conv(rin, "refine.c0", rc, 3, 1, 1, P)
+        x = r.conv(x, "refine.c1", rc, 3, 1, 1, P)
+        x = r.conv(x, "refine.c2", rc, 3, 1, 1, P)
+        res = O.round_storage(O.refine_out(x[0], wro, bro), O.F32).astype(np.float32)
+        outs.append(O.flow_out(tmp8[0].astype(np.float32), rgba0, rgba1, res=res))
+    return outs

@@ -118,11 +118,27 @@ def test_companions_reject_before_launch(A):
     assert A.acnn_frame_prep_quarter(10, 16, X, W, 0.5, 1, Y, 0) == 2          # h % 4
     assert A.acnn_frame_prep_quarter(16, 16, X, None, 0.5, 1, Y, 0) == 1
     # flow out: h, w multiples of 8, dtype enum, pointers, alignment, aliasing
-    assert A.acnn_frame_flow_out(12, 16, X, 1, W, Y, Y + (1 << 20), 0) == 2
-    assert A.acnn_frame_flow_out(16, 16, X, 9, W, Y, Y + (1 << 20), 0) == 7
-    assert A.acnn_frame_flow_out(16, 16, None, 1, W, Y, Y + (1 << 20), 0) == 1
-    assert A.acnn_frame_flow_out(16, 16, X, 1, W + 4, Y, Y + (1 << 20), 0) == 4
-    assert A.acnn_frame_flow_out(16, 16, X, 1, W, Y, W + 512, 0) == 6
+    assert A.acnn_frame_flow_out(12, 16, X, 1, W, Y, None, Y + (1 << 20), 0) == 2
+    assert A.acnn_frame_flow_out(16, 16, X, 9, W, Y, None, Y + (1 << 20), 0) == 7
+    assert A.acnn_frame_flow_out(16, 16, None, 1, W, Y, None, Y + (1 << 20), 0) == 1
+    assert A.acnn_frame_flow_out(16, 16, X, 1, W + 4, Y, None, Y + (1 << 20), 0) == 4
+    assert A.acnn_frame_flow_out(16, 16, X, 1, W, Y, None, W + 512, 0) == 6
+    assert A.acnn_frame_flow_out(16, 16, X, 1, W, Y, R + 4, Y + (1 << 20), 0) == 4  # residual
+    assert A.acnn_frame_flow_out(16, 16, X, 1, W, Y, Y + (1 << 20), Y + (1 << 20), 0) == 6
+    # t-factored stack: refine prep / refine out / FiLM argument checks
+    assert A.acnn_frame_refine_prep(12, 16, X, 1, W, Y, 1, R, 0) == 2
+    assert A.acnn_frame_refine_prep(16, 16, X, 1, W, Y, 5, R, 0) == 7
+    assert A.acnn_frame_refine_prep(16, 16, X, 1, None, Y, 1, R, 0) == 1
+    assert A.acnn_frame_refine_prep(16, 16, X, 1, W, Y, 1, W + 64, 0) == 6
+    assert A.acnn_frame_refine_out(0, 4, 4, X, 1, W, W + 512, R, 0) == 2
+    assert A.acnn_frame_refine_out(8, 4, 4, X, 1, W, None, R, 0) == 1
+    assert A.acnn_frame_refine_out(8, 4, 4, X, 1, W, W + 512, X + 16, 0) == 6
+    assert A.acnn_frame_refine_out(8, 4, 4, X + 4, 1, W, W + 512, R, 0) == 4
+    assert A.acnn_film(8, 16, 1, X, 0.5, W, W, 4, W, W, X, 0) != 6              # in place ok
+    assert A.acnn_film(8, 16, 1, X, 0.5, W, W, 4, W, W, X + 2, 0) == 6
+    assert A.acnn_film(8, 16, 1, X, 0.5, W, W, 0, W, W, Y, 0) == 2
+    assert A.acnn_film(8, 16, 1, X, 0.5, W, None, 4, W, W, Y, 0) == 1
+    assert A.acnn_film(70000, 16, 1, X, 0.5, W, W, 4, W, W, Y, 0) == 10         # c > 65535
     # folded concat conv: NHWC fp16/bf16 only, c_a a multiple of 64, c_b > 0
     d = desc(A, c_in=128, c_out=64)
     assert A.acnn_conv2d_fused_cat2(d, X, 64, R, W, None, None, None, 0, 1, Y, None, 0, 0) != 1

@@ -116,6 +116,59 @@ def test_frame_out_reduced_end_to_end():
         np.mean(d == 0) >= 0.75, (np.mean(d == 0), np.mean(d <= 1), d.mean(), d.max())
 
 
+def _tfact_stages(net, ts, h, w):
+    """Teacher-forced check of the t-factored stack's non-conv stages on the
+    GPU's own stored inputs: FiLM and the refine pair against the fp64 oracle,
+    the flow-out bytes (with the refine residual) exactly."""
+    T = net.tensors
+    f0, f1 = net.inputs["frame0"].cpu().numpy(), net.inputs["frame1"].cpu().numpy()
+    prm = [to64(p) for p in net.params["film"]]
+    w3, b3, _ = net.params["refine.c3"]
+    for i, t in enumerate(ts):
+        sfx = f"@t{i}"
+        assert_parity(T["film" + sfx][0], O.film(to64(T["convblock.5"][0]), t, *prm),
+                      torch.float16, "film" + sfx)
+        tmp8 = to64(T["tmp8" + sfx][0])
+        assert_parity(T["rin" + sfx][0], O.refine_prep(tmp8, f0, f1), torch.float16,
+                      "refine_prep" + sfx)
+        assert_parity(T["rres" + sfx][0], O.refine_out(to64(T["refine.c2" + sfx][0]), to64(w3),
+                                                       to64(b3)), torch.float32,
+                      "refine_out" + sfx)
+        ref = O.flow_out(tmp8.astype(np.float32), f0, f1,
+                         res=T["rres" + sfx][0].cpu().numpy())
+        assert_bitexact(T["out" + sfx].cpu(), torch.from_numpy(ref), "flow_out" + sfx)
+
+
+def test_frame_tfact_reduced_end_to_end():
+    """The t-factored stack with the refine head at 128x192, three timesteps.
+
+    Teacher-forced, every stage matches (convs on all pixels, FiLM and the
+    refine pair to parity, flow-out bytes exactly).  End to end against the
+    oracle's stack the bytes are compared statistically, as for frame_out, with
+    one more noise source: the fp32 residual comes out of three fp16-stored
+    convs (relative noise ~2^-11 per store, variance-preserving weights) and
+    2 sigmoid - 1 (slope <= 1/2), so it differs by a few 1e-3, which moves a
+    byte by at most about 1 on top of the warp's moves."""
+    ts = (0.25, 0.5, 0.75)
+    net = N.frame_tfact_net(h=128, w=192, ts=ts)
+    outs = run_graph(net)
+    assert len(outs) == 3 and all(tuple(o.shape) == (128, 192, 4) for o in outs)
+    assert check_layers(net, samples=10**6) == 8 + 3 * 5
+    _tfact_stages(net, ts, 128, 192)
+    f0, f1 = net.inputs["frame0"].cpu().numpy(), net.inputs["frame1"].cpu().numpy()
+    refs = M.frame_tfact(f0, f1, ts)
+    for i, (y, ref) in enumerate(zip(outs, refs)):
+        got = y.cpu().numpy()
+        assert (got[..., 3] == 255).all()
+        d = np.abs(got[..., :3].astype(np.int32) - ref[..., :3].astype(np.int32))
+        print(f"frame_tfact t={ts[i]}: exact {np.mean(d == 0):.4f}, within 1 "
+              f"{np.mean(d <= 1):.4f}, mean {d.mean():.4f}, max {d.max()}")
+        assert d.max() <= 6 and np.mean(d <= 1) >= 0.98 and d.mean() <= 0.6, \
+            (ts[i], np.mean(d == 0), np.mean(d <= 1), d.mean(), d.max())
+    # different timesteps give different frames
+    assert not torch.equal(outs[0], outs[2])
+
+
 def test_backbone_reduced_end_to_end():
     net = N.backbone_net(n=1, h=128, w=160)
     outs = run_graph(net)
@@ -135,6 +188,8 @@ def test_backbone_csp_reduced_end_to_end():
 
 # ------------------------------------------------------------------ full size, per layer
 def _sample_pixels(n, oh, ow, k, rng):
+    if k >= n * oh * ow:  # every pixel
+        return [(b, y, x) for b in range(n) for y in range(oh) for x in range(ow)]
     pts = {(0, 0, 0), (n - 1, oh - 1, ow - 1), (0, oh - 1, 0), (n - 1, 0, ow - 1)}
     while len(pts) < k:
         pts.add((int(rng.integers(n)), int(rng.integers(oh)), int(rng.integers(ow))))
@@ -217,3 +272,14 @@ def test_frame_full_size_layers():
     assert_parity(T["tmp8"], ref, torch.float16, "deconv")
     ref = O.resize2d(to64(T["tmp8"]), O.BILINEAR, 1088, 1920, layout=O.NCHW)
     assert_parity(flow, ref, torch.float16, "bilinear x8")
+
+
+def test_frame_tfact_full_size_layers():
+    """1088x1920, three timesteps: the 23 convs on sampled pixels, the other
+    stages on whole maps, teacher-forced."""
+    ts = (0.25, 0.5, 0.75)
+    net = N.frame_tfact_net(ts=ts)
+    outs = run_graph(net)
+    assert [tuple(o.shape) for o in outs] == [(1088, 1920, 4)] * 3
+    assert check_layers(net, samples=32) == 8 + 3 * 5
+    _tfact_stages(net, ts, 1088, 1920)

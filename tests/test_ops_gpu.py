@@ -473,6 +473,103 @@ def test_flow_out_extremes_bitexact(flow, mask_std):
     assert_bitexact(y.cpu(), torch.from_numpy(ref), f"flow_out extremes {flow} {mask_std}")
 
 
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("hw", [(8, 8), (64, 96), (1088, 1920)])
+def test_flow_out_refine_residual_bitexact(dt, hw):
+    """With the refine residual (x4 bilinear upsample added before the clamp),
+    every byte still equals the binary32 oracle's."""
+    h, w = hw
+    t, f0, f1 = _flow_inputs(h, w, dt, seed=23)
+    res = G.tensor(23, "flow.res", (3, h // 4, w // 4), "uniform", -0.4, 0.4)
+    y = A.frame_flow_out(t.cuda(), f0.cuda(), f1.cuda(), refine_res=res.cuda())
+    torch.cuda.synchronize()
+    ref = O.flow_out(t.float().numpy(), f0.numpy(), f1.numpy(), res=res.numpy())
+    assert_bitexact(y.cpu(), torch.from_numpy(ref), f"flow_out+res {dt} {hw}")
+    # a residual moves bytes: the frame differs from the one without it
+    y0 = A.frame_flow_out(t.cuda(), f0.cuda(), f1.cuda())
+    assert not torch.equal(y0, y)
+
+
+# ---------------------------------------------------------------- t-factored stack (NEXT-3)
+def _prep_bound(h, w, flow):
+    """Refine prep in fp32 against the fp64 oracle.  Every value is a bilinear
+    (continuous, slope <= 1 per pixel for [0, 1] planes) function of tap
+    positions that fp32 carries with an absolute error of a few ulp of the
+    largest coordinate (max(h, w) + 8 * flow pixels); the flow planes are
+    scaled down by 80.  So 8 ulp of that coordinate, plus fp32 rounding of
+    the results themselves, bounds the difference."""
+    return 8 * (max(h, w) + 8 * flow) * 2.0 ** -24 + 1e-6
+
+
+@pytest.mark.parametrize("dt,out", [("f32", "f32"), ("f16", "f16"), ("bf16", "bf16"),
+                                    ("f16", "f32")])
+@pytest.mark.parametrize("hw", [(8, 8), (64, 96), (136, 200)])
+def test_refine_prep(dt, out, hw):
+    h, w = hw
+    t, f0, f1 = _flow_inputs(h, w, dt, seed=24)
+    y = A.frame_refine_prep(t.cuda(), f0.cuda(), f1.cuda(), out_dtype=TDT[out])
+    torch.cuda.synchronize()
+    ref = O.refine_prep(t.double().numpy(), f0.numpy(), f1.numpy())
+    assert tuple(y.shape) == (11, h // 4, w // 4)
+    if out == "f32":
+        err = np.abs(to64(y) - ref).max()
+        assert err <= _prep_bound(h, w, 3.0), (hw, err)
+    else:
+        assert_parity(y, ref, TDT[out], f"refine_prep {dt}->{out} {hw}")
+
+
+def test_refine_prep_full_size():
+    """1088x1920 (the workload's size), fp16 in and out, on every value."""
+    h, w = 1088, 1920
+    t, f0, f1 = _flow_inputs(h, w, "f16", seed=25)
+    y = A.frame_refine_prep(t.cuda(), f0.cuda(), f1.cuda(), out_dtype=torch.float16)
+    torch.cuda.synchronize()
+    ref = O.refine_prep(t.double().numpy(), f0.numpy(), f1.numpy())
+    assert_parity(y, ref, torch.float16, "refine_prep full")
+    y32 = A.frame_refine_prep(t.cuda(), f0.cuda(), f1.cuda(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    err = np.abs(to64(y32) - ref).max()
+    assert err <= _prep_bound(h, w, 3.0), err
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("c,hh,hw", [(32, 272, 480), (11, 7, 9), (70, 33, 65), (1, 1, 1),
+                                     (4, 1, 37), (64, 40, 1)])
+def test_refine_out(dt, c, hh, hw):
+    """Replicate-padded 3x3 C -> 3, fp32 accumulation and output; sizes off the
+    32x8 block, a channel count across the 64-channel weight chunks, 1-pixel
+    rows and columns where every tap clamps."""
+    x = G.tensor(26, f"ro.x{c}", (c, hh, hw), "normal", dtype=DT[dt])
+    wt = G.conv_weight(26, f"ro{c}", 3, c, 3, 3, G.NCHW, G.F32)
+    b = G.conv_bias(26, f"ro{c}", 3)
+    y = A.frame_refine_out(x.cuda(), wt.cuda(), b.cuda())
+    torch.cuda.synchronize()
+    ref = O.refine_out(to64(x), to64(wt), to64(b))
+    assert_parity(y, ref, torch.float32, f"refine_out {dt} {c}x{hh}x{hw}")
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("t", [0.0, 0.5, 1.0])
+@pytest.mark.parametrize("c,n,hn", [(240, 68 * 120, 64), (3, 1, 1), (17, 1000, 5)])
+def test_film(dt, t, c, n, hn):
+    x = G.tensor(27, f"film.x{c}", (c, n), "normal", dtype=DT[dt])
+    prm = G.film_mlp(27, f"film{c}", c, hn)
+    y = A.film(x.cuda(), t, *[p.cuda() for p in prm])
+    torch.cuda.synchronize()
+    ref = O.film(to64(x), t, *[to64(p) for p in prm])
+    assert_parity(y, ref, TDT[dt], f"film {dt} t={t} {c}x{n}")
+
+
+def test_film_in_place():
+    c, n = 64, 4096
+    x = G.tensor(28, "film.xi", (c, n), "normal", dtype=G.F16).cuda()
+    prm = [p.cuda() for p in G.film_mlp(28, "filmi", c, 32)]
+    y = A.film(x, 0.3, *prm)
+    A.film(x, 0.3, *prm, out=x)
+    torch.cuda.synchronize()
+    assert torch.equal(x, y)
+
+
 # ---------------------------------------------------------------- concat folded into the conv (NEXT-2)
 CAT_CASES = [
     # name, n, h, w, c_a, c_b, cout, k, s, p, act, res
