@@ -241,8 +241,11 @@ def run_ours(args, rank, world, local_rank):
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def flush():
-        flush_buf.add_(1)  # read + write of a buffer 4x the L2, on torch's stream
-        torch.cuda.current_stream().synchronize()
+        # read + write of a buffer 4x the L2, enqueued on the launching stream so
+        # it completes after the previous step and before the next start event
+        # (a flush on another stream would overlap the previous step's tail)
+        with torch.cuda.stream(stream):
+            flush_buf.add_(1)
 
     # one eager pass (checks every call), then one CUDA graph per section
     with torch.cuda.stream(stream):
