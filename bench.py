@@ -93,10 +93,17 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        # the timed region starts only once samples are flowing
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -307,7 +314,9 @@ def run_ours(args, rank, world, local_rank):
                 "launches_per_step": len(ig),
                 "flops_per_launch": ig_flops / max(1, len(ig)),
                 "avg_launch_us": 1e6 * ig_s / max(1, len(ig)),
-                "share_of_step": round(ig_s / (total / args.steps / 1), 4) if world == 1 else None}
+                # share of the per-op (serialised) time; the step itself overlaps
+                # consecutive launches, so it is shorter than the per-op sum
+                "share_of_ops": round(ig_s / sum(r["s"] for r in rows), 4)}
 
     # ------------------------------------------------ end to end through host buffers
     e2e = None
@@ -438,7 +447,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="backbone",
