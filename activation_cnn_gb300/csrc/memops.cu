@@ -482,28 +482,56 @@ constexpr int kDeconvCoBlock = 8;
 // 3x3 input neighbourhood of (a, b) -- rows a (ky = 1) and a - 1 (ky = 3) for
 // py = 0, rows a + 1 (ky = 0) and a (ky = 2) for py = 1, the same along x --
 // so one thread per input pixel accumulates the 2 x 2 outputs it owns.  A
-// block covers 32 input pixels of one row and up to 8 output channels; its 16
-// warps split C_in (warp g takes ci = g, g + 16, ...) and add their partial
-// sums through shared memory in warp order.  A (ci, co) pair's 16 taps are
-// one 64-byte row of the weight, read as four 16-byte vectors (the same
-// address across the warp: a broadcast).
-constexpr int kDeconvWarps = 16;
+// block covers 32 input pixels of one row and up to 8 output channels; its 8
+// warps split C_in (warp g takes ci = g, g + 8, ...) and add their partial
+// sums through shared memory in warp order.  Per channel a lane loads its own
+// column of the three rows (issued one channel ahead of the arithmetic); the
+// left and right columns come from the neighbouring lanes by shuffles, and
+// lanes 0 and 31 load the two columns beyond the span.
+// The weights of the block's output channels are staged in shared memory 64
+// input channels at a time; a (ci, co) pair's 16 taps are four 16-byte
+// broadcast reads.
+constexpr int kDeconvWarps = 8;
+constexpr int kDeconvChunk = 64;  // input channels per staged weight chunk
 
 template <typename Ti, typename To>
-__global__ void __launch_bounds__(32 * kDeconvWarps, 2) deconv4s2_kernel(
+__global__ void __launch_bounds__(32 * kDeconvWarps) deconv4s2_kernel(
     const Ti* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
     const float* __restrict__ alpha, To* __restrict__ y, int layout, int N, int CI, int CO, int H,
     int W, int act) {
     griddep_wait();  // inputs may come from the previous kernel on the stream
     constexpr int CB = kDeconvCoBlock;
-    extern __shared__ float red[];  // [warp][lane][4 * nco + 1]
+    extern __shared__ float4 dsm[];  // weight chunk [ci][j][4] float4, then partial sums
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles_x = (W + 31) / 32;
     const int a = (blockIdx.x / tiles_x) % H, n = (blockIdx.x / tiles_x) / H;
-    const int b = (blockIdx.x % tiles_x) * 32 + lane;
+    const int b0 = (blockIdx.x % tiles_x) * 32;
+    const int b = b0 + lane;
     const int co0 = blockIdx.y * CB;
     const int nco = min(CB, CO - co0);
     const int rs = 4 * nco + 1;
+    float4* sw = dsm;                                            // kDeconvChunk * nco * 4
+    float* red = reinterpret_cast<float*>(dsm + kDeconvChunk * nco * 4);  // [warp][lane][rs]
+    // this lane's own column and its halo column (lanes 0 and 31 only)
+    const int hxc = lane == 0 ? b0 - 1 : b0 + 32;
+    const bool own_ok = b < W;
+    const bool halo_ok = (lane == 0 || lane == 31) && hxc >= 0 && hxc < W;
+    bool row_ok[3];
+#pragma unroll
+    for (int dy = 0; dy < 3; ++dy) row_ok[dy] = a - 1 + dy >= 0 && a - 1 + dy < H;
+    // element strides: along a row, from one channel to the next, between rows
+    const int64_t sx = layout == ACNN_NHWC ? CI : 1;
+    const int64_t sc = layout == ACNN_NHWC ? 1 : (int64_t)H * W;
+    const int64_t sy = layout == ACNN_NHWC ? (int64_t)W * CI : W;
+    const Ti* xrow = x + act_index(layout, CI, H, W, n, 0, a - 1, 0);  // row a - 1, channel 0
+    auto load = [&](int ci, float (&own)[3], float (&halo)[3]) {
+#pragma unroll
+        for (int dy = 0; dy < 3; ++dy) {
+            const Ti* r = xrow + dy * sy + ci * sc;
+            own[dy] = (row_ok[dy] && own_ok) ? to_f32(r[b * sx]) : 0.0f;
+            halo[dy] = (row_ok[dy] && halo_ok) ? to_f32(r[hxc * sx]) : 0.0f;
+        }
+    };
     float acc[2][2][CB];
 #pragma unroll
     for (int py = 0; py < 2; ++py)
@@ -511,27 +539,37 @@ __global__ void __launch_bounds__(32 * kDeconvWarps, 2) deconv4s2_kernel(
         for (int px = 0; px < 2; ++px)
 #pragma unroll
             for (int j = 0; j < CB; ++j) acc[py][px][j] = 0.0f;
-    if (b < W) {
-        for (int ci = warp; ci < CI; ci += kDeconvWarps) {
+    float own[3] = {0.0f, 0.0f, 0.0f}, halo[3] = {0.0f, 0.0f, 0.0f};
+    if (warp < CI) load(warp, own, halo);
+    for (int c0 = 0; c0 < CI; c0 += kDeconvChunk) {
+        const int nc = min(kDeconvChunk, CI - c0);
+        __syncthreads();  // the previous chunk is consumed
+        for (int i = threadIdx.x; i < nc * nco * 4; i += 32 * kDeconvWarps) {
+            const int cc = i / (nco * 4), r = i - cc * nco * 4;  // r = j * 4 + ky
+            sw[i] = __ldg(reinterpret_cast<const float4*>(w + ((long long)(c0 + cc) * CO + co0) * 16) + r);
+        }
+        __syncthreads();
+        for (int cc = warp; cc < nc; cc += kDeconvWarps) {
+            const int ci = c0 + cc;
+            float own_n[3] = {0.0f, 0.0f, 0.0f}, halo_n[3] = {0.0f, 0.0f, 0.0f};
+            if (ci + kDeconvWarps < CI) load(ci + kDeconvWarps, own_n, halo_n);
             float nb[3][3];  // x at rows a-1..a+1, cols b-1..b+1 (zero outside)
 #pragma unroll
-            for (int dy = 0; dy < 3; ++dy)
-#pragma unroll
-                for (int dx = 0; dx < 3; ++dx) {
-                    const int iy = a - 1 + dy, ix = b - 1 + dx;
-                    nb[dy][dx] = (iy >= 0 && iy < H && ix >= 0 && ix < W)
-                                     ? to_f32(x[act_index(layout, CI, H, W, n, ci, iy, ix)])
-                                     : 0.0f;
-                }
+            for (int dy = 0; dy < 3; ++dy) {
+                const float left = __shfl_up_sync(0xffffffffu, own[dy], 1);
+                const float right = __shfl_down_sync(0xffffffffu, own[dy], 1);
+                nb[dy][0] = lane == 0 ? halo[dy] : left;
+                nb[dy][1] = own[dy];
+                nb[dy][2] = lane == 31 ? halo[dy] : right;
+            }
+            const float4* wc = sw + cc * nco * 4;
 #pragma unroll
             for (int j = 0; j < CB; ++j) {
                 if (j >= nco) break;
-                const float4* wk =
-                    reinterpret_cast<const float4*>(w + ((long long)ci * CO + co0 + j) * 16);
                 float wt[4][4];  // [ky][kx]
 #pragma unroll
                 for (int ky = 0; ky < 4; ++ky) {
-                    const float4 v = __ldg(wk + ky);
+                    const float4 v = wc[j * 4 + ky];
                     wt[ky][0] = v.x, wt[ky][1] = v.y, wt[ky][2] = v.z, wt[ky][3] = v.w;
                 }
 #pragma unroll
@@ -550,6 +588,11 @@ __global__ void __launch_bounds__(32 * kDeconvWarps, 2) deconv4s2_kernel(
                                 acc[py][px][j] = fmaf(nb[dy][dx], wt[ky][kx], acc[py][px][j]);
                             }
             }
+#pragma unroll
+            for (int dy = 0; dy < 3; ++dy) {
+                own[dy] = own_n[dy];
+                halo[dy] = halo_n[dy];
+            }
         }
     }
     float* mine = red + ((size_t)warp * 32 + lane) * rs;
@@ -566,7 +609,7 @@ __global__ void __launch_bounds__(32 * kDeconvWarps, 2) deconv4s2_kernel(
     for (int i = threadIdx.x; i < 32 * 4 * nco; i += 32 * kDeconvWarps) {
         const int l = i / (4 * nco), r = i - l * 4 * nco;
         const int pp = r / nco, j = r - pp * nco;
-        const int bb = (blockIdx.x % tiles_x) * 32 + l;
+        const int bb = b0 + l;
         if (bb >= W) continue;
         float v = bias ? bias[co0 + j] : 0.0f;
         for (int g = 0; g < kDeconvWarps; ++g) v += red[((size_t)g * 32 + l) * rs + r];
@@ -888,10 +931,14 @@ cudaError_t deconv_typed(const acnn_conv_desc& d, int oh, int ow, const void* x,
         const int cob = (d.c_out + kDeconvCoBlock - 1) / kDeconvCoBlock;
         if (rows <= 0x7fffffffLL && cob <= 65535) {
             const int nco = d.c_out < kDeconvCoBlock ? d.c_out : kDeconvCoBlock;
-            const size_t smem = (size_t)kDeconvWarps * 32 * (4 * nco + 1) * sizeof(float);
-            static bool attr = false;  // per instantiation: the largest partial-sum buffer
+            auto smem_for = [](int c) {  // weight chunk + partial sums
+                return (size_t)kDeconvChunk * c * 64 +
+                       (size_t)kDeconvWarps * 32 * (4 * c + 1) * sizeof(float);
+            };
+            const size_t smem = smem_for(nco);
+            static bool attr = false;  // per instantiation: the largest buffer
             if (!attr) {
-                const size_t mx = (size_t)kDeconvWarps * 32 * (4 * kDeconvCoBlock + 1) * 4;
+                const size_t mx = smem_for(kDeconvCoBlock);
                 cudaFuncSetAttribute(deconv4s2_kernel<Ti, To>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx);
                 attr = true;
