@@ -69,9 +69,18 @@ __device__ __forceinline__ float up(const FlowIn<T>& in, int c, float sx, float 
     return mixf(top, bot, fy);
 }
 
+// byte / 255 for every byte value, correctly rounded (one division each),
+// filled by the block before use: a shared-memory read per tap channel in
+// place of a division
+__device__ __forceinline__ void fill_unorm_lut(float* lut) {
+    for (int i = threadIdx.y * blockDim.x + threadIdx.x; i < 256; i += blockDim.x * blockDim.y)
+        lut[i] = __fdiv_rn(__uint2float_rn((unsigned)i), 255.0f);
+    __syncthreads();
+}
+
 // B, G, R of an RGBA8 frame at pixel-space (px, py), bilinear, clamped taps
-__device__ __forceinline__ void warp_bgr(const uint32_t* __restrict__ f, int H, int W, float px,
-                                         float py, float (&bgr)[3]) {
+__device__ __forceinline__ void warp_bgr(const uint32_t* __restrict__ f, const float* lut, int H,
+                                         int W, float px, float py, float (&bgr)[3]) {
     const float fx0 = floorf(px), fy0 = floorf(py);
     const float fx = __fsub_rn(px, fx0), fy = __fsub_rn(py, fy0);
     // clamp in float first: a large flow can put the tap beyond the int range
@@ -84,7 +93,7 @@ __device__ __forceinline__ void warp_bgr(const uint32_t* __restrict__ f, int H, 
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
         const int sh = 8 * (2 - k);  // B, G, R = bytes 2, 1, 0
-        auto ch = [&](uint32_t p) { return __fdiv_rn(__uint2float_rn((p >> sh) & 255u), 255.0f); };
+        auto ch = [&](uint32_t p) { return lut[(p >> sh) & 255u]; };
         bgr[k] = mixf(mixf(ch(p00), ch(p01), fx), mixf(ch(p10), ch(p11), fx), fy);
     }
 }
@@ -95,6 +104,8 @@ __global__ void __launch_bounds__(256) flow_out_kernel(const T* __restrict__ tmp
                                                        const uint32_t* __restrict__ f1,
                                                        const float* __restrict__ res,
                                                        uint32_t* __restrict__ out, int H, int W) {
+    __shared__ float lut[256];
+    fill_unorm_lut(lut);
     griddep_wait();  // inputs may come from the previous kernel on the stream
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
@@ -106,8 +117,8 @@ __global__ void __launch_bounds__(256) flow_out_kernel(const T* __restrict__ tmp
     const float u1 = __fmul_rn(up(in, 2, sx, sy), 8.0f), v1 = __fmul_rn(up(in, 3, sx, sy), 8.0f);
     const float m = __fdiv_rn(1.0f, __fadd_rn(1.0f, flow_exp(-up(in, 4, sx, sy))));
     float w0[3], w1[3];
-    warp_bgr(f0, H, W, __fadd_rn((float)x, u0), __fadd_rn((float)y, v0), w0);
-    warp_bgr(f1, H, W, __fadd_rn((float)x, u1), __fadd_rn((float)y, v1), w1);
+    warp_bgr(f0, lut, H, W, __fadd_rn((float)x, u0), __fadd_rn((float)y, v0), w0);
+    warp_bgr(f1, lut, H, W, __fadd_rn((float)x, u1), __fadd_rn((float)y, v1), w1);
     const float om = __fsub_rn(1.0f, m);
     // refine residual (t-factored stack): x4 bilinear upsample, added before the clamp
     float rv[3] = {0.0f, 0.0f, 0.0f};
@@ -150,6 +161,8 @@ __global__ void __launch_bounds__(256) refine_prep_kernel(const T* __restrict__ 
                                                           const uint32_t* __restrict__ f0,
                                                           const uint32_t* __restrict__ f1,
                                                           To* __restrict__ out, int H, int W) {
+    __shared__ float lut[256];
+    fill_unorm_lut(lut);
     griddep_wait();  // inputs may come from the previous kernel on the stream
     const int QH = H / 4, QW = W / 4;
     const int hx = blockIdx.x * blockDim.x + threadIdx.x;
@@ -170,8 +183,8 @@ __global__ void __launch_bounds__(256) refine_prep_kernel(const T* __restrict__ 
             const float u1 = __fmul_rn(up(in, 2, gx, gy), 8.0f), v1 = __fmul_rn(up(in, 3, gx, gy), 8.0f);
             acc[6] += __fdiv_rn(1.0f, __fadd_rn(1.0f, flow_exp(-up(in, 4, gx, gy))));
             float w0[3], w1[3];
-            warp_bgr(f0, H, W, __fadd_rn((float)X, u0), __fadd_rn((float)Y, v0), w0);
-            warp_bgr(f1, H, W, __fadd_rn((float)X, u1), __fadd_rn((float)Y, v1), w1);
+            warp_bgr(f0, lut, H, W, __fadd_rn((float)X, u0), __fadd_rn((float)Y, v0), w0);
+            warp_bgr(f1, lut, H, W, __fadd_rn((float)X, u1), __fadd_rn((float)Y, v1), w1);
 #pragma unroll
             for (int k = 0; k < 3; ++k) {
                 acc[k] += w0[k];
@@ -347,7 +360,9 @@ cudaError_t launch_refine_out(int c, int hh, int hw, const void* x, int dtype, c
 cudaError_t launch_film(int c, int n, int dtype, const void* x, float t, const float* w0,
                         const float* b0, int hn, const float* w2, const float* b2, void* y,
                         cudaStream_t s) {
-    const int bx = (n + 255) / 256 < 64 ? (n + 255) / 256 : 64;
+    // about eight elements per thread: each block also evaluates its channel's
+    // two MLP outputs, so fewer, longer blocks per channel
+    const int bx = (n + 2047) / 2048 < 64 ? (n + 2047) / 2048 : 64;
     const dim3 grid(bx, c);
     switch (dtype) {
     case ACNN_F32:
