@@ -122,6 +122,31 @@ def test_conv_tensor_multi_tile_epilogue(shape, act, res_mode):
     assert_parity(y, ref, torch.bfloat16, f"multi-tile {shape}")
 
 
+@pytest.mark.parametrize("n,hw,cin,cout,k", [(80, 320, 256, 256, 1), (320, 320, 64, 64, 3)])
+def test_conv_tensor_near_index_limit(n, hw, cin, cout, k):
+    """Output maps of just under 2^31 elements (4.3 GB of bf16 each way): one
+    seeded 320x320 image repeated n times, so every image's output equals the
+    first's; sampled pixels across all images, the last pixel included, against
+    the oracle on that one image (64-bit offsets in every load and store)."""
+    name = f"big{k}"
+    x1 = G.tensor(12, name + ".x", (1, hw, hw, cin), "normal", dtype=G.BF16)
+    wt = G.conv_weight(12, name, cout, cin, k, k, G.NHWC, G.BF16)
+    b = G.conv_bias(12, name, cout)
+    assert n * hw * hw * cout < 2**31 and n * hw * hw * cout > 2**31 - 2**28
+    x = x1.cuda().expand(n, hw, hw, cin).contiguous()
+    y = A.conv2d_fused(x, wt.cuda(), b.cuda(), stride=1, pad=k // 2, act=A.ACT_RELU)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    pts = [(n - 1, hw - 1, hw - 1), (0, 0, 0), (n // 2, 0, hw - 1), (n - 1, 0, 0)]
+    pts += [(int(rng.integers(n)), int(rng.integers(hw)), int(rng.integers(hw))) for _ in range(60)]
+    got = torch.stack([y[i, oy, ox] for i, oy, ox in pts]).cpu()
+    ref = O.conv2d_points(to64(x1), to64(wt), to64(b), [(0, oy, ox) for _, oy, ox in pts],
+                          stride=1, pad=k // 2, act=A.ACT_RELU)
+    del x, y
+    torch.cuda.empty_cache()
+    assert_parity(got, ref, torch.bfloat16, name)
+
+
 def test_conv_tensor_no_bias():
     y, ref = conv_case("nobias", 1, 9, 9, 64, 64, 1, 1, 0, "f16", bias=False)
     assert_parity(y, ref, torch.float16)
