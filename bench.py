@@ -417,6 +417,13 @@ def run_ours(args, rank, world, local_rank):
                 # share of the per-op (serialised) time; the step itself overlaps
                 # consecutive launches, so it is shorter than the per-op sum
                 "share_of_ops": round(ig_s / sum(r["s"] for r in rows), 4)}
+    # each conv launch against its own roof, max(FLOPs / tensor peak, bytes /
+    # HBM peak): the fraction of the attainable time the launches achieve
+    ideal = sum(max(r["flops"] / (peak * 1e12), r["bytes"] / (pk["hbm"] * 1e9)) for r in ig)
+    roofline["attainable"] = {"ideal_us_per_step": round(ideal * 1e6, 1),
+                              "measured_us_per_step": round(ig_s * 1e6, 1),
+                              "frac": round(ideal / ig_s, 4) if ig_s > 0 else None,
+                              "per_launch_roof": "max(flops / tensor peak, bytes / hbm peak)"}
 
     # ------------------------------------------------ end to end through host buffers
     e2e = None
