@@ -38,6 +38,8 @@ EXPORTS = (
     "acnn_conv2d_fused", "acnn_conv2d_out_hw", "acnn_conv2d_workspace_size", "acnn_conv2d_path",
     "acnn_pool2d", "acnn_resize2d", "acnn_concat", "acnn_deconv2d", "acnn_frame_prep_quarter",
     "acnn_frame_flow_out", "acnn_frame_refine_prep", "acnn_frame_refine_out", "acnn_film",
+    "acnn_conv2d_prepacked_size", "acnn_conv2d_prepack", "acnn_conv2d_prepacked_workspace_size",
+    "acnn_conv2d_fused_prepacked",
     "acnn_status_string", "acnn_last_device_status", "acnn_set_wait_budget",
     "acnn_section_begin", "acnn_section_end", "acnn_section_launch", "acnn_section_destroy",
     "acnn_device_sm_count", "acnn_conv2d_fused_noalloc", "acnn_conv2d_plan",
@@ -77,6 +79,13 @@ def lib() -> ctypes.CDLL:
                                              ctypes.c_size_t, _P]
         L.acnn_conv2d_workspace_size.argtypes = [D]
         L.acnn_conv2d_workspace_size.restype = ctypes.c_size_t
+        L.acnn_conv2d_prepacked_size.argtypes = [D]
+        L.acnn_conv2d_prepacked_size.restype = ctypes.c_size_t
+        L.acnn_conv2d_prepacked_workspace_size.argtypes = [D]
+        L.acnn_conv2d_prepacked_workspace_size.restype = ctypes.c_size_t
+        L.acnn_conv2d_prepack.argtypes = [D, _P, _P, _P]
+        L.acnn_conv2d_fused_prepacked.argtypes = [D, _P, _P, _P, _P, _P, _I, _I, _P, _P,
+                                                  ctypes.c_size_t, _P]
         L.acnn_conv2d_path.argtypes = [D]
         L.acnn_pool2d.argtypes = [_I] * 10 + [_P, _P, _P]
         L.acnn_resize2d.argtypes = [_I] * 10 + [_P, _P, _P]
@@ -148,6 +157,27 @@ def acnn_conv2d_out_hw(desc):
 
 def acnn_conv2d_workspace_size(desc) -> int:
     return lib().acnn_conv2d_workspace_size(ctypes.byref(desc))
+
+
+def acnn_conv2d_prepacked_size(desc) -> int:
+    return lib().acnn_conv2d_prepacked_size(ctypes.byref(desc))
+
+
+def acnn_conv2d_prepacked_workspace_size(desc) -> int:
+    return lib().acnn_conv2d_prepacked_workspace_size(ctypes.byref(desc))
+
+
+def acnn_conv2d_prepack(desc, w, w_packed, stream=None) -> int:
+    return lib().acnn_conv2d_prepack(ctypes.byref(desc), _ptr(w), _ptr(w_packed),
+                                     _stream(stream))
+
+
+def acnn_conv2d_fused_prepacked(desc, x, w_packed, bias, alpha, residual, res_mode, act, y,
+                                workspace, ws_bytes, stream=None) -> int:
+    return lib().acnn_conv2d_fused_prepacked(ctypes.byref(desc), _ptr(x), _ptr(w_packed),
+                                             _ptr(bias), _ptr(alpha), _ptr(residual), res_mode,
+                                             act, _ptr(y), _ptr(workspace), ws_bytes,
+                                             _stream(stream))
 
 
 def acnn_conv2d_plan(desc, ws_bytes):
@@ -290,6 +320,14 @@ def conv2d_fused(x, w, bias=None, *, stride=1, pad=0, act=ACT_NONE, alpha=None, 
                            ws_bytes if workspace is not None else 0, stream)
     check(st, "acnn_conv2d_fused")
     return y
+
+
+def conv2d_prepack(desc, w, stream=None):
+    """The weights of geometry desc in the form the conv kernels read (a uint8
+    device buffer) for conv2d_fused(..., prepacked=True)."""
+    wp = torch.empty(acnn_conv2d_prepacked_size(desc), dtype=torch.uint8, device=w.device)
+    check(acnn_conv2d_prepack(desc, w, wp, stream), "acnn_conv2d_prepack")
+    return wp
 
 
 def conv2d_fused_cat2(x_a, x_b, w, bias=None, *, stride=1, pad=0, act=ACT_NONE, alpha=None,

@@ -230,9 +230,20 @@ int acnn_conv2d_plan(const acnn_conv_desc* d, size_t ws_bytes, int* rows, int* b
     return 0;
 }
 
-int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w, const float* bias,
-                      const float* alpha, const void* residual, int res_mode, int act, void* y,
-                      void* workspace, size_t ws_bytes, acnn_stream_t stream) {
+namespace {
+
+// Bytes of the weight operand as the conv kernels consume it (prepacked form):
+// the packed [c_out, kp] matrix on the packed path, OHWI on the tensor-core
+// paths, the caller's own layout on the direct path.
+size_t prepacked_bytes(const acnn_conv_desc* d, const Route& r) {
+    const size_t es = elem_size(d->dtype);
+    if (r.path == 3) return (size_t)d->c_out * r.g.c_in * es;
+    return (size_t)d->c_out * d->kh * d->kw * d->c_in * es;
+}
+
+int conv_fused_impl(const acnn_conv_desc* d, const void* x, const void* w, bool prepacked,
+                    const float* bias, const float* alpha, const void* residual, int res_mode,
+                    int act, void* y, void* workspace, size_t ws_bytes, acnn_stream_t stream) {
     int st = check_desc(d);
     if (st != ACNN_OK) return st;
     if (act < ACNN_ACT_NONE || act > ACNN_ACT_PRELU || res_mode < ACNN_RES_NONE ||
@@ -250,7 +261,8 @@ int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w, con
         return ACNN_ERR_MISALIGNED;
     const size_t es = elem_size(d->dtype);
     const size_t xb = (size_t)d->n * d->h * d->w * d->c_in * es;
-    const size_t wb = (size_t)d->c_out * d->kh * d->kw * d->c_in * es;
+    const size_t wb = prepacked ? prepacked_bytes(d, route(d, oh, ow))
+                                : (size_t)d->c_out * d->kh * d->kw * d->c_in * es;
     const size_t yb = (size_t)d->n * oh * ow * d->c_out * es;
     if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) ||
         (residual && res_mode != ACNN_RES_NONE && overlaps(y, yb, residual, yb)) ||
@@ -277,9 +289,11 @@ int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w, con
     const Route r = route(d, oh, ow);
     if (r.path == 0) return status_of(launch_direct_conv(a, s));
 
-    // Workspace: [staged x | staged w] (required for NCHW and packed convs), then
-    // split-K partial sums (optional: a smaller remainder selects fewer splits).
-    const size_t stage = r.stage_x + r.stage_w;
+    // Workspace: [staged x | staged w] (required for NCHW and packed convs; no
+    // staged w with prepacked weights), then split-K partial sums (optional: a
+    // smaller remainder selects fewer splits).
+    const size_t stage_w = prepacked ? 0 : r.stage_w;
+    const size_t stage = r.stage_x + stage_w;
     if (!workspace) ws_bytes = 0;
     if (ws_bytes < stage) return ACNN_ERR_WORKSPACE;
     if (ws_bytes > 0 &&
@@ -294,11 +308,12 @@ int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w, con
     if (r.path == 3) {
         // explicit im2col: [n*oh*ow, kp] and [c_out, kp], then a 1x1 GEMM whose
         // epilogue writes y in the caller's layout
-        e = launch_im2col_pack(*d, oh, ow, r.g.c_in, x, ws, w, ws + r.stage_x, s);
+        e = launch_im2col_pack(*d, oh, ow, r.g.c_in, x, ws, prepacked ? nullptr : w,
+                               ws + r.stage_x, s);
         if (e != cudaSuccess) return ACNN_ERR_CUDA;
         a.d = r.g;
         a.x = ws;
-        a.w = ws + r.stage_x;
+        a.w = prepacked ? w : ws + r.stage_x;
         return launch_igemm_conv(a, s);
     }
     if (d->layout == ACNN_NHWC) return launch_igemm_conv(a, s);
@@ -307,13 +322,69 @@ int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w, con
     // implicit GEMM writing NCHW directly.
     e = launch_nchw_to_nhwc(d->n, d->c_in, d->h * d->w, 2, x, ws, s);
     if (e != cudaSuccess) return ACNN_ERR_CUDA;
-    e = launch_nchw_to_nhwc(d->c_out, d->c_in, d->kh * d->kw, 2, w, ws + r.stage_x, s);
-    if (e != cudaSuccess) return ACNN_ERR_CUDA;
+    if (!prepacked) {
+        e = launch_nchw_to_nhwc(d->c_out, d->c_in, d->kh * d->kw, 2, w, ws + r.stage_x, s);
+        if (e != cudaSuccess) return ACNN_ERR_CUDA;
+    }
     a.x = ws;
-    a.w = ws + r.stage_x;
+    a.w = prepacked ? w : ws + r.stage_x;
     a.d.layout = ACNN_NHWC;
     a.out_layout = ACNN_NCHW;
     return launch_igemm_conv(a, s);
+}
+
+}  // namespace
+
+int acnn_conv2d_fused(const acnn_conv_desc* d, const void* x, const void* w, const float* bias,
+                      const float* alpha, const void* residual, int res_mode, int act, void* y,
+                      void* workspace, size_t ws_bytes, acnn_stream_t stream) {
+    return conv_fused_impl(d, x, w, false, bias, alpha, residual, res_mode, act, y, workspace,
+                           ws_bytes, stream);
+}
+
+int acnn_conv2d_fused_prepacked(const acnn_conv_desc* d, const void* x, const void* w_packed,
+                                const float* bias, const float* alpha, const void* residual,
+                                int res_mode, int act, void* y, void* workspace,
+                                size_t ws_bytes, acnn_stream_t stream) {
+    return conv_fused_impl(d, x, w_packed, true, bias, alpha, residual, res_mode, act, y,
+                           workspace, ws_bytes, stream);
+}
+
+size_t acnn_conv2d_prepacked_size(const acnn_conv_desc* d) {
+    int oh, ow;
+    if (check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK) return 0;
+    return prepacked_bytes(d, route(d, oh, ow));
+}
+
+size_t acnn_conv2d_prepacked_workspace_size(const acnn_conv_desc* d) {
+    int oh, ow;
+    if (check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK) return 0;
+    const Route r = route(d, oh, ow);
+    if (r.path == 0) return 0;
+    return r.stage_x + round256(igemm_plan(r.g, oh, ow, SIZE_MAX).part_bytes);
+}
+
+int acnn_conv2d_prepack(const acnn_conv_desc* d, const void* w, void* w_packed,
+                        acnn_stream_t stream) {
+    int st = check_desc(d);
+    if (st != ACNN_OK) return st;
+    int oh, ow;
+    st = conv_out(d, &oh, &ow);
+    if (st != ACNN_OK) return st;
+    if (!w || !w_packed) return ACNN_ERR_NULL_POINTER;
+    if (!aligned16(w) || !aligned16(w_packed)) return ACNN_ERR_MISALIGNED;
+    const Route r = route(d, oh, ow);
+    const size_t wb = (size_t)d->c_out * d->kh * d->kw * d->c_in * elem_size(d->dtype);
+    if (overlaps(w_packed, prepacked_bytes(d, r), w, wb)) return ACNN_ERR_ALIAS;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (r.path == 3)
+        e = launch_weight_pack(*d, r.g.c_in, w, w_packed, s);
+    else if (r.path != 0 && d->layout == ACNN_NCHW)
+        e = launch_nchw_to_nhwc(d->c_out, d->c_in, d->kh * d->kw, 2, w, w_packed, s);
+    else
+        e = cudaMemcpyAsync(w_packed, w, wb, cudaMemcpyDeviceToDevice, s);
+    return status_of(e);
 }
 
 int acnn_conv2d_fused_cat2(const acnn_conv_desc* d, const void* x_a, int c_a, const void* x_b,

@@ -148,6 +148,9 @@ cudaError_t launch_film(int c, int n, int dtype, const void* x, float t, const f
 // im2col pack of x into a [n*oh*ow, kp] matrix and of w into [c_out, kp] (2-byte types)
 cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, const void* x,
                                void* a, const void* w, void* wp, cudaStream_t s);
+// the packed weight operand [c_out, kp] alone (kp >= kh*kw*c_in, zero padded)
+cudaError_t launch_weight_pack(const acnn_conv_desc& d, int kp, const void* w, void* wp,
+                               cudaStream_t s);
 // NCHW -> NHWC activation transpose and OIHW -> OHWI weight transpose (2-byte types)
 cudaError_t launch_nchw_to_nhwc(int n, int c, int hw, int elem_bytes, const void* x, void* y,
                                 cudaStream_t s);

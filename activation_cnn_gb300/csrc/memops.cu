@@ -1043,8 +1043,13 @@ cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, 
         static_cast<const uint16_t*>(x), static_cast<uint16_t*>(a), d.layout, d.h, d.w, d.c_in,
         d.kh, d.kw, d.stride, d.pad, oh, ow, kp, tp, segs);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    launch_pdl(weight_pack_kernel, grid_occ(weight_pack_kernel, (long long)d.c_out * kp, kThreads), kThreads, 0, s, 
+    if (e != cudaSuccess || !w) return e;  // no w: the weights are prepacked
+    return launch_weight_pack(d, kp, w, wp, s);
+}
+
+cudaError_t launch_weight_pack(const acnn_conv_desc& d, int kp, const void* w, void* wp,
+                               cudaStream_t s) {
+    launch_pdl(weight_pack_kernel, grid_occ(weight_pack_kernel, (long long)d.c_out * kp, kThreads), kThreads, 0, s,
         static_cast<const uint16_t*>(w), static_cast<uint16_t*>(wp), d.layout, d.c_out, d.c_in,
         d.kh, d.kw, kp);
     return cudaGetLastError();

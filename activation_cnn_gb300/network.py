@@ -162,22 +162,35 @@ class Builder:
         y = self.buffer(out or spec.name, spec.c_out, spec.oh, spec.ow)
         res = net.tensors[residual] if residual else None
         d = A.conv_desc(x, spec.c_out, spec.k, spec.k, spec.stride, spec.pad, net.layout)
-        ws_bytes = A.acnn_conv2d_workspace_size(d)
+        path = A.acnn_conv2d_path(d)
+        # convs whose weights would be restaged on every call (the packed path,
+        # NCHW convs on the tensor cores) take them prepacked once, here
+        staged = path == 3 or (path in (1, 2) and net.layout == G.NCHW)
+        if staged:
+            wd = A.conv2d_prepack(d, wd)
+            torch.cuda.synchronize()
+            ws_bytes = A.acnn_conv2d_prepacked_workspace_size(d)
+        else:
+            ws_bytes = A.acnn_conv2d_workspace_size(d)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device) if ws_bytes else None
         net.tensors[spec.name + ".ws"] = ws
         res_mode = spec.res_mode if residual else A.RES_NONE
         net.conv_inputs[spec.name] = src
         if residual:
             net.conv_residuals[spec.name] = residual
+        call = A.acnn_conv2d_fused_prepacked if staged else A.acnn_conv2d_fused
 
         def fn(stream, d=d, x=x, wd=wd, bd=bd, ald=ald, res=res, y=y, ws=ws, res_mode=res_mode):
-            A.check(A.acnn_conv2d_fused(d, x, wd, bd, ald, res, res_mode, spec.act, y, ws,
-                                        ws_bytes, stream), spec.name)
+            A.check(call(d, x, wd, bd, ald, res, res_mode, spec.act, y, ws, ws_bytes, stream),
+                    spec.name)
 
         n = net.batch
         byts = (x.numel() + w.numel() + y.numel() + (y.numel() if res is not None else 0)) * \
             self.es + 4 * spec.c_out
-        net.ops.append(Op("conv", self.section, fn, _conv_flops(n, spec), byts, spec.name, spec))
+        # kernels per call: the conv, plus the activation staging (NCHW -> NHWC
+        # copy or im2col pack) of a staged conv
+        net.ops.append(Op("conv", self.section, fn, _conv_flops(n, spec), byts, spec.name, spec,
+                          launches=2 if staged else 1))
         return out or spec.name
 
     def conv_cat(self, src_a, src_b, spec: ConvSpec, residual=None):

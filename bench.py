@@ -162,29 +162,12 @@ def workload_config(name, net, world):
 
 
 def launches_per_step(net):
-    """Kernels of this library launched by one pass of the network.
-
-    A tensor-core conv is one implicit-GEMM launch (a K split reduces inside it;
-    the split's counter reset is a memset, not a kernel), plus the two packing
-    kernels of the explicit-im2col path or the two NCHW->NHWC staging transposes
-    of an NCHW conv; every other op is one."""
-    from activation_cnn_gb300 import acnn as A
-    n = 0
-    for op in net.ops:
-        if op.kind != "conv":
-            n += op.launches
-            continue
-        s = op.spec
-        d = A.ConvDesc(net.batch, s.h, s.w, s.c_in, s.c_out, s.k, s.k, s.stride, s.pad,
-                       net.layout, net.dtype)
-        path = A.acnn_conv2d_path(d)
-        if path == 0:
-            n += 1
-            continue
-        n += 1
-        if path == 3 or net.layout == A.NCHW:
-            n += 2
-    return n
+    """Kernels of this library launched by one pass of the network: each op
+    records its own count (a conv is one implicit-GEMM launch -- a K split
+    reduces inside it, and the split's counter reset is a memset, not a kernel
+    -- plus, for the packed path or an NCHW conv, the activation staging
+    kernel; the weights of those are prepacked once when the network is built)."""
+    return sum(op.launches for op in net.ops)
 
 
 def time_ops(net, stream, steps, flush):

@@ -154,6 +154,36 @@ int acnn_conv2d_path(const acnn_conv_desc* d);
  * depends on the current device's SM count). */
 int acnn_conv2d_plan(const acnn_conv_desc* d, size_t ws_bytes, int* rows, int* bn, int* splits);
 
+/* ---- prepacked weights --------------------------------------------------------
+ * The weights in the form the conv kernels read, made once (the pages convert
+ * their weights once at start-up too), so that a call does not restage them:
+ *   acnn_conv2d_prepacked_size(d)  bytes of the prepacked weight of geometry d
+ *                                  (0 for an invalid d);
+ *   acnn_conv2d_prepack(d, w, w_packed, stream)
+ *                                  w (device, the layout acnn_conv2d_fused takes:
+ *                                  OHWI for NHWC, OIHW for NCHW) -> w_packed
+ *                                  (device, caller-owned, 16-byte aligned, no
+ *                                  overlap with w): the packed [c_out][kp]
+ *                                  matrix (K = kh*kw*c_in in (ky, kx, ci) order,
+ *                                  zero-padded to kp) on path 3, OHWI on paths
+ *                                  1-2, an unchanged copy on path 0;
+ *   acnn_conv2d_prepacked_workspace_size(d)
+ *                                  the workspace of the prepacked call: the
+ *                                  staged activation only, plus split-K sums;
+ *   acnn_conv2d_fused_prepacked(...)
+ *                                  acnn_conv2d_fused with w_packed in place of
+ *                                  w: same arguments, results and errors.
+ * A prepacked weight is valid for the geometry it was packed for only.
+ */
+size_t acnn_conv2d_prepacked_size(const acnn_conv_desc* d);
+int acnn_conv2d_prepack(const acnn_conv_desc* d, const void* w, void* w_packed,
+                        acnn_stream_t stream);
+size_t acnn_conv2d_prepacked_workspace_size(const acnn_conv_desc* d);
+int acnn_conv2d_fused_prepacked(const acnn_conv_desc* d, const void* x, const void* w_packed,
+                                const float* bias, const float* alpha, const void* residual,
+                                int res_mode, int act, void* y, void* workspace,
+                                size_t ws_bytes, acnn_stream_t stream);
+
 /* ---- conv2d_fused without caller workspace ----------------------------------
  * No counterpart on the pages: an addition for callers that cannot allocate
  * device memory where they run a conv -- e.g. a plugin inside a framework

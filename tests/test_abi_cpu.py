@@ -125,6 +125,16 @@ def test_companions_reject_before_launch(A):
     assert A.acnn_frame_flow_out(16, 16, X, 1, W, Y, None, W + 512, 0) == 6
     assert A.acnn_frame_flow_out(16, 16, X, 1, W, Y, R + 4, Y + (1 << 20), 0) == 4  # residual
     assert A.acnn_frame_flow_out(16, 16, X, 1, W, Y, Y + (1 << 20), Y + (1 << 20), 0) == 6
+    # prepacked weights: pointers, alignment, aliasing, geometry
+    d3 = desc(A, kh=3, kw=3, stride=1, pad=1)
+    assert A.acnn_conv2d_prepack(d3, None, Y, 0) == 1
+    assert A.acnn_conv2d_prepack(d3, W, W + 16, 0) == 6
+    assert A.acnn_conv2d_prepack(d3, W + 4, Y, 0) == 4
+    bad = desc(A, kh=3, kw=3, stride=0, pad=1)
+    assert A.acnn_conv2d_prepack(bad, W, Y, 0) != 0
+    assert A.acnn_conv2d_prepacked_size(bad) == 0
+    assert A.acnn_conv2d_fused_prepacked(d3, X, None, None, None, None, 0, 1, Y, None, 0, 0) == 1
+    assert A.acnn_conv2d_fused_prepacked(d3, X, W, None, None, None, 0, 9, Y, None, 0, 0) == 7
     # t-factored stack: refine prep / refine out / FiLM argument checks
     assert A.acnn_frame_refine_prep(12, 16, X, 1, W, Y, 1, R, 0) == 2
     assert A.acnn_frame_refine_prep(16, 16, X, 1, W, Y, 5, R, 0) == 7

@@ -147,6 +147,44 @@ def test_conv_tensor_near_index_limit(n, hw, cin, cout, k):
     assert_parity(got, ref, torch.bfloat16, name)
 
 
+PREPACK_CASES = [
+    # name, layout, dtype, n, h, w, cin, cout, k, s, p, act
+    ("nchw_3x3", G.NCHW, "f16", 1, 17, 30, 120, 240, 3, 1, 1, A.ACT_PRELU),
+    ("nchw_packed_7", G.NCHW, "f16", 1, 36, 52, 7, 120, 3, 2, 1, A.ACT_PRELU),
+    ("nhwc_packed_rgb", G.NHWC, "bf16", 2, 40, 48, 3, 32, 3, 2, 1, A.ACT_RELU),
+    ("nhwc_3x3", G.NHWC, "bf16", 2, 13, 17, 64, 64, 3, 1, 1, A.ACT_SILU),
+    ("nchw_1x1", G.NCHW, "f16", 1, 9, 15, 240, 64, 1, 1, 0, A.ACT_RELU),
+    ("f32_direct", G.NHWC, "f32", 1, 12, 12, 16, 32, 3, 1, 1, A.ACT_RELU),
+]
+
+
+@pytest.mark.parametrize("case", PREPACK_CASES, ids=[c[0] for c in PREPACK_CASES])
+def test_conv_prepacked_equals_plain(case):
+    """Prepacked weights give the same bits as the per-call staging, on every
+    path (direct, tiled, im2col, packed; NHWC and NCHW), and match the oracle."""
+    name, layout, dt, n, h, w, cin, cout, k, s, p, act = case
+    seed = 13
+    x = G.tensor(seed, name + ".x", G.activation_shape(layout, n, cin, h, w), "normal",
+                 dtype=DT[dt]).cuda()
+    wt = G.conv_weight(seed, name, cout, cin, k, k, layout, DT[dt]).cuda()
+    b = G.conv_bias(seed, name, cout).cuda()
+    al = G.prelu_alpha(seed, name, cout).cuda()
+    y = A.conv2d_fused(x, wt, b, stride=s, pad=p, act=act, alpha=al, layout=layout)
+    d = A.conv_desc(x, cout, k, k, s, p, layout)
+    wp = A.conv2d_prepack(d, wt)
+    wsb = A.acnn_conv2d_prepacked_workspace_size(d)
+    assert wsb <= A.acnn_conv2d_workspace_size(d)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    y2 = torch.empty_like(y)
+    A.check(A.acnn_conv2d_fused_prepacked(d, x, wp, b, al, None, A.RES_NONE, act, y2, ws, wsb,
+                                          None), name)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2), name
+    ref = O.conv2d(to64(x), to64(wt), to64(b), stride=s, pad=p, act=act, alpha=to64(al),
+                   layout=layout)
+    assert_parity(y2, ref, TDT[dt], name)
+
+
 def test_conv_tensor_no_bias():
     y, ref = conv_case("nobias", 1, 9, 9, 64, 64, 1, 1, 0, "f16", bias=False)
     assert_parity(y, ref, torch.float16)
