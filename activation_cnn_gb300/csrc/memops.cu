@@ -797,6 +797,37 @@ __global__ void __launch_bounds__(1024) transpose_kernel(const uint16_t* __restr
     if (c < C && p < HW) yi[(long long)p * C + c] = tile[threadIdx.x][threadIdx.y];
 }
 
+// The same transpose for even C and HW through a 64 x 64 tile, 4-byte
+// accesses: each warp reads 128-byte channel-row segments (2 pixels a lane)
+// and writes 128-byte pixel-row segments (2 channels a lane).
+__global__ void __launch_bounds__(256) transpose64_kernel(const uint16_t* __restrict__ x,
+                                                          uint16_t* __restrict__ y, int C,
+                                                          int HW) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+    __shared__ uint16_t tile[64][66];  // [channel][pixel], rows 4-byte aligned
+    const int n = blockIdx.z;
+    const int c0 = blockIdx.y * 64, p0 = blockIdx.x * 64;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint16_t* xi = x + (long long)n * C * HW;
+    uint16_t* yi = y + (long long)n * C * HW;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int cc = warp * 8 + r, c = c0 + cc, p = p0 + 2 * lane;
+        uint32_t v = 0;
+        if (c < C && p < HW) v = *reinterpret_cast<const uint32_t*>(xi + (long long)c * HW + p);
+        *reinterpret_cast<uint32_t*>(&tile[cc][2 * lane]) = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int pp = warp * 8 + r, p = p0 + pp, c = c0 + 2 * lane;
+        if (p < HW && c < C) {
+            const uint32_t v = (uint32_t)tile[2 * lane][pp] | ((uint32_t)tile[2 * lane + 1][pp] << 16);
+            *reinterpret_cast<uint32_t*>(yi + (long long)p * C + c) = v;
+        }
+    }
+}
+
 template <typename T> int vec_for(int elems) {
     constexpr int V = 16 / sizeof(T);
     return elems % V == 0 ? V : 1;
@@ -1058,6 +1089,13 @@ cudaError_t launch_weight_pack(const acnn_conv_desc& d, int kp, const void* w, v
 cudaError_t launch_nchw_to_nhwc(int n, int c, int hw, int elem_bytes, const void* x, void* y,
                                 cudaStream_t s) {
     if (elem_bytes != 2) return cudaErrorInvalidValue;
+    if (c % 2 == 0 && hw % 2 == 0 && (hw + 63) / 64 <= 0x7fffffff && (c + 63) / 64 <= 65535 &&
+        n <= 65535) {
+        dim3 grid((hw + 63) / 64, (c + 63) / 64, n);
+        launch_pdl(transpose64_kernel, grid, dim3(256), 0, s, static_cast<const uint16_t*>(x),
+                   static_cast<uint16_t*>(y), c, hw);
+        return cudaGetLastError();
+    }
     dim3 grid((hw + 31) / 32, (c + 31) / 32, n), block(32, 32);
     launch_pdl(transpose_kernel, grid, block, 0, s, static_cast<const uint16_t*>(x),
                                             static_cast<uint16_t*>(y), c, hw);
