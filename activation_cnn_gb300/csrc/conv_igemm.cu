@@ -97,7 +97,7 @@ struct Params {
     int res_depth;     // residual boxes in flight per epilogue warp (0: no residual)
     int b_resident;    // 1: all num_kb weight blocks loaded once, the ring carries A only
     int par_floats;    // NHWC epilogue: shared copy of bias [cpad] then alpha [cpad] (0: none)
-    int ring_slots;    // NHWC epilogue: 2 KB slots per epilogue warp (0: other epilogues)
+    int ring_slots;    // 2 KB epilogue slots per epilogue warp (NHWC ring / NCHW transpose stage)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -947,10 +947,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         cp_async_wait_newer(0);  // no copy into shared memory outlives the CTA
     } else {
         // ---------------------------------------------------- epilogue warps, NCHW
-        // Same row/chunk split as above; lane l holds output pixel m0 + 32q + l,
-        // so each of the 32 channel planes is written by 32 consecutive pixels
-        // (and the residual read the same way).  Bias and alpha come from the
-        // shared copy.
+        // Same row/chunk split as above; lane l holds output pixel m0 + 32q + l.
+        // Without a residual, a chunk whose 32 pixels lie in one image and start
+        // on an 8-pixel boundary goes out through the warp's shared-memory slot:
+        // written [channel][pixel], read back as 16-byte runs of 8 pixels of one
+        // channel and stored as such (4 stores a lane instead of 32).  Other
+        // chunks, and the residual (read per element), take the per-element
+        // path: each of the 32 channel planes written by 32 consecutive pixels.
+        // Bias and alpha come from the shared copy.
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int grp = (warp - 2) >> 2;
         const int row = q * 32 + lane;
@@ -960,6 +964,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool pre = p.res_mode == ACNN_RES_ADD_THEN_ACT;
         const bool prelu = p.act == ACNN_ACT_PRELU;
         const int cpad = prelu ? p.par_floats / 2 : p.par_floats;
+        uint16_t* slot = reinterpret_cast<uint16_t*>(sR + (size_t)(warp - 2) * kStageBytes);
+        const bool vec_ok = !has_res && p.ring_slots > 0 && p.OHW % 8 == 0;
         for (int i = threadIdx.x - 64; i < cpad; i += 32 * kEpiWarps) {
             sP[i] = (p.bias && i < p.C_out) ? __ldg(p.bias + i) : 0.f;
             if (prelu) sP[cpad + i] = i < p.C_out ? __ldg(p.alpha + i) : 0.f;
@@ -987,6 +993,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                               (uint32_t)(acc * MS * BN + ms * BN + c),
                           v);
                 const int nj = p.C_out - (n0 + c) < 32 ? p.C_out - (n0 + c) : 32;
+                // the chunk's 32 pixels: all in range, one image, 8-aligned start
+                const int r0 = m0 + ms * BM + q * 32;
+                const int img0 = r0 / p.OHW;
+                const bool vec = vec_ok && r0 + 31 < p.M && (r0 + 31) / p.OHW == img0 &&
+                                 (r0 - img0 * p.OHW) % 8 == 0;
+                if (vec) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int ch = n0 + c + j;  // < the padded bias copy
+                        const float al = prelu ? sP[cpad + ch] : 0.f;
+                        const T o = from_f32<T>(apply_act(p.act, v[j] + sP[ch], al));
+                        slot[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&o);
+                    }
+                    __syncwarp();
+                    const long long base0 = (long long)img0 * p.C_out * p.OHW + (r0 - img0 * p.OHW);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int piece = lane + 32 * k, j = piece >> 2, pb = piece & 3;
+                        if (j < nj) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(slot + j * 32 + pb * 8);
+                            *reinterpret_cast<uint4*>(y + base0 + (long long)(n0 + c + j) * p.OHW +
+                                                      pb * 8) = u;
+                        }
+                    }
+                    __syncwarp();  // the slot is read out before the next chunk
+                    continue;
+                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     if (j >= nj) break;
@@ -1066,7 +1099,9 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     const bool nhwc_epi = prm.out_layout == ACNN_NHWC;
     prm.par_floats = prm.num_n_tiles * BN * (prm.act == ACNN_ACT_PRELU ? 2 : 1);
     const size_t par_bytes = (size_t)prm.par_floats * 4;
-    prm.ring_slots = nhwc_epi ? (rd > 0 ? rd : 1) : 0;  // split-K: rd = 0, one slot
+    // NHWC: the residual ring (split-K: rd = 0, one slot); NCHW: one slot, the
+    // transposing stage of the vectorised stores
+    prm.ring_slots = nhwc_epi ? (rd > 0 ? rd : 1) : 1;
     const size_t ring_bytes = (size_t)kEpiWarps * prm.ring_slots * kStageBytes;
     auto stages_for = [&](bool resident) -> int {
         if (kSmemFixed + ring_bytes + par_bytes > kSmemMax) return 0;

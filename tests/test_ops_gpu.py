@@ -202,7 +202,12 @@ def test_conv_tensor_integer_bitexact(k, s, p):
                                           (A.ACT_RELU, A.RES_ADD_THEN_ACT),
                                           (A.ACT_NONE, A.RES_NONE)])
 @pytest.mark.parametrize("shape", [(1, 17, 30, 120, 240, 2), (1, 9, 15, 240, 240, 1),
-                                   (2, 8, 8, 64, 32, 1)])
+                                   (2, 8, 8, 64, 32, 1),
+                                   # output planes of 8k pixels: the vectorised
+                                   # stores, with chunks inside one image (384)
+                                   # and straddling two (40), ragged C_out (72)
+                                   (1, 16, 24, 120, 240, 1), (3, 5, 8, 64, 72, 1),
+                                   (1, 68, 120, 240, 240, 1)])
 def test_conv_tensor_nchw(shape, act, res_mode):
     """NCHW fp16 on the tensor path (workspace transpose + NCHW-writing epilogue)."""
     n, h, w, cin, cout, s = shape
