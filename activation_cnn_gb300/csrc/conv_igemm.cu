@@ -1230,7 +1230,10 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     const CUtensorMapDataType dt =
         d.dtype == ACNN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const bool tiled = d.kh == 1 && d.kw == 1 && d.stride == 1 && d.pad == 0;
-    const IgemmPlan plan = igemm_plan(d, a.oh, a.ow, a.ws_part ? a.ws_part_bytes : 0);
+    // no K split for NCHW output: its split epilogue stores element by element,
+    // while the unsplit one writes 16-byte runs
+    const IgemmPlan plan = igemm_plan(d, a.oh, a.ow,
+                                      a.ws_part && a.out_layout == ACNN_NHWC ? a.ws_part_bytes : 0);
     const int bk = plan.bk;
     const CUtensorMapSwizzle swz = bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
 
