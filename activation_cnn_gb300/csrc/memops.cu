@@ -728,14 +728,14 @@ __global__ void __launch_bounds__(kThreads) im2col_pack_kernel(
                     if (e0 + u * kThreads < RL) row[e0 + u * kThreads] = v[u];
             }
         } else {
-            // NCHW: pixel fastest for coalesced plane reads
-            for (int e = threadIdx.x; e < RL; e += blockDim.x) {
-                const int c = e / RW, px = e - c * RW;
-                const int ix = ix0 + px;
-                row[px * C + c] = (ix >= 0 && ix < W)
-                                      ? x[(((long long)n * C + c) * H + iy) * W + ix]
-                                      : (uint16_t)0;
-            }
+            // NCHW: one channel plane at a time, pixels fastest (coalesced)
+            const long long plane = (long long)H * W;
+            const uint16_t* xr = x + ((long long)n * C * H + iy) * W;
+            for (int c = 0; c < C; ++c, xr += plane)
+                for (int px = threadIdx.x; px < RW; px += blockDim.x) {
+                    const int ix = ix0 + px;
+                    row[px * C + c] = (ix >= 0 && ix < W) ? xr[ix] : (uint16_t)0;
+                }
         }
     }
     __syncthreads();
