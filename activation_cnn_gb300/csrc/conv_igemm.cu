@@ -948,12 +948,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------------------------------------------- epilogue warps, NCHW
         // Same row/chunk split as above; lane l holds output pixel m0 + 32q + l.
-        // Without a residual, a chunk whose 32 pixels lie in one image and start
-        // on an 8-pixel boundary goes out through the warp's shared-memory slot:
-        // written [channel][pixel], read back as 16-byte runs of 8 pixels of one
-        // channel and stored as such (4 stores a lane instead of 32).  Other
-        // chunks, and the residual (read per element), take the per-element
-        // path: each of the 32 channel planes written by 32 consecutive pixels.
+        // A chunk whose 32 pixels lie in one image and start on an 8-pixel
+        // boundary goes through the warp's shared-memory slot: its residual (if
+        // any) comes in as 16-byte runs of 8 pixels of one channel and is read
+        // back one pixel per lane; the result is written [channel][pixel] and
+        // leaves as 16-byte runs (4 loads and 4 stores a lane instead of 32).
+        // Other chunks take the per-element path: each of the 32 channel planes
+        // read and written by 32 consecutive pixels.
         // Bias and alpha come from the shared copy.
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int grp = (warp - 2) >> 2;
@@ -965,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool prelu = p.act == ACNN_ACT_PRELU;
         const int cpad = prelu ? p.par_floats / 2 : p.par_floats;
         uint16_t* slot = reinterpret_cast<uint16_t*>(sR + (size_t)(warp - 2) * kStageBytes);
-        const bool vec_ok = !has_res && p.ring_slots > 0 && p.OHW % 8 == 0;
+        const bool vec_ok = p.ring_slots > 0 && p.OHW % 8 == 0;
         for (int i = threadIdx.x - 64; i < cpad; i += 32 * kEpiWarps) {
             sP[i] = (p.bias && i < p.C_out) ? __ldg(p.bias + i) : 0.f;
             if (prelu) sP[cpad + i] = i < p.C_out ? __ldg(p.alpha + i) : 0.f;
@@ -999,15 +1000,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool vec = vec_ok && r0 + 31 < p.M && (r0 + 31) / p.OHW == img0 &&
                                  (r0 - img0 * p.OHW) % 8 == 0;
                 if (vec) {
+                    const long long base0 = (long long)img0 * p.C_out * p.OHW + (r0 - img0 * p.OHW);
+                    if (has_res) {
+                        // the chunk's residual, [channel][pixel] in the slot
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int piece = lane + 32 * k, j = piece >> 2, pb = piece & 3;
+                            if (j < nj)
+                                *reinterpret_cast<uint4*>(slot + j * 32 + pb * 8) =
+                                    *reinterpret_cast<const uint4*>(
+                                        res + base0 + (long long)(n0 + c + j) * p.OHW + pb * 8);
+                        }
+                        __syncwarp();
+                    }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int ch = n0 + c + j;  // < the padded bias copy
                         const float al = prelu ? sP[cpad + ch] : 0.f;
-                        const T o = from_f32<T>(apply_act(p.act, v[j] + sP[ch], al));
+                        float o;
+                        if (has_res) {
+                            uint16_t rb = slot[j * 32 + lane];
+                            const float rv = j < nj ? to_f32(*reinterpret_cast<const T*>(&rb)) : 0.f;
+                            const float x = v[j] + sP[ch];
+                            o = pre ? apply_act(p.act, x + rv, al) : apply_act(p.act, x, al) + rv;
+                        } else {
+                            o = apply_act(p.act, v[j] + sP[ch], al);
+                        }
+                        v[j] = o;
+                    }
+                    if (has_res) __syncwarp();  // every lane has its residual before the slot is reused
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const T o = from_f32<T>(v[j]);
                         slot[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&o);
                     }
                     __syncwarp();
-                    const long long base0 = (long long)img0 * p.C_out * p.OHW + (r0 - img0 * p.OHW);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int piece = lane + 32 * k, j = piece >> 2, pb = piece & 3;
