@@ -1194,7 +1194,9 @@ IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget
     const int sms = sm_count();
     const double io_bytes = 2.0 * ((double)d.n * d.h * d.w * d.c_in + (double)M * d.c_out +
                                    (double)d.c_out * d.kh * d.kw * d.c_in);
-    IgemmPlan best{64, 1, 1, num_kb, 0, bk}, best1{64, 1, 1, num_kb, 0, bk};
+    // defaults are instantiated shapes too (32-channel k-blocks come with MS = 2)
+    const int ms0 = bk == 32 ? 2 : 1;
+    IgemmPlan best{64, ms0, 1, num_kb, 0, bk}, best1{64, ms0, 1, num_kb, 0, bk};
     double best_cost = 1e30, best1_cost = 1e30;
     int bn0, bn_min;
     if (bk == 64) {
