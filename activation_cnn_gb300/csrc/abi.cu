@@ -213,7 +213,9 @@ size_t acnn_conv2d_workspace_size(const acnn_conv_desc* d) {
     if (check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK) return 0;
     const Route r = route(d, oh, ow);
     if (r.path == 0) return 0;
-    return r.stage_x + r.stage_w + round256(igemm_plan(r.g, oh, ow, SIZE_MAX).part_bytes);
+    // NCHW-output convs are never split (no partial sums to hold)
+    const size_t part = d->layout == ACNN_NHWC ? igemm_plan(r.g, oh, ow, SIZE_MAX).part_bytes : 0;
+    return r.stage_x + r.stage_w + round256(part);
 }
 
 int acnn_conv2d_plan(const acnn_conv_desc* d, size_t ws_bytes, int* rows, int* bn,
@@ -223,7 +225,8 @@ int acnn_conv2d_plan(const acnn_conv_desc* d, size_t ws_bytes, int* rows, int* b
         return -1;
     const Route r = route(d, oh, ow);
     if (r.path == 0 || ws_bytes < r.stage_x + r.stage_w) return -1;
-    const IgemmPlan pl = igemm_plan(r.g, oh, ow, ws_bytes - r.stage_x - r.stage_w);
+    const size_t budget = d->layout == ACNN_NHWC ? ws_bytes - r.stage_x - r.stage_w : 0;
+    const IgemmPlan pl = igemm_plan(r.g, oh, ow, budget);
     *rows = 128 * pl.ms;
     *bn = pl.bn;
     *splits = pl.splits;
@@ -361,7 +364,8 @@ size_t acnn_conv2d_prepacked_workspace_size(const acnn_conv_desc* d) {
     if (check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK) return 0;
     const Route r = route(d, oh, ow);
     if (r.path == 0) return 0;
-    return r.stage_x + round256(igemm_plan(r.g, oh, ow, SIZE_MAX).part_bytes);
+    const size_t part = d->layout == ACNN_NHWC ? igemm_plan(r.g, oh, ow, SIZE_MAX).part_bytes : 0;
+    return r.stage_x + round256(part);
 }
 
 int acnn_conv2d_prepack(const acnn_conv_desc* d, const void* w, void* w_packed,

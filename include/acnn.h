@@ -149,7 +149,7 @@ int acnn_conv2d_path(const acnn_conv_desc* d);
 
 /* Tensor-core plan for d given ws_bytes of workspace: output pixels per tile
  * (*rows: 128/256), output channels per tile (*bn: 32/64/128/256) and K splits
- * (*splits, 1 = none).  Returns 0, or -1 when d does not take the tensor-core
+ * (*splits, 1 = none; always 1 for NCHW, whose convs are never split).  Returns 0, or -1 when d does not take the tensor-core
  * path or ws_bytes is below the required staging (host pointers; the plan
  * depends on the current device's SM count). */
 int acnn_conv2d_plan(const acnn_conv_desc* d, size_t ws_bytes, int* rows, int* bn, int* splits);

@@ -413,7 +413,7 @@ SPLITK_CASES = [
     # name, n, h, w, cin, cout, k, s, p, layout, act, res
     ("s4_3x3", 8, 20, 20, 512, 512, 3, 1, 1, G.NHWC, A.ACT_RELU, A.RES_NONE),
     ("pan5_silu", 2, 20, 20, 512, 256, 3, 1, 1, G.NHWC, A.ACT_SILU, A.RES_NONE),
-    ("res_prelu_nchw", 1, 17, 30, 240, 240, 3, 1, 1, G.NCHW, A.ACT_PRELU, A.RES_ACT_THEN_ADD),
+    ("res_prelu", 1, 17, 30, 240, 240, 3, 1, 1, G.NHWC, A.ACT_PRELU, A.RES_ACT_THEN_ADD),
     ("1x1_addres", 2, 10, 10, 2048, 256, 1, 1, 0, G.NHWC, A.ACT_RELU, A.RES_ADD_THEN_ACT),
 ]
 
@@ -430,6 +430,18 @@ def min_workspace(d, full):
         else:
             lo = mid
     return hi
+
+
+def test_conv_nchw_never_splits():
+    """NCHW-output convs run unsplit (the plan query says so, and the workspace
+    holds only the staging) even where the same NHWC conv splits K."""
+    dn = A.ConvDesc(1, 17, 30, 240, 240, 3, 3, 1, 1, G.NCHW, G.F16)
+    dh = A.ConvDesc(1, 17, 30, 240, 240, 3, 3, 1, 1, G.NHWC, G.F16)
+    assert A.acnn_conv2d_plan(dh, A.acnn_conv2d_workspace_size(dh))[3] > 1
+    st, _, _, sp = A.acnn_conv2d_plan(dn, A.acnn_conv2d_workspace_size(dn))
+    assert st == 0 and sp == 1
+    assert A.acnn_conv2d_workspace_size(dn) == A.acnn_conv2d_prepacked_workspace_size(dn) + \
+        (240 * 9 * 240 * 2 + 255) // 256 * 256
 
 
 @pytest.mark.parametrize("case", SPLITK_CASES, ids=[c[0] for c in SPLITK_CASES])
