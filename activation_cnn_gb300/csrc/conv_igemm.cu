@@ -130,17 +130,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same phase (returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Slow path of a bounded wait for the phase of `bar` with parity `parity`.
 // Returns false if the CTA is aborting or this wait expired; on expiry it
 // records the timeout in the device status word and raises the abort flag.
 // Time is measured with the SM's cycle counter (cheap to read, unlike the
-// global timer); kTimeoutCycles is ~4 s at the maximum SM clock.
+// global timer); kTimeoutCycles is ~4 s at the maximum SM clock.  With a poll
+// budget (> 0) each poll is a non-blocking test, so the budget counts tests
+// exactly (a try_wait may suspend the thread for a hardware-chosen time).
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag, long long budget,
                                              int* status) {
     long long t0 = -1;
     for (long long i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (budget > 0 ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         bool expired = budget > 0 && i >= budget;
         if ((i & 255) == 0) {
             if (*abort_flag) return false;
@@ -248,6 +263,20 @@ __device__ __forceinline__ void cp_async_wait_newer(int n) {
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// One lane of a converged warp (the lowest active one, the same lane on every
+// call while all 32 are active) gets true.  The producer and MMA warps run
+// their loops on all 32 lanes -- every wait, counter and coordinate warp-wide --
+// and only the elected lane issues the TMA copies, MMAs and commits.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -493,24 +522,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int num_tiles = p.num_m_tiles * p.num_n_tiles * p.splits;
 
     if (warp == 0) {
-        if (lane == 0) {
+        {
             // ------------------------------------------------ TMA producer
+            // (all 32 lanes walk the loop; the elected lane issues)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
             if (bres) {
                 // every weight block of the (single) column tile, once
-                mbar_arrive_expect_tx(wres_bar, (uint32_t)p.num_kb * C::kBBytes);
-                int tap = 0, c0 = 0;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    tma_load_3d(smem_u32(sB + kb * C::kBBytes), &tmap_b, wres_bar, c0, tap, 0);
-                    c0 += BK;
-                    if (c0 >= p.kb_per_tap * BK) {
-                        c0 = 0;
-                        ++tap;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(wres_bar, (uint32_t)p.num_kb * C::kBBytes);
+                    int tap = 0, c0 = 0;
+                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                        tma_load_3d(smem_u32(sB + kb * C::kBBytes), &tmap_b, wres_bar, c0, tap, 0);
+                        c0 += BK;
+                        if (c0 >= p.kb_per_tap * BK) {
+                            c0 = 0;
+                            ++tap;
+                        }
                     }
                 }
+                __syncwarp();
             }
             const uint32_t stage_tx = C::kAB + (bres ? 0u : C::kBBytes);
             for (int unit = blockIdx.x; ok && unit < num_tiles; unit += gridDim.x) {
@@ -527,25 +560,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int c0 = (kb0 - tap * p.kb_per_tap) * BK;
                 int ky = tap / p.KW, kx = tap - ky * p.KW;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) {
+                    if (!__all_sync(0xffffffffu,
+                                    wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p))) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, stage_tx);
                     const uint32_t a_dst = smem_u32(sA + stage * C::kAB);
                     // a folded concat: channel blocks from c_split on come from
                     // the second source (c_split is a multiple of BK)
                     const bool second = p.c_split && c0 >= p.c_split;
                     const CUtensorMap* am = second ? &tmap_a2 : &tmap_a;
                     const int ca = second ? c0 - p.c_split : c0;
-                    if (p.a_mode == 0)
-                        tma_load_2d(a_dst, am, fb, ca, m0);
-                    else
-                        tma_load_im2col(a_dst, am, fb, ca, wc, hc, img, (uint16_t)kx,
-                                        (uint16_t)ky);
-                    if (!bres)
-                        tma_load_3d(smem_u32(sB + stage * C::kBBytes), &tmap_b, fb, c0, tap, n0);
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(fb, stage_tx);
+                        if (p.a_mode == 0)
+                            tma_load_2d(a_dst, am, fb, ca, m0);
+                        else
+                            tma_load_im2col(a_dst, am, fb, ca, wc, hc, img, (uint16_t)kx,
+                                            (uint16_t)ky);
+                        if (!bres)
+                            tma_load_3d(smem_u32(sB + stage * C::kBBytes), &tmap_b, fb, c0, tap,
+                                        n0);
+                    }
+                    __syncwarp();
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == S) {
@@ -564,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) {
-                // let every copy this thread started land before the CTA exits
+                // let every copy this warp started land before the CTA exits
                 for (int s = 0; s < S; ++s)
                     if (issued_mask & (1u << s)) wait_drain(full_bar(s), (issued_parity >> s) & 1u);
                 if (bres) wait_drain(wres_bar, 0);
@@ -575,54 +613,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         // launch (its CTAs start as SMs free up and wait for this grid to end)
         griddep_launch_dependents();
     } else if (warp == 1) {
-        if (lane == 0) {
+        {
             // ------------------------------------------------ MMA issuer
+            // (all 32 lanes walk the loop; the elected lane -- lane 0 of the
+            // converged warp every time -- issues the MMAs and their commits)
             constexpr uint32_t idesc = make_idesc(BM, BN, IsBf16<T>::v);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            bool ok = !bres || wait_phase(wres_bar, 0, abort_flag, p);
+            bool ok = !bres || __all_sync(0xffffffffu, wait_phase(wres_bar, 0, abort_flag, p));
             for (int unit = blockIdx.x; ok && unit < num_tiles; unit += gridDim.x) {
                 const int split = unit % p.splits;
                 const int kb0 = split * p.kb_per_split;
                 const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-                if (!wait_phase(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p)) {
+                if (!__all_sync(0xffffffffu,
+                                wait_phase(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MS * BN);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(full_bar(stage), phase, abort_flag, p)) {
+                    if (!__all_sync(0xffffffffu, wait_phase(full_bar(stage), phase, abort_flag, p))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint64_t bdesc =
                         smem_desc<BK>(smem_u32(sB + (bres ? kb : stage) * C::kBBytes));
+                    const uint64_t adesc0 = smem_desc<BK>(smem_u32(sA + stage * C::kAB));
+                    if (elect_one()) {
 #pragma unroll
-                    for (int ms = 0; ms < MS; ++ms) {
-                        const uint64_t adesc =
-                            smem_desc<BK>(smem_u32(sA + stage * C::kAB + ms * C::kABytes));
+                        for (int ms = 0; ms < MS; ++ms) {
+                            // the row blocks of a stage lie kABytes apart (>> 4 in the descriptor)
+                            const uint64_t adesc = adesc0 + (uint64_t)(ms * (C::kABytes >> 4));
 #pragma unroll
-                        for (int k = 0; k < BK / 16; ++k)
-                            mma_f16(d_tmem + (uint32_t)(ms * BN), adesc + 2u * k, bdesc + 2u * k,
-                                    idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+                            for (int k = 0; k < BK / 16; ++k)
+                                mma_f16(d_tmem + (uint32_t)(ms * BN), adesc + 2u * k,
+                                        bdesc + 2u * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+                        }
+                        mma_commit(empty_bar(stage));  // frees the slot once these MMAs finish
                     }
-                    mma_commit(empty_bar(stage));  // frees the slot once these MMAs finish
+                    __syncwarp();
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+                if (elect_one()) mma_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+                __syncwarp();
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
-            if (!ok) {
-                mma_commit(drain_bar);  // wait for every MMA this thread issued
+            if (!ok && lane == 0) {
+                mma_commit(drain_bar);  // wait for every MMA this warp issued
                 wait_drain(drain_bar, 0);
             }
         }

@@ -12,36 +12,19 @@
 //     truncated from clamp(v, 0, 1) * 255, alpha 255.
 // The page computes this in binary32 and truncates to bytes, so a float
 // decides each output byte.  Every step is written with a round-to-nearest
-// intrinsic (no fused multiply-adds) in one fixed order, and exp is computed
-// by a named method (Cody-Waite reduction, degree-7 Taylor polynomial) rather
-// than the library's, so that the result is a function of the inputs alone.
+// intrinsic (no fused multiply-adds) in the page's order; the mask's exp is
+// CUDA's expf (the page's WGSL exp is a binary32 function of unstated
+// rounding), so a byte can differ by one from another faithful binary32
+// evaluation only where clamp(v, 0, 1) * 255 lies within a few ulp of an
+// integer.
 #include "common.cuh"
 
 namespace acnn {
 
 namespace {
 
-// e^x: x = n ln2 + r with n = rint(x log2 e) and ln 2 split into a 15-bit head
-// and a tail (Cody and Waite's reduction), e^r by the Taylor polynomial of
-// degree 7 in Horner form (each step one correctly rounded fma), times 2^n.
-__device__ __forceinline__ float flow_exp(float x) {
-    const float log2e = 1.44269504088896341f;
-    const float ln2_hi = 0.693145751953125f;
-    const float ln2_lo = 1.42860682030941723e-6f;
-    x = fminf(fmaxf(x, -87.0f), 88.0f);
-    const float n = rintf(__fmul_rn(x, log2e));
-    float r = __fsub_rn(x, __fmul_rn(n, ln2_hi));
-    r = __fsub_rn(r, __fmul_rn(n, ln2_lo));
-    float q = 1.0f / 5040.0f;
-    q = __fmaf_rn(q, r, 1.0f / 720.0f);
-    q = __fmaf_rn(q, r, 1.0f / 120.0f);
-    q = __fmaf_rn(q, r, 1.0f / 24.0f);
-    q = __fmaf_rn(q, r, 1.0f / 6.0f);
-    q = __fmaf_rn(q, r, 0.5f);
-    q = __fmaf_rn(q, r, 1.0f);
-    q = __fmaf_rn(q, r, 1.0f);
-    return ldexpf(q, (int)n);
-}
+// e^x for the mask's sigmoid: the CUDA math library's binary32 exp.
+__device__ __forceinline__ float flow_exp(float x) { return expf(x); }
 
 // mix(a, b, f) = a * (1 - f) + b * f, three roundings
 __device__ __forceinline__ float mixf(float a, float b, float f) {

@@ -412,8 +412,7 @@ int oracle_prep_quarter(int H, int W, const uint8_t* rgba0, const uint8_t* rgba1
 /* frames.  The page computes it in binary32 and truncates to bytes, so a     */
 /* float decides an integer here: this function computes in float, one       */
 /* operation at a time in the order below (gcc -ffp-contract=off: no fused    */
-/* multiply-adds), and the CUDA kernel follows the same order, so the bytes   */
-/* agree exactly.                                                            */
+/* multiply-adds).                                                           */
 /*                                                                          */
 /*   t = tmp8, 5 planes (flow0 x,y, flow1 x,y, mask) at (H/8, W/8)           */
 /*   for output pixel (x, y):                                                */
@@ -429,32 +428,14 @@ int oracle_prep_quarter(int H, int W, const uint8_t* rgba0, const uint8_t* rgba1
 /*     bgr = w0 * m + w1 * (1 - m)                                           */
 /*     out = bytes R, G, B, 255 with each = (uint)(clamp(v, 0, 1) * 255)     */
 /*                                                                          */
-/* exp is computed by a method named here rather than taken from a math      */
-/* library, so that the CUDA side can implement the same steps: Cody and     */
-/* Waite's argument reduction x = n ln2 + r, |r| <= ln2 / 2, with ln2 split   */
-/* into a head exact in a few bits and a tail, then the degree-7 Taylor       */
-/* polynomial of e^r (error below 1e-8 relative for |r| <= 0.35) in Horner    */
-/* form, each step a correctly rounded fmaf, then scaling by 2^n.             */
+/* The page's WGSL exp is a binary32 function whose rounding the page does   */
+/* not fix; here it is the C library's double exp rounded to float (within    */
+/* an ulp of e^x).  Any binary32 exp of similar accuracy moves a byte only     */
+/* where clamp(v, 0, 1) * 255 lies within a few ulp of an integer.           */
 /* ------------------------------------------------------------------------ */
 static float flow_exp(float x)
 {
-    const float log2e = 1.44269504088896341f;
-    const float ln2_hi = 0.693145751953125f;      /* 0x3f317200: 15 significant bits */
-    const float ln2_lo = 1.42860682030941723e-6f; /* ln 2 - ln2_hi */
-    if (x > 88.0f) x = 88.0f;
-    if (x < -87.0f) x = -87.0f;
-    const float n = rintf(x * log2e);
-    float r = x - n * ln2_hi;
-    r = r - n * ln2_lo;
-    float q = 1.0f / 5040.0f;
-    q = fmaf(q, r, 1.0f / 720.0f);
-    q = fmaf(q, r, 1.0f / 120.0f);
-    q = fmaf(q, r, 1.0f / 24.0f);
-    q = fmaf(q, r, 1.0f / 6.0f);
-    q = fmaf(q, r, 0.5f);
-    q = fmaf(q, r, 1.0f);
-    q = fmaf(q, r, 1.0f);
-    return ldexpf(q, (int)n);
+    return (float)exp((double)x);
 }
 
 static float flow_mix(float a, float b, float f)

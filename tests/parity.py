@@ -55,3 +55,33 @@ def assert_bitexact(got, ref, what=""):
     assert g.shape == r.shape, (what, g.shape, r.shape)
     bad = g != r
     assert not bad.any(), (what, int(bad.sum()), np.argwhere(bad)[:5].tolist())
+
+
+# A byte of the flow-out stage is trunc(v * 255) of a binary32 value v in
+# [0, 1].  Kernel and oracle compute v in the same binary32 operation order
+# except for the mask's exp (CUDA's expf, within 2 ulp; the C library's
+# double exp rounded to float, within 1 ulp), which moves the sigmoid m by at
+# most ~3 ulp (< 2e-7) and the blended v by < 1e-6; times 255 that is < 3e-4.
+# So a byte may differ by one only where the oracle's v * 255 lies within
+# BYTE_WINDOW of an integer; everywhere else the bytes must be equal.
+BYTE_WINDOW = 5e-4
+
+
+def assert_bytes_boundary(got, ref, pre, what=""):
+    """`got`, `ref`: [H, W, 4] uint8 (R, G, B, A); `pre`: the oracle's clamped
+    R, G, B values [3, H, W] before the byte scale.  Returns the number of
+    channel values that differ by one at a byte boundary (all others equal)."""
+    g = got.detach().cpu().numpy().astype(np.int32) if isinstance(got, torch.Tensor) \
+        else np.asarray(got, np.int32)
+    r = np.asarray(ref, np.int32)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    assert (g[..., 3] == r[..., 3]).all(), f"{what}: alpha differs"
+    d = g[..., :3] - r[..., :3]
+    scaled = np.moveaxis(np.asarray(pre, np.float64), 0, -1) * 255.0
+    near = np.abs(scaled - np.rint(scaled)) <= BYTE_WINDOW
+    bad = (d != 0) & ~((np.abs(d) == 1) & near)
+    assert not bad.any(), (what, int(bad.sum()), np.argwhere(bad)[:5].tolist())
+    n1 = int((d != 0).sum())
+    print(f"{what}: {n1} of {d.size} channel bytes differ by 1 at a byte boundary "
+          f"({int(near.sum())} values within {BYTE_WINDOW} of one)")
+    return n1
