@@ -22,8 +22,10 @@ __device__ int g_device_status = 0;
 namespace {
 std::atomic<long long> g_wait_budget{0};
 constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices] = {};
-int g_sm_count[kMaxDevices] = {};
+// Per-device values looked up once (static storage: zero until set).  Read
+// with an acquire load; the first caller on a device fills them in.
+std::atomic<int*> g_status_ptr[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
 std::mutex g_mu;
 
 int current_device() {
@@ -35,13 +37,43 @@ int current_device() {
 
 int sm_count() {
     const int dev = current_device();
-    if (g_sm_count[dev] == 0) {
-        int n = 0;
+    int n = g_sm_count[dev].load(std::memory_order_acquire);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 1;
-        g_sm_count[dev] = n;
+        g_sm_count[dev].store(n, std::memory_order_release);
     }
-    return g_sm_count[dev];
+    return n;
+}
+
+// cudaFuncSetAttribute acts on the current device only, so the dynamic
+// shared-memory opt-in of each kernel is recorded per (kernel, device): a
+// process that drives several GPUs opts in on each before its first launch
+// there.  Thread-safe; a larger request than the one recorded is set again.
+int ensure_smem_optin(const void* kernel, size_t bytes) {
+    struct Entry {
+        const void* k;
+        int dev;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(mu);
+    for (Entry& e : done)
+        if (e.k == kernel && e.dev == dev) {
+            if (e.bytes >= bytes) return ACNN_OK;
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)bytes) != cudaSuccess)
+                return ACNN_ERR_CUDA;
+            e.bytes = bytes;
+            return ACNN_OK;
+        }
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess)
+        return ACNN_ERR_CUDA;
+    done.push_back(Entry{kernel, dev, bytes});
+    return ACNN_OK;
 }
 
 int occupancy_blocks(const void* kernel, int threads, size_t smem) {
@@ -68,15 +100,17 @@ int occupancy_blocks(const void* kernel, int threads, size_t smem) {
 
 int* device_status_ptr() {
     const int dev = current_device();
-    if (!g_status_ptr[dev]) {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!g_status_ptr[dev]) {
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-            g_status_ptr[dev] = static_cast<int*>(p);
-        }
+    int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    std::lock_guard<std::mutex> lk(g_mu);
+    p = g_status_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+        void* q = nullptr;
+        if (cudaGetSymbolAddress(&q, g_device_status) != cudaSuccess) return nullptr;
+        p = static_cast<int*>(q);
+        g_status_ptr[dev].store(p, std::memory_order_release);
     }
-    return g_status_ptr[dev];
+    return p;
 }
 
 long long wait_budget_polls() { return g_wait_budget.load(); }
@@ -694,22 +728,25 @@ int acnn_device_sm_count(void) { return sm_count(); }
 // ---------------------------------------------------------------------------
 namespace {
 __device__ __align__(256) uint8_t g_noalloc_scratch[ACNN_NOALLOC_SCRATCH_BYTES];
-void* g_noalloc_scratch_ptr[kMaxDevices] = {};
+std::atomic<void*> g_noalloc_scratch_ptr[kMaxDevices];
 std::mutex g_noalloc_mu;
 
 // Device address of the scratch array on the current device, looked up once
 // per device with that device current (the host-side symbol is only a
-// stand-in, never a device address).  NULL if the lookup fails.
+// stand-in, never a device address); later calls take the cached address
+// without locking.  NULL if the lookup fails.
 void* noalloc_scratch() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    void* p = g_noalloc_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_scratch_ptr[dev]) {
-        void* p = nullptr;
+    p = g_noalloc_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
-        g_noalloc_scratch_ptr[dev] = p;
+        g_noalloc_scratch_ptr[dev].store(p, std::memory_order_release);
     }
-    return g_noalloc_scratch_ptr[dev];
+    return p;
 }
 }  // namespace
 

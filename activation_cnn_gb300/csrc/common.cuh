@@ -116,6 +116,7 @@ IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget
 
 int sm_count();
 int* device_status_ptr();         // device address of the status word
+int ensure_smem_optin(const void* kernel, size_t bytes);  // per (kernel, device); ACNN_OK or ACNN_ERR_CUDA
 long long wait_budget_polls();    // 0 = default (time-bounded)
 
 cudaError_t launch_direct_conv(const ConvArgs& a, cudaStream_t s);

@@ -206,11 +206,9 @@ cudaError_t launch_typed(const ConvArgs& a, cudaStream_t s) {
     while (cic > 1 && smem_for(cic) > 40 * 1024) --cic;
     const size_t smem = smem_for(cic);
     auto kern = direct_conv_kernel<T, KH_, KW_>;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    if (smem > 48 * 1024 &&
+        ensure_smem_optin(reinterpret_cast<const void*>(kern), smem) != ACNN_OK)
+        return cudaErrorInvalidValue;
     const int tiles = ((a.oh + kTH - 1) / kTH) * ((a.ow + kTW - 1) / kTW);
     dim3 grid(tiles, (d.c_out + kCOB - 1) / kCOB, d.n);
     launch_pdl(kern, grid, kThreads, smem, s, 

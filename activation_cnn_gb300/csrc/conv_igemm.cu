@@ -1149,14 +1149,9 @@ struct Maps {
 template <int BN, int MS, int BK, typename T>
 int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     using C = Cfg<BN, MS, BK>;
-    static bool attr_set = false;  // per instantiation; set once per process
     auto kern = igemm_conv_kernel<BN, MS, BK, T>;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemMax) != cudaSuccess)
-            return ACNN_ERR_CUDA;
-        attr_set = true;
-    }
+    if (ensure_smem_optin(reinterpret_cast<const void*>(kern), kSmemMax) != ACNN_OK)
+        return ACNN_ERR_CUDA;
     prm.num_n_tiles = (a.d.c_out + BN - 1) / BN;
     // Residual ring: deep (4 boxes per warp) when a tile has few k-blocks and
     // the epilogue's memory traffic dominates, else 3.

@@ -804,7 +804,11 @@ __global__ void __launch_bounds__(256) transpose64_kernel(const uint16_t* __rest
                                                           uint16_t* __restrict__ y, int C,
                                                           int HW) {
     griddep_wait();  // inputs may come from the previous kernel on the stream
-    __shared__ uint16_t tile[64][66];  // [channel][pixel], rows 4-byte aligned
+    // [channel][pixel], 32 words a row; the 4-byte pixel pair w of row r is
+    // stored at word w ^ (r / 2), so that both the row-wise writes (one row,
+    // 32 words) and the column-wise reads (rows 2l and 2l + 1 for lane l, one
+    // word each) touch 32 distinct banks
+    __shared__ uint32_t tile[64][32];
     const int n = blockIdx.z;
     const int c0 = blockIdx.y * 64, p0 = blockIdx.x * 64;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -815,14 +819,17 @@ __global__ void __launch_bounds__(256) transpose64_kernel(const uint16_t* __rest
         const int cc = warp * 8 + r, c = c0 + cc, p = p0 + 2 * lane;
         uint32_t v = 0;
         if (c < C && p < HW) v = *reinterpret_cast<const uint32_t*>(xi + (long long)c * HW + p);
-        *reinterpret_cast<uint32_t*>(&tile[cc][2 * lane]) = v;
+        tile[cc][lane ^ ((cc >> 1) & 31)] = v;
     }
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         const int pp = warp * 8 + r, p = p0 + pp, c = c0 + 2 * lane;
         if (p < HW && c < C) {
-            const uint32_t v = (uint32_t)tile[2 * lane][pp] | ((uint32_t)tile[2 * lane + 1][pp] << 16);
+            // rows 2 lane and 2 lane + 1 both carry the swizzle lane
+            const int wd = (pp >> 1) ^ lane, sh = (pp & 1) * 16;
+            const uint32_t v = ((tile[2 * lane][wd] >> sh) & 0xffffu) |
+                               (((tile[2 * lane + 1][wd] >> sh) & 0xffffu) << 16);
             *reinterpret_cast<uint32_t*>(yi + (long long)p * C + c) = v;
         }
     }
@@ -967,13 +974,9 @@ cudaError_t deconv_typed(const acnn_conv_desc& d, int oh, int ow, const void* x,
                        (size_t)kDeconvWarps * 32 * (4 * c + 1) * sizeof(float);
             };
             const size_t smem = smem_for(nco);
-            static bool attr = false;  // per instantiation: the largest buffer
-            if (!attr) {
-                const size_t mx = smem_for(kDeconvCoBlock);
-                cudaFuncSetAttribute(deconv4s2_kernel<Ti, To>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx);
-                attr = true;
-            }
+            if (ensure_smem_optin(reinterpret_cast<const void*>(deconv4s2_kernel<Ti, To>),
+                                  smem_for(kDeconvCoBlock)) != ACNN_OK)
+                return cudaErrorInvalidValue;
             launch_pdl(deconv4s2_kernel<Ti, To>, dim3((unsigned)rows, cob), 32 * kDeconvWarps,
                        smem, s, static_cast<const Ti*>(x), w, bias, alpha, static_cast<To*>(y),
                        d.layout, d.n, d.c_in, d.c_out, d.h, d.w, act);

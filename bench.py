@@ -47,24 +47,27 @@ def kernel_source_hash():
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def measured_traffic(workload):
-    """Per-launch DRAM bytes of the conv kernel from the committed ncu summary, or None
-    when the summary was taken on another workload or another version of the kernel."""
-    path = os.path.join(ROOT, "profiles", f"igemm_conv_{workload}_traffic.md")
-    if not os.path.exists(path):
+# DRAM traffic of the tensor-core conv kernel, per launch, averaged over the
+# conv launches of one backbone step: dram__bytes_read.sum +
+# dram__bytes_write.sum from an ncu capture (a one-pass metric pair) of the
+# kernel source with this sha256 prefix.  None once the source has changed
+# since the counters were taken.
+CONV_TRAFFIC = {"kernel_sha16": None, "bytes_per_launch": None, "how": None}
+
+
+def conv_traffic(workload, batch):
+    """Per-launch DRAM bytes of the conv kernel for the default backbone step,
+    or None when they were measured on another version of the kernel."""
+    if workload != "backbone" or batch not in (None, 8):
         return None
-    fields = {}
-    with open(path) as f:
-        for line in f:
-            if line.startswith("- ") and ":" in line:
-                k, v = line[2:].split(":", 1)
-                fields[k.strip()] = v.strip().strip("`")
-    if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+    if CONV_TRAFFIC["kernel_sha16"] != kernel_source_hash():
         return None
-    try:
-        return float(fields["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    return CONV_TRAFFIC["bytes_per_launch"]
+
+
+# FP32 FFMA peak of a GB300 (derived, not measured): 152 SMs x 128 FP32 lanes x
+# 2 FLOP per FMA x 2.07 GHz maximum SM clock.
+FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def peaks():
@@ -212,8 +215,118 @@ def time_ops(net, stream, steps, flush):
                            net.layout, net.dtype)
             path = A.acnn_conv2d_path(d)
         rows.append({"name": op.label, "kind": op.kind, "path": path, "flops": op.flops,
-                     "bytes": op.bytes, "s": statistics.mean(per_op[id(op)])})
+                     "bytes": op.bytes, "section": op.section,
+                     "s": statistics.mean(per_op[id(op)])})
     return rows
+
+
+def time_sections(net, stream, steps, flush):
+    """Device time of each captured section graph replayed alone after an L2
+    flush (CUDA events on the launching stream), averaged over `steps`."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = {sec: 0.0 for sec, _ in net.graphs}
+    for _ in range(steps):
+        for sec, g in net.graphs:
+            flush()
+            e0.record(stream)
+            g.launch(stream)
+            e1.record(stream)
+            stream.synchronize()
+            out[sec] += e0.elapsed_time(e1) * 1e-3
+    return {k: v / steps for k, v in out.items()}
+
+
+def apportion(rows, sections, step_s):
+    """Split the measured step time over the ops (key "t", seconds per step).
+
+    Each op gets its section's share of the step (sections replayed alone,
+    time_sections) times its own share of that section's per-op event time
+    (time_ops).  The per-op times, bracketed by event nodes, serialise the
+    launches and so overstate every op by its launch gap; the step and the
+    sections keep the overlap of consecutive launches.  The apportioned times
+    sum to the step, so no op is credited with more time than the step has."""
+    tot_sec = sum(sections.values())
+    by_sec = {}
+    for r in rows:
+        by_sec[r["section"]] = by_sec.get(r["section"], 0.0) + r["s"]
+    for r in rows:
+        r["t"] = step_s * (sections[r["section"]] / tot_sec) * (r["s"] / by_sec[r["section"]])
+    return rows
+
+
+def op_summary(r, pk):
+    """One op's apportioned time, throughput and fraction of its roof."""
+    t = r["t"]
+    d = {"name": r["name"], "kind": r["kind"], "us": round(t * 1e6, 2)}
+    if r["flops"]:
+        d["TFLOP_s"] = round(r["flops"] / t / 1e12, 2)
+    if r["bytes"]:
+        d["GB_s"] = round(r["bytes"] / t / 1e9, 1)
+    if r["kind"] == "conv":
+        d["path"] = r["path"]
+        if r["path"] == 0:
+            d["frac_fp32_ffma"] = round(r["flops"] / t / 1e12 / FP32_FFMA_TFLOPS, 4)
+        else:
+            d["frac_tensor_peak"] = round(r["flops"] / t / 1e12 / pk["bf16_burst"], 4)
+            roof = max(r["flops"] / (pk["bf16_burst"] * 1e12), r["bytes"] / (pk["hbm"] * 1e9))
+            d["attainable_frac"] = round(roof / t, 4)
+    elif r["bytes"]:
+        d["frac_hbm"] = round(r["bytes"] / t / 1e9 / pk["hbm"], 4)
+    return d
+
+
+def time_steps(net, stream, steps, flush):
+    """Device time of `steps` whole steps (every section graph), L2 flushed
+    before each step outside the timed interval; returns seconds per step."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        net.replay(stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends)]
+
+
+def measure_config(name, dev, stream, flush, steps, pk):
+    """One of the other workloads (single conv, fp32 stem, bottleneck blocks,
+    frame stack), timed like the main one: step time, then every op's share of
+    it against its own roof."""
+    import torch
+    from activation_cnn_gb300 import acnn as A
+    net = build_net(name, dev)
+    with torch.cuda.stream(stream):
+        net.run_eager(stream)
+    stream.synchronize()
+    st = A.acnn_last_device_status(stream.cuda_stream)
+    if st != 0:
+        raise RuntimeError(f"{name}: device status after eager pass: {A.status_string(st)}")
+    net.capture(stream)
+    for _ in range(3):
+        net.replay(stream)
+    step = statistics.mean(time_steps(net, stream, steps, flush))
+    rows = apportion(time_ops(net, stream, max(3, min(steps, 20)), flush),
+                     time_sections(net, stream, max(3, min(steps, 20)), flush), step)
+    net.release()
+    st = A.acnn_last_device_status(stream.cuda_stream)
+    if st != 0:
+        raise RuntimeError(f"{name}: device status after timing: {A.status_string(st)}")
+    out = {"workload": name, "us_per_step": round(step * 1e6, 2),
+           "steps": steps, "dtype": dtype_name(net),
+           "layout": "NHWC" if net.layout == 0 else "NCHW", "batch": net.batch}
+    unit = "frames/s" if name.startswith("frame") else "img/s"
+    out[unit.replace("/", "_")] = round(net.batch / step, 2)
+    conv = [r for r in rows if r["kind"] == "conv"]
+    if conv:
+        ct = sum(r["t"] for r in conv)
+        out["conv_TFLOP_s"] = round(sum(r["flops"] for r in conv) / ct / 1e12, 3)
+    out["ops"] = [op_summary(r, pk) for r in rows]
+    del net
+    torch.cuda.empty_cache()
+    return out
 
 
 def end_to_end(net, stream, steps, world):
@@ -379,33 +492,44 @@ def run_ours(args, rank, world, local_rank):
     conv_tflops = net.conv_flops() * world * args.steps / total / 1e12
 
     # ------------------------------------------------ roofline of the dominant kernel
-    rows = time_ops(net, stream, max(3, min(args.steps, 10)), flush)
+    # Per-op times apportioned from the step itself (apportion): the sections
+    # replayed alone give each section's share of the step, the event-bracketed
+    # per-op times each op's share of its section.
+    pk = peaks()
+    nrep = max(3, min(args.steps, 10))
+    rows = apportion(time_ops(net, stream, nrep, flush), time_sections(net, stream, nrep, flush),
+                     total / args.steps)
     ig = [r for r in rows if r["kind"] == "conv" and r["path"] in (1, 2)]
     ig_flops = sum(r["flops"] for r in ig)
-    ig_s = sum(r["s"] for r in ig)
-    pk = peaks()
-    achieved = ig_flops / ig_s / 1e12 if ig_s > 0 else 0.0
-    peak = pk["bf16_sustained"]
+    ig_t = sum(r["t"] for r in ig)
+    achieved = ig_flops / ig_t / 1e12 if ig_t > 0 else 0.0
+    peak = pk["bf16_burst"]
+    step_s = total / args.steps
     roofline = {"kernel": "igemm_conv_kernel (tcgen05 implicit-GEMM conv)",
                 "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4) if peak else None,
-                "peak_source": f"{pk['source']} bf16 sustained",
-                "traffic": measured_traffic(args.workload) if args.batch in (None, 8) else None,
-                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the "
-                                  "conv launches of one step, averaged per launch "
-                                  f"(profiles/igemm_conv_{args.workload}_traffic.md)",
+                "peak_source": f"{pk['source']} bf16 burst (a step lasts "
+                               f"{1e3 * step_s:.2f} ms)",
+                "frac_of_sustained": round(achieved / pk["bf16_sustained"], 4),
+                "traffic": conv_traffic(args.workload, args.batch),
+                "traffic_how": CONV_TRAFFIC["how"],
+                "algorithmic_bytes_per_launch": round(sum(r["bytes"] for r in ig) / max(1, len(ig))),
                 "launches_per_step": len(ig),
                 "flops_per_launch": ig_flops / max(1, len(ig)),
-                "avg_launch_us": 1e6 * ig_s / max(1, len(ig)),
-                # share of the per-op (serialised) time; the step itself overlaps
-                # consecutive launches, so it is shorter than the per-op sum
-                "share_of_ops": round(ig_s / sum(r["s"] for r in rows), 4)}
+                "avg_launch_us": round(1e6 * ig_t / max(1, len(ig)), 3),
+                "kernel_us_per_step": round(1e6 * ig_t, 1),
+                "step_us": round(1e6 * step_s, 1),
+                "share_of_step": round(ig_t / step_s, 4),
+                "time_source": "CUDA events on the launching stream: the timed steps, each "
+                               "section graph replayed alone, and each op bracketed by event "
+                               "nodes; the step is split over the ops by section share x "
+                               "op share of its section"}
     # each conv launch against its own roof, max(FLOPs / tensor peak, bytes /
     # HBM peak): the fraction of the attainable time the launches achieve
     ideal = sum(max(r["flops"] / (peak * 1e12), r["bytes"] / (pk["hbm"] * 1e9)) for r in ig)
     roofline["attainable"] = {"ideal_us_per_step": round(ideal * 1e6, 1),
-                              "measured_us_per_step": round(ig_s * 1e6, 1),
-                              "frac": round(ideal / ig_s, 4) if ig_s > 0 else None,
+                              "measured_us_per_step": round(ig_t * 1e6, 1),
+                              "frac": round(ideal / ig_t, 4) if ig_t > 0 else None,
                               "per_launch_roof": "max(flops / tensor peak, bytes / hbm peak)"}
 
     # ------------------------------------------------ end to end through host buffers
@@ -421,34 +545,36 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded; He-normal weights, BN folded into bias)",
         "config": workload_config(args.workload, net, world),
         "conv_tflops": round(conv_tflops, 2),
-        "conv_frac_bf16_peak": round(conv_tflops / pk["bf16_sustained"], 4),
+        "conv_frac_bf16_peak": round(conv_tflops / pk["bf16_burst"], 4),
         "conv_gflop_per_step": round(net.conv_flops() / 1e9, 2),
         "roofline": roofline, "e2e": e2e,
         "gpu_launches": launches_per_step(net) * args.steps,
         "clocks": clk, "wall_s_timed": round(t_wall, 3),
     }
-    # memory-bound companions: algorithmic bytes / launch time vs HBM
+    # memory-bound companions: algorithmic bytes / apportioned time vs HBM
     mem = {}
     for r in rows:
         if r["kind"] in ("pool", "resize", "concat", "prep", "deconv"):
-            k = mem.setdefault(r["label_kind"] if "label_kind" in r else r["kind"],
-                               {"launches": 0, "bytes": 0.0, "s": 0.0})
+            k = mem.setdefault(r["kind"], {"launches": 0, "bytes": 0.0, "t": 0.0})
             k["launches"] += 1
             k["bytes"] += r["bytes"]
-            k["s"] += r["s"]
-    line["memops"] = {k: {"launches": v["launches"], "GB_s": round(v["bytes"] / v["s"] / 1e9, 1),
-                          "frac_hbm": round(v["bytes"] / v["s"] / 1e9 / pk["hbm"], 4),
-                          "us_per_step": round(1e6 * v["s"], 1)}
+            k["t"] += r["t"]
+    line["memops"] = {k: {"launches": v["launches"], "GB_s": round(v["bytes"] / v["t"] / 1e9, 1),
+                          "frac_hbm": round(v["bytes"] / v["t"] / 1e9 / pk["hbm"], 4),
+                          "us_per_step": round(1e6 * v["t"], 1)}
                       for k, v in mem.items()}
     line["memops_peak"] = f"{pk['source']} HBM copy {pk['hbm']} GB/s"
     direct = [r for r in rows if r["kind"] == "conv" and r["path"] == 0]
     if direct:
-        ds = sum(r["s"] for r in direct)
+        ds = sum(r["t"] for r in direct)
         line["direct_conv"] = {"launches": len(direct), "us_per_step": round(1e6 * ds, 1),
                                "TFLOP_s": round(sum(r["flops"] for r in direct) / ds / 1e12, 2)}
     if args.layers:
-        line["layers"] = [{k: (round(v, 9) if isinstance(v, float) else v) for k, v in r.items()}
-                          for r in rows]
+        line["layers"] = [op_summary(r, pk) for r in rows]
+    # the other workloads, each timed the same way
+    if args.configs and args.workload == "backbone" and args.batch in (None, 8):
+        line["configs"] = {name: measure_config(name, dev, stream, flush, 50, pk)
+                           for name in ("conv1", "stem", "block", "block_down", "frame")}
     return line
 
 
@@ -523,7 +649,10 @@ def main():
                              "frame_out", "frame_tfact"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
-    ap.add_argument("--layers", action="store_true", help="add per-conv timings")
+    ap.add_argument("--layers", action="store_true", help="add per-op timings")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the other workloads' sub-objects (single conv, fp32 stem, "
+                         "bottleneck blocks, frame stack)")
     ap.add_argument("--batch", type=int, default=None,
                     help="batch per GPU of the backbone (default 8) or a bottleneck block (default 4); "
                          "other sizes for profiler captures")

@@ -85,3 +85,40 @@ def assert_bytes_boundary(got, ref, pre, what=""):
     print(f"{what}: {n1} of {d.size} channel bytes differ by 1 at a byte boundary "
           f"({int(near.sum())} values within {BYTE_WINDOW} of one)")
     return n1
+
+
+# Canary guards: the compute-sanitizer's out-of-bounds check is closed on this
+# pool, so every output (and workspace) of the op tests lives inside a byte
+# buffer whose GUARD bytes before and after it hold a canary pattern; a store
+# past either end (a ragged tile tail written too far) changes them.  The
+# interior starts as the same pattern (0xFF bytes are NaN in fp32, fp16 and
+# bf16), so an element the op forgot to write stays NaN and fails the parity
+# check's finiteness test.
+GUARD = 4096
+CANARY = 0xFF
+
+
+class Guarded:
+    """A device tensor of `shape`/`dtype` with canary bytes on both sides."""
+
+    def __init__(self, shape, dtype, device="cuda"):
+        shape = tuple(int(s) for s in shape)
+        es = torch.empty((), dtype=dtype).element_size()
+        self.nbytes = int(np.prod(shape, dtype=np.int64)) * es
+        self.raw = torch.full((GUARD + self.nbytes + GUARD,), CANARY, dtype=torch.uint8,
+                              device=device)
+        self.t = self.raw[GUARD:GUARD + self.nbytes].view(dtype).view(shape)
+
+    def check(self, what=""):
+        torch.cuda.synchronize()
+        head = self.raw[:GUARD]
+        tail = self.raw[GUARD + self.nbytes:]
+        bad_h = int((head != CANARY).sum())
+        bad_t = int((tail != CANARY).sum())
+        assert bad_h == 0 and bad_t == 0, f"{what}: {bad_h} bytes before and {bad_t} after " \
+                                          f"the buffer were overwritten"
+
+
+def guarded_bytes(nbytes, device="cuda"):
+    """A uint8 workspace of nbytes (None for 0) with canaries on both sides."""
+    return Guarded((nbytes,), torch.uint8, device) if nbytes else None

@@ -12,7 +12,8 @@ import torch
 from activation_cnn_gb300 import acnn as A
 from activation_cnn_gb300 import inputs as G
 from oracle import oracle as O
-from tests.parity import assert_bitexact, assert_bytes_boundary, assert_parity, to64
+from tests.parity import (Guarded, assert_bitexact, assert_bytes_boundary, assert_parity,
+                           guarded_bytes, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -53,9 +54,16 @@ def conv_case(name, n, h, w, cin, cout, k, s, p, dt, layout=G.NHWC, act=A.ACT_RE
     ys = G.activation_shape(layout, n, cout, oh, ow)
     r = G.tensor(seed, name + ".r", ys, "normal", dtype=DT[dt]) if res_mode else None
     dev = lambda t: None if t is None else t.cuda()
+    # output and workspace inside canary guards (see tests.parity.Guarded)
+    d = A.conv_desc(x, cout, k, kw, s, p, layout)
+    gy = Guarded(A.conv_out_shape(d), TDT[dt])
+    gws = guarded_bytes(A.acnn_conv2d_workspace_size(d))
     y = A.conv2d_fused(dev(x), dev(wt), dev(b), stride=s, pad=p, act=act, alpha=dev(al),
-                       residual=dev(r), res_mode=res_mode, layout=layout)
-    torch.cuda.synchronize()
+                       residual=dev(r), res_mode=res_mode, layout=layout, out=gy.t,
+                       workspace=None if gws is None else gws.t)
+    gy.check(name + " output")
+    if gws is not None:
+        gws.check(name + " workspace")
     ref = O.conv2d(to64(x), to64(wt), None if b is None else to64(b), stride=s, pad=p, act=act,
                    alpha=to64(al), residual=None if r is None else to64(r), res_mode=res_mode,
                    layout=layout)
@@ -298,9 +306,11 @@ def test_conv_direct_integer_bitexact_f32():
 def test_maxpool_bitexact(dt, layout, shape):
     n, h, w, c = shape
     x = G.tensor(3, f"mp{shape}", G.activation_shape(layout, n, c, h, w), "normal", dtype=DT[dt])
-    y = A.pool2d(x.cuda(), A.POOL_MAX, 3, 2, 1, layout=layout)
-    torch.cuda.synchronize()
-    assert_bitexact(y, O.pool2d(to64(x), O.MAX, 3, 2, 1, layout=layout), f"{dt} {shape}")
+    ref = O.pool2d(to64(x), O.MAX, 3, 2, 1, layout=layout)
+    g = Guarded(ref.shape, TDT[dt])
+    y = A.pool2d(x.cuda(), A.POOL_MAX, 3, 2, 1, layout=layout, out=g.t)
+    g.check(f"maxpool {dt} {shape}")
+    assert_bitexact(y, ref, f"{dt} {shape}")
 
 
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
@@ -309,9 +319,11 @@ def test_maxpool_bitexact(dt, layout, shape):
 def test_avgpool(dt, layout, shape):
     n, h, w, c = shape
     x = G.tensor(4, f"ap{shape}", G.activation_shape(layout, n, c, h, w), "normal", dtype=DT[dt])
-    y = A.pool2d(x.cuda(), A.POOL_AVG, 2, 2, 0, layout=layout)
-    torch.cuda.synchronize()
-    assert_parity(y, O.pool2d(to64(x), O.AVG, 2, 2, 0, layout=layout), TDT[dt])
+    ref = O.pool2d(to64(x), O.AVG, 2, 2, 0, layout=layout)
+    g = Guarded(ref.shape, TDT[dt])
+    y = A.pool2d(x.cuda(), A.POOL_AVG, 2, 2, 0, layout=layout, out=g.t)
+    g.check(f"avgpool {dt} {shape}")
+    assert_parity(y, ref, TDT[dt])
 
 
 def test_avgpool_integer_bitexact():
@@ -328,9 +340,11 @@ def test_avgpool_integer_bitexact():
 def test_nearest_bitexact(dt, layout, io):
     (h, w), (oh, ow) = io
     x = G.tensor(5, f"nn{io}", G.activation_shape(layout, 2, 24, h, w), "normal", dtype=DT[dt])
-    y = A.resize2d(x.cuda(), A.RESIZE_NEAREST, oh, ow, layout=layout)
-    torch.cuda.synchronize()
-    assert_bitexact(y, O.resize2d(to64(x), O.NEAREST, oh, ow, layout=layout))
+    ref = O.resize2d(to64(x), O.NEAREST, oh, ow, layout=layout)
+    g = Guarded(ref.shape, TDT[dt])
+    y = A.resize2d(x.cuda(), A.RESIZE_NEAREST, oh, ow, layout=layout, out=g.t)
+    g.check(f"nearest {dt} {io}")
+    assert_bitexact(y, ref)
 
 
 @pytest.mark.parametrize("dt_in,dt_out", [("f32", "f32"), ("f16", "f16"), ("bf16", "bf16"),
@@ -340,9 +354,12 @@ def test_nearest_bitexact(dt, layout, io):
 def test_bilinear(dt_in, dt_out, layout, io):
     (h, w), (oh, ow) = io
     x = G.tensor(6, f"bl{io}", G.activation_shape(layout, 2, 8, h, w), "normal", dtype=DT[dt_in])
-    y = A.resize2d(x.cuda(), A.RESIZE_BILINEAR, oh, ow, layout=layout, out_dtype=TDT[dt_out])
-    torch.cuda.synchronize()
-    assert_parity(y, O.resize2d(to64(x), O.BILINEAR, oh, ow, layout=layout), TDT[dt_out])
+    ref = O.resize2d(to64(x), O.BILINEAR, oh, ow, layout=layout)
+    g = Guarded(ref.shape, TDT[dt_out])
+    y = A.resize2d(x.cuda(), A.RESIZE_BILINEAR, oh, ow, layout=layout, out_dtype=TDT[dt_out],
+                   out=g.t)
+    g.check(f"bilinear {dt_in}->{dt_out} {io}")
+    assert_parity(y, ref, TDT[dt_out])
 
 
 # ---------------------------------------------------------------- concat
@@ -353,9 +370,11 @@ def test_concat_bitexact(dt, layout, cc):
     ca, cb = cc
     a = G.tensor(7, f"ca{cc}", G.activation_shape(layout, 2, ca, 9, 11), "normal", dtype=DT[dt])
     b = G.tensor(7, f"cb{cc}", G.activation_shape(layout, 2, cb, 9, 11), "normal", dtype=DT[dt])
-    y = A.concat(a.cuda(), b.cuda(), layout=layout)
-    torch.cuda.synchronize()
-    assert_bitexact(y, O.concat(to64(a), to64(b), layout=layout))
+    ref = O.concat(to64(a), to64(b), layout=layout)
+    g = Guarded(ref.shape, TDT[dt])
+    y = A.concat(a.cuda(), b.cuda(), layout=layout, out=g.t)
+    g.check(f"concat {dt} {cc}")
+    assert_bitexact(y, ref)
 
 
 # ---------------------------------------------------------------- deconv
@@ -367,9 +386,10 @@ def test_deconv(dt_in, dt_out, layout, shape):
     x = G.tensor(8, "dcx", G.activation_shape(layout, n, ci, h, w), "normal", dtype=DT[dt_in])
     wt = G.deconv_weight(8, "dc", ci, co, 4)
     b = G.conv_bias(8, "dc", co)
-    y = A.deconv2d(x.cuda(), wt.cuda(), b.cuda(), layout=layout, out_dtype=TDT[dt_out])
-    torch.cuda.synchronize()
     ref = O.deconv2d(to64(x), to64(wt), to64(b), layout=layout)
+    g = Guarded(ref.shape, TDT[dt_out])
+    y = A.deconv2d(x.cuda(), wt.cuda(), b.cuda(), layout=layout, out_dtype=TDT[dt_out], out=g.t)
+    g.check(f"deconv {shape}")
     assert_parity(y, ref, TDT[dt_out])
 
 
@@ -380,8 +400,9 @@ def test_frame_prep_quarter(hw, dt):
     h, w = hw
     f0 = G.rgba_frame(9, "f0", h, w)
     f1 = G.rgba_frame(9, "f1", h, w)
-    y = A.frame_prep_quarter(f0.cuda(), f1.cuda(), 0.5, out_dtype=TDT[dt])
-    torch.cuda.synchronize()
+    g = Guarded((7, h // 4, w // 4), TDT[dt])
+    y = A.frame_prep_quarter(f0.cuda(), f1.cuda(), 0.5, out_dtype=TDT[dt], out=g.t)
+    g.check(f"prep {hw}")
     assert_parity(y, O.prep_quarter(f0.numpy(), f1.numpy(), 0.5), TDT[dt])
 
 
@@ -537,8 +558,9 @@ def test_flow_out_bytes(dt, hw):
     from different libraries (CUDA's expf, the C library's exp)."""
     h, w = hw
     t, f0, f1 = _flow_inputs(h, w, dt)
-    y = A.frame_flow_out(t.cuda(), f0.cuda(), f1.cuda())
-    torch.cuda.synchronize()
+    g = Guarded((h, w, 4), torch.uint8)
+    y = A.frame_flow_out(t.cuda(), f0.cuda(), f1.cuda(), out=g.t)
+    g.check(f"flow_out {hw}")
     ref, pre = O.flow_out(t.float().numpy(), f0.numpy(), f1.numpy(), with_pre=True)
     assert_bytes_boundary(y, ref, pre, f"flow_out {dt} {hw}")
 
@@ -592,8 +614,9 @@ def _prep_bound(h, w, flow):
 def test_refine_prep(dt, out, hw):
     h, w = hw
     t, f0, f1 = _flow_inputs(h, w, dt, seed=24)
-    y = A.frame_refine_prep(t.cuda(), f0.cuda(), f1.cuda(), out_dtype=TDT[out])
-    torch.cuda.synchronize()
+    g = Guarded((11, h // 4, w // 4), TDT[out])
+    y = A.frame_refine_prep(t.cuda(), f0.cuda(), f1.cuda(), out_dtype=TDT[out], out=g.t)
+    g.check(f"refine_prep {hw}")
     ref = O.refine_prep(t.double().numpy(), f0.numpy(), f1.numpy())
     assert tuple(y.shape) == (11, h // 4, w // 4)
     if out == "f32":
@@ -627,8 +650,9 @@ def test_refine_out(dt, c, hh, hw):
     x = G.tensor(26, f"ro.x{c}", (c, hh, hw), "normal", dtype=DT[dt])
     wt = G.conv_weight(26, f"ro{c}", 3, c, 3, 3, G.NCHW, G.F32)
     b = G.conv_bias(26, f"ro{c}", 3)
-    y = A.frame_refine_out(x.cuda(), wt.cuda(), b.cuda())
-    torch.cuda.synchronize()
+    g = Guarded((3, hh, hw), torch.float32)
+    y = A.frame_refine_out(x.cuda(), wt.cuda(), b.cuda(), out=g.t)
+    g.check(f"refine_out {c}x{hh}x{hw}")
     ref = O.refine_out(to64(x), to64(wt), to64(b))
     assert_parity(y, ref, torch.float32, f"refine_out {dt} {c}x{hh}x{hw}")
 
@@ -639,8 +663,9 @@ def test_refine_out(dt, c, hh, hw):
 def test_film(dt, t, c, n, hn):
     x = G.tensor(27, f"film.x{c}", (c, n), "normal", dtype=DT[dt])
     prm = G.film_mlp(27, f"film{c}", c, hn)
-    y = A.film(x.cuda(), t, *[p.cuda() for p in prm])
-    torch.cuda.synchronize()
+    g = Guarded(x.shape, TDT[dt])
+    y = A.film(x.cuda(), t, *[p.cuda() for p in prm], out=g.t)
+    g.check(f"film {c}x{n}")
     ref = O.film(to64(x), t, *[to64(p) for p in prm])
     assert_parity(y, ref, TDT[dt], f"film {dt} t={t} {c}x{n}")
 

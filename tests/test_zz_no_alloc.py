@@ -15,7 +15,7 @@ import torch
 from activation_cnn_gb300 import acnn as A
 from activation_cnn_gb300 import inputs as G
 from oracle import oracle as O
-from tests.parity import assert_parity, to64
+from tests.parity import assert_bitexact, assert_parity, to64
 
 
 def test_noalloc_rejects_oversized_scratch():
@@ -56,8 +56,57 @@ def test_noalloc_matches_workspace_entry_point_twice():
                                          A.ACT_PRELU, y_na)
         assert st == 0, A.status_string(st)
         torch.cuda.synchronize()
-        assert_parity(y_na, to64(y_ref), torch.float16, f"call {call} vs workspace entry")
+        # same path, same plan, same staging layout: the same bits
+        assert_bitexact(y_na, y_ref, f"call {call} vs workspace entry")
         ref = O.conv2d(to64(x), to64(wt), to64(b), pad=1, act=O.ACT_PRELU, alpha=to64(al),
                        residual=to64(r), res_mode=O.RES_ACT_THEN_ADD, layout=O.NCHW)
         assert_parity(y_na, ref, torch.float16, f"call {call} vs oracle")
+    assert A.acnn_last_device_status() == 0
+
+
+@pytest.mark.gpu
+def test_noalloc_nhwc_split_k_beyond_the_array_twice():
+    """An NHWC bf16 conv whose full split-K workspace is larger than the static
+    array (it needs no staging): the entry point plans fewer splits into the
+    array.  Two calls in a row give the same bits, the same bits as the
+    workspace entry point given a workspace of the array's size (the same
+    plan), and match the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from activation_cnn_gb300 import build
+    build.build()
+    A.lib()
+    cands = [(8, 20, 20, 512, 512), (8, 40, 40, 256, 256), (16, 20, 20, 512, 512),
+             (8, 20, 20, 1024, 1024)]
+    pick = None
+    for n, h, w, ci, co in cands:
+        d = A.ConvDesc(n, h, w, ci, co, 3, 3, 1, 1, G.NHWC, G.BF16)
+        if A.acnn_conv2d_workspace_size(d) > A.NOALLOC_SCRATCH_BYTES:
+            pick = (n, h, w, ci, co, d)
+            break
+    assert pick is not None, "no candidate splits K beyond the static array"
+    n, h, w, ci, co, d = pick
+    st, _, _, splits = A.acnn_conv2d_plan(d, A.NOALLOC_SCRATCH_BYTES)
+    assert st == 0
+    print(f"geometry {pick[:5]}: {splits} splits within the array")
+    x = G.tensor(22, "nah.x", (n, h, w, ci), "normal", dtype=G.BF16)
+    wt = G.conv_weight(22, "nah", co, ci, 3, 3, G.NHWC, G.BF16)
+    b = G.conv_bias(22, "nah", co)
+    xd, wd, bd = x.cuda(), wt.cuda(), b.cuda()
+    ws = torch.empty(A.NOALLOC_SCRATCH_BYTES, dtype=torch.uint8, device="cuda")
+    y_ref = torch.empty((n, h, w, co), dtype=torch.bfloat16, device="cuda")
+    st = A.acnn_conv2d_fused(d, xd, wd, bd, None, None, A.RES_NONE, A.ACT_RELU, y_ref, ws,
+                             A.NOALLOC_SCRATCH_BYTES)
+    assert st == 0, A.status_string(st)
+    ref = O.conv2d(to64(x), to64(wt), to64(b), pad=1, act=O.ACT_RELU)
+    outs = []
+    for call in range(2):
+        y_na = torch.full((n, h, w, co), float("nan"), dtype=torch.bfloat16, device="cuda")
+        st = A.acnn_conv2d_fused_noalloc(d, xd, wd, bd, None, None, A.RES_NONE, A.ACT_RELU, y_na)
+        assert st == 0, A.status_string(st)
+        torch.cuda.synchronize()
+        assert_bitexact(y_na, y_ref, f"call {call} vs workspace entry")
+        assert_parity(y_na, ref, torch.bfloat16, f"call {call} vs oracle")
+        outs.append(y_na)
+    assert torch.equal(outs[0], outs[1])
     assert A.acnn_last_device_status() == 0
