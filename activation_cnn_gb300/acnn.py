@@ -43,7 +43,7 @@ EXPORTS = (
     "acnn_status_string", "acnn_last_device_status", "acnn_set_wait_budget",
     "acnn_section_begin", "acnn_section_end", "acnn_section_launch", "acnn_section_destroy",
     "acnn_device_sm_count", "acnn_conv2d_fused_noalloc", "acnn_conv2d_plan",
-    "acnn_conv2d_fused_cat2",
+    "acnn_conv2d_fused_cat2", "acnn_conv2d_force_plan", "acnn_conv2d_force_path",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # ACNN_NOALLOC_SCRATCH_BYTES in include/acnn.h
 
@@ -108,6 +108,8 @@ def lib() -> ctypes.CDLL:
         L.acnn_device_sm_count.argtypes = []
         L.acnn_conv2d_fused_noalloc.argtypes = [D, _P, _P, _P, _P, _P, _I, _I, _P, _P]
         L.acnn_conv2d_plan.argtypes = [D, ctypes.c_size_t] + [ctypes.POINTER(_I)] * 3
+        L.acnn_conv2d_force_plan.argtypes = [_I, _I, _I]
+        L.acnn_conv2d_force_path.argtypes = [_I, _I]
         _lib = L
     return _lib
 
@@ -186,6 +188,14 @@ def acnn_conv2d_plan(desc, ws_bytes):
     st = lib().acnn_conv2d_plan(ctypes.byref(desc), ws_bytes, ctypes.byref(rows),
                                 ctypes.byref(bn), ctypes.byref(sp))
     return st, rows.value, bn.value, sp.value
+
+
+def acnn_conv2d_force_plan(bn: int, rows: int = 128, splits: int = 1) -> int:
+    return lib().acnn_conv2d_force_plan(bn, rows, splits)
+
+
+def acnn_conv2d_force_path(path: int, variant: int = 0) -> int:
+    return lib().acnn_conv2d_force_path(path, variant)
 
 
 def acnn_conv2d_path(desc) -> int:

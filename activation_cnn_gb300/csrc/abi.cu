@@ -205,6 +205,10 @@ struct Route {
     acnn_conv_desc g;   // geometry of the tensor-core launch (NHWC)
 };
 
+// Path forced by acnn_conv2d_force_path (0: the router decides).
+std::atomic<int> g_force_path{0};
+std::atomic<int> g_tiny_shuffle{kTinyWeightsByShuffle};
+
 Route route(const acnn_conv_desc* d, int oh, int ow) {
     Route r{0, 0, 0, *d};
     const size_t es = elem_size(d->dtype);
@@ -215,6 +219,11 @@ Route route(const acnn_conv_desc* d, int oh, int ow) {
             r.stage_w = round256((size_t)d->c_out * d->kh * d->kw * d->c_in * es);
         }
         r.g.layout = ACNN_NHWC;
+    } else if (tiny_conv_ok(*d, oh, ow) && (g_force_path.load() == 4 || !packed_path_ok(d, oh, ow))) {
+        // direct kernel for 3/6/7 input channels (no staging): used where the
+        // packed path cannot go, or when forced; the packed tensor-core path
+        // measured faster on the RGB stem and the 7-plane frame input
+        r.path = 4;
     } else if (packed_path_ok(d, oh, ow)) {
         const int kp = packed_k(d);
         r.path = 3;
@@ -246,10 +255,30 @@ size_t acnn_conv2d_workspace_size(const acnn_conv_desc* d) {
     int oh, ow;
     if (check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK) return 0;
     const Route r = route(d, oh, ow);
-    if (r.path == 0) return 0;
+    if (r.path == 0 || r.path == 4) return 0;
     // NCHW-output convs are never split (no partial sums to hold)
     const size_t part = d->layout == ACNN_NHWC ? igemm_plan(r.g, oh, ow, SIZE_MAX).part_bytes : 0;
     return r.stage_x + r.stage_w + round256(part);
+}
+
+int acnn_conv2d_force_path(int path, int variant) {
+    if (path != 0 && path != 4) return ACNN_ERR_BAD_ENUM;
+    if (variant != 0 && variant != 1) return ACNN_ERR_BAD_ENUM;
+    g_tiny_shuffle.store(path == 4 ? variant : kTinyWeightsByShuffle);
+    g_force_path.store(path);
+    return ACNN_OK;
+}
+
+int acnn_conv2d_force_plan(int bn, int rows, int splits) {
+    if (bn == 0) {
+        force_plan(0, 0, 0);
+        return ACNN_OK;
+    }
+    if ((bn != 32 && bn != 64 && bn != 128 && bn != 256) || (rows != 128 && rows != 256) ||
+        splits < 1 || splits > 64)
+        return ACNN_ERR_BAD_GEOMETRY;
+    force_plan(bn, rows / 128, splits);
+    return ACNN_OK;
 }
 
 int acnn_conv2d_plan(const acnn_conv_desc* d, size_t ws_bytes, int* rows, int* bn,
@@ -258,7 +287,7 @@ int acnn_conv2d_plan(const acnn_conv_desc* d, size_t ws_bytes, int* rows, int* b
     if (!rows || !bn || !splits || check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK)
         return -1;
     const Route r = route(d, oh, ow);
-    if (r.path == 0 || ws_bytes < r.stage_x + r.stage_w) return -1;
+    if (r.path == 0 || r.path == 4 || ws_bytes < r.stage_x + r.stage_w) return -1;
     const size_t budget = d->layout == ACNN_NHWC ? ws_bytes - r.stage_x - r.stage_w : 0;
     const IgemmPlan pl = igemm_plan(r.g, oh, ow, budget);
     *rows = 128 * pl.ms;
@@ -325,6 +354,7 @@ int conv_fused_impl(const acnn_conv_desc* d, const void* x, const void* w, bool 
 
     const Route r = route(d, oh, ow);
     if (r.path == 0) return status_of(launch_direct_conv(a, s));
+    if (r.path == 4) return status_of(launch_tiny_conv(a, g_tiny_shuffle.load(), s));
 
     // Workspace: [staged x | staged w] (required for NCHW and packed convs; no
     // staged w with prepacked weights), then split-K partial sums (optional: a
@@ -397,7 +427,7 @@ size_t acnn_conv2d_prepacked_workspace_size(const acnn_conv_desc* d) {
     int oh, ow;
     if (check_desc(d) != ACNN_OK || conv_out(d, &oh, &ow) != ACNN_OK) return 0;
     const Route r = route(d, oh, ow);
-    if (r.path == 0) return 0;
+    if (r.path == 0 || r.path == 4) return 0;
     const size_t part = d->layout == ACNN_NHWC ? igemm_plan(r.g, oh, ow, SIZE_MAX).part_bytes : 0;
     return r.stage_x + round256(part);
 }
@@ -418,7 +448,7 @@ int acnn_conv2d_prepack(const acnn_conv_desc* d, const void* w, void* w_packed,
     cudaError_t e;
     if (r.path == 3)
         e = launch_weight_pack(*d, r.g.c_in, w, w_packed, s);
-    else if (r.path != 0 && d->layout == ACNN_NCHW)
+    else if ((r.path == 1 || r.path == 2) && d->layout == ACNN_NCHW)
         e = launch_nchw_to_nhwc(d->c_out, d->c_in, d->kh * d->kw, 2, w, w_packed, s);
     else
         e = cudaMemcpyAsync(w_packed, w, wb, cudaMemcpyDeviceToDevice, s);

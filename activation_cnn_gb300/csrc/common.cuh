@@ -113,6 +113,8 @@ struct IgemmPlan {
     int bk;             // channels per k-block: 64, or 32 when C_in <= 32
 };
 IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget);
+// Force the tile shape of later plans (bn = 0 clears; see acnn_conv2d_force_plan).
+void force_plan(int bn, int ms, int splits);
 
 int sm_count();
 int* device_status_ptr();         // device address of the status word
@@ -120,6 +122,14 @@ int ensure_smem_optin(const void* kernel, size_t bytes);  // per (kernel, device
 long long wait_budget_polls();    // 0 = default (time-bounded)
 
 cudaError_t launch_direct_conv(const ConvArgs& a, cudaStream_t s);
+// Direct 3x3 conv for fp16/bf16 inputs of 3, 6 or 7 channels (conv_tiny.cu):
+// whether it serves a geometry, and the launch (weights broadcast through
+// shared memory, or by warp shuffles when weights_by_shuffle is set).
+bool tiny_conv_ok(const acnn_conv_desc& d, int oh, int ow);
+cudaError_t launch_tiny_conv(const ConvArgs& a, int weights_by_shuffle, cudaStream_t s);
+// The weight-broadcast form of the tiny-C_in kernel by default (shared-memory
+// broadcast: measured faster than the shuffle form on the frame input).
+constexpr int kTinyWeightsByShuffle = 0;
 // tensor-core path; returns ACNN_OK or an ACNN_ERR_* status
 int launch_igemm_conv(const ConvArgs& a, cudaStream_t s);
 

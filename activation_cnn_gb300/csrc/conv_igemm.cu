@@ -30,6 +30,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -1224,7 +1226,45 @@ int launch_typed(const ConvArgs& a, const IgemmPlan& pl, const Maps& m, const Pa
 // expect-tx and two TMA issues of one thread) and the MMA time of the block;
 // units run in waves of one per SM; the layer cannot beat its HBM traffic;
 // split-K adds a reduce launch that reads the fp32 partials and writes y.
+// Tile shape forced by acnn_conv2d_force_plan (bn = 0: none), for plan sweeps.
+namespace {
+std::atomic<int> g_force_bn{0}, g_force_ms{0}, g_force_splits{0};
+
+bool instantiated(int bk, int bn, int ms) {
+    if (bk == 32) return ms == 2 && (bn == 128 || bn == 64 || bn == 32);
+    return (bn == 256 && ms == 1) || ((bn == 128 || bn == 64) && (ms == 1 || ms == 2));
+}
+}  // namespace
+
+void force_plan(int bn, int ms, int splits) {
+    g_force_ms.store(ms);
+    g_force_splits.store(splits);
+    g_force_bn.store(bn);
+}
+
 IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget) {
+    {
+        // a forced shape, when this geometry has an instantiation of it; the
+        // split count is lowered until the split units fit in one wave and
+        // their partial tiles in the budget
+        const int fbn = g_force_bn.load(), fms = g_force_ms.load();
+        const int bk = d.c_in <= 32 ? 32 : 64;
+        if (fbn > 0 && instantiated(bk, fbn, fms)) {
+            const long long M = (long long)d.n * oh * ow;
+            const int num_kb = d.kh * d.kw * ((d.c_in + bk - 1) / bk);
+            const long long tiles = ((M + BM * fms - 1) / (BM * fms)) * ((d.c_out + fbn - 1) / fbn);
+            for (int sp = std::max(1, std::min(g_force_splits.load(), num_kb)); sp >= 1; --sp) {
+                const int kbs = (num_kb + sp - 1) / sp;
+                const int eff = (num_kb + kbs - 1) / kbs;
+                const size_t tile_bytes = (size_t)BM * fms * fbn * sizeof(float);
+                const size_t part = eff > 1 ? (((size_t)tiles * 4 + 255) & ~(size_t)255) +
+                                                  (size_t)tiles * eff * tile_bytes
+                                            : 0;
+                if (eff == 1 || (part <= part_budget && tiles * eff <= sm_count()))
+                    return IgemmPlan{fbn, fms, eff, kbs, part, bk};
+            }
+        }
+    }
     const double kIssueUs = 0.30, kMmaUsPerMflop = 1.0 / 15.0, kHbmBytesPerUs = 6.0e6;
     const double kSplitUs = 1.5, kEpiUsPerChunk = 0.15;
     const double kL2GBsPerSm = 100.0, kL2Bytes = 96.0e6;

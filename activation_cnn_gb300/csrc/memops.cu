@@ -397,6 +397,43 @@ __global__ void __launch_bounds__(kThreads) resize_nchw_kernel(
     }
 }
 
+// NCHW resize, one block per output row (plane nc, row oy): the row's source
+// rows and y weight are computed once, each thread produces V consecutive
+// outputs of the row (its taps are L1 hits: a x8 upsample reads 2-3 source
+// columns for 8 outputs) and writes them as one 16-byte vector.  Same
+// arithmetic, in the same order, as resize_nchw_kernel.
+template <typename Ti, typename To, int V>
+__global__ void __launch_bounds__(kThreads) resize_nchw_rows_kernel(
+    const Ti* __restrict__ x, To* __restrict__ y, int mode, int H, int W, int OH, int OW,
+    float sy, float sx) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+    const long long r = blockIdx.x;  // nc * OH + oy
+    const int oy = (int)(r % OH);
+    const long long nc = r / OH;
+    const int ox0 = (blockIdx.y * kThreads + threadIdx.x) * V;
+    if (ox0 >= OW) return;
+    const Ti* plane = x + nc * H * W;
+    Vec<To, V> o;
+    if (mode == ACNN_RESIZE_NEAREST) {
+        const Ti* row = plane + (long long)(((long long)oy * H) / OH) * W;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            o.v[v] = from_f32<To>(to_f32(row[((long long)(ox0 + v) * W) / OW]));
+    } else {
+        const BilinearTap ty = bilinear_tap(oy, sy, H);
+        const Ti* ra = plane + (long long)ty.a * W;
+        const Ti* rb = plane + (long long)ty.b * W;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const BilinearTap tx = bilinear_tap(ox0 + v, sx, W);
+            const float top = mixf(to_f32(ra[tx.a]), to_f32(ra[tx.b]), tx.f);
+            const float bot = mixf(to_f32(rb[tx.a]), to_f32(rb[tx.b]), tx.f);
+            o.v[v] = from_f32<To>(mixf(top, bot, ty.f));
+        }
+    }
+    *reinterpret_cast<Vec<To, V>*>(y + r * OW + ox0) = o;
+}
+
 // ----------------------------------------------------------------------------
 // concat: rtdetr_gpu.rs CONCAT_SRC, y = [a | b] along channels.  NHWC: per
 // pixel; NCHW: per image, the c_a planes of a then the c_b planes of b.  Both
@@ -913,9 +950,18 @@ cudaError_t resize_typed(int mode, int n, int c, int h, int w, int oh, int ow, i
                 xt, yt, mode, n, h, w, c, oh, ow, sy, sx);
         }
     } else {
-        long long work = (long long)n * c * oh * ow;
-        launch_pdl(resize_nchw_kernel<Ti, To>, grid_occ(resize_nchw_kernel<Ti, To>, work, kThreads), kThreads, 0, s, 
-            xt, yt, mode, n * c, h, w, oh, ow, sy, sx);
+        constexpr int VO = 16 / sizeof(To);
+        const long long rows = (long long)n * c * oh;
+        const int chunks = (ow / VO + kThreads - 1) / kThreads;
+        if (ow % VO == 0 && rows <= 0x7fffffffLL && chunks <= 65535) {
+            // whole 16-byte output vectors per row (rows start aligned)
+            launch_pdl(resize_nchw_rows_kernel<Ti, To, VO>, dim3((unsigned)rows, chunks), kThreads, 0,
+                       s, xt, yt, mode, h, w, oh, ow, sy, sx);
+        } else {
+            long long work = (long long)n * c * oh * ow;
+            launch_pdl(resize_nchw_kernel<Ti, To>, grid_occ(resize_nchw_kernel<Ti, To>, work, kThreads), kThreads, 0, s,
+                xt, yt, mode, n * c, h, w, oh, ow, sy, sx);
+        }
     }
     return cudaGetLastError();
 }

@@ -291,6 +291,69 @@ def time_steps(net, stream, steps, flush):
     return [a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends)]
 
 
+def time_call(fn, stream, flush, reps):
+    """Median device time of fn(stream) captured as a graph, L2 flushed before each replay."""
+    import torch
+    from activation_cnn_gb300 import acnn as A
+    with torch.cuda.stream(stream):
+        fn(stream)
+    stream.synchronize()
+    sec = A.Section(stream)
+    with torch.cuda.stream(stream):
+        with sec:
+            fn(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ts = []
+    for _ in range(reps):
+        flush()
+        e0.record(stream)
+        sec.launch(stream)
+        e1.record(stream)
+        stream.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    sec.close()
+    return statistics.median(ts)
+
+
+def tiny_cin_compare(dev, stream, flush, reps=30):
+    """The convs with 3 or 7 input channels (the backbone's RGB stem, the frame
+    stack's first conv) on each kernel that serves them: the packed tensor-core
+    path the router uses, and the direct kernel with its weights broadcast from
+    shared memory or by warp shuffles (forced with acnn_conv2d_force_path)."""
+    import torch
+    from activation_cnn_gb300 import acnn as A
+    from activation_cnn_gb300 import inputs as G
+    out = {}
+    for name, (n, c, h, w, co, layout, dt, act) in {
+            "rgb_stem_8x640x640_3to32_s2_bf16_nhwc": (8, 3, 640, 640, 32, G.NHWC, G.BF16, A.ACT_RELU),
+            "frame_input_7x272x480_7to120_s2_f16_nchw": (1, 7, 272, 480, 120, G.NCHW, G.F16,
+                                                        A.ACT_PRELU)}.items():
+        x = G.tensor(91, name, G.activation_shape(layout, n, c, h, w), "uniform", 0.0, 1.0,
+                     dtype=dt).to(dev)
+        wt = G.conv_weight(91, name, co, c, 3, 3, layout, dt).to(dev)
+        b = G.conv_bias(91, name, co).to(dev)
+        al = G.prelu_alpha(91, name, co).to(dev)
+        d = A.conv_desc(x, co, 3, 3, 2, 1, layout)
+        y = torch.empty(A.conv_out_shape(d), dtype=x.dtype, device=dev)
+        flops = 2.0 * y.numel() * c * 9  # y elements x (c_in x 3 x 3) multiply-adds
+        res = {}
+        for label, (path, variant) in {"packed_tensor_core": (0, 0), "direct_smem_weights": (4, 0),
+                                       "direct_shfl_weights": (4, 1)}.items():
+            A.acnn_conv2d_force_path(path, variant)
+            ws_bytes = A.acnn_conv2d_workspace_size(d)
+            ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+            def fn(s, ws=ws, ws_bytes=ws_bytes):
+                A.check(A.acnn_conv2d_fused(d, x, wt, b, al, None, A.RES_NONE, act, y, ws,
+                                            ws_bytes, s), name)
+            t = time_call(fn, stream, flush, reps)
+            res[label] = {"path": A.acnn_conv2d_path(d), "us": round(t * 1e6, 2),
+                          "TFLOP_s": round(flops / t / 1e12, 2)}
+        A.acnn_conv2d_force_path(0, 0)
+        out[name] = res
+    return out
+
+
 def measure_config(name, dev, stream, flush, steps, pk):
     """One of the other workloads (single conv, fp32 stem, bottleneck blocks,
     frame stack), timed like the main one: step time, then every op's share of
@@ -575,6 +638,7 @@ def run_ours(args, rank, world, local_rank):
     if args.configs and args.workload == "backbone" and args.batch in (None, 8):
         line["configs"] = {name: measure_config(name, dev, stream, flush, 50, pk)
                            for name in ("conv1", "stem", "block", "block_down", "frame")}
+        line["tiny_cin_conv"] = tiny_cin_compare(dev, stream, flush)
     return line
 
 

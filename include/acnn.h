@@ -144,7 +144,13 @@ size_t acnn_conv2d_workspace_size(const acnn_conv_desc* d);
 /* Which kernel acnn_conv2d_fused would run for d: 0 = direct FFMA,
  * 1 = tcgen05 implicit GEMM with a tiled A load (1x1/s1/p0),
  * 2 = tcgen05 implicit GEMM with TMA im2col A loads,
- * 3 = explicit im2col pack, then the tcgen05 GEMM; negative = invalid. */
+ * 3 = explicit im2col pack, then the tcgen05 GEMM,
+ * 4 = direct 3x3 kernel for fp16/bf16 inputs of 3, 6 or 7 channels (the input
+ *     patch staged in shared memory, weights broadcast from shared memory or by
+ *     warp shuffles); chosen only where path 3 cannot serve the geometry (path 3
+ *     measured faster on the RGB stem and the 7-plane frame input) or when
+ *     forced with acnn_conv2d_force_path;
+ * negative = invalid. */
 int acnn_conv2d_path(const acnn_conv_desc* d);
 
 /* Tensor-core plan for d given ws_bytes of workspace: output pixels per tile
@@ -153,6 +159,26 @@ int acnn_conv2d_path(const acnn_conv_desc* d);
  * path or ws_bytes is below the required staging (host pointers; the plan
  * depends on the current device's SM count). */
 int acnn_conv2d_plan(const acnn_conv_desc* d, size_t ws_bytes, int* rows, int* bn, int* splits);
+
+/* Tuning hook (the offline counterpart of rt.js's one-shot conv autotune,
+ * tuneConvRB): force the tensor-core tile shape of every later conv call,
+ * workspace query and plan query in this process -- bn output channels
+ * (32/64/128/256) x rows output pixels (128/256) per tile, at most `splits`
+ * K splits.  A shape the geometry has no kernel instantiation for is ignored
+ * (the plan query reports what is used); splits are lowered until the split
+ * units fit in one wave on the device and their partial sums in the
+ * workspace.  bn = 0 restores the planner.  Process-wide, not per stream:
+ * meant for tile sweeps (activation_cnn_gb300/tune.py), not for serving.
+ * Returns ACNN_OK, or ACNN_ERR_BAD_GEOMETRY for values outside those sets. */
+int acnn_conv2d_force_plan(int bn, int rows, int splits);
+
+/* Tuning hook: force the direct tiny-C_in kernel (path = 4) for every later
+ * conv whose geometry it serves (3, 6 or 7 input channels, 3x3, stride 1 or 2,
+ * fp16/bf16), with its weights broadcast from shared memory (variant 0) or by
+ * warp shuffles (variant 1); path = 0 restores the router.  Process-wide,
+ * like acnn_conv2d_force_plan: for measuring one kernel against the other.
+ * Returns ACNN_OK or ACNN_ERR_BAD_ENUM. */
+int acnn_conv2d_force_path(int path, int variant);
 
 /* ---- prepacked weights --------------------------------------------------------
  * The weights in the form the conv kernels read, made once (the pages convert
@@ -166,7 +192,7 @@ int acnn_conv2d_plan(const acnn_conv_desc* d, size_t ws_bytes, int* rows, int* b
  *                                  overlap with w): the packed [c_out][kp]
  *                                  matrix (K = kh*kw*c_in in (ky, kx, ci) order,
  *                                  zero-padded to kp) on path 3, OHWI on paths
- *                                  1-2, an unchanged copy on path 0;
+ *                                  1-2, an unchanged copy on paths 0 and 4;
  *   acnn_conv2d_prepacked_workspace_size(d)
  *                                  the workspace of the prepacked call: the
  *                                  staged activation only, plus split-K sums;

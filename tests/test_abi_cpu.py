@@ -79,6 +79,8 @@ def test_conv_path_selection(A):
     assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=64, stride=2)) == 2
     assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=32)) == 3         # tiny C_in: packed
     assert A.acnn_conv2d_path(desc(A, c_in=7, c_out=120, layout=1, dtype=1)) == 3
+    assert A.acnn_conv2d_path(desc(A, c_in=5, c_out=32)) == 3
+    assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=32, dtype=0)) == 0  # fp32: FFMA direct
     assert A.acnn_conv2d_path(desc(A, dtype=0)) == 0                  # fp32
     assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=120)) == 2       # C_out % 8 == 0
     assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=30)) == 0        # C_out % 8 != 0
@@ -87,10 +89,30 @@ def test_conv_path_selection(A):
     assert A.acnn_conv2d_path(desc(A, c_in=100, c_out=64, kh=3, kw=3)) == 0  # K > 512
     assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=4096)) == 2
     assert A.acnn_conv2d_path(desc(A, c_in=64, c_out=4104)) == 0      # C_out > 4096
-    assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=4104)) == 0
+    # beyond the packed path's C_out limit the tiny-C_in direct kernel serves
+    assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=4104)) == 4
+    assert A.acnn_conv2d_path(desc(A, c_in=5, c_out=4104)) == 0
+    assert A.acnn_conv2d_workspace_size(desc(A, c_in=3, c_out=4104)) == 0
     assert A.acnn_conv2d_workspace_size(desc(A, c_in=3, c_out=32)) >= 64 * 32 * 2
     assert A.acnn_conv2d_path(desc(A, n=0)) == -1
     assert A.acnn_conv2d_workspace_size(desc(A, c_in=64, c_out=64)) == 0
+
+
+def test_force_path_selects_the_tiny_kernel(A):
+    """The tuning hook routes the 3/6/7-channel 3x3 convs to the direct kernel
+    (and nothing else), and path 0 restores the router."""
+    try:
+        assert A.acnn_conv2d_force_path(4, 1) == 0
+        assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=32)) == 4
+        assert A.acnn_conv2d_path(desc(A, c_in=6, c_out=120, layout=1, dtype=1)) == 4
+        assert A.acnn_conv2d_workspace_size(desc(A, c_in=7, c_out=120, layout=1, dtype=1)) == 0
+        assert A.acnn_conv2d_path(desc(A, c_in=5, c_out=32)) == 3      # not a tiny geometry
+        assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=32, stride=3)) == 3
+        assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=32, dtype=0)) == 0
+    finally:
+        assert A.acnn_conv2d_force_path(0, 0) == 0
+    assert A.acnn_conv2d_path(desc(A, c_in=3, c_out=32)) == 3
+    assert A.acnn_conv2d_force_path(2, 0) == 7 and A.acnn_conv2d_force_path(4, 2) == 7
 
 
 def test_conv_out_hw(A):

@@ -193,6 +193,25 @@ def test_conv_prepacked_equals_plain(case):
     assert_parity(y2, ref, TDT[dt], name)
 
 
+@pytest.mark.parametrize("layout", [G.NHWC, G.NCHW])
+def test_conv_tiny_prepacked_equals_plain(layout, tiny_path):
+    """On the direct tiny-C_in kernel the prepacked weights are an unchanged copy."""
+    dt = "f16"
+    x = G.tensor(14, "tpp.x", G.activation_shape(layout, 1, 7, 30, 44), "normal",
+                 dtype=DT[dt]).cuda()
+    wt = G.conv_weight(14, "tpp", 48, 7, 3, 3, layout, DT[dt]).cuda()
+    b = G.conv_bias(14, "tpp", 48).cuda()
+    y = A.conv2d_fused(x, wt, b, stride=2, pad=1, act=A.ACT_RELU, layout=layout)
+    d = A.conv_desc(x, 48, 3, 3, 2, 1, layout)
+    assert A.acnn_conv2d_path(d) == 4
+    wp = A.conv2d_prepack(d, wt)
+    y2 = torch.empty_like(y)
+    A.check(A.acnn_conv2d_fused_prepacked(d, x, wp, b, None, None, A.RES_NONE, A.ACT_RELU, y2,
+                                          None, 0, None), "tiny prepacked")
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+
+
 def test_conv_tensor_no_bias():
     y, ref = conv_case("nobias", 1, 9, 9, 64, 64, 1, 1, 0, "f16", bias=False)
     assert_parity(y, ref, torch.float16)
@@ -265,6 +284,7 @@ PACKED_CASES = [
     ("stem_s2_big", 2, 160, 150, 3, 32, 3, 3, 2, 1, "bf16", G.NHWC),
     ("prep7_nchw_f16", 1, 34, 60, 7, 120, 3, 3, 2, 1, "f16", G.NCHW),
     ("cin5_7x7_s2", 1, 41, 37, 5, 64, 7, 7, 2, 3, "bf16", G.NHWC),
+    ("cin5_3x3_s2", 2, 33, 30, 5, 32, 3, 3, 2, 1, "bf16", G.NHWC),
     ("nonsq_1x3", 2, 12, 17, 16, 48, 1, 3, 1, 0, "f16", G.NHWC),
     ("cin12_3x3", 1, 23, 29, 12, 40, 3, 3, 1, 1, "bf16", G.NCHW),
 ]
@@ -278,6 +298,65 @@ def test_conv_packed_path(case):
     assert A.acnn_conv2d_path(d) == 3
     y, ref = conv_case(name, n, h, w, cin, cout, k, s, p, dt, layout=layout, kw=kw)
     assert_parity(y, ref, TDT[dt], name)
+
+
+# ---------------------------------------------------------------- tiny C_in (path 4)
+TINY_CASES = [
+    # name, n, h, w, cin, cout, s, p, dt, layout
+    ("stem_rgb", 2, 33, 30, 3, 32, 2, 1, "bf16", G.NHWC),
+    ("stem_rgb_big", 2, 160, 150, 3, 32, 2, 1, "bf16", G.NHWC),
+    ("stem_rgb_f16", 1, 64, 66, 3, 32, 2, 1, "f16", G.NHWC),
+    ("frame7", 1, 34, 60, 7, 120, 2, 1, "f16", G.NCHW),
+    ("frame7_bf16", 1, 36, 44, 7, 120, 2, 1, "bf16", G.NCHW),
+    ("frame6", 1, 68, 120, 6, 120, 2, 1, "f16", G.NCHW),
+    ("s1_nhwc", 2, 21, 37, 3, 40, 1, 1, "bf16", G.NHWC),   # ragged channel chunk
+    ("s1_nchw", 1, 19, 45, 7, 24, 1, 1, "f16", G.NCHW),    # OW % 4 != 0: scalar stores
+    ("nhwc_cout12", 1, 17, 29, 3, 12, 2, 1, "bf16", G.NHWC),  # C_out % 8 != 0
+    ("p0_s2", 2, 23, 41, 6, 64, 2, 0, "f16", G.NCHW),
+    ("p2_s1", 1, 9, 12, 7, 16, 1, 2, "bf16", G.NHWC),
+    ("one_px", 3, 1, 1, 3, 8, 1, 1, "bf16", G.NHWC),
+]
+
+
+@pytest.fixture(params=[0, 1], ids=["smem_weights", "shfl_weights"])
+def tiny_path(request):
+    """Route the tiny-C_in geometries to the direct kernel (the router prefers the
+    packed path for them), with weights broadcast from shared memory or by warp
+    shuffles."""
+    assert A.acnn_conv2d_force_path(4, request.param) == 0
+    yield request.param
+    assert A.acnn_conv2d_force_path(0, 0) == 0
+
+
+@pytest.mark.parametrize("case", TINY_CASES, ids=[c[0] for c in TINY_CASES])
+def test_conv_tiny_path(case, tiny_path):
+    """3, 6 or 7 input channels, fp16/bf16, 3x3: the direct kernel with the input
+    patch in shared memory."""
+    name, n, h, w, cin, cout, s, p, dt, layout = case
+    d = A.ConvDesc(n, h, w, cin, cout, 3, 3, s, p, layout, DT[dt])
+    assert A.acnn_conv2d_path(d) == 4 and A.acnn_conv2d_workspace_size(d) == 0
+    y, ref = conv_case("tiny" + name, n, h, w, cin, cout, 3, s, p, dt, layout=layout,
+                       act=A.ACT_PRELU if layout == G.NCHW else A.ACT_RELU)
+    assert_parity(y, ref, TDT[dt], name)
+
+
+@pytest.mark.parametrize("act", [A.ACT_NONE, A.ACT_RELU, A.ACT_SILU, A.ACT_PRELU])
+@pytest.mark.parametrize("res_mode", [A.RES_NONE, A.RES_ADD_THEN_ACT, A.RES_ACT_THEN_ADD])
+@pytest.mark.parametrize("layout", [G.NHWC, G.NCHW])
+def test_conv_tiny_epilogue_modes(act, res_mode, layout, tiny_path):
+    y, ref = conv_case(f"tepi{act}{res_mode}{layout}", 2, 18, 36, 7, 40, 3, 2, 1, "f16",
+                       layout=layout, act=act, res_mode=res_mode)
+    assert_parity(y, ref, torch.float16, f"tiny act{act} res{res_mode} layout{layout}")
+
+
+@pytest.mark.parametrize("layout", [G.NHWC, G.NCHW])
+@pytest.mark.parametrize("s", [1, 2])
+def test_conv_tiny_integer_bitexact(layout, s, tiny_path):
+    """Integer data: every fp32 partial sum is exact, so the stored value is the
+    oracle's rounded once."""
+    y, ref = conv_case(f"tint{layout}{s}", 2, 19, 26, 7, 48, 3, s, 1, "bf16", layout=layout,
+                       act=A.ACT_PRELU, integer=True)
+    assert_bitexact(y, O.round_storage(ref, O.BF16), f"tiny int layout{layout} s{s}")
 
 
 def test_conv_direct_nonsquare():
