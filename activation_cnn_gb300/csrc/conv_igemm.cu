@@ -68,6 +68,11 @@ template <int BN, int MS, int BK> struct Cfg {
     static constexpr uint32_t kABytes = BM * BK * 2;  // one 128-row block
     static constexpr uint32_t kAB = MS * kABytes;     // A bytes per stage
     static constexpr uint32_t kBBytes = BN * BK * 2;
+    // halo rows (3x3, stride 1): one box of TM + 2 virtual pixels per kernel
+    // row serves the three horizontal taps; the slot rounded up to 1024 bytes
+    // so that every stage starts on a swizzle-atom boundary
+    static constexpr uint32_t kAhTx = (BM * MS + 2) * BK * 2;
+    static constexpr uint32_t kABh = (kAhTx + 1023u) / 1024u * 1024u;
     static constexpr uint32_t kTmemCols = 2 * MS * BN < 32 ? 32 : 2 * MS * BN;
     static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
     static_assert(kSmemFixed + (size_t)kEpiWarps * kMaxResDepth * kStageBytes + 2 * (kAB + kBBytes) +
@@ -85,7 +90,16 @@ struct Params {
     float* part;
     unsigned* cnt;
     int OW, OHW, S, P;
-    int a_mode;       // 0: tiled A (1x1/s1/p0); 1: im2col A
+    // Halo rows (a_mode 2): output pixels are indexed on a virtual grid whose
+    // rows are vw = OW + 2 wide (the two extra columns per row are computed
+    // and discarded), M counts virtual pixels, and K runs over (kernel row,
+    // channel block): num_kbh = 3 x kb_per_tap units of three taps each.
+    // Without halo rows vw = OW.  vw_magic = floor((2^64 - 1) / vw) + 1 gives
+    // v / vw as the high 64 bits of v * vw_magic (exact for v < 2^32).
+    int vw;
+    unsigned long long vw_magic;
+    int num_kbh;
+    int a_mode;       // 0: tiled A (1x1/s1/p0); 1: im2col A; 2: im2col A with halo rows
     int c_split;      // channels [c_split, C_in) come from the second A map (0: none)
     int out_layout;   // ACNN_NHWC or ACNN_NCHW for y and the residual
     int act, res_mode;
@@ -101,6 +115,17 @@ struct Params {
     int par_floats;    // NHWC epilogue: shared copy of bias [cpad] then alpha [cpad] (0: none)
     int ring_slots;    // 2 KB epilogue slots per epilogue warp (NHWC ring / NCHW transpose stage)
 };
+
+// Output pixel (row of the GEMM) v -> index of the real output pixel in
+// [0, N*OH*OW), or -1 for a virtual column of a halo-row grid or a row past
+// the end of the tile range.
+__device__ __forceinline__ int real_pixel(const Params& p, int v) {
+    if (v >= p.M) return -1;
+    if (p.a_mode != 2) return v;
+    const int row = (int)__umul64hi((unsigned long long)v, p.vw_magic);  // v / vw
+    const int j = v - row * p.vw;
+    return j < p.OW ? row * p.OW + j : -1;
+}
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -352,6 +377,16 @@ template <int BK> __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) 
            | (layout << 61);
 }
 
+// Descriptor of an operand that starts inside a swizzle atom (the halo-row A
+// operand of horizontal tap kx starts kx rows into its stage): the tensor core
+// takes the swizzle phase of each row from its absolute shared-memory address,
+// the same address bits the TMA swizzled the rows by, so the plain descriptor
+// at the shifted start is right (measured: also setting the matrix base offset
+// field to the start's phase, bits 49-51, gives wrong sums).
+template <int BK> __device__ __forceinline__ uint64_t smem_desc_at(uint32_t saddr) {
+    return smem_desc<BK>(saddr);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B both bf16 or
 // both fp16, both K-major, N >> 3 and M >> 4 in their fields.
 __host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool bf16) {
@@ -472,10 +507,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int S = p.stages;
     const bool bres = p.b_resident != 0;
+    const bool halo = p.a_mode == 2;
+    // per stage: A (one box; TM + 2 virtual pixels with halo rows) and, unless
+    // the weights are resident, B (one tap's block; three with halo rows)
+    const uint32_t a_slot = halo ? C::kABh : C::kAB;
+    const uint32_t b_slot = halo ? 3u * C::kBBytes : C::kBBytes;
     uint8_t* sA = smem_raw;
-    uint8_t* sB = sA + S * C::kAB;  // B ring (S slots) or all num_kb resident B blocks
+    uint8_t* sB = sA + (size_t)S * a_slot;  // B ring (S slots) or all num_kb resident B blocks
     // epilogue slots: kEpiWarps x ring_slots x 2 KB, 1024-aligned
-    uint8_t* sR = sB + (size_t)(bres ? p.num_kb : S) * C::kBBytes;
+    uint8_t* sR = sB + (bres ? (size_t)p.num_kb * C::kBBytes : (size_t)S * b_slot);
     float* sP = reinterpret_cast<float*>(sR + (size_t)kEpiWarps * p.ring_slots * kStageBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sP + p.par_floats);
     // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, weights
@@ -547,16 +587,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            const uint32_t stage_tx = C::kAB + (bres ? 0u : C::kBBytes);
+            const uint32_t stage_tx =
+                halo ? C::kAhTx + (bres ? 0u : 3u * C::kBBytes) : C::kAB + (bres ? 0u : C::kBBytes);
+            const int num_k = halo ? p.num_kbh : p.num_kb;
+            const int OHV = p.OHW / p.OW * p.vw;  // virtual pixels per image
             for (int unit = blockIdx.x; ok && unit < num_tiles; unit += gridDim.x) {
                 const int tile = unit / p.splits, split = unit - tile * p.splits;
                 const int m0 = (tile / p.num_n_tiles) * TM;
                 const int n0 = (tile % p.num_n_tiles) * BN;
                 const int kb0 = split * p.kb_per_split;
-                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-                // window corner of the tile's first output pixel
-                const int img = m0 / p.OHW, r = m0 % p.OHW;
-                const int wc = (r % p.OW) * p.S - p.P, hc = (r / p.OW) * p.S - p.P;
+                const int kb1 = min(num_k, kb0 + p.kb_per_split);
+                // window corner of the tile's first (virtual) output pixel
+                const int img = m0 / OHV, r = m0 % OHV;
+                const int wc = (r % p.vw) * p.S - p.P, hc = (r / p.vw) * p.S - p.P;
+                if (halo) {
+                    // unit kb = (kernel row ky, channel block cb): one A box of
+                    // TM + 2 virtual pixels at tap (0, ky), the B blocks of taps
+                    // (ky, 0..2) unless resident
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!__all_sync(0xffffffffu,
+                                        wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p))) {
+                            ok = false;
+                            break;
+                        }
+                        const int ky = kb / p.kb_per_tap, cb = kb - ky * p.kb_per_tap;
+                        const int c0h = cb * BK;
+                        const uint32_t fb = full_bar(stage);
+                        const uint32_t a_dst = smem_u32(sA + (size_t)stage * a_slot);
+                        const bool second = p.c_split && c0h >= p.c_split;
+                        const CUtensorMap* am = second ? &tmap_a2 : &tmap_a;
+                        const int ca = second ? c0h - p.c_split : c0h;
+                        if (elect_one()) {
+                            mbar_arrive_expect_tx(fb, stage_tx);
+                            tma_load_im2col(a_dst, am, fb, ca, wc, hc, img, (uint16_t)0, (uint16_t)ky);
+                            if (!bres)
+                                for (int kx = 0; kx < 3; ++kx)
+                                    tma_load_3d(smem_u32(sB + (size_t)stage * b_slot + kx * C::kBBytes),
+                                                &tmap_b, fb, c0h, ky * 3 + kx, n0);
+                        }
+                        __syncwarp();
+                        issued_mask |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    continue;
+                }
                 // (tap, channel block) of k-block kb0, then stepped without divisions
                 int tap = kb0 / p.kb_per_tap;
                 int c0 = (kb0 - tap * p.kb_per_tap) * BK;
@@ -568,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t fb = full_bar(stage);
-                    const uint32_t a_dst = smem_u32(sA + stage * C::kAB);
+                    const uint32_t a_dst = smem_u32(sA + (size_t)stage * a_slot);
                     // a folded concat: channel blocks from c_split on come from
                     // the second source (c_split is a multiple of BK)
                     const bool second = p.c_split && c0 >= p.c_split;
@@ -582,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_im2col(a_dst, am, fb, ca, wc, hc, img, (uint16_t)kx,
                                             (uint16_t)ky);
                         if (!bres)
-                            tma_load_3d(smem_u32(sB + stage * C::kBBytes), &tmap_b, fb, c0, tap,
+                            tma_load_3d(smem_u32(sB + (size_t)stage * b_slot), &tmap_b, fb, c0, tap,
                                         n0);
                     }
                     __syncwarp();
@@ -628,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int unit = blockIdx.x; ok && unit < num_tiles; unit += gridDim.x) {
                 const int split = unit % p.splits;
                 const int kb0 = split * p.kb_per_split;
-                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+                const int kb1 = min(halo ? p.num_kbh : p.num_kb, kb0 + p.kb_per_split);
                 if (!__all_sync(0xffffffffu,
                                 wait_phase(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p))) {
                     ok = false;
@@ -636,15 +714,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MS * BN);
+                if (halo) {
+                    // unit kb = (ky, cb): horizontal tap kx reads the A box from
+                    // row kx on (row block ms from row ms * 128 + kx), B tap (ky, kx)
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!__all_sync(0xffffffffu,
+                                        wait_phase(full_bar(stage), phase, abort_flag, p))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int ky = kb / p.kb_per_tap, cb = kb - ky * p.kb_per_tap;
+                        const uint32_t a_base = smem_u32(sA + (size_t)stage * a_slot);
+                        if (elect_one()) {
+#pragma unroll
+                            for (int kx = 0; kx < 3; ++kx) {
+                                const uint32_t b_addr =
+                                    bres ? smem_u32(sB + (size_t)((ky * 3 + kx) * p.kb_per_tap + cb) *
+                                                             C::kBBytes)
+                                         : smem_u32(sB + (size_t)stage * b_slot + kx * C::kBBytes);
+                                const uint64_t bdesc = smem_desc<BK>(b_addr);
+#pragma unroll
+                                for (int ms = 0; ms < MS; ++ms) {
+                                    const uint64_t adesc =
+                                        smem_desc_at<BK>(a_base + (uint32_t)((ms * BM + kx) * BK * 2));
+#pragma unroll
+                                    for (int k = 0; k < BK / 16; ++k)
+                                        mma_f16(d_tmem + (uint32_t)(ms * BN), adesc + 2u * k,
+                                                bdesc + 2u * k, idesc,
+                                                (kb != kb0 || kx != 0 || k != 0) ? 1u : 0u);
+                                }
+                            }
+                            mma_commit(empty_bar(stage));  // frees the slot once these MMAs finish
+                        }
+                        __syncwarp();
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    if (elect_one()) mma_commit(tfull_bar(acc));
+                    __syncwarp();
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1u;
+                    continue;
+                }
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!__all_sync(0xffffffffu, wait_phase(full_bar(stage), phase, abort_flag, p))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t bdesc =
-                        smem_desc<BK>(smem_u32(sB + (bres ? kb : stage) * C::kBBytes));
-                    const uint64_t adesc0 = smem_desc<BK>(smem_u32(sA + stage * C::kAB));
+                    const uint64_t bdesc = smem_desc<BK>(smem_u32(
+                        bres ? sB + (size_t)kb * C::kBBytes : sB + (size_t)stage * b_slot));
+                    const uint64_t adesc0 = smem_desc<BK>(smem_u32(sA + (size_t)stage * a_slot));
                     if (elect_one()) {
 #pragma unroll
                         for (int ms = 0; ms < MS; ++ms) {
@@ -770,12 +894,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.out_layout == ACNN_NHWC) {
                     // residual row of this lane into its slot row, then the
                     // NHWC epilogue arithmetic and coalesced stores
-                    const int m = row0 + lane;
+                    const int mr = real_pixel(p, row0 + lane);
                     if (p.res_mode != ACNN_RES_NONE) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const bool in = m < p.M && n0 + c + j * 8 < p.C_out;
-                            const T* src = res + (in ? (long long)m * p.C_out + n0 + c + j * 8 : 0);
+                            const bool in = mr >= 0 && n0 + c + j * 8 < p.C_out;
+                            const T* src = res + (in ? (long long)mr * p.C_out + n0 + c + j * 8 : 0);
                             cp_async16(smem_u32(slot + lane * 64 + ((j ^ swz) << 4)), src, in ? 16u : 0u);
                         }
                         cp_async_commit();
@@ -795,13 +919,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < 4; ++k) {
                         const int rr = 8 * k + crow;
                         const uint4 u = *reinterpret_cast<const uint4*>(slot + piece(rr, cpiece));
-                        if (row0 + rr < p.M && col < p.C_out)
-                            *reinterpret_cast<uint4*>(y + (long long)(row0 + rr) * p.C_out + col) = u;
+                        const int mo = real_pixel(p, row0 + rr);
+                        if (mo >= 0 && col < p.C_out)
+                            *reinterpret_cast<uint4*>(y + (long long)mo * p.C_out + col) = u;
                     }
                     __syncwarp();  // the slot is read out before the next block reuses it
                 } else {
-                    const int m = row0 + lane;
-                    const bool valid = m < p.M;
+                    const int mr = real_pixel(p, row0 + lane);
+                    const bool valid = mr >= 0;
+                    const int m = valid ? mr : 0;
                     const int img = m / p.OHW;
                     const long long base = (long long)img * p.C_out * p.OHW + (m - img * p.OHW);
                     const bool pre = p.res_mode == ACNN_RES_ADD_THEN_ACT;
@@ -909,8 +1035,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int r = 8 * k + crow;
-                    const bool in = row0 + r < p.M && col < p.C_out;
-                    const T* src = res + (in ? (long long)(row0 + r) * p.C_out + col : 0);
+                    const int mr = real_pixel(p, row0 + r);
+                    const bool in = mr >= 0 && col < p.C_out;
+                    const T* src = res + (in ? (long long)mr * p.C_out + col : 0);
                     cp_async16(sl + piece(r, cpiece), src, in ? 16u : 0u);
                 }
                 cp_async_commit();
@@ -980,8 +1107,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 4; ++k) {
                     const int rr = 8 * k + crow;
                     const uint4 u = *reinterpret_cast<const uint4*>(slot + piece(rr, cpiece));
-                    if (row0 + rr < p.M && col < p.C_out)
-                        *reinterpret_cast<uint4*>(y + (long long)(row0 + rr) * p.C_out + col) = u;
+                    const int mo = real_pixel(p, row0 + rr);
+                    if (mo >= 0 && col < p.C_out)
+                        *reinterpret_cast<uint4*>(y + (long long)mo * p.C_out + col) = u;
                 }
                 __syncwarp();  // the slot is read out before a refill overwrites it
                 refill();
@@ -1033,8 +1161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nch = ((p.C_out - n0 < BN ? p.C_out - n0 : BN) + 31) >> 5;
             for (int i = grp; i < MS * nch; i += kEpiGroups) {
                 const int ms = i / nch, c = (i - ms * nch) * 32;
-                const int m = m0 + ms * BM + row;
-                const bool valid = m < p.M;
+                const int mr = real_pixel(p, m0 + ms * BM + row);
+                const bool valid = mr >= 0;
+                const int m = valid ? mr : 0;
                 const int img = m / p.OHW;
                 const long long base = (long long)img * p.C_out * p.OHW + (m - img * p.OHW);
                 float v[32];
@@ -1043,9 +1172,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                           v);
                 const int nj = p.C_out - (n0 + c) < 32 ? p.C_out - (n0 + c) : 32;
                 // the chunk's 32 pixels: all in range, one image, 8-aligned start
-                const int r0 = m0 + ms * BM + q * 32;
+                // (real pixels of the chunk's first and last rows: consecutive
+                // when no virtual column of a halo-row grid lies between them)
+                const int r0 = real_pixel(p, m0 + ms * BM + q * 32);
+                const int r31 = real_pixel(p, m0 + ms * BM + q * 32 + 31);
                 const int img0 = r0 / p.OHW;
-                const bool vec = vec_ok && r0 + 31 < p.M && (r0 + 31) / p.OHW == img0 &&
+                const bool vec = vec_ok && r0 >= 0 && r31 == r0 + 31 && r31 / p.OHW == img0 &&
                                  (r0 - img0 * p.OHW) % 8 == 0;
                 if (vec) {
                     const long long base0 = (long long)img0 * p.C_out * p.OHW + (r0 - img0 * p.OHW);
@@ -1173,6 +1305,11 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     // transposing stage of the vectorised stores
     prm.ring_slots = nhwc_epi ? (rd > 0 ? rd : 1) : 1;
     const size_t ring_bytes = (size_t)kEpiWarps * prm.ring_slots * kStageBytes;
+    // bytes a stage holds: A, plus B unless resident (halo rows: the larger A
+    // box and the three taps' B blocks)
+    const bool halo = prm.a_mode == 2;
+    const size_t a_slot = halo ? C::kABh : C::kAB;
+    const size_t b_slot = halo ? 3 * (size_t)C::kBBytes : C::kBBytes;
     auto stages_for = [&](bool resident) -> int {
         if (kSmemFixed + ring_bytes + par_bytes > kSmemMax) return 0;
         size_t left = kSmemMax - kSmemFixed - ring_bytes - par_bytes;
@@ -1180,7 +1317,7 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
             if (left < b_all) return 0;
             left -= b_all;
         }
-        const size_t n = left / (C::kAB + (resident ? 0 : C::kBBytes));
+        const size_t n = left / (a_slot + (resident ? 0 : b_slot));
         return n > (size_t)kMaxStages ? kMaxStages : (int)n;
     };
     const int s_ring = stages_for(false);
@@ -1189,9 +1326,11 @@ int launch_bn(const ConvArgs& a, const Maps& m, Params prm, cudaStream_t s) {
     prm.b_resident = resident ? 1 : 0;
     prm.stages = resident ? s_res : s_ring;
     prm.res_depth = rd;
-    if (prm.stages < 2) return ACNN_ERR_UNSUPPORTED;  // C_out too large for the bias copy
+    // fewer than two stages: C_out too large for the bias copy, or (halo rows)
+    // a stage too large for the ring -- the caller retries without halo rows
+    if (prm.stages < 2) return ACNN_ERR_UNSUPPORTED;
     const size_t smem = kSmemFixed + ring_bytes + par_bytes +
-                        (size_t)prm.stages * (C::kAB + (resident ? 0 : C::kBBytes)) +
+                        (size_t)prm.stages * (a_slot + (resident ? 0 : b_slot)) +
                         (resident ? b_all : 0);
     const int tiles = prm.num_m_tiles * prm.num_n_tiles * prm.splits;
     const int grid = tiles < sm_count() ? tiles : sm_count();
@@ -1332,6 +1471,17 @@ IgemmPlan igemm_plan(const acnn_conv_desc& d, int oh, int ow, size_t part_budget
     return best.splits > 1 && best_cost > 0.85 * best1_cost ? best1 : best;
 }
 
+// Halo rows serve 3x3, stride 1, pad 1 convs on plans of at most 128 output
+// channels per tile and no K split (the wider layers already run near the MMA
+// rate); with 32-channel k-blocks (64-byte swizzle) too when kHaloBk32 holds.
+constexpr bool kHaloBk32 = true;
+
+bool halo_rows_ok(const acnn_conv_desc& d, int oh, int ow, const IgemmPlan& plan) {
+    if (d.kh != 3 || d.kw != 3 || d.stride != 1 || d.pad != 1) return false;
+    if (plan.splits != 1 || plan.bn > 128 || (plan.bk == 32 && !kHaloBk32)) return false;
+    return (long long)d.n * oh * (ow + 2) <= 0x7fffffffLL;
+}
+
 int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     const acnn_conv_desc& d = a.d;
     if (!load_encoders()) return ACNN_ERR_CUDA;
@@ -1346,92 +1496,108 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
                                       a.ws_part && a.out_layout == ACNN_NHWC ? a.ws_part_bytes : 0);
     const int bk = plan.bk;
     const CUtensorMapSwizzle swz = bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-
-    alignas(64) Maps maps;
-    CUtensorMap& tb = maps.b;
-    // the A operand's map over an NHWC tensor of `ch` channels (a folded
-    // concat has two: channels [0, c_split) and [c_split, c_in))
-    auto encode_a = [&](CUtensorMap* ta, const void* ptr, int ch) {
-        if (tiled) {
-            cuuint64_t dims[2] = {(cuuint64_t)ch, (cuuint64_t)M};
-            cuuint64_t strides[1] = {(cuuint64_t)ch * 2};
-            cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)(BM * plan.ms)};
-            cuuint32_t es[2] = {1, 1};
-            return g_encode_tiled(ta, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        }
-        cuuint64_t dims[4] = {(cuuint64_t)ch, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
-        cuuint64_t strides[3] = {(cuuint64_t)ch * 2, (cuuint64_t)d.w * ch * 2,
-                                 (cuuint64_t)d.h * d.w * ch * 2};
-        // window corners range over [-pad, dim - 1 + pad - (k - 1)] (W then H)
-        int lower[2] = {-d.pad, -d.pad};
-        int upper[2] = {d.pad - (d.kw - 1), d.pad - (d.kh - 1)};
-        cuuint32_t es[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
-        return g_encode_im2col(ta, dt, 4, const_cast<void*>(ptr), dims, strides, lower, upper, bk,
-                               BM * plan.ms, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    };
     const bool cat = a.x2 && a.c_split > 0;
     if (cat && a.c_split % bk != 0) return ACNN_ERR_UNSUPPORTED;  // a k-block must not straddle
-    CUresult r = encode_a(&maps.a, a.x, cat ? a.c_split : d.c_in);
-    if (r == CUDA_SUCCESS) {
-        if (cat) r = encode_a(&maps.a2, a.x2, d.c_in - a.c_split);
-        else maps.a2 = maps.a;
-    }
-    if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
 
-    const int num_m_tiles = (int)((M + BM * plan.ms - 1) / (BM * plan.ms));
-    const int bn = plan.bn;
-    {
-        cuuint64_t dims[3] = {(cuuint64_t)d.c_in, (cuuint64_t)taps, (cuuint64_t)d.c_out};
-        cuuint64_t strides[2] = {(cuuint64_t)d.c_in * 2, (cuuint64_t)taps * d.c_in * 2};
-        cuuint32_t box[3] = {(cuuint32_t)bk, 1, (cuuint32_t)bn};
-        cuuint32_t es[3] = {1, 1, 1};
-        r = g_encode_tiled(&tb, dt, 3, const_cast<void*>(a.w), dims, strides, box, es,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    // first with halo rows where they apply, then (also when a halo-row stage
+    // does not fit in shared memory) without
+    for (int h = halo_rows_ok(d, a.oh, a.ow, plan) ? 1 : 0; h >= 0; --h) {
+        const bool halo = h == 1;
+        const int vw = halo ? a.ow + 2 : a.ow;  // row width of the (virtual) output grid
+        const long long Mv = (long long)d.n * a.oh * vw;
+        alignas(64) Maps maps;
+        CUtensorMap& tb = maps.b;
+        // the A operand's map over an NHWC tensor of `ch` channels (a folded
+        // concat has two: channels [0, c_split) and [c_split, c_in))
+        auto encode_a = [&](CUtensorMap* ta, const void* ptr, int ch) {
+            if (tiled) {
+                cuuint64_t dims[2] = {(cuuint64_t)ch, (cuuint64_t)M};
+                cuuint64_t strides[1] = {(cuuint64_t)ch * 2};
+                cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)(BM * plan.ms)};
+                cuuint32_t es[2] = {1, 1};
+                return g_encode_tiled(ta, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                                      CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            }
+            cuuint64_t dims[4] = {(cuuint64_t)ch, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
+            cuuint64_t strides[3] = {(cuuint64_t)ch * 2, (cuuint64_t)d.w * ch * 2,
+                                     (cuuint64_t)d.h * d.w * ch * 2};
+            // window corners range over [-pad, dim - 1 + pad - (k - 1)] (W then H);
+            // with halo rows W runs two corners further (the two virtual columns
+            // of each output row), and a box holds TM + 2 pixels
+            int lower[2] = {-d.pad, -d.pad};
+            int upper[2] = {halo ? d.pad : d.pad - (d.kw - 1), d.pad - (d.kh - 1)};
+            cuuint32_t es[4] = {1, (cuuint32_t)d.stride, (cuuint32_t)d.stride, 1};
+            return g_encode_im2col(ta, dt, 4, const_cast<void*>(ptr), dims, strides, lower, upper, bk,
+                                   BM * plan.ms + (halo ? 2 : 0), es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                   swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        };
+        CUresult r = encode_a(&maps.a, a.x, cat ? a.c_split : d.c_in);
+        if (r == CUDA_SUCCESS) {
+            if (cat) r = encode_a(&maps.a2, a.x2, d.c_in - a.c_split);
+            else maps.a2 = maps.a;
+        }
+        if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
+
+        const int num_m_tiles = (int)((Mv + BM * plan.ms - 1) / (BM * plan.ms));
+        const int bn = plan.bn;
+        {
+            cuuint64_t dims[3] = {(cuuint64_t)d.c_in, (cuuint64_t)taps, (cuuint64_t)d.c_out};
+            cuuint64_t strides[2] = {(cuuint64_t)d.c_in * 2, (cuuint64_t)taps * d.c_in * 2};
+            cuuint32_t box[3] = {(cuuint32_t)bk, 1, (cuuint32_t)bn};
+            cuuint32_t es[3] = {1, 1, 1};
+            r = g_encode_tiled(&tb, dt, 3, const_cast<void*>(a.w), dims, strides, box, es,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        }
+        if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
+        Params prm{};
+        prm.M = (int)Mv;
+        prm.C_out = d.c_out;
+        prm.taps = taps;
+        prm.KW = d.kw;
+        prm.kb_per_tap = (d.c_in + bk - 1) / bk;
+        prm.num_kb = taps * prm.kb_per_tap;
+        prm.num_kbh = halo ? d.kh * prm.kb_per_tap : 0;
+        prm.num_m_tiles = num_m_tiles;
+        prm.splits = plan.splits;
+        prm.kb_per_split = halo ? prm.num_kbh : plan.kb_per_split;
+        // split-K workspace: tile counters, then the partial tiles
+        const int out_tiles = num_m_tiles * ((d.c_out + plan.bn - 1) / plan.bn);
+        const size_t cnt_bytes = ((size_t)out_tiles * 4 + 255) & ~(size_t)255;
+        prm.cnt = plan.splits > 1 ? static_cast<unsigned*>(a.ws_part) : nullptr;
+        prm.part = plan.splits > 1
+                       ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws_part) + cnt_bytes)
+                       : nullptr;
+        if (plan.splits > 1 && cudaMemsetAsync(a.ws_part, 0, cnt_bytes, s) != cudaSuccess)
+            return ACNN_ERR_CUDA;
+        prm.OW = a.ow;
+        prm.OHW = a.oh * a.ow;
+        prm.vw = vw;
+        prm.vw_magic = ~0ull / (unsigned long long)vw + 1ull;
+        prm.S = d.stride;
+        prm.P = d.pad;
+        prm.a_mode = tiled ? 0 : (halo ? 2 : 1);
+        prm.c_split = cat ? a.c_split : 0;
+        prm.out_layout = a.out_layout;
+        prm.act = a.act;
+        prm.res_mode = a.res_mode;
+        prm.bias = a.bias;
+        prm.alpha = a.alpha;
+        prm.res = a.residual;
+        prm.y = a.y;
+        prm.status = device_status_ptr();
+        prm.budget = wait_budget_polls();
+        if (!prm.status) return ACNN_ERR_CUDA;
+        const bool bf16 = d.dtype == ACNN_BF16;
+        const int st = bf16 ? launch_typed<__nv_bfloat16>(a, plan, maps, prm, s)
+                            : launch_typed<__half>(a, plan, maps, prm, s);
+        if (halo && st == ACNN_ERR_UNSUPPORTED) continue;  // nothing launched: retry without
+        return st;
     }
-    if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
-    Params prm{};
-    prm.M = (int)M;
-    prm.C_out = d.c_out;
-    prm.taps = taps;
-    prm.KW = d.kw;
-    prm.kb_per_tap = (d.c_in + bk - 1) / bk;
-    prm.num_kb = taps * prm.kb_per_tap;
-    prm.num_m_tiles = num_m_tiles;
-    prm.splits = plan.splits;
-    prm.kb_per_split = plan.kb_per_split;
-    // split-K workspace: tile counters, then the partial tiles
-    const int out_tiles = num_m_tiles * ((d.c_out + plan.bn - 1) / plan.bn);
-    const size_t cnt_bytes = ((size_t)out_tiles * 4 + 255) & ~(size_t)255;
-    prm.cnt = plan.splits > 1 ? static_cast<unsigned*>(a.ws_part) : nullptr;
-    prm.part = plan.splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws_part) + cnt_bytes)
-                               : nullptr;
-    if (plan.splits > 1 && cudaMemsetAsync(a.ws_part, 0, cnt_bytes, s) != cudaSuccess)
-        return ACNN_ERR_CUDA;
-    prm.OW = a.ow;
-    prm.OHW = a.oh * a.ow;
-    prm.S = d.stride;
-    prm.P = d.pad;
-    prm.a_mode = tiled ? 0 : 1;
-    prm.c_split = cat ? a.c_split : 0;
-    prm.out_layout = a.out_layout;
-    prm.act = a.act;
-    prm.res_mode = a.res_mode;
-    prm.bias = a.bias;
-    prm.alpha = a.alpha;
-    prm.res = a.residual;
-    prm.y = a.y;
-    prm.status = device_status_ptr();
-    prm.budget = wait_budget_polls();
-    if (!prm.status) return ACNN_ERR_CUDA;
-    const bool bf16 = d.dtype == ACNN_BF16;
-    return bf16 ? launch_typed<__nv_bfloat16>(a, plan, maps, prm, s)
-                : launch_typed<__half>(a, plan, maps, prm, s);
+    return ACNN_ERR_UNSUPPORTED;
 }
 
 }  // namespace acnn

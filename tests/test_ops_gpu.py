@@ -300,6 +300,47 @@ def test_conv_packed_path(case):
     assert_parity(y, ref, TDT[dt], name)
 
 
+# ---------------------------------------------------------------- halo rows
+# 3x3 stride-1 pad-1 convs run on a virtual output grid two columns wider than
+# the map (one box of 128 + 2 pixels per kernel row serves its three horizontal
+# taps; the two extra columns of each row are computed and discarded): widths
+# where those columns are most of a row, tiles straddling rows and images,
+# 32- and 64-channel k-blocks, both layouts, residual modes.
+HALO_CASES = [
+    # name, n, h, w, cin, cout, layout, res_mode
+    ("w1", 3, 7, 1, 64, 64, G.NHWC, A.RES_NONE),
+    ("w2", 2, 9, 2, 64, 128, G.NHWC, A.RES_ADD_THEN_ACT),
+    ("w3_cin32", 4, 5, 3, 32, 64, G.NHWC, A.RES_NONE),
+    ("w126", 1, 3, 126, 64, 64, G.NHWC, A.RES_ACT_THEN_ADD),  # vw = 128: rows on tile edges
+    ("w127_cin32", 2, 4, 127, 32, 32, G.NHWC, A.RES_NONE),
+    ("h1", 5, 1, 37, 128, 64, G.NHWC, A.RES_NONE),
+    ("nchw_w5", 2, 11, 5, 64, 48, G.NCHW, A.RES_ACT_THEN_ADD),
+    ("nchw_w120", 1, 9, 120, 240, 240, G.NCHW, A.RES_NONE),
+    ("cin96", 3, 13, 29, 96, 64, G.NHWC, A.RES_ADD_THEN_ACT),
+]
+
+
+@pytest.mark.parametrize("case", HALO_CASES, ids=[c[0] for c in HALO_CASES])
+def test_conv_halo_rows(case):
+    name, n, h, w, cin, cout, layout, res_mode = case
+    dt = "bf16" if layout == G.NHWC else "f16"
+    d = A.ConvDesc(n, h, w, cin, cout, 3, 3, 1, 1, layout, DT[dt])
+    assert A.acnn_conv2d_path(d) == 2
+    y, ref = conv_case("halo" + name, n, h, w, cin, cout, 3, 1, 1, dt, layout=layout,
+                       act=A.ACT_PRELU, res_mode=res_mode)
+    assert_parity(y, ref, TDT[dt], name)
+
+
+@pytest.mark.parametrize("cin", [32, 64])
+def test_conv_halo_rows_integer_bitexact(cin):
+    """Integer data on the halo-row path: every product and partial sum exact, so
+    each stored value is the oracle's rounded once (a tap read from the wrong
+    row or column of the box would change it)."""
+    y, ref = conv_case(f"hint{cin}", 2, 15, 23, cin, 64, 3, 1, 1, "bf16", act=A.ACT_PRELU,
+                       integer=True)
+    assert_bitexact(y, O.round_storage(ref, O.BF16), f"halo int cin{cin}")
+
+
 # ---------------------------------------------------------------- tiny C_in (path 4)
 TINY_CASES = [
     # name, n, h, w, cin, cout, s, p, dt, layout
