@@ -44,6 +44,7 @@ EXPORTS = (
     "acnn_section_begin", "acnn_section_end", "acnn_section_launch", "acnn_section_destroy",
     "acnn_device_sm_count", "acnn_conv2d_fused_noalloc", "acnn_conv2d_plan",
     "acnn_conv2d_fused_cat2", "acnn_conv2d_force_plan", "acnn_conv2d_force_path",
+    "acnn_conv2d_fused_pool2",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # ACNN_NOALLOC_SCRATCH_BYTES in include/acnn.h
 
@@ -109,6 +110,7 @@ def lib() -> ctypes.CDLL:
         L.acnn_conv2d_fused_noalloc.argtypes = [D, _P, _P, _P, _P, _P, _I, _I, _P, _P]
         L.acnn_conv2d_plan.argtypes = [D, ctypes.c_size_t] + [ctypes.POINTER(_I)] * 3
         L.acnn_conv2d_force_plan.argtypes = [_I, _I, _I]
+        L.acnn_conv2d_fused_pool2.argtypes = [D, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P]
         L.acnn_conv2d_force_path.argtypes = [_I, _I]
         _lib = L
     return _lib
@@ -306,6 +308,13 @@ def acnn_conv2d_fused_cat2(desc, x_a, c_a, x_b, w, bias, alpha, residual, res_mo
                                         _ptr(y), _ptr(workspace), ws_bytes, _stream(stream))
 
 
+def acnn_conv2d_fused_pool2(desc, x, w, bias, alpha, residual, res_mode, act, y, y_pool,
+                            stream=None) -> int:
+    return lib().acnn_conv2d_fused_pool2(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias),
+                                         _ptr(alpha), _ptr(residual), res_mode, act, _ptr(y),
+                                         _ptr(y_pool), _stream(stream))
+
+
 def conv_out_shape(desc: ConvDesc):
     st, oh, ow = acnn_conv2d_out_hw(desc)
     check(st, "acnn_conv2d_out_hw")
@@ -330,6 +339,20 @@ def conv2d_fused(x, w, bias=None, *, stride=1, pad=0, act=ACT_NONE, alpha=None, 
                            ws_bytes if workspace is not None else 0, stream)
     check(st, "acnn_conv2d_fused")
     return y
+
+
+def conv2d_fused_pool2(x, w, bias=None, *, act=ACT_NONE, alpha=None, residual=None,
+                       res_mode=RES_NONE, out=None, out_pool=None, stream=None):
+    """1x1 NHWC conv2d_fused that also returns the 2x2/s2 average pool of its output."""
+    c_out = w.shape[0]
+    d = conv_desc(x, c_out, 1, 1, 1, 0, NHWC)
+    shape = conv_out_shape(d)
+    y = out if out is not None else torch.empty(shape, dtype=x.dtype, device=x.device)
+    yp = out_pool if out_pool is not None else torch.empty(
+        (shape[0], shape[1] // 2, shape[2] // 2, shape[3]), dtype=x.dtype, device=x.device)
+    check(acnn_conv2d_fused_pool2(d, x, w, bias, alpha, residual, res_mode, act, y, yp, stream),
+          "acnn_conv2d_fused_pool2")
+    return y, yp
 
 
 def conv2d_prepack(desc, w, stream=None):

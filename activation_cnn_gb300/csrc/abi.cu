@@ -516,6 +516,60 @@ int acnn_conv2d_fused_cat2(const acnn_conv_desc* d, const void* x_a, int c_a, co
     return launch_igemm_conv(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int acnn_conv2d_fused_pool2(const acnn_conv_desc* d, const void* x, const void* w,
+                            const float* bias, const float* alpha, const void* residual,
+                            int res_mode, int act, void* y, void* y_pool, acnn_stream_t stream) {
+    int st = check_desc(d);
+    if (st != ACNN_OK) return st;
+    if (act < ACNN_ACT_NONE || act > ACNN_ACT_PRELU || res_mode < ACNN_RES_NONE ||
+        res_mode > ACNN_RES_ACT_THEN_ADD)
+        return ACNN_ERR_BAD_ENUM;
+    if (!x || !w || !y || !y_pool) return ACNN_ERR_NULL_POINTER;
+    if (act == ACNN_ACT_PRELU && !alpha) return ACNN_ERR_NULL_POINTER;
+    if (res_mode != ACNN_RES_NONE && !residual) return ACNN_ERR_NULL_POINTER;
+    int oh, ow;
+    st = conv_out(d, &oh, &ow);
+    if (st != ACNN_OK) return st;
+    // a 1x1/s1/p0 NHWC 16-bit conv on the tiled tensor-core path, 64-channel
+    // k-blocks, an even output map
+    const Route r = route(d, oh, ow);
+    if (r.path != 1 || d->layout != ACNN_NHWC || d->c_in < 64 || oh % 2 || ow % 2)
+        return ACNN_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || !aligned16(y_pool) ||
+        (bias && !aligned16(bias)) || (alpha && !aligned16(alpha)) ||
+        (residual && !aligned16(residual)))
+        return ACNN_ERR_MISALIGNED;
+    const size_t es = elem_size(d->dtype);
+    const size_t xb = (size_t)d->n * d->h * d->w * d->c_in * es;
+    const size_t wb = (size_t)d->c_out * d->c_in * es;
+    const size_t yb = (size_t)d->n * oh * ow * d->c_out * es;
+    const size_t pb = yb / 4;
+    const bool res = residual && res_mode != ACNN_RES_NONE;
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) || (res && overlaps(y, yb, residual, yb)) ||
+        (bias && overlaps(y, yb, bias, d->c_out * 4)) ||
+        (alpha && act == ACNN_ACT_PRELU && overlaps(y, yb, alpha, d->c_out * 4)) ||
+        overlaps(y_pool, pb, y, yb) || overlaps(y_pool, pb, x, xb) || overlaps(y_pool, pb, w, wb) ||
+        (res && overlaps(y_pool, pb, residual, yb)) ||
+        (bias && overlaps(y_pool, pb, bias, d->c_out * 4)) ||
+        (alpha && act == ACNN_ACT_PRELU && overlaps(y_pool, pb, alpha, d->c_out * 4)))
+        return ACNN_ERR_ALIAS;
+    ConvArgs a{};
+    a.d = *d;
+    a.oh = oh;
+    a.ow = ow;
+    a.x = x;
+    a.w = w;
+    a.bias = bias;
+    a.alpha = act == ACNN_ACT_PRELU ? alpha : nullptr;
+    a.residual = res ? residual : nullptr;
+    a.res_mode = res_mode;
+    a.act = act;
+    a.y = y;
+    a.y2 = y_pool;
+    a.out_layout = ACNN_NHWC;
+    return launch_igemm_conv(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int acnn_pool2d(int kind, int n, int h, int w, int c, int k, int stride, int pad, int layout,
                 int dtype, const void* x, void* y, acnn_stream_t stream) {
     if (kind != ACNN_POOL_MAX && kind != ACNN_POOL_AVG) return ACNN_ERR_BAD_ENUM;

@@ -100,6 +100,9 @@ struct ConvArgs {
     // and x2 channels [c_split, c_in), both NHWC (c_split = 0: x holds all)
     const void* x2 = nullptr;
     int c_split = 0;
+    // 1x1 convs only: NHWC [n][oh/2][ow/2][c_out], the 2x2/s2 average pool of y
+    // written by the conv's epilogue (NULL: none)
+    void* y2 = nullptr;
 };
 
 // Tile width and K split of the tensor-core conv for a geometry, given the

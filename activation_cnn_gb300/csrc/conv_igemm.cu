@@ -89,7 +89,7 @@ struct Params {
     // host before the launch); NULL without a split
     float* part;
     unsigned* cnt;
-    int OW, OHW, S, P;
+    int OW, OHW, OH, S, P;
     // Halo rows (a_mode 2): output pixels are indexed on a virtual grid whose
     // rows are vw = OW + 2 wide (the two extra columns per row are computed
     // and discarded), M counts virtual pixels, and K runs over (kernel row,
@@ -99,7 +99,15 @@ struct Params {
     int vw;
     unsigned long long vw_magic;
     int num_kbh;
-    int a_mode;       // 0: tiled A (1x1/s1/p0); 1: im2col A; 2: im2col A with halo rows
+    // Rectangular tiles (a_mode 3, 1x1 convs with a pooled second output):
+    // tile t = (n * rty + ty) * rtx + tx covers output rows ty * rh ... and
+    // columns tx * rw ... of image n (rw = 2^rw_log2, rw * rh = 128), loaded as
+    // one 4-D box; rtx_magic / rty_magic divide by rtx / rty as vw_magic does.
+    int rw_log2, rh, rtx, rty;
+    unsigned long long rtx_magic, rty_magic;
+    void* y2;         // a_mode 3: NHWC [N][OH/2][OW/2][C_out], the 2x2/s2 average of y
+    int a_mode;       // 0: tiled A (1x1/s1/p0); 1: im2col A; 2: im2col A with halo rows;
+                      // 3: tiled A in rectangular tiles (1x1/s1/p0, pooled second output)
     int c_split;      // channels [c_split, C_in) come from the second A map (0: none)
     int out_layout;   // ACNN_NHWC or ACNN_NCHW for y and the residual
     int act, res_mode;
@@ -119,12 +127,54 @@ struct Params {
 // Output pixel (row of the GEMM) v -> index of the real output pixel in
 // [0, N*OH*OW), or -1 for a virtual column of a halo-row grid or a row past
 // the end of the tile range.
+// Rectangular tile: tile t -> (image, first row, first column).
+// (A divisor of 1 has no 64-bit magic number: 2^64 wraps to 0.)
+__device__ __forceinline__ void rect_tile(const Params& p, int t, int& n, int& y0, int& x0) {
+    const int t2 = p.rtx == 1 ? t : (int)__umul64hi((unsigned long long)t, p.rtx_magic);  // t / rtx
+    const int tx = t - t2 * p.rtx;
+    n = p.rty == 1 ? t2 : (int)__umul64hi((unsigned long long)t2, p.rty_magic);  // t2 / rty
+    y0 = (t2 - n * p.rty) * p.rh;
+    x0 = tx << p.rw_log2;
+}
+
 __device__ __forceinline__ int real_pixel(const Params& p, int v) {
     if (v >= p.M) return -1;
+    if (p.a_mode == 3) {
+        int n, y0, x0;
+        rect_tile(p, v >> 7, n, y0, x0);
+        const int r = v & 127;
+        const int oy = y0 + (r >> p.rw_log2), ox = x0 + (r & ((1 << p.rw_log2) - 1));
+        return oy < p.OH && ox < p.OW ? (n * p.OH + oy) * p.OW + ox : -1;
+    }
     if (p.a_mode != 2) return v;
     const int row = (int)__umul64hi((unsigned long long)v, p.vw_magic);  // v / vw
     const int j = v - row * p.vw;
     return j < p.OW ? row * p.OW + j : -1;
+}
+
+// Rows v0 .. v0 + 31 of one epilogue chunk -> real output pixels.  With
+// rectangular tiles the tile's image and corner are decomposed once per chunk
+// and a row then costs a shift and a mask; the other modes use real_pixel.
+struct ChunkMap {
+    int v0;
+    int n, y0, x0, tr0;  // rectangular tiles: image, corner, first tile row of the chunk
+};
+
+__device__ __forceinline__ ChunkMap chunk_map(const Params& p, int v0) {
+    ChunkMap c{v0, 0, 0, 0, 0};
+    if (p.a_mode == 3 && v0 < p.M) {
+        rect_tile(p, v0 >> 7, c.n, c.y0, c.x0);
+        c.tr0 = v0 & 127;
+    }
+    return c;
+}
+
+__device__ __forceinline__ int map_row(const Params& p, const ChunkMap& c, int r) {
+    if (p.a_mode != 3) return real_pixel(p, c.v0 + r);
+    if (c.v0 >= p.M) return -1;
+    const int tr = c.tr0 + r;
+    const int oy = c.y0 + (tr >> p.rw_log2), ox = c.x0 + (tr & ((1 << p.rw_log2) - 1));
+    return oy < p.OH && ox < p.OW ? (c.n * p.OH + oy) * p.OW + ox : -1;
 }
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -252,6 +302,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
 
@@ -600,6 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // window corner of the tile's first (virtual) output pixel
                 const int img = m0 / OHV, r = m0 % OHV;
                 const int wc = (r % p.vw) * p.S - p.P, hc = (r / p.vw) * p.S - p.P;
+                // rectangular tile: image and corner of the 4-D box
+                int rn = 0, ry0 = 0, rx0 = 0;
+                if (p.a_mode == 3) rect_tile(p, m0 >> 7, rn, ry0, rx0);
                 if (halo) {
                     // unit kb = (kernel row ky, channel block cb): one A box of
                     // TM + 2 virtual pixels at tap (0, ky), the B blocks of taps
@@ -656,6 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(fb, stage_tx);
                         if (p.a_mode == 0)
                             tma_load_2d(a_dst, am, fb, ca, m0);
+                        else if (p.a_mode == 3)
+                            tma_load_4d(a_dst, am, fb, ca, rx0, ry0, rn);
                         else
                             tma_load_im2col(a_dst, am, fb, ca, wc, hc, img, (uint16_t)kx,
                                             (uint16_t)ky);
@@ -1032,10 +1096,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row0 = (nnt == 1 ? rc.t : rc.t / nnt) * TM + rc.ms * BM + q * 32;
                 const int col = rc.nt * BN + rc.ci * 32 + cpiece * 8;
                 const uint32_t sl = smem_u32(ring + wb * kStageBytes);
+                const ChunkMap cm = chunk_map(p, row0);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int r = 8 * k + crow;
-                    const int mr = real_pixel(p, row0 + r);
+                    const int mr = map_row(p, cm, r);
                     const bool in = mr >= 0 && col < p.C_out;
                     const T* src = res + (in ? (long long)mr * p.C_out + col : 0);
                     cp_async16(sl + piece(r, cpiece), src, in ? 16u : 0u);
@@ -1103,13 +1168,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 // eight rows per instruction out to y
                 const int col = n0 + c + cpiece * 8;
+                const ChunkMap cm = chunk_map(p, row0);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int rr = 8 * k + crow;
                     const uint4 u = *reinterpret_cast<const uint4*>(slot + piece(rr, cpiece));
-                    const int mo = real_pixel(p, row0 + rr);
+                    const int mo = map_row(p, cm, rr);
                     if (mo >= 0 && col < p.C_out)
                         *reinterpret_cast<uint4*>(y + (long long)mo * p.C_out + col) = u;
+                }
+                if (p.y2) {
+                    // pooled second output (rectangular tiles): a chunk holds
+                    // 32 / rw >= 2 whole tile rows, i.e. 8 whole 2x2 windows;
+                    // lane l averages the 16-byte piece l & 3 (8 channels) of
+                    // window l >> 2 from the window's four stored rows of the
+                    // slot, as the 2x2/s2 average pool does:
+                    // ((tl + tr) + bl) + br in fp32, times 0.25, rounded once
+                    const int rw = 1 << p.rw_log2;
+                    const int w = lane >> 2, j = lane & 3;
+                    const int half = rw >> 1;  // windows per pair of pixel rows
+                    const int rtl = (w / half) * 2 * rw + 2 * (w % half);  // top-left chunk row
+                    const int tr = cm.tr0 + rtl;
+                    const int oy = cm.y0 + (tr >> p.rw_log2), ox = cm.x0 + (tr & (rw - 1));
+                    if (row0 < p.M && oy < p.OH && ox < p.OW && n0 + c + 8 * j < p.C_out) {
+                        T* yp = static_cast<T*>(p.y2) +
+                                ((long long)(cm.n * (p.OH >> 1) + (oy >> 1)) * (p.OW >> 1) +
+                                 (ox >> 1)) * p.C_out +
+                                n0 + c + 8 * j;
+                        const int rows[4] = {rtl, rtl + 1, rtl + rw, rtl + rw + 1};
+                        float acc[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(slot + piece(rows[k], j));
+                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                float lo, hi;
+                                unpack2<T>(w4[e], lo, hi);
+                                acc[2 * e] = __fadd_rn(acc[2 * e], lo);
+                                acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], hi);
+                            }
+                        }
+                        *reinterpret_cast<uint4*>(yp) = make_uint4(
+                            pack2<T>(__fmul_rn(acc[0], 0.25f), __fmul_rn(acc[1], 0.25f)),
+                            pack2<T>(__fmul_rn(acc[2], 0.25f), __fmul_rn(acc[3], 0.25f)),
+                            pack2<T>(__fmul_rn(acc[4], 0.25f), __fmul_rn(acc[5], 0.25f)),
+                            pack2<T>(__fmul_rn(acc[6], 0.25f), __fmul_rn(acc[7], 0.25f)));
+                    }
                 }
                 __syncwarp();  // the slot is read out before a refill overwrites it
                 refill();
@@ -1492,8 +1599,23 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     const bool tiled = d.kh == 1 && d.kw == 1 && d.stride == 1 && d.pad == 0;
     // no K split for NCHW output: its split epilogue stores element by element,
     // while the unsplit one writes 16-byte runs
-    const IgemmPlan plan = igemm_plan(d, a.oh, a.ow,
-                                      a.ws_part && a.out_layout == ACNN_NHWC ? a.ws_part_bytes : 0);
+    IgemmPlan plan = igemm_plan(d, a.oh, a.ow,
+                                a.ws_part && a.out_layout == ACNN_NHWC ? a.ws_part_bytes : 0);
+    // A pooled second output (1x1/s1/p0 only): rectangular tiles of 128 pixels,
+    // rw columns x 128 / rw rows with rw = 16 or 8, so that each epilogue warp's
+    // 32 rows hold whole 2x2 windows; one 128-row block, no K split.
+    const bool rect = a.y2 != nullptr;
+    if (rect) {
+        if (!tiled || plan.bk != 64 || a.out_layout != ACNN_NHWC || a.oh % 2 || a.ow % 2)
+            return ACNN_ERR_UNSUPPORTED;
+        plan.ms = 1;
+        plan.splits = 1;
+        plan.kb_per_split = d.kh * d.kw * ((d.c_in + 63) / 64);
+        plan.part_bytes = 0;
+    }
+    const int rw = a.ow % 16 == 0 ? 16 : (a.ow % 8 == 0 ? 8 : 16);
+    const int rh = 128 / rw;
+    const int rtx = (a.ow + rw - 1) / rw, rty = (a.oh + rh - 1) / rh;
     const int bk = plan.bk;
     const CUtensorMapSwizzle swz = bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     const bool cat = a.x2 && a.c_split > 0;
@@ -1510,6 +1632,19 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
         // the A operand's map over an NHWC tensor of `ch` channels (a folded
         // concat has two: channels [0, c_split) and [c_split, c_in))
         auto encode_a = [&](CUtensorMap* ta, const void* ptr, int ch) {
+            if (rect) {
+                // the NHWC map as {C, W, H, N}; a box is one rectangular tile
+                cuuint64_t dims[4] = {(cuuint64_t)ch, (cuuint64_t)d.w, (cuuint64_t)d.h,
+                                      (cuuint64_t)d.n};
+                cuuint64_t strides[3] = {(cuuint64_t)ch * 2, (cuuint64_t)d.w * ch * 2,
+                                         (cuuint64_t)d.h * d.w * ch * 2};
+                cuuint32_t box[4] = {(cuuint32_t)bk, (cuuint32_t)rw, (cuuint32_t)rh, 1};
+                cuuint32_t es[4] = {1, 1, 1, 1};
+                return g_encode_tiled(ta, dt, 4, const_cast<void*>(ptr), dims, strides, box, es,
+                                      CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            }
             if (tiled) {
                 cuuint64_t dims[2] = {(cuuint64_t)ch, (cuuint64_t)M};
                 cuuint64_t strides[1] = {(cuuint64_t)ch * 2};
@@ -1541,7 +1676,7 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
         }
         if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
 
-        const int num_m_tiles = (int)((Mv + BM * plan.ms - 1) / (BM * plan.ms));
+        const int num_m_tiles = rect ? d.n * rty * rtx : (int)((Mv + BM * plan.ms - 1) / (BM * plan.ms));
         const int bn = plan.bn;
         {
             cuuint64_t dims[3] = {(cuuint64_t)d.c_in, (cuuint64_t)taps, (cuuint64_t)d.c_out};
@@ -1554,7 +1689,7 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
         }
         if (r != CUDA_SUCCESS) return ACNN_ERR_CUDA;
         Params prm{};
-        prm.M = (int)Mv;
+        prm.M = rect ? num_m_tiles * BM : (int)Mv;
         prm.C_out = d.c_out;
         prm.taps = taps;
         prm.KW = d.kw;
@@ -1574,12 +1709,20 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
         if (plan.splits > 1 && cudaMemsetAsync(a.ws_part, 0, cnt_bytes, s) != cudaSuccess)
             return ACNN_ERR_CUDA;
         prm.OW = a.ow;
+        prm.OH = a.oh;
         prm.OHW = a.oh * a.ow;
         prm.vw = vw;
         prm.vw_magic = ~0ull / (unsigned long long)vw + 1ull;
         prm.S = d.stride;
         prm.P = d.pad;
-        prm.a_mode = tiled ? 0 : (halo ? 2 : 1);
+        prm.a_mode = rect ? 3 : (tiled ? 0 : (halo ? 2 : 1));
+        prm.rw_log2 = rw == 16 ? 4 : 3;
+        prm.rh = rh;
+        prm.rtx = rtx;
+        prm.rty = rty;
+        prm.rtx_magic = ~0ull / (unsigned long long)rtx + 1ull;
+        prm.rty_magic = ~0ull / (unsigned long long)rty + 1ull;
+        prm.y2 = a.y2;
         prm.c_split = cat ? a.c_split : 0;
         prm.out_layout = a.out_layout;
         prm.act = a.act;

@@ -80,6 +80,7 @@ class Net:
     order: list = field(default_factory=list)    # section names in execution order
     conv_inputs: dict = field(default_factory=dict)     # conv name -> input tensor name(s)
     conv_residuals: dict = field(default_factory=dict)  # conv name -> residual tensor name
+    pooled: dict = field(default_factory=dict)  # pooled map written by a conv -> that conv's name
 
     # ------------------------------------------------------------ execution
     def sections(self):
@@ -148,8 +149,10 @@ class Builder:
         self.net.tensors[name] = t
         return t
 
-    def conv(self, src, spec: ConvSpec, residual=None, out=None):
+    def conv(self, src, spec: ConvSpec, residual=None, out=None, pool2=None):
         net = self.net
+        if pool2:
+            return self._conv_pool2(src, spec, residual, pool2)
         x = net.tensors[src]
         pn = spec.param or spec.name
         w = G.conv_weight(self.seed, pn, spec.c_out, spec.c_in, spec.k, spec.k, net.layout,
@@ -192,6 +195,39 @@ class Builder:
         net.ops.append(Op("conv", self.section, fn, _conv_flops(n, spec), byts, spec.name, spec,
                           launches=2 if staged else 1))
         return out or spec.name
+
+    def _conv_pool2(self, src, spec: ConvSpec, residual, pool_name):
+        """A 1x1 NHWC conv that also writes the 2x2/s2 average pool of its output
+        (tensor pool_name), for the next stage's shortcut (acnn_conv2d_fused_pool2)."""
+        net = self.net
+        x = net.tensors[src]
+        w = G.conv_weight(self.seed, spec.param or spec.name, spec.c_out, spec.c_in, 1, 1,
+                          net.layout, net.dtype)
+        b = G.conv_bias(self.seed, spec.param or spec.name, spec.c_out)
+        al = G.prelu_alpha(self.seed, spec.param or spec.name, spec.c_out) \
+            if spec.act == A.ACT_PRELU else None
+        net.params[spec.name] = (w, b, al)
+        wd, bd = w.to(self.device), b.to(self.device)
+        ald = al.to(self.device) if al is not None else None
+        y = self.buffer(spec.name, spec.c_out, spec.oh, spec.ow)
+        yp = self.buffer(pool_name, spec.c_out, spec.oh // 2, spec.ow // 2)
+        res = net.tensors[residual] if residual else None
+        res_mode = spec.res_mode if residual else A.RES_NONE
+        d = A.conv_desc(x, spec.c_out, 1, 1, 1, 0, net.layout)
+        net.conv_inputs[spec.name] = src
+        if residual:
+            net.conv_residuals[spec.name] = residual
+        net.pooled[pool_name] = spec.name
+
+        def fn(stream):
+            A.check(A.acnn_conv2d_fused_pool2(d, x, wd, bd, ald, res, res_mode, spec.act, y, yp,
+                                              stream), spec.name)
+
+        byts = (x.numel() + w.numel() + y.numel() + yp.numel() +
+                (y.numel() if res is not None else 0)) * self.es + 4 * spec.c_out
+        net.ops.append(Op("conv", self.section, fn, _conv_flops(net.batch, spec), byts, spec.name,
+                          spec))
+        return spec.name
 
     def conv_cat(self, src_a, src_b, spec: ConvSpec, residual=None):
         """spec over the channel concat [src_a | src_b] (NHWC), the concat folded
@@ -317,11 +353,16 @@ def stem_net(device="cuda", n=1, h=640, w=640) -> Net:
     return net
 
 
-def bottleneck(b: Builder, src, name, c_in, width, h, w, stride, shortcut):
+def bottleneck(b: Builder, src, name, c_in, width, h, w, stride, shortcut, pooled=None,
+               pool_out=False):
     """ResNet-D bottleneck: 1x1 -> 3x3 (stride here) -> 1x1, shortcut, add, ReLU.
 
     shortcut: 'identity', 'conv' (1x1, stride 1) or 'pool' (avgpool 2x2/s2 then 1x1).
     The add and the ReLU run in the last conv's epilogue (residual before act).
+    pooled: the name of src's 2x2/s2 average pool when the previous block's last
+    conv already wrote it (the 'pool' shortcut then runs no pool of its own);
+    pool_out: this block's last conv also writes the average pool of its output
+    (tensor f"{name}.pooled"), for the next stage's shortcut.
     """
     mid = width // 4
     c1 = ConvSpec(f"{name}.conv1", c_in, mid, 1, 1, 0, A.ACT_RELU, h, w)
@@ -333,12 +374,13 @@ def bottleneck(b: Builder, src, name, c_in, width, h, w, stride, shortcut):
     elif shortcut == "conv":
         res = b.conv(src, ConvSpec(f"{name}.short", c_in, width, 1, 1, 0, A.ACT_NONE, h, w))
     else:
-        pooled = b.pool(src, f"{name}.pool", A.POOL_AVG, 2, 2, 0, c_in, h, w)
+        if pooled is None:
+            pooled = b.pool(src, f"{name}.pool", A.POOL_AVG, 2, 2, 0, c_in, h, w)
         res = b.conv(pooled, ConvSpec(f"{name}.short", c_in, width, 1, 1, 0, A.ACT_NONE,
                                       h // 2, w // 2))
     t = b.conv(src, c1)
     t = b.conv(t, c2)
-    out = b.conv(t, c3, residual=res)
+    out = b.conv(t, c3, residual=res, pool2=f"{name}.pooled" if pool_out else None)
     return out, c2.oh, c2.ow
 
 
@@ -401,12 +443,20 @@ def backbone_net(device="cuda", n=8, h=640, w=640, neck="fusion") -> Net:
     cur, ch, cw = _stem(b, "x", h, w)
     c_in = 64
     feats = []
+    pooled = None
     for si, (blocks, width, stride, first_short) in enumerate(STAGES):
         b.set_section(f"stage{si + 1}")
         for bi in range(blocks):
             short = first_short if bi == 0 else "identity"
-            cur, ch, cw = bottleneck(b, cur, f"s{si + 1}.b{bi}", c_in, width, ch, cw,
-                                     stride if bi == 0 else 1, short)
+            # a stage's last block also writes the average pool of its output
+            # when the next stage's shortcut pools it (cross-op fusion)
+            pool_out = (bi == blocks - 1 and si + 1 < len(STAGES) and STAGES[si + 1][3] == "pool"
+                        and ch % 2 == 0 and cw % 2 == 0)
+            name = f"s{si + 1}.b{bi}"
+            cur, ch, cw = bottleneck(b, cur, name, c_in, width, ch, cw,
+                                     stride if bi == 0 else 1, short,
+                                     pooled=pooled if bi == 0 else None, pool_out=pool_out)
+            pooled = f"{name}.pooled" if pool_out else None
             c_in = width
         feats.append((cur, ch, cw, width))
     b.set_section("neck")

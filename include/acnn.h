@@ -236,6 +236,25 @@ int acnn_conv2d_fused_noalloc(const acnn_conv_desc* d, const void* x, const void
                               const float* bias, const float* alpha, const void* residual,
                               int res_mode, int act, void* y, acnn_stream_t stream);
 
+/* ---- conv with a pooled second output (cross-op fusion) --------------------
+ * acnn_conv2d_fused_pool2: acnn_conv2d_fused of a 1x1/s1/p0 NHWC fp16/bf16
+ * conv (C_in >= 64, even output height and width) that also writes
+ * y_pool = the 2x2/s2 average pool of y (NHWC [n][oh/2][ow/2][c_out], same
+ * dtype, caller-owned device buffer, 16-byte aligned, overlapping none of the
+ * other buffers).  rtdetr_gpu.rs RtDetrGpu::encoder_maps runs AVGPOOL_SRC as a
+ * kernel of its own on a stage's last bottleneck output, feeding the next
+ * stage's shortcut; here the conv that writes that output also writes its
+ * pooled map: each epilogue warp owns whole 2x2 windows (the conv's tiles are
+ * rectangles of 16 x 8 or 8 x 16 pixels) and averages the four stored values
+ * as the pool does, ((a + b) + c) + d in fp32 times 0.25 rounded once, so
+ * y_pool equals acnn_pool2d(ACNN_POOL_AVG, 2, 2, 0) of y bit for bit.  No
+ * workspace (no K split).  Returns ACNN_ERR_UNSUPPORTED for other geometries,
+ * otherwise the errors of acnn_conv2d_fused; nothing is launched on error.
+ */
+int acnn_conv2d_fused_pool2(const acnn_conv_desc* d, const void* x, const void* w,
+                            const float* bias, const float* alpha, const void* residual,
+                            int res_mode, int act, void* y, void* y_pool, acnn_stream_t stream);
+
 /* ---- pool2d ----------------------------------------------------------------
  * MAX: y = max over the in-range taps of each k x k window at stride s, pad p
  *      (taps outside the input are skipped: -inf padding), rtdetr_gpu.rs

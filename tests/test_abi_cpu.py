@@ -98,6 +98,27 @@ def test_conv_path_selection(A):
     assert A.acnn_conv2d_workspace_size(desc(A, c_in=64, c_out=64)) == 0
 
 
+def test_conv_pool2_rejects_before_launch(A):
+    """The conv with a pooled second output validates on the host: geometry it
+    does not serve, a missing pooled buffer, misalignment and aliasing."""
+    def c(*args):
+        return A.acnn_conv2d_fused_pool2(*args, 0)  # stream 0: nothing is enqueued
+    ok = desc(A, c_in=64, c_out=64, kh=1, kw=1, pad=0)
+    P = 0x6000000
+    assert c(desc(A, c_in=64, c_out=64), X, W, None, None, None, 0, 0, Y, P) == 3     # 3x3
+    assert c(desc(A, c_in=64, c_out=64, kh=1, kw=1, pad=0, h=7), X, W, None, None, None, 0, 0,
+             Y, P) == 3                                                              # odd height
+    assert c(desc(A, c_in=32, c_out=64, kh=1, kw=1, pad=0), X, W, None, None, None, 0, 0,
+             Y, P) == 3                                                              # C_in < 64
+    assert c(desc(A, c_in=64, c_out=64, kh=1, kw=1, pad=0, layout=1), X, W, None, None, None,
+             0, 0, Y, P) == 3                                                        # NCHW
+    assert c(ok, X, W, None, None, None, 0, 0, Y, None) == 1                           # no y_pool
+    assert c(ok, X, W, None, None, None, 0, 0, Y, P + 8) == 4                          # misaligned
+    assert c(ok, X, W, None, None, None, 0, 0, Y, Y + 64) == 6                         # y_pool in y
+    assert c(ok, X, W, None, None, None, 0, 0, Y, X) == 6                              # y_pool in x
+    assert c(ok, X, W, None, None, None, 0, 9, Y, P) == 7                              # bad act
+
+
 def test_force_path_selects_the_tiny_kernel(A):
     """The tuning hook routes the 3/6/7-channel 3x3 convs to the direct kernel
     (and nothing else), and path 0 restores the router."""

@@ -341,6 +341,67 @@ def test_conv_halo_rows_integer_bitexact(cin):
     assert_bitexact(y, O.round_storage(ref, O.BF16), f"halo int cin{cin}")
 
 
+# ---------------------------------------------------------------- conv + pooled output
+POOL2_CASES = [
+    # name, n, h, w, cin, cout, act, res_mode
+    ("s1_like", 2, 16, 32, 64, 256, A.ACT_RELU, A.RES_ADD_THEN_ACT),      # 16 x 8 tiles
+    ("s3_like", 2, 40, 40, 256, 512, A.ACT_RELU, A.RES_ADD_THEN_ACT),     # 8 x 16, rows ragged
+    ("ragged_both", 1, 6, 10, 128, 64, A.ACT_SILU, A.RES_NONE),          # neither divides
+    ("w24", 3, 20, 24, 64, 128, A.ACT_PRELU, A.RES_ACT_THEN_ADD),
+    ("one_window", 1, 2, 2, 64, 64, A.ACT_NONE, A.RES_NONE),
+    ("cout72", 2, 8, 16, 96, 72, A.ACT_RELU, A.RES_NONE),                # ragged column tile
+]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("case", POOL2_CASES, ids=[c[0] for c in POOL2_CASES])
+def test_conv_fused_pool2(case, dt):
+    """The 1x1 conv with a pooled second output: y bit-identical to acnn_conv2d_fused,
+    y_pool bit-identical to acnn_pool2d (average 2x2/s2) of y, both within
+    tolerance of the oracle, nothing written outside either buffer."""
+    name, n, h, w, cin, cout, act, res_mode = case
+    seed = 15
+    x = G.tensor(seed, name + ".x", (n, h, w, cin), "normal", dtype=DT[dt]).cuda()
+    wt = G.conv_weight(seed, name, cout, cin, 1, 1, G.NHWC, DT[dt]).cuda()
+    b = G.conv_bias(seed, name, cout).cuda()
+    al = G.prelu_alpha(seed, name, cout).cuda()
+    r = G.tensor(seed, name + ".r", (n, h, w, cout), "normal", dtype=DT[dt]).cuda() \
+        if res_mode else None
+    gy = Guarded((n, h, w, cout), TDT[dt])
+    gp = Guarded((n, h // 2, w // 2, cout), TDT[dt])
+    d = A.conv_desc(x, cout, 1, 1, 1, 0, G.NHWC)
+    st = A.acnn_conv2d_fused_pool2(d, x, wt, b, al, r, res_mode, act, gy.t, gp.t)
+    assert st == 0, A.status_string(st)
+    gy.check(name + " y")
+    gp.check(name + " y_pool")
+    y_ref = A.conv2d_fused(x, wt, b, act=act, alpha=al, residual=r, res_mode=res_mode)
+    p_ref = A.pool2d(y_ref, A.POOL_AVG, 2, 2, 0)
+    torch.cuda.synchronize()
+    assert_bitexact(gy.t, y_ref, name + " y vs conv2d_fused")
+    assert_bitexact(gp.t, p_ref, name + " y_pool vs pool2d")
+    ref = O.conv2d(to64(x), to64(wt), to64(b), act=act, alpha=to64(al),
+                   residual=None if r is None else to64(r), res_mode=res_mode)
+    assert_parity(gy.t, ref, TDT[dt], name)
+    # the oracle pools the stored (rounded) conv output, as the workloads do
+    ref_p = O.pool2d(O.round_storage(ref, ODT[dt]), O.AVG, 2, 2, 0)
+    assert_parity(gp.t, ref_p, TDT[dt], name + " pooled")
+
+
+def test_conv_fused_pool2_rejects():
+    """Only 1x1/s1/p0 NHWC 16-bit convs with C_in >= 64 and an even output map."""
+    X, W, Y, P = (torch.empty(4 << 20, dtype=torch.uint8, device="cuda") for _ in range(4))
+    for desc in (A.ConvDesc(1, 8, 8, 64, 64, 3, 3, 1, 1, G.NHWC, G.BF16),   # 3x3
+                 A.ConvDesc(1, 7, 8, 64, 64, 1, 1, 1, 0, G.NHWC, G.BF16),   # odd height
+                 A.ConvDesc(1, 8, 8, 32, 64, 1, 1, 1, 0, G.NHWC, G.BF16),   # 32-channel blocks
+                 A.ConvDesc(1, 8, 8, 64, 64, 1, 1, 1, 0, G.NCHW, G.F16),    # NCHW
+                 A.ConvDesc(1, 8, 8, 64, 64, 1, 1, 1, 0, G.NHWC, G.F32)):   # fp32
+        st = A.acnn_conv2d_fused_pool2(desc, X, W, None, None, None, 0, 0, Y, P)
+        assert st == 3, A.status_string(st)  # ACNN_ERR_UNSUPPORTED
+    d = A.ConvDesc(1, 8, 8, 64, 64, 1, 1, 1, 0, G.NHWC, G.BF16)
+    assert A.acnn_conv2d_fused_pool2(d, X, W, None, None, None, 0, 0, Y, None) == 1
+    assert A.acnn_conv2d_fused_pool2(d, X, W, None, None, None, 0, 0, Y, Y) == 6  # alias
+
+
 # ---------------------------------------------------------------- tiny C_in (path 4)
 TINY_CASES = [
     # name, n, h, w, cin, cout, s, p, dt, layout
