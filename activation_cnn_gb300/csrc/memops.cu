@@ -1116,6 +1116,10 @@ cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, 
     };
     int tp = ow;
     while (tp > 1 && staged(tp) > 32768) tp = (tp + 1) / 2;
+    // and short enough that the launch has at least four blocks per SM (the
+    // frame input: 136 output rows would otherwise give 136 blocks)
+    while (tp > 16 && (long long)d.n * oh * ((ow + tp - 1) / tp) < 4LL * sm_count())
+        tp = (tp + 1) / 2;
     const int segs = (ow + tp - 1) / tp;
     const long long blocks = (long long)d.n * oh * segs;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
