@@ -37,7 +37,7 @@ def sources():
 
 
 def _inputs():
-    return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + \
+    return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 

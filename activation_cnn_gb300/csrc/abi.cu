@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "per_device.h"
 
 namespace acnn {
 
@@ -51,29 +52,12 @@ int sm_count() {
 // process that drives several GPUs opts in on each before its first launch
 // there.  Thread-safe; a larger request than the one recorded is set again.
 int ensure_smem_optin(const void* kernel, size_t bytes) {
-    struct Entry {
-        const void* k;
-        int dev;
-        size_t bytes;
-    };
-    static std::mutex mu;
-    static std::vector<Entry> done;
-    const int dev = current_device();
-    std::lock_guard<std::mutex> lk(mu);
-    for (Entry& e : done)
-        if (e.k == kernel && e.dev == dev) {
-            if (e.bytes >= bytes) return ACNN_OK;
-            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)bytes) != cudaSuccess)
-                return ACNN_ERR_CUDA;
-            e.bytes = bytes;
-            return ACNN_OK;
-        }
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
-        cudaSuccess)
-        return ACNN_ERR_CUDA;
-    done.push_back(Entry{kernel, dev, bytes});
-    return ACNN_OK;
+    static PerDeviceSizes done;
+    const bool ok = done.ensure(kernel, current_device(), bytes, [&] {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)bytes) == cudaSuccess;
+    });
+    return ok ? ACNN_OK : ACNN_ERR_CUDA;
 }
 
 int occupancy_blocks(const void* kernel, int threads, size_t smem) {

@@ -213,3 +213,22 @@ def test_section_end_null(A):
     assert A.lib().acnn_section_end(None, None) == 1
     assert A.acnn_section_launch(None, 0) == 1
     assert A.acnn_section_destroy(None) == 0
+
+
+def test_per_device_opt_in_bookkeeping(tmp_path):
+    """The per-device record behind the dynamic shared-memory opt-in
+    (csrc/per_device.h), compiled on the host with g++: a kernel opted in on
+    one device is not taken as opted in on another, larger requests are
+    applied again, failures are not recorded, concurrent callers apply once."""
+    import shutil
+    import subprocess
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("g++ not found")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    exe = str(tmp_path / "per_device_check")
+    subprocess.run([gxx, "-std=c++17", "-O1", "-pthread",
+                    "-I", os.path.join(root, "activation_cnn_gb300", "csrc"),
+                    os.path.join(root, "tests", "per_device_check.cpp"), "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
