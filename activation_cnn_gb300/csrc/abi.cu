@@ -554,6 +554,73 @@ int acnn_conv2d_fused_pool2(const acnn_conv_desc* d, const void* x, const void* 
     return launch_igemm_conv(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int acnn_conv2d_fused_up2(const acnn_conv_desc* d, const void* x_a, int c_a, const void* x_b,
+                          const void* w, const float* bias, const float* alpha,
+                          const void* residual, int res_mode, int act, void* y, void* y_up,
+                          void* workspace, size_t ws_bytes, acnn_stream_t stream) {
+    int st = check_desc(d);
+    if (st != ACNN_OK) return st;
+    if (act < ACNN_ACT_NONE || act > ACNN_ACT_PRELU || res_mode < ACNN_RES_NONE ||
+        res_mode > ACNN_RES_ACT_THEN_ADD)
+        return ACNN_ERR_BAD_ENUM;
+    if (!x_a || !w || !y || !y_up) return ACNN_ERR_NULL_POINTER;
+    if (act == ACNN_ACT_PRELU && !alpha) return ACNN_ERR_NULL_POINTER;
+    if (res_mode != ACNN_RES_NONE && !residual) return ACNN_ERR_NULL_POINTER;
+    // x_b NULL: x_a holds all c_in channels (c_a is ignored)
+    const bool cat = x_b != nullptr;
+    const int ca = cat ? c_a : d->c_in, cb = d->c_in - ca;
+    if (d->layout != ACNN_NHWC || d->dtype == ACNN_F32) return ACNN_ERR_UNSUPPORTED;
+    if (cat && (ca <= 0 || cb <= 0 || ca % 64 != 0 || cb % 8 != 0)) return ACNN_ERR_UNSUPPORTED;
+    int oh, ow;
+    st = conv_out(d, &oh, &ow);
+    if (st != ACNN_OK) return st;
+    const Route r = route(d, oh, ow);
+    if (r.path != 1 && r.path != 2) return ACNN_ERR_UNSUPPORTED;
+    if (4ll * d->n * oh * ow > kIndexLimit) return ACNN_ERR_TOO_LARGE;
+    if (!aligned16(x_a) || (cat && !aligned16(x_b)) || !aligned16(w) || !aligned16(y) ||
+        !aligned16(y_up) || (bias && !aligned16(bias)) || (alpha && !aligned16(alpha)) ||
+        (residual && !aligned16(residual)) || (workspace && !aligned16(workspace)))
+        return ACNN_ERR_MISALIGNED;
+    const size_t es = elem_size(d->dtype);
+    const size_t px = (size_t)d->n * d->h * d->w;
+    const size_t xab = px * ca * es, xbb = px * cb * es;
+    const size_t wb = (size_t)d->c_out * d->kh * d->kw * d->c_in * es;
+    const size_t yb = (size_t)d->n * oh * ow * d->c_out * es;
+    const size_t ub = 4 * yb;
+    const bool res = residual && res_mode != ACNN_RES_NONE;
+    auto hits = [&](const void* p, size_t n) {
+        return overlaps(p, n, x_a, xab) || (cat && overlaps(p, n, x_b, xbb)) ||
+               overlaps(p, n, w, wb) || (res && overlaps(p, n, residual, yb)) ||
+               (bias && overlaps(p, n, bias, d->c_out * 4)) ||
+               (alpha && act == ACNN_ACT_PRELU && overlaps(p, n, alpha, d->c_out * 4));
+    };
+    if (hits(y, yb) || hits(y_up, ub) || overlaps(y, yb, y_up, ub)) return ACNN_ERR_ALIAS;
+    if (!workspace) ws_bytes = 0;
+    if (ws_bytes > 0 && (hits(workspace, ws_bytes) || overlaps(workspace, ws_bytes, y, yb) ||
+                         overlaps(workspace, ws_bytes, y_up, ub)))
+        return ACNN_ERR_ALIAS;
+    ConvArgs a{};
+    a.d = *d;
+    a.oh = oh;
+    a.ow = ow;
+    a.x = x_a;
+    a.x2 = cat ? x_b : nullptr;
+    a.c_split = cat ? ca : 0;
+    a.w = w;
+    a.bias = bias;
+    a.alpha = act == ACNN_ACT_PRELU ? alpha : nullptr;
+    a.residual = res ? residual : nullptr;
+    a.res_mode = res_mode;
+    a.act = act;
+    a.y = y;
+    a.y2 = y_up;
+    a.y2_up = 1;
+    a.out_layout = ACNN_NHWC;
+    a.ws_part = ws_bytes > 0 ? workspace : nullptr;  // NHWC: no staging, all for split-K
+    a.ws_part_bytes = ws_bytes;
+    return launch_igemm_conv(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int acnn_pool2d(int kind, int n, int h, int w, int c, int k, int stride, int pad, int layout,
                 int dtype, const void* x, void* y, acnn_stream_t stream) {
     if (kind != ACNN_POOL_MAX && kind != ACNN_POOL_AVG) return ACNN_ERR_BAD_ENUM;

@@ -100,9 +100,11 @@ struct ConvArgs {
     // and x2 channels [c_split, c_in), both NHWC (c_split = 0: x holds all)
     const void* x2 = nullptr;
     int c_split = 0;
-    // 1x1 convs only: NHWC [n][oh/2][ow/2][c_out], the 2x2/s2 average pool of y
-    // written by the conv's epilogue (NULL: none)
+    // A second output written by the conv's epilogue (NULL: none), NHWC:
+    // y2_up = 0: [n][oh/2][ow/2][c_out], the 2x2/s2 average pool of y (1x1 convs);
+    // y2_up = 1: [n][2 oh][2 ow][c_out], the nearest 2x upsample of y
     void* y2 = nullptr;
+    int y2_up = 0;
 };
 
 // Tile width and K split of the tensor-core conv for a geometry, given the

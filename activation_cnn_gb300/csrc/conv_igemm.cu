@@ -105,7 +105,9 @@ struct Params {
     // one 4-D box; rtx_magic / rty_magic divide by rtx / rty as vw_magic does.
     int rw_log2, rh, rtx, rty;
     unsigned long long rtx_magic, rty_magic;
-    void* y2;         // a_mode 3: NHWC [N][OH/2][OW/2][C_out], the 2x2/s2 average of y
+    void* y2;         // a_mode 3: NHWC [N][OH/2][OW/2][C_out], the 2x2/s2 average of y;
+                      // y2_up: NHWC [N][2 OH][2 OW][C_out], the nearest 2x upsample of y
+    int y2_up;
     int a_mode;       // 0: tiled A (1x1/s1/p0); 1: im2col A; 2: im2col A with halo rows;
                       // 3: tiled A in rectangular tiles (1x1/s1/p0, pooled second output)
     int c_split;      // channels [c_split, C_in) come from the second A map (0: none)
@@ -150,6 +152,21 @@ __device__ __forceinline__ int real_pixel(const Params& p, int v) {
     const int row = (int)__umul64hi((unsigned long long)v, p.vw_magic);  // v / vw
     const int j = v - row * p.vw;
     return j < p.OW ? row * p.OW + j : -1;
+}
+
+// The nearest 2x upsample of y as a second output: the 16-byte piece u of
+// real output pixel m (row n * OH + oy, column ox) at channel col goes to the
+// 2 x 2 block of pixels (2 oy + dy, 2 ox + dx), whose upsampled row index is
+// 2 (n * OH + oy) + dy.
+template <typename T>
+__device__ __forceinline__ void store_up2(const Params& p, int m, int col, uint4 u) {
+    const int row = m / p.OW, ox = m - row * p.OW;
+    const long long W2 = 2ll * p.OW;
+    T* up = static_cast<T*>(p.y2) + ((2ll * row) * W2 + 2 * ox) * p.C_out + col;
+    *reinterpret_cast<uint4*>(up) = u;
+    *reinterpret_cast<uint4*>(up + p.C_out) = u;
+    *reinterpret_cast<uint4*>(up + W2 * p.C_out) = u;
+    *reinterpret_cast<uint4*>(up + W2 * p.C_out + p.C_out) = u;
 }
 
 // Rows v0 .. v0 + 31 of one epilogue chunk -> real output pixels.  With
@@ -984,8 +1001,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int rr = 8 * k + crow;
                         const uint4 u = *reinterpret_cast<const uint4*>(slot + piece(rr, cpiece));
                         const int mo = real_pixel(p, row0 + rr);
-                        if (mo >= 0 && col < p.C_out)
+                        if (mo >= 0 && col < p.C_out) {
                             *reinterpret_cast<uint4*>(y + (long long)mo * p.C_out + col) = u;
+                            if (p.y2_up) store_up2<T>(p, mo, col, u);
+                        }
                     }
                     __syncwarp();  // the slot is read out before the next block reuses it
                 } else {
@@ -1174,10 +1193,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int rr = 8 * k + crow;
                     const uint4 u = *reinterpret_cast<const uint4*>(slot + piece(rr, cpiece));
                     const int mo = map_row(p, cm, rr);
-                    if (mo >= 0 && col < p.C_out)
+                    if (mo >= 0 && col < p.C_out) {
                         *reinterpret_cast<uint4*>(y + (long long)mo * p.C_out + col) = u;
+                        if (p.y2_up) store_up2<T>(p, mo, col, u);
+                    }
                 }
-                if (p.y2) {
+                if (p.y2 && !p.y2_up) {
                     // pooled second output (rectangular tiles): a chunk holds
                     // 32 / rw >= 2 whole tile rows, i.e. 8 whole 2x2 windows;
                     // lane l averages the 16-byte piece l & 3 (8 channels) of
@@ -1604,7 +1625,7 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
     // A pooled second output (1x1/s1/p0 only): rectangular tiles of 128 pixels,
     // rw columns x 128 / rw rows with rw = 16 or 8, so that each epilogue warp's
     // 32 rows hold whole 2x2 windows; one 128-row block, no K split.
-    const bool rect = a.y2 != nullptr;
+    const bool rect = a.y2 != nullptr && !a.y2_up;
     if (rect) {
         if (!tiled || plan.bk != 64 || a.out_layout != ACNN_NHWC || a.oh % 2 || a.ow % 2)
             return ACNN_ERR_UNSUPPORTED;
@@ -1723,6 +1744,7 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
         prm.rtx_magic = ~0ull / (unsigned long long)rtx + 1ull;
         prm.rty_magic = ~0ull / (unsigned long long)rty + 1ull;
         prm.y2 = a.y2;
+        prm.y2_up = a.y2_up;
         prm.c_split = cat ? a.c_split : 0;
         prm.out_layout = a.out_layout;
         prm.act = a.act;

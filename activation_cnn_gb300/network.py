@@ -81,6 +81,7 @@ class Net:
     conv_inputs: dict = field(default_factory=dict)     # conv name -> input tensor name(s)
     conv_residuals: dict = field(default_factory=dict)  # conv name -> residual tensor name
     pooled: dict = field(default_factory=dict)  # pooled map written by a conv -> that conv's name
+    upsampled: dict = field(default_factory=dict)  # 2x-upsampled map written by a conv -> its name
 
     # ------------------------------------------------------------ execution
     def sections(self):
@@ -149,10 +150,12 @@ class Builder:
         self.net.tensors[name] = t
         return t
 
-    def conv(self, src, spec: ConvSpec, residual=None, out=None, pool2=None):
+    def conv(self, src, spec: ConvSpec, residual=None, out=None, pool2=None, up2=None):
         net = self.net
         if pool2:
             return self._conv_pool2(src, spec, residual, pool2)
+        if up2:
+            return self._conv_up2(src, None, spec, residual, up2)
         x = net.tensors[src]
         pn = spec.param or spec.name
         w = G.conv_weight(self.seed, pn, spec.c_out, spec.c_in, spec.k, spec.k, net.layout,
@@ -229,9 +232,52 @@ class Builder:
                           spec))
         return spec.name
 
-    def conv_cat(self, src_a, src_b, spec: ConvSpec, residual=None):
+    def _conv_up2(self, src_a, src_b, spec: ConvSpec, residual, up_name):
+        """An NHWC conv (over [src_a | src_b] when src_b is given) that also
+        writes the nearest 2x upsample of its output (tensor up_name)
+        (acnn_conv2d_fused_up2)."""
+        net = self.net
+        xa = net.tensors[src_a]
+        xb = net.tensors[src_b] if src_b else None
+        ca = xa.shape[3]
+        pn = spec.param or spec.name
+        w = G.conv_weight(self.seed, pn, spec.c_out, spec.c_in, spec.k, spec.k, net.layout,
+                          net.dtype)
+        b = G.conv_bias(self.seed, pn, spec.c_out)
+        al = G.prelu_alpha(self.seed, pn, spec.c_out) if spec.act == A.ACT_PRELU else None
+        net.params[spec.name] = (w, b, al)
+        wd, bd = w.to(self.device), b.to(self.device)
+        ald = al.to(self.device) if al is not None else None
+        y = self.buffer(spec.name, spec.c_out, spec.oh, spec.ow)
+        yu = self.buffer(up_name, spec.c_out, 2 * spec.oh, 2 * spec.ow)
+        d = A.ConvDesc(net.batch, spec.h, spec.w, spec.c_in, spec.c_out, spec.k, spec.k,
+                       spec.stride, spec.pad, net.layout, net.dtype)
+        ws_bytes = A.acnn_conv2d_workspace_size(d)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device) if ws_bytes else None
+        net.tensors[spec.name + ".ws"] = ws
+        net.conv_inputs[spec.name] = (src_a, src_b) if src_b else src_a
+        res = net.tensors[residual] if residual else None
+        res_mode = spec.res_mode if residual else A.RES_NONE
+        if residual:
+            net.conv_residuals[spec.name] = residual
+        net.upsampled[up_name] = spec.name
+
+        def fn(stream):
+            A.check(A.acnn_conv2d_fused_up2(d, xa, ca, xb, wd, bd, ald, res, res_mode, spec.act,
+                                            y, yu, ws, ws_bytes, stream), spec.name)
+
+        byts = (xa.numel() + (xb.numel() if xb is not None else 0) + w.numel() + y.numel() +
+                yu.numel() + (y.numel() if res is not None else 0)) * self.es + 4 * spec.c_out
+        net.ops.append(Op("conv", self.section, fn, _conv_flops(net.batch, spec), byts, spec.name,
+                          spec))
+        return spec.name
+
+    def conv_cat(self, src_a, src_b, spec: ConvSpec, residual=None, up2=None):
         """spec over the channel concat [src_a | src_b] (NHWC), the concat folded
-        into the conv's operand loads (acnn_conv2d_fused_cat2)."""
+        into the conv's operand loads (acnn_conv2d_fused_cat2); up2: also write
+        the nearest 2x upsample of the output under that name."""
+        if up2:
+            return self._conv_up2(src_a, src_b, spec, residual, up2)
         net = self.net
         xa, xb = net.tensors[src_a], net.tensors[src_b]
         ca = xa.shape[3]
@@ -404,7 +450,7 @@ def block_net(device="cuda", variant="identity", n=4, h=80, w=80) -> Net:
 STAGES = [(3, 256, 1, "conv"), (4, 512, 2, "pool"), (6, 1024, 2, "pool"), (3, 2048, 2, "pool")]
 
 
-def csp_block(b: Builder, src_a, src_b, name, h, w, blocks=3, hidden=256):
+def csp_block(b: Builder, src_a, src_b, name, h, w, blocks=3, hidden=256, up2=None):
     """CSP block over [src_a | src_b] (512 channels) -> 256, as P1
     RtDetrGpu::csp composes it: a = conv1(x); per RepVGG bottleneck
     a = SiLU(conv3x3(a) + conv1x1(a)); out = a + conv2(x).  conv1 and conv2 are
@@ -418,7 +464,7 @@ def csp_block(b: Builder, src_a, src_b, name, h, w, blocks=3, hidden=256):
         a = b.conv(a, ConvSpec(f"{name}.rep{i}.conv3x3", hidden, hidden, 3, 1, 1, S, h, w,
                                res_mode=A.RES_ADD_THEN_ACT), residual=q)
     return b.conv_cat(src_a, src_b, ConvSpec(name, 512, 256, 1, 1, 0, S, h, w,
-                                             res_mode=A.RES_ACT_THEN_ADD), residual=a)
+                                             res_mode=A.RES_ACT_THEN_ADD), residual=a, up2=up2)
 
 
 def backbone_net(device="cuda", n=8, h=640, w=640, neck="fusion") -> Net:
@@ -464,15 +510,25 @@ def backbone_net(device="cuda", n=8, h=640, w=640, neck="fusion") -> Net:
     S = A.ACT_SILU
     lat3 = b.conv(c3, ConvSpec("neck.lat3", ch3, 256, 1, 1, 0, S, h3, w3))
     lat4 = b.conv(c4, ConvSpec("neck.lat4", ch4, 256, 1, 1, 0, S, h4, w4))
-    f5 = b.conv(c5, ConvSpec("neck.lat5", ch5, 256, 1, 1, 0, S, h5, w5))
-    def fuse(src_a, src_b, name, hh, ww):
-        if neck == "csp":
-            return csp_block(b, src_a, src_b, name, hh, ww)
-        return b.conv_cat(src_a, src_b, ConvSpec(name, 512, 256, 3, 1, 1, S, hh, ww))
 
-    up5 = b.resize(f5, "neck.up5", A.RESIZE_NEAREST, 256, h5, w5, h4, w4)
-    f4 = fuse(up5, lat4, "neck.fpn4", h4, w4)
-    up4 = b.resize(f4, "neck.up4", A.RESIZE_NEAREST, 256, h4, w4, h3, w3)
+    def fuse(src_a, src_b, name, hh, ww, up2=None):
+        if neck == "csp":
+            return csp_block(b, src_a, src_b, name, hh, ww, up2=up2)
+        return b.conv_cat(src_a, src_b, ConvSpec(name, 512, 256, 3, 1, 1, S, hh, ww), up2=up2)
+
+    # the two top-down nearest 2x upsamples are written by the convs that
+    # produce the maps they upsample (cross-op fusion), when the sizes double
+    fold = 2 * h5 == h4 and 2 * w5 == w4 and 2 * h4 == h3 and 2 * w4 == w3
+    if fold:
+        f5 = b.conv(c5, ConvSpec("neck.lat5", ch5, 256, 1, 1, 0, S, h5, w5), up2="neck.up5")
+        up5 = "neck.up5"
+        f4 = fuse(up5, lat4, "neck.fpn4", h4, w4, up2="neck.up4")
+        up4 = "neck.up4"
+    else:
+        f5 = b.conv(c5, ConvSpec("neck.lat5", ch5, 256, 1, 1, 0, S, h5, w5))
+        up5 = b.resize(f5, "neck.up5", A.RESIZE_NEAREST, 256, h5, w5, h4, w4)
+        f4 = fuse(up5, lat4, "neck.fpn4", h4, w4)
+        up4 = b.resize(f4, "neck.up4", A.RESIZE_NEAREST, 256, h4, w4, h3, w3)
     f3 = fuse(up4, lat3, "neck.fpn3", h3, w3)
     d3 = b.conv(f3, ConvSpec("neck.down3", 256, 256, 3, 2, 1, S, h3, w3))
     n4 = fuse(d3, f4, "neck.pan4", h4, w4)

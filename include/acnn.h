@@ -255,6 +255,25 @@ int acnn_conv2d_fused_pool2(const acnn_conv_desc* d, const void* x, const void* 
                             const float* bias, const float* alpha, const void* residual,
                             int res_mode, int act, void* y, void* y_pool, acnn_stream_t stream);
 
+/* acnn_conv2d_fused_up2: acnn_conv2d_fused (x_b NULL; c_a ignored) or
+ * acnn_conv2d_fused_cat2 (x_b non-NULL: channels [0, c_a) from x_a, the rest
+ * from x_b) of an NHWC fp16/bf16 conv on the tensor-core paths that also
+ * writes y_up = the nearest 2x upsample of y (NHWC [n][2 oh][2 ow][c_out],
+ * same dtype, caller-owned device buffer, 16-byte aligned, overlapping none of
+ * the other buffers).  rtdetr_gpu.rs RtDetrGpu::encoder_maps upsamples a
+ * neck map with UPSAMPLE_SRC, a kernel of its own, right after the conv that
+ * writes it; here that conv's epilogue writes each stored 16-byte piece of y
+ * into the 2 x 2 block of y_up it maps to as well, so y_up equals
+ * acnn_resize2d(ACNN_RESIZE_NEAREST, 2 oh, 2 ow) of y bit for bit.  Workspace
+ * as acnn_conv2d_fused (split-K partial sums only).  Returns
+ * ACNN_ERR_UNSUPPORTED for other geometries, ACNN_ERR_TOO_LARGE when y_up
+ * would pass 2^31 - 1 pixels, otherwise the errors of acnn_conv2d_fused.
+ */
+int acnn_conv2d_fused_up2(const acnn_conv_desc* d, const void* x_a, int c_a, const void* x_b,
+                          const void* w, const float* bias, const float* alpha,
+                          const void* residual, int res_mode, int act, void* y, void* y_up,
+                          void* workspace, size_t ws_bytes, acnn_stream_t stream);
+
 /* ---- pool2d ----------------------------------------------------------------
  * MAX: y = max over the in-range taps of each k x k window at stride s, pad p
  *      (taps outside the input are skipped: -inf padding), rtdetr_gpu.rs

@@ -119,6 +119,22 @@ def test_conv_pool2_rejects_before_launch(A):
     assert c(ok, X, W, None, None, None, 0, 9, Y, P) == 7                              # bad act
 
 
+def test_conv_up2_rejects_before_launch(A):
+    """The conv with an upsampled second output validates on the host."""
+    def c(dsc, x_b, y_up, c_a=0, act=0):
+        return A.acnn_conv2d_fused_up2(dsc, X, c_a, x_b, W, None, None, None, 0, act, Y, y_up,
+                                       None, 0, 0)
+    U = 0x7000000
+    ok = desc(A, c_in=64, c_out=64)
+    assert c(desc(A, c_in=64, c_out=64, layout=1, dtype=1), None, U) == 3     # NCHW
+    assert c(desc(A, c_in=64, c_out=64, dtype=0), None, U) == 3               # fp32
+    assert c(desc(A, c_in=128, c_out=64), R, U, c_a=32) == 3                  # c_a % 64
+    assert c(ok, None, None) == 1                                             # no y_up
+    assert c(ok, None, U + 8) == 4                                            # misaligned
+    assert c(ok, None, Y + 64) == 6                                           # y_up in y
+    assert c(ok, None, U, act=9) == 7
+
+
 def test_force_path_selects_the_tiny_kernel(A):
     """The tuning hook routes the 3/6/7-channel 3x3 convs to the direct kernel
     (and nothing else), and path 0 restores the router."""

@@ -387,6 +387,56 @@ def test_conv_fused_pool2(case, dt):
     assert_parity(gp.t, ref_p, TDT[dt], name + " pooled")
 
 
+UP2_CASES = [
+    # name, n, h, w, c_a, c_b, cout, k, act, res_mode
+    ("lat5_like", 8, 20, 20, 2048, 0, 256, 1, A.ACT_SILU, A.RES_NONE),      # split K
+    ("fpn4_like", 2, 40, 40, 256, 256, 256, 3, A.ACT_SILU, A.RES_NONE),     # folded concat
+    ("odd", 1, 5, 7, 64, 0, 64, 3, A.ACT_RELU, A.RES_ADD_THEN_ACT),
+    ("csp_out", 2, 10, 12, 256, 256, 256, 1, A.ACT_SILU, A.RES_ACT_THEN_ADD),
+]
+
+
+@pytest.mark.parametrize("case", UP2_CASES, ids=[c[0] for c in UP2_CASES])
+def test_conv_fused_up2(case):
+    """A conv that also writes the nearest 2x upsample of its output: y bit-identical
+    to the plain (or concat-folded) conv, y_up bit-identical to resize2d nearest of y,
+    nothing written outside either buffer."""
+    name, n, h, w, ca, cb, cout, k, act, res_mode = case
+    seed, dt = 16, "bf16"
+    cin = ca + cb
+    xa = G.tensor(seed, name + ".xa", (n, h, w, ca), "normal", dtype=DT[dt]).cuda()
+    xb = G.tensor(seed, name + ".xb", (n, h, w, cb), "normal", dtype=DT[dt]).cuda() if cb else None
+    wt = G.conv_weight(seed, name, cout, cin, k, k, G.NHWC, DT[dt]).cuda()
+    b = G.conv_bias(seed, name, cout).cuda()
+    r = G.tensor(seed, name + ".r", (n, h, w, cout), "normal", dtype=DT[dt]).cuda() \
+        if res_mode else None
+    d = A.ConvDesc(n, h, w, cin, cout, k, k, 1, k // 2, G.NHWC, DT[dt])
+    ws_bytes = A.acnn_conv2d_workspace_size(d)
+    gws = guarded_bytes(ws_bytes)
+    gy = Guarded((n, h, w, cout), TDT[dt])
+    gu = Guarded((n, 2 * h, 2 * w, cout), TDT[dt])
+    st = A.acnn_conv2d_fused_up2(d, xa, ca, xb, wt, b, None, r, res_mode, act, gy.t, gu.t,
+                                 None if gws is None else gws.t, ws_bytes)
+    assert st == 0, A.status_string(st)
+    gy.check(name + " y")
+    gu.check(name + " y_up")
+    if gws is not None:
+        gws.check(name + " workspace")
+    if xb is None:
+        y_ref = A.conv2d_fused(xa, wt, b, pad=k // 2, act=act, residual=r, res_mode=res_mode)
+    else:
+        y_ref = A.conv2d_fused_cat2(xa, xb, wt, b, pad=k // 2, act=act, residual=r,
+                                    res_mode=res_mode)
+    u_ref = A.resize2d(y_ref, A.RESIZE_NEAREST, 2 * h, 2 * w)
+    torch.cuda.synchronize()
+    assert_bitexact(gy.t, y_ref, name + " y")
+    assert_bitexact(gu.t, u_ref, name + " y_up")
+    x64 = to64(xa) if xb is None else O.concat(to64(xa), to64(xb))
+    ref = O.conv2d(x64, to64(wt), to64(b), pad=k // 2, act=act,
+                   residual=None if r is None else to64(r), res_mode=res_mode)
+    assert_parity(gy.t, ref, TDT[dt], name)
+
+
 def test_conv_fused_pool2_rejects():
     """Only 1x1/s1/p0 NHWC 16-bit convs with C_in >= 64 and an even output map."""
     X, W, Y, P = (torch.empty(4 << 20, dtype=torch.uint8, device="cuda") for _ in range(4))
