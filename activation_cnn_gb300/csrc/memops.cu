@@ -434,6 +434,58 @@ __global__ void __launch_bounds__(kThreads) resize_nchw_rows_kernel(
     *reinterpret_cast<Vec<To, V>*>(y + r * OW + ox0) = o;
 }
 
+// NCHW bilinear upsample by 4 or more (the frame stack's x8 of the flow map),
+// eight output rows per block: those rows read at most four source rows, so
+// each thread interpolates its V columns along x on those source rows once
+// (kept in registers) and every output is then one interpolation along y --
+// the same operations, in the same order, as resize_nchw_kernel
+// (mix(mix(v00, v10, fx), mix(v01, v11, fx), fy)), so the same bits.
+constexpr int kUpRows = 8, kUpSpan = 4;
+
+template <typename Ti, typename To, int V>
+__global__ void __launch_bounds__(kThreads) resize_nchw_up_kernel(
+    const Ti* __restrict__ x, To* __restrict__ y, int H, int W, int OH, int OW, float sy,
+    float sx) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+    const int groups = (OH + kUpRows - 1) / kUpRows;
+    const long long nc = blockIdx.x / groups;
+    const int oy0 = (blockIdx.x % groups) * kUpRows;
+    const int ox0 = (blockIdx.y * kThreads + threadIdx.x) * V;
+    if (ox0 >= OW) return;
+    const Ti* plane = x + nc * H * W;
+    const int a0 = bilinear_tap(oy0, sy, H).a;  // first source row of the group
+    // x-interpolated values of source rows a0 .. a0 + kUpSpan - 1 (clamped)
+    float xi[kUpSpan][V];
+    BilinearTap tx[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) tx[v] = bilinear_tap(ox0 + v, sx, W);
+#pragma unroll
+    for (int j = 0; j < kUpSpan; ++j) {
+        const Ti* row = plane + (long long)min(a0 + j, H - 1) * W;
+#pragma unroll
+        for (int v = 0; v < V; ++v) xi[j][v] = mixf(to_f32(row[tx[v].a]), to_f32(row[tx[v].b]), tx[v].f);
+    }
+#pragma unroll 1
+    for (int r = 0; r < kUpRows; ++r) {
+        const int oy = oy0 + r;
+        if (oy >= OH) break;
+        const BilinearTap ty = bilinear_tap(oy, sy, H);
+        const int ja = ty.a - a0, jb = ty.b - a0;  // in [0, kUpSpan) (checked on the host)
+        Vec<To, V> o;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            float top = xi[0][v], bot = xi[0][v];
+#pragma unroll
+            for (int j = 1; j < kUpSpan; ++j) {
+                if (ja == j) top = xi[j][v];
+                if (jb == j) bot = xi[j][v];
+            }
+            o.v[v] = from_f32<To>(mixf(top, bot, ty.f));
+        }
+        *reinterpret_cast<Vec<To, V>*>(y + (nc * OH + oy) * OW + ox0) = o;
+    }
+}
+
 // ----------------------------------------------------------------------------
 // concat: rtdetr_gpu.rs CONCAT_SRC, y = [a | b] along channels.  NHWC: per
 // pixel; NCHW: per image, the c_a planes of a then the c_b planes of b.  Both
@@ -953,7 +1005,14 @@ cudaError_t resize_typed(int mode, int n, int c, int h, int w, int oh, int ow, i
         constexpr int VO = 16 / sizeof(To);
         const long long rows = (long long)n * c * oh;
         const int chunks = (ow / VO + kThreads - 1) / kThreads;
-        if (ow % VO == 0 && rows <= 0x7fffffffLL && chunks <= 65535) {
+        const long long ublocks = (long long)n * c * ((oh + kUpRows - 1) / kUpRows);
+        // eight output rows read at most kUpSpan source rows when the height
+        // grows 4x or more: (8 - 1) / 4 + 2 = 3.75
+        if (mode == ACNN_RESIZE_BILINEAR && oh >= 4 * h && ow % VO == 0 && ublocks <= 0x7fffffffLL &&
+            chunks <= 65535) {
+            launch_pdl(resize_nchw_up_kernel<Ti, To, VO>, dim3((unsigned)ublocks, chunks), kThreads, 0,
+                       s, xt, yt, h, w, oh, ow, sy, sx);
+        } else if (ow % VO == 0 && rows <= 0x7fffffffLL && chunks <= 65535) {
             // whole 16-byte output vectors per row (rows start aligned)
             launch_pdl(resize_nchw_rows_kernel<Ti, To, VO>, dim3((unsigned)rows, chunks), kThreads, 0,
                        s, xt, yt, mode, h, w, oh, ow, sy, sx);
