@@ -44,7 +44,8 @@ EXPORTS = (
     "acnn_section_begin", "acnn_section_end", "acnn_section_launch", "acnn_section_destroy",
     "acnn_device_sm_count", "acnn_conv2d_fused_noalloc", "acnn_conv2d_plan",
     "acnn_conv2d_fused_cat2", "acnn_conv2d_force_plan", "acnn_conv2d_force_path",
-    "acnn_conv2d_fused_pool2", "acnn_conv2d_fused_up2",
+    "acnn_conv2d_fused_pool2", "acnn_conv2d_fused_up2", "acnn_deconv2d_workspace_size",
+    "acnn_deconv2d_ws",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # ACNN_NOALLOC_SCRATCH_BYTES in include/acnn.h
 
@@ -111,6 +112,9 @@ def lib() -> ctypes.CDLL:
         L.acnn_conv2d_plan.argtypes = [D, ctypes.c_size_t] + [ctypes.POINTER(_I)] * 3
         L.acnn_conv2d_force_plan.argtypes = [_I, _I, _I]
         L.acnn_conv2d_fused_pool2.argtypes = [D, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P]
+        L.acnn_deconv2d_workspace_size.argtypes = [D, _I]
+        L.acnn_deconv2d_workspace_size.restype = ctypes.c_size_t
+        L.acnn_deconv2d_ws.argtypes = [D, _P, _P, _P, _P, _I, _I, _P, _P, ctypes.c_size_t, _P]
         L.acnn_conv2d_fused_up2.argtypes = [D, _P, _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P,
                                             ctypes.c_size_t, _P]
         L.acnn_conv2d_force_path.argtypes = [_I, _I]
@@ -323,6 +327,17 @@ def acnn_conv2d_fused_up2(desc, x_a, c_a, x_b, w, bias, alpha, residual, res_mod
                                        _ptr(bias), _ptr(alpha), _ptr(residual), res_mode, act,
                                        _ptr(y), _ptr(y_up), _ptr(workspace), ws_bytes,
                                        _stream(stream))
+
+
+def acnn_deconv2d_workspace_size(desc, out_dtype) -> int:
+    return lib().acnn_deconv2d_workspace_size(ctypes.byref(desc), out_dtype)
+
+
+def acnn_deconv2d_ws(desc, x, w, bias, alpha, act, out_dtype, y, workspace, ws_bytes,
+                     stream=None) -> int:
+    return lib().acnn_deconv2d_ws(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(alpha),
+                                  act, out_dtype, _ptr(y), _ptr(workspace), ws_bytes,
+                                  _stream(stream))
 
 
 def conv_out_shape(desc: ConvDesc):

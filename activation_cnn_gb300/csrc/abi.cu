@@ -699,6 +699,101 @@ int acnn_deconv2d(const acnn_conv_desc* d, const void* x, const float* w, const 
                                      act, out_dtype, y, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+// The tensor-core form of the 4x4/s2/p1 deconv (a 3x3/s1/p1 conv to 4 c_out
+// channels, then a pixel shuffle): whether it serves d, and its workspace
+// [x staged NHWC (NCHW input only) | regrouped weights | bias | alpha | conv
+// output], each 256-byte aligned; 0 when it does not serve d.
+struct DeconvGemm {
+    int co4;
+    size_t x_stage, wg, bg, ag, ys, total;
+};
+DeconvGemm deconv_gemm_plan(const acnn_conv_desc* d, int out_dtype) {
+    DeconvGemm g{};
+    // fp16 only: the weights are rounded to the storage type, and bf16's 8-bit
+    // significand moves an output by more than one unit of its storage there
+    if (d->dtype != ACNN_F16 || out_dtype != d->dtype || d->c_in % 8 != 0) return g;
+    if (d->kh != 4 || d->kw != 4 || d->stride != 2 || d->pad != 1) return g;
+    const int co4 = (4 * d->c_out + 7) / 8 * 8;
+    const acnn_conv_desc d3{d->n, d->h, d->w, d->c_in, co4, 3, 3, 1, 1, ACNN_NHWC, d->dtype};
+    if (!tensor_path_ok(&d3, d->h, d->w)) return g;
+    const size_t es = elem_size(d->dtype);
+    g.co4 = co4;
+    g.x_stage = d->layout == ACNN_NCHW ? round256((size_t)d->n * d->h * d->w * d->c_in * es) : 0;
+    g.wg = round256((size_t)co4 * 9 * d->c_in * es);
+    g.bg = round256((size_t)co4 * 4);
+    g.ag = g.bg;
+    g.ys = round256((size_t)d->n * d->h * d->w * co4 * es);
+    g.total = g.x_stage + g.wg + g.bg + g.ag + g.ys;
+    return g;
+}
+}  // namespace
+
+size_t acnn_deconv2d_workspace_size(const acnn_conv_desc* d, int out_dtype) {
+    if (check_desc(d) != ACNN_OK || !valid_dtype(out_dtype)) return 0;
+    return deconv_gemm_plan(d, out_dtype).total;
+}
+
+int acnn_deconv2d_ws(const acnn_conv_desc* d, const void* x, const float* w, const float* bias,
+                     const float* alpha, int act, int out_dtype, void* y, void* workspace,
+                     size_t ws_bytes, acnn_stream_t stream) {
+    const DeconvGemm g = deconv_gemm_plan(d, out_dtype);
+    if (!workspace || g.total == 0 || ws_bytes < g.total)
+        return acnn_deconv2d(d, x, w, bias, alpha, act, out_dtype, y, stream);
+    // the same validation as the direct form, then the workspace
+    int st = check_desc(d);
+    if (st != ACNN_OK) return st;
+    if (act < ACNN_ACT_NONE || act > ACNN_ACT_PRELU || !valid_dtype(out_dtype))
+        return ACNN_ERR_BAD_ENUM;
+    if (!x || !w || !y) return ACNN_ERR_NULL_POINTER;
+    if (act == ACNN_ACT_PRELU && !alpha) return ACNN_ERR_NULL_POINTER;
+    const int oh = 2 * d->h, ow = 2 * d->w;
+    if ((long long)d->n * d->c_out * oh * ow > kIndexLimit ||
+        (long long)d->n * d->c_in * d->h * d->w > kIndexLimit)
+        return ACNN_ERR_TOO_LARGE;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || !aligned16(workspace) ||
+        (bias && !aligned16(bias)) || (alpha && !aligned16(alpha)))
+        return ACNN_ERR_MISALIGNED;
+    const size_t es = elem_size(d->dtype);
+    const size_t xb = (size_t)d->n * d->c_in * d->h * d->w * es;
+    const size_t wb = (size_t)d->c_in * d->c_out * 16 * 4;
+    const size_t yb = (size_t)d->n * d->c_out * oh * ow * es;
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, wb) || overlaps(workspace, ws_bytes, x, xb) ||
+        overlaps(workspace, ws_bytes, w, wb) || overlaps(workspace, ws_bytes, y, yb) ||
+        (bias && overlaps(workspace, ws_bytes, bias, d->c_out * 4)) ||
+        (alpha && overlaps(workspace, ws_bytes, alpha, d->c_out * 4)))
+        return ACNN_ERR_ALIAS;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* x_nhwc = g.x_stage ? ws : const_cast<void*>(x);
+    void* wg = ws + g.x_stage;
+    float* bg = reinterpret_cast<float*>(ws + g.x_stage + g.wg);
+    float* ag = reinterpret_cast<float*>(ws + g.x_stage + g.wg + g.bg);
+    void* ys = ws + g.x_stage + g.wg + g.bg + g.ag;
+    cudaError_t e = launch_deconv_gemm_weights(d->dtype, w, bias, act == ACNN_ACT_PRELU ? alpha : nullptr,
+                                               wg, bg, ag, d->c_in, d->c_out, g.co4, s);
+    if (e == cudaSuccess && g.x_stage)
+        e = launch_nchw_to_nhwc(d->n, d->c_in, d->h * d->w, 2, x, x_nhwc, s);
+    if (e != cudaSuccess) return ACNN_ERR_CUDA;
+    ConvArgs a{};
+    a.d = acnn_conv_desc{d->n, d->h, d->w, d->c_in, g.co4, 3, 3, 1, 1, ACNN_NHWC, d->dtype};
+    a.oh = d->h;
+    a.ow = d->w;
+    a.x = x_nhwc;
+    a.w = wg;
+    a.bias = bg;
+    a.alpha = act == ACNN_ACT_PRELU ? ag : nullptr;
+    a.residual = nullptr;
+    a.res_mode = ACNN_RES_NONE;
+    a.act = act;
+    a.y = ys;
+    a.out_layout = ACNN_NHWC;
+    st = launch_igemm_conv(a, s);
+    if (st != ACNN_OK) return st;
+    return status_of(launch_deconv_shuffle(d->dtype, ys, y, d->layout, d->n, d->h, d->w, d->c_out,
+                                           g.co4, s));
+}
+
 int acnn_frame_prep_quarter(int h, int w, const uint8_t* rgba0, const uint8_t* rgba1, float t,
                             int out_dtype, void* y, acnn_stream_t stream) {
     if (!valid_dtype(out_dtype)) return ACNN_ERR_BAD_ENUM;

@@ -167,6 +167,15 @@ cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, 
 // the packed weight operand [c_out, kp] alone (kp >= kh*kw*c_in, zero padded)
 cudaError_t launch_weight_pack(const acnn_conv_desc& d, int kp, const void* w, void* wp,
                                cudaStream_t s);
+// The 4x4/s2/p1 transposed conv on the tensor cores (memops.cu): its weights,
+// bias and PReLU alpha regrouped for a 3x3/s1/p1 conv of 4 co (rounded up to
+// co4) output channels, and the pixel shuffle of that conv's NHWC output into
+// the deconv's output (fp16/bf16)
+cudaError_t launch_deconv_gemm_weights(int dtype, const float* w, const float* bias,
+                                       const float* alpha, void* wg, float* bg, float* ag, int ci,
+                                       int co, int co4, cudaStream_t s);
+cudaError_t launch_deconv_shuffle(int dtype, const void* ys, void* y, int layout, int n, int h,
+                                  int w, int co, int co4, cudaStream_t s);
 // NCHW -> NHWC activation transpose and OIHW -> OHWI weight transpose (2-byte types)
 cudaError_t launch_nchw_to_nhwc(int n, int c, int hw, int elem_bytes, const void* x, void* y,
                                 cudaStream_t s);

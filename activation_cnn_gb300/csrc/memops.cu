@@ -487,6 +487,75 @@ __global__ void __launch_bounds__(kThreads) resize_nchw_up_kernel(
 }
 
 // ----------------------------------------------------------------------------
+// The 4x4/s2/p1 transposed conv as a 3x3/s1/p1 conv with four outputs per
+// output channel, one per output parity (py, px): output (2a + py, 2b + px)
+// of channel co takes input (a - 1 + dy, b - 1 + dx) through kernel tap
+// (ky, kx) = (py + 3 - 2 dy, px + 3 - 2 dx) when both lie in [0, 3] (rt.js
+// wgslDeconv's gather form, regrouped).  The conv's output channel
+// co * 4 + py * 2 + px then holds output pixel (2a + py, 2b + px) of co at
+// its pixel (a, b), and a pixel shuffle puts it in place.
+// Weights: w (fp32 [CI][CO][4][4]) -> wg ([CO4][3][3][CI], storage type, OHWI
+// for the NHWC conv), CO4 = 4 CO rounded up to 8 (extra channels zero); bias
+// and PReLU alpha repeated four times ([CO4] fp32, zero past 4 CO).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) deconv_gemm_weights_kernel(
+    const float* __restrict__ w, const float* __restrict__ bias, const float* __restrict__ alpha,
+    T* __restrict__ wg, float* __restrict__ bg, float* __restrict__ ag, int CI, int CO, int CO4) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+    const long long total = (long long)CO4 * 9 * CI;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int ci = (int)(i % CI);
+        const long long q = i / CI;
+        const int t = (int)(q % 9), o = (int)(q / 9);
+        const int dy = t / 3, dx = t % 3;
+        float v = 0.0f;
+        if (o < 4 * CO) {
+            const int co = o >> 2, py = (o >> 1) & 1, px = o & 1;
+            const int ky = py + 3 - 2 * dy, kx = px + 3 - 2 * dx;
+            if (ky >= 0 && ky < 4 && kx >= 0 && kx < 4)
+                v = w[(((long long)ci * CO + co) * 4 + ky) * 4 + kx];
+        }
+        wg[i] = from_f32<T>(v);
+    }
+    for (int o = blockIdx.x * blockDim.x + threadIdx.x; o < CO4; o += gridDim.x * blockDim.x) {
+        bg[o] = (bias && o < 4 * CO) ? bias[o >> 2] : 0.0f;
+        ag[o] = (alpha && o < 4 * CO) ? alpha[o >> 2] : 0.0f;
+    }
+}
+
+// Pixel shuffle: ys (NHWC [N][H][W][CO4]) -> y ([N][CO][2H][2W] or NHWC
+// [N][2H][2W][CO]): y(co, 2a + py, 2b + px) = ys(a, b, co * 4 + py * 2 + px).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) deconv_shuffle_kernel(
+    const T* __restrict__ ys, T* __restrict__ y, int layout, int N, int H, int W, int CO, int CO4) {
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+    const int OH = 2 * H, OW = 2 * W;
+    const long long total = (long long)N * CO * OH * OW;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        int n, co, oy, ox;
+        if (layout == ACNN_NCHW) {  // consecutive threads: consecutive x of one plane
+            ox = (int)(i % OW);
+            long long q = i / OW;
+            oy = (int)(q % OH);
+            q /= OH;
+            co = (int)(q % CO);
+            n = (int)(q / CO);
+        } else {  // consecutive threads: consecutive channels of one pixel
+            co = (int)(i % CO);
+            long long q = i / CO;
+            ox = (int)(q % OW);
+            q /= OW;
+            oy = (int)(q % OH);
+            n = (int)(q / OH);
+        }
+        const int a = oy >> 1, py = oy & 1, b = ox >> 1, px = ox & 1;
+        y[i] = ys[(((long long)n * H + a) * W + b) * CO4 + co * 4 + py * 2 + px];
+    }
+}
+
+// ----------------------------------------------------------------------------
 // concat: rtdetr_gpu.rs CONCAT_SRC, y = [a | b] along channels.  NHWC: per
 // pixel; NCHW: per image, the c_a planes of a then the c_b planes of b.  Both
 // reduce to copying runs of `ra` elements from a and `rb` from b into
@@ -1188,6 +1257,36 @@ cudaError_t launch_im2col_pack(const acnn_conv_desc& d, int oh, int ow, int kp, 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !w) return e;  // no w: the weights are prepacked
     return launch_weight_pack(d, kp, w, wp, s);
+}
+
+cudaError_t launch_deconv_gemm_weights(int dtype, const float* w, const float* bias,
+                                       const float* alpha, void* wg, float* bg, float* ag, int ci,
+                                       int co, int co4, cudaStream_t s) {
+    const long long work = (long long)co4 * 9 * ci;
+    if (dtype == ACNN_BF16)
+        launch_pdl(deconv_gemm_weights_kernel<__nv_bfloat16>,
+                   grid_occ(deconv_gemm_weights_kernel<__nv_bfloat16>, work, kThreads), kThreads, 0, s,
+                   w, bias, alpha, static_cast<__nv_bfloat16*>(wg), bg, ag, ci, co, co4);
+    else
+        launch_pdl(deconv_gemm_weights_kernel<__half>,
+                   grid_occ(deconv_gemm_weights_kernel<__half>, work, kThreads), kThreads, 0, s, w,
+                   bias, alpha, static_cast<__half*>(wg), bg, ag, ci, co, co4);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_deconv_shuffle(int dtype, const void* ys, void* y, int layout, int n, int h,
+                                  int w, int co, int co4, cudaStream_t s) {
+    const long long work = (long long)n * co * 4 * h * w;
+    if (dtype == ACNN_BF16)
+        launch_pdl(deconv_shuffle_kernel<__nv_bfloat16>,
+                   grid_occ(deconv_shuffle_kernel<__nv_bfloat16>, work, kThreads), kThreads, 0, s,
+                   static_cast<const __nv_bfloat16*>(ys), static_cast<__nv_bfloat16*>(y), layout, n, h,
+                   w, co, co4);
+    else
+        launch_pdl(deconv_shuffle_kernel<__half>, grid_occ(deconv_shuffle_kernel<__half>, work, kThreads),
+                   kThreads, 0, s, static_cast<const __half*>(ys), static_cast<__half*>(y), layout, n,
+                   h, w, co, co4);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_weight_pack(const acnn_conv_desc& d, int kp, const void* w, void* wp,

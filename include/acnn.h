@@ -317,6 +317,26 @@ int acnn_concat(int n, int h, int w, int c_a, int c_b, int layout, int dtype,
 int acnn_deconv2d(const acnn_conv_desc* d, const void* x, const float* w, const float* bias,
                   const float* alpha, int act, int out_dtype, void* y, acnn_stream_t stream);
 
+/* The deconv on the tensor cores, for fp16 with out_dtype fp16 and
+ * c_in % 8 == 0 (its weights are rounded to fp16): regrouped as a 3x3/s1/p1 conv to 4 c_out output
+ * channels (channel co * 4 + py * 2 + px of the conv's pixel (a, b) is the
+ * deconv's output (co, 2a + py, 2b + px): rt.js wgslDeconv's gather form,
+ * grouped by output parity), then a pixel shuffle.  The weights and bias are
+ * regrouped (and the weights rounded to the storage type) in the workspace on
+ * every call.
+ *   acnn_deconv2d_workspace_size(d, out_dtype)  bytes of workspace, 0 when
+ *                                  this form does not serve d;
+ *   acnn_deconv2d_ws(...)          acnn_deconv2d's arguments plus the
+ *                                  workspace (caller-owned device memory,
+ *                                  16-byte aligned, overlapping no argument);
+ *                                  with no or too small a workspace, or a
+ *                                  geometry this form does not serve, it is
+ *                                  acnn_deconv2d.  Same errors. */
+size_t acnn_deconv2d_workspace_size(const acnn_conv_desc* d, int out_dtype);
+int acnn_deconv2d_ws(const acnn_conv_desc* d, const void* x, const float* w, const float* bias,
+                     const float* alpha, int act, int out_dtype, void* y, void* workspace,
+                     size_t ws_bytes, acnn_stream_t stream);
+
 /* ---- frame prep ------------------------------------------------------------
  * rt.js wgslPrepQuarter: two h x w RGBA8 frames (bytes R,G,B,A per pixel,
  * device) -> y = [7, h/4, w/4] NCHW of out_dtype (device): the planes B, G, R

@@ -135,6 +135,25 @@ def test_conv_up2_rejects_before_launch(A):
     assert c(ok, None, U, act=9) == 7
 
 
+def test_deconv_tensor_core_workspace(A):
+    """The tensor-core deconv's workspace: for fp16/bf16 with out = in dtype and
+    c_in % 8 == 0 only (0 otherwise: the direct kernel serves)."""
+    def d(**kw):
+        return desc(A, **dict(dict(c_in=240, c_out=5, kh=4, kw=4, stride=2, pad=1, layout=1,
+                                   dtype=1, h=68, w=120), **kw))
+    es = 2
+    co4 = 24
+    want = (((68 * 120 * 240 * es + 255) // 256 * 256) + ((co4 * 9 * 240 * es + 255) // 256 * 256)
+            + 2 * 256 + ((68 * 120 * co4 * es + 255) // 256 * 256))
+    assert A.acnn_deconv2d_workspace_size(d(), 1) == want
+    assert A.acnn_deconv2d_workspace_size(d(layout=0), 1) == want - (68 * 120 * 240 * es + 255) // 256 * 256
+    assert A.acnn_deconv2d_workspace_size(d(), 0) == 0          # fp32 output
+    assert A.acnn_deconv2d_workspace_size(d(dtype=0), 0) == 0   # fp32 input
+    assert A.acnn_deconv2d_workspace_size(d(c_in=20), 1) == 0   # c_in % 8
+    assert A.acnn_deconv2d_workspace_size(d(dtype=2), 2) == 0   # bf16: the direct kernel
+    assert A.acnn_deconv2d_workspace_size(d(stride=1), 1) == 0
+
+
 def test_force_path_selects_the_tiny_kernel(A):
     """The tuning hook routes the 3/6/7-channel 3x3 convs to the direct kernel
     (and nothing else), and path 0 restores the router."""

@@ -624,6 +624,35 @@ def test_deconv(dt_in, dt_out, layout, shape):
     assert_parity(y, ref, TDT[dt_out])
 
 
+@pytest.mark.parametrize("dt", ["f16"])
+@pytest.mark.parametrize("layout", [G.NCHW, G.NHWC])
+@pytest.mark.parametrize("shape", [(2, 24, 5, 7, 9), (1, 240, 5, 68, 120), (1, 40, 20, 11, 70),
+                                   (3, 64, 3, 1, 1)])
+def test_deconv_tensor_core(dt, layout, shape):
+    """The 4x4/s2/p1 deconv regrouped as a 3x3 conv to 4 c_out channels on the
+    tensor cores, then a pixel shuffle (acnn_deconv2d_ws): within tolerance of the
+    oracle (whose weights stay fp32; here they are rounded to the storage type),
+    nothing written outside the output or the workspace; the PReLU path too."""
+    n, ci, co, h, w = shape
+    x = G.tensor(8, "dcx", G.activation_shape(layout, n, ci, h, w), "normal", dtype=DT[dt])
+    wt = G.deconv_weight(8, "dc", ci, co, 4)
+    b = G.conv_bias(8, "dc", co)
+    al = G.prelu_alpha(8, "dc", co)
+    d = A.ConvDesc(n, h, w, ci, co, 4, 4, 2, 1, layout, DT[dt])
+    ws_bytes = A.acnn_deconv2d_workspace_size(d, DT[dt])
+    assert ws_bytes > 0
+    gws = guarded_bytes(ws_bytes)
+    for act in (A.ACT_NONE, A.ACT_PRELU):
+        ref = O.deconv2d(to64(x), to64(wt), to64(b), layout=layout, act=act, alpha=to64(al))
+        g = Guarded(ref.shape, TDT[dt])
+        st = A.acnn_deconv2d_ws(d, x.cuda(), wt.cuda(), b.cuda(), al.cuda(), act, DT[dt], g.t,
+                                gws.t, ws_bytes)
+        assert st == 0, A.status_string(st)
+        g.check(f"deconv tc {shape} act{act}")
+        gws.check(f"deconv tc workspace {shape}")
+        assert_parity(g.t, ref, TDT[dt], f"deconv tc {dt} {shape} act{act}")
+
+
 # ---------------------------------------------------------------- frame prep
 @pytest.mark.parametrize("hw", [(16, 24), (68, 120)])
 @pytest.mark.parametrize("dt", ["f16", "f32"])
