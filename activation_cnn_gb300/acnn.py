@@ -45,7 +45,7 @@ EXPORTS = (
     "acnn_device_sm_count", "acnn_conv2d_fused_noalloc", "acnn_conv2d_plan",
     "acnn_conv2d_fused_cat2", "acnn_conv2d_force_plan", "acnn_conv2d_force_path",
     "acnn_conv2d_fused_pool2", "acnn_conv2d_fused_up2", "acnn_deconv2d_workspace_size",
-    "acnn_deconv2d_ws",
+    "acnn_deconv2d_ws", "acnn_conv2d_fused_prepacked_staged",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # ACNN_NOALLOC_SCRATCH_BYTES in include/acnn.h
 
@@ -112,6 +112,8 @@ def lib() -> ctypes.CDLL:
         L.acnn_conv2d_plan.argtypes = [D, ctypes.c_size_t] + [ctypes.POINTER(_I)] * 3
         L.acnn_conv2d_force_plan.argtypes = [_I, _I, _I]
         L.acnn_conv2d_fused_pool2.argtypes = [D, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P]
+        L.acnn_conv2d_fused_prepacked_staged.argtypes = [D, _P, _P, _P, _P, _P, _P, _I, _I, _P,
+                                                         _P, _P, ctypes.c_size_t, _P]
         L.acnn_deconv2d_workspace_size.argtypes = [D, _I]
         L.acnn_deconv2d_workspace_size.restype = ctypes.c_size_t
         L.acnn_deconv2d_ws.argtypes = [D, _P, _P, _P, _P, _I, _I, _P, _P, ctypes.c_size_t, _P]
@@ -327,6 +329,15 @@ def acnn_conv2d_fused_up2(desc, x_a, c_a, x_b, w, bias, alpha, residual, res_mod
                                        _ptr(bias), _ptr(alpha), _ptr(residual), res_mode, act,
                                        _ptr(y), _ptr(y_up), _ptr(workspace), ws_bytes,
                                        _stream(stream))
+
+
+def acnn_conv2d_fused_prepacked_staged(desc, x, x_nhwc, w_packed, bias, alpha, residual,
+                                       res_mode, act, y, y_nhwc, workspace, ws_bytes,
+                                       stream=None) -> int:
+    return lib().acnn_conv2d_fused_prepacked_staged(
+        ctypes.byref(desc), _ptr(x), _ptr(x_nhwc), _ptr(w_packed), _ptr(bias), _ptr(alpha),
+        _ptr(residual), res_mode, act, _ptr(y), _ptr(y_nhwc), _ptr(workspace), ws_bytes,
+        _stream(stream))
 
 
 def acnn_deconv2d_workspace_size(desc, out_dtype) -> int:

@@ -293,7 +293,8 @@ size_t prepacked_bytes(const acnn_conv_desc* d, const Route& r) {
 
 int conv_fused_impl(const acnn_conv_desc* d, const void* x, const void* w, bool prepacked,
                     const float* bias, const float* alpha, const void* residual, int res_mode,
-                    int act, void* y, void* workspace, size_t ws_bytes, acnn_stream_t stream) {
+                    int act, void* y, void* workspace, size_t ws_bytes, acnn_stream_t stream,
+                    const void* x_nhwc = nullptr, void* y_nhwc = nullptr) {
     int st = check_desc(d);
     if (st != ACNN_OK) return st;
     if (act < ACNN_ACT_NONE || act > ACNN_ACT_PRELU || res_mode < ACNN_RES_NONE ||
@@ -337,6 +338,18 @@ int conv_fused_impl(const acnn_conv_desc* d, const void* x, const void* w, bool 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     const Route r = route(d, oh, ow);
+    // NHWC copies (NCHW convs on the implicit-GEMM paths only): an input copy
+    // the caller staged already, an output copy to write beside y
+    const bool nchw_tc = d->layout == ACNN_NCHW && (r.path == 1 || r.path == 2);
+    if ((x_nhwc && !nchw_tc) || (y_nhwc && !(d->layout == ACNN_NCHW && r.path >= 1 && r.path <= 3)))
+        return ACNN_ERR_UNSUPPORTED;
+    if ((x_nhwc && !aligned16(x_nhwc)) || (y_nhwc && !aligned16(y_nhwc))) return ACNN_ERR_MISALIGNED;
+    if (y_nhwc && (overlaps(y_nhwc, yb, y, yb) || overlaps(y_nhwc, yb, x, xb) ||
+                   overlaps(y_nhwc, yb, w, wb) || (x_nhwc && overlaps(y_nhwc, yb, x_nhwc, xb)) ||
+                   (residual && res_mode != ACNN_RES_NONE && overlaps(y_nhwc, yb, residual, yb))))
+        return ACNN_ERR_ALIAS;
+    if (x_nhwc && overlaps(y, yb, x_nhwc, xb)) return ACNN_ERR_ALIAS;
+    a.y_nhwc = y_nhwc;
     if (r.path == 0) return status_of(launch_direct_conv(a, s));
     if (r.path == 4) return status_of(launch_tiny_conv(a, g_tiny_shuffle.load(), s));
 
@@ -344,13 +357,15 @@ int conv_fused_impl(const acnn_conv_desc* d, const void* x, const void* w, bool 
     // staged w with prepacked weights), then split-K partial sums (optional: a
     // smaller remainder selects fewer splits).
     const size_t stage_w = prepacked ? 0 : r.stage_w;
-    const size_t stage = r.stage_x + stage_w;
+    const size_t stage = (x_nhwc ? 0 : r.stage_x) + stage_w;
     if (!workspace) ws_bytes = 0;
     if (ws_bytes < stage) return ACNN_ERR_WORKSPACE;
     if (ws_bytes > 0 &&
         (overlaps(workspace, ws_bytes, y, yb) || overlaps(workspace, ws_bytes, x, xb) ||
          overlaps(workspace, ws_bytes, w, wb) ||
-         (a.residual && overlaps(workspace, ws_bytes, residual, yb))))
+         (a.residual && overlaps(workspace, ws_bytes, residual, yb)) ||
+         (x_nhwc && overlaps(workspace, ws_bytes, x_nhwc, xb)) ||
+         (y_nhwc && overlaps(workspace, ws_bytes, y_nhwc, yb))))
         return ACNN_ERR_ALIAS;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.ws_part = ws_bytes > stage ? ws + stage : nullptr;
@@ -369,16 +384,19 @@ int conv_fused_impl(const acnn_conv_desc* d, const void* x, const void* w, bool 
     }
     if (d->layout == ACNN_NHWC) return launch_igemm_conv(a, s);
 
-    // NCHW on the TMA paths: NHWC copy of x and OHWI copy of w, then the
-    // implicit GEMM writing NCHW directly.
-    e = launch_nchw_to_nhwc(d->n, d->c_in, d->h * d->w, 2, x, ws, s);
-    if (e != cudaSuccess) return ACNN_ERR_CUDA;
-    if (!prepacked) {
-        e = launch_nchw_to_nhwc(d->c_out, d->c_in, d->kh * d->kw, 2, w, ws + r.stage_x, s);
+    // NCHW on the TMA paths: NHWC copy of x (unless the caller has it) and
+    // OHWI copy of w, then the implicit GEMM writing NCHW directly.
+    const size_t xs = x_nhwc ? 0 : r.stage_x;
+    if (!x_nhwc) {
+        e = launch_nchw_to_nhwc(d->n, d->c_in, d->h * d->w, 2, x, ws, s);
         if (e != cudaSuccess) return ACNN_ERR_CUDA;
     }
-    a.x = ws;
-    a.w = prepacked ? w : ws + r.stage_x;
+    if (!prepacked) {
+        e = launch_nchw_to_nhwc(d->c_out, d->c_in, d->kh * d->kw, 2, w, ws + xs, s);
+        if (e != cudaSuccess) return ACNN_ERR_CUDA;
+    }
+    a.x = x_nhwc ? x_nhwc : ws;
+    a.w = prepacked ? w : ws + xs;
     a.d.layout = ACNN_NHWC;
     a.out_layout = ACNN_NCHW;
     return launch_igemm_conv(a, s);
@@ -399,6 +417,18 @@ int acnn_conv2d_fused_prepacked(const acnn_conv_desc* d, const void* x, const vo
                                 size_t ws_bytes, acnn_stream_t stream) {
     return conv_fused_impl(d, x, w_packed, true, bias, alpha, residual, res_mode, act, y,
                            workspace, ws_bytes, stream);
+}
+
+int acnn_conv2d_fused_prepacked_staged(const acnn_conv_desc* d, const void* x,
+                                       const void* x_nhwc, const void* w_packed,
+                                       const float* bias, const float* alpha,
+                                       const void* residual, int res_mode, int act, void* y,
+                                       void* y_nhwc, void* workspace, size_t ws_bytes,
+                                       acnn_stream_t stream) {
+    if (!d) return ACNN_ERR_NULL_POINTER;
+    if (d->layout != ACNN_NCHW && (x_nhwc || y_nhwc)) return ACNN_ERR_UNSUPPORTED;
+    return conv_fused_impl(d, x, w_packed, true, bias, alpha, residual, res_mode, act, y, workspace,
+                           ws_bytes, stream, x_nhwc, y_nhwc);
 }
 
 size_t acnn_conv2d_prepacked_size(const acnn_conv_desc* d) {

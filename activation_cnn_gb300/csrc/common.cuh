@@ -105,6 +105,11 @@ struct ConvArgs {
     // y2_up = 1: [n][2 oh][2 ow][c_out], the nearest 2x upsample of y
     void* y2 = nullptr;
     int y2_up = 0;
+    // NCHW convs on the tensor cores: an NHWC copy of x the caller already has
+    // (the staging transpose is then skipped), and an NHWC copy of y to write
+    // beside it (NULL: none)
+    const void* x_nhwc = nullptr;
+    void* y_nhwc = nullptr;
 };
 
 // Tile width and K split of the tensor-core conv for a geometry, given the

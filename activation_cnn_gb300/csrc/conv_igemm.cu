@@ -108,6 +108,7 @@ struct Params {
     void* y2;         // a_mode 3: NHWC [N][OH/2][OW/2][C_out], the 2x2/s2 average of y;
                       // y2_up: NHWC [N][2 OH][2 OW][C_out], the nearest 2x upsample of y
     int y2_up;
+    void* y_nhwc;     // NCHW output: also an NHWC copy of y (the next conv's staged input), or NULL
     int a_mode;       // 0: tiled A (1x1/s1/p0); 1: im2col A; 2: im2col A with halo rows;
                       // 3: tiled A in rectangular tiles (1x1/s1/p0, pooled second output)
     int c_split;      // channels [c_split, C_in) come from the second A map (0: none)
@@ -492,6 +493,21 @@ template <> __device__ __forceinline__ void unpack2<__half>(uint32_t u, float& l
     __half2 h = *reinterpret_cast<__half2*>(&u);
     lo = __low2float(h);
     hi = __high2float(h);
+}
+
+// NCHW epilogue: the lane's 32 output channels (values v, channels ch0 ..,
+// the first nj valid, nj a multiple of 8) of real pixel m also to the NHWC
+// copy, as 16-byte pieces (the same rounding as the NCHW stores).
+template <typename T>
+__device__ __forceinline__ void store_nhwc_row(const Params& p, int m, int ch0, const float (&v)[32],
+                                               int nj) {
+    T* dst = static_cast<T*>(p.y_nhwc) + (long long)m * p.C_out + ch0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        if (8 * k < nj)
+            *reinterpret_cast<uint4*>(dst + 8 * k) =
+                make_uint4(pack2<T>(v[8 * k], v[8 * k + 1]), pack2<T>(v[8 * k + 2], v[8 * k + 3]),
+                           pack2<T>(v[8 * k + 4], v[8 * k + 5]), pack2<T>(v[8 * k + 6], v[8 * k + 7]));
 }
 
 // Activation with the code fixed at compile time (no per-element branching).
@@ -1337,6 +1353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         v[j] = o;
                     }
                     if (has_res) __syncwarp();  // every lane has its residual before the slot is reused
+                    if (p.y_nhwc) store_nhwc_row<T>(p, r0 + lane, n0 + c, v, nj);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const T o = from_f32<T>(v[j]);
@@ -1364,8 +1381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float x = v[j] + sP[ch];
                     const float al = prelu ? sP[cpad + ch] : 0.f;
                     const float o = pre ? apply_act(p.act, x + rv, al) : apply_act(p.act, x, al) + rv;
+                    v[j] = o;
                     if (valid) y[idx] = from_f32<T>(o);
                 }
+                if (p.y_nhwc && valid) store_nhwc_row<T>(p, mr, n0 + c, v, nj);
             }
             tc_fence_before();
             __syncwarp();
@@ -1745,6 +1764,7 @@ int launch_igemm_conv(const ConvArgs& a, cudaStream_t s) {
         prm.rty_magic = ~0ull / (unsigned long long)rty + 1ull;
         prm.y2 = a.y2;
         prm.y2_up = a.y2_up;
+        prm.y_nhwc = a.out_layout == ACNN_NCHW ? a.y_nhwc : nullptr;
         prm.c_split = cat ? a.c_split : 0;
         prm.out_layout = a.out_layout;
         prm.act = a.act;

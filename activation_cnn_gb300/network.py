@@ -150,7 +150,11 @@ class Builder:
         self.net.tensors[name] = t
         return t
 
-    def conv(self, src, spec: ConvSpec, residual=None, out=None, pool2=None, up2=None):
+    def conv(self, src, spec: ConvSpec, residual=None, out=None, pool2=None, up2=None,
+             nhwc_copy=False):
+        """nhwc_copy (NCHW convs on the tensor cores): also write an NHWC copy of
+        the output (tensor f"{name}.nhwc"); a conv whose input has such a copy
+        reads it instead of staging the input itself."""
         net = self.net
         if pool2:
             return self._conv_pool2(src, spec, residual, pool2)
@@ -184,19 +188,38 @@ class Builder:
         net.conv_inputs[spec.name] = src
         if residual:
             net.conv_residuals[spec.name] = residual
-        call = A.acnn_conv2d_fused_prepacked if staged else A.acnn_conv2d_fused
+        # NHWC copies along a chain of NCHW tensor-core convs: the input's copy
+        # (written by the conv that produced it) spares this conv its staging
+        # transpose; this conv writes its own output's copy when asked to
+        tc_nchw = net.layout == G.NCHW and path in (1, 2)
+        x_copy = net.tensors.get(src + ".nhwc") if tc_nchw else None
+        y_copy = None
+        if nhwc_copy and net.layout == G.NCHW and path in (1, 2, 3):
+            y_copy = torch.empty((net.batch, spec.oh, spec.ow, spec.c_out), dtype=y.dtype,
+                                 device=self.device)
+            net.tensors[(out or spec.name) + ".nhwc"] = y_copy
+        if x_copy is not None or y_copy is not None:
+            def fn(stream, d=d, x=x, wd=wd, bd=bd, ald=ald, res=res, y=y, ws=ws, res_mode=res_mode,
+                   x_copy=x_copy, y_copy=y_copy):
+                A.check(A.acnn_conv2d_fused_prepacked_staged(d, x, x_copy, wd, bd, ald, res,
+                                                             res_mode, spec.act, y, y_copy, ws,
+                                                             ws_bytes, stream), spec.name)
+        else:
+            call = A.acnn_conv2d_fused_prepacked if staged else A.acnn_conv2d_fused
 
-        def fn(stream, d=d, x=x, wd=wd, bd=bd, ald=ald, res=res, y=y, ws=ws, res_mode=res_mode):
-            A.check(call(d, x, wd, bd, ald, res, res_mode, spec.act, y, ws, ws_bytes, stream),
-                    spec.name)
+            def fn(stream, d=d, x=x, wd=wd, bd=bd, ald=ald, res=res, y=y, ws=ws, res_mode=res_mode):
+                A.check(call(d, x, wd, bd, ald, res, res_mode, spec.act, y, ws, ws_bytes, stream),
+                        spec.name)
 
         n = net.batch
         byts = (x.numel() + w.numel() + y.numel() + (y.numel() if res is not None else 0)) * \
             self.es + 4 * spec.c_out
         # kernels per call: the conv, plus the activation staging (NCHW -> NHWC
-        # copy or im2col pack) of a staged conv
+        # copy or im2col pack) of a staged conv unless its input's copy exists
+        if y_copy is not None:
+            byts += y.numel() * self.es
         net.ops.append(Op("conv", self.section, fn, _conv_flops(n, spec), byts, spec.name, spec,
-                          launches=2 if staged else 1))
+                          launches=2 if staged and x_copy is None else 1))
         return out or spec.name
 
     def _conv_pool2(self, src, spec: ConvSpec, residual, pool_name):
@@ -564,16 +587,19 @@ def frame_net(device="cuda", h=1088, w=1920, c1=120, c2=240, t=0.5, flow_out=Fal
     touched = 2 * (2 * qh) * w * 4  # two source rows per output row, both frames
     net.ops.append(Op("prep", "frame", prep, 0.0, touched + xq.numel() * 2, "prep"))
     P = A.ACT_PRELU
-    a = b.conv("xq", ConvSpec("conv0a", 7, c1, 3, 2, 1, P, qh, qw))
+    # each conv of the chain writes an NHWC copy of its output for the next
+    # (rt.js keeps one layout throughout; here the NCHW maps stay as stored
+    # and the tensor-core convs read the copies instead of staging)
+    a = b.conv("xq", ConvSpec("conv0a", 7, c1, 3, 2, 1, P, qh, qw), nhwc_copy=True)
     s0 = ConvSpec("conv0b", c1, c2, 3, 2, 1, P, qh // 2, qw // 2)
-    cur = b.conv(a, s0)
+    cur = b.conv(a, s0, nhwc_copy=True)
     skip = cur
     hh, ww = s0.oh, s0.ow
     for i in range(8):
         last = i == 7
         spec = ConvSpec(f"convblock.{i}", c2, c2, 3, 1, 1, P, hh, ww,
                         res_mode=A.RES_ACT_THEN_ADD if last else A.RES_NONE)
-        cur = b.conv(cur, spec, residual=skip if last else None)
+        cur = b.conv(cur, spec, residual=skip if last else None, nhwc_copy=not last)
     wdc = G.deconv_weight(seed, "lastconv", c2, 5, 4)
     bdc = G.conv_bias(seed, "lastconv", 5)
     net.params["lastconv"] = (wdc, bdc, None)
@@ -641,13 +667,14 @@ def frame_tfact_net(device="cuda", h=1088, w=1920, c1=120, c2=240, ts=(0.25, 0.5
     touched = 2 * (2 * qh) * w * 4
     net.ops.append(Op("prep", "frame", prep, 0.0, touched + xq.numel() * 2, "prep"))
     P = A.ACT_PRELU
-    a = b.conv("xq6", ConvSpec("conv0a", 6, c1, 3, 2, 1, P, qh, qw))
+    a = b.conv("xq6", ConvSpec("conv0a", 6, c1, 3, 2, 1, P, qh, qw), nhwc_copy=True)
     s0 = ConvSpec("conv0b", c1, c2, 3, 2, 1, P, qh // 2, qw // 2)
-    feat0 = b.conv(a, s0)
+    feat0 = b.conv(a, s0, nhwc_copy=True)
     hh, ww = s0.oh, s0.ow
     cur = feat0
     for i in range(6):
-        cur = b.conv(cur, ConvSpec(f"convblock.{i}", c2, c2, 3, 1, 1, P, hh, ww))
+        cur = b.conv(cur, ConvSpec(f"convblock.{i}", c2, c2, 3, 1, 1, P, hh, ww),
+                     nhwc_copy=i < 5)  # the trunk's last map feeds FiLM (NCHW)
     trunk = net.tensors[cur]
     fw = [t.to(device) for t in G.film_mlp(seed, "film", c2, hn)]
     net.params["film"] = G.film_mlp(seed, "film", c2, hn)
@@ -672,7 +699,7 @@ def frame_tfact_net(device="cuda", h=1088, w=1920, c1=120, c2=240, ts=(0.25, 0.5
         net.ops.append(Op("film", "frame", film, 2.0 * c2 * hh * ww + 4.0 * c2 * hn,
                           2 * trunk.numel() * 2, "film" + sfx))
         cur = b.conv("film" + sfx, ConvSpec("convblock.6" + sfx, c2, c2, 3, 1, 1, P, hh, ww,
-                                            param="convblock.6"))
+                                            param="convblock.6"), nhwc_copy=True)
         cur = b.conv(cur, ConvSpec("convblock.7" + sfx, c2, c2, 3, 1, 1, P, hh, ww,
                                    res_mode=A.RES_ACT_THEN_ADD, param="convblock.7"),
                      residual=feat0)
@@ -697,8 +724,9 @@ def frame_tfact_net(device="cuda", h=1088, w=1920, c1=120, c2=240, ts=(0.25, 0.5
                           tmp8.numel() * 2 + 2 * (h * w * 4) // 2 + rin.numel() * 2,
                           "refine_prep" + sfx))
         r = b.conv("rin" + sfx, ConvSpec("refine.c0" + sfx, 11, rc, 3, 1, 1, P, qh, qw,
-                                         param="refine.c0"))
-        r = b.conv(r, ConvSpec("refine.c1" + sfx, rc, rc, 3, 1, 1, P, qh, qw, param="refine.c1"))
+                                         param="refine.c0"), nhwc_copy=True)
+        r = b.conv(r, ConvSpec("refine.c1" + sfx, rc, rc, 3, 1, 1, P, qh, qw, param="refine.c1"),
+                   nhwc_copy=True)
         r = b.conv(r, ConvSpec("refine.c2" + sfx, rc, rc, 3, 1, 1, P, qh, qw, param="refine.c2"))
         rx = net.tensors[r]
         rres = b.buffer("rres" + sfx, 3, qh, qw, dtype=G.F32)

@@ -210,6 +210,26 @@ int acnn_conv2d_fused_prepacked(const acnn_conv_desc* d, const void* x, const vo
                                 int res_mode, int act, void* y, void* workspace,
                                 size_t ws_bytes, acnn_stream_t stream);
 
+/* acnn_conv2d_fused_prepacked for an NCHW conv on the implicit-GEMM paths
+ * (acnn_conv2d_path 1 or 2; y_nhwc also on path 3), with NHWC copies of its
+ * activations, so that a chain of NCHW convs (rt.js run()'s conv stack) stages
+ * each map once instead of per conv:
+ *   x_nhwc  the input as NHWC [n][h][w][c_in] (device, 16-byte aligned), or
+ *           NULL: staged from x in the workspace as acnn_conv2d_fused does.
+ *           With x_nhwc the workspace needs no staging part (split-K sums only).
+ *   y_nhwc  NHWC [n][oh][ow][c_out] (device, 16-byte aligned): the epilogue
+ *           also writes y there -- the same values, bit for bit -- for the next
+ *           conv's x_nhwc; NULL: none.
+ * Neither may overlap another argument.  Returns ACNN_ERR_UNSUPPORTED when
+ * d is NHWC or the path does not take the copies, otherwise the errors of
+ * acnn_conv2d_fused_prepacked. */
+int acnn_conv2d_fused_prepacked_staged(const acnn_conv_desc* d, const void* x,
+                                       const void* x_nhwc, const void* w_packed,
+                                       const float* bias, const float* alpha,
+                                       const void* residual, int res_mode, int act, void* y,
+                                       void* y_nhwc, void* workspace, size_t ws_bytes,
+                                       acnn_stream_t stream);
+
 /* ---- conv2d_fused without caller workspace ----------------------------------
  * No counterpart on the pages: an addition for callers that cannot allocate
  * device memory where they run a conv -- e.g. a plugin inside a framework

@@ -212,6 +212,63 @@ def test_conv_tiny_prepacked_equals_plain(layout, tiny_path):
     assert torch.equal(y, y2)
 
 
+@pytest.mark.parametrize("case", [(1, 17, 30, 120, 240, 2, A.RES_NONE, 3),
+                                  (1, 9, 15, 240, 240, 1, A.RES_ACT_THEN_ADD, 3),
+                                  (2, 8, 8, 64, 32, 1, A.RES_NONE, 3),
+                                  (1, 34, 60, 7, 120, 2, A.RES_NONE, 3),      # packed path
+                                  (1, 13, 21, 96, 64, 1, A.RES_ADD_THEN_ACT, 1)])
+def test_conv_nchw_staged_copies(case):
+    """NCHW conv with an NHWC copy of its input supplied and/or of its output
+    written (acnn_conv2d_fused_prepacked_staged): y bit-identical to the plain
+    prepacked call, the output copy equal to y in NHWC, nothing written outside
+    either; the input copy spares the staging (a workspace without it works)."""
+    n, h, w, cin, cout, s_, res_mode, k = case
+    dt = "f16"
+    seed = 17
+    x = G.tensor(seed, "stc.x", (n, cin, h, w), "normal", dtype=DT[dt]).cuda()
+    wt = G.conv_weight(seed, "stc", cout, cin, k, k, G.NCHW, DT[dt]).cuda()
+    b = G.conv_bias(seed, "stc", cout).cuda()
+    al = G.prelu_alpha(seed, "stc", cout).cuda()
+    p_ = k // 2
+    d = A.conv_desc(x, cout, k, k, s_, p_, G.NCHW)
+    oh, ow = (h + 2 * p_ - k) // s_ + 1, (w + 2 * p_ - k) // s_ + 1
+    r = G.tensor(seed, "stc.r", (n, cout, oh, ow), "normal", dtype=DT[dt]).cuda() if res_mode else None
+    wp = A.conv2d_prepack(d, wt)
+    wsb = A.acnn_conv2d_prepacked_workspace_size(d)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    y_ref = torch.empty((n, cout, oh, ow), dtype=torch.float16, device="cuda")
+    A.check(A.acnn_conv2d_fused_prepacked(d, x, wp, b, al, r, res_mode, A.ACT_PRELU, y_ref, ws,
+                                          wsb, None), "plain")
+    path = A.acnn_conv2d_path(d)
+    x_copy = x.permute(0, 2, 3, 1).contiguous() if path in (1, 2) else None
+    gy = Guarded((n, cout, oh, ow), torch.float16)
+    gc = Guarded((n, oh, ow, cout), torch.float16)
+    # with the input copy the staging part of the workspace is not needed
+    st = A.acnn_conv2d_fused_prepacked_staged(d, x, x_copy, wp, b, al, r, res_mode, A.ACT_PRELU,
+                                              gy.t, gc.t, ws if x_copy is None else None,
+                                              wsb if x_copy is None else 0)
+    assert st == 0, A.status_string(st)
+    gy.check("staged y")
+    gc.check("staged y copy")
+    torch.cuda.synchronize()
+    assert_bitexact(gy.t, y_ref, f"staged y {case}")
+    assert_bitexact(gc.t, y_ref.permute(0, 2, 3, 1).contiguous(), f"staged copy {case}")
+
+
+def test_conv_staged_copies_rejected():
+    """Copies only for NCHW convs on the tensor-core paths (input copy: paths 1-2)."""
+    X, W, Y, C = (torch.empty(1 << 20, dtype=torch.uint8, device="cuda") for _ in range(4))
+    nhwc = A.ConvDesc(1, 8, 8, 64, 64, 3, 3, 1, 1, G.NHWC, G.F16)
+    assert A.acnn_conv2d_fused_prepacked_staged(nhwc, X, C, W, None, None, None, 0, 0, Y, None,
+                                                None, 0) == 3
+    f32 = A.ConvDesc(1, 8, 8, 16, 32, 3, 3, 1, 1, G.NCHW, G.F32)
+    assert A.acnn_conv2d_fused_prepacked_staged(f32, X, None, W, None, None, None, 0, 0, Y, C,
+                                                None, 0) == 3
+    packed = A.ConvDesc(1, 8, 8, 7, 64, 3, 3, 1, 1, G.NCHW, G.F16)
+    assert A.acnn_conv2d_fused_prepacked_staged(packed, X, C, W, None, None, None, 0, 0, Y, None,
+                                                None, 0) == 3
+
+
 def test_conv_tensor_no_bias():
     y, ref = conv_case("nobias", 1, 9, 9, 64, 64, 1, 1, 0, "f16", bias=False)
     assert_parity(y, ref, torch.float16)
