@@ -272,6 +272,33 @@ def test_backbone_full_size():
         assert_parity(T[pooled], O.pool2d(to64(T[src]), O.AVG, 2, 2, 0), torch.bfloat16, pooled)
 
 
+def test_backbone_full_size_replays_are_bitwise_identical():
+    """Two replays of the 8x640x640 graphs give the same bits in every map the
+    step writes: no kernel depends on timing or arrival order (split-K sums its
+    partial tiles in split order, every other output has one writer)."""
+    net = N.backbone_net()
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        net.run_eager(s)
+    s.synchronize()
+    net.capture(s)
+    names = [n for n, t in net.tensors.items() if t is not None and not n.endswith(".ws")
+             and n not in net.inputs]
+    snaps = []
+    for _ in range(2):
+        for n in names:
+            net.tensors[n].fill_(float("nan")) if net.tensors[n].is_floating_point() else None
+        torch.cuda.synchronize()
+        net.replay(s)
+        s.synchronize()
+        snaps.append({n: net.tensors[n].clone() for n in names})
+    net.release()
+    for n in names:
+        assert torch.equal(snaps[0][n], snaps[1][n]), n
+    assert A.acnn_last_device_status() == 0
+
+
 def test_backbone_csp_full_size():
     """The CSP-neck variant at 8x640x640: end to end against the oracle, and its
     92 convs teacher-forced on sampled pixels."""
