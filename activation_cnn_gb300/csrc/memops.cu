@@ -899,17 +899,33 @@ __global__ void __launch_bounds__(kThreads) im2col_pack_kernel(
     __syncthreads();
     const int KG = Kp / 8;
     uint16_t* out = a + ((long long)(n * OH + oy) * OW + ox0) * Kp;
-    for (int j = threadIdx.x; j < np * KG; j += blockDim.x) {
-        const int px = j / KG, g = j - px * KG;
-        const uint16_t* src = st + px * S * C;
-        const int* t8 = tab + g * 8;
-        Vec<uint16_t, 8> v;
+    if (blockDim.x % KG == 0) {
+        // a thread's k-group g is the same on every iteration: its eight
+        // staged offsets are read from the table once
+        const int g = threadIdx.x % KG;
+        int o8[8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            const int o = t8[jj];
-            v.v[jj] = o >= 0 ? src[o] : (uint16_t)0;
+        for (int jj = 0; jj < 8; ++jj) o8[jj] = tab[g * 8 + jj];
+        for (int px = threadIdx.x / KG; px < np; px += blockDim.x / KG) {
+            const uint16_t* src = st + px * S * C;
+            Vec<uint16_t, 8> v;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) v.v[jj] = o8[jj] >= 0 ? src[o8[jj]] : (uint16_t)0;
+            *reinterpret_cast<Vec<uint16_t, 8>*>(out + (long long)px * Kp + g * 8) = v;
         }
-        *reinterpret_cast<Vec<uint16_t, 8>*>(out + (long long)px * Kp + g * 8) = v;
+    } else {
+        for (int j = threadIdx.x; j < np * KG; j += blockDim.x) {
+            const int px = j / KG, g = j - px * KG;
+            const uint16_t* src = st + px * S * C;
+            const int* t8 = tab + g * 8;
+            Vec<uint16_t, 8> v;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int o = t8[jj];
+                v.v[jj] = o >= 0 ? src[o] : (uint16_t)0;
+            }
+            *reinterpret_cast<Vec<uint16_t, 8>*>(out + (long long)px * Kp + g * 8) = v;
+        }
     }
 }
 
