@@ -563,8 +563,12 @@ def run_ours(args, rank, world, local_rank):
     # per-op times each op's share of its section.
     pk = peaks()
     nrep = max(3, min(args.steps, 10))
-    rows = apportion(time_ops(net, stream, nrep, flush), time_sections(net, stream, nrep, flush),
-                     total / args.steps)
+    sec_t = time_sections(net, stream, nrep, flush)
+    rows = apportion(time_ops(net, stream, nrep, flush), sec_t, total / args.steps)
+    # each section's share of the measured step (sections replayed alone after
+    # an L2 flush give the shares)
+    sec_tot = sum(sec_t.values())
+    sections_us = {k: round(1e6 * (total / args.steps) * v / sec_tot, 1) for k, v in sec_t.items()}
     ig = [r for r in rows if r["kind"] == "conv" and r["path"] in (1, 2)]
     ig_flops = sum(r["flops"] for r in ig)
     ig_t = sum(r["t"] for r in ig)
@@ -613,7 +617,7 @@ def run_ours(args, rank, world, local_rank):
         "conv_tflops": round(conv_tflops, 2),
         "conv_frac_bf16_peak": round(conv_tflops / pk["bf16_burst"], 4),
         "conv_gflop_per_step": round(net.conv_flops() / 1e9, 2),
-        "roofline": roofline, "e2e": e2e,
+        "roofline": roofline, "e2e": e2e, "sections_us": sections_us,
         "gpu_launches": launches_per_step(net) * args.steps,
         "clocks": clk, "wall_s_timed": round(t_wall, 3),
     }
