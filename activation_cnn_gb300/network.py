@@ -63,6 +63,11 @@ class Op:
     label: str = ""
     spec: object = None
     launches: int = 1        # kernels one call launches (non-conv ops)
+    # Parallel branch: a `side` op runs on the net's side stream (forked from
+    # the main stream at the first side op of a section); a `join` op waits on
+    # the main stream for every side op before it.  A section ends joined.
+    side: bool = False
+    join: bool = False
 
 
 @dataclass
@@ -87,11 +92,50 @@ class Net:
     def sections(self):
         return list(self.order)
 
+    def side_stream(self, device):
+        """The stream side ops run on (created once per net)."""
+        if getattr(self, "_side", None) is None:
+            self._side = torch.cuda.Stream(device=device)
+        return self._side
+
+    def enqueue(self, stream, section=None, hook=None):
+        """Enqueue the ops (of one section, or all) on `stream`, side ops on the
+        side stream between a fork and a join (events: under stream capture they
+        become parallel branches of the section's graph).  hook(op, stream, when)
+        runs before ("pre") and after ("post") each op on the stream it uses."""
+        side = None
+        pending = False  # side work not yet joined
+        for op in self.ops:
+            if section is not None and op.section != section:
+                continue
+            if op.join and pending:
+                ev = torch.cuda.Event()
+                ev.record(side)
+                stream.wait_event(ev)
+                pending = False
+            target = stream
+            if op.side:
+                if side is None:
+                    side = self.side_stream(stream.device)
+                if not pending:
+                    ev = torch.cuda.Event()
+                    ev.record(stream)
+                    side.wait_event(ev)
+                    pending = True
+                target = side
+            if hook:
+                hook(op, target, "pre")
+            op.fn(target)
+            if hook:
+                hook(op, target, "post")
+        if pending:
+            ev = torch.cuda.Event()
+            ev.record(side)
+            stream.wait_event(ev)
+
     def run_eager(self, stream=None, section=None):
         s = stream if stream is not None else torch.cuda.current_stream()
-        for op in self.ops:
-            if section is None or op.section == section:
-                op.fn(s)
+        self.enqueue(s, section)
 
     def capture(self, stream):
         """Record one CUDA graph per section on `stream` (ops must have run once)."""
@@ -136,6 +180,20 @@ class Builder:
         self.device = device
         self.section = "main"
         self.es = 4 if net.dtype == G.F32 else 2
+
+    def side(self):
+        """Ops appended inside `with b.side():` run on the net's side stream."""
+        b = self
+
+        class _Side:
+            def __enter__(self_):
+                self_.start = len(b.net.ops)
+
+            def __exit__(self_, *exc):
+                for op in b.net.ops[self_.start:]:
+                    op.side = True
+                return False
+        return _Side()
 
     def set_section(self, name):
         self.section = name
@@ -438,18 +496,24 @@ def bottleneck(b: Builder, src, name, c_in, width, h, w, stride, shortcut, poole
     c2 = ConvSpec(f"{name}.conv2", mid, mid, 3, stride, 1, A.ACT_RELU, h, w)
     c3 = ConvSpec(f"{name}.conv3", mid, width, 1, 1, 0, A.ACT_RELU, c2.oh, c2.ow,
                   res_mode=A.RES_ADD_THEN_ACT)
+    # the shortcut branch runs beside conv1 -> conv2 (a parallel branch of the
+    # section's graph: these layers leave SMs idle), joined before conv3
     if shortcut == "identity":
         res = src
-    elif shortcut == "conv":
-        res = b.conv(src, ConvSpec(f"{name}.short", c_in, width, 1, 1, 0, A.ACT_NONE, h, w))
     else:
-        if pooled is None:
-            pooled = b.pool(src, f"{name}.pool", A.POOL_AVG, 2, 2, 0, c_in, h, w)
-        res = b.conv(pooled, ConvSpec(f"{name}.short", c_in, width, 1, 1, 0, A.ACT_NONE,
-                                      h // 2, w // 2))
+        with b.side():
+            if shortcut == "conv":
+                res = b.conv(src, ConvSpec(f"{name}.short", c_in, width, 1, 1, 0, A.ACT_NONE,
+                                           h, w))
+            else:
+                if pooled is None:
+                    pooled = b.pool(src, f"{name}.pool", A.POOL_AVG, 2, 2, 0, c_in, h, w)
+                res = b.conv(pooled, ConvSpec(f"{name}.short", c_in, width, 1, 1, 0,
+                                              A.ACT_NONE, h // 2, w // 2))
     t = b.conv(src, c1)
     t = b.conv(t, c2)
     out = b.conv(t, c3, residual=res, pool2=f"{name}.pooled" if pool_out else None)
+    b.net.ops[-1].join = True
     return out, c2.oh, c2.ow
 
 
@@ -531,8 +595,11 @@ def backbone_net(device="cuda", n=8, h=640, w=640, neck="fusion") -> Net:
     b.set_section("neck")
     (c3, h3, w3, ch3), (c4, h4, w4, ch4), (c5, h5, w5, ch5) = feats[1], feats[2], feats[3]
     S = A.ACT_SILU
-    lat3 = b.conv(c3, ConvSpec("neck.lat3", ch3, 256, 1, 1, 0, S, h3, w3))
-    lat4 = b.conv(c4, ConvSpec("neck.lat4", ch4, 256, 1, 1, 0, S, h4, w4))
+    # lat3 and lat4 run beside lat5 (parallel branch), joined before the first
+    # fusion conv that reads them
+    with b.side():
+        lat3 = b.conv(c3, ConvSpec("neck.lat3", ch3, 256, 1, 1, 0, S, h3, w3))
+        lat4 = b.conv(c4, ConvSpec("neck.lat4", ch4, 256, 1, 1, 0, S, h4, w4))
 
     def fuse(src_a, src_b, name, hh, ww, up2=None):
         if neck == "csp":
@@ -545,13 +612,16 @@ def backbone_net(device="cuda", n=8, h=640, w=640, neck="fusion") -> Net:
     if fold:
         f5 = b.conv(c5, ConvSpec("neck.lat5", ch5, 256, 1, 1, 0, S, h5, w5), up2="neck.up5")
         up5 = "neck.up5"
+        first = len(net.ops)
         f4 = fuse(up5, lat4, "neck.fpn4", h4, w4, up2="neck.up4")
         up4 = "neck.up4"
     else:
         f5 = b.conv(c5, ConvSpec("neck.lat5", ch5, 256, 1, 1, 0, S, h5, w5))
         up5 = b.resize(f5, "neck.up5", A.RESIZE_NEAREST, 256, h5, w5, h4, w4)
+        first = len(net.ops)
         f4 = fuse(up5, lat4, "neck.fpn4", h4, w4)
         up4 = b.resize(f4, "neck.up4", A.RESIZE_NEAREST, 256, h4, w4, h3, w3)
+    net.ops[first].join = True
     f3 = fuse(up4, lat3, "neck.fpn3", h3, w3)
     d3 = b.conv(f3, ConvSpec("neck.down3", 256, 256, 3, 2, 1, S, h3, w3))
     n4 = fuse(d3, f4, "neck.pan4", h4, w4)
