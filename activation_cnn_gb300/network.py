@@ -63,10 +63,11 @@ class Op:
     label: str = ""
     spec: object = None
     launches: int = 1        # kernels one call launches (non-conv ops)
-    # Parallel branch: a `side` op runs on the net's side stream (forked from
-    # the main stream at the first side op of a section); a `join` op waits on
-    # the main stream for every side op before it.  A section ends joined.
-    side: bool = False
+    # Parallel branch: an op with side = k > 0 runs on the net's side stream k
+    # (forked from the main stream at the first such op of a section); a `join`
+    # op waits on the main stream for every side op before it.  A section ends
+    # joined.
+    side: int = 0
     join: bool = False
 
 
@@ -92,46 +93,48 @@ class Net:
     def sections(self):
         return list(self.order)
 
-    def side_stream(self, device):
-        """The stream side ops run on (created once per net)."""
-        if getattr(self, "_side", None) is None:
-            self._side = torch.cuda.Stream(device=device)
-        return self._side
+    def side_stream(self, device, k=1):
+        """Side stream k (created once per net)."""
+        if getattr(self, "_sides", None) is None:
+            self._sides = {}
+        if k not in self._sides:
+            self._sides[k] = torch.cuda.Stream(device=device)
+        return self._sides[k]
 
     def enqueue(self, stream, section=None, hook=None):
-        """Enqueue the ops (of one section, or all) on `stream`, side ops on the
-        side stream between a fork and a join (events: under stream capture they
+        """Enqueue the ops (of one section, or all) on `stream`, side ops on their
+        side streams between a fork and a join (events: under stream capture they
         become parallel branches of the section's graph).  hook(op, stream, when)
         runs before ("pre") and after ("post") each op on the stream it uses."""
-        side = None
-        pending = False  # side work not yet joined
-        for op in self.ops:
-            if section is not None and op.section != section:
-                continue
-            if op.join and pending:
+        pending = {}  # side id -> its stream, forked and not yet joined
+
+        def join_all():
+            for side in pending.values():
                 ev = torch.cuda.Event()
                 ev.record(side)
                 stream.wait_event(ev)
-                pending = False
+            pending.clear()
+
+        for op in self.ops:
+            if section is not None and op.section != section:
+                continue
+            if op.join:
+                join_all()
             target = stream
             if op.side:
-                if side is None:
-                    side = self.side_stream(stream.device)
-                if not pending:
+                if op.side not in pending:
+                    side = self.side_stream(stream.device, op.side)
                     ev = torch.cuda.Event()
                     ev.record(stream)
                     side.wait_event(ev)
-                    pending = True
-                target = side
+                    pending[op.side] = side
+                target = pending[op.side]
             if hook:
                 hook(op, target, "pre")
             op.fn(target)
             if hook:
                 hook(op, target, "post")
-        if pending:
-            ev = torch.cuda.Event()
-            ev.record(side)
-            stream.wait_event(ev)
+        join_all()
 
     def run_eager(self, stream=None, section=None):
         s = stream if stream is not None else torch.cuda.current_stream()
@@ -181,8 +184,8 @@ class Builder:
         self.section = "main"
         self.es = 4 if net.dtype == G.F32 else 2
 
-    def side(self):
-        """Ops appended inside `with b.side():` run on the net's side stream."""
+    def side(self, k=1):
+        """Ops appended inside `with b.side(k):` run on the net's side stream k."""
         b = self
 
         class _Side:
@@ -191,7 +194,7 @@ class Builder:
 
             def __exit__(self_, *exc):
                 for op in b.net.ops[self_.start:]:
-                    op.side = True
+                    op.side = k
                 return False
         return _Side()
 
